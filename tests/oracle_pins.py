@@ -1,0 +1,404 @@
+"""Pins for the CPU oracle: checks against what the pages and mathematics fix.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` and raises ``AssertionError`` when
+the oracle disagrees with something other than itself:
+
+* values the pages print (``tests/golden/``),
+* closed forms of the matmul (all-zero codes, all-15 codes, identity-like
+  weights, ramps) computed here with numpy/fractions from bf16 values decoded
+  by torch (a library routine, not the oracle's decoder),
+* brute force in exact rational arithmetic on tiny inputs,
+* an independent bit-level formulation of bf16 round-to-nearest-even, and
+  torch's own float32 -> bfloat16 cast on a sample.
+
+``test_oracle_pins.py`` runs them on the oracle; ``test_oracle_mutants.py``
+runs them on deliberately broken copies of the oracle to show each plausible
+mistake is caught by at least one pin.
+
+Citations (page titles; sections in quotes):
+  [W2D2] tiny-llm book, "Week 2 Day 2: Keep W4 Packed"
+  [G4MK] "Gemma 4 E4B & E2B -- single-launch Metal megakernels" model card
+"""
+from __future__ import annotations
+
+import os
+import struct
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+G = 64
+
+
+# ---- independent helpers (no oracle code) -------------------------------------
+
+def torch_bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Decode bf16 bit patterns with torch's bfloat16 -> float64 conversion."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return torch.from_numpy(b.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+
+
+def torch_f32_to_bf16(v: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(v, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def bits_bf16_from_f32(u: np.ndarray) -> np.ndarray:
+    """Round-to-nearest-even on the float32 bit pattern: add 0x7FFF plus the
+    lowest kept bit, then drop the low 16 bits.  NaNs are compared separately."""
+    u = u.astype(np.uint64)
+    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return (r & 0xFFFF).astype(np.uint16)
+
+
+def frac_from_bf16(h: int) -> Fraction:
+    """Exact value of a finite bf16 pattern (via the float32 it widens to)."""
+    return Fraction(struct.unpack("<f", struct.pack("<I", (h & 0xFFFF) << 16))[0])
+
+
+def frac_to_bf16(v: Fraction) -> int:
+    """Exact nearest-even rounding of a rational to bf16 (finite results only)."""
+    sign = 0x8000 if v < 0 else 0
+    a = abs(v)
+    if a == 0:
+        return sign
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    sp = Fraction(2) ** (max(e, -126) - 7)
+    q = a / sp
+    fl = q.numerator // q.denominator
+    d = q - fl
+    r = fl + 1 if d > Fraction(1, 2) or (d == Fraction(1, 2) and fl % 2 == 1) else fl
+    val = r * sp
+    if val < Fraction(2) ** -126:
+        return sign | int(r)
+    e2 = val.numerator.bit_length() - val.denominator.bit_length()
+    while Fraction(2) ** e2 > val:
+        e2 -= 1
+    while Fraction(2) ** (e2 + 1) <= val:
+        e2 += 1
+    sig = val / Fraction(2) ** (e2 - 7)
+    assert sig.denominator == 1 and 128 <= sig < 256
+    return sign | ((e2 + 127) << 7) | (int(sig) - 128)
+
+
+def nibble_bitwise(word: int, i: int) -> int:
+    """Code i of a packed word, assembled one bit at a time."""
+    q = 0
+    for bit in range(4):
+        q |= ((word >> (4 * i + bit)) & 1) << bit
+    return q
+
+
+def pack_page_order(codes) -> int:
+    """[W2D2 "Packed Storage Layout"]: (h<<28)|(g<<24)|...|(b<<4)|a."""
+    word = 0
+    for i, c in enumerate(codes):
+        word |= (int(c) & 0xF) << (4 * i)
+    return word
+
+
+def bf16_const(v: float) -> int:
+    return int(torch_f32_to_bf16(np.array([v], dtype=np.float32))[0])
+
+
+def _rng(seed: int) -> np.random.Generator:
+    return np.random.default_rng(seed)
+
+
+def random_bf16(rng, shape, lo=-2.0, hi=2.0) -> np.ndarray:
+    return torch_f32_to_bf16(rng.uniform(lo, hi, size=shape).astype(np.float32))
+
+
+# ---- unpack --------------------------------------------------------------------
+
+def pin_packing_golden(o):
+    with open(os.path.join(GOLDEN, "w2d2_packing.txt")) as f:
+        for line in f:
+            if not line.strip() or line.startswith("#"):
+                continue
+            parts = line.split()
+            codes, word = [int(p) for p in parts[:8]], int(parts[8], 16)
+            assert pack_page_order(codes) == word, "fixture inconsistent with the page's formula"
+            q = o.unpack(np.array([[word]], dtype=np.uint32), 1, 8)
+            assert list(q[0]) == codes, f"unpack({word:#x}) = {list(q[0])}, page gives {codes}"
+
+
+def pin_unpack_exhaustive(o):
+    words = []
+    expect = []
+    for v in range(16):
+        for i in range(8):
+            words.append(v << (4 * i))
+            e = [0] * 8
+            e[i] = v
+            expect.append(e)
+    q = o.unpack(np.array(words, dtype=np.uint32).reshape(-1, 1), len(words), 8)
+    assert np.array_equal(q, np.array(expect, dtype=np.uint8)), "single-code words unpack wrongly"
+    rng = _rng(11)
+    W = rng.integers(0, 2**32, size=(5, 24), dtype=np.uint64).astype(np.uint32)
+    q = o.unpack(W, 5, 192)
+    for n in range(5):
+        for k in range(192):
+            assert q[n, k] == nibble_bitwise(int(W[n, k // 8]), k % 8)
+
+
+# ---- dequant -------------------------------------------------------------------
+
+def pin_dequant_endpoints(o):
+    """[W2D2 "Reconstruct a Stored Group"]: both orientations of a signed scale."""
+    with open(os.path.join(GOLDEN, "w2d2_dequant_endpoints.txt")) as f:
+        rows = [l.split() for l in f if l.strip() and not l.startswith("#")]
+    for s, b, q, val, kind in rows:
+        sb, bb, q = bf16_const(float(s)), bf16_const(float(b)), int(q)
+        w = o.dequant(np.full((1, 8), q * 0x11111111, dtype=np.uint32), np.array([[sb]], dtype=np.uint16),
+                      np.array([[bb]], dtype=np.uint16), 1, 64)  # all 64 codes of the group = q
+        exact = q * float(torch_bf16_to_f64(np.array([sb]))[0]) + float(torch_bf16_to_f64(np.array([bb]))[0])
+        assert np.all(w == exact), f"dequant(q={q}, s={s}, b={b}) = {w[0, 0]}, q*s+b = {exact}"
+        if kind == "exact":
+            assert w[0, 0] == float(torch_bf16_to_f64(np.array([bf16_const(float(val))]))[0])
+        else:
+            assert abs(w[0, 0] - float(val)) <= 0.01, f"{w[0, 0]} is not about {val}"
+        # orientation: positive scale puts code 15 above code 0, negative below
+        w0 = o.dequant(np.zeros((1, 8), dtype=np.uint32), np.array([[sb]], dtype=np.uint16),
+                       np.array([[bb]], dtype=np.uint16), 1, 64)[0, 0]
+        w15 = o.dequant(np.full((1, 8), 0xFFFFFFFF, dtype=np.uint32), np.array([[sb]], dtype=np.uint16),
+                        np.array([[bb]], dtype=np.uint16), 1, 64)[0, 0]
+        assert (w15 > w0) == (float(s) > 0)
+
+
+def pin_dequant_random(o):
+    rng = _rng(12)
+    N, K = 3, 192
+    W = rng.integers(0, 2**32, size=(N, K // 8), dtype=np.uint64).astype(np.uint32)
+    S = random_bf16(rng, (N, K // G), -0.05, 0.05)
+    B = random_bf16(rng, (N, K // G), -1.0, 1.0)
+    w = o.dequant(W, S, B, N, K)
+    s64, b64 = torch_bf16_to_f64(S), torch_bf16_to_f64(B)
+    for n in range(N):
+        for k in range(K):
+            q = nibble_bitwise(int(W[n, k // 8]), k % 8)
+            assert w[n, k] == q * s64[n, k // G] + b64[n, k // G]
+
+
+# ---- bf16 ----------------------------------------------------------------------
+
+def pin_bf16_decode_all(o):
+    h = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    mine = o.bf16_to_f64(h)
+    ref = torch_bf16_to_f64(h)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(mine), nan)
+    assert np.array_equal(mine[~nan], ref[~nan]), "bf16 decode differs from torch"
+
+
+def pin_bf16_special(o):
+    cases = [(0.0, 0x0000), (-0.0, 0x8000), (1.0, 0x3F80), (-2.0, 0xC000), (float("inf"), 0x7F80),
+             (float("-inf"), 0xFF80), (2.0**-133, 0x0001), (2.0**-134, 0x0000),  # tie at half the min -> even 0
+             (1.5 * 2.0**-134, 0x0001), (2.0**-126, 0x0080), (3.3895313892515355e38, 0x7F7F),
+             (3.4e38, 0x7F80),  # rounds past the largest finite bf16
+             (1.0 + 2.0**-8, 0x3F80),                 # exact tie -> even
+             (1.0 + 3 * 2.0**-8, 0x3F82),             # exact tie -> even (up)
+             (1.0 + 2.0**-8 + 2.0**-40, 0x3F81),      # just above a tie: up (a float32 detour would tie)
+             (-(1.0 + 2.0**-8 + 2.0**-40), 0xBF81)]
+    for v, want in cases:
+        got = int(o.bf16_from_f64(np.array([v]))[0])
+        assert got == want, f"bf16({v!r}) = {got:#06x}, want {want:#06x}"
+    n = int(o.bf16_from_f64(np.array([float("nan")]))[0])
+    assert (n & 0x7F80) == 0x7F80 and (n & 0x7F) != 0
+
+
+def pin_bf16_from_f32_sweep(o):
+    """Every float32 high half, with low halves that cover each rounding class."""
+    lows = np.array([0x0000, 0x0001, 0x1234, 0x7FFE, 0x7FFF, 0x8000, 0x8001, 0xBEEF, 0xFFFE, 0xFFFF], dtype=np.uint32)
+    hi = np.arange(65536, dtype=np.uint32)
+    u = ((hi[:, None] << 16) | lows[None, :]).ravel()
+    rng = _rng(13)
+    u = np.concatenate([u, rng.integers(0, 2**32, size=1 << 21, dtype=np.uint64).astype(np.uint32)])
+    f = u.view(np.float32)
+    mine = o.bf16_from_f32(f)
+    nan = np.isnan(f)
+    ref = bits_bf16_from_f32(u)
+    assert np.array_equal(mine[~nan], ref[~nan]), "bf16 RNE differs from the bit-level formulation"
+    m = mine[nan]
+    assert np.all((m & 0x7F80) == 0x7F80) and np.all((m & 0x7F) != 0), "NaN must stay NaN"
+    sample = f[::97]
+    ok = ~np.isnan(sample)
+    assert np.array_equal(o.bf16_from_f32(sample)[ok], torch_f32_to_bf16(sample)[ok]), "differs from torch"
+
+
+def pin_bf16_from_f64_exact(o):
+    """Direct fp64 -> bf16 rounding against exact rational rounding."""
+    rng = _rng(14)
+    vals = list(rng.normal(0, 1, 300)) + list(rng.normal(0, 1, 100) * 1e-38) + list(rng.normal(0, 1, 100) * 1e30)
+    for i in range(64):  # near-ties that differ only below float32 precision
+        base = 1.0 + (2 * i + 1) * 2.0**-8
+        vals += [base + 2.0**-40, base - 2.0**-40, -base - 2.0**-45]
+    got = o.bf16_from_f64(np.array(vals, dtype=np.float64))
+    for v, g in zip(vals, got):
+        want = frac_to_bf16(Fraction(float(v)))
+        assert int(g) == want, f"bf16({v!r}) = {int(g):#06x}, exact rounding gives {want:#06x}"
+
+
+def pin_ulp(o):
+    cases = [(1.0, 2.0**-7), (1.99, 2.0**-7), (2.0, 2.0**-6), (-3.0, 2.0**-6), (0.75, 2.0**-8),
+             (2.0**-126, 2.0**-133), (2.0**-130, 2.0**-133), (0.0, 2.0**-133), (1e30, 2.0**(99 - 7))]
+    for v, want in cases:
+        got = float(o.ulp_bf16(np.array([v]))[0])
+        assert got == want, f"ulp_bf16({v}) = {got}, want {want}"
+
+
+# ---- matmul closed forms ---------------------------------------------------------
+
+def _group_sums(x64: np.ndarray) -> np.ndarray:
+    M, K = x64.shape
+    return x64.reshape(M, K // G, G).sum(axis=2)
+
+
+def _check_close(y, want, absdot, rel=1e-12, what=""):
+    err = np.abs(y - want)
+    bound = rel * np.maximum(absdot, 1e-300) + 1e-300
+    worst = int(np.argmax((err - bound).ravel()))
+    assert np.all(err <= bound), f"{what}: err {err.ravel()[worst]:.3e} exceeds bound {bound.ravel()[worst]:.3e}"
+
+
+def pin_mm_zero_codes(o):
+    """All codes 0: y = sum_g b_g * sum_{k in g} x_k  ([W2D2] affine identity with q = 0)."""
+    rng = _rng(21)
+    for (M, N, K) in [(1, 5, 64), (3, 9, 320), (2, 1, 128)]:
+        x = random_bf16(rng, (M, K))
+        S = random_bf16(rng, (N, K // G), -0.02, 0.02)
+        B = random_bf16(rng, (N, K // G))
+        y, ad = o.mm(x, np.zeros((N, K // 8), dtype=np.uint32), S, B, M, N, K)
+        want = _group_sums(torch_bf16_to_f64(x)) @ torch_bf16_to_f64(B).T
+        _check_close(y, want, ad, what=f"zero codes {M}x{N}x{K}")
+        want_abs = np.abs(torch_bf16_to_f64(x)).reshape(M, K // G, G).sum(2) @ np.abs(torch_bf16_to_f64(B)).T
+        _check_close(ad, want_abs, ad, what="absdot, zero codes")
+
+
+def pin_mm_all15(o):
+    """All codes 15: y = sum_g (15 s_g + b_g) sum_{k in g} x_k, with signed scales."""
+    rng = _rng(22)
+    for (M, N, K) in [(1, 4, 64), (4, 7, 256)]:
+        x = random_bf16(rng, (M, K))
+        S = random_bf16(rng, (N, K // G), -0.1, 0.1)
+        B = random_bf16(rng, (N, K // G))
+        y, ad = o.mm(x, np.full((N, K // 8), 0xFFFFFFFF, dtype=np.uint32), S, B, M, N, K)
+        eff = 15.0 * torch_bf16_to_f64(S) + torch_bf16_to_f64(B)
+        want = _group_sums(torch_bf16_to_f64(x)) @ eff.T
+        _check_close(y, want, ad, what=f"all-15 codes {M}x{N}x{K}")
+
+
+def pin_mm_identity(o):
+    """s = 1, b = 0, code 1 on the diagonal: y = x exactly."""
+    rng = _rng(23)
+    for K in (64, 128):
+        N = K
+        W = np.zeros((N, K // 8), dtype=np.uint32)
+        for n in range(N):
+            W[n, n // 8] = 1 << (4 * (n % 8))
+        S = np.full((N, K // G), bf16_const(1.0), dtype=np.uint16)
+        B = np.zeros((N, K // G), dtype=np.uint16)
+        x = random_bf16(rng, (2, K), -100.0, 100.0)
+        y, _ = o.mm(x, W, S, B, 2, N, K)
+        assert np.array_equal(y, torch_bf16_to_f64(x)), "identity-like weights must reproduce x"
+        assert np.array_equal(o.bf16_from_f64(y), x)
+
+
+def pin_mm_ramp(o):
+    """x_k = k/K, codes (k + n) mod 16, s = 1/16, b = -1/2: exact rational sum."""
+    for K in (128, 256):
+        N = 3
+        x = torch_f32_to_bf16((np.arange(K) / K).astype(np.float32))[None, :]
+        W = np.zeros((N, K // 8), dtype=np.uint32)
+        for n in range(N):
+            for k in range(K):
+                W[n, k // 8] |= ((k + n) % 16) << (4 * (k % 8))
+        S = np.full((N, K // G), bf16_const(1 / 16), dtype=np.uint16)
+        B = np.full((N, K // G), bf16_const(-0.5), dtype=np.uint16)
+        y, _ = o.mm(x, W, S, B, 1, N, K)
+        for n in range(N):
+            want = sum(Fraction(k, K) * (Fraction((k + n) % 16, 16) - Fraction(1, 2)) for k in range(K))
+            assert Fraction(y[0, n]) == want, f"ramp n={n}: {y[0, n]} != {float(want)}"
+
+
+def pin_mm_bruteforce(o):
+    """Tiny random cases in exact rational arithmetic, including the bf16 rounding."""
+    rng = _rng(24)
+    for (M, N, K) in [(1, 1, 64), (2, 4, 64), (2, 3, 128), (1, 4, 128)]:
+        x = random_bf16(rng, (M, K))
+        W = rng.integers(0, 2**32, size=(N, K // 8), dtype=np.uint64).astype(np.uint32)
+        S = random_bf16(rng, (N, K // G), -0.05, 0.05)
+        B = random_bf16(rng, (N, K // G), -0.5, 0.5)
+        y, ad = o.mm(x, W, S, B, M, N, K)
+        yb = o.bf16_from_f64(y)
+        for m in range(M):
+            for n in range(N):
+                tot = Fraction(0)
+                tot_abs = Fraction(0)
+                for k in range(K):
+                    q = nibble_bitwise(int(W[n, k // 8]), k % 8)
+                    w = q * frac_from_bf16(int(S[n, k // G])) + frac_from_bf16(int(B[n, k // G]))
+                    p = frac_from_bf16(int(x[m, k])) * w
+                    tot += p
+                    tot_abs += abs(p)
+                assert abs(Fraction(y[m, n]) - tot) <= Fraction(1, 2**50) * tot_abs, f"brute force ({m},{n})"
+                assert abs(Fraction(ad[m, n]) - tot_abs) <= Fraction(1, 2**50) * tot_abs, "absdot"
+                assert int(yb[m, n]) == frac_to_bf16(tot), f"bf16 of ({m},{n})"
+
+
+def pin_mm_sampled_columns(o):
+    """Sampled columns equal the full result; the thread count changes nothing."""
+    rng = _rng(25)
+    M, N, K = 3, 37, 192
+    x = random_bf16(rng, (M, K))
+    W = rng.integers(0, 2**32, size=(N, K // 8), dtype=np.uint64).astype(np.uint32)
+    S = random_bf16(rng, (N, K // G), -0.05, 0.05)
+    B = random_bf16(rng, (N, K // G), -0.5, 0.5)
+    y, ad = o.mm(x, W, S, B, M, N, K, threads=1)
+    y4, _ = o.mm(x, W, S, B, M, N, K, threads=4)
+    assert np.array_equal(y, y4)
+    cols = np.array([36, 0, 17, 17, 5])
+    ys, ads = o.mm(x, W, S, B, M, N, K, cols=cols)
+    assert np.array_equal(ys, y[:, cols]) and np.array_equal(ads, ad[:, cols])
+    # row m of an M-row call is the 1-row call on x[m]
+    for m in range(M):
+        y1, _ = o.mm(x[m:m + 1], W, S, B, 1, N, K)
+        assert np.array_equal(y1[0], y[m])
+
+
+def pin_mm_id(o):
+    """Routed experts: per-expert closed form (zero codes), zero rows for bad ids."""
+    rng = _rng(26)
+    E, N, K, T = 3, 6, 128, 7
+    x = random_bf16(rng, (T, K))
+    B = random_bf16(rng, (E, N, K // G))
+    S = random_bf16(rng, (E, N, K // G), -0.02, 0.02)
+    ids = np.array([2, 0, -1, 1, 3, 2, 0], dtype=np.int32)
+    y, ad = o.mm_id(x, np.zeros((E, N, K // 8), dtype=np.uint32), S, B, ids, T, N, K, E)
+    xs = _group_sums(torch_bf16_to_f64(x))
+    for t in range(T):
+        if 0 <= ids[t] < E:
+            want = xs[t] @ torch_bf16_to_f64(B[ids[t]]).T
+            _check_close(y[t], want, ad[t], what=f"mm_id token {t}")
+        else:
+            assert np.all(y[t] == 0) and np.all(ad[t] == 0), "out-of-range id must give a zero row"
+    # random codes: token t equals the plain matmul on expert ids[t]
+    W = rng.integers(0, 2**32, size=(E, N, K // 8), dtype=np.uint64).astype(np.uint32)
+    y, _ = o.mm_id(x, W, S, B, ids, T, N, K, E)
+    for t in range(T):
+        if 0 <= ids[t] < E:
+            e = ids[t]
+            ym, _ = o.mm(x[t:t + 1], W[e], S[e], B[e], 1, N, K)
+            assert np.array_equal(ym[0], y[t])
+
+
+PINS = [pin_packing_golden, pin_unpack_exhaustive, pin_dequant_endpoints, pin_dequant_random,
+        pin_ulp, pin_bf16_special, pin_mm_zero_codes, pin_mm_all15, pin_mm_identity, pin_mm_ramp,
+        pin_mm_sampled_columns, pin_mm_id, pin_mm_bruteforce, pin_bf16_decode_all,
+        pin_bf16_from_f64_exact, pin_bf16_from_f32_sweep]
