@@ -1,0 +1,182 @@
+/*
+ * w4a16.h -- C ABI of libw4a16.so: weight-only 4-bit, group-64 affine
+ * quantized matmul (W4A16) for skinny activations on GB300 (sm_103a).
+ *
+ * Citations (page titles; sections in quotes):
+ *   [W2D2] tiny-llm book, "Week 2 Day 2: Keep W4 Packed"
+ *   [G4MK] "Gemma 4 E4B & E2B -- single-launch Metal megakernels + lossless
+ *          speculative decoding" (RESMP-DEV model card)
+ *   [HY4]  "Hy4-preview Metal kernels for llama.cpp"
+ *
+ * The operation ([W2D2 "Mathematical Formulation", C = A B^T, and
+ * "Reconstruct a Stored Group", w^ = q s + b]):
+ *
+ *   q[n,k] = (Wq[n][k/8] >> 4*(k%8)) & 0xF            (low nibble first,
+ *                                                      [W2D2 "Packed Storage Layout"])
+ *   y[m,n] = bf16( sum_k x[m,k] * (q[n,k]*scales[n][k/64] + biases[n][k/64]) )
+ *
+ * with the group size fixed at 64 ([G4MK "Usage": 4-bit weights at group
+ * size 64; the dequant path assumes it]).  The page writes A (M x N), B
+ * (K x N), C (M x K) with the reduction over N; this header uses
+ * x[M][K], Wq[N][K/8], y[M][N] with the reduction over K.
+ *
+ * Layout.  Every tensor is dense and row-major with no strides (the
+ * row-contiguous contract of [W2D2 "Tune the SIMD Schedule"]):
+ *   x       bf16 [M][K]        activations
+ *   Wq      u32  [N][K/8]      eight 4-bit codes per word, code k%8 in bits 4*(k%8)..+3
+ *   scales  bf16 [N][K/64]     signed; used as stored ([W2D2 "Reconstruct a Stored Group"])
+ *   biases  bf16 [N][K/64]
+ *   y       bf16 [M][N]        round-to-nearest-even of the fp32 accumulation
+ * bf16 values are passed as raw 16-bit patterns (w4a16_bf16).
+ *
+ * Batch invariance ([G4MK "What it does" and "Implementation notes": the
+ * verify GEMM is arithmetic-identical to the sequential GEMV, batch equals
+ * sequential bitwise]).  The kernel and its reduction order are chosen from
+ * (N, K) only, never from M, so row m of any call equals, bit for bit, the
+ * M = 1 call on x[m].  Calls with M > 8 run as consecutive chunks of at most
+ * eight rows through the same kernels.  w4a16_mm_id rows equal w4a16_mm on
+ * the selected expert, bit for bit.
+ *
+ * Ownership and synchronisation.  All tensor pointers are DEVICE pointers
+ * owned by the caller.  `stream` is a cudaStream_t (NULL = legacy default
+ * stream).  Compute calls only enqueue work: they return before the GPU is
+ * done and never synchronise, except w4a16_device_status and the one-time
+ * workspace set-up below.
+ *
+ * Workspace.  When the tensor-core kernel splits K across warps of different
+ * SMs (w4a16_get_plan: ksplit > 1) it exchanges fp32 slice sums through a
+ * workspace the library owns, one per (device, stream): 4.77 MiB, enough for
+ * every shape, allocated with cudaMalloc (and its counters zeroed on the
+ * stream) by the first call that needs it on that stream.  It stays
+ * allocated until the process exits.  Calls
+ * on one stream are ordered and share it safely; calls on different streams
+ * use different workspaces.  A call that would need to allocate while its
+ * stream is being captured into a CUDA graph fails with W4A16_ERR_CUDA, so
+ * make one call on a stream before capturing it.
+ *
+ * Alignment.  x and Wq must be 16-byte aligned (their rows then are too,
+ * because K % 64 == 0); scales and biases 8-byte aligned; y 2-byte; ids
+ * 4-byte.
+ *
+ * Errors ("fail closed": arguments are checked on the host before any
+ * launch, and a rejected call writes nothing, after [W2D2 "Task 2": validate
+ * inputs and reject unsupported evaluation explicitly]).  Every call returns
+ * a w4a16_status; the message of the last failure on the calling host
+ * thread is kept for w4a16_last_error().
+ */
+#ifndef W4A16_H
+#define W4A16_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t w4a16_bf16; /* raw bfloat16 bits */
+
+typedef enum {
+  W4A16_OK = 0,
+  W4A16_ERR_NULL = -1,      /* a required pointer is NULL */
+  W4A16_ERR_SHAPE = -2,     /* K <= 0, K % 64 != 0, N <= 0, M < 0, or too large */
+  W4A16_ERR_ALIGN = -3,     /* x / Wq not 16-byte aligned, or another pointer misaligned */
+  W4A16_ERR_EXPERTS = -4,   /* E <= 0 or T < 0 */
+  W4A16_ERR_CUDA = -5,      /* a CUDA call or launch failed; see w4a16_last_error() */
+  W4A16_ERR_KERNEL = -6,    /* unknown kernel selector */
+  W4A16_ERR_DEVICE = -7     /* w4a16_device_status: a kernel reported bad input */
+} w4a16_status;
+
+/* Kernel families (all compute the operation above). */
+typedef enum {
+  W4A16_KERNEL_AUTO = 0,    /* the dispatcher's choice for (N, K) */
+  W4A16_KERNEL_SIMT = 1,    /* CUDA-core kernel: fp32 FMA, warp-shuffle split-K */
+  W4A16_KERNEL_TC = 2,      /* tensor-core kernel: TMA-fed bf16 MMA on codes, fp32 group
+                               rescale; needs K % 256 == 0 */
+  W4A16_KERNEL_VANILLA = 3  /* debug control: one thread per output, no sharing */
+} w4a16_kernel;
+
+/* y[M][N] = x[M][K] W^T.  M == 0 is a successful no-op.  The kernel family
+ * is the dispatcher's choice for (N, K) unless the environment variable
+ * W4A16_FORCE_KERNEL names one (simt, tc, vanilla). */
+int w4a16_mm(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* scales,
+             const w4a16_bf16* biases, w4a16_bf16* y, int M, int N, int K, void* stream);
+
+/* w4a16_mm with an explicit kernel family (for A/B comparisons and tests). */
+int w4a16_mm_kernel(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* scales,
+                    const w4a16_bf16* biases, w4a16_bf16* y, int M, int N, int K,
+                    int kernel, void* stream);
+
+/* Routed experts, top-1 (the W4A16 analogue of llama.cpp's mul_mat_id named
+ * in [HY4] "What was missing and what this adds"):
+ *   y[t][n] = sum_k x[t][k] * w_{ids[t]}[n][k]
+ * Wq is u32 [E][N][K/8], scales/biases bf16 [E][N][K/64], ids int32 [T] on
+ * the DEVICE, y bf16 [T][N].  Each expert's weights are streamed once for
+ * all tokens routed to it (in chunks of up to eight tokens); experts no
+ * token selects are not read.  An id outside 0..E-1 cannot be checked on the
+ * host without a synchronisation: its row of y is written as zeros and the
+ * sticky device flag W4A16_DEVICE_BAD_ID is raised (see w4a16_device_status).
+ * T == 0 is a successful no-op. */
+int w4a16_mm_id(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* scales,
+                const w4a16_bf16* biases, const int32_t* ids, w4a16_bf16* y,
+                int T, int N, int K, int E, void* stream);
+
+/* w4a16_mm_id with an explicit kernel family. */
+int w4a16_mm_id_kernel(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* scales,
+                       const w4a16_bf16* biases, const int32_t* ids, w4a16_bf16* y,
+                       int T, int N, int K, int E, int kernel, void* stream);
+
+/* Debug: q[N][K] (one byte per code) from Wq[N][K/8].  Bit-exact
+ * ([W2D2 "Packed Storage Layout"]). */
+int w4a16_unpack(const uint32_t* Wq, uint8_t* q, int N, int K, void* stream);
+
+/* Debug: w[N][K] = fp32 fma(q, s, b) (one rounding), K % 64 == 0
+ * ([W2D2 "Reconstruct a Stored Group"]). */
+int w4a16_dequant(const uint32_t* Wq, const w4a16_bf16* scales, const w4a16_bf16* biases,
+                  float* w, int N, int K, void* stream);
+
+/* The dispatcher's decision for a shape.  `ksplit` and `slice_k` fix the
+ * reduction order of every output row: K is cut into `ksplit` consecutive
+ * slices of `slice_k` codes (the last one may be shorter); each slice is
+ * reduced on its own and the slice sums are added in slice order.  Both
+ * depend on (N, K) only, never on M.  The other fields describe the launch
+ * of one chunk of at most eight activation rows on this device (152 SMs are
+ * assumed when no GPU is present). */
+typedef struct {
+  int kernel;        /* w4a16_kernel actually used */
+  int ksplit;        /* K-slices per output row */
+  int slice_k;       /* codes per K-slice */
+  int rows_per_tile; /* output rows of one work unit */
+  int units;         /* work units (row tile x K-slice) of one chunk */
+  int threads;       /* threads per CTA */
+  int grid_x;        /* CTAs per chunk */
+  int smem_bytes;    /* dynamic shared memory per CTA (M = 1) */
+} w4a16_plan;
+
+int w4a16_get_plan(int N, int K, int kernel, w4a16_plan* out);
+
+/* Sticky device-side error flags, raised by kernels instead of trapping. */
+#define W4A16_DEVICE_BAD_ID 1   /* mm_id: an expert id outside 0..E-1 */
+#define W4A16_DEVICE_TIMEOUT 2  /* a bounded wait on an asynchronous copy gave up */
+
+/* Synchronises `stream`, reads and clears the device flags of the current
+ * device.  Returns W4A16_OK when no flag was set, W4A16_ERR_DEVICE when one
+ * was (flags stored in *flags if non-NULL), W4A16_ERR_CUDA on a CUDA error. */
+int w4a16_device_status(void* stream, int* flags);
+
+/* Message of the last failed call on this host thread ("" if none). */
+const char* w4a16_last_error(void);
+
+/* Debug: re-read the environment switches W4A16_FAULT (validate | launch:
+ * every compute call then fails with that error before launching anything)
+ * and W4A16_FORCE_KERNEL (simt | tc | vanilla).  They are read once, at the
+ * first call, otherwise. */
+void w4a16_debug_reload_env(void);
+
+/* Library version string. */
+const char* w4a16_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H */

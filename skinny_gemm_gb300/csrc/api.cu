@@ -1,0 +1,270 @@
+// api.cu -- the C ABI of libw4a16.so (declared and documented in include/w4a16.h).
+//
+// Host-side validation happens before any launch and a rejected call writes
+// nothing (fail closed, after tiny-llm "Week 2 Day 2: Keep W4 Packed",
+// section "Task 2": validate inputs, reject unsupported evaluation
+// explicitly).  The kernel family and its reduction order are chosen from
+// (N, K) only; M only decides how many chunks of at most eight rows run.
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace w4a16 {
+namespace {
+
+__device__ int g_device_flags;
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(W4A16_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+// ---- debug switches read once from the environment -----------------------------
+
+enum Fault { kFaultNone = 0, kFaultValidate = 1, kFaultLaunch = 2 };
+
+struct EnvConfig {
+  int fault = kFaultNone;
+  int force_kernel = W4A16_KERNEL_AUTO;
+};
+
+std::mutex g_env_mu;
+bool g_env_loaded = false;
+EnvConfig g_env;
+
+void load_env_locked() {
+  EnvConfig c;
+  if (const char* f = std::getenv("W4A16_FAULT")) {
+    if (!std::strcmp(f, "validate")) c.fault = kFaultValidate;
+    else if (!std::strcmp(f, "launch")) c.fault = kFaultLaunch;
+  }
+  if (const char* k = std::getenv("W4A16_FORCE_KERNEL")) {
+    if (!std::strcmp(k, "simt")) c.force_kernel = W4A16_KERNEL_SIMT;
+    else if (!std::strcmp(k, "tc")) c.force_kernel = W4A16_KERNEL_TC;
+    else if (!std::strcmp(k, "vanilla")) c.force_kernel = W4A16_KERNEL_VANILLA;
+  }
+  g_env = c;
+  g_env_loaded = true;
+}
+
+EnvConfig env() {
+  std::lock_guard<std::mutex> lk(g_env_mu);
+  if (!g_env_loaded) load_env_locked();
+  return g_env;
+}
+
+// ---- device flag word, one per device ------------------------------------------
+
+constexpr int kMaxDevices = 64;
+std::mutex g_flag_mu;
+int* g_flag_ptr[kMaxDevices] = {};
+
+int flag_pointer(int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(W4A16_ERR_CUDA, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_flag_mu);
+  if (!g_flag_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_flags);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(device flags)");
+    g_flag_ptr[dev] = static_cast<int*>(p);
+  }
+  *out = g_flag_ptr[dev];
+  return W4A16_OK;
+}
+
+// ---- validation ------------------------------------------------------------------
+
+constexpr int kMaxDim = 1 << 30;
+
+bool misaligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) != 0; }
+
+int check_nk(int N, int K) {
+  if (N <= 0 || N > kMaxDim) return fail(W4A16_ERR_SHAPE, "N = %d must be in 1..2^30", N);
+  if (K <= 0 || K > kMaxDim || K % kGroup) return fail(W4A16_ERR_SHAPE, "K = %d must be a positive multiple of 64", K);
+  return W4A16_OK;
+}
+
+int resolve_kernel(int requested, int N, int K, w4a16_plan* plan) {
+  int k = requested;
+  if (k == W4A16_KERNEL_AUTO) k = env().force_kernel;
+  // Default: the tensor-core family wherever it applies (K % 256 == 0), the
+  // CUDA-core family otherwise.  The choice depends on (N, K) only.
+  if (k == W4A16_KERNEL_AUTO) k = tc_supported(N, K) ? W4A16_KERNEL_TC : W4A16_KERNEL_SIMT;
+  switch (k) {
+    case W4A16_KERNEL_SIMT: plan_simt(N, K, plan); return W4A16_OK;
+    case W4A16_KERNEL_VANILLA: plan_vanilla(N, K, plan); return W4A16_OK;
+    case W4A16_KERNEL_TC:
+      if (!tc_supported(N, K)) return fail(W4A16_ERR_KERNEL, "the tensor-core kernel needs K %% 256 == 0 (K = %d)", K);
+      plan_tc(N, K, plan);
+      return W4A16_OK;
+    default: return fail(W4A16_ERR_KERNEL, "unknown kernel selector %d", requested);
+  }
+}
+
+int validate_mm(const void* x, const void* Wq, const void* S, const void* B, const void* y, int M, int N, int K) {
+  if (M < 0 || M > kMaxDim) return fail(W4A16_ERR_SHAPE, "M = %d must be in 0..2^30", M);
+  if (int rc = check_nk(N, K)) return rc;
+  if (M == 0) return W4A16_OK;
+  if (!x || !Wq || !S || !B || !y) return fail(W4A16_ERR_NULL, "null tensor pointer");
+  if (misaligned(x, 16) || misaligned(Wq, 16)) return fail(W4A16_ERR_ALIGN, "x and Wq must be 16-byte aligned");
+  if (misaligned(S, 8) || misaligned(B, 8)) return fail(W4A16_ERR_ALIGN, "scales and biases must be 8-byte aligned");
+  if (misaligned(y, 2)) return fail(W4A16_ERR_ALIGN, "y must be 2-byte aligned");
+  return W4A16_OK;
+}
+
+int run_mm(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* S, const w4a16_bf16* B, w4a16_bf16* y,
+           int M, int N, int K, int kernel, void* stream) {
+  if (env().fault == kFaultValidate) return fail(W4A16_ERR_SHAPE, "injected validation fault (W4A16_FAULT)");
+  if (int rc = validate_mm(x, Wq, S, B, y, M, N, K)) return rc;
+  w4a16_plan plan;
+  if (int rc = resolve_kernel(kernel, N, K, &plan)) return rc;
+  if (M == 0) return W4A16_OK;
+  if (env().fault == kFaultLaunch) return fail(W4A16_ERR_CUDA, "injected launch fault (W4A16_FAULT)");
+  LaunchArgs a{};
+  a.x = x; a.Wq = Wq; a.S = S; a.B = B; a.y = y;
+  a.N = N; a.K = K;
+  a.stream = static_cast<cudaStream_t>(stream);
+  if (int rc = flag_pointer(&a.flags)) return rc;
+  for (int row0 = 0; row0 < M; row0 += kMaxChunk) {
+    a.row0 = row0;
+    a.M = (M - row0 < kMaxChunk) ? M - row0 : kMaxChunk;
+    cudaError_t e = cudaSuccess;
+    switch (plan.kernel) {
+      case W4A16_KERNEL_SIMT: e = launch_simt(a, plan); break;
+      case W4A16_KERNEL_TC: e = launch_tc(a, plan); break;
+      case W4A16_KERNEL_VANILLA: e = launch_vanilla(a, plan); break;
+      default: return fail(W4A16_ERR_KERNEL, "kernel %d cannot run", plan.kernel);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "w4a16_mm launch");
+  }
+  return W4A16_OK;
+}
+
+}  // namespace
+}  // namespace w4a16
+
+using namespace w4a16;
+
+extern "C" {
+
+int w4a16_mm(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* scales, const w4a16_bf16* biases,
+             w4a16_bf16* y, int M, int N, int K, void* stream) {
+  return run_mm(x, Wq, scales, biases, y, M, N, K, W4A16_KERNEL_AUTO, stream);
+}
+
+int w4a16_mm_kernel(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* scales, const w4a16_bf16* biases,
+                    w4a16_bf16* y, int M, int N, int K, int kernel, void* stream) {
+  return run_mm(x, Wq, scales, biases, y, M, N, K, kernel, stream);
+}
+
+int w4a16_mm_id(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* scales, const w4a16_bf16* biases,
+                const int32_t* ids, w4a16_bf16* y, int T, int N, int K, int E, void* stream) {
+  return w4a16_mm_id_kernel(x, Wq, scales, biases, ids, y, T, N, K, E, W4A16_KERNEL_AUTO, stream);
+}
+
+int w4a16_mm_id_kernel(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* scales,
+                       const w4a16_bf16* biases, const int32_t* ids, w4a16_bf16* y, int T, int N, int K, int E,
+                       int kernel, void* stream) {
+  if (env().fault == kFaultValidate) return fail(W4A16_ERR_SHAPE, "injected validation fault (W4A16_FAULT)");
+  if (T < 0 || T > kMaxDim) return fail(W4A16_ERR_EXPERTS, "T = %d must be in 0..2^30", T);
+  if (E <= 0 || E > 65535) return fail(W4A16_ERR_EXPERTS, "E = %d must be in 1..65535", E);
+  if (int rc = check_nk(N, K)) return rc;
+  w4a16_plan plan;
+  if (int rc = resolve_kernel(kernel, N, K, &plan)) return rc;
+  if (T == 0) return W4A16_OK;
+  if (!x || !Wq || !scales || !biases || !ids || !y) return fail(W4A16_ERR_NULL, "null tensor pointer");
+  if (misaligned(x, 16) || misaligned(Wq, 16)) return fail(W4A16_ERR_ALIGN, "x and Wq must be 16-byte aligned");
+  if (misaligned(scales, 8) || misaligned(biases, 8) || misaligned(y, 2) || misaligned(ids, 4))
+    return fail(W4A16_ERR_ALIGN, "scales/biases must be 8-byte, y 2-byte and ids 4-byte aligned");
+  if (plan.kernel == W4A16_KERNEL_VANILLA && T > 65535)
+    return fail(W4A16_ERR_SHAPE, "the vanilla control kernel takes at most 65535 tokens");
+  if (env().fault == kFaultLaunch) return fail(W4A16_ERR_CUDA, "injected launch fault (W4A16_FAULT)");
+  LaunchArgs a{};
+  a.x = x; a.Wq = Wq; a.S = scales; a.B = biases; a.y = y;
+  a.N = N; a.K = K; a.ids = ids; a.T = T; a.E = E;
+  a.stream = static_cast<cudaStream_t>(stream);
+  if (int rc = flag_pointer(&a.flags)) return rc;
+  cudaError_t e = cudaSuccess;
+  switch (plan.kernel) {
+    case W4A16_KERNEL_SIMT: e = launch_simt_id(a, plan); break;
+    case W4A16_KERNEL_TC: e = launch_tc_id(a, plan); break;
+    case W4A16_KERNEL_VANILLA: e = launch_vanilla_id(a, plan); break;
+    default: return fail(W4A16_ERR_KERNEL, "kernel %d cannot run", plan.kernel);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "w4a16_mm_id launch");
+  return W4A16_OK;
+}
+
+int w4a16_unpack(const uint32_t* Wq, uint8_t* q, int N, int K, void* stream) {
+  if (N <= 0 || N > kMaxDim) return fail(W4A16_ERR_SHAPE, "N = %d must be in 1..2^30", N);
+  if (K <= 0 || K > kMaxDim || K % 8) return fail(W4A16_ERR_SHAPE, "K = %d must be a positive multiple of 8", K);
+  if (!Wq || !q) return fail(W4A16_ERR_NULL, "null tensor pointer");
+  if (misaligned(Wq, 4) || misaligned(q, 8)) return fail(W4A16_ERR_ALIGN, "Wq must be 4-byte and q 8-byte aligned");
+  cudaError_t e = launch_unpack(Wq, q, N, K, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? W4A16_OK : cuda_fail(e, "w4a16_unpack launch");
+}
+
+int w4a16_dequant(const uint32_t* Wq, const w4a16_bf16* scales, const w4a16_bf16* biases, float* w, int N, int K,
+                  void* stream) {
+  if (int rc = check_nk(N, K)) return rc;
+  if (!Wq || !scales || !biases || !w) return fail(W4A16_ERR_NULL, "null tensor pointer");
+  if (misaligned(Wq, 4) || misaligned(scales, 2) || misaligned(biases, 2) || misaligned(w, 16))
+    return fail(W4A16_ERR_ALIGN, "Wq 4-byte, scales/biases 2-byte and w 16-byte alignment required");
+  cudaError_t e = launch_dequant(Wq, scales, biases, w, N, K, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? W4A16_OK : cuda_fail(e, "w4a16_dequant launch");
+}
+
+int w4a16_get_plan(int N, int K, int kernel, w4a16_plan* out) {
+  if (!out) return fail(W4A16_ERR_NULL, "null plan pointer");
+  if (int rc = check_nk(N, K)) return rc;
+  return resolve_kernel(kernel, N, K, out);
+}
+
+int w4a16_device_status(void* stream, int* flags) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int* p = nullptr;
+  if (int rc = flag_pointer(&p)) return rc;
+  int v = 0;
+  e = cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read device flags");
+  if (flags) *flags = v;
+  if (v) {
+    const int zero = 0;
+    e = cudaMemcpy(p, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "clear device flags");
+    return fail(W4A16_ERR_DEVICE, "a kernel reported bad input (flags 0x%x)", v);
+  }
+  return W4A16_OK;
+}
+
+const char* w4a16_last_error(void) { return g_last_error.c_str(); }
+
+const char* w4a16_version(void) { return "w4a16 0.1.0 (sm_103a)"; }
+
+void w4a16_debug_reload_env(void) {
+  std::lock_guard<std::mutex> lk(g_env_mu);
+  load_env_locked();
+}
+
+}  // extern "C"

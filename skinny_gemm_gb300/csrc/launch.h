@@ -1,0 +1,51 @@
+// launch.h -- internal interface between the C-ABI (api.cu) and the kernel
+// translation units.  Host-side only; no torch types anywhere.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "w4a16.h"
+
+namespace w4a16 {
+
+// One launch computes at most this many activation rows.
+constexpr int kMaxChunk = 8;
+
+// Arguments of one launch.  Plain mm: rows x[row0 .. row0+M) -> y rows of the
+// same index.  Routed mm_id: ids != nullptr, T tokens, E experts; each CTA
+// column blockIdx.y is one expert and gathers its own tokens.
+struct LaunchArgs {
+  const uint16_t* x;
+  const uint32_t* Wq;
+  const uint16_t* S;
+  const uint16_t* B;
+  uint16_t* y;
+  int M;          // rows in this chunk (1..8); unused for mm_id
+  int row0;       // first activation row of the chunk
+  int N, K;
+  const int32_t* ids;  // mm_id only
+  int T, E;            // mm_id only
+  int* flags;          // device flag word (mm_id bad ids)
+  cudaStream_t stream;
+};
+
+// Per-family planning (depends on N and K only) and launching.
+void plan_simt(int N, int K, w4a16_plan* p);
+cudaError_t launch_simt(const LaunchArgs& a, const w4a16_plan& p);
+cudaError_t launch_simt_id(const LaunchArgs& a, const w4a16_plan& p);
+
+void plan_tc(int N, int K, w4a16_plan* p);
+bool tc_supported(int N, int K);
+cudaError_t launch_tc(const LaunchArgs& a, const w4a16_plan& p);
+cudaError_t launch_tc_id(const LaunchArgs& a, const w4a16_plan& p);
+
+void plan_vanilla(int N, int K, w4a16_plan* p);
+cudaError_t launch_vanilla(const LaunchArgs& a, const w4a16_plan& p);
+cudaError_t launch_vanilla_id(const LaunchArgs& a, const w4a16_plan& p);
+
+cudaError_t launch_unpack(const uint32_t* Wq, uint8_t* q, int N, int K, cudaStream_t s);
+cudaError_t launch_dequant(const uint32_t* Wq, const uint16_t* S, const uint16_t* B, float* w, int N, int K,
+                           cudaStream_t s);
+
+}  // namespace w4a16

@@ -1,0 +1,242 @@
+"""Python binding of libw4a16.so: argument marshalling only.
+
+Every computation runs in the library's CUDA kernels.  PyTorch supplies the
+device memory, the current CUDA stream and the output allocation; there is
+no CPU or PyTorch fallback, and a missing or unbuildable library raises.
+
+Names follow the C ABI in ``include/w4a16.h``: ``mm``, ``mm_id``,
+``unpack``, ``dequant``, ``get_plan``, ``device_status``.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+from dataclasses import dataclass
+
+import torch
+
+from . import _build
+
+GROUP = 64
+
+OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_EXPERTS, ERR_CUDA, ERR_KERNEL, ERR_DEVICE = 0, -1, -2, -3, -4, -5, -6, -7
+KERNELS = {"auto": 0, "simt": 1, "tc": 2, "vanilla": 3}
+KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
+DEVICE_BAD_ID = 1
+
+EXPORTS = ("w4a16_mm", "w4a16_mm_kernel", "w4a16_mm_id", "w4a16_mm_id_kernel", "w4a16_unpack",
+           "w4a16_dequant", "w4a16_get_plan", "w4a16_device_status", "w4a16_last_error",
+           "w4a16_debug_reload_env", "w4a16_version")
+
+
+class W4A16Error(RuntimeError):
+    """A library call failed; ``status`` is the w4a16_status code."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"w4a16 status {status}: {message}")
+        self.status = status
+
+
+class W4A16ValueError(W4A16Error, ValueError):
+    pass
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int), ("ksplit", ctypes.c_int), ("slice_k", ctypes.c_int),
+                ("rows_per_tile", ctypes.c_int), ("units", ctypes.c_int), ("threads", ctypes.c_int),
+                ("grid_x", ctypes.c_int), ("smem_bytes", ctypes.c_int)]
+
+    def as_dict(self) -> dict:
+        d = {f: getattr(self, f) for f, _ in self._fields_}
+        d["kernel"] = KERNEL_NAMES.get(self.kernel, self.kernel)
+        return d
+
+
+_lock = threading.Lock()
+_lib: ctypes.CDLL | None = None
+
+
+def library_path() -> str:
+    return _build.CUDA_LIB
+
+
+def lib() -> ctypes.CDLL:
+    """Open libw4a16.so (building it in-tree if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build_cuda()
+            L = ctypes.CDLL(path)
+            P, i = ctypes.c_void_p, ctypes.c_int
+            L.w4a16_mm.argtypes = [P, P, P, P, P, i, i, i, P]
+            L.w4a16_mm_kernel.argtypes = [P, P, P, P, P, i, i, i, i, P]
+            L.w4a16_mm_id.argtypes = [P, P, P, P, P, P, i, i, i, i, P]
+            L.w4a16_mm_id_kernel.argtypes = [P, P, P, P, P, P, i, i, i, i, i, P]
+            L.w4a16_unpack.argtypes = [P, P, i, i, P]
+            L.w4a16_dequant.argtypes = [P, P, P, P, i, i, P]
+            L.w4a16_get_plan.argtypes = [i, i, i, ctypes.POINTER(Plan)]
+            L.w4a16_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
+            for f in ("w4a16_mm", "w4a16_mm_kernel", "w4a16_mm_id", "w4a16_mm_id_kernel", "w4a16_unpack",
+                      "w4a16_dequant", "w4a16_get_plan", "w4a16_device_status"):
+                getattr(L, f).restype = ctypes.c_int
+            L.w4a16_last_error.restype = ctypes.c_char_p
+            L.w4a16_version.restype = ctypes.c_char_p
+            L.w4a16_debug_reload_env.restype = None
+            _lib = L
+    return _lib
+
+
+def _raise(rc: int) -> None:
+    if rc == OK:
+        return
+    msg = (lib().w4a16_last_error() or b"").decode()
+    if rc in (ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_EXPERTS, ERR_KERNEL):
+        raise W4A16ValueError(rc, msg)
+    raise W4A16Error(rc, msg)
+
+
+def _stream_ptr(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _dev_tensor(t: torch.Tensor, dtype: torch.dtype, name: str) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype} (got {t.dtype})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _kernel_id(kernel) -> int:
+    if kernel is None:
+        return 0
+    if isinstance(kernel, str):
+        if kernel not in KERNELS:
+            raise ValueError(f"unknown kernel {kernel!r}; one of {sorted(KERNELS)}")
+        return KERNELS[kernel]
+    return int(kernel)
+
+
+@dataclass
+class W4Matrix:
+    """Packed W4A16 weights on the GPU.
+
+    Wq: int32 [.., N, K/8] (bit pattern of the uint32 words, eight codes each,
+    low nibble first); scales, biases: bfloat16 [.., N, K/64].  With E > 1
+    the leading dimension stacks E experts.
+    """
+
+    Wq: torch.Tensor
+    scales: torch.Tensor
+    biases: torch.Tensor
+    N: int
+    K: int
+    E: int = 1
+
+    def __post_init__(self):
+        lead = () if self.E == 1 else (self.E,)
+        if tuple(self.Wq.shape) != lead + (self.N, self.K // 8):
+            raise ValueError(f"Wq shape {tuple(self.Wq.shape)} does not match N={self.N}, K={self.K}, E={self.E}")
+        for name in ("scales", "biases"):
+            t = getattr(self, name)
+            if tuple(t.shape) != lead + (self.N, self.K // GROUP):
+                raise ValueError(f"{name} shape {tuple(t.shape)} does not match N={self.N}, K={self.K}")
+        _dev_tensor(self.Wq, torch.int32, "Wq")
+        _dev_tensor(self.scales, torch.bfloat16, "scales")
+        _dev_tensor(self.biases, torch.bfloat16, "biases")
+
+    @classmethod
+    def from_host(cls, host, device="cuda") -> "W4Matrix":
+        """From numpy arrays (``synth.HostW4``: uint32 codes, bf16 bit patterns)."""
+        wq = torch.from_numpy(host.Wq.view("int32")).to(device)
+        s = torch.from_numpy(host.scales.view("int16")).view(torch.bfloat16).to(device)
+        b = torch.from_numpy(host.biases.view("int16")).view(torch.bfloat16).to(device)
+        return cls(wq, s, b, host.N, host.K, host.E)
+
+    @property
+    def nbytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in (self.Wq, self.scales, self.biases))
+
+
+def mm(x: torch.Tensor, w: W4Matrix, out: torch.Tensor | None = None, kernel=None, stream=None) -> torch.Tensor:
+    """y[..., N] = x[..., K] W^T through ``w4a16_mm`` (leading dims flatten into M)."""
+    if w.E != 1:
+        raise ValueError("mm takes a single matrix; use mm_id for stacked experts")
+    _dev_tensor(x, torch.bfloat16, "x")
+    if x.shape[-1] != w.K:
+        raise ValueError(f"x has K={x.shape[-1]}, weights have K={w.K}")
+    M = x.numel() // w.K
+    if out is None:
+        out = torch.empty(*x.shape[:-1], w.N, dtype=torch.bfloat16, device=x.device)
+    _dev_tensor(out, torch.bfloat16, "out")
+    if out.numel() != M * w.N:
+        raise ValueError("out has the wrong number of elements")
+    L = lib()
+    k = _kernel_id(kernel)
+    args = (x.data_ptr(), w.Wq.data_ptr(), w.scales.data_ptr(), w.biases.data_ptr(), out.data_ptr(), M, w.N, w.K)
+    if k == 0:
+        rc = L.w4a16_mm(*args, _stream_ptr(stream))
+    else:
+        rc = L.w4a16_mm_kernel(*args, k, _stream_ptr(stream))
+    _raise(rc)
+    return out
+
+
+def mm_id(x: torch.Tensor, w: W4Matrix, ids: torch.Tensor, out: torch.Tensor | None = None, kernel=None,
+          stream=None) -> torch.Tensor:
+    """y[t] = W[ids[t]] x[t] through ``w4a16_mm_id``; x [T, K], ids int32 [T] on the GPU."""
+    _dev_tensor(x, torch.bfloat16, "x")
+    _dev_tensor(ids, torch.int32, "ids")
+    if x.dim() != 2 or x.shape[1] != w.K:
+        raise ValueError("x must be [T, K]")
+    T = x.shape[0]
+    if ids.numel() != T:
+        raise ValueError("ids must hold one expert id per token")
+    if out is None:
+        out = torch.empty(T, w.N, dtype=torch.bfloat16, device=x.device)
+    _dev_tensor(out, torch.bfloat16, "out")
+    L = lib()
+    rc = L.w4a16_mm_id_kernel(x.data_ptr(), w.Wq.data_ptr(), w.scales.data_ptr(), w.biases.data_ptr(),
+                              ids.data_ptr(), out.data_ptr(), T, w.N, w.K, w.E, _kernel_id(kernel),
+                              _stream_ptr(stream))
+    _raise(rc)
+    return out
+
+
+def unpack(w: W4Matrix, stream=None) -> torch.Tensor:
+    """Codes q[N][K] as uint8 through ``w4a16_unpack`` (bit-exact debug path)."""
+    q = torch.empty(w.N, w.K, dtype=torch.uint8, device=w.Wq.device)
+    _raise(lib().w4a16_unpack(w.Wq.data_ptr(), q.data_ptr(), w.N, w.K, _stream_ptr(stream)))
+    return q
+
+
+def dequant(w: W4Matrix, stream=None) -> torch.Tensor:
+    """fp32 weights fma(q, s, b) [N][K] through ``w4a16_dequant``."""
+    out = torch.empty(w.N, w.K, dtype=torch.float32, device=w.Wq.device)
+    _raise(lib().w4a16_dequant(w.Wq.data_ptr(), w.scales.data_ptr(), w.biases.data_ptr(), out.data_ptr(),
+                               w.N, w.K, _stream_ptr(stream)))
+    return out
+
+
+def get_plan(N: int, K: int, kernel=None) -> dict:
+    p = Plan()
+    _raise(lib().w4a16_get_plan(N, K, _kernel_id(kernel), ctypes.byref(p)))
+    return p.as_dict()
+
+
+def device_status(stream=None) -> int:
+    """Synchronise and return (then clear) the device flags; raises on CUDA errors only."""
+    flags = ctypes.c_int(0)
+    rc = lib().w4a16_device_status(_stream_ptr(stream), ctypes.byref(flags))
+    if rc not in (OK, ERR_DEVICE):
+        _raise(rc)
+    return flags.value
+
+
+def version() -> str:
+    return lib().w4a16_version().decode()

@@ -1,0 +1,167 @@
+"""The C-ABI library on the host: it loads, exports what include/*.h declares,
+and rejects bad arguments before any launch (no GPU needed).
+
+Fake device pointers below are never dereferenced: every call here fails in
+host validation (or is an M == 0 no-op) before the library touches CUDA.
+"""
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+from skinny_gemm_gb300 import _build, ops, synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+DECL = re.compile(r"^\s*(?:int|void|const char\s*\*)\s+(w4a16_\w+)\s*\(", re.M)
+
+P = 0x10000  # 16-byte-aligned fake address
+
+
+def _declared(header: str) -> list[str]:
+    return DECL.findall(open(os.path.join(ROOT, "include", header)).read())
+
+
+def _exported(path: str) -> set[str]:
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True, check=True).stdout
+    return {line.split()[-1] for line in out.splitlines() if line.strip()}
+
+
+def test_every_declared_symbol_is_exported():
+    headers = sorted(os.path.basename(h) for h in glob.glob(os.path.join(ROOT, "include", "*.h")))
+    assert headers == ["w4a16.h", "w4a16_synth.h"]
+    cuda_syms = _exported(_build.build_cuda())
+    decl = _declared("w4a16.h")
+    assert len(decl) >= 10
+    missing = [s for s in decl if s not in cuda_syms]
+    assert not missing, f"declared but not exported by libw4a16.so: {missing}"
+    synth_syms = _exported(_build.build_synth())
+    decl = _declared("w4a16_synth.h")
+    assert len(decl) == 6
+    assert not [s for s in decl if s not in synth_syms]
+    # the binding names exactly the exported C calls
+    assert set(ops.EXPORTS) <= cuda_syms
+
+
+@pytest.fixture()
+def L(monkeypatch):
+    monkeypatch.delenv("W4A16_FAULT", raising=False)
+    monkeypatch.delenv("W4A16_FORCE_KERNEL", raising=False)
+    lib = ops.lib()
+    lib.w4a16_debug_reload_env()
+    yield lib
+    monkeypatch.delenv("W4A16_FAULT", raising=False)
+    lib.w4a16_debug_reload_env()
+
+
+def _mm(L, x=P, w=P, s=P, b=P, y=P, M=1, N=256, K=512, kernel=None):
+    if kernel is None:
+        return L.w4a16_mm(x, w, s, b, y, M, N, K, None)
+    return L.w4a16_mm_kernel(x, w, s, b, y, M, N, K, kernel, None)
+
+
+def _err(L) -> str:
+    return L.w4a16_last_error().decode()
+
+
+def test_shape_errors(L):
+    assert _mm(L, K=100) == ops.ERR_SHAPE and "multiple of 64" in _err(L)
+    assert _mm(L, K=0) == ops.ERR_SHAPE
+    assert _mm(L, K=-64) == ops.ERR_SHAPE
+    assert _mm(L, N=0) == ops.ERR_SHAPE
+    assert _mm(L, N=-3) == ops.ERR_SHAPE
+    assert _mm(L, M=-1) == ops.ERR_SHAPE
+
+
+def test_null_and_alignment_errors(L):
+    assert _mm(L, x=None) == ops.ERR_NULL
+    assert _mm(L, y=None) == ops.ERR_NULL
+    assert _mm(L, x=P + 8) == ops.ERR_ALIGN
+    assert _mm(L, w=P + 4) == ops.ERR_ALIGN
+    assert _mm(L, s=P + 1) == ops.ERR_ALIGN
+    assert _mm(L, b=P + 4) == ops.ERR_ALIGN
+    assert _mm(L, y=P + 1) == ops.ERR_ALIGN
+    assert "16-byte" in (_mm(L, x=P + 2) and _err(L))
+
+
+def test_empty_batch_is_a_noop_without_cuda(L):
+    # M == 0 returns before any CUDA call, so it succeeds even with no GPU
+    assert _mm(L, x=None, w=None, s=None, b=None, y=None, M=0) == ops.OK
+    assert L.w4a16_mm_id(None, None, None, None, None, None, 0, 64, 64, 4, None) == ops.OK
+
+
+def test_unknown_kernel(L):
+    assert _mm(L, kernel=42) == ops.ERR_KERNEL
+
+
+def test_mm_id_errors(L):
+    assert L.w4a16_mm_id(P, P, P, P, P, P, 8, 64, 64, 0, None) == ops.ERR_EXPERTS
+    assert L.w4a16_mm_id(P, P, P, P, P, P, -1, 64, 64, 8, None) == ops.ERR_EXPERTS
+    assert L.w4a16_mm_id(P, P, P, P, P, P, 8, 64, 96, 8, None) == ops.ERR_SHAPE
+    assert L.w4a16_mm_id(P, P, P, P, P + 2, P, 8, 64, 64, 8, None) == ops.ERR_ALIGN
+    assert L.w4a16_mm_id(P, P, P, P, None, P, 8, 64, 64, 8, None) == ops.ERR_NULL
+
+
+def test_debug_entry_point_errors(L):
+    assert L.w4a16_unpack(P, P, 4, 12, None) == ops.ERR_SHAPE
+    assert L.w4a16_unpack(None, P, 4, 64, None) == ops.ERR_NULL
+    assert L.w4a16_dequant(P, P, P, P + 4, 4, 64, None) == ops.ERR_ALIGN
+    assert L.w4a16_dequant(P, P, P, P, 4, 32, None) == ops.ERR_SHAPE
+
+
+def test_injected_faults(L, monkeypatch):
+    monkeypatch.setenv("W4A16_FAULT", "validate")
+    L.w4a16_debug_reload_env()
+    assert _mm(L) == ops.ERR_SHAPE and "injected" in _err(L)
+    assert L.w4a16_mm_id(P, P, P, P, P, P, 8, 64, 64, 8, None) == ops.ERR_SHAPE
+    monkeypatch.setenv("W4A16_FAULT", "launch")
+    L.w4a16_debug_reload_env()
+    assert _mm(L) == ops.ERR_CUDA and "injected launch" in _err(L)
+    # arguments are still validated first
+    assert _mm(L, K=65) == ops.ERR_SHAPE
+
+
+def test_plans_depend_on_shape_only_and_fill_the_gpu(L):
+    shapes = [(256, 512), (2048, 2560), (512, 2560), (2560, 2048), (10240, 2560), (2560, 10240),
+              (12288, 1536), (1536, 12288), (262144, 1536), (262144, 2560), (16384, 16384), (6144, 2048)]
+    for N, K in shapes:
+        for kern in ("auto", "simt", "tc", "vanilla"):
+            p = ops.get_plan(N, K, kern)
+            assert p["units"] * p["rows_per_tile"] >= N or p["kernel"] == "tc"
+            assert p["ksplit"] * p["slice_k"] >= K or p["kernel"] == "simt"
+            assert p["ksplit"] >= 1 and p["threads"] % 32 == 0
+    with pytest.raises(ValueError):
+        ops.get_plan(100, 100)
+    with pytest.raises(ValueError):
+        ops.get_plan(100, 192, "tc")
+    assert ops.get_plan(100, 192)["kernel"] == "simt"
+    assert ops.get_plan(100, 2560)["kernel"] == "tc"
+    # the reduction order is a pure function of (N, K) -- the plan call has no M
+    for N, K in shapes:
+        a, b = ops.get_plan(N, K), ops.get_plan(N, K)
+        assert (a["ksplit"], a["slice_k"]) == (b["ksplit"], b["slice_k"])
+        if a["kernel"] == "tc":
+            assert (a["ksplit"] - 1) * a["slice_k"] < K <= a["ksplit"] * a["slice_k"]
+
+
+def test_split_plans_fit_the_fixed_workspace(L):
+    # the tensor-core kernel's workspace holds 4096 tile counters and 4864 unit partials
+    for K in (256, 512, 768, 1536, 2048, 2560, 4096, 10240, 12288, 16384, 65536):
+        for N in (1, 31, 32, 500, 1621 * 32, 2431 * 32, 2432 * 32, 5000 * 32, 262144):
+            p = ops.get_plan(N, K, "tc")
+            if p["ksplit"] > 1:
+                assert p["units"] <= 4864 and p["units"] // p["ksplit"] <= 4096, (N, K, p)
+
+
+def test_python_layer_rejects_host_tensors():
+    import torch
+    w = synth.make_weights(0, 64, 64)
+    with pytest.raises(ValueError):
+        ops.W4Matrix(torch.from_numpy(w.Wq.view("int32")), torch.zeros(64, 1, dtype=torch.bfloat16),
+                     torch.zeros(64, 1, dtype=torch.bfloat16), 64, 64)
+
+
+def test_version_string(L):
+    assert "sm_103a" in L.w4a16_version().decode()

@@ -1,0 +1,97 @@
+"""Lossless-verify invariance: row m of an M-row call equals the M = 1 call on
+x[m], bit for bit ("Gemma 4 E4B & E2B -- single-launch Metal megakernels"
+model card, "Measured performance": batch verify vs sequential, max abs diff
+0.0).  Also routed rows vs the plain call on the chosen expert."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_cases import (DECODE_SET, DENSE, EXPERTS, LM_HEADS, VERIFY_SHAPES, assert_parity, bf16_bits, dev_weights,
+                       to_dev_bf16)
+from skinny_gemm_gb300 import ops, synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _rows_equal_single(N, K, Ms, kernel="auto", seed=0):
+    w = dev_weights(seed, N, K)
+    Mmax = max(Ms)
+    x = to_dev_bf16(synth.make_x(21, Mmax, K))
+    singles = [bf16_bits(ops.mm(x[m:m + 1], w, kernel=kernel)) for m in range(Mmax)]
+    for M in Ms:
+        batch = bf16_bits(ops.mm(x[:M], w, kernel=kernel))
+        for m in range(M):
+            assert np.array_equal(batch[m], singles[m][0]), f"{N}x{K} {kernel}: row {m} of M={M} differs"
+
+
+@pytest.mark.parametrize("N,K", VERIFY_SHAPES + [DECODE_SET["k"], DECODE_SET["o"], (33, 2560), (1, 64)])
+def test_verify_rows_bitwise(N, K):
+    _rows_equal_single(N, K, [2, 3, 4, 5, 6, 7, 8, 9, 16])
+
+
+@pytest.mark.parametrize("kernel", ["simt", "tc", "vanilla"])
+def test_every_family_is_batch_invariant(kernel):
+    _rows_equal_single(1000, 3072, [3, 8, 11], kernel=kernel, seed=2)
+
+
+def test_lm_head_rows_bitwise():
+    N, K = LM_HEADS[0]
+    _rows_equal_single(N, K, [3], seed=4)
+
+
+def test_dense_rows_bitwise():
+    N, K = DENSE
+    _rows_equal_single(N, K, [2, 4, 8], seed=5)
+
+
+def test_row_order_and_neighbours_do_not_matter():
+    N, K = 2560, 10240
+    w = dev_weights(3, N, K)
+    x = to_dev_bf16(synth.make_x(22, 8, K))
+    a = bf16_bits(ops.mm(x, w))
+    perm = torch.tensor([5, 2, 7, 0, 1, 6, 3, 4], device="cuda")
+    b = bf16_bits(ops.mm(x[perm].contiguous(), w))
+    assert np.array_equal(a[perm.cpu().numpy()], b)
+
+
+def test_n_sharding_concatenates_bitwise():
+    """Splitting the output rows into independent launches (the multi-GPU
+    sharding, run here on one GPU) reproduces the unsharded call exactly
+    whenever a shard gets the same reduction plan (ksplit, slice_k) as the
+    full matrix; every shard stays within the oracle tolerance regardless."""
+    E_unused, N, K = EXPERTS
+    hw = synth.make_weights(8, N, K)
+    w = ops.W4Matrix.from_host(hw)
+    xb = synth.make_x(23, 3, K)
+    x = to_dev_bf16(xb)
+    full = bf16_bits(ops.mm(x, w))
+    full_plan = ops.get_plan(N, K)
+    same_plan = 0
+    for lo, hi in [(0, 1536), (1536, 4096), (4096, N), (0, 3072), (3072, N)]:
+        shard = synth.HostW4(hw.Wq[lo:hi].copy(), hw.scales[lo:hi].copy(), hw.biases[lo:hi].copy(), hi - lo, K)
+        part = bf16_bits(ops.mm(x, ops.W4Matrix.from_host(shard)))
+        pl = ops.get_plan(hi - lo, K)
+        if (pl["ksplit"], pl["slice_k"]) == (full_plan["ksplit"], full_plan["slice_k"]):
+            same_plan += 1
+            assert np.array_equal(part, full[:, lo:hi]), f"shard {lo}:{hi}"
+        else:
+            yr, ad = oracle.mm(xb, shard.Wq, shard.scales, shard.biases, 3, hi - lo, K)
+            assert_parity(torch.from_numpy(part.view(np.int16)).view(torch.bfloat16), yr, ad, f"shard {lo}:{hi}")
+    assert same_plan >= 1
+
+
+def test_mm_id_rows_equal_mm_on_selected_expert():
+    E, N, K = EXPERTS
+    hw = synth.make_weights(30, N, K, E)
+    w = ops.W4Matrix.from_host(hw)
+    T = 13
+    ids_np = synth.make_ids(30, T, E)
+    ids = torch.from_numpy(ids_np).cuda()
+    x = to_dev_bf16(synth.make_x(31, T, K))
+    y = bf16_bits(ops.mm_id(x, w, ids))
+    for t in range(T):
+        e = int(ids_np[t])
+        we = ops.W4Matrix(w.Wq[e].contiguous(), w.scales[e].contiguous(), w.biases[e].contiguous(), N, K)
+        ref = bf16_bits(ops.mm(x[t:t + 1], we))
+        assert np.array_equal(y[t], ref[0]), f"token {t} (expert {e})"

@@ -1,0 +1,75 @@
+"""Routed experts (w4a16_mm_id) vs the oracle, plus bad ids and empty calls."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_cases import EXPERTS, assert_parity, bf16_bits, sample_cols, to_dev_bf16
+from skinny_gemm_gb300 import ops, synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _experts(seed, E, N, K):
+    hw = synth.make_weights(seed, N, K, E)
+    return hw, ops.W4Matrix.from_host(hw)
+
+
+@pytest.mark.parametrize("kernel", ["auto", "simt", "tc", "vanilla"])
+def test_routed_experts_config(kernel):
+    E, N, K = EXPERTS
+    hw, w = _experts(0, E, N, K)
+    T = 8
+    ids_np = synth.make_ids(0, T, E)
+    xb = synth.make_x(0, T, K)
+    y = ops.mm_id(to_dev_bf16(xb), w, torch.from_numpy(ids_np).cuda(), kernel=kernel)
+    cols = sample_cols(N, 2048)
+    yr, ad = oracle.mm_id(xb, hw.Wq, hw.scales, hw.biases, ids_np, T, N, K, E, cols=cols,
+                          threads=oracle.host_threads())
+    assert_parity(y[:, torch.from_numpy(cols).cuda()], yr, ad, f"mm_id {kernel}")
+    assert ops.device_status() == 0
+
+
+@pytest.mark.parametrize("T,E", [(1, 1), (3, 5), (20, 3), (64, 8)])
+def test_routed_small_full(T, E):
+    N, K = 70, 512
+    hw, w = _experts(T * 10 + E, E, N, K)
+    ids_np = synth.make_ids(T, T, E)
+    xb = synth.make_x(E, T, K)
+    y = ops.mm_id(to_dev_bf16(xb), w, torch.from_numpy(ids_np).cuda())
+    yr, ad = oracle.mm_id(xb, hw.Wq, hw.scales, hw.biases, ids_np, T, N, K, E)
+    assert_parity(y, yr, ad, f"mm_id T={T} E={E}")
+
+
+def test_bad_ids_give_zero_rows_and_raise_the_flag():
+    E, N, K, T = 4, 40, 128, 6
+    hw, w = _experts(5, E, N, K)
+    ids_np = np.array([1, -1, 3, 4, 0, 99], dtype=np.int32)
+    xb = synth.make_x(5, T, K)
+    y = torch.full((T, N), 7.0, dtype=torch.bfloat16, device="cuda")
+    ops.mm_id(to_dev_bf16(xb), w, torch.from_numpy(ids_np).cuda(), out=y)
+    assert ops.device_status() & ops.DEVICE_BAD_ID
+    assert ops.device_status() == 0  # reading clears it
+    yr, ad = oracle.mm_id(xb, hw.Wq, hw.scales, hw.biases, ids_np, T, N, K, E)
+    assert_parity(y, yr, ad, "bad ids")
+    yb = bf16_bits(y)
+    for t in (1, 3, 5):
+        assert np.all(yb[t] == 0)
+
+
+def test_empty_token_list():
+    E, N, K = 3, 32, 64
+    _, w = _experts(6, E, N, K)
+    x = torch.empty(0, K, dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty(0, dtype=torch.int32, device="cuda")
+    assert ops.mm_id(x, w, ids).shape == (0, N)
+
+
+def test_all_tokens_on_one_expert_spans_chunks():
+    E, N, K, T = 4, 96, 256, 19
+    hw, w = _experts(7, E, N, K)
+    ids_np = np.full(T, 2, dtype=np.int32)
+    xb = synth.make_x(7, T, K)
+    y = ops.mm_id(to_dev_bf16(xb), w, torch.from_numpy(ids_np).cuda())
+    yr, ad = oracle.mm_id(xb, hw.Wq, hw.scales, hw.biases, ids_np, T, N, K, E)
+    assert_parity(y, yr, ad, "one expert, 19 tokens")
