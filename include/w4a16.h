@@ -106,6 +106,33 @@ int w4a16_mm_kernel(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* s
                     const w4a16_bf16* biases, w4a16_bf16* y, int M, int N, int K,
                     int kernel, void* stream);
 
+/* w4a16_mm for callers that must not allocate device memory (no counterpart
+ * on the pages; this is a deployment variant, not part of the method).
+ * Who needs it: code running inside an engine that reserved all device
+ * memory at start-up and hands out nothing more, processes under a hard
+ * device-memory cap where a late cudaMalloc could fail mid-service, and
+ * deployments that forbid allocation after initialisation.  w4a16_mm may
+ * cudaMalloc its split-K workspace on the first call on a stream; this
+ * entry point never calls cudaMalloc, cudaFree or any allocating routine.
+ *
+ * It runs the same tensor-core kernel with the same arithmetic, so its
+ * results equal w4a16_mm's bit for bit.  Its split-K scratch is one fixed
+ * 4,997,120-byte device array inside the library (16 KiB of tile counters +
+ * 4864 KiB of fp32 partials), which every GPU that loads the library holds
+ * until the process exits; every (N, K) with K % 256 == 0 fits in it, and a
+ * shape that would not is rejected with W4A16_ERR_SHAPE.  K % 256 != 0 is
+ * rejected with W4A16_ERR_KERNEL.
+ *
+ * The first call on a device looks up the array's device address and sets
+ * the kernel's shared-memory limit; make that first call before any CUDA
+ * graph capture.  All calls share the one array and it keeps the last
+ * call's contents: each call clears the counters it uses (a memset on
+ * `stream`) before its kernel.  Calls whose executions overlap on the GPU
+ * (different streams, or graphs replayed concurrently) race on the array;
+ * keep them ordered. */
+int w4a16_mm_noalloc(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* scales,
+                     const w4a16_bf16* biases, w4a16_bf16* y, int M, int N, int K, void* stream);
+
 /* Routed experts, top-1 (the W4A16 analogue of llama.cpp's mul_mat_id named
  * in [HY4] "What was missing and what this adds"):
  *   y[t][n] = sum_k x[t][k] * w_{ids[t]}[n][k]

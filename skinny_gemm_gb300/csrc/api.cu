@@ -234,6 +234,30 @@ int w4a16_dequant(const uint32_t* Wq, const w4a16_bf16* scales, const w4a16_bf16
   return e == cudaSuccess ? W4A16_OK : cuda_fail(e, "w4a16_dequant launch");
 }
 
+int w4a16_mm_noalloc(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* scales, const w4a16_bf16* biases,
+                     w4a16_bf16* y, int M, int N, int K, void* stream) {
+  if (int rc = validate_mm(x, Wq, scales, biases, y, M, N, K)) return rc;
+  if (!tc_supported(N, K))
+    return fail(W4A16_ERR_KERNEL, "w4a16_mm_noalloc runs the tensor-core kernel, which needs K %% 256 == 0 (K = %d)", K);
+  if (!tc_noalloc_fits(N, K))
+    return fail(W4A16_ERR_SHAPE, "N = %d, K = %d needs more than the %zu-byte fixed scratch of w4a16_mm_noalloc", N, K,
+                tc_noalloc_scratch_bytes());
+  if (M == 0) return W4A16_OK;
+  LaunchArgs a{};
+  a.x = x; a.Wq = Wq; a.S = scales; a.B = biases; a.y = y;
+  a.N = N; a.K = K;
+  a.stream = static_cast<cudaStream_t>(stream);
+  if (int rc = flag_pointer(&a.flags)) return rc;
+  for (int row0 = 0; row0 < M; row0 += kMaxChunk) {
+    a.row0 = row0;
+    a.M = (M - row0 < kMaxChunk) ? M - row0 : kMaxChunk;
+    cudaError_t e = launch_tc_noalloc(a);
+    if (e == cudaErrorInvalidValue) return fail(W4A16_ERR_SHAPE, "shape exceeds the fixed scratch of w4a16_mm_noalloc");
+    if (e != cudaSuccess) return cuda_fail(e, "w4a16_mm_noalloc launch");
+  }
+  return W4A16_OK;
+}
+
 int w4a16_get_plan(int N, int K, int kernel, w4a16_plan* out) {
   if (!out) return fail(W4A16_ERR_NULL, "null plan pointer");
   if (int rc = check_nk(N, K)) return rc;

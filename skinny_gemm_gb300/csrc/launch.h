@@ -39,6 +39,10 @@ void plan_tc(int N, int K, w4a16_plan* p);
 bool tc_supported(int N, int K);
 cudaError_t launch_tc(const LaunchArgs& a, const w4a16_plan& p);
 cudaError_t launch_tc_id(const LaunchArgs& a, const w4a16_plan& p);
+// Tensor-core w4a16_mm with its split-K scratch in a fixed device array (no allocation).
+cudaError_t launch_tc_noalloc(const LaunchArgs& a);
+size_t tc_noalloc_scratch_bytes();
+bool tc_noalloc_fits(int N, int K);
 
 void plan_vanilla(int N, int K, w4a16_plan* p);
 cudaError_t launch_vanilla(const LaunchArgs& a, const w4a16_plan& p);

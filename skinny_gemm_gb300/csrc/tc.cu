@@ -837,4 +837,84 @@ cudaError_t launch_tc_id(const LaunchArgs& a, const w4a16_plan& plan) {
   return cudaGetLastError();
 }
 
+
+// ---- no-allocation variant ----------------------------------------------------------------
+//
+// Some callers may not call cudaMalloc at all: code that runs inside an
+// engine which reserved all device memory up front and hands out nothing
+// else, processes under a hard device-memory cap where a late allocation can
+// fail in the middle of serving, and deployments that forbid any allocation
+// after start-up.  For them w4a16_mm_noalloc runs the same persistent kernel
+// as w4a16_mm, but its split-K workspace is this fixed array, which every GPU
+// that loads the library holds until the process exits.
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kWsBytes];
+
+// Device address of g_noalloc_scratch, looked up once per device.  In host
+// code the array's name is only a stand-in for the symbol, never a pointer a
+// kernel may use.
+void* g_noalloc_ptr[64] = {};
+
+}  // namespace
+
+size_t tc_noalloc_scratch_bytes() { return kWsBytes; }
+
+bool tc_noalloc_fits(int N, int K) {
+  const Shape s = tc_shape(N, K);
+  return s.ks == 1 || (s.tiles <= kWsTiles && s.units <= kWsUnits);
+}
+
+cudaError_t launch_tc_noalloc(const LaunchArgs& a) {
+  const Shape s = tc_shape(a.N, a.K);
+  if (s.ks > 1 && (s.tiles > kWsTiles || s.units > kWsUnits)) return cudaErrorInvalidValue;
+  int dev = 0;
+  if (cudaError_t e = cudaGetDevice(&dev)) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int sms;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo& d = device_info(dev);
+    sms = d.sms;
+    if (!d.attr_set[0]) {
+      if (cudaError_t e = cudaFuncSetAttribute(tc_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               kSmemLimit))
+        return e;
+      d.attr_set[0] = true;
+    }
+    if (!g_noalloc_ptr[dev]) {
+      void* ptr = nullptr;
+      if (cudaError_t e = cudaGetSymbolAddress((void**)&ptr, g_noalloc_scratch)) return e;
+      g_noalloc_ptr[dev] = ptr;
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+  StreamParams p;
+  p.x = a.x; p.S = a.S; p.B = a.B; p.y = a.y; p.flags = a.flags;
+  p.N = a.N; p.K = a.K; p.M = a.M; p.row0 = a.row0;
+  p.nst = s.nst; p.sl = s.sl; p.ks = s.ks; p.tiles = s.tiles; p.units = s.units;
+  p.stages = stream_stages(a.M);
+  p.part = nullptr;
+  p.cnt = nullptr;
+  if (s.ks > 1) {
+    p.cnt = static_cast<int*>(scratch);
+    p.part = reinterpret_cast<float*>(static_cast<char*>(scratch) + kWsCounterBytes);
+    // the array keeps whatever the previous call left: the counters must start at zero
+    if (cudaError_t e = cudaMemsetAsync(p.cnt, 0, (size_t)s.tiles * 4, a.stream)) return e;
+  }
+  CUtensorMap map;
+  if (cudaError_t e = make_code_map(&map, a.Wq, a.N, a.K)) return e;
+  const int smem = stream_smem(p.stages, a.M);
+  int per_sm = 0;
+  if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_stream_kernel, kStreamWarps * 32, smem))
+    return e;
+  if (per_sm < 1) per_sm = 1;
+  int grid = sms * per_sm;
+  const int need = (s.units + kStreamWarps - 1) / kStreamWarps;
+  if (grid > need) grid = need;
+  tc_stream_kernel<<<grid, kStreamWarps * 32, smem, a.stream>>>(map, p);
+  return cudaGetLastError();
+}
+
 }  // namespace w4a16

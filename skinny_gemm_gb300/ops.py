@@ -70,13 +70,14 @@ def lib() -> ctypes.CDLL:
             P, i = ctypes.c_void_p, ctypes.c_int
             L.w4a16_mm.argtypes = [P, P, P, P, P, i, i, i, P]
             L.w4a16_mm_kernel.argtypes = [P, P, P, P, P, i, i, i, i, P]
+            L.w4a16_mm_noalloc.argtypes = [P, P, P, P, P, i, i, i, P]
             L.w4a16_mm_id.argtypes = [P, P, P, P, P, P, i, i, i, i, P]
             L.w4a16_mm_id_kernel.argtypes = [P, P, P, P, P, P, i, i, i, i, i, P]
             L.w4a16_unpack.argtypes = [P, P, i, i, P]
             L.w4a16_dequant.argtypes = [P, P, P, P, i, i, P]
             L.w4a16_get_plan.argtypes = [i, i, i, ctypes.POINTER(Plan)]
             L.w4a16_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
-            for f in ("w4a16_mm", "w4a16_mm_kernel", "w4a16_mm_id", "w4a16_mm_id_kernel", "w4a16_unpack",
+            for f in ("w4a16_mm", "w4a16_mm_kernel", "w4a16_mm_noalloc", "w4a16_mm_id", "w4a16_mm_id_kernel", "w4a16_unpack",
                       "w4a16_dequant", "w4a16_get_plan", "w4a16_device_status"):
                 getattr(L, f).restype = ctypes.c_int
             L.w4a16_last_error.restype = ctypes.c_char_p
