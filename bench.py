@@ -14,9 +14,9 @@ over them is > 3x the L2 size, and step s uses copy s mod L, so every step
 streams its weights from HBM (no L2 flush needed).  Each copy's seven calls
 are captured once in a CUDA graph; the timed region replays K graphs between
 CUDA events on the launching stream, bracketed by a barrier and a
-synchronize.  Per-launch durations (roofline) come from external event nodes
-inside the graphs.  SM clocks are sampled with nvidia-smi during the timed
-region.
+synchronize.  Per-launch durations (roofline) come from a second pass over
+twin graphs that carry event nodes between the launches.  SM clocks are
+sampled with nvidia-smi during the timed region.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 Under torchrun (N > 1) every rank runs its own independent layers (weak
@@ -46,6 +46,11 @@ DECODE_LAYER = [("q", 2048, 2560), ("k", 512, 2560), ("v", 512, 2560), ("o", 256
                 ("gate", 10240, 2560), ("up", 10240, 2560), ("down", 2560, 10240)]
 WORKLOAD = ("W4A16 g64 decode-layer projection set at M=1, hidden 2560: q 2048x2560, k 512x2560, "
             "v 512x2560, o 2560x2048, gate 10240x2560, up 10240x2560, down 2560x10240")
+# Single workloads for --case: name -> (N, K, E)
+CASES = {"q": (2048, 2560, 1), "kv": (512, 2560, 1), "o": (2560, 2048, 1), "gate": (10240, 2560, 1),
+         "down": (2560, 10240, 1), "wide_up": (12288, 1536, 1), "wide_down": (1536, 12288, 1),
+         "lm_head_1536": (262144, 1536, 1), "lm_head_2560": (262144, 2560, 1), "dense_16384": (16384, 16384, 1),
+         "routed": (6144, 2048, 8)}
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 
@@ -60,6 +65,10 @@ def parse_args():
     ap.add_argument("--no-extras", action="store_true", help="skip the per-config context measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work budget of the oracle baseline")
+    ap.add_argument("--case", default=None,
+                    help="time one workload alone instead of the step: " + ", ".join(sorted(CASES)) +
+                         " (with --M; eager launches over rotating cold copies; handy under ncu)")
+    ap.add_argument("--M", type=int, default=1, help="activation rows for --case")
     return ap.parse_args()
 
 
@@ -245,18 +254,23 @@ def run_ours(args, world, rank, local):
         if evs is not None:
             evs[len(DECODE_LAYER)].record()
 
-    graphs, graph_events = [], []
+    graphs, ev_graphs, graph_events = [], [], []
     with torch.cuda.stream(stream):
         for layer in layers:  # eager warm-up of every launch before capture
             enqueue_layer(layer)
         torch.cuda.synchronize()
         for layer in layers:
             g = torch.cuda.CUDAGraph()
-            evs = [make_ev() for _ in range(len(DECODE_LAYER) + 1)] if external_ok else None
             with torch.cuda.graph(g, stream=stream):
-                enqueue_layer(layer, evs)
+                enqueue_layer(layer)
             graphs.append(g)
-            graph_events.append(evs)
+            if external_ok:  # a twin graph with event nodes between the launches
+                ge = torch.cuda.CUDAGraph()
+                evs = [make_ev() for _ in range(len(DECODE_LAYER) + 1)]
+                with torch.cuda.graph(ge, stream=stream):
+                    enqueue_layer(layer, evs)
+                ev_graphs.append(ge)
+                graph_events.append(evs)
     torch.cuda.synchronize()
 
     def replay(s):
@@ -285,9 +299,15 @@ def run_ours(args, world, rank, local):
     ms_per_step = ms_total / args.steps
     value = world * step_bytes * args.steps / (ms_total * 1e-3) / 1e9
 
-    # per-launch durations of the timed kernel: the last replay of every graph
+    # Per-launch durations of the timed kernel, from a second pass over the
+    # same rotating layers whose graphs carry event nodes between launches.
     launch_ms, launch_bytes = [], []
     if external_ok:
+        with torch.cuda.stream(stream):
+            for rep in range(3):
+                for ge in ev_graphs:
+                    ge.replay()
+        torch.cuda.synchronize()
         for evs in graph_events:
             for i, (_, N, K) in enumerate(DECODE_LAYER):
                 launch_ms.append(evs[i].elapsed_time(evs[i + 1]))
@@ -335,7 +355,8 @@ def run_ours(args, world, rank, local):
                          if peak_kind == "measured" else "fallback 6.8 TB/s",
                          "frac_of_nominal_8TBps": round(achieved / NOMINAL_HBM_GBS, 4),
                          "launches_timed": len(launch_ms),
-                         "timing": "external events inside the graphs" if external_ok else "events behind spin"},
+                         "timing": ("per-launch event nodes in twin graphs, replayed after the timed region"
+                                    if external_ok else "events behind a spin kernel")},
             "per_matrix": per_matrix,
             "e2e": e2e,
             "gpu_launches": args.steps * len(DECODE_LAYER),
@@ -542,9 +563,49 @@ def run_reference(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def run_case(args):
+    """One workload, `steps` eager launches round-robin over cold copies."""
+    import torch
+    from skinny_gemm_gb300 import ops, roofline, synth
+    N, K, E = CASES[args.case]
+    M = args.M
+    l2 = int(getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 126 * 2**20))
+    hw = synth.make_weights(11, N, K, E)
+    base = ops.W4Matrix.from_host(hw)
+    copies = max(1, math.ceil(3 * l2 / base.nbytes))
+    ws = [base] + [ops.W4Matrix(base.Wq.clone(), base.scales.clone(), base.biases.clone(), N, K, E)
+                   for _ in range(copies - 1)]
+    x = torch.randn(M, K, device="cuda").to(torch.bfloat16)
+    y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    if E > 1:
+        ids_np = synth.make_ids(0, M, E)
+        ids = torch.from_numpy(ids_np).cuda()
+        call = lambda w: ops.mm_id(x, w, ids, out=y, kernel=args.kernel)  # noqa: E731
+        nbytes = roofline.mm_id_bytes(ids_np, M, N, K, E)[0]
+    else:
+        call = lambda w: ops.mm(x, w, out=y, kernel=args.kernel)  # noqa: E731
+        nbytes = roofline.mm_bytes(M, N, K)
+    for i in range(args.warmup):
+        call(ws[i % copies])
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(20_000_000)  # queue the launches behind a spin so the CPU never starves the GPU
+    a.record()
+    for i in range(args.steps):
+        call(ws[i % copies])
+    b.record()
+    torch.cuda.synchronize()
+    us = 1e3 * a.elapsed_time(b) / args.steps
+    print(json.dumps({"case": args.case, "M": M, "N": N, "K": K, "E": E, "us_per_call": round(us, 3),
+                      "GBps": round(nbytes / (us * 1e-6) / 1e9, 1), "plan": ops.get_plan(N, K, args.kernel)}))
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_env()
+    if args.case:
+        run_case(args)
+        return
     if args.impl == "reference":
         run_reference(args, world, rank, local)
     else:

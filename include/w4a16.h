@@ -91,7 +91,7 @@ typedef enum {
   W4A16_KERNEL_AUTO = 0,    /* the dispatcher's choice for (N, K) */
   W4A16_KERNEL_SIMT = 1,    /* CUDA-core kernel: fp32 FMA, warp-shuffle split-K */
   W4A16_KERNEL_TC = 2,      /* tensor-core kernel: TMA-fed bf16 MMA on codes, fp32 group
-                               rescale; needs K % 256 == 0 */
+                               rescale; needs K % 512 == 0 */
   W4A16_KERNEL_VANILLA = 3  /* debug control: one thread per output, no sharing */
 } w4a16_kernel;
 
@@ -119,8 +119,8 @@ int w4a16_mm_kernel(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* s
  * results equal w4a16_mm's bit for bit.  Its split-K scratch is one fixed
  * 4,997,120-byte device array inside the library (16 KiB of tile counters +
  * 4864 KiB of fp32 partials), which every GPU that loads the library holds
- * until the process exits; every (N, K) with K % 256 == 0 fits in it, and a
- * shape that would not is rejected with W4A16_ERR_SHAPE.  K % 256 != 0 is
+ * until the process exits; every (N, K) with K % 512 == 0 fits in it, and a
+ * shape that would not is rejected with W4A16_ERR_SHAPE.  K % 512 != 0 is
  * rejected with W4A16_ERR_KERNEL.
  *
  * The first call on a device looks up the array's device address and sets

@@ -107,14 +107,14 @@ int check_nk(int N, int K) {
 int resolve_kernel(int requested, int N, int K, w4a16_plan* plan) {
   int k = requested;
   if (k == W4A16_KERNEL_AUTO) k = env().force_kernel;
-  // Default: the tensor-core family wherever it applies (K % 256 == 0), the
+  // Default: the tensor-core family wherever it applies (K % 512 == 0), the
   // CUDA-core family otherwise.  The choice depends on (N, K) only.
   if (k == W4A16_KERNEL_AUTO) k = tc_supported(N, K) ? W4A16_KERNEL_TC : W4A16_KERNEL_SIMT;
   switch (k) {
     case W4A16_KERNEL_SIMT: plan_simt(N, K, plan); return W4A16_OK;
     case W4A16_KERNEL_VANILLA: plan_vanilla(N, K, plan); return W4A16_OK;
     case W4A16_KERNEL_TC:
-      if (!tc_supported(N, K)) return fail(W4A16_ERR_KERNEL, "the tensor-core kernel needs K %% 256 == 0 (K = %d)", K);
+      if (!tc_supported(N, K)) return fail(W4A16_ERR_KERNEL, "the tensor-core kernel needs K %% 512 == 0 (K = %d)", K);
       plan_tc(N, K, plan);
       return W4A16_OK;
     default: return fail(W4A16_ERR_KERNEL, "unknown kernel selector %d", requested);
@@ -238,7 +238,7 @@ int w4a16_mm_noalloc(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* 
                      w4a16_bf16* y, int M, int N, int K, void* stream) {
   if (int rc = validate_mm(x, Wq, scales, biases, y, M, N, K)) return rc;
   if (!tc_supported(N, K))
-    return fail(W4A16_ERR_KERNEL, "w4a16_mm_noalloc runs the tensor-core kernel, which needs K %% 256 == 0 (K = %d)", K);
+    return fail(W4A16_ERR_KERNEL, "w4a16_mm_noalloc runs the tensor-core kernel, which needs K %% 512 == 0 (K = %d)", K);
   if (!tc_noalloc_fits(N, K))
     return fail(W4A16_ERR_SHAPE, "N = %d, K = %d needs more than the %zu-byte fixed scratch of w4a16_mm_noalloc", N, K,
                 tc_noalloc_scratch_bytes());

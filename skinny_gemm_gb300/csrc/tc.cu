@@ -66,11 +66,29 @@
 namespace w4a16 {
 namespace {
 
+// Tuning knobs (compile-time; the defaults are the measured choice).
+#ifndef W4A16_TC_MIN_BLOCKS
+#define W4A16_TC_MIN_BLOCKS 3      // persistent CTAs per SM the register budget must allow
+#endif
+#ifndef W4A16_TC_MAX_STAGES
+#define W4A16_TC_MAX_STAGES 4      // deepest per-warp ring
+#endif
+#ifndef W4A16_TC_SMEM_TARGET
+#define W4A16_TC_SMEM_TARGET (76 * 1024)  // shared memory per CTA the ring depth aims below
+#endif
+#ifndef W4A16_TC_GROUP_BATCH
+#define W4A16_TC_GROUP_BATCH 2     // 64-groups whose loads and MMA chains are interleaved
+#endif
+
 constexpr int kTileRows = 32;           // two m16 subtiles per warp
-constexpr int kStageK = 256;            // codes per stage per row (one 128-byte box row)
+constexpr int kBoxWords = 32;           // one TMA box row: 128 bytes = 256 codes
+constexpr int kBoxBytes = kTileRows * kBoxWords * 4;            // 4096
+constexpr int kStageK = 512;            // codes per stage per row (two boxes)
 constexpr int kStageWords = kStageK / 8;
-constexpr int kCodeSlotBytes = kTileRows * kStageWords * 4;  // 4096
-constexpr int kXPitch = kStageK * 2 + 64;                     // 576: conflict-free LDS.128
+constexpr int kCodeBytes = 2 * kBoxBytes;                        // 8192 codes per stage
+constexpr int kParamBytes = kTileRows * 8 * 2;                   // 512: 8 bf16 per row per stage
+constexpr int kCodeSlotBytes = kCodeBytes + 2 * kParamBytes;     // 9216: codes | scales | biases
+constexpr int kXPitch = kStageK * 2 + 64;                        // 1088: conflict-free LDS.128
 constexpr int kStreamWarps = 4;          // warps per CTA of the persistent kernel
 constexpr int kRoutedWarps = 8;          // max warps per CTA of the routed kernel
 constexpr int kTargetUnits = 152 * 16;   // work units wanted per chunk (~16 per SM)
@@ -116,17 +134,35 @@ __device__ __forceinline__ uint32_t ordered(uint32_t v) {
   return r;
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int cx, int cy, uint32_t bar) {
+// L2 eviction policies: the packed codes are read exactly once and go first;
+// activations and group parameters are reused and should stay.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int cx, int cy, uint32_t bar,
+                                            uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-      ::"r"(dst), "l"(map), "r"(cx), "r"(cy), "r"(bar)
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;"
+      ::"r"(dst), "l"(map), "r"(cx), "r"(cy), "r"(bar), "l"(policy)
       : "memory");
 }
 
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -164,11 +200,6 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint2 ldg_params(const uint16_t* p) {
-  uint2 v;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-  return v;
-}
 
 __device__ __forceinline__ float half_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float half_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
@@ -179,19 +210,31 @@ struct Ring {
   uint32_t codes0, xs0, bars0;
   int S, x_slot;
   uint32_t issued, consumed;
+  uint64_t pol_stream, pol_keep;
 };
 
-// Lane 0 only: start the loads of one stage (codes of rows tensor_row.., x of
-// the listed activation rows) into the next free slot.
-__device__ __forceinline__ void ring_issue(Ring& R, const CUtensorMap* map, int st, int tensor_row,
+// Lane 0 only: start the loads of stage `st` (codes of 32 rows from
+// tensor_row: two 128-byte boxes; x of the listed activation rows) into the
+// next free slot.
+struct Maps {
+  CUtensorMap codes;   // u32 [rows][K/8], box 32 words x 32 rows, 128-byte swizzle
+  CUtensorMap scales;  // bf16 [rows][K/64], box 8 groups x 32 rows
+  CUtensorMap biases;
+};
+
+__device__ __forceinline__ void ring_issue(Ring& R, const Maps* maps, int st, int tensor_row,
                                            const uint16_t* x, const int* toks, int mc, int K) {
   const uint32_t slot = R.issued % (uint32_t)R.S;
   const uint32_t bar = R.bars0 + 8 * slot;
+  const uint32_t dst = R.codes0 + slot * kCodeSlotBytes;
   mbar_expect_tx(bar, kCodeSlotBytes + (uint32_t)(mc * kStageK * 2));
-  tma_load_2d(R.codes0 + slot * kCodeSlotBytes, map, st * kStageWords, tensor_row, bar);
+  tma_load_2d(dst, &maps->codes, st * kStageWords, tensor_row, bar, R.pol_stream);
+  tma_load_2d(dst + kBoxBytes, &maps->codes, st * kStageWords + kBoxWords, tensor_row, bar, R.pol_stream);
+  tma_load_2d(dst + kCodeBytes, &maps->scales, st * 8, tensor_row, bar, R.pol_keep);
+  tma_load_2d(dst + kCodeBytes + kParamBytes, &maps->biases, st * 8, tensor_row, bar, R.pol_keep);
+  const uint16_t* xs = x + (int64_t)st * kStageK;
   for (int n = 0; n < mc; ++n)
-    bulk_load(R.xs0 + slot * R.x_slot + n * kXPitch, x + (int64_t)toks[n] * K + (int64_t)st * kStageK,
-              kStageK * 2, bar);
+    bulk_load(R.xs0 + slot * R.x_slot + n * kXPitch, xs + (int64_t)toks[n] * K, kStageK * 2, bar, R.pol_keep);
   ++R.issued;
 }
 
@@ -203,80 +246,115 @@ __device__ __forceinline__ bool ring_wait(Ring& R, uint32_t& slot) {
   return __all_sync(0xffffffffu, ok);
 }
 
-// Group parameters (scale, bias) of the 4 groups of stage `st` for this
-// lane's rows prow[i] (matrix rows; rows >= N read nothing).
-__device__ __forceinline__ void load_params(const uint16_t* Se, const uint16_t* Be, const int (&prow)[4], int N,
-                                            int groups_per_row, int st, uint2 (&sv)[4], uint2 (&bv)[4]) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    if (prow[i] < N) {
-      const int64_t off = (int64_t)prow[i] * groups_per_row + st * (kStageK / kGroup);
-      sv[i] = ldg_params(Se + off);
-      bv[i] = ldg_params(Be + off);
-    } else {
-      sv[i] = make_uint2(0, 0);
-      bv[i] = make_uint2(0, 0);
-    }
-  }
+__device__ __forceinline__ uint32_t component(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-// One stage (32 rows x 256 codes) of the canonical recurrence into p[s][i]:
-// subtile s, i = (row g: tokens 2t, 2t+1; row g+8: tokens 2t, 2t+1).
-__device__ __forceinline__ void compute_stage(uint32_t cbase, uint32_t xbase, bool xvalid, const uint2 (&ps)[4],
-                                              const uint2 (&pb)[4], float (&p)[2][4], int lane) {
+// Per-lane byte offsets of the ldmatrix rows inside a 128-byte-swizzled box,
+// for subtile s and group-in-box gl: rows g / g+8, chunks 2gl and 2gl+1.
+__device__ __forceinline__ void ldsm_offsets(int lane, uint32_t (&off)[2][4]) {
+  const int mi = lane >> 3, r8 = lane & 7;
 #pragma unroll
-  for (int gi = 0; gi < 4; ++gi) {
-    uint32_t bx[2][2][2];
+  for (int s = 0; s < 2; ++s)
 #pragma unroll
-    for (int cb = 0; cb < 2; ++cb) {
-      uint4 u = make_uint4(0, 0, 0, 0);
-      if (xvalid) u = lds128(xbase + 128 * gi + 64 * cb);
-      bx[cb][0][0] = prmt(u.x, u.z, 0x5410);
-      bx[cb][0][1] = prmt(u.x, u.z, 0x7632);
-      bx[cb][1][0] = prmt(u.y, u.w, 0x5410);
-      bx[cb][1][1] = prmt(u.y, u.w, 0x7632);
+    for (int gl = 0; gl < 4; ++gl) {
+      const int row = 16 * s + 8 * (mi & 1) + r8;
+      const int chunk = 2 * gl + (mi >> 1);
+      off[s][gl] = (uint32_t)(row * 128 + ((chunk ^ r8) << 4));
     }
-    float sx[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int cb = 0; cb < 2; ++cb)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) mma_bf16(sx, kOnes, kOnes, kOnes, kOnes, bx[cb][h][0], bx[cb][h][1]);
+}
 
+// One stage (32 rows x 512 codes, 8 groups) of the canonical recurrence into
+// p[s][i]: subtile s, i = (row g: columns 2t, 2t+1; row g+8: columns 2t,
+// 2t+1).  GB groups at a time: their loads are issued first and their MMA
+// chains interleaved.  With ALLCOLS false (one activation row) the odd
+// columns are not rescaled; the even columns' arithmetic is unchanged.
+template <bool ALLCOLS>
+__device__ __forceinline__ void compute_stage(uint32_t cbase, uint32_t xbase, bool xvalid, float (&p)[2][4],
+                                              const uint32_t (&loff)[2][4], int g) {
+  constexpr int GB = W4A16_TC_GROUP_BATCH;
+  // scale / bias of the 8 groups for this lane's rows 16(i>>1) + g + 8(i&1)
+  uint4 ps[4], pb[4];
 #pragma unroll
-    for (int s = 0; s < 2; ++s) {
-      uint32_t w[4];  // rows g / g+8 for chunk 2gi, then for chunk 2gi+1
-      {
-        const int mi = lane >> 3, r8 = lane & 7;
-        const int row = 16 * s + 8 * (mi & 1) + r8;
-        const int chunk = 2 * gi + (mi >> 1);
-        ldsm_x4(cbase + row * 128 + ((chunk ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
-      }
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t r = 16 * (i >> 1) + g + 8 * (i & 1);
+    ps[i] = lds128(cbase + kCodeBytes + r * 16);
+    pb[i] = lds128(cbase + kCodeBytes + kParamBytes + r * 16);
+  }
+#pragma unroll
+  for (int gp = 0; gp < 8; gp += GB) {
+    uint32_t w[GB][2][4];  // [group][subtile]: rows g / g+8 of chunk 2gl, then of chunk 2gl+1
+    uint4 u[GB][2];        // [group][chunk] activations
+#pragma unroll
+    for (int j = 0; j < GB; ++j) {
+      const int gi = gp + j;
+#pragma unroll
+      for (int s = 0; s < 2; ++s)
+        ldsm_x4(cbase + (gi >> 2) * kBoxBytes + loff[s][gi & 3], w[j][s][0], w[j][s][1], w[j][s][2], w[j][s][3]);
 #pragma unroll
       for (int cb = 0; cb < 2; ++cb) {
-        const uint32_t wg = w[2 * cb], wg8 = w[2 * cb + 1];
+        u[j][cb] = make_uint4(0, 0, 0, 0);
+        if (xvalid) u[j][cb] = lds128(xbase + 128 * gi + 64 * cb);
+      }
+    }
+    uint32_t bx[GB][2][2][2];  // [group][chunk][h][reg]
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+    for (int j = 0; j < GB; ++j)
+#pragma unroll
+      for (int cb = 0; cb < 2; ++cb) {
+        bx[j][cb][0][0] = prmt(u[j][cb].x, u[j][cb].z, 0x5410);
+        bx[j][cb][0][1] = prmt(u[j][cb].x, u[j][cb].z, 0x7632);
+        bx[j][cb][1][0] = prmt(u[j][cb].y, u[j][cb].w, 0x5410);
+        bx[j][cb][1][1] = prmt(u[j][cb].y, u[j][cb].w, 0x7632);
+      }
+    float sx[GB][4], acc[GB][2][4];
+#pragma unroll
+    for (int j = 0; j < GB; ++j)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        sx[j][i] = 0.f;
+        acc[j][0][i] = 0.f;
+        acc[j][1][i] = 0.f;
+      }
+    // the four (chunk, h) steps of every chain, in the canonical order, chains interleaved
+#pragma unroll
+    for (int step = 0; step < 4; ++step) {
+      const int cb = step >> 1, h = step & 1;
+#pragma unroll
+      for (int j = 0; j < GB; ++j) {
+        mma_bf16(sx[j], kOnes, kOnes, kOnes, kOnes, bx[j][cb][h][0], bx[j][cb][h][1]);
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          const uint32_t wg = w[j][s][2 * cb], wg8 = w[j][s][2 * cb + 1];
           const uint32_t a0 = codes_as_bf16x2(wg >> (8 * h));
           const uint32_t a1 = codes_as_bf16x2(wg8 >> (8 * h));
           const uint32_t a2 = codes_as_bf16x2(wg >> (8 * h + 4));
           const uint32_t a3 = codes_as_bf16x2(wg8 >> (8 * h + 4));
-          mma_bf16(acc, a0, a1, a2, a3, bx[cb][h][0], bx[cb][h][1]);
+          mma_bf16(acc[j][s], a0, a1, a2, a3, bx[j][cb][h][0], bx[j][cb][h][1]);
         }
       }
+    }
+    // group rescale, groups in order
 #pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const int i = 2 * s + rr;
-        const uint32_t sw = (gi < 2) ? ps[i].x : ps[i].y;
-        const uint32_t bw = (gi < 2) ? pb[i].x : pb[i].y;
-        const float sc = (gi & 1) ? half_hi(sw) : half_lo(sw);
-        const float bi = (gi & 1) ? half_hi(bw) : half_lo(bw);
-        const float cc = __fmaf_rn(-128.0f, sc, bi);
-        p[s][2 * rr + 0] = __fmaf_rn(sc, acc[2 * rr + 0], p[s][2 * rr + 0]);
-        p[s][2 * rr + 0] = __fmaf_rn(cc, sx[0], p[s][2 * rr + 0]);
-        p[s][2 * rr + 1] = __fmaf_rn(sc, acc[2 * rr + 1], p[s][2 * rr + 1]);
-        p[s][2 * rr + 1] = __fmaf_rn(cc, sx[1], p[s][2 * rr + 1]);
-      }
+    for (int j = 0; j < GB; ++j) {
+      const int gi = gp + j;
+#pragma unroll
+      for (int s = 0; s < 2; ++s)
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          const int i = 2 * s + rr;
+          const uint32_t sw = component(ps[i], gi >> 1);
+          const uint32_t bw = component(pb[i], gi >> 1);
+          const float sc = (gi & 1) ? half_hi(sw) : half_lo(sw);
+          const float bi = (gi & 1) ? half_hi(bw) : half_lo(bw);
+          const float cc = __fmaf_rn(-128.0f, sc, bi);
+          p[s][2 * rr + 0] = __fmaf_rn(sc, acc[j][s][2 * rr + 0], p[s][2 * rr + 0]);
+          p[s][2 * rr + 0] = __fmaf_rn(cc, sx[j][0], p[s][2 * rr + 0]);
+          if (ALLCOLS) {
+            p[s][2 * rr + 1] = __fmaf_rn(sc, acc[j][s][2 * rr + 1], p[s][2 * rr + 1]);
+            p[s][2 * rr + 1] = __fmaf_rn(cc, sx[j][1], p[s][2 * rr + 1]);
+          }
+        }
     }
   }
 }
@@ -317,15 +395,35 @@ struct StreamParams {
   int stages;
 };
 
-__global__ void __launch_bounds__(kStreamWarps * 32, 3) tc_stream_kernel(const __grid_constant__ CUtensorMap tmW,
-                                                                      StreamParams p) {
+// Position of a work unit u = tile * ks + slice, advanced by a fixed stride
+// without divisions.
+struct UnitCursor {
+  int u, tile, slice;
+  __device__ __forceinline__ void init(int u0, int ks) {
+    u = u0;
+    tile = u0 / ks;
+    slice = u0 - tile * ks;
+  }
+  __device__ __forceinline__ void advance(int step, int step_tiles, int step_slices, int ks) {
+    u += step;
+    tile += step_tiles;
+    slice += step_slices;
+    if (slice >= ks) {
+      slice -= ks;
+      ++tile;
+    }
+  }
+};
+
+template <bool ALLCOLS>
+__global__ void __launch_bounds__(kStreamWarps * 32, W4A16_TC_MIN_BLOCKS) tc_stream_kernel(
+    const __grid_constant__ Maps maps, StreamParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int S = p.stages, mc = p.M;
   const int x_slot = mc * kXPitch;
-  const int groups_per_row = p.K / kGroup;
 
   // layout: codes ring of every warp | x ring of every warp | barriers | tokens
   Ring R;
@@ -337,6 +435,8 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 3) tc_stream_kernel(const _
   R.bars0 = smem_u32(base) + bar_off + (uint32_t)(warp * S * 8);
   int* s_tok = reinterpret_cast<int*>(base + bar_off + kStreamWarps * S * 8);
   R.issued = R.consumed = 0;
+  R.pol_stream = policy_evict_first();
+  R.pol_keep = policy_evict_last();
 
   if (lane == 0)
     for (int i = 0; i < S; ++i) mbar_init(R.bars0 + 8 * i, 1);
@@ -348,20 +448,23 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 3) tc_stream_kernel(const _
   const int gw = warp * gridDim.x + blockIdx.x;
   const int TW = gridDim.x * kStreamWarps;
   if (gw >= p.units) return;
+  const int tw_tiles = TW / p.ks, tw_slices = TW - tw_tiles * p.ks;
 
-  // issue cursor: unit iu, stage ist (stages of a unit are [slice*sl, ...))
-  int iu = gw;
-  int ist = (iu % p.ks) * p.sl;
-  auto unit_end = [&](int u) {
-    const int e = (u % p.ks + 1) * p.sl;
-    return e < p.nst ? e : p.nst;
-  };
+  uint32_t loff[2][4];
+  ldsm_offsets(lane, loff);
+
+  // issue cursor (lane 0): unit, stage, end of the unit's stages
+  UnitCursor ic;
+  ic.init(gw, p.ks);
+  int ist = ic.slice * p.sl;
+  int iend = min(ist + p.sl, p.nst);
   auto issue_next = [&]() {
-    if (iu >= p.units) return;
-    ring_issue(R, &tmW, ist, (iu / p.ks) * kTileRows, p.x, s_tok, mc, p.K);
-    if (++ist == unit_end(iu)) {
-      iu += TW;
-      if (iu < p.units) ist = (iu % p.ks) * p.sl;
+    if (ic.u >= p.units) return;
+    ring_issue(R, &maps, ist, ic.tile * kTileRows, p.x, s_tok, mc, p.K);
+    if (++ist == iend) {
+      ic.advance(TW, tw_tiles, tw_slices, p.ks);
+      ist = ic.slice * p.sl;
+      iend = min(ist + p.sl, p.nst);
     }
   };
   if (lane == 0) {
@@ -373,8 +476,11 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 3) tc_stream_kernel(const _
   int pend_tile = -1, pend_old = 0;
 
   auto reduce_tile = [&](int tile) {
-    // Sum the ksplit partials of a finished tile in slice order.
-    __threadfence();
+    // Sum the ksplit partials of a finished tile in slice order.  Lane 0's
+    // fence (after it saw the last arrival) and the warp barrier order every
+    // lane's loads after the other units' partial stores.
+    if (lane == 0) __threadfence();
+    __syncwarp();
     const int row = tile * kTileRows + lane;
     for (int n = 0; n < mc; ++n) {
       const float* q = p.part + ((int64_t)tile * p.ks * 8 + n) * 32 + lane;
@@ -385,12 +491,20 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 3) tc_stream_kernel(const _
     if (lane == 0) p.cnt[tile] = 0;
   };
 
-  for (int u = gw; u < p.units && !timed_out; u += TW) {
-    const int tile = u / p.ks, slice = u % p.ks;
-    const int s0 = slice * p.sl, s1 = unit_end(u);
-    int prow[4];
+  auto rows_of = [&](int tile, int (&pr)[4]) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) prow[i] = tile * kTileRows + 16 * (i >> 1) + g + 8 * (i & 1);
+    for (int i = 0; i < 4; ++i) pr[i] = tile * kTileRows + 16 * (i >> 1) + g + 8 * (i & 1);
+  };
+
+  // consume cursor
+  UnitCursor cc;
+  cc.init(gw, p.ks);
+
+  for (; cc.u < p.units && !timed_out;) {
+    const int tile = cc.tile;
+    const int s0 = cc.slice * p.sl, s1 = min(s0 + p.sl, p.nst);
+    int prow[4];
+    rows_of(tile, prow);
 
     float acc[2][4];
 #pragma unroll
@@ -398,29 +512,20 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 3) tc_stream_kernel(const _
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[s][i] = 0.0f;
 
-    uint2 ps[4], pb[4];
-    load_params(p.S, p.B, prow, p.N, groups_per_row, s0, ps, pb);
     for (int st = s0; st < s1; ++st) {
       uint32_t slot;
       if (!ring_wait(R, slot)) {
         timed_out = true;
         break;
       }
-      uint2 ns[4] = {}, nb[4] = {};
-      if (st + 1 < s1) load_params(p.S, p.B, prow, p.N, groups_per_row, st + 1, ns, nb);
       const uint32_t cbase = ordered(R.codes0 + slot * kCodeSlotBytes);
       const uint32_t xbase = ordered(R.xs0 + slot * x_slot + g * kXPitch + 16 * t);
-      compute_stage(cbase, xbase, g < mc, ps, pb, acc, lane);
+      compute_stage<ALLCOLS>(cbase, xbase, g < mc, acc, loff, g);
       ++R.consumed;
       __syncwarp();
       if (lane == 0) {
         fence_proxy_async();
         issue_next();
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        ps[i] = ns[i];
-        pb[i] = nb[i];
       }
     }
     if (timed_out) break;
@@ -441,7 +546,7 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 3) tc_stream_kernel(const _
           if (n < mc && row < p.N) p.y[(int64_t)s_tok[n] * p.N + row] = f32_to_bf16_bits(acc[s][i]);
         }
     } else {
-      float* q = p.part + (int64_t)u * 8 * 32;
+      float* q = p.part + (int64_t)cc.u * 8 * 32;
 #pragma unroll
       for (int s = 0; s < 2; ++s)
 #pragma unroll
@@ -450,11 +555,15 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 3) tc_stream_kernel(const _
           const int n = 2 * t + (i & 1);
           if (n < mc) __stcg(q + n * 32 + r, acc[s][i]);
         }
-      __threadfence();
+      // warp barrier, then one release fence by lane 0 before it counts the arrival
       __syncwarp();
-      if (lane == 0) pend_old = atomicAdd(p.cnt + tile, 1);
+      if (lane == 0) {
+        __threadfence();
+        pend_old = atomicAdd(p.cnt + tile, 1);
+      }
       pend_tile = tile;
     }
+    cc.advance(TW, tw_tiles, tw_slices, p.ks);
   }
   if (!timed_out && pend_tile >= 0) {
     const int old = __shfl_sync(0xffffffffu, pend_old, 0);
@@ -463,7 +572,8 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 3) tc_stream_kernel(const _
   if (timed_out) {
     if (lane == 0) atomicOr(p.flags, W4A16_DEVICE_TIMEOUT);
     // let copies already in flight land before shared memory is released
-    while (R.consumed < R.issued) {
+    const uint32_t issued = __shfl_sync(0xffffffffu, R.issued, 0);
+    while (R.consumed < issued) {
       mbar_wait(R.bars0 + 8 * (R.consumed % (uint32_t)S), (R.consumed / (uint32_t)S) & 1u);
       ++R.consumed;
     }
@@ -488,7 +598,7 @@ __host__ __device__ inline int routed_smem(int warps, int stages, int ks) {
   return warps * ring_bytes(stages, kMaxChunk) + warps * stages * 8 + ks * kTileRows * 8 * 4 + 16 * 4 + 1024;
 }
 
-__global__ void __launch_bounds__(kRoutedWarps * 32) tc_routed_kernel(const __grid_constant__ CUtensorMap tmW,
+__global__ void __launch_bounds__(kRoutedWarps * 32) tc_routed_kernel(const __grid_constant__ Maps maps,
                                                                       RoutedParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -496,12 +606,9 @@ __global__ void __launch_bounds__(kRoutedWarps * 32) tc_routed_kernel(const __gr
   const int g = lane >> 2, t = lane & 3;
   const int S = p.stages, W = p.warps;
   const int x_slot = kMaxChunk * kXPitch;
-  const int groups_per_row = p.K / kGroup;
   const int e = blockIdx.y;
   const int row_base = blockIdx.x * kTileRows;
   const int tensor_row = e * p.N + row_base;
-  const uint16_t* Se = p.S + (int64_t)e * p.N * groups_per_row;
-  const uint16_t* Be = p.B + (int64_t)e * p.N * groups_per_row;
 
   Ring R;
   R.S = S;
@@ -510,10 +617,12 @@ __global__ void __launch_bounds__(kRoutedWarps * 32) tc_routed_kernel(const __gr
   R.xs0 = smem_u32(base) + (uint32_t)(W * S * kCodeSlotBytes + warp * S * x_slot);
   const uint32_t bar_off = (uint32_t)(W * ring_bytes(S, kMaxChunk));
   R.bars0 = smem_u32(base) + bar_off + (uint32_t)(warp * S * 8);
-  float* red = reinterpret_cast<float*>(base + bar_off + W * S * 8);  // [ks][32 rows][8 tokens]
+  float* red = reinterpret_cast<float*>(base + bar_off + W * S * 8);  // [ks][32 rows][8 columns]
   int* s_tok = reinterpret_cast<int*>(red + p.ks * kTileRows * 8);
   int* s_state = s_tok + kMaxChunk;  // [0] scan position, [1] count, [2] abort
   R.issued = R.consumed = 0;
+  R.pol_stream = policy_evict_first();
+  R.pol_keep = policy_evict_last();
 
   if (lane == 0)
     for (int i = 0; i < S; ++i) mbar_init(R.bars0 + 8 * i, 1);
@@ -524,15 +633,11 @@ __global__ void __launch_bounds__(kRoutedWarps * 32) tc_routed_kernel(const __gr
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   __syncthreads();
 
-  int prow[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) prow[i] = row_base + 16 * (i >> 1) + g + 8 * (i & 1);
+  uint32_t loff[2][4];
+  ldsm_offsets(lane, loff);
 
   // this warp's stages: slices warp, warp + W, ... each [slice*sl, min(nst, ...))
-  auto slice_end = [&](int sidx) {
-    const int e2 = (sidx + 1) * p.sl;
-    return e2 < p.nst ? e2 : p.nst;
-  };
+  auto slice_end = [&](int sidx) { return min((sidx + 1) * p.sl, p.nst); };
 
   for (;;) {
     const int mc = gather_tokens(p.ids, p.T, p.E, e, s_tok, s_state);
@@ -541,7 +646,7 @@ __global__ void __launch_bounds__(kRoutedWarps * 32) tc_routed_kernel(const __gr
     int isl = warp, ist = warp * p.sl;  // issue cursor
     auto issue_next = [&]() {
       if (isl >= p.ks) return;
-      ring_issue(R, &tmW, ist, tensor_row, p.x, s_tok, mc, p.K);
+      ring_issue(R, &maps, ist, tensor_row, p.x, s_tok, mc, p.K);
       if (++ist == slice_end(isl)) {
         isl += W;
         ist = isl * p.sl;
@@ -559,29 +664,20 @@ __global__ void __launch_bounds__(kRoutedWarps * 32) tc_routed_kernel(const __gr
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[s][i] = 0.0f;
       const int s0 = sidx * p.sl, s1 = slice_end(sidx);
-      uint2 ps[4], pb[4];
-      load_params(Se, Be, prow, p.N, groups_per_row, s0, ps, pb);
       for (int st = s0; st < s1; ++st) {
         uint32_t slot;
         if (!ring_wait(R, slot)) {
           timed_out = true;
           break;
         }
-        uint2 ns[4] = {}, nb[4] = {};
-        if (st + 1 < s1) load_params(Se, Be, prow, p.N, groups_per_row, st + 1, ns, nb);
         const uint32_t cbase = ordered(R.codes0 + slot * kCodeSlotBytes);
         const uint32_t xbase = ordered(R.xs0 + slot * x_slot + g * kXPitch + 16 * t);
-        compute_stage(cbase, xbase, g < mc, ps, pb, acc, lane);
+        compute_stage<true>(cbase, xbase, g < mc, acc, loff, g);
         ++R.consumed;
         __syncwarp();
         if (lane == 0) {
           fence_proxy_async();
           issue_next();
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          ps[i] = ns[i];
-          pb[i] = nb[i];
         }
       }
       float* rs = red + sidx * kTileRows * 8;
@@ -595,7 +691,8 @@ __global__ void __launch_bounds__(kRoutedWarps * 32) tc_routed_kernel(const __gr
         atomicOr(p.flags, W4A16_DEVICE_TIMEOUT);
         s_state[2] = 1;
       }
-      while (R.consumed < R.issued) {
+      const uint32_t issued = __shfl_sync(0xffffffffu, R.issued, 0);
+      while (R.consumed < issued) {
         mbar_wait(R.bars0 + 8 * (R.consumed % (uint32_t)S), (R.consumed / (uint32_t)S) & 1u);
         ++R.consumed;
       }
@@ -651,11 +748,25 @@ cudaError_t get_encoder() {
   return g_encode_status;
 }
 
+cudaError_t make_param_map(CUtensorMap* map, const uint16_t* P, int64_t rows, int K) {
+  if (cudaError_t e = get_encoder()) return e;
+  cuuint64_t dims[2] = {(cuuint64_t)(K / kGroup), (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(K / kGroup) * 2};
+  cuuint32_t box[2] = {8, (cuuint32_t)kTileRows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t*>(P), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t make_maps(Maps* m, const uint32_t* Wq, const uint16_t* S, const uint16_t* B, int64_t rows, int K);
+
 cudaError_t make_code_map(CUtensorMap* map, const uint32_t* Wq, int64_t rows, int K) {
   if (cudaError_t e = get_encoder()) return e;
   cuuint64_t dims[2] = {(cuuint64_t)(K / 8), (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)K / 2};
-  cuuint32_t box[2] = {(cuuint32_t)kStageWords, (cuuint32_t)kTileRows};
+  cuuint32_t box[2] = {(cuuint32_t)kBoxWords, (cuuint32_t)kTileRows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(Wq), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -663,21 +774,62 @@ cudaError_t make_code_map(CUtensorMap* map, const uint32_t* Wq, int64_t rows, in
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t make_maps(Maps* m, const uint32_t* Wq, const uint16_t* S, const uint16_t* B, int64_t rows, int K) {
+  if (cudaError_t e = make_code_map(&m->codes, Wq, rows, K)) return e;
+  if (cudaError_t e = make_param_map(&m->scales, S, rows, K)) return e;
+  return make_param_map(&m->biases, B, rows, K);
+}
+
 int stream_smem(int stages, int mc) {
   return kStreamWarps * ring_bytes(stages, mc) + kStreamWarps * stages * 8 + 64 + 1024;
 }
 
-// Deepest ring (4..2 stages per warp) that still lets three CTAs share an SM.
+// Deepest ring (up to W4A16_TC_MAX_STAGES, at least 2 stages per warp) that
+// keeps a CTA's shared memory under W4A16_TC_SMEM_TARGET.
 int stream_stages(int mc) {
-  for (int s = 4; s > 2; --s)
-    if (stream_smem(s, mc) <= 76 * 1024) return s;
+  for (int s = W4A16_TC_MAX_STAGES; s > 2; --s)
+    if (stream_smem(s, mc) <= W4A16_TC_SMEM_TARGET) return s;
   return 2;
 }
 
 struct DeviceInfo {
   int sms = 152;
-  bool attr_set[2] = {false, false};
+  bool attr_set[3] = {false, false, false};  // stream<false>, stream<true>, routed
 };
+
+// Opt the stream kernel instantiation into the large shared-memory carve-out once per device.
+cudaError_t prepare_stream_kernel(DeviceInfo& d, bool allcols) {
+  const int i = allcols ? 1 : 0;
+  if (d.attr_set[i]) return cudaSuccess;
+  cudaError_t e = allcols ? cudaFuncSetAttribute(tc_stream_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 kSmemLimit)
+                          : cudaFuncSetAttribute(tc_stream_kernel<false>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+  if (e == cudaSuccess) d.attr_set[i] = true;
+  return e;
+}
+
+// Persistent grid for one chunk: every SM filled to its occupancy, never more
+// CTAs than there are groups of four work units.
+cudaError_t launch_stream(const Maps& map, const StreamParams& p, int sms, cudaStream_t stream) {
+  const bool allcols = p.M > 1;
+  const int smem = stream_smem(p.stages, p.M);
+  int per_sm = 0;
+  cudaError_t e = allcols ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_stream_kernel<true>,
+                                                                          kStreamWarps * 32, smem)
+                          : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_stream_kernel<false>,
+                                                                          kStreamWarps * 32, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  int grid = sms * per_sm;
+  const int need = (p.units + kStreamWarps - 1) / kStreamWarps;
+  if (grid > need) grid = need;
+  if (allcols)
+    tc_stream_kernel<true><<<grid, kStreamWarps * 32, smem, stream>>>(map, p);
+  else
+    tc_stream_kernel<false><<<grid, kStreamWarps * 32, smem, stream>>>(map, p);
+  return cudaGetLastError();
+}
 
 std::mutex g_dev_mu;
 std::map<int, DeviceInfo> g_dev;
@@ -777,12 +929,7 @@ cudaError_t launch_tc(const LaunchArgs& a, const w4a16_plan& plan) {
     std::lock_guard<std::mutex> lk(g_dev_mu);
     DeviceInfo& d = device_info(dev);
     sms = d.sms;
-    if (!d.attr_set[0]) {
-      if (cudaError_t e = cudaFuncSetAttribute(tc_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               kSmemLimit))
-        return e;
-      d.attr_set[0] = true;
-    }
+    if (cudaError_t e = prepare_stream_kernel(d, a.M > 1)) return e;
     if (s.ks > 1) {
       if (s.tiles > kWsTiles || s.units > kWsUnits) return cudaErrorInvalidValue;
       void* ws = nullptr;
@@ -791,18 +938,9 @@ cudaError_t launch_tc(const LaunchArgs& a, const w4a16_plan& plan) {
       p.part = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsCounterBytes);
     }
   }
-  CUtensorMap map;
-  if (cudaError_t e = make_code_map(&map, a.Wq, a.N, a.K)) return e;
-  const int smem = stream_smem(p.stages, a.M);
-  int per_sm = 0;
-  if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_stream_kernel, kStreamWarps * 32, smem))
-    return e;
-  if (per_sm < 1) per_sm = 1;
-  int grid = sms * per_sm;
-  const int need = (s.units + kStreamWarps - 1) / kStreamWarps;
-  if (grid > need) grid = need;
-  tc_stream_kernel<<<grid, kStreamWarps * 32, smem, a.stream>>>(map, p);
-  return cudaGetLastError();
+  Maps maps;
+  if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, a.N, a.K)) return e;
+  return launch_stream(maps, p, sms, a.stream);
 }
 
 cudaError_t launch_tc_id(const LaunchArgs& a, const w4a16_plan& plan) {
@@ -823,17 +961,17 @@ cudaError_t launch_tc_id(const LaunchArgs& a, const w4a16_plan& plan) {
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);
     DeviceInfo& d = device_info(dev);
-    if (!d.attr_set[1]) {
+    if (!d.attr_set[2]) {
       if (cudaError_t e = cudaFuncSetAttribute(tc_routed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                kSmemLimit))
         return e;
-      d.attr_set[1] = true;
+      d.attr_set[2] = true;
     }
   }
-  CUtensorMap map;
-  if (cudaError_t e = make_code_map(&map, a.Wq, (int64_t)a.N * a.E, a.K)) return e;
+  Maps maps;
+  if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, (int64_t)a.N * a.E, a.K)) return e;
   dim3 grid(s.tiles, a.E);
-  tc_routed_kernel<<<grid, p.warps * 32, smem, a.stream>>>(map, p);
+  tc_routed_kernel<<<grid, p.warps * 32, smem, a.stream>>>(maps, p);
   return cudaGetLastError();
 }
 
@@ -877,12 +1015,7 @@ cudaError_t launch_tc_noalloc(const LaunchArgs& a) {
     std::lock_guard<std::mutex> lk(g_dev_mu);
     DeviceInfo& d = device_info(dev);
     sms = d.sms;
-    if (!d.attr_set[0]) {
-      if (cudaError_t e = cudaFuncSetAttribute(tc_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               kSmemLimit))
-        return e;
-      d.attr_set[0] = true;
-    }
+    if (cudaError_t e = prepare_stream_kernel(d, a.M > 1)) return e;
     if (!g_noalloc_ptr[dev]) {
       void* ptr = nullptr;
       if (cudaError_t e = cudaGetSymbolAddress((void**)&ptr, g_noalloc_scratch)) return e;
@@ -903,18 +1036,9 @@ cudaError_t launch_tc_noalloc(const LaunchArgs& a) {
     // the array keeps whatever the previous call left: the counters must start at zero
     if (cudaError_t e = cudaMemsetAsync(p.cnt, 0, (size_t)s.tiles * 4, a.stream)) return e;
   }
-  CUtensorMap map;
-  if (cudaError_t e = make_code_map(&map, a.Wq, a.N, a.K)) return e;
-  const int smem = stream_smem(p.stages, a.M);
-  int per_sm = 0;
-  if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_stream_kernel, kStreamWarps * 32, smem))
-    return e;
-  if (per_sm < 1) per_sm = 1;
-  int grid = sms * per_sm;
-  const int need = (s.units + kStreamWarps - 1) / kStreamWarps;
-  if (grid > need) grid = need;
-  tc_stream_kernel<<<grid, kStreamWarps * 32, smem, a.stream>>>(map, p);
-  return cudaGetLastError();
+  Maps maps;
+  if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, a.N, a.K)) return e;
+  return launch_stream(maps, p, sms, a.stream);
 }
 
 }  // namespace w4a16

@@ -136,6 +136,9 @@ def test_plans_depend_on_shape_only_and_fill_the_gpu(L):
         ops.get_plan(100, 100)
     with pytest.raises(ValueError):
         ops.get_plan(100, 192, "tc")
+    with pytest.raises(ValueError):
+        ops.get_plan(100, 768, "tc")  # the tensor-core family needs K % 512 == 0
+    assert ops.get_plan(100, 768)["kernel"] == "simt"
     assert ops.get_plan(100, 192)["kernel"] == "simt"
     assert ops.get_plan(100, 2560)["kernel"] == "tc"
     # the reduction order is a pure function of (N, K) -- the plan call has no M
@@ -148,7 +151,7 @@ def test_plans_depend_on_shape_only_and_fill_the_gpu(L):
 
 def test_split_plans_fit_the_fixed_workspace(L):
     # the tensor-core kernel's workspace holds 4096 tile counters and 4864 unit partials
-    for K in (256, 512, 768, 1536, 2048, 2560, 4096, 10240, 12288, 16384, 65536):
+    for K in (512, 1024, 1536, 2048, 2560, 4096, 10240, 12288, 16384, 65536):
         for N in (1, 31, 32, 500, 1621 * 32, 2431 * 32, 2432 * 32, 5000 * 32, 262144):
             p = ops.get_plan(N, K, "tc")
             if p["ksplit"] > 1:

@@ -14,7 +14,7 @@ CANARY = 0x7FA1  # a NaN pattern no kernel writes
 
 
 @pytest.mark.parametrize("kernel", ["simt", "tc", "vanilla"])
-@pytest.mark.parametrize("M,N,K", [(1, 7, 256), (5, 33, 2560), (9, 129, 1280), (3, 1000, 3072)])
+@pytest.mark.parametrize("M,N,K", [(1, 7, 512), (5, 33, 2560), (9, 129, 1536), (3, 1000, 3072)])
 def test_output_guard_bands(kernel, M, N, K):
     w = dev_weights(50 + N, N, K)
     x = to_dev_bf16(synth.make_x(50, M, K))
@@ -30,7 +30,7 @@ def test_output_guard_bands(kernel, M, N, K):
 
 
 def test_mm_id_guard_bands():
-    E, N, K, T = 3, 45, 768, 10
+    E, N, K, T = 3, 45, 1024, 10
     hw = synth.make_weights(60, N, K, E)
     w = ops.W4Matrix.from_host(hw)
     ids = torch.from_numpy(synth.make_ids(60, T, E)).cuda()

@@ -66,7 +66,7 @@ def test_empty_token_list():
 
 
 def test_all_tokens_on_one_expert_spans_chunks():
-    E, N, K, T = 4, 96, 256, 19
+    E, N, K, T = 4, 96, 1024, 19
     hw, w = _experts(7, E, N, K)
     ids_np = np.full(T, 2, dtype=np.int32)
     xb = synth.make_x(7, T, K)

@@ -39,7 +39,7 @@ def test_ragged_shapes(kernel, N, K, M):
     assert_parity(y, yr, ad, f"{kernel} M={M} N={N} K={K}")
 
 
-@pytest.mark.parametrize("N,K", [(1, 256), (7, 512), (31, 768), (33, 2560), (95, 1536), (1000, 3072), (4099, 4096)])
+@pytest.mark.parametrize("N,K", [(1, 512), (7, 1024), (31, 1536), (33, 2560), (95, 1536), (1000, 3072), (4099, 4096)])
 @pytest.mark.parametrize("M", [1, 2, 5, 8, 13])
 def test_tc_ragged_shapes(N, K, M):
     xb, hw, y = _run(M, N, K, "tc", seed=N + K + 1, xseed=M + 40)
@@ -47,9 +47,9 @@ def test_tc_ragged_shapes(N, K, M):
     assert_parity(y, yr, ad, f"tc M={M} N={N} K={K}")
 
 
-def test_tc_rejects_k_not_multiple_of_256():
+def test_tc_rejects_k_not_multiple_of_512():
     with pytest.raises(ValueError):
-        _run(1, 64, 192, "tc")
+        _run(1, 64, 768, "tc")
 
 
 def _special_case(N, K, codes, scale, bias, M=4):
@@ -132,7 +132,7 @@ def test_workspace_reuse_across_shapes():
     """Split-K shapes of different sizes share one stream's workspace; each
     call must find its counters at zero whatever ran before."""
     for (M, N, K) in [(2, 1024, 2560), (1, 10240, 2560), (3, 2560, 10240), (1, 1024, 2560), (1, 10240, 2560),
-                      (4, 96, 768), (1, 10240, 2560)]:
+                      (4, 96, 1024), (1, 10240, 2560)]:
         xb, hw, y = _run(M, N, K, "tc", seed=N % 7, xseed=M)
         cols = sample_cols(N, 1024, seed=N)
         yr, ad = oracle_mm(xb, hw, cols)
