@@ -246,6 +246,27 @@ __device__ __forceinline__ bool ring_wait(Ring& R, uint32_t& slot) {
   return __all_sync(0xffffffffu, ok);
 }
 
+// Activation B fragments of one 16-byte chunk x0..x7 of a column: for the
+// code pairing (i, i+4) of a packed word, h = 0 takes (x0,x4),(x1,x5) and
+// h = 1 takes (x2,x6),(x3,x7).
+__device__ __forceinline__ void frag_from_chunk(const uint4& u, uint32_t (&b)[2][2]) {
+  b[0][0] = prmt(u.x, u.z, 0x5410);
+  b[0][1] = prmt(u.x, u.z, 0x7632);
+  b[1][0] = prmt(u.y, u.w, 0x5410);
+  b[1][1] = prmt(u.y, u.w, 0x7632);
+}
+
+__device__ __forceinline__ float2 lds64f(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, const uint4& v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
 __device__ __forceinline__ uint32_t component(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
@@ -269,8 +290,9 @@ __device__ __forceinline__ void ldsm_offsets(int lane, uint32_t (&off)[2][4]) {
 // 2t+1).  GB groups at a time: their loads are issued first and their MMA
 // chains interleaved.  With ALLCOLS false (one activation row) the odd
 // columns are not rescaled; the even columns' arithmetic is unchanged.
-template <bool ALLCOLS>
-__device__ __forceinline__ void compute_stage(uint32_t cbase, uint32_t xbase, bool xvalid, float (&p)[2][4],
+template <bool ALLCOLS, bool XSTAGED>
+__device__ __forceinline__ void compute_stage(uint32_t cbase, uint32_t xbase, bool xvalid, uint32_t sxbase,
+                                              uint32_t sx_stride, bool xvalid_cols, float (&p)[2][4],
                                               const uint32_t (&loff)[2][4], int g) {
   constexpr int GB = W4A16_TC_GROUP_BATCH;
   // scale / bias of the 8 groups for this lane's rows 16(i>>1) + g + 8(i&1)
@@ -298,31 +320,39 @@ __device__ __forceinline__ void compute_stage(uint32_t cbase, uint32_t xbase, bo
       }
     }
     uint32_t bx[GB][2][2][2];  // [group][chunk][h][reg]
-#pragma unroll
-    for (int j = 0; j < GB; ++j)
-#pragma unroll
-      for (int cb = 0; cb < 2; ++cb) {
-        bx[j][cb][0][0] = prmt(u[j][cb].x, u[j][cb].z, 0x5410);
-        bx[j][cb][0][1] = prmt(u[j][cb].x, u[j][cb].z, 0x7632);
-        bx[j][cb][1][0] = prmt(u[j][cb].y, u[j][cb].w, 0x5410);
-        bx[j][cb][1][1] = prmt(u[j][cb].y, u[j][cb].w, 0x7632);
-      }
     float sx[GB][4], acc[GB][2][4];
 #pragma unroll
-    for (int j = 0; j < GB; ++j)
+    for (int j = 0; j < GB; ++j) {
+#pragma unroll
+      for (int cb = 0; cb < 2; ++cb) {
+        if (XSTAGED) {  // already in fragment order
+          bx[j][cb][0][0] = u[j][cb].x;
+          bx[j][cb][0][1] = u[j][cb].y;
+          bx[j][cb][1][0] = u[j][cb].z;
+          bx[j][cb][1][1] = u[j][cb].w;
+        } else {
+          frag_from_chunk(u[j][cb], bx[j][cb]);
+        }
+      }
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         sx[j][i] = 0.f;
         acc[j][0][i] = 0.f;
         acc[j][1][i] = 0.f;
       }
+      if (XSTAGED && xvalid_cols) {  // precomputed group sums of columns 2t, 2t+1
+        const float2 v = lds64f(sxbase + sx_stride * (gp + j));
+        sx[j][0] = v.x;
+        sx[j][1] = v.y;
+      }
+    }
     // the four (chunk, h) steps of every chain, in the canonical order, chains interleaved
 #pragma unroll
     for (int step = 0; step < 4; ++step) {
       const int cb = step >> 1, h = step & 1;
 #pragma unroll
       for (int j = 0; j < GB; ++j) {
-        mma_bf16(sx[j], kOnes, kOnes, kOnes, kOnes, bx[j][cb][h][0], bx[j][cb][h][1]);
+        if (!XSTAGED) mma_bf16(sx[j], kOnes, kOnes, kOnes, kOnes, bx[j][cb][h][0], bx[j][cb][h][1]);
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
           const uint32_t wg = w[j][s][2 * cb], wg8 = w[j][s][2 * cb + 1];
@@ -393,7 +423,18 @@ struct StreamParams {
   int N, K, M, row0;
   int nst, sl, ks, tiles, units;
   int stages;
+  int xpitch;       // bytes per activation row of the pre-staged copy (0: per-stage copies)
 };
+
+// Columns of the group-sum table: the even count >= mc (lane t reads columns 2t, 2t+1).
+__host__ __device__ inline int sx_cols(int mc) { return (mc + 1) & ~1; }
+
+// Bytes of shared memory the pre-staged activations and their group sums
+// take: mc rows of 2K + 64 bytes (fragment order, padded for conflict-free
+// reads) and K/64 groups x sx_cols(mc) fp32 sums.
+__host__ __device__ inline int xstage_bytes(int mc, int K) {
+  return mc * (2 * K + 64) + (K / kGroup) * sx_cols(mc) * 4;
+}
 
 // Position of a work unit u = tile * ks + slice, advanced by a fixed stride
 // without divisions.
@@ -415,7 +456,7 @@ struct UnitCursor {
   }
 };
 
-template <bool ALLCOLS>
+template <bool ALLCOLS, bool XSTAGED>
 __global__ void __launch_bounds__(kStreamWarps * 32, W4A16_TC_MIN_BLOCKS) tc_stream_kernel(
     const __grid_constant__ Maps maps, StreamParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -423,17 +464,21 @@ __global__ void __launch_bounds__(kStreamWarps * 32, W4A16_TC_MIN_BLOCKS) tc_str
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int S = p.stages, mc = p.M;
-  const int x_slot = mc * kXPitch;
+  const int xring = XSTAGED ? 0 : mc;  // activation rows copied per stage
+  const int x_slot = xring * kXPitch;
 
   // layout: codes ring of every warp | x ring of every warp | barriers | tokens
+  //         | pre-staged activations | their group sums
   Ring R;
   R.S = S;
   R.x_slot = x_slot;
   R.codes0 = smem_u32(base) + (uint32_t)(warp * S * kCodeSlotBytes);
   R.xs0 = smem_u32(base) + (uint32_t)(kStreamWarps * S * kCodeSlotBytes + warp * S * x_slot);
-  const uint32_t bar_off = (uint32_t)(kStreamWarps * ring_bytes(S, mc));
+  const uint32_t bar_off = (uint32_t)(kStreamWarps * ring_bytes(S, xring));
   R.bars0 = smem_u32(base) + bar_off + (uint32_t)(warp * S * 8);
   int* s_tok = reinterpret_cast<int*>(base + bar_off + kStreamWarps * S * 8);
+  const uint32_t xst = smem_u32(base) + bar_off + (uint32_t)(kStreamWarps * S * 8 + 64);  // 16-byte aligned
+  const uint32_t sxs = xst + (uint32_t)(mc * p.xpitch);
   R.issued = R.consumed = 0;
   R.pol_stream = policy_evict_first();
   R.pol_keep = policy_evict_last();
@@ -447,11 +492,7 @@ __global__ void __launch_bounds__(kStreamWarps * 32, W4A16_TC_MIN_BLOCKS) tc_str
   // warp-major numbering: every pass over the units spreads them evenly over CTAs
   const int gw = warp * gridDim.x + blockIdx.x;
   const int TW = gridDim.x * kStreamWarps;
-  if (gw >= p.units) return;
   const int tw_tiles = TW / p.ks, tw_slices = TW - tw_tiles * p.ks;
-
-  uint32_t loff[2][4];
-  ldsm_offsets(lane, loff);
 
   // issue cursor (lane 0): unit, stage, end of the unit's stages
   UnitCursor ic;
@@ -460,17 +501,58 @@ __global__ void __launch_bounds__(kStreamWarps * 32, W4A16_TC_MIN_BLOCKS) tc_str
   int iend = min(ist + p.sl, p.nst);
   auto issue_next = [&]() {
     if (ic.u >= p.units) return;
-    ring_issue(R, &maps, ist, ic.tile * kTileRows, p.x, s_tok, mc, p.K);
+    ring_issue(R, &maps, ist, ic.tile * kTileRows, p.x, s_tok, xring, p.K);
     if (++ist == iend) {
       ic.advance(TW, tw_tiles, tw_slices, p.ks);
       ist = ic.slice * p.sl;
       iend = min(ist + p.sl, p.nst);
     }
   };
+  // the first weight stages are in flight while the activations are staged
   if (lane == 0) {
     fence_proxy_async();
     for (int i = 0; i < S; ++i) issue_next();
   }
+
+  if (XSTAGED) {
+    // Activation rows in B-fragment order, then the sum of every 64-group of
+    // every row with the same MMA chain the per-stage path uses.
+    const int chunks = p.K / 8;
+    for (int c = threadIdx.x; c < mc * chunks; c += blockDim.x) {
+      const int n = c / chunks, wd = c - n * chunks;
+      const uint4 u = ld_nc_v4(p.x + (int64_t)(p.row0 + n) * p.K + 8 * wd);
+      uint32_t b[2][2];
+      frag_from_chunk(u, b);
+      sts128(xst + n * p.xpitch + 16 * wd, make_uint4(b[0][0], b[0][1], b[1][0], b[1][1]));
+    }
+    __syncthreads();
+    for (int G = warp; G < p.K / kGroup; G += kStreamWarps) {
+      uint32_t b[2][2][2];
+#pragma unroll
+      for (int cb = 0; cb < 2; ++cb) {
+        uint4 u = make_uint4(0, 0, 0, 0);
+        if (g < mc) u = lds128(xst + g * p.xpitch + 128 * G + 64 * cb + 16 * t);
+        b[cb][0][0] = u.x;
+        b[cb][0][1] = u.y;
+        b[cb][1][0] = u.z;
+        b[cb][1][1] = u.w;
+      }
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int step = 0; step < 4; ++step) mma_bf16(v, kOnes, kOnes, kOnes, kOnes, b[step >> 1][step & 1][0],
+                                                    b[step >> 1][step & 1][1]);
+      if (g == 0 && 2 * t < mc) {
+        asm volatile("st.shared.v2.f32 [%0], {%1,%2};" ::"r"(sxs + (G * sx_cols(mc) + 2 * t) * 4), "f"(v[0]),
+                     "f"(v[1])
+                     : "memory");
+      }
+    }
+    __syncthreads();
+  }
+  if (gw >= p.units) return;
+
+  uint32_t loff[2][4];
+  ldsm_offsets(lane, loff);
 
   bool timed_out = false;
   int pend_tile = -1, pend_old = 0;
@@ -478,14 +560,22 @@ __global__ void __launch_bounds__(kStreamWarps * 32, W4A16_TC_MIN_BLOCKS) tc_str
   auto reduce_tile = [&](int tile) {
     // Sum the ksplit partials of a finished tile in slice order.  Lane 0's
     // fence (after it saw the last arrival) and the warp barrier order every
-    // lane's loads after the other units' partial stores.
+    // lane's loads after the other units' partial stores.  Loads are issued
+    // eight slices at a time; the additions stay in slice order.
     if (lane == 0) __threadfence();
     __syncwarp();
     const int row = tile * kTileRows + lane;
     for (int n = 0; n < mc; ++n) {
       const float* q = p.part + ((int64_t)tile * p.ks * 8 + n) * 32 + lane;
-      float sum = __ldcg(q);
-      for (int sidx = 1; sidx < p.ks; ++sidx) sum = __fadd_rn(sum, __ldcg(q + (int64_t)sidx * 8 * 32));
+      float sum = 0.0f;
+      for (int s0 = 0; s0 < p.ks; s0 += 8) {
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = (s0 + j < p.ks) ? __ldcg(q + (int64_t)(s0 + j) * 8 * 32) : 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (s0 + j < p.ks) sum = (s0 + j == 0) ? v[0] : __fadd_rn(sum, v[j]);
+      }
       if (row < p.N) p.y[(int64_t)s_tok[n] * p.N + row] = f32_to_bf16_bits(sum);
     }
     if (lane == 0) p.cnt[tile] = 0;
@@ -519,8 +609,14 @@ __global__ void __launch_bounds__(kStreamWarps * 32, W4A16_TC_MIN_BLOCKS) tc_str
         break;
       }
       const uint32_t cbase = ordered(R.codes0 + slot * kCodeSlotBytes);
-      const uint32_t xbase = ordered(R.xs0 + slot * x_slot + g * kXPitch + 16 * t);
-      compute_stage<ALLCOLS>(cbase, xbase, g < mc, acc, loff, g);
+      uint32_t xbase, sxbase = 0;
+      if (XSTAGED) {
+        xbase = xst + g * p.xpitch + 16 * t + st * (kStageK * 2);
+        sxbase = sxs + (st * (kStageK / kGroup) * sx_cols(mc) + 2 * t) * 4;
+      } else {
+        xbase = ordered(R.xs0 + slot * x_slot + g * kXPitch + 16 * t);
+      }
+      compute_stage<ALLCOLS, XSTAGED>(cbase, xbase, g < mc, sxbase, sx_cols(mc) * 4, 2 * t < mc, acc, loff, g);
       ++R.consumed;
       __syncwarp();
       if (lane == 0) {
@@ -672,7 +768,7 @@ __global__ void __launch_bounds__(kRoutedWarps * 32) tc_routed_kernel(const __gr
         }
         const uint32_t cbase = ordered(R.codes0 + slot * kCodeSlotBytes);
         const uint32_t xbase = ordered(R.xs0 + slot * x_slot + g * kXPitch + 16 * t);
-        compute_stage<true>(cbase, xbase, g < mc, acc, loff, g);
+        compute_stage<true, false>(cbase, xbase, g < mc, 0u, 0u, false, acc, loff, g);
         ++R.consumed;
         __syncwarp();
         if (lane == 0) {
@@ -794,41 +890,59 @@ int stream_stages(int mc) {
 
 struct DeviceInfo {
   int sms = 152;
-  bool attr_set[3] = {false, false, false};  // stream<false>, stream<true>, routed
+  bool attr_set[5] = {false, false, false, false, false};  // stream<cols, staged> x4, routed
 };
 
-// Opt the stream kernel instantiation into the large shared-memory carve-out once per device.
-cudaError_t prepare_stream_kernel(DeviceInfo& d, bool allcols) {
-  const int i = allcols ? 1 : 0;
-  if (d.attr_set[i]) return cudaSuccess;
-  cudaError_t e = allcols ? cudaFuncSetAttribute(tc_stream_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 kSmemLimit)
-                          : cudaFuncSetAttribute(tc_stream_kernel<false>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-  if (e == cudaSuccess) d.attr_set[i] = true;
-  return e;
+// The activations are pre-staged (once per CTA) when the CTA, with a
+// two-stage ring per warp, still fits twice on an SM; otherwise every stage
+// carries its own activation chunk.
+constexpr int kHalfSm = 228 * 1024 / 2 - 1024;  // per-CTA budget for two CTAs per SM (1 KB reserved each)
+
+// Staging costs each CTA a prologue (copy + group sums over all of K); it
+// pays off when every warp has several work units to amortise it over.
+bool stage_activations(int M, int K, int units, int sms) {
+  return units >= 2 * kStreamWarps * 2 * sms && stream_smem(2, 0) + xstage_bytes(M, K) <= kHalfSm;
 }
 
-// Persistent grid for one chunk: every SM filled to its occupancy, never more
-// CTAs than there are groups of four work units.
-cudaError_t launch_stream(const Maps& map, const StreamParams& p, int sms, cudaStream_t stream) {
-  const bool allcols = p.M > 1;
-  const int smem = stream_smem(p.stages, p.M);
+int staged_stages(int M, int K) {
+  for (int s = W4A16_TC_MAX_STAGES; s > 2; --s)
+    if (stream_smem(s, 0) + xstage_bytes(M, K) <= kHalfSm) return s;
+  return 2;
+}
+
+template <bool A, bool X>
+cudaError_t stream_launch_t(const Maps& map, const StreamParams& p, int sms, int smem, DeviceInfo& d,
+                            cudaStream_t stream) {
+  auto* fn = tc_stream_kernel<A, X>;
+  const int idx = (A ? 1 : 0) + (X ? 2 : 0);
+  if (!d.attr_set[idx]) {
+    if (cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit)) return e;
+    d.attr_set[idx] = true;
+  }
   int per_sm = 0;
-  cudaError_t e = allcols ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_stream_kernel<true>,
-                                                                          kStreamWarps * 32, smem)
-                          : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_stream_kernel<false>,
-                                                                          kStreamWarps * 32, smem);
-  if (e != cudaSuccess) return e;
+  if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kStreamWarps * 32, smem)) return e;
   if (per_sm < 1) per_sm = 1;
   int grid = sms * per_sm;
   const int need = (p.units + kStreamWarps - 1) / kStreamWarps;
   if (grid > need) grid = need;
-  if (allcols)
-    tc_stream_kernel<true><<<grid, kStreamWarps * 32, smem, stream>>>(map, p);
-  else
-    tc_stream_kernel<false><<<grid, kStreamWarps * 32, smem, stream>>>(map, p);
+  fn<<<grid, kStreamWarps * 32, smem, stream>>>(map, p);
   return cudaGetLastError();
+}
+
+// Persistent grid for one chunk: every SM filled to its occupancy, never more
+// CTAs than there are groups of four work units.  The caller holds g_dev_mu.
+cudaError_t launch_stream(const Maps& map, StreamParams p, int sms, DeviceInfo& d, cudaStream_t stream) {
+  const bool allcols = p.M > 1;
+  const bool staged = stage_activations(p.M, p.K, p.units, sms);
+  p.xpitch = staged ? 2 * p.K + 64 : 0;
+  p.stages = staged ? staged_stages(p.M, p.K) : stream_stages(p.M);
+  int smem = stream_smem(p.stages, staged ? 0 : p.M);
+  if (staged) smem += xstage_bytes(p.M, p.K);
+  if (allcols)
+    return staged ? stream_launch_t<true, true>(map, p, sms, smem, d, stream)
+                  : stream_launch_t<true, false>(map, p, sms, smem, d, stream);
+  return staged ? stream_launch_t<false, true>(map, p, sms, smem, d, stream)
+                : stream_launch_t<false, false>(map, p, sms, smem, d, stream);
 }
 
 std::mutex g_dev_mu;
@@ -897,7 +1011,8 @@ void plan_tc(int N, int K, w4a16_plan* p) {
   } else {
     cudaGetLastError();
   }
-  const int smem = stream_smem(stream_stages(1), 1);
+  const bool staged = stage_activations(1, K, s.units, sms);
+  const int smem = staged ? stream_smem(staged_stages(1, K), 0) + xstage_bytes(1, K) : stream_smem(stream_stages(1), 1);
   const int per_sm = kSmemLimit / smem > 0 ? kSmemLimit / smem : 1;
   int grid = sms * per_sm;
   const int need = (s.units + kStreamWarps - 1) / kStreamWarps;
@@ -921,26 +1036,22 @@ cudaError_t launch_tc(const LaunchArgs& a, const w4a16_plan& plan) {
   p.x = a.x; p.S = a.S; p.B = a.B; p.y = a.y; p.flags = a.flags;
   p.N = a.N; p.K = a.K; p.M = a.M; p.row0 = a.row0;
   p.nst = s.nst; p.sl = s.sl; p.ks = s.ks; p.tiles = s.tiles; p.units = s.units;
-  p.stages = stream_stages(a.M);
+  p.stages = 2;
+  p.xpitch = 0;
   p.part = nullptr;
   p.cnt = nullptr;
-  int sms;
-  {
-    std::lock_guard<std::mutex> lk(g_dev_mu);
-    DeviceInfo& d = device_info(dev);
-    sms = d.sms;
-    if (cudaError_t e = prepare_stream_kernel(d, a.M > 1)) return e;
-    if (s.ks > 1) {
-      if (s.tiles > kWsTiles || s.units > kWsUnits) return cudaErrorInvalidValue;
-      void* ws = nullptr;
-      if (cudaError_t e = workspace(dev, a.stream, &ws)) return e;
-      p.cnt = static_cast<int*>(ws);
-      p.part = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsCounterBytes);
-    }
-  }
   Maps maps;
   if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, a.N, a.K)) return e;
-  return launch_stream(maps, p, sms, a.stream);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = device_info(dev);
+  if (s.ks > 1) {
+    if (s.tiles > kWsTiles || s.units > kWsUnits) return cudaErrorInvalidValue;
+    void* ws = nullptr;
+    if (cudaError_t e = workspace(dev, a.stream, &ws)) return e;
+    p.cnt = static_cast<int*>(ws);
+    p.part = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsCounterBytes);
+  }
+  return launch_stream(maps, p, d.sms, d, a.stream);
 }
 
 cudaError_t launch_tc_id(const LaunchArgs& a, const w4a16_plan& plan) {
@@ -961,11 +1072,11 @@ cudaError_t launch_tc_id(const LaunchArgs& a, const w4a16_plan& plan) {
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);
     DeviceInfo& d = device_info(dev);
-    if (!d.attr_set[2]) {
+    if (!d.attr_set[4]) {
       if (cudaError_t e = cudaFuncSetAttribute(tc_routed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                kSmemLimit))
         return e;
-      d.attr_set[2] = true;
+      d.attr_set[4] = true;
     }
   }
   Maps maps;
@@ -1009,36 +1120,30 @@ cudaError_t launch_tc_noalloc(const LaunchArgs& a) {
   int dev = 0;
   if (cudaError_t e = cudaGetDevice(&dev)) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  int sms;
-  void* scratch = nullptr;
-  {
-    std::lock_guard<std::mutex> lk(g_dev_mu);
-    DeviceInfo& d = device_info(dev);
-    sms = d.sms;
-    if (cudaError_t e = prepare_stream_kernel(d, a.M > 1)) return e;
-    if (!g_noalloc_ptr[dev]) {
-      void* ptr = nullptr;
-      if (cudaError_t e = cudaGetSymbolAddress((void**)&ptr, g_noalloc_scratch)) return e;
-      g_noalloc_ptr[dev] = ptr;
-    }
-    scratch = g_noalloc_ptr[dev];
-  }
   StreamParams p;
   p.x = a.x; p.S = a.S; p.B = a.B; p.y = a.y; p.flags = a.flags;
   p.N = a.N; p.K = a.K; p.M = a.M; p.row0 = a.row0;
   p.nst = s.nst; p.sl = s.sl; p.ks = s.ks; p.tiles = s.tiles; p.units = s.units;
-  p.stages = stream_stages(a.M);
+  p.stages = 2;
+  p.xpitch = 0;
   p.part = nullptr;
   p.cnt = nullptr;
+  Maps maps;
+  if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, a.N, a.K)) return e;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = device_info(dev);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaError_t e = cudaGetSymbolAddress((void**)&ptr, g_noalloc_scratch)) return e;
+    g_noalloc_ptr[dev] = ptr;
+  }
   if (s.ks > 1) {
-    p.cnt = static_cast<int*>(scratch);
-    p.part = reinterpret_cast<float*>(static_cast<char*>(scratch) + kWsCounterBytes);
+    p.cnt = static_cast<int*>(g_noalloc_ptr[dev]);
+    p.part = reinterpret_cast<float*>(static_cast<char*>(g_noalloc_ptr[dev]) + kWsCounterBytes);
     // the array keeps whatever the previous call left: the counters must start at zero
     if (cudaError_t e = cudaMemsetAsync(p.cnt, 0, (size_t)s.tiles * 4, a.stream)) return e;
   }
-  Maps maps;
-  if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, a.N, a.K)) return e;
-  return launch_stream(maps, p, sms, a.stream);
+  return launch_stream(maps, p, d.sms, d, a.stream);
 }
 
 }  // namespace w4a16
