@@ -91,8 +91,15 @@ typedef enum {
   W4A16_KERNEL_AUTO = 0,    /* the dispatcher's choice for (N, K) */
   W4A16_KERNEL_SIMT = 1,    /* CUDA-core kernel: fp32 FMA, warp-shuffle split-K */
   W4A16_KERNEL_TC = 2,      /* tensor-core kernel: TMA-fed bf16 MMA on codes, fp32 group
-                               rescale; needs K % 512 == 0 */
-  W4A16_KERNEL_VANILLA = 3  /* debug control: one thread per output, no sharing */
+                               rescale; needs K % 512 == 0.  Runs as one of the two
+                               launch shapes below, chosen from (N, K, M); both give
+                               identical bits */
+  W4A16_KERNEL_VANILLA = 3, /* debug control: one thread per output, no sharing */
+  W4A16_KERNEL_TC_STREAM = 4, /* tensor-core kernel, persistent grid: work units dealt to
+                                 warps round-robin, split-K through the workspace */
+  W4A16_KERNEL_TC_TILE = 5  /* tensor-core kernel, one CTA per 16-row tile holding the
+                               tile's whole K range; needs that to fit in shared memory
+                               (otherwise W4A16_ERR_KERNEL) */
 } w4a16_kernel;
 
 /* y[M][N] = x[M][K] W^T.  M == 0 is a successful no-op.  The kernel family

@@ -43,6 +43,7 @@ enum Fault { kFaultNone = 0, kFaultValidate = 1, kFaultLaunch = 2 };
 struct EnvConfig {
   int fault = kFaultNone;
   int force_kernel = W4A16_KERNEL_AUTO;
+  int pdl = 2;  // W4A16_PDL: 0 plain launches, 1 overlap launches only, 2 also fetch weights early
 };
 
 std::mutex g_env_mu;
@@ -54,6 +55,9 @@ void load_env_locked() {
   if (const char* f = std::getenv("W4A16_FAULT")) {
     if (!std::strcmp(f, "validate")) c.fault = kFaultValidate;
     else if (!std::strcmp(f, "launch")) c.fault = kFaultLaunch;
+  }
+  if (const char* v = std::getenv("W4A16_PDL")) {
+    if (v[0] >= '0' && v[0] <= '2' && v[1] == 0) c.pdl = v[0] - '0';
   }
   if (const char* k = std::getenv("W4A16_FORCE_KERNEL")) {
     if (!std::strcmp(k, "simt")) c.force_kernel = W4A16_KERNEL_SIMT;
@@ -114,9 +118,15 @@ int resolve_kernel(int requested, int N, int K, w4a16_plan* plan) {
     case W4A16_KERNEL_SIMT: plan_simt(N, K, plan); return W4A16_OK;
     case W4A16_KERNEL_VANILLA: plan_vanilla(N, K, plan); return W4A16_OK;
     case W4A16_KERNEL_TC:
+    case W4A16_KERNEL_TC_STREAM:
+    case W4A16_KERNEL_TC_TILE: {
       if (!tc_supported(N, K)) return fail(W4A16_ERR_KERNEL, "the tensor-core kernel needs K %% 512 == 0 (K = %d)", K);
-      plan_tc(N, K, plan);
+      const int path = k == W4A16_KERNEL_TC_STREAM ? 1 : k == W4A16_KERNEL_TC_TILE ? 2 : 0;
+      if (path == 2 && !tc_tile_fits(N, K, 1))
+        return fail(W4A16_ERR_KERNEL, "the tile kernel cannot hold K = %d in shared memory", K);
+      plan_tc(N, K, path, plan);
       return W4A16_OK;
+    }
     default: return fail(W4A16_ERR_KERNEL, "unknown kernel selector %d", requested);
   }
 }
@@ -144,14 +154,20 @@ int run_mm(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* S, const w
   a.x = x; a.Wq = Wq; a.S = S; a.B = B; a.y = y;
   a.N = N; a.K = K;
   a.stream = static_cast<cudaStream_t>(stream);
+  a.pdl = env().pdl;
+  a.tc_path = plan.kernel == W4A16_KERNEL_TC_STREAM ? 1 : plan.kernel == W4A16_KERNEL_TC_TILE ? 2 : 0;
   if (int rc = flag_pointer(&a.flags)) return rc;
   for (int row0 = 0; row0 < M; row0 += kMaxChunk) {
     a.row0 = row0;
     a.M = (M - row0 < kMaxChunk) ? M - row0 : kMaxChunk;
+    if (a.tc_path == 2 && !tc_tile_fits(N, K, a.M))
+      return fail(W4A16_ERR_KERNEL, "the tile kernel cannot hold K = %d for %d rows in shared memory", K, a.M);
     cudaError_t e = cudaSuccess;
     switch (plan.kernel) {
       case W4A16_KERNEL_SIMT: e = launch_simt(a, plan); break;
-      case W4A16_KERNEL_TC: e = launch_tc(a, plan); break;
+      case W4A16_KERNEL_TC:
+      case W4A16_KERNEL_TC_STREAM:
+      case W4A16_KERNEL_TC_TILE: e = launch_tc(a, plan); break;
       case W4A16_KERNEL_VANILLA: e = launch_vanilla(a, plan); break;
       default: return fail(W4A16_ERR_KERNEL, "kernel %d cannot run", plan.kernel);
     }
@@ -203,11 +219,14 @@ int w4a16_mm_id_kernel(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16
   a.x = x; a.Wq = Wq; a.S = scales; a.B = biases; a.y = y;
   a.N = N; a.K = K; a.ids = ids; a.T = T; a.E = E;
   a.stream = static_cast<cudaStream_t>(stream);
+  a.pdl = env().pdl;
   if (int rc = flag_pointer(&a.flags)) return rc;
   cudaError_t e = cudaSuccess;
   switch (plan.kernel) {
     case W4A16_KERNEL_SIMT: e = launch_simt_id(a, plan); break;
-    case W4A16_KERNEL_TC: e = launch_tc_id(a, plan); break;
+    case W4A16_KERNEL_TC:
+    case W4A16_KERNEL_TC_STREAM:
+    case W4A16_KERNEL_TC_TILE: e = launch_tc_id(a, plan); break;
     case W4A16_KERNEL_VANILLA: e = launch_vanilla_id(a, plan); break;
     default: return fail(W4A16_ERR_KERNEL, "kernel %d cannot run", plan.kernel);
   }
@@ -247,6 +266,7 @@ int w4a16_mm_noalloc(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* 
   a.x = x; a.Wq = Wq; a.S = scales; a.B = biases; a.y = y;
   a.N = N; a.K = K;
   a.stream = static_cast<cudaStream_t>(stream);
+  a.pdl = env().pdl;
   if (int rc = flag_pointer(&a.flags)) return rc;
   for (int row0 = 0; row0 < M; row0 += kMaxChunk) {
     a.row0 = row0;

@@ -27,6 +27,8 @@ struct LaunchArgs {
   const int32_t* ids;  // mm_id only
   int T, E;            // mm_id only
   int* flags;          // device flag word (mm_id bad ids)
+  int pdl;             // 0: plain launch; 1: programmatic dependent launch; 2: and weights fetched before the wait
+  int tc_path;         // tensor-core launch shape: 0 the dispatcher's choice, 1 persistent, 2 tile
   cudaStream_t stream;
 };
 
@@ -35,8 +37,10 @@ void plan_simt(int N, int K, w4a16_plan* p);
 cudaError_t launch_simt(const LaunchArgs& a, const w4a16_plan& p);
 cudaError_t launch_simt_id(const LaunchArgs& a, const w4a16_plan& p);
 
-void plan_tc(int N, int K, w4a16_plan* p);
+// tc_path: 0 the dispatcher's choice, 1 the persistent grid, 2 the tile kernel.
+void plan_tc(int N, int K, int tc_path, w4a16_plan* p);
 bool tc_supported(int N, int K);
+bool tc_tile_fits(int N, int K, int M);
 cudaError_t launch_tc(const LaunchArgs& a, const w4a16_plan& p);
 cudaError_t launch_tc_id(const LaunchArgs& a, const w4a16_plan& p);
 // Tensor-core w4a16_mm with its split-K scratch in a fixed device array (no allocation).

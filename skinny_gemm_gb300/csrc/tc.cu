@@ -79,6 +79,15 @@ namespace {
 #ifndef W4A16_TC_GROUP_BATCH
 #define W4A16_TC_GROUP_BATCH 2     // 64-groups whose loads and MMA chains are interleaved
 #endif
+#ifndef W4A16_TC_TILE_MAX_UNITS
+#define W4A16_TC_TILE_MAX_UNITS 4863  // largest stages x row tiles the tile kernel takes
+#endif
+#ifndef W4A16_TC_TILE_REGS
+#define W4A16_TC_TILE_REGS 80         // registers per thread the tile kernel is assumed to use
+#endif
+#ifndef W4A16_TC_TILE_SLICES
+#define W4A16_TC_TILE_SLICES 5        // most K-slices one CTA of the tile kernel takes, where a cluster can split
+#endif
 
 constexpr int kTileRows = 32;           // two m16 subtiles per warp
 constexpr int kBoxWords = 32;           // one TMA box row: 128 bytes = 256 codes
@@ -167,6 +176,23 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel on
+// the stream start its CTAs (and their prologue) while this one runs; wait
+// blocks until every kernel this one depends on has completed and its writes
+// are visible.  Without a programmatic dependency both are no-ops.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// 16-byte global load cached in L2 only (activations another kernel may just
+// have written).
+__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
@@ -222,20 +248,46 @@ struct Maps {
   CUtensorMap biases;
 };
 
-__device__ __forceinline__ void ring_issue(Ring& R, const Maps* maps, int st, int tensor_row,
-                                           const uint16_t* x, const int* toks, int mc, int K) {
-  const uint32_t slot = R.issued % (uint32_t)R.S;
-  const uint32_t bar = R.bars0 + 8 * slot;
-  const uint32_t dst = R.codes0 + slot * kCodeSlotBytes;
+// The weight part of a stage: codes (two boxes) and the 8 groups' scales and
+// biases of 32 rows from tensor_row, into slot memory dst; arms `bar` for
+// those bytes plus `mc` activation chunks still to come.
+__device__ __forceinline__ void issue_weights(uint32_t dst, uint32_t bar, const Maps* maps, int st, int tensor_row,
+                                              int mc, uint64_t pol_stream, uint64_t pol_keep) {
   mbar_expect_tx(bar, kCodeSlotBytes + (uint32_t)(mc * kStageK * 2));
-  tma_load_2d(dst, &maps->codes, st * kStageWords, tensor_row, bar, R.pol_stream);
-  tma_load_2d(dst + kBoxBytes, &maps->codes, st * kStageWords + kBoxWords, tensor_row, bar, R.pol_stream);
-  tma_load_2d(dst + kCodeBytes, &maps->scales, st * 8, tensor_row, bar, R.pol_keep);
-  tma_load_2d(dst + kCodeBytes + kParamBytes, &maps->biases, st * 8, tensor_row, bar, R.pol_keep);
+  tma_load_2d(dst, &maps->codes, st * kStageWords, tensor_row, bar, pol_stream);
+  tma_load_2d(dst + kBoxBytes, &maps->codes, st * kStageWords + kBoxWords, tensor_row, bar, pol_stream);
+  tma_load_2d(dst + kCodeBytes, &maps->scales, st * 8, tensor_row, bar, pol_keep);
+  tma_load_2d(dst + kCodeBytes + kParamBytes, &maps->biases, st * 8, tensor_row, bar, pol_keep);
+}
+
+// The activation part of a stage: 512 bf16 of each row toks[0..mc) into rows
+// of kXPitch bytes at xdst.
+__device__ __forceinline__ void issue_x(uint32_t xdst, uint32_t bar, int st, const uint16_t* x, const int* toks,
+                                        int mc, int K, uint64_t pol_keep) {
   const uint16_t* xs = x + (int64_t)st * kStageK;
   for (int n = 0; n < mc; ++n)
-    bulk_load(R.xs0 + slot * R.x_slot + n * kXPitch, xs + (int64_t)toks[n] * K, kStageK * 2, bar, R.pol_keep);
+    bulk_load(xdst + n * kXPitch, xs + (int64_t)toks[n] * K, kStageK * 2, bar, pol_keep);
+}
+
+// Lane 0 only: the weights of stage `st` into the next free slot; returns the slot.
+__device__ __forceinline__ uint32_t ring_issue_w(Ring& R, const Maps* maps, int st, int tensor_row, int mc) {
+  const uint32_t slot = R.issued % (uint32_t)R.S;
+  issue_weights(R.codes0 + slot * kCodeSlotBytes, R.bars0 + 8 * slot, maps, st, tensor_row, mc, R.pol_stream,
+                R.pol_keep);
   ++R.issued;
+  return slot;
+}
+
+// Lane 0 only: the activation chunks of stage `st` into `slot`.
+__device__ __forceinline__ void ring_issue_x(const Ring& R, uint32_t slot, int st, const uint16_t* x, const int* toks,
+                                             int mc, int K) {
+  issue_x(R.xs0 + slot * R.x_slot, R.bars0 + 8 * slot, st, x, toks, mc, K, R.pol_keep);
+}
+
+__device__ __forceinline__ void ring_issue(Ring& R, const Maps* maps, int st, int tensor_row, const uint16_t* x,
+                                           const int* toks, int mc, int K) {
+  const uint32_t slot = ring_issue_w(R, maps, st, tensor_row, mc);
+  ring_issue_x(R, slot, st, x, toks, mc, K);
 }
 
 // All lanes: wait for the oldest outstanding slot.  Returns false on timeout.
@@ -285,42 +337,44 @@ __device__ __forceinline__ void ldsm_offsets(int lane, uint32_t (&off)[2][4]) {
     }
 }
 
-// One stage (32 rows x 512 codes, 8 groups) of the canonical recurrence into
-// p[s][i]: subtile s, i = (row g: columns 2t, 2t+1; row g+8: columns 2t,
+// One stage (16 NSUB rows x 512 codes, 8 groups) of the canonical recurrence
+// into p[s][i]: subtile s, i = (row g: columns 2t, 2t+1; row g+8: columns 2t,
 // 2t+1).  GB groups at a time: their loads are issued first and their MMA
 // chains interleaved.  With ALLCOLS false (one activation row) the odd
 // columns are not rescaled; the even columns' arithmetic is unchanged.
-template <bool ALLCOLS, bool XSTAGED>
+template <int NSUB, bool ALLCOLS, bool XSTAGED>
 __device__ __forceinline__ void compute_stage(uint32_t cbase, uint32_t xbase, bool xvalid, uint32_t sxbase,
-                                              uint32_t sx_stride, bool xvalid_cols, float (&p)[2][4],
-                                              const uint32_t (&loff)[2][4], int g) {
+                                              uint32_t sx_stride, bool xvalid_cols, float (&p)[NSUB][4],
+                                              const uint32_t (&loff)[NSUB][4], int g) {
   constexpr int GB = W4A16_TC_GROUP_BATCH;
+  // Slot layout for 16 * NSUB rows: two code boxes, then scales, then biases.
+  constexpr uint32_t kBox = 16 * NSUB * 128, kScales = 2 * kBox, kBiases = kScales + 16 * NSUB * 16;
   // scale / bias of the 8 groups for this lane's rows 16(i>>1) + g + 8(i&1)
-  uint4 ps[4], pb[4];
+  uint4 ps[2 * NSUB], pb[2 * NSUB];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < 2 * NSUB; ++i) {
     const uint32_t r = 16 * (i >> 1) + g + 8 * (i & 1);
-    ps[i] = lds128(cbase + kCodeBytes + r * 16);
-    pb[i] = lds128(cbase + kCodeBytes + kParamBytes + r * 16);
+    ps[i] = lds128(cbase + kScales + r * 16);
+    pb[i] = lds128(cbase + kBiases + r * 16);
   }
 #pragma unroll
   for (int gp = 0; gp < 8; gp += GB) {
-    uint32_t w[GB][2][4];  // [group][subtile]: rows g / g+8 of chunk 2gl, then of chunk 2gl+1
-    uint4 u[GB][2];        // [group][chunk] activations
+    uint32_t w[GB][NSUB][4];  // [group][subtile]: rows g / g+8 of chunk 2gl, then of chunk 2gl+1
+    uint4 u[GB][2];           // [group][chunk] activations
 #pragma unroll
     for (int j = 0; j < GB; ++j) {
       const int gi = gp + j;
 #pragma unroll
-      for (int s = 0; s < 2; ++s)
-        ldsm_x4(cbase + (gi >> 2) * kBoxBytes + loff[s][gi & 3], w[j][s][0], w[j][s][1], w[j][s][2], w[j][s][3]);
+      for (int s = 0; s < NSUB; ++s)
+        ldsm_x4(cbase + (gi >> 2) * kBox + loff[s][gi & 3], w[j][s][0], w[j][s][1], w[j][s][2], w[j][s][3]);
 #pragma unroll
-      for (int cb = 0; cb < 2; ++cb) {
+    for (int cb = 0; cb < 2; ++cb) {
         u[j][cb] = make_uint4(0, 0, 0, 0);
         if (xvalid) u[j][cb] = lds128(xbase + 128 * gi + 64 * cb);
       }
     }
     uint32_t bx[GB][2][2][2];  // [group][chunk][h][reg]
-    float sx[GB][4], acc[GB][2][4];
+    float sx[GB][4], acc[GB][NSUB][4];
 #pragma unroll
     for (int j = 0; j < GB; ++j) {
 #pragma unroll
@@ -337,8 +391,8 @@ __device__ __forceinline__ void compute_stage(uint32_t cbase, uint32_t xbase, bo
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         sx[j][i] = 0.f;
-        acc[j][0][i] = 0.f;
-        acc[j][1][i] = 0.f;
+#pragma unroll
+        for (int s = 0; s < NSUB; ++s) acc[j][s][i] = 0.f;
       }
       if (XSTAGED && xvalid_cols) {  // precomputed group sums of columns 2t, 2t+1
         const float2 v = lds64f(sxbase + sx_stride * (gp + j));
@@ -354,7 +408,7 @@ __device__ __forceinline__ void compute_stage(uint32_t cbase, uint32_t xbase, bo
       for (int j = 0; j < GB; ++j) {
         if (!XSTAGED) mma_bf16(sx[j], kOnes, kOnes, kOnes, kOnes, bx[j][cb][h][0], bx[j][cb][h][1]);
 #pragma unroll
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < NSUB; ++s) {
           const uint32_t wg = w[j][s][2 * cb], wg8 = w[j][s][2 * cb + 1];
           const uint32_t a0 = codes_as_bf16x2(wg >> (8 * h));
           const uint32_t a1 = codes_as_bf16x2(wg8 >> (8 * h));
@@ -369,7 +423,7 @@ __device__ __forceinline__ void compute_stage(uint32_t cbase, uint32_t xbase, bo
     for (int j = 0; j < GB; ++j) {
       const int gi = gp + j;
 #pragma unroll
-      for (int s = 0; s < 2; ++s)
+      for (int s = 0; s < NSUB; ++s)
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
           const int i = 2 * s + rr;
@@ -424,6 +478,7 @@ struct StreamParams {
   int nst, sl, ks, tiles, units;
   int stages;
   int xpitch;       // bytes per activation row of the pre-staged copy (0: per-stage copies)
+  int prefetch;     // request the first weight stages before waiting for earlier kernels
 };
 
 // Columns of the group-sum table: the even count >= mc (lane t reads columns 2t, 2t+1).
@@ -460,6 +515,7 @@ template <bool ALLCOLS, bool XSTAGED>
 __global__ void __launch_bounds__(kStreamWarps * 32, W4A16_TC_MIN_BLOCKS) tc_stream_kernel(
     const __grid_constant__ Maps maps, StreamParams p) {
   extern __shared__ uint8_t smem_raw[];
+  pdl_launch_dependents();
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -499,19 +555,42 @@ __global__ void __launch_bounds__(kStreamWarps * 32, W4A16_TC_MIN_BLOCKS) tc_str
   ic.init(gw, p.ks);
   int ist = ic.slice * p.sl;
   int iend = min(ist + p.sl, p.nst);
-  auto issue_next = [&]() {
-    if (ic.u >= p.units) return;
-    ring_issue(R, &maps, ist, ic.tile * kTileRows, p.x, s_tok, xring, p.K);
-    if (++ist == iend) {
-      ic.advance(TW, tw_tiles, tw_slices, p.ks);
-      ist = ic.slice * p.sl;
-      iend = min(ist + p.sl, p.nst);
+  auto step = [&](UnitCursor& c, int& st, int& end) {
+    if (++st == end) {
+      c.advance(TW, tw_tiles, tw_slices, p.ks);
+      st = c.slice * p.sl;
+      end = min(st + p.sl, p.nst);
     }
   };
-  // the first weight stages are in flight while the activations are staged
+  auto issue_next = [&](bool with_x) {
+    if (ic.u >= p.units) return;
+    const uint32_t slot = ring_issue_w(R, &maps, ist, ic.tile * kTileRows, xring);
+    if (with_x) ring_issue_x(R, slot, ist, p.x, s_tok, xring, p.K);
+    step(ic, ist, iend);
+  };
+  // The weights never depend on earlier kernels: with p.prefetch the first
+  // stages are requested before the wait for those kernels and their
+  // activation chunks after it (replaying the cursor from the start).
+  // Activations, outputs and the workspace are only touched after the wait.
+  // The first stages stay in flight while the activations are staged.
   if (lane == 0) {
     fence_proxy_async();
-    for (int i = 0; i < S; ++i) issue_next();
+    if (p.prefetch)
+      for (int i = 0; i < S; ++i) issue_next(false);
+  }
+  pdl_wait();
+  if (lane == 0) {
+    if (p.prefetch) {
+      UnitCursor rc;
+      rc.init(gw, p.ks);
+      int rst = rc.slice * p.sl, rend = min(rst + p.sl, p.nst);
+      for (uint32_t i = 0; i < R.issued; ++i) {
+        ring_issue_x(R, i, rst, p.x, s_tok, xring, p.K);
+        step(rc, rst, rend);
+      }
+    } else {
+      for (int i = 0; i < S; ++i) issue_next(true);
+    }
   }
 
   if (XSTAGED) {
@@ -520,7 +599,7 @@ __global__ void __launch_bounds__(kStreamWarps * 32, W4A16_TC_MIN_BLOCKS) tc_str
     const int chunks = p.K / 8;
     for (int c = threadIdx.x; c < mc * chunks; c += blockDim.x) {
       const int n = c / chunks, wd = c - n * chunks;
-      const uint4 u = ld_nc_v4(p.x + (int64_t)(p.row0 + n) * p.K + 8 * wd);
+      const uint4 u = ld_cg_v4(p.x + (int64_t)(p.row0 + n) * p.K + 8 * wd);
       uint32_t b[2][2];
       frag_from_chunk(u, b);
       sts128(xst + n * p.xpitch + 16 * wd, make_uint4(b[0][0], b[0][1], b[1][0], b[1][1]));
@@ -616,12 +695,12 @@ __global__ void __launch_bounds__(kStreamWarps * 32, W4A16_TC_MIN_BLOCKS) tc_str
       } else {
         xbase = ordered(R.xs0 + slot * x_slot + g * kXPitch + 16 * t);
       }
-      compute_stage<ALLCOLS, XSTAGED>(cbase, xbase, g < mc, sxbase, sx_cols(mc) * 4, 2 * t < mc, acc, loff, g);
+      compute_stage<2, ALLCOLS, XSTAGED>(cbase, xbase, g < mc, sxbase, sx_cols(mc) * 4, 2 * t < mc, acc, loff, g);
       ++R.consumed;
       __syncwarp();
       if (lane == 0) {
         fence_proxy_async();
-        issue_next();
+        issue_next(true);
       }
     }
     if (timed_out) break;
@@ -676,6 +755,169 @@ __global__ void __launch_bounds__(kStreamWarps * 32, W4A16_TC_MIN_BLOCKS) tc_str
   }
 }
 
+// ---- tile kernel (w4a16_mm when every warp would get about one unit) ---------------------
+//
+// A 16-row tile's K range is split over a cluster of kc CTAs (kc = 1: one
+// CTA); each CTA holds its share in shared memory at once, one slot per
+// 512-code stage, all requested up front.  Warp w of a CTA computes its
+// slices w, w + W, ... (one m16 subtile), so a warp's serial work is a single
+// 16-row slice.  Every slice sum goes to the shared memory of the cluster's
+// first CTA (distributed shared memory), which adds them in slice order --
+// the same canonical arithmetic as the persistent kernel, with no workspace,
+// atomics or global fences.
+
+constexpr int kTile16 = 16;
+constexpr int kBox16 = kTile16 * 128;    // one 128-byte box row for 16 rows
+constexpr int kParam16 = kTile16 * 16;   // 8 bf16 per row
+constexpr int kSlot16 = 5 * 1024;        // codes 2 x 2 KB | scales 256 | biases 256 | pad (1 KB alignment)
+constexpr int kTileMaxWarps = 16;
+constexpr int kMaxCluster = 8;
+
+struct TileParams {
+  const uint16_t* x;
+  uint16_t* y;
+  int* flags;
+  int N, K, M, row0;
+  int nst, sl, ks;
+  int kc;        // CTAs (one cluster) per 16-row tile
+  int nloc;      // stage slots per CTA: ceil(ks / kc) * sl
+  int prefetch;  // request the weights before waiting for earlier kernels
+};
+
+// Shared memory (the same layout in every CTA of a cluster): slots
+// [nloc][kSlot16] | activation chunks [nloc][mc][kXPitch] | barriers [nloc] |
+// slice sums [ks][16][8] fp32 (used in the first CTA) | tokens [8], abort flag.
+__host__ __device__ inline int tile_smem(int nloc, int mc, int ks) {
+  return nloc * (kSlot16 + mc * kXPitch) + nloc * 8 + ks * kTile16 * 8 * 4 + 64 + 1024;
+}
+
+__host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+template <bool ALLCOLS>
+// The bound of 768 threads caps registers at 80, so that five CTAs of five
+// warps fit on an SM.
+__global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Maps maps, TileParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  pdl_launch_dependents();
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, W = blockDim.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int mc = p.M, kc = p.kc;
+  // with cluster dimensions (kc, 1, 1) the rank in the cluster is blockIdx.x % kc
+  const int tile = blockIdx.x / kc, crank = blockIdx.x - tile * kc;
+  const int j0 = crank * p.ks / kc, j1 = (crank + 1) * p.ks / kc;  // this CTA's slices
+  const int st0 = j0 * p.sl, nloc = min(j1 * p.sl, p.nst) - st0;  // and stages
+  const int tensor_row = tile * kTile16;
+  const int x_slot = mc * kXPitch;
+  const uint32_t codes0 = smem_u32(base);
+  const uint32_t xs0 = codes0 + (uint32_t)(p.nloc * kSlot16);
+  const uint32_t bars0 = xs0 + (uint32_t)(p.nloc * x_slot);
+  float* red = reinterpret_cast<float*>(base + (bars0 - codes0) + p.nloc * 8);
+  int* s_tok = reinterpret_cast<int*>(red + p.ks * kTile16 * 8);
+  int* s_abort = s_tok + kMaxChunk;
+
+  for (int i = threadIdx.x; i < nloc; i += blockDim.x) mbar_init(bars0 + 8 * i, 1);
+  if (threadIdx.x < mc) s_tok[threadIdx.x] = p.row0 + threadIdx.x;
+  if (threadIdx.x == 0) *s_abort = 0;
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  __syncthreads();
+  // announce that this CTA runs (its shared memory may now be written by the others)
+  if (kc > 1) cluster_arrive_relaxed();
+
+  // lane 0 of warp w requests local stages w, w + W, ...
+  auto weights = [&](int i) {
+    const int st = st0 + i;
+    const uint32_t dst = codes0 + i * kSlot16, bar = bars0 + 8 * i;
+    const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_last();
+    mbar_expect_tx(bar, 2 * kBox16 + 2 * kParam16 + (uint32_t)(mc * kStageK * 2));
+    tma_load_2d(dst, &maps.codes, st * kStageWords, tensor_row, bar, pol_stream);
+    tma_load_2d(dst + kBox16, &maps.codes, st * kStageWords + kBoxWords, tensor_row, bar, pol_stream);
+    tma_load_2d(dst + 2 * kBox16, &maps.scales, st * 8, tensor_row, bar, pol_keep);
+    tma_load_2d(dst + 2 * kBox16 + kParam16, &maps.biases, st * 8, tensor_row, bar, pol_keep);
+  };
+  if (lane == 0 && p.prefetch)
+    for (int i = warp; i < nloc; i += W) weights(i);
+  pdl_wait();
+  if (lane == 0)
+    for (int i = warp; i < nloc; i += W) {
+      if (!p.prefetch) weights(i);
+      issue_x(xs0 + i * x_slot, bars0 + 8 * i, st0 + i, p.x, s_tok, mc, p.K, policy_evict_last());
+    }
+
+  // slice sums go to the first CTA of the cluster, once every CTA of it runs
+  uint32_t red_dst = smem_u32(red);
+  __syncwarp();  // the cluster barrier instructions are .aligned: whole warps only
+  if (kc > 1) {
+    red_dst = map_to_rank(red_dst, 0);
+    cluster_wait();
+  }
+  uint32_t loff2[2][4];
+  ldsm_offsets(lane, loff2);
+  const uint32_t loff[1][4] = {{loff2[0][0], loff2[0][1], loff2[0][2], loff2[0][3]}};
+  bool ok = true;
+  for (int j = j0 + warp; j < j1 && ok; j += W) {
+    float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+    const int s1 = min((j + 1) * p.sl, p.nst);
+    for (int st = j * p.sl; st < s1; ++st) {
+      const int i = st - st0;
+      if (!__all_sync(0xffffffffu, mbar_wait(bars0 + 8 * i, 0u))) {
+        ok = false;
+        break;
+      }
+      const uint32_t cbase = ordered(codes0 + i * kSlot16);
+      const uint32_t xbase = ordered(xs0 + i * x_slot + g * kXPitch + 16 * t);
+      compute_stage<1, ALLCOLS, false>(cbase, xbase, g < mc, 0u, 0u, false, acc, loff, g);
+    }
+    if (!ok) break;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      st_cluster_f32(red_dst + 4 * ((j * kTile16 + g + 8 * (i >> 1)) * 8 + 2 * t + (i & 1)), acc[0][i]);
+  }
+  if (!ok && lane == 0) {
+    atomicOr(p.flags, W4A16_DEVICE_TIMEOUT);
+    *s_abort = 1;
+  }
+  __syncwarp();
+  if (kc > 1) {
+    cluster_arrive();
+    cluster_wait();
+  } else {
+    __syncthreads();
+  }
+  if (*s_abort) {
+    // let every copy this warp requested land before shared memory is released
+    if (lane == 0)
+      for (int i = warp; i < nloc; i += W) mbar_wait(bars0 + 8 * i, 0u);
+    return;
+  }
+  if (crank != 0) return;
+  for (int i = threadIdx.x; i < kTile16 * mc; i += blockDim.x) {
+    const int n = i / kTile16, r = i - n * kTile16;
+    const int row = tensor_row + r;
+    if (row < p.N) {
+      float sum = red[r * 8 + n];
+      for (int j = 1; j < p.ks; ++j) sum = __fadd_rn(sum, red[(j * kTile16 + r) * 8 + n]);
+      p.y[(int64_t)s_tok[n] * p.N + row] = f32_to_bf16_bits(sum);
+    }
+  }
+}
+
 // ---- routed kernel (w4a16_mm_id) -------------------------------------------------------
 
 struct RoutedParams {
@@ -720,12 +962,14 @@ __global__ void __launch_bounds__(kRoutedWarps * 32) tc_routed_kernel(const __gr
   R.pol_stream = policy_evict_first();
   R.pol_keep = policy_evict_last();
 
+  pdl_launch_dependents();
   if (lane == 0)
     for (int i = 0; i < S; ++i) mbar_init(R.bars0 + 8 * i, 1);
   if (threadIdx.x == 0) {
     s_state[0] = 0;
     s_state[2] = 0;
   }
+  pdl_wait();  // ids, activations and outputs belong to earlier kernels
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   __syncthreads();
 
@@ -768,7 +1012,7 @@ __global__ void __launch_bounds__(kRoutedWarps * 32) tc_routed_kernel(const __gr
         }
         const uint32_t cbase = ordered(R.codes0 + slot * kCodeSlotBytes);
         const uint32_t xbase = ordered(R.xs0 + slot * x_slot + g * kXPitch + 16 * t);
-        compute_stage<true, false>(cbase, xbase, g < mc, 0u, 0u, false, acc, loff, g);
+        compute_stage<2, true, false>(cbase, xbase, g < mc, 0u, 0u, false, acc, loff, g);
         ++R.consumed;
         __syncwarp();
         if (lane == 0) {
@@ -844,11 +1088,11 @@ cudaError_t get_encoder() {
   return g_encode_status;
 }
 
-cudaError_t make_param_map(CUtensorMap* map, const uint16_t* P, int64_t rows, int K) {
+cudaError_t make_param_map(CUtensorMap* map, const uint16_t* P, int64_t rows, int K, int box_rows) {
   if (cudaError_t e = get_encoder()) return e;
   cuuint64_t dims[2] = {(cuuint64_t)(K / kGroup), (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)(K / kGroup) * 2};
-  cuuint32_t box[2] = {8, (cuuint32_t)kTileRows};
+  cuuint32_t box[2] = {8, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t*>(P), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -856,13 +1100,11 @@ cudaError_t make_param_map(CUtensorMap* map, const uint16_t* P, int64_t rows, in
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t make_maps(Maps* m, const uint32_t* Wq, const uint16_t* S, const uint16_t* B, int64_t rows, int K);
-
-cudaError_t make_code_map(CUtensorMap* map, const uint32_t* Wq, int64_t rows, int K) {
+cudaError_t make_code_map(CUtensorMap* map, const uint32_t* Wq, int64_t rows, int K, int box_rows) {
   if (cudaError_t e = get_encoder()) return e;
   cuuint64_t dims[2] = {(cuuint64_t)(K / 8), (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)K / 2};
-  cuuint32_t box[2] = {(cuuint32_t)kBoxWords, (cuuint32_t)kTileRows};
+  cuuint32_t box[2] = {(cuuint32_t)kBoxWords, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(Wq), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -870,10 +1112,13 @@ cudaError_t make_code_map(CUtensorMap* map, const uint32_t* Wq, int64_t rows, in
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t make_maps(Maps* m, const uint32_t* Wq, const uint16_t* S, const uint16_t* B, int64_t rows, int K) {
-  if (cudaError_t e = make_code_map(&m->codes, Wq, rows, K)) return e;
-  if (cudaError_t e = make_param_map(&m->scales, S, rows, K)) return e;
-  return make_param_map(&m->biases, B, rows, K);
+// Tensor maps of one weight set with boxes of box_rows rows (32 for the
+// persistent and routed kernels, 16 for the tile kernel).
+cudaError_t make_maps(Maps* m, const uint32_t* Wq, const uint16_t* S, const uint16_t* B, int64_t rows, int K,
+                      int box_rows = kTileRows) {
+  if (cudaError_t e = make_code_map(&m->codes, Wq, rows, K, box_rows)) return e;
+  if (cudaError_t e = make_param_map(&m->scales, S, rows, K, box_rows)) return e;
+  return make_param_map(&m->biases, B, rows, K, box_rows);
 }
 
 int stream_smem(int stages, int mc) {
@@ -890,7 +1135,7 @@ int stream_stages(int mc) {
 
 struct DeviceInfo {
   int sms = 152;
-  bool attr_set[5] = {false, false, false, false, false};  // stream<cols, staged> x4, routed
+  bool attr_set[7] = {};  // stream<cols, staged> x4, routed, tile<one column>, tile<all columns>
 };
 
 // The activations are pre-staged (once per CTA) when the CTA, with a
@@ -910,9 +1155,40 @@ int staged_stages(int M, int K) {
   return 2;
 }
 
+// Launch with, when pdl is set, a programmatic dependency on the previous
+// kernel of the stream (the kernels wait for it with griddepcontrol.wait
+// before touching anything it may have written), and with clusters of
+// `cluster` CTAs along x when cluster > 1.
+template <typename Kern, typename Params>
+cudaError_t launch_ex(Kern fn, dim3 grid, dim3 block, int smem, cudaStream_t stream, bool pdl, const Maps& maps,
+                      const Params& p, int cluster = 1) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, fn, maps, p);
+}
+
 template <bool A, bool X>
 cudaError_t stream_launch_t(const Maps& map, const StreamParams& p, int sms, int smem, DeviceInfo& d,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, bool pdl) {
   auto* fn = tc_stream_kernel<A, X>;
   const int idx = (A ? 1 : 0) + (X ? 2 : 0);
   if (!d.attr_set[idx]) {
@@ -925,24 +1201,111 @@ cudaError_t stream_launch_t(const Maps& map, const StreamParams& p, int sms, int
   int grid = sms * per_sm;
   const int need = (p.units + kStreamWarps - 1) / kStreamWarps;
   if (grid > need) grid = need;
-  fn<<<grid, kStreamWarps * 32, smem, stream>>>(map, p);
-  return cudaGetLastError();
+  return launch_ex(fn, dim3(grid), dim3(kStreamWarps * 32), smem, stream, pdl, map, p);
 }
 
 // Persistent grid for one chunk: every SM filled to its occupancy, never more
 // CTAs than there are groups of four work units.  The caller holds g_dev_mu.
-cudaError_t launch_stream(const Maps& map, StreamParams p, int sms, DeviceInfo& d, cudaStream_t stream) {
+cudaError_t launch_stream(const Maps& map, StreamParams p, int sms, DeviceInfo& d, cudaStream_t stream, int pdl) {
   const bool allcols = p.M > 1;
   const bool staged = stage_activations(p.M, p.K, p.units, sms);
   p.xpitch = staged ? 2 * p.K + 64 : 0;
   p.stages = staged ? staged_stages(p.M, p.K) : stream_stages(p.M);
+  p.prefetch = pdl >= 2;
   int smem = stream_smem(p.stages, staged ? 0 : p.M);
   if (staged) smem += xstage_bytes(p.M, p.K);
+  const bool on = pdl > 0;
   if (allcols)
-    return staged ? stream_launch_t<true, true>(map, p, sms, smem, d, stream)
-                  : stream_launch_t<true, false>(map, p, sms, smem, d, stream);
-  return staged ? stream_launch_t<false, true>(map, p, sms, smem, d, stream)
-                : stream_launch_t<false, false>(map, p, sms, smem, d, stream);
+    return staged ? stream_launch_t<true, true>(map, p, sms, smem, d, stream, on)
+                  : stream_launch_t<true, false>(map, p, sms, smem, d, stream, on);
+  return staged ? stream_launch_t<false, true>(map, p, sms, smem, d, stream, on)
+                : stream_launch_t<false, false>(map, p, sms, smem, d, stream, on);
+}
+
+// Launch shape of the tile kernel for one chunk of M rows.
+struct TilePlan {
+  int kc = 0;     // CTAs per 16-row tile (cluster size); 0: the tile kernel does not apply
+  int nloc = 0;   // stage slots per CTA
+  int warps = 0;  // warps per CTA
+  int smem = 0;   // dynamic shared memory per CTA
+  int ctas = 0;   // grid size
+};
+
+// Registers per thread of the tile kernel as compiled (rounded up to the
+// allocation unit of 8), read once from the runtime; the assumed value
+// without a GPU.
+int tile_regs() {
+  static int regs = [] {
+    int r = W4A16_TC_TILE_REGS;
+    cudaFuncAttributes fa0, fa1;
+    if (cudaFuncGetAttributes(&fa0, tc_tile_kernel<false>) == cudaSuccess &&
+        cudaFuncGetAttributes(&fa1, tc_tile_kernel<true>) == cudaSuccess)
+      r = max(fa0.numRegs, fa1.numRegs);
+    else
+      cudaGetLastError();
+    return (r + 7) & ~7;
+  }();
+  return regs;
+}
+
+// CTAs of `threads` threads and `smem` bytes of shared memory that fit on one SM.
+int tile_ctas_per_sm(int threads, int smem) {
+  int per_sm = (228 * 1024) / (smem + 1024);
+  const int by_regs = 65536 / (threads * tile_regs());
+  const int by_warps = 64 / (threads / 32);
+  if (by_regs < per_sm) per_sm = by_regs;
+  if (by_warps < per_sm) per_sm = by_warps;
+  return per_sm < 32 ? per_sm : 32;
+}
+
+// The tile kernel serves shapes whose canonical slices are single stages (a
+// persistent grid would give each warp about one unit).  A tile's slices are
+// dealt to clusters of kc CTAs with at most W4A16_TC_TILE_SLICES each; kc
+// grows (up to 8) until every CTA fits in shared memory and all of them fit
+// on the GPU at once.  `force` drops the last condition (the CTAs then run
+// in waves).
+TilePlan tile_plan(const Shape& s, int N, int M, int sms, bool force) {
+  TilePlan tp;
+  if (!force && s.nst * s.tiles > W4A16_TC_TILE_MAX_UNITS) return tp;
+  const int tiles16 = cdiv(N, kTile16);
+  for (int kc = min(kMaxCluster, max(1, cdiv(s.ks, W4A16_TC_TILE_SLICES))); kc <= kMaxCluster; ++kc) {
+    if (kc > s.ks) break;
+    const int ksl = cdiv(s.ks, kc);
+    const int nloc = ksl * s.sl;
+    const int smem = tile_smem(nloc, M, s.ks);
+    if (smem > kSmemLimit) continue;
+    const int warps = ksl < kTileMaxWarps ? ksl : kTileMaxWarps;
+    const int ctas = tiles16 * kc;
+    if (force || ctas <= tile_ctas_per_sm(warps * 32, smem) * sms) {
+      tp.kc = kc;
+      tp.nloc = nloc;
+      tp.warps = warps;
+      tp.smem = smem;
+      tp.ctas = ctas;
+      return tp;
+    }
+  }
+  return tp;
+}
+
+cudaError_t launch_tile(const LaunchArgs& a, const Shape& s, const TilePlan& tp, DeviceInfo& d) {
+  Maps maps;
+  if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, a.N, a.K, kTile16)) return e;
+  TileParams p;
+  p.x = a.x; p.y = a.y; p.flags = a.flags;
+  p.N = a.N; p.K = a.K; p.M = a.M; p.row0 = a.row0;
+  p.nst = s.nst; p.sl = s.sl; p.ks = s.ks;
+  p.kc = tp.kc;
+  p.nloc = tp.nloc;
+  p.prefetch = a.pdl >= 2;
+  const bool allcols = a.M > 1;
+  auto* fn = allcols ? tc_tile_kernel<true> : tc_tile_kernel<false>;
+  const int idx = allcols ? 6 : 5;
+  if (!d.attr_set[idx]) {
+    if (cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit)) return e;
+    d.attr_set[idx] = true;
+  }
+  return launch_ex(fn, dim3(tp.ctas), dim3(tp.warps * 32), tp.smem, a.stream, a.pdl > 0, maps, p, tp.kc);
 }
 
 std::mutex g_dev_mu;
@@ -1001,7 +1364,9 @@ bool tc_supported(int N, int K) {
   return K % kStageK == 0;
 }
 
-void plan_tc(int N, int K, w4a16_plan* p) {
+bool tc_tile_fits(int N, int K, int M) { return tile_plan(tc_shape(N, K), N, M, 152, true).kc > 0; }
+
+void plan_tc(int N, int K, int tc_path, w4a16_plan* p) {
   const Shape s = tc_shape(N, K);
   int sms = 152;
   int dev = 0;
@@ -1011,17 +1376,25 @@ void plan_tc(int N, int K, w4a16_plan* p) {
   } else {
     cudaGetLastError();
   }
+  p->ksplit = s.ks;
+  p->slice_k = s.sl * kStageK;
+  p->rows_per_tile = kTileRows;
+  p->units = s.units;
+  p->kernel = tc_path == 1 ? W4A16_KERNEL_TC_STREAM : tc_path == 2 ? W4A16_KERNEL_TC_TILE : W4A16_KERNEL_TC;
+  const TilePlan tp = tc_path == 1 ? TilePlan() : tile_plan(s, N, 1, sms, tc_path == 2);
+  if (tp.kc > 0) {  // clusters of kc CTAs per 16-row tile
+    p->rows_per_tile = kTile16;
+    p->threads = tp.warps * 32;
+    p->grid_x = tp.ctas;
+    p->smem_bytes = tp.smem;
+    return;
+  }
   const bool staged = stage_activations(1, K, s.units, sms);
   const int smem = staged ? stream_smem(staged_stages(1, K), 0) + xstage_bytes(1, K) : stream_smem(stream_stages(1), 1);
   const int per_sm = kSmemLimit / smem > 0 ? kSmemLimit / smem : 1;
   int grid = sms * per_sm;
   const int need = (s.units + kStreamWarps - 1) / kStreamWarps;
   if (grid > need) grid = need;
-  p->kernel = W4A16_KERNEL_TC;
-  p->ksplit = s.ks;
-  p->slice_k = s.sl * kStageK;
-  p->rows_per_tile = kTileRows;
-  p->units = s.units;
   p->threads = kStreamWarps * 32;
   p->grid_x = grid;
   p->smem_bytes = smem;
@@ -1040,10 +1413,15 @@ cudaError_t launch_tc(const LaunchArgs& a, const w4a16_plan& plan) {
   p.xpitch = 0;
   p.part = nullptr;
   p.cnt = nullptr;
-  Maps maps;
-  if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, a.N, a.K)) return e;
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DeviceInfo& d = device_info(dev);
+  if (a.tc_path != 1) {
+    const TilePlan tp = tile_plan(s, a.N, a.M, d.sms, a.tc_path == 2);
+    if (tp.kc > 0) return launch_tile(a, s, tp, d);
+    if (a.tc_path == 2) return cudaErrorInvalidConfiguration;
+  }
+  Maps maps;
+  if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, a.N, a.K)) return e;
   if (s.ks > 1) {
     if (s.tiles > kWsTiles || s.units > kWsUnits) return cudaErrorInvalidValue;
     void* ws = nullptr;
@@ -1051,7 +1429,7 @@ cudaError_t launch_tc(const LaunchArgs& a, const w4a16_plan& plan) {
     p.cnt = static_cast<int*>(ws);
     p.part = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsCounterBytes);
   }
-  return launch_stream(maps, p, d.sms, d, a.stream);
+  return launch_stream(maps, p, d.sms, d, a.stream, a.pdl);
 }
 
 cudaError_t launch_tc_id(const LaunchArgs& a, const w4a16_plan& plan) {
@@ -1081,9 +1459,7 @@ cudaError_t launch_tc_id(const LaunchArgs& a, const w4a16_plan& plan) {
   }
   Maps maps;
   if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, (int64_t)a.N * a.E, a.K)) return e;
-  dim3 grid(s.tiles, a.E);
-  tc_routed_kernel<<<grid, p.warps * 32, smem, a.stream>>>(maps, p);
-  return cudaGetLastError();
+  return launch_ex(tc_routed_kernel, dim3(s.tiles, a.E), dim3(p.warps * 32), smem, a.stream, a.pdl > 0, maps, p);
 }
 
 
@@ -1143,7 +1519,7 @@ cudaError_t launch_tc_noalloc(const LaunchArgs& a) {
     // the array keeps whatever the previous call left: the counters must start at zero
     if (cudaError_t e = cudaMemsetAsync(p.cnt, 0, (size_t)s.tiles * 4, a.stream)) return e;
   }
-  return launch_stream(maps, p, d.sms, d, a.stream);
+  return launch_stream(maps, p, d.sms, d, a.stream, a.pdl);
 }
 
 }  // namespace w4a16

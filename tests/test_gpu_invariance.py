@@ -35,6 +35,24 @@ def test_every_family_is_batch_invariant(kernel):
     _rows_equal_single(1000, 3072, [3, 8, 11], kernel=kernel, seed=2)
 
 
+@pytest.mark.parametrize("N,K", [(1, 512), (33, 2560), (1000, 3072), (4099, 4096), (12288, 1536), (6144, 2048)]
+                         + sorted(set(DECODE_SET.values())))
+def test_tc_launch_shapes_agree_bitwise(N, K):
+    """The persistent grid and the tile kernel implement the same canonical
+    slice order, so the dispatcher may pick either for any M."""
+    w = dev_weights(6, N, K)
+    x = to_dev_bf16(synth.make_x(24, 8, K))
+    for M in (1, 3, 8):
+        a = bf16_bits(ops.mm(x[:M], w, kernel="tc_stream"))
+        try:
+            b = bf16_bits(ops.mm(x[:M], w, kernel="tc_tile"))
+        except ops.W4A16ValueError:
+            assert M > 1, "the tile kernel holds every decode shape at M = 1"
+            continue
+        assert np.array_equal(a, b), f"{N}x{K} M={M}: tile and persistent launches differ"
+        assert np.array_equal(a, bf16_bits(ops.mm(x[:M], w))), f"{N}x{K} M={M}: dispatcher differs"
+
+
 def test_lm_head_rows_bitwise():
     N, K = LM_HEADS[0]
     _rows_equal_single(N, K, [3], seed=4)

@@ -47,6 +47,26 @@ def test_tc_ragged_shapes(N, K, M):
     assert_parity(y, yr, ad, f"tc M={M} N={N} K={K}")
 
 
+@pytest.mark.parametrize("N,K", [(1, 512), (7, 1024), (31, 1536), (33, 2560), (95, 1536), (1000, 3072), (4099, 4096)])
+@pytest.mark.parametrize("M", [1, 5, 8])
+def test_tc_persistent_grid_ragged_shapes(N, K, M):
+    """The persistent launch shape (split-K through the workspace), forced on
+    shapes the dispatcher would give to the tile kernel."""
+    xb, hw, y = _run(M, N, K, "tc_stream", seed=N + K + 1, xseed=M + 40)
+    yr, ad = oracle_mm(xb, hw)
+    assert_parity(y, yr, ad, f"tc_stream M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("N,K", [(1, 512), (31, 1536), (1000, 3072), (2560, 10240), (1536, 12288)])
+@pytest.mark.parametrize("M", [1, 3])
+def test_tc_tile_kernel_ragged_shapes(N, K, M):
+    """The tile launch shape, forced on shapes the dispatcher may give to the
+    persistent grid (more CTAs than fit at once run in waves)."""
+    xb, hw, y = _run(M, N, K, "tc_tile", seed=N + K + 2, xseed=M + 50)
+    yr, ad = oracle_mm(xb, hw)
+    assert_parity(y, yr, ad, f"tc_tile M={M} N={N} K={K}")
+
+
 def test_tc_rejects_k_not_multiple_of_512():
     with pytest.raises(ValueError):
         _run(1, 64, 768, "tc")
