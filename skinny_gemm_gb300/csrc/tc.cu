@@ -57,6 +57,7 @@
 
 #include <map>
 #include <mutex>
+#include <set>
 #include <utility>
 
 #include "common.cuh"
@@ -82,8 +83,8 @@ namespace {
 #ifndef W4A16_TC_TILE_MAX_UNITS
 #define W4A16_TC_TILE_MAX_UNITS 4863  // largest stages x row tiles the tile kernel takes
 #endif
-#ifndef W4A16_TC_TILE_REGS
-#define W4A16_TC_TILE_REGS 80         // registers per thread the tile kernel is assumed to use
+#ifndef W4A16_TC_STREAM_NSUB1_MIN_M
+#define W4A16_TC_STREAM_NSUB1_MIN_M 2  // smallest chunk the persistent kernel runs with 16-row warps
 #endif
 #ifndef W4A16_TC_TILE_SLICES
 #define W4A16_TC_TILE_SLICES 5        // most K-slices one CTA of the tile kernel takes, where a cluster can split
@@ -100,11 +101,27 @@ constexpr int kCodeSlotBytes = kCodeBytes + 2 * kParamBytes;     // 9216: codes 
 constexpr int kXPitch = kStageK * 2 + 64;                        // 1088: conflict-free LDS.128
 constexpr int kStreamWarps = 4;          // warps per CTA of the persistent kernel
 constexpr int kRoutedWarps = 8;          // max warps per CTA of the routed kernel
-constexpr int kTargetUnits = 152 * 16;   // work units wanted per chunk (~16 per SM)
+#ifndef W4A16_TC_TARGET_UNITS
+#define W4A16_TC_TARGET_UNITS (152 * 16)
+#endif
+constexpr int kTargetUnits = W4A16_TC_TARGET_UNITS;  // work units wanted per chunk (~16 per SM)
 constexpr int kSmemLimit = 227 * 1024;
 constexpr uint32_t kWaitLimit = 1u << 20;
 constexpr uint32_t kMagic = 0x43004300u;  // two bf16 128.0
 constexpr uint32_t kOnes = 0x3F803F80u;   // two bf16 1.0
+
+// Geometry of a work unit of 16 * NSUB rows (NSUB m16 subtiles per warp):
+// one 128-byte TMA box row per row, two boxes (512 codes) per stage, then
+// the stage's 8 scales and 8 biases per row; slots are kept 1 KB aligned
+// for the 128-byte swizzle.
+template <int NSUB>
+struct Geo {
+  static constexpr int kRows = 16 * NSUB;
+  static constexpr int kBox = kRows * 128;
+  static constexpr int kParam = kRows * 16;
+  static constexpr int kSlot = (2 * kBox + 2 * kParam + 1023) / 1024 * 1024;  // 9216 | 5120
+  static constexpr int kWarps = NSUB == 2 ? 4 : 8;  // warps per CTA of the persistent kernel
+};
 
 // ---- PTX wrappers -------------------------------------------------------------------
 
@@ -249,15 +266,17 @@ struct Maps {
 };
 
 // The weight part of a stage: codes (two boxes) and the 8 groups' scales and
-// biases of 32 rows from tensor_row, into slot memory dst; arms `bar` for
-// those bytes plus `mc` activation chunks still to come.
+// biases of 16 * NSUB rows from tensor_row, into slot memory dst; arms `bar`
+// for those bytes plus `mc` activation chunks still to come.
+template <int NSUB>
 __device__ __forceinline__ void issue_weights(uint32_t dst, uint32_t bar, const Maps* maps, int st, int tensor_row,
                                               int mc, uint64_t pol_stream, uint64_t pol_keep) {
-  mbar_expect_tx(bar, kCodeSlotBytes + (uint32_t)(mc * kStageK * 2));
+  using G = Geo<NSUB>;
+  mbar_expect_tx(bar, 2 * G::kBox + 2 * G::kParam + (uint32_t)(mc * kStageK * 2));
   tma_load_2d(dst, &maps->codes, st * kStageWords, tensor_row, bar, pol_stream);
-  tma_load_2d(dst + kBoxBytes, &maps->codes, st * kStageWords + kBoxWords, tensor_row, bar, pol_stream);
-  tma_load_2d(dst + kCodeBytes, &maps->scales, st * 8, tensor_row, bar, pol_keep);
-  tma_load_2d(dst + kCodeBytes + kParamBytes, &maps->biases, st * 8, tensor_row, bar, pol_keep);
+  tma_load_2d(dst + G::kBox, &maps->codes, st * kStageWords + kBoxWords, tensor_row, bar, pol_stream);
+  tma_load_2d(dst + 2 * G::kBox, &maps->scales, st * 8, tensor_row, bar, pol_keep);
+  tma_load_2d(dst + 2 * G::kBox + G::kParam, &maps->biases, st * 8, tensor_row, bar, pol_keep);
 }
 
 // The activation part of a stage: 512 bf16 of each row toks[0..mc) into rows
@@ -270,10 +289,11 @@ __device__ __forceinline__ void issue_x(uint32_t xdst, uint32_t bar, int st, con
 }
 
 // Lane 0 only: the weights of stage `st` into the next free slot; returns the slot.
+template <int NSUB>
 __device__ __forceinline__ uint32_t ring_issue_w(Ring& R, const Maps* maps, int st, int tensor_row, int mc) {
   const uint32_t slot = R.issued % (uint32_t)R.S;
-  issue_weights(R.codes0 + slot * kCodeSlotBytes, R.bars0 + 8 * slot, maps, st, tensor_row, mc, R.pol_stream,
-                R.pol_keep);
+  issue_weights<NSUB>(R.codes0 + slot * Geo<NSUB>::kSlot, R.bars0 + 8 * slot, maps, st, tensor_row, mc,
+                      R.pol_stream, R.pol_keep);
   ++R.issued;
   return slot;
 }
@@ -284,9 +304,10 @@ __device__ __forceinline__ void ring_issue_x(const Ring& R, uint32_t slot, int s
   issue_x(R.xs0 + slot * R.x_slot, R.bars0 + 8 * slot, st, x, toks, mc, K, R.pol_keep);
 }
 
+template <int NSUB>
 __device__ __forceinline__ void ring_issue(Ring& R, const Maps* maps, int st, int tensor_row, const uint16_t* x,
                                            const int* toks, int mc, int K) {
-  const uint32_t slot = ring_issue_w(R, maps, st, tensor_row, mc);
+  const uint32_t slot = ring_issue_w<NSUB>(R, maps, st, tensor_row, mc);
   ring_issue_x(R, slot, st, x, toks, mc, K);
 }
 
@@ -460,8 +481,9 @@ __host__ __device__ inline Shape tc_shape(int N, int K) {
   return s;
 }
 
+template <int NSUB>
 __host__ __device__ inline int ring_bytes(int stages, int mcap) {
-  return stages * (kCodeSlotBytes + mcap * kXPitch);
+  return stages * (Geo<NSUB>::kSlot + mcap * kXPitch);
 }
 
 // ---- persistent kernel (w4a16_mm) ------------------------------------------------------
@@ -471,11 +493,11 @@ struct StreamParams {
   const uint16_t* S;
   const uint16_t* B;
   uint16_t* y;
-  float* part;      // [units][8][32] slice partials (ksplit > 1)
+  float* part;      // [units][8][rows] slice partials (ksplit > 1)
   int* cnt;         // [tiles] arrival counters, zero between launches
   int* flags;
   int N, K, M, row0;
-  int nst, sl, ks, tiles, units;
+  int nst, sl, ks, tiles, units;  // tiles and units of 16 * NSUB rows
   int stages;
   int xpitch;       // bytes per activation row of the pre-staged copy (0: per-stage copies)
   int prefetch;     // request the first weight stages before waiting for earlier kernels
@@ -511,9 +533,17 @@ struct UnitCursor {
   }
 };
 
-template <bool ALLCOLS, bool XSTAGED>
-__global__ void __launch_bounds__(kStreamWarps * 32, W4A16_TC_MIN_BLOCKS) tc_stream_kernel(
+// Persistent CTAs of Geo<NSUB>::kWarps warps; a warp's work unit is
+// 16 * NSUB rows x one K-slice.  With NSUB = 1 a warp needs half the
+// registers and shared memory, so twice as many warps fit on an SM.
+template <int NSUB>
+constexpr int stream_min_blocks() { return NSUB == 2 ? W4A16_TC_MIN_BLOCKS : 2; }
+
+template <int NSUB, bool ALLCOLS, bool XSTAGED>
+__global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB>()) tc_stream_kernel(
     const __grid_constant__ Maps maps, StreamParams p) {
+  using G = Geo<NSUB>;
+  constexpr int kW = G::kWarps, kRows = G::kRows;
   extern __shared__ uint8_t smem_raw[];
   pdl_launch_dependents();
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -528,12 +558,12 @@ __global__ void __launch_bounds__(kStreamWarps * 32, W4A16_TC_MIN_BLOCKS) tc_str
   Ring R;
   R.S = S;
   R.x_slot = x_slot;
-  R.codes0 = smem_u32(base) + (uint32_t)(warp * S * kCodeSlotBytes);
-  R.xs0 = smem_u32(base) + (uint32_t)(kStreamWarps * S * kCodeSlotBytes + warp * S * x_slot);
-  const uint32_t bar_off = (uint32_t)(kStreamWarps * ring_bytes(S, xring));
+  R.codes0 = smem_u32(base) + (uint32_t)(warp * S * G::kSlot);
+  R.xs0 = smem_u32(base) + (uint32_t)(kW * S * G::kSlot + warp * S * x_slot);
+  const uint32_t bar_off = (uint32_t)(kW * ring_bytes<NSUB>(S, xring));
   R.bars0 = smem_u32(base) + bar_off + (uint32_t)(warp * S * 8);
-  int* s_tok = reinterpret_cast<int*>(base + bar_off + kStreamWarps * S * 8);
-  const uint32_t xst = smem_u32(base) + bar_off + (uint32_t)(kStreamWarps * S * 8 + 64);  // 16-byte aligned
+  int* s_tok = reinterpret_cast<int*>(base + bar_off + kW * S * 8);
+  const uint32_t xst = smem_u32(base) + bar_off + (uint32_t)(kW * S * 8 + 64);  // 16-byte aligned
   const uint32_t sxs = xst + (uint32_t)(mc * p.xpitch);
   R.issued = R.consumed = 0;
   R.pol_stream = policy_evict_first();
@@ -547,7 +577,7 @@ __global__ void __launch_bounds__(kStreamWarps * 32, W4A16_TC_MIN_BLOCKS) tc_str
 
   // warp-major numbering: every pass over the units spreads them evenly over CTAs
   const int gw = warp * gridDim.x + blockIdx.x;
-  const int TW = gridDim.x * kStreamWarps;
+  const int TW = gridDim.x * kW;
   const int tw_tiles = TW / p.ks, tw_slices = TW - tw_tiles * p.ks;
 
   // issue cursor (lane 0): unit, stage, end of the unit's stages
@@ -564,7 +594,7 @@ __global__ void __launch_bounds__(kStreamWarps * 32, W4A16_TC_MIN_BLOCKS) tc_str
   };
   auto issue_next = [&](bool with_x) {
     if (ic.u >= p.units) return;
-    const uint32_t slot = ring_issue_w(R, &maps, ist, ic.tile * kTileRows, xring);
+    const uint32_t slot = ring_issue_w<NSUB>(R, &maps, ist, ic.tile * kRows, xring);
     if (with_x) ring_issue_x(R, slot, ist, p.x, s_tok, xring, p.K);
     step(ic, ist, iend);
   };
@@ -605,12 +635,12 @@ __global__ void __launch_bounds__(kStreamWarps * 32, W4A16_TC_MIN_BLOCKS) tc_str
       sts128(xst + n * p.xpitch + 16 * wd, make_uint4(b[0][0], b[0][1], b[1][0], b[1][1]));
     }
     __syncthreads();
-    for (int G = warp; G < p.K / kGroup; G += kStreamWarps) {
+    for (int gi = warp; gi < p.K / kGroup; gi += kW) {
       uint32_t b[2][2][2];
 #pragma unroll
       for (int cb = 0; cb < 2; ++cb) {
         uint4 u = make_uint4(0, 0, 0, 0);
-        if (g < mc) u = lds128(xst + g * p.xpitch + 128 * G + 64 * cb + 16 * t);
+        if (g < mc) u = lds128(xst + g * p.xpitch + 128 * gi + 64 * cb + 16 * t);
         b[cb][0][0] = u.x;
         b[cb][0][1] = u.y;
         b[cb][1][0] = u.z;
@@ -621,7 +651,7 @@ __global__ void __launch_bounds__(kStreamWarps * 32, W4A16_TC_MIN_BLOCKS) tc_str
       for (int step = 0; step < 4; ++step) mma_bf16(v, kOnes, kOnes, kOnes, kOnes, b[step >> 1][step & 1][0],
                                                     b[step >> 1][step & 1][1]);
       if (g == 0 && 2 * t < mc) {
-        asm volatile("st.shared.v2.f32 [%0], {%1,%2};" ::"r"(sxs + (G * sx_cols(mc) + 2 * t) * 4), "f"(v[0]),
+        asm volatile("st.shared.v2.f32 [%0], {%1,%2};" ::"r"(sxs + (gi * sx_cols(mc) + 2 * t) * 4), "f"(v[0]),
                      "f"(v[1])
                      : "memory");
       }
@@ -630,11 +660,17 @@ __global__ void __launch_bounds__(kStreamWarps * 32, W4A16_TC_MIN_BLOCKS) tc_str
   }
   if (gw >= p.units) return;
 
-  uint32_t loff[2][4];
-  ldsm_offsets(lane, loff);
+  uint32_t loff2[2][4];
+  ldsm_offsets(lane, loff2);
+  uint32_t loff[NSUB][4];
+#pragma unroll
+  for (int s = 0; s < NSUB; ++s)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) loff[s][i] = loff2[s][i];
 
   bool timed_out = false;
-  int pend_tile = -1, pend_old = 0;
+  int pend_tile = -1;               // partials stored, arrival not yet counted
+  int cnt_tile = -1, cnt_old = 0;   // arrival counted (lane 0 holds the old count)
 
   auto reduce_tile = [&](int tile) {
     // Sum the ksplit partials of a finished tile in slice order.  Lane 0's
@@ -643,14 +679,16 @@ __global__ void __launch_bounds__(kStreamWarps * 32, W4A16_TC_MIN_BLOCKS) tc_str
     // eight slices at a time; the additions stay in slice order.
     if (lane == 0) __threadfence();
     __syncwarp();
-    const int row = tile * kTileRows + lane;
-    for (int n = 0; n < mc; ++n) {
-      const float* q = p.part + ((int64_t)tile * p.ks * 8 + n) * 32 + lane;
+    // lane = (column n0, row r): with 16 rows two columns at a time
+    const int r = lane % kRows, n0 = lane / kRows;
+    const int row = tile * kRows + r;
+    for (int n = n0; n < mc; n += 32 / kRows) {
+      const float* q = p.part + ((int64_t)tile * p.ks * 8 + n) * kRows + r;
       float sum = 0.0f;
       for (int s0 = 0; s0 < p.ks; s0 += 8) {
         float v[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = (s0 + j < p.ks) ? __ldcg(q + (int64_t)(s0 + j) * 8 * 32) : 0.0f;
+        for (int j = 0; j < 8; ++j) v[j] = (s0 + j < p.ks) ? __ldcg(q + (int64_t)(s0 + j) * 8 * kRows) : 0.0f;
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           if (s0 + j < p.ks) sum = (s0 + j == 0) ? v[0] : __fadd_rn(sum, v[j]);
@@ -660,9 +698,20 @@ __global__ void __launch_bounds__(kStreamWarps * 32, W4A16_TC_MIN_BLOCKS) tc_str
     if (lane == 0) p.cnt[tile] = 0;
   };
 
-  auto rows_of = [&](int tile, int (&pr)[4]) {
+  // Count the arrival of this warp's stored partials of `tile`: a warp
+  // barrier, then one release fence by lane 0 before its atomic.
+  auto count_arrival = [&](int tile) {
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence();
+      cnt_old = atomicAdd(p.cnt + tile, 1);
+    }
+    cnt_tile = tile;
+  };
+
+  auto rows_of = [&](int tile, int (&pr)[2 * NSUB]) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) pr[i] = tile * kTileRows + 16 * (i >> 1) + g + 8 * (i & 1);
+    for (int i = 0; i < 2 * NSUB; ++i) pr[i] = tile * kRows + 16 * (i >> 1) + g + 8 * (i & 1);
   };
 
   // consume cursor
@@ -672,12 +721,12 @@ __global__ void __launch_bounds__(kStreamWarps * 32, W4A16_TC_MIN_BLOCKS) tc_str
   for (; cc.u < p.units && !timed_out;) {
     const int tile = cc.tile;
     const int s0 = cc.slice * p.sl, s1 = min(s0 + p.sl, p.nst);
-    int prow[4];
+    int prow[2 * NSUB];
     rows_of(tile, prow);
 
-    float acc[2][4];
+    float acc[NSUB][4];
 #pragma unroll
-    for (int s = 0; s < 2; ++s)
+    for (int s = 0; s < NSUB; ++s)
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[s][i] = 0.0f;
 
@@ -687,7 +736,7 @@ __global__ void __launch_bounds__(kStreamWarps * 32, W4A16_TC_MIN_BLOCKS) tc_str
         timed_out = true;
         break;
       }
-      const uint32_t cbase = ordered(R.codes0 + slot * kCodeSlotBytes);
+      const uint32_t cbase = ordered(R.codes0 + slot * G::kSlot);
       uint32_t xbase, sxbase = 0;
       if (XSTAGED) {
         xbase = xst + g * p.xpitch + 16 * t + st * (kStageK * 2);
@@ -695,7 +744,7 @@ __global__ void __launch_bounds__(kStreamWarps * 32, W4A16_TC_MIN_BLOCKS) tc_str
       } else {
         xbase = ordered(R.xs0 + slot * x_slot + g * kXPitch + 16 * t);
       }
-      compute_stage<2, ALLCOLS, XSTAGED>(cbase, xbase, g < mc, sxbase, sx_cols(mc) * 4, 2 * t < mc, acc, loff, g);
+      compute_stage<NSUB, ALLCOLS, XSTAGED>(cbase, xbase, g < mc, sxbase, sx_cols(mc) * 4, 2 * t < mc, acc, loff, g);
       ++R.consumed;
       __syncwarp();
       if (lane == 0) {
@@ -705,15 +754,22 @@ __global__ void __launch_bounds__(kStreamWarps * 32, W4A16_TC_MIN_BLOCKS) tc_str
     }
     if (timed_out) break;
 
-    // the previous unit's arrival count has had a whole unit to come back
+    // Split-K arrivals run two units behind the stores: the arrival counted
+    // one unit ago has had a whole unit to come back, and the partials
+    // stored one unit ago have had a whole unit to land, so neither the
+    // fence nor the atomic stalls the warp.
+    if (cnt_tile >= 0) {
+      const int old = __shfl_sync(0xffffffffu, cnt_old, 0);
+      if (old == p.ks - 1) reduce_tile(cnt_tile);
+      cnt_tile = -1;
+    }
     if (pend_tile >= 0) {
-      const int old = __shfl_sync(0xffffffffu, pend_old, 0);
-      if (old == p.ks - 1) reduce_tile(pend_tile);
+      count_arrival(pend_tile);
       pend_tile = -1;
     }
     if (p.ks == 1) {
 #pragma unroll
-      for (int s = 0; s < 2; ++s)
+      for (int s = 0; s < NSUB; ++s)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int row = prow[2 * s + (i >> 1)];
@@ -721,28 +777,29 @@ __global__ void __launch_bounds__(kStreamWarps * 32, W4A16_TC_MIN_BLOCKS) tc_str
           if (n < mc && row < p.N) p.y[(int64_t)s_tok[n] * p.N + row] = f32_to_bf16_bits(acc[s][i]);
         }
     } else {
-      float* q = p.part + (int64_t)cc.u * 8 * 32;
+      float* q = p.part + (int64_t)cc.u * 8 * kRows;
 #pragma unroll
-      for (int s = 0; s < 2; ++s)
+      for (int s = 0; s < NSUB; ++s)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int r = 16 * s + g + 8 * (i >> 1);
           const int n = 2 * t + (i & 1);
-          if (n < mc) __stcg(q + n * 32 + r, acc[s][i]);
+          if (n < mc) __stcg(q + n * kRows + r, acc[s][i]);
         }
-      // warp barrier, then one release fence by lane 0 before it counts the arrival
-      __syncwarp();
-      if (lane == 0) {
-        __threadfence();
-        pend_old = atomicAdd(p.cnt + tile, 1);
-      }
       pend_tile = tile;
     }
     cc.advance(TW, tw_tiles, tw_slices, p.ks);
   }
-  if (!timed_out && pend_tile >= 0) {
-    const int old = __shfl_sync(0xffffffffu, pend_old, 0);
-    if (old == p.ks - 1) reduce_tile(pend_tile);
+  if (!timed_out) {
+    if (cnt_tile >= 0) {
+      const int old = __shfl_sync(0xffffffffu, cnt_old, 0);
+      if (old == p.ks - 1) reduce_tile(cnt_tile);
+    }
+    if (pend_tile >= 0) {
+      count_arrival(pend_tile);
+      const int old = __shfl_sync(0xffffffffu, cnt_old, 0);
+      if (old == p.ks - 1) reduce_tile(cnt_tile);
+    }
   }
   if (timed_out) {
     if (lane == 0) atomicOr(p.flags, W4A16_DEVICE_TIMEOUT);
@@ -766,10 +823,8 @@ __global__ void __launch_bounds__(kStreamWarps * 32, W4A16_TC_MIN_BLOCKS) tc_str
 // the same canonical arithmetic as the persistent kernel, with no workspace,
 // atomics or global fences.
 
-constexpr int kTile16 = 16;
-constexpr int kBox16 = kTile16 * 128;    // one 128-byte box row for 16 rows
-constexpr int kParam16 = kTile16 * 16;   // 8 bf16 per row
-constexpr int kSlot16 = 5 * 1024;        // codes 2 x 2 KB | scales 256 | biases 256 | pad (1 KB alignment)
+constexpr int kTile16 = Geo<1>::kRows;
+constexpr int kSlot16 = Geo<1>::kSlot;   // codes 2 x 2 KB | scales 256 | biases 256 | pad (1 KB alignment)
 constexpr int kTileMaxWarps = 16;
 constexpr int kMaxCluster = 8;
 
@@ -811,10 +866,9 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
 
 template <bool ALLCOLS>
 // The bound of 768 threads caps registers at 80, so that five CTAs of five
-// warps fit on an SM.
+// warps fit on an SM (by registers).
 __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Maps maps, TileParams p) {
   extern __shared__ uint8_t smem_raw[];
-  pdl_launch_dependents();
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, W = blockDim.x >> 5;
   const int g = lane >> 2, t = lane & 3;
@@ -842,18 +896,16 @@ __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Ma
 
   // lane 0 of warp w requests local stages w, w + W, ...
   auto weights = [&](int i) {
-    const int st = st0 + i;
-    const uint32_t dst = codes0 + i * kSlot16, bar = bars0 + 8 * i;
-    const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_last();
-    mbar_expect_tx(bar, 2 * kBox16 + 2 * kParam16 + (uint32_t)(mc * kStageK * 2));
-    tma_load_2d(dst, &maps.codes, st * kStageWords, tensor_row, bar, pol_stream);
-    tma_load_2d(dst + kBox16, &maps.codes, st * kStageWords + kBoxWords, tensor_row, bar, pol_stream);
-    tma_load_2d(dst + 2 * kBox16, &maps.scales, st * 8, tensor_row, bar, pol_keep);
-    tma_load_2d(dst + 2 * kBox16 + kParam16, &maps.biases, st * 8, tensor_row, bar, pol_keep);
+    issue_weights<1>(codes0 + i * kSlot16, bars0 + 8 * i, &maps, st0 + i, tensor_row, mc, policy_evict_first(),
+                     policy_evict_last());
   };
   if (lane == 0 && p.prefetch)
     for (int i = warp; i < nloc; i += W) weights(i);
   pdl_wait();
+  // Only now let the next kernel launch: its CTAs then fetch their weights
+  // while this one computes, and at most one kernel waits ahead (CTAs
+  // launched further ahead would only hold SM resources and slow this one).
+  pdl_launch_dependents();
   if (lane == 0)
     for (int i = warp; i < nloc; i += W) {
       if (!p.prefetch) weights(i);
@@ -933,7 +985,7 @@ struct RoutedParams {
 };
 
 __host__ __device__ inline int routed_smem(int warps, int stages, int ks) {
-  return warps * ring_bytes(stages, kMaxChunk) + warps * stages * 8 + ks * kTileRows * 8 * 4 + 16 * 4 + 1024;
+  return warps * ring_bytes<2>(stages, kMaxChunk) + warps * stages * 8 + ks * kTileRows * 8 * 4 + 16 * 4 + 1024;
 }
 
 __global__ void __launch_bounds__(kRoutedWarps * 32) tc_routed_kernel(const __grid_constant__ Maps maps,
@@ -953,7 +1005,7 @@ __global__ void __launch_bounds__(kRoutedWarps * 32) tc_routed_kernel(const __gr
   R.x_slot = x_slot;
   R.codes0 = smem_u32(base) + (uint32_t)(warp * S * kCodeSlotBytes);
   R.xs0 = smem_u32(base) + (uint32_t)(W * S * kCodeSlotBytes + warp * S * x_slot);
-  const uint32_t bar_off = (uint32_t)(W * ring_bytes(S, kMaxChunk));
+  const uint32_t bar_off = (uint32_t)(W * ring_bytes<2>(S, kMaxChunk));
   R.bars0 = smem_u32(base) + bar_off + (uint32_t)(warp * S * 8);
   float* red = reinterpret_cast<float*>(base + bar_off + W * S * 8);  // [ks][32 rows][8 columns]
   int* s_tok = reinterpret_cast<int*>(red + p.ks * kTileRows * 8);
@@ -986,7 +1038,7 @@ __global__ void __launch_bounds__(kRoutedWarps * 32) tc_routed_kernel(const __gr
     int isl = warp, ist = warp * p.sl;  // issue cursor
     auto issue_next = [&]() {
       if (isl >= p.ks) return;
-      ring_issue(R, &maps, ist, tensor_row, p.x, s_tok, mc, p.K);
+      ring_issue<2>(R, &maps, ist, tensor_row, p.x, s_tok, mc, p.K);
       if (++ist == slice_end(isl)) {
         isl += W;
         ist = isl * p.sl;
@@ -1121,37 +1173,56 @@ cudaError_t make_maps(Maps* m, const uint32_t* Wq, const uint16_t* S, const uint
   return make_param_map(&m->biases, B, rows, K, box_rows);
 }
 
+template <int NSUB>
 int stream_smem(int stages, int mc) {
-  return kStreamWarps * ring_bytes(stages, mc) + kStreamWarps * stages * 8 + 64 + 1024;
+  using G = Geo<NSUB>;
+  return G::kWarps * ring_bytes<NSUB>(stages, mc) + G::kWarps * stages * 8 + 64 + 1024;
 }
 
+// Per-CTA shared-memory budget of the persistent kernel: the measured best
+// for 32-row warps; two CTAs per SM for 16-row warps.
+constexpr int kHalfSm = 228 * 1024 / 2 - 1024;  // per-CTA budget for two CTAs per SM (1 KB reserved each)
+template <int NSUB>
+constexpr int stream_smem_target() { return NSUB == 2 ? W4A16_TC_SMEM_TARGET : kHalfSm; }
+
 // Deepest ring (up to W4A16_TC_MAX_STAGES, at least 2 stages per warp) that
-// keeps a CTA's shared memory under W4A16_TC_SMEM_TARGET.
+// keeps a CTA's shared memory under the budget.
+template <int NSUB>
 int stream_stages(int mc) {
   for (int s = W4A16_TC_MAX_STAGES; s > 2; --s)
-    if (stream_smem(s, mc) <= W4A16_TC_SMEM_TARGET) return s;
+    if (stream_smem<NSUB>(s, mc) <= stream_smem_target<NSUB>()) return s;
   return 2;
 }
 
 struct DeviceInfo {
   int sms = 152;
-  bool attr_set[7] = {};  // stream<cols, staged> x4, routed, tile<one column>, tile<all columns>
+  std::set<const void*> attr_done;  // kernels whose shared-memory limit is raised
 };
+
+// Raise a kernel's dynamic shared-memory limit once per device.
+template <typename Kern>
+cudaError_t allow_smem(Kern fn, DeviceInfo& d) {
+  const void* key = reinterpret_cast<const void*>(fn);
+  if (d.attr_done.count(key)) return cudaSuccess;
+  if (cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit)) return e;
+  d.attr_done.insert(key);
+  return cudaSuccess;
+}
 
 // The activations are pre-staged (once per CTA) when the CTA, with a
 // two-stage ring per warp, still fits twice on an SM; otherwise every stage
-// carries its own activation chunk.
-constexpr int kHalfSm = 228 * 1024 / 2 - 1024;  // per-CTA budget for two CTAs per SM (1 KB reserved each)
-
-// Staging costs each CTA a prologue (copy + group sums over all of K); it
-// pays off when every warp has several work units to amortise it over.
+// carries its own activation chunk.  Staging costs each CTA a prologue (copy
+// + group sums over all of K); it pays off when every warp has several work
+// units to amortise it over.
+template <int NSUB>
 bool stage_activations(int M, int K, int units, int sms) {
-  return units >= 2 * kStreamWarps * 2 * sms && stream_smem(2, 0) + xstage_bytes(M, K) <= kHalfSm;
+  return units >= 2 * Geo<NSUB>::kWarps * 2 * sms && stream_smem<NSUB>(2, 0) + xstage_bytes(M, K) <= kHalfSm;
 }
 
+template <int NSUB>
 int staged_stages(int M, int K) {
   for (int s = W4A16_TC_MAX_STAGES; s > 2; --s)
-    if (stream_smem(s, 0) + xstage_bytes(M, K) <= kHalfSm) return s;
+    if (stream_smem<NSUB>(s, 0) + xstage_bytes(M, K) <= kHalfSm) return s;
   return 2;
 }
 
@@ -1186,41 +1257,45 @@ cudaError_t launch_ex(Kern fn, dim3 grid, dim3 block, int smem, cudaStream_t str
   return cudaLaunchKernelEx(&cfg, fn, maps, p);
 }
 
-template <bool A, bool X>
+template <int NSUB, bool A, bool X>
 cudaError_t stream_launch_t(const Maps& map, const StreamParams& p, int sms, int smem, DeviceInfo& d,
                             cudaStream_t stream, bool pdl) {
-  auto* fn = tc_stream_kernel<A, X>;
-  const int idx = (A ? 1 : 0) + (X ? 2 : 0);
-  if (!d.attr_set[idx]) {
-    if (cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit)) return e;
-    d.attr_set[idx] = true;
-  }
+  constexpr int kW = Geo<NSUB>::kWarps;
+  auto* fn = tc_stream_kernel<NSUB, A, X>;
+  if (cudaError_t e = allow_smem(fn, d)) return e;
   int per_sm = 0;
-  if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kStreamWarps * 32, smem)) return e;
+  if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kW * 32, smem)) return e;
   if (per_sm < 1) per_sm = 1;
   int grid = sms * per_sm;
-  const int need = (p.units + kStreamWarps - 1) / kStreamWarps;
+  const int need = (p.units + kW - 1) / kW;
   if (grid > need) grid = need;
-  return launch_ex(fn, dim3(grid), dim3(kStreamWarps * 32), smem, stream, pdl, map, p);
+  return launch_ex(fn, dim3(grid), dim3(kW * 32), smem, stream, pdl, map, p);
 }
 
 // Persistent grid for one chunk: every SM filled to its occupancy, never more
-// CTAs than there are groups of four work units.  The caller holds g_dev_mu.
-cudaError_t launch_stream(const Maps& map, StreamParams p, int sms, DeviceInfo& d, cudaStream_t stream, int pdl) {
+// CTAs than there are groups of kWarps work units.  p.tiles / p.units count
+// 16 * NSUB-row tiles.  The caller holds g_dev_mu.
+template <int NSUB>
+cudaError_t launch_stream_t(const Maps& map, StreamParams p, int sms, DeviceInfo& d, cudaStream_t stream, int pdl) {
   const bool allcols = p.M > 1;
-  const bool staged = stage_activations(p.M, p.K, p.units, sms);
+  const bool staged = stage_activations<NSUB>(p.M, p.K, p.units, sms);
   p.xpitch = staged ? 2 * p.K + 64 : 0;
-  p.stages = staged ? staged_stages(p.M, p.K) : stream_stages(p.M);
+  p.stages = staged ? staged_stages<NSUB>(p.M, p.K) : stream_stages<NSUB>(p.M);
   p.prefetch = pdl >= 2;
-  int smem = stream_smem(p.stages, staged ? 0 : p.M);
+  int smem = stream_smem<NSUB>(p.stages, staged ? 0 : p.M);
   if (staged) smem += xstage_bytes(p.M, p.K);
   const bool on = pdl > 0;
   if (allcols)
-    return staged ? stream_launch_t<true, true>(map, p, sms, smem, d, stream, on)
-                  : stream_launch_t<true, false>(map, p, sms, smem, d, stream, on);
-  return staged ? stream_launch_t<false, true>(map, p, sms, smem, d, stream, on)
-                : stream_launch_t<false, false>(map, p, sms, smem, d, stream, on);
+    return staged ? stream_launch_t<NSUB, true, true>(map, p, sms, smem, d, stream, on)
+                  : stream_launch_t<NSUB, true, false>(map, p, sms, smem, d, stream, on);
+  return staged ? stream_launch_t<NSUB, false, true>(map, p, sms, smem, d, stream, on)
+                : stream_launch_t<NSUB, false, false>(map, p, sms, smem, d, stream, on);
 }
+
+// Row subtiles per warp of the persistent kernel for a chunk of M rows: at
+// M = 1 32-row warps stream faster (measured); with more activation rows
+// 16-row warps, twice as many per SM, do.
+int stream_nsub(int M) { return M >= W4A16_TC_STREAM_NSUB1_MIN_M ? 1 : 2; }
 
 // Launch shape of the tile kernel for one chunk of M rows.
 struct TilePlan {
@@ -1231,40 +1306,13 @@ struct TilePlan {
   int ctas = 0;   // grid size
 };
 
-// Registers per thread of the tile kernel as compiled (rounded up to the
-// allocation unit of 8), read once from the runtime; the assumed value
-// without a GPU.
-int tile_regs() {
-  static int regs = [] {
-    int r = W4A16_TC_TILE_REGS;
-    cudaFuncAttributes fa0, fa1;
-    if (cudaFuncGetAttributes(&fa0, tc_tile_kernel<false>) == cudaSuccess &&
-        cudaFuncGetAttributes(&fa1, tc_tile_kernel<true>) == cudaSuccess)
-      r = max(fa0.numRegs, fa1.numRegs);
-    else
-      cudaGetLastError();
-    return (r + 7) & ~7;
-  }();
-  return regs;
-}
-
-// CTAs of `threads` threads and `smem` bytes of shared memory that fit on one SM.
-int tile_ctas_per_sm(int threads, int smem) {
-  int per_sm = (228 * 1024) / (smem + 1024);
-  const int by_regs = 65536 / (threads * tile_regs());
-  const int by_warps = 64 / (threads / 32);
-  if (by_regs < per_sm) per_sm = by_regs;
-  if (by_warps < per_sm) per_sm = by_warps;
-  return per_sm < 32 ? per_sm : 32;
-}
-
 // The tile kernel serves shapes whose canonical slices are single stages (a
-// persistent grid would give each warp about one unit).  A tile's slices are
-// dealt to clusters of kc CTAs with at most W4A16_TC_TILE_SLICES each; kc
-// grows (up to 8) until every CTA fits in shared memory and all of them fit
-// on the GPU at once.  `force` drops the last condition (the CTAs then run
-// in waves).
-TilePlan tile_plan(const Shape& s, int N, int M, int sms, bool force) {
+// persistent grid would give each warp about one unit); measured faster
+// there at every M even when its CTAs run in several waves, and slower on
+// larger shapes.  A tile's slices are dealt to clusters of kc CTAs with at
+// most W4A16_TC_TILE_SLICES each; kc grows (up to 8) until a CTA fits in
+// shared memory.  `force` drops the size condition.
+TilePlan tile_plan(const Shape& s, int N, int M, bool force) {
   TilePlan tp;
   if (!force && s.nst * s.tiles > W4A16_TC_TILE_MAX_UNITS) return tp;
   const int tiles16 = cdiv(N, kTile16);
@@ -1274,16 +1322,12 @@ TilePlan tile_plan(const Shape& s, int N, int M, int sms, bool force) {
     const int nloc = ksl * s.sl;
     const int smem = tile_smem(nloc, M, s.ks);
     if (smem > kSmemLimit) continue;
-    const int warps = ksl < kTileMaxWarps ? ksl : kTileMaxWarps;
-    const int ctas = tiles16 * kc;
-    if (force || ctas <= tile_ctas_per_sm(warps * 32, smem) * sms) {
-      tp.kc = kc;
-      tp.nloc = nloc;
-      tp.warps = warps;
-      tp.smem = smem;
-      tp.ctas = ctas;
-      return tp;
-    }
+    tp.kc = kc;
+    tp.nloc = nloc;
+    tp.warps = ksl < kTileMaxWarps ? ksl : kTileMaxWarps;
+    tp.smem = smem;
+    tp.ctas = tiles16 * kc;
+    return tp;
   }
   return tp;
 }
@@ -1300,11 +1344,7 @@ cudaError_t launch_tile(const LaunchArgs& a, const Shape& s, const TilePlan& tp,
   p.prefetch = a.pdl >= 2;
   const bool allcols = a.M > 1;
   auto* fn = allcols ? tc_tile_kernel<true> : tc_tile_kernel<false>;
-  const int idx = allcols ? 6 : 5;
-  if (!d.attr_set[idx]) {
-    if (cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit)) return e;
-    d.attr_set[idx] = true;
-  }
+  if (cudaError_t e = allow_smem(fn, d)) return e;
   return launch_ex(fn, dim3(tp.ctas), dim3(tp.warps * 32), tp.smem, a.stream, a.pdl > 0, maps, p, tp.kc);
 }
 
@@ -1323,14 +1363,43 @@ DeviceInfo& device_info(int dev) {
 }
 
 // Workspace of one (device, stream), fixed layout:
-//   [kWsTiles] int arrival counters (zero between launches) | [kWsUnits][8][32] fp32 slice partials.
-// ksplit > 1 only happens when a chunk has fewer than kTargetUnits row tiles,
-// and then it never has more than kWsUnits work units (checked at launch), so
-// one fixed-size buffer serves every shape and never needs to grow.
-constexpr int kWsTiles = 4096;
-constexpr int kWsUnits = 4864;
+//   [kWsTiles] int arrival counters (zero between launches) | fp32 slice
+//   partials [units][8][rows] (rows = 16 or 32 per unit).
+// ksplit > 1 only happens when a chunk has fewer than kTargetUnits 32-row
+// tiles, and then (from the slicing rule of tc_shape) it has fewer than
+// 2 kTargetUnits 32-row units: twice as many 16-row ones, the same bytes.
+// One fixed-size buffer serves every shape and never needs to grow; the
+// launch checks it all the same.
+constexpr int kWsTiles = 8192;
 constexpr size_t kWsCounterBytes = (size_t)kWsTiles * 4;
-constexpr size_t kWsBytes = kWsCounterBytes + (size_t)kWsUnits * 8 * 32 * 4;
+constexpr size_t kWsPartBytes = (size_t)2 * kTargetUnits * 8 * 32 * 4;
+constexpr size_t kWsBytes = kWsCounterBytes + kWsPartBytes;
+
+// Work decomposition of the persistent kernel for a chunk of M rows.
+struct StreamWork {
+  int nsub, rows, tiles, units;
+};
+
+StreamWork stream_work(const Shape& s, int N, int M) {
+  StreamWork w;
+  w.nsub = stream_nsub(M);
+  w.rows = 16 * w.nsub;
+  w.tiles = cdiv(N, w.rows);
+  w.units = w.tiles * s.ks;
+  return w;
+}
+
+bool workspace_fits(const Shape& s, const StreamWork& w) {
+  return s.ks == 1 || (w.tiles <= kWsTiles && (size_t)w.units * 8 * w.rows * 4 <= kWsPartBytes);
+}
+
+cudaError_t launch_stream(const Maps& maps, StreamParams p, const StreamWork& w, DeviceInfo& d,
+                          cudaStream_t stream, int pdl) {
+  p.tiles = w.tiles;
+  p.units = w.units;
+  return w.nsub == 1 ? launch_stream_t<1>(maps, p, d.sms, d, stream, pdl)
+                     : launch_stream_t<2>(maps, p, d.sms, d, stream, pdl);
+}
 
 struct Workspace {
   void* ptr = nullptr;
@@ -1364,7 +1433,7 @@ bool tc_supported(int N, int K) {
   return K % kStageK == 0;
 }
 
-bool tc_tile_fits(int N, int K, int M) { return tile_plan(tc_shape(N, K), N, M, 152, true).kc > 0; }
+bool tc_tile_fits(int N, int K, int M) { return tile_plan(tc_shape(N, K), N, M, true).kc > 0; }
 
 void plan_tc(int N, int K, int tc_path, w4a16_plan* p) {
   const Shape s = tc_shape(N, K);
@@ -1381,7 +1450,7 @@ void plan_tc(int N, int K, int tc_path, w4a16_plan* p) {
   p->rows_per_tile = kTileRows;
   p->units = s.units;
   p->kernel = tc_path == 1 ? W4A16_KERNEL_TC_STREAM : tc_path == 2 ? W4A16_KERNEL_TC_TILE : W4A16_KERNEL_TC;
-  const TilePlan tp = tc_path == 1 ? TilePlan() : tile_plan(s, N, 1, sms, tc_path == 2);
+  const TilePlan tp = tc_path == 1 ? TilePlan() : tile_plan(s, N, 1, tc_path == 2);
   if (tp.kc > 0) {  // clusters of kc CTAs per 16-row tile
     p->rows_per_tile = kTile16;
     p->threads = tp.warps * 32;
@@ -1389,13 +1458,24 @@ void plan_tc(int N, int K, int tc_path, w4a16_plan* p) {
     p->smem_bytes = tp.smem;
     return;
   }
-  const bool staged = stage_activations(1, K, s.units, sms);
-  const int smem = staged ? stream_smem(staged_stages(1, K), 0) + xstage_bytes(1, K) : stream_smem(stream_stages(1), 1);
+  const StreamWork w = stream_work(s, N, 1);
+  int smem, warps;
+  if (w.nsub == 1) {
+    const bool staged = stage_activations<1>(1, K, w.units, sms);
+    smem = staged ? stream_smem<1>(staged_stages<1>(1, K), 0) + xstage_bytes(1, K) : stream_smem<1>(stream_stages<1>(1), 1);
+    warps = Geo<1>::kWarps;
+  } else {
+    const bool staged = stage_activations<2>(1, K, w.units, sms);
+    smem = staged ? stream_smem<2>(staged_stages<2>(1, K), 0) + xstage_bytes(1, K) : stream_smem<2>(stream_stages<2>(1), 1);
+    warps = Geo<2>::kWarps;
+  }
   const int per_sm = kSmemLimit / smem > 0 ? kSmemLimit / smem : 1;
   int grid = sms * per_sm;
-  const int need = (s.units + kStreamWarps - 1) / kStreamWarps;
+  const int need = (w.units + warps - 1) / warps;
   if (grid > need) grid = need;
-  p->threads = kStreamWarps * 32;
+  p->rows_per_tile = w.rows;
+  p->units = w.units;
+  p->threads = warps * 32;
   p->grid_x = grid;
   p->smem_bytes = smem;
 }
@@ -1416,20 +1496,21 @@ cudaError_t launch_tc(const LaunchArgs& a, const w4a16_plan& plan) {
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DeviceInfo& d = device_info(dev);
   if (a.tc_path != 1) {
-    const TilePlan tp = tile_plan(s, a.N, a.M, d.sms, a.tc_path == 2);
+    const TilePlan tp = tile_plan(s, a.N, a.M, a.tc_path == 2);
     if (tp.kc > 0) return launch_tile(a, s, tp, d);
     if (a.tc_path == 2) return cudaErrorInvalidConfiguration;
   }
+  const StreamWork w = stream_work(s, a.N, a.M);
   Maps maps;
-  if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, a.N, a.K)) return e;
+  if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, a.N, a.K, w.rows)) return e;
   if (s.ks > 1) {
-    if (s.tiles > kWsTiles || s.units > kWsUnits) return cudaErrorInvalidValue;
+    if (!workspace_fits(s, w)) return cudaErrorInvalidValue;
     void* ws = nullptr;
     if (cudaError_t e = workspace(dev, a.stream, &ws)) return e;
     p.cnt = static_cast<int*>(ws);
     p.part = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsCounterBytes);
   }
-  return launch_stream(maps, p, d.sms, d, a.stream, a.pdl);
+  return launch_stream(maps, p, w, d, a.stream, a.pdl);
 }
 
 cudaError_t launch_tc_id(const LaunchArgs& a, const w4a16_plan& plan) {
@@ -1450,12 +1531,7 @@ cudaError_t launch_tc_id(const LaunchArgs& a, const w4a16_plan& plan) {
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);
     DeviceInfo& d = device_info(dev);
-    if (!d.attr_set[4]) {
-      if (cudaError_t e = cudaFuncSetAttribute(tc_routed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               kSmemLimit))
-        return e;
-      d.attr_set[4] = true;
-    }
+    if (cudaError_t e = allow_smem(tc_routed_kernel, d)) return e;
   }
   Maps maps;
   if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, (int64_t)a.N * a.E, a.K)) return e;
@@ -1487,12 +1563,15 @@ size_t tc_noalloc_scratch_bytes() { return kWsBytes; }
 
 bool tc_noalloc_fits(int N, int K) {
   const Shape s = tc_shape(N, K);
-  return s.ks == 1 || (s.tiles <= kWsTiles && s.units <= kWsUnits);
+  for (int M = 1; M <= kMaxChunk; ++M)
+    if (!workspace_fits(s, stream_work(s, N, M))) return false;
+  return true;
 }
 
 cudaError_t launch_tc_noalloc(const LaunchArgs& a) {
   const Shape s = tc_shape(a.N, a.K);
-  if (s.ks > 1 && (s.tiles > kWsTiles || s.units > kWsUnits)) return cudaErrorInvalidValue;
+  const StreamWork w = stream_work(s, a.N, a.M);
+  if (!workspace_fits(s, w)) return cudaErrorInvalidValue;
   int dev = 0;
   if (cudaError_t e = cudaGetDevice(&dev)) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -1505,7 +1584,7 @@ cudaError_t launch_tc_noalloc(const LaunchArgs& a) {
   p.part = nullptr;
   p.cnt = nullptr;
   Maps maps;
-  if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, a.N, a.K)) return e;
+  if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, a.N, a.K, w.rows)) return e;
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DeviceInfo& d = device_info(dev);
   if (!g_noalloc_ptr[dev]) {
@@ -1517,9 +1596,9 @@ cudaError_t launch_tc_noalloc(const LaunchArgs& a) {
     p.cnt = static_cast<int*>(g_noalloc_ptr[dev]);
     p.part = reinterpret_cast<float*>(static_cast<char*>(g_noalloc_ptr[dev]) + kWsCounterBytes);
     // the array keeps whatever the previous call left: the counters must start at zero
-    if (cudaError_t e = cudaMemsetAsync(p.cnt, 0, (size_t)s.tiles * 4, a.stream)) return e;
+    if (cudaError_t e = cudaMemsetAsync(p.cnt, 0, (size_t)w.tiles * 4, a.stream)) return e;
   }
-  return launch_stream(maps, p, d.sms, d, a.stream, a.pdl);
+  return launch_stream(maps, p, w, d, a.stream, a.pdl);
 }
 
 }  // namespace w4a16

@@ -150,12 +150,13 @@ def test_plans_depend_on_shape_only_and_fill_the_gpu(L):
 
 
 def test_split_plans_fit_the_fixed_workspace(L):
-    # the tensor-core kernel's workspace holds 4096 tile counters and 4864 unit partials
+    # the persistent kernel's workspace holds 8192 tile counters and 4864 x 32 rows of unit partials
     for K in (512, 1024, 1536, 2048, 2560, 4096, 10240, 12288, 16384, 65536):
         for N in (1, 31, 32, 500, 1621 * 32, 2431 * 32, 2432 * 32, 5000 * 32, 262144):
-            p = ops.get_plan(N, K, "tc")
+            p = ops.get_plan(N, K, "tc_stream")
             if p["ksplit"] > 1:
-                assert p["units"] <= 4864 and p["units"] // p["ksplit"] <= 4096, (N, K, p)
+                assert p["units"] * p["rows_per_tile"] <= 4864 * 32, (N, K, p)
+                assert p["units"] // p["ksplit"] <= 8192, (N, K, p)
 
 
 def test_python_layer_rejects_host_tensors():
