@@ -43,11 +43,13 @@
  * done and never synchronise, except w4a16_device_status and the one-time
  * workspace set-up below.
  *
- * Workspace.  When the tensor-core kernel splits K across warps of different
- * SMs (w4a16_get_plan: ksplit > 1) it exchanges fp32 slice sums through a
- * workspace the library owns, one per (device, stream): 4.77 MiB, enough for
- * every shape, allocated with cudaMalloc (and its counters zeroed on the
- * stream) by the first call that needs it on that stream.  It stays
+ * Workspace.  When the tensor-core kernel's persistent grid splits K across
+ * warps of different SMs (w4a16_get_plan: ksplit > 1 with that launch shape)
+ * it exchanges fp32 slice sums through a workspace the library owns, one per
+ * (device, stream): 4.78 MiB, enough for every shape, allocated with
+ * cudaMalloc (and its counters zeroed on the stream) by the first call that
+ * needs it on that stream.  The tile kernel exchanges them in shared memory
+ * and needs none.  It stays
  * allocated until the process exits.  Calls
  * on one stream are ordered and share it safely; calls on different streams
  * use different workspaces.  A call that would need to allocate while its
@@ -124,7 +126,7 @@ int w4a16_mm_kernel(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* s
  *
  * It runs the same tensor-core kernel with the same arithmetic, so its
  * results equal w4a16_mm's bit for bit.  Its split-K scratch is one fixed
- * 4,997,120-byte device array inside the library (16 KiB of tile counters +
+ * 5,013,504-byte device array inside the library (32 KiB of tile counters +
  * 4864 KiB of fp32 partials), which every GPU that loads the library holds
  * until the process exits; every (N, K) with K % 512 == 0 fits in it, and a
  * shape that would not is rejected with W4A16_ERR_SHAPE.  K % 512 != 0 is
