@@ -220,6 +220,7 @@ int w4a16_mm_id_kernel(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16
   a.N = N; a.K = K; a.ids = ids; a.T = T; a.E = E;
   a.stream = static_cast<cudaStream_t>(stream);
   a.pdl = env().pdl;
+  a.tc_path = plan.kernel == W4A16_KERNEL_TC_STREAM ? 1 : plan.kernel == W4A16_KERNEL_TC_TILE ? 2 : 0;
   if (int rc = flag_pointer(&a.flags)) return rc;
   cudaError_t e = cudaSuccess;
   switch (plan.kernel) {

@@ -7,18 +7,18 @@
 
 namespace w4a16 {
 
-// Collect, in token order, up to kMaxChunk tokens t >= s_state[0] with
-// ids[t] == e (or, when e < 0, with ids[t] outside 0..E-1) into s_tok.
+// Collect, in token order, up to `cap` (<= kMaxChunk) tokens t >= s_state[0]
+// with ids[t] == e (or, when e < 0, with ids[t] outside 0..E-1) into s_tok.
 // All threads of the CTA call it; warp 0 scans 32 ids per step with a
 // ballot.  On return s_state[0] is the scan position for the next call and
 // the return value is the number of tokens collected (0 = none left).
 __device__ __forceinline__ int gather_tokens(const int32_t* __restrict__ ids, int T, int E, int e, int* s_tok,
-                                             int* s_state) {
+                                             int* s_state, int cap = kMaxChunk) {
   const int lane = threadIdx.x & 31;
   if (threadIdx.x < 32) {
     int pos = s_state[0];
     int cnt = 0;
-    while (pos < T && cnt < kMaxChunk) {
+    while (pos < T && cnt < cap) {
       const int t = pos + lane;
       bool match = false;
       if (t < T) {
@@ -28,7 +28,7 @@ __device__ __forceinline__ int gather_tokens(const int32_t* __restrict__ ids, in
       const unsigned mask = __ballot_sync(0xffffffffu, match);
       const int rank = __popc(mask & ((1u << lane) - 1u));
       const int n = __popc(mask);
-      const int need = kMaxChunk - cnt;
+      const int need = cap - cnt;
       if (n <= need) {
         if (match) s_tok[cnt + rank] = t;
         cnt += n;
@@ -37,7 +37,7 @@ __device__ __forceinline__ int gather_tokens(const int32_t* __restrict__ ids, in
         if (match && rank < need) s_tok[cnt + rank] = t;
         const unsigned last = __ballot_sync(0xffffffffu, match && rank == need - 1);
         pos += (__ffs(last) - 1) + 1;
-        cnt = kMaxChunk;
+        cnt = cap;
       }
     }
     if (lane == 0) {

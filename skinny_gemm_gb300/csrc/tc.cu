@@ -68,6 +68,9 @@ namespace w4a16 {
 namespace {
 
 // Tuning knobs (compile-time; the defaults are the measured choice).
+#ifndef W4A16_TC_STREAM_WARPS
+#define W4A16_TC_STREAM_WARPS 4    // warps per CTA of the persistent kernel (32-row warps)
+#endif
 #ifndef W4A16_TC_MIN_BLOCKS
 #define W4A16_TC_MIN_BLOCKS 3      // persistent CTAs per SM the register budget must allow
 #endif
@@ -84,7 +87,7 @@ namespace {
 #define W4A16_TC_TILE_MAX_UNITS 4863  // largest stages x row tiles the tile kernel takes
 #endif
 #ifndef W4A16_TC_STREAM_NSUB1_MIN_M
-#define W4A16_TC_STREAM_NSUB1_MIN_M 2  // smallest chunk the persistent kernel runs with 16-row warps
+#define W4A16_TC_STREAM_NSUB1_MIN_M 9  // smallest chunk the persistent kernel runs with 16-row warps
 #endif
 #ifndef W4A16_TC_TILE_SLICES
 #define W4A16_TC_TILE_SLICES 5        // most K-slices one CTA of the tile kernel takes, where a cluster can split
@@ -99,7 +102,6 @@ constexpr int kCodeBytes = 2 * kBoxBytes;                        // 8192 codes p
 constexpr int kParamBytes = kTileRows * 8 * 2;                   // 512: 8 bf16 per row per stage
 constexpr int kCodeSlotBytes = kCodeBytes + 2 * kParamBytes;     // 9216: codes | scales | biases
 constexpr int kXPitch = kStageK * 2 + 64;                        // 1088: conflict-free LDS.128
-constexpr int kStreamWarps = 4;          // warps per CTA of the persistent kernel
 constexpr int kRoutedWarps = 8;          // max warps per CTA of the routed kernel
 #ifndef W4A16_TC_TARGET_UNITS
 #define W4A16_TC_TARGET_UNITS (152 * 16)
@@ -120,7 +122,7 @@ struct Geo {
   static constexpr int kBox = kRows * 128;
   static constexpr int kParam = kRows * 16;
   static constexpr int kSlot = (2 * kBox + 2 * kParam + 1023) / 1024 * 1024;  // 9216 | 5120
-  static constexpr int kWarps = NSUB == 2 ? 4 : 8;  // warps per CTA of the persistent kernel
+  static constexpr int kWarps = NSUB == 2 ? W4A16_TC_STREAM_WARPS : 8;  // warps per CTA of the persistent kernel
 };
 
 // ---- PTX wrappers -------------------------------------------------------------------
@@ -488,6 +490,9 @@ __host__ __device__ inline int ring_bytes(int stages, int mcap) {
 
 // ---- persistent kernel (w4a16_mm) ------------------------------------------------------
 
+// Bytes after the barriers: token rows [8] and every warp's unit ring [8] (ints).
+constexpr int kStreamMisc = 4 * (kMaxChunk + 8 * 8) + 32;
+
 struct StreamParams {
   const uint16_t* x;
   const uint16_t* S;
@@ -495,6 +500,7 @@ struct StreamParams {
   uint16_t* y;
   float* part;      // [units][8][rows] slice partials (ksplit > 1)
   int* cnt;         // [tiles] arrival counters, zero between launches
+  int* sched;       // [2] unit-grab and finished-warp counters, zero between launches
   int* flags;
   int N, K, M, row0;
   int nst, sl, ks, tiles, units;  // tiles and units of 16 * NSUB rows
@@ -513,31 +519,11 @@ __host__ __device__ inline int xstage_bytes(int mc, int K) {
   return mc * (2 * K + 64) + (K / kGroup) * sx_cols(mc) * 4;
 }
 
-// Position of a work unit u = tile * ks + slice, advanced by a fixed stride
-// without divisions.
-struct UnitCursor {
-  int u, tile, slice;
-  __device__ __forceinline__ void init(int u0, int ks) {
-    u = u0;
-    tile = u0 / ks;
-    slice = u0 - tile * ks;
-  }
-  __device__ __forceinline__ void advance(int step, int step_tiles, int step_slices, int ks) {
-    u += step;
-    tile += step_tiles;
-    slice += step_slices;
-    if (slice >= ks) {
-      slice -= ks;
-      ++tile;
-    }
-  }
-};
-
 // Persistent CTAs of Geo<NSUB>::kWarps warps; a warp's work unit is
 // 16 * NSUB rows x one K-slice.  With NSUB = 1 a warp needs half the
 // registers and shared memory, so twice as many warps fit on an SM.
 template <int NSUB>
-constexpr int stream_min_blocks() { return NSUB == 2 ? W4A16_TC_MIN_BLOCKS : 2; }
+constexpr int stream_min_blocks() { return NSUB == 1 ? 2 : Geo<NSUB>::kWarps >= 8 ? 1 : W4A16_TC_MIN_BLOCKS; }
 
 template <int NSUB, bool ALLCOLS, bool XSTAGED>
 __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB>()) tc_stream_kernel(
@@ -563,7 +549,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
   const uint32_t bar_off = (uint32_t)(kW * ring_bytes<NSUB>(S, xring));
   R.bars0 = smem_u32(base) + bar_off + (uint32_t)(warp * S * 8);
   int* s_tok = reinterpret_cast<int*>(base + bar_off + kW * S * 8);
-  const uint32_t xst = smem_u32(base) + bar_off + (uint32_t)(kW * S * 8 + 64);  // 16-byte aligned
+  const uint32_t xst = smem_u32(base) + bar_off + (uint32_t)(kW * S * 8 + kStreamMisc);  // 16-byte aligned
   const uint32_t sxs = xst + (uint32_t)(mc * p.xpitch);
   R.issued = R.consumed = 0;
   R.pol_stream = policy_evict_first();
@@ -575,91 +561,132 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   __syncthreads();
 
-  // warp-major numbering: every pass over the units spreads them evenly over CTAs
+  // warp-major numbering: the first pass over the units spreads them evenly over CTAs
   const int gw = warp * gridDim.x + blockIdx.x;
   const int TW = gridDim.x * kW;
-  const int tw_tiles = TW / p.ks, tw_slices = TW - tw_tiles * p.ks;
 
-  // issue cursor (lane 0): unit, stage, end of the unit's stages
-  UnitCursor ic;
-  ic.init(gw, p.ks);
-  int ist = ic.slice * p.sl;
-  int iend = min(ist + p.sl, p.nst);
-  auto step = [&](UnitCursor& c, int& st, int& end) {
-    if (++st == end) {
-      c.advance(TW, tw_tiles, tw_slices, p.ks);
-      st = c.slice * p.sl;
-      end = min(st + p.sl, p.nst);
+  // Work units of this warp.  The first is static (unit gw), so its weights
+  // can be requested before the wait for earlier kernels; every later one is
+  // grabbed from a counter in the workspace (unit TW + count) as soon as the
+  // previous one starts streaming, so warps on faster SMs take more units.
+  // Lane 0 streams the units in order and records each in s_units (a ring
+  // of 8 per warp, ahead of the computing lanes by at most S stages); -1
+  // marks the end.
+  int* s_units = s_tok + kMaxChunk + 8 * warp;
+  int iu = -1, ist = 0, iend = 0, nxt = -1;  // lane 0: unit being issued, its stage cursor, the next unit
+  uint32_t iseq = 0;
+  auto grab = [&]() {
+    const int v = TW + atomicAdd(p.sched, 1);
+    return v < p.units ? v : -1;
+  };
+  auto begin_unit = [&](int u) {
+    iu = u;
+    s_units[iseq++ & 7u] = u;
+    if (u >= 0) {
+      ist = (u % p.ks) * p.sl;
+      iend = min(ist + p.sl, p.nst);
     }
   };
-  auto issue_next = [&](bool with_x) {
-    if (ic.u >= p.units) return;
-    const uint32_t slot = ring_issue_w<NSUB>(R, &maps, ist, ic.tile * kRows, xring);
+  auto issue_stage = [&](bool with_x) {
+    const uint32_t slot = ring_issue_w<NSUB>(R, &maps, ist, (iu / p.ks) * kRows, xring);
     if (with_x) ring_issue_x(R, slot, ist, p.x, s_tok, xring, p.K);
-    step(ic, ist, iend);
+    ++ist;
+  };
+  auto issue_next = [&](bool with_x) {  // after the wait only (grabs touch the workspace)
+    if (iu < 0) return;
+    if (ist == iend) {
+      begin_unit(nxt);
+      if (iu < 0) return;
+      nxt = grab();
+    }
+    issue_stage(with_x);
   };
   // The weights never depend on earlier kernels: with p.prefetch the first
-  // stages are requested before the wait for those kernels and their
-  // activation chunks after it (replaying the cursor from the start).
-  // Activations, outputs and the workspace are only touched after the wait.
-  // The first stages stay in flight while the activations are staged.
+  // unit's first stages are requested before the wait for those kernels and
+  // their activation chunks after it.  Activations, outputs and the
+  // workspace are only touched after the wait.  The first stages stay in
+  // flight while the activations are staged.
   if (lane == 0) {
     fence_proxy_async();
+    begin_unit(gw < p.units ? gw : -1);
     if (p.prefetch)
-      for (int i = 0; i < S; ++i) issue_next(false);
+      for (int i = 0; i < S && iu >= 0 && ist < iend; ++i) issue_stage(false);
   }
   pdl_wait();
   if (lane == 0) {
-    if (p.prefetch) {
-      UnitCursor rc;
-      rc.init(gw, p.ks);
-      int rst = rc.slice * p.sl, rend = min(rst + p.sl, p.nst);
-      for (uint32_t i = 0; i < R.issued; ++i) {
-        ring_issue_x(R, i, rst, p.x, s_tok, xring, p.K);
-        step(rc, rst, rend);
-      }
-    } else {
-      for (int i = 0; i < S; ++i) issue_next(true);
+    if (iu >= 0) {
+      nxt = grab();
+      const int first = (iu % p.ks) * p.sl;
+      for (uint32_t i = 0; i < R.issued; ++i) ring_issue_x(R, i, first + (int)i, p.x, s_tok, xring, p.K);
     }
+    for (int i = (int)R.issued; i < S; ++i) issue_next(true);
   }
+  __syncwarp();
 
   if (XSTAGED) {
     // Activation rows in B-fragment order, then the sum of every 64-group of
     // every row with the same MMA chain the per-stage path uses.
-    const int chunks = p.K / 8;
-    for (int c = threadIdx.x; c < mc * chunks; c += blockDim.x) {
-      const int n = c / chunks, wd = c - n * chunks;
-      const uint4 u = ld_cg_v4(p.x + (int64_t)(p.row0 + n) * p.K + 8 * wd);
-      uint32_t b[2][2];
-      frag_from_chunk(u, b);
-      sts128(xst + n * p.xpitch + 16 * wd, make_uint4(b[0][0], b[0][1], b[1][0], b[1][1]));
+    // Four chunks per thread per round, loads first, so their latencies overlap.
+    const int chunks = p.K / 8, total = mc * chunks;
+    for (int c0 = threadIdx.x; c0 < total; c0 += 4 * blockDim.x) {
+      uint4 u[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = c0 + j * blockDim.x;
+        if (c < total) {
+          const int n = c / chunks, wd = c - n * chunks;
+          u[j] = ld_cg_v4(p.x + (int64_t)(p.row0 + n) * p.K + 8 * wd);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = c0 + j * blockDim.x;
+        if (c < total) {
+          const int n = c / chunks, wd = c - n * chunks;
+          uint32_t b[2][2];
+          frag_from_chunk(u[j], b);
+          sts128(xst + n * p.xpitch + 16 * wd, make_uint4(b[0][0], b[0][1], b[1][0], b[1][1]));
+        }
+      }
     }
     __syncthreads();
-    for (int gi = warp; gi < p.K / kGroup; gi += kW) {
-      uint32_t b[2][2][2];
+    // Group sums, four groups per warp at a time with their MMA chains interleaved.
+    const int ngroups = p.K / kGroup;
+    for (int g0 = warp; g0 < ngroups; g0 += 4 * kW) {
+      uint32_t b[4][2][2][2];
+      float v[4][4];
 #pragma unroll
-      for (int cb = 0; cb < 2; ++cb) {
-        uint4 u = make_uint4(0, 0, 0, 0);
-        if (g < mc) u = lds128(xst + g * p.xpitch + 128 * gi + 64 * cb + 16 * t);
-        b[cb][0][0] = u.x;
-        b[cb][0][1] = u.y;
-        b[cb][1][0] = u.z;
-        b[cb][1][1] = u.w;
+      for (int j = 0; j < 4; ++j) {
+        const int gi = g0 + j * kW;
+#pragma unroll
+        for (int cb = 0; cb < 2; ++cb) {
+          uint4 u = make_uint4(0, 0, 0, 0);
+          if (g < mc && gi < ngroups) u = lds128(xst + g * p.xpitch + 128 * gi + 64 * cb + 16 * t);
+          b[j][cb][0][0] = u.x;
+          b[j][cb][0][1] = u.y;
+          b[j][cb][1][0] = u.z;
+          b[j][cb][1][1] = u.w;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[j][i] = 0.f;
       }
-      float v[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int step = 0; step < 4; ++step) mma_bf16(v, kOnes, kOnes, kOnes, kOnes, b[step >> 1][step & 1][0],
-                                                    b[step >> 1][step & 1][1]);
-      if (g == 0 && 2 * t < mc) {
-        asm volatile("st.shared.v2.f32 [%0], {%1,%2};" ::"r"(sxs + (gi * sx_cols(mc) + 2 * t) * 4), "f"(v[0]),
-                     "f"(v[1])
-                     : "memory");
+      for (int step = 0; step < 4; ++step)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          mma_bf16(v[j], kOnes, kOnes, kOnes, kOnes, b[j][step >> 1][step & 1][0], b[j][step >> 1][step & 1][1]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int gi = g0 + j * kW;
+        if (g == 0 && 2 * t < mc && gi < ngroups) {
+          asm volatile("st.shared.v2.f32 [%0], {%1,%2};" ::"r"(sxs + (gi * sx_cols(mc) + 2 * t) * 4), "f"(v[j][0]),
+                       "f"(v[j][1])
+                       : "memory");
+        }
       }
     }
     __syncthreads();
   }
-  if (gw >= p.units) return;
-
   uint32_t loff2[2][4];
   ldsm_offsets(lane, loff2);
   uint32_t loff[NSUB][4];
@@ -714,13 +741,13 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
     for (int i = 0; i < 2 * NSUB; ++i) pr[i] = tile * kRows + 16 * (i >> 1) + g + 8 * (i & 1);
   };
 
-  // consume cursor
-  UnitCursor cc;
-  cc.init(gw, p.ks);
-
-  for (; cc.u < p.units && !timed_out;) {
-    const int tile = cc.tile;
-    const int s0 = cc.slice * p.sl, s1 = min(s0 + p.sl, p.nst);
+  // consume cursor: the units in the order lane 0 recorded them
+  for (uint32_t cseq = 0; !timed_out; ++cseq) {
+    __syncwarp();
+    const int u = s_units[cseq & 7u];
+    if (u < 0) break;
+    const int tile = u / p.ks, slice = u - tile * p.ks;
+    const int s0 = slice * p.sl, s1 = min(s0 + p.sl, p.nst);
     int prow[2 * NSUB];
     rows_of(tile, prow);
 
@@ -777,7 +804,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
           if (n < mc && row < p.N) p.y[(int64_t)s_tok[n] * p.N + row] = f32_to_bf16_bits(acc[s][i]);
         }
     } else {
-      float* q = p.part + (int64_t)cc.u * 8 * kRows;
+      float* q = p.part + (int64_t)u * 8 * kRows;
 #pragma unroll
       for (int s = 0; s < NSUB; ++s)
 #pragma unroll
@@ -788,7 +815,6 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
         }
       pend_tile = tile;
     }
-    cc.advance(TW, tw_tiles, tw_slices, p.ks);
   }
   if (!timed_out) {
     if (cnt_tile >= 0) {
@@ -808,6 +834,17 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
     while (R.consumed < issued) {
       mbar_wait(R.bars0 + 8 * (R.consumed % (uint32_t)S), (R.consumed / (uint32_t)S) & 1u);
       ++R.consumed;
+    }
+  }
+  // The last warp out resets the unit counters for the next launch (every
+  // warp has made its last grab before it counts itself out).
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence();
+    if (atomicAdd(p.sched + 1, 1) == TW - 1) {
+      __threadfence();
+      p.sched[0] = 0;
+      p.sched[1] = 0;
     }
   }
 }
@@ -832,18 +869,22 @@ struct TileParams {
   const uint16_t* x;
   uint16_t* y;
   int* flags;
-  int N, K, M, row0;
+  const int32_t* ids;  // routed mode: expert id per token
+  int N, K, M, row0;   // plain mode: rows row0 .. row0 + M of x (M <= xcap)
+  int T, E;            // routed mode: tokens, experts
   int nst, sl, ks;
   int kc;        // CTAs (one cluster) per 16-row tile
   int nloc;      // stage slots per CTA: ceil(ks / kc) * sl
+  int xcap;      // activation rows per x slot (plain: M; routed: tokens per chunk)
   int prefetch;  // request the weights before waiting for earlier kernels
 };
 
 // Shared memory (the same layout in every CTA of a cluster): slots
-// [nloc][kSlot16] | activation chunks [nloc][mc][kXPitch] | barriers [nloc] |
-// slice sums [ks][16][8] fp32 (used in the first CTA) | tokens [8], abort flag.
-__host__ __device__ inline int tile_smem(int nloc, int mc, int ks) {
-  return nloc * (kSlot16 + mc * kXPitch) + nloc * 8 + ks * kTile16 * 8 * 4 + 64 + 1024;
+// [nloc][kSlot16] | activation chunks [nloc][xcap][kXPitch] | barriers
+// [nloc] | slice sums [ks][16][8] fp32 (used in the first CTA) | tokens [8],
+// abort flag, token-scan state [2].
+__host__ __device__ inline int tile_smem(int nloc, int xcap, int ks) {
+  return nloc * (kSlot16 + xcap * kXPitch) + nloc * 8 + ks * kTile16 * 8 * 4 + 64 + 1024;
 }
 
 __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
@@ -864,51 +905,88 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
-template <bool ALLCOLS>
+// Plain mode (w4a16_mm): blockIdx.x = tile * kc + rank; one chunk of M rows.
+// Routed mode (w4a16_mm_id): blockIdx.y = expert e.  After the wait for
+// earlier kernels every CTA collects, in token order, the tokens routed to e
+// (at most xcap at a time) and exits when there are none, so an untouched
+// expert's weights are never read.  Its weights are requested once and stay
+// in shared memory while the token chunks stream through; the CTAs of e = 0
+// also write zero rows for tokens whose id is out of range and raise the
+// flag.  Every row's arithmetic is the canonical one, so routed rows equal
+// w4a16_mm on the selected expert bit for bit.
+//
 // The bound of 768 threads caps registers at 80, so that five CTAs of five
 // warps fit on an SM (by registers).
+template <bool ALLCOLS, bool ROUTED>
 __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Maps maps, TileParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, W = blockDim.x >> 5;
   const int g = lane >> 2, t = lane & 3;
-  const int mc = p.M, kc = p.kc;
+  const int kc = p.kc;
   // with cluster dimensions (kc, 1, 1) the rank in the cluster is blockIdx.x % kc
   const int tile = blockIdx.x / kc, crank = blockIdx.x - tile * kc;
   const int j0 = crank * p.ks / kc, j1 = (crank + 1) * p.ks / kc;  // this CTA's slices
   const int st0 = j0 * p.sl, nloc = min(j1 * p.sl, p.nst) - st0;  // and stages
-  const int tensor_row = tile * kTile16;
-  const int x_slot = mc * kXPitch;
+  const int e = ROUTED ? (int)blockIdx.y : 0;
+  const int tile_row = tile * kTile16;
+  const int tensor_row = e * p.N + tile_row;  // row of the stacked [E][N] weights
+  const int x_slot = p.xcap * kXPitch;
   const uint32_t codes0 = smem_u32(base);
   const uint32_t xs0 = codes0 + (uint32_t)(p.nloc * kSlot16);
   const uint32_t bars0 = xs0 + (uint32_t)(p.nloc * x_slot);
   float* red = reinterpret_cast<float*>(base + (bars0 - codes0) + p.nloc * 8);
   int* s_tok = reinterpret_cast<int*>(red + p.ks * kTile16 * 8);
   int* s_abort = s_tok + kMaxChunk;
+  int* s_state = s_abort + 1;  // token scan: [0] position, [1] count
 
   for (int i = threadIdx.x; i < nloc; i += blockDim.x) mbar_init(bars0 + 8 * i, 1);
-  if (threadIdx.x < mc) s_tok[threadIdx.x] = p.row0 + threadIdx.x;
-  if (threadIdx.x == 0) *s_abort = 0;
+  if (!ROUTED && threadIdx.x < p.M) s_tok[threadIdx.x] = p.row0 + threadIdx.x;
+  if (threadIdx.x == 0) {
+    *s_abort = 0;
+    s_state[0] = 0;
+  }
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   __syncthreads();
-  // announce that this CTA runs (its shared memory may now be written by the others)
-  if (kc > 1) cluster_arrive_relaxed();
 
   // lane 0 of warp w requests local stages w, w + W, ...
-  auto weights = [&](int i) {
-    issue_weights<1>(codes0 + i * kSlot16, bars0 + 8 * i, &maps, st0 + i, tensor_row, mc, policy_evict_first(),
+  auto weights = [&](int i, int xrows) {
+    issue_weights<1>(codes0 + i * kSlot16, bars0 + 8 * i, &maps, st0 + i, tensor_row, xrows, policy_evict_first(),
                      policy_evict_last());
   };
-  if (lane == 0 && p.prefetch)
-    for (int i = warp; i < nloc; i += W) weights(i);
+  if (!ROUTED && lane == 0 && p.prefetch)
+    for (int i = warp; i < nloc; i += W) weights(i, p.M);
   pdl_wait();
   // Only now let the next kernel launch: its CTAs then fetch their weights
   // while this one computes, and at most one kernel waits ahead (CTAs
   // launched further ahead would only hold SM resources and slow this one).
   pdl_launch_dependents();
+
+  int mc = p.M;
+  if (ROUTED) {
+    if (e == 0 && crank == 0) {
+      // tokens whose expert id is out of range: zero rows, raise the flag
+      for (;;) {
+        const int cnt = gather_tokens(p.ids, p.T, p.E, -1, s_tok, s_state);
+        if (cnt == 0) break;
+        if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(p.flags, W4A16_DEVICE_BAD_ID);
+        for (int i = threadIdx.x; i < cnt * kTile16; i += blockDim.x) {
+          const int row = tile_row + i % kTile16;
+          if (row < p.N) p.y[(int64_t)s_tok[i / kTile16] * p.N + row] = 0;
+        }
+        __syncthreads();
+      }
+      if (threadIdx.x == 0) s_state[0] = 0;
+      __syncthreads();
+    }
+    mc = gather_tokens(p.ids, p.T, p.E, e, s_tok, s_state, p.xcap);
+    if (mc == 0) return;  // the same for every CTA of the cluster: no cluster barrier has run
+  }
+  // announce that this CTA runs (its shared memory may now be written by the others)
+  if (kc > 1) cluster_arrive_relaxed();
   if (lane == 0)
     for (int i = warp; i < nloc; i += W) {
-      if (!p.prefetch) weights(i);
+      if (ROUTED || !p.prefetch) weights(i, mc);
       issue_x(xs0 + i * x_slot, bars0 + 8 * i, st0 + i, p.x, s_tok, mc, p.K, policy_evict_last());
     }
 
@@ -922,51 +1000,75 @@ __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Ma
   uint32_t loff2[2][4];
   ldsm_offsets(lane, loff2);
   const uint32_t loff[1][4] = {{loff2[0][0], loff2[0][1], loff2[0][2], loff2[0][3]}};
-  bool ok = true;
-  for (int j = j0 + warp; j < j1 && ok; j += W) {
-    float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
-    const int s1 = min((j + 1) * p.sl, p.nst);
-    for (int st = j * p.sl; st < s1; ++st) {
-      const int i = st - st0;
-      if (!__all_sync(0xffffffffu, mbar_wait(bars0 + 8 * i, 0u))) {
-        ok = false;
-        break;
+  auto cta_sync = [&]() {
+    __syncwarp();
+    if (kc > 1) {
+      cluster_arrive();
+      cluster_wait();
+    } else {
+      __syncthreads();
+    }
+  };
+
+  uint32_t last_issued = 0;  // the chunk whose copies were requested last
+  for (uint32_t chunk = 0;; ++chunk) {
+    // every stage barrier completes one phase per chunk (weights + x, then x)
+    const uint32_t parity = chunk & 1u;
+    bool ok = *s_abort == 0;
+    for (int j = j0 + warp; j < j1 && ok; j += W) {
+      float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+      const int s1 = min((j + 1) * p.sl, p.nst);
+      for (int st = j * p.sl; st < s1; ++st) {
+        const int i = st - st0;
+        if (!__all_sync(0xffffffffu, mbar_wait(bars0 + 8 * i, parity))) {
+          ok = false;
+          break;
+        }
+        const uint32_t cbase = ordered(codes0 + i * kSlot16);
+        const uint32_t xbase = ordered(xs0 + i * x_slot + g * kXPitch + 16 * t);
+        compute_stage<1, ALLCOLS, false>(cbase, xbase, g < mc, 0u, 0u, false, acc, loff, g);
       }
-      const uint32_t cbase = ordered(codes0 + i * kSlot16);
-      const uint32_t xbase = ordered(xs0 + i * x_slot + g * kXPitch + 16 * t);
-      compute_stage<1, ALLCOLS, false>(cbase, xbase, g < mc, 0u, 0u, false, acc, loff, g);
-    }
-    if (!ok) break;
+      if (!ok) break;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      st_cluster_f32(red_dst + 4 * ((j * kTile16 + g + 8 * (i >> 1)) * 8 + 2 * t + (i & 1)), acc[0][i]);
-  }
-  if (!ok && lane == 0) {
-    atomicOr(p.flags, W4A16_DEVICE_TIMEOUT);
-    *s_abort = 1;
-  }
-  __syncwarp();
-  if (kc > 1) {
-    cluster_arrive();
-    cluster_wait();
-  } else {
-    __syncthreads();
-  }
-  if (*s_abort) {
-    // let every copy this warp requested land before shared memory is released
-    if (lane == 0)
-      for (int i = warp; i < nloc; i += W) mbar_wait(bars0 + 8 * i, 0u);
-    return;
-  }
-  if (crank != 0) return;
-  for (int i = threadIdx.x; i < kTile16 * mc; i += blockDim.x) {
-    const int n = i / kTile16, r = i - n * kTile16;
-    const int row = tensor_row + r;
-    if (row < p.N) {
-      float sum = red[r * 8 + n];
-      for (int j = 1; j < p.ks; ++j) sum = __fadd_rn(sum, red[(j * kTile16 + r) * 8 + n]);
-      p.y[(int64_t)s_tok[n] * p.N + row] = f32_to_bf16_bits(sum);
+      for (int i = 0; i < 4; ++i)
+        st_cluster_f32(red_dst + 4 * ((j * kTile16 + g + 8 * (i >> 1)) * 8 + 2 * t + (i & 1)), acc[0][i]);
     }
+    if (!ok && lane == 0 && *s_abort == 0) {
+      atomicOr(p.flags, W4A16_DEVICE_TIMEOUT);
+      *s_abort = 1;
+    }
+    cta_sync();
+    const bool aborted = *s_abort != 0;  // sticky: later chunks skip the work but keep the barriers
+    if (crank == 0 && !aborted) {
+      for (int i = threadIdx.x; i < kTile16 * mc; i += blockDim.x) {
+        const int n = i / kTile16, r = i - n * kTile16;
+        const int row = tile_row + r;
+        if (row < p.N) {
+          float sum = red[r * 8 + n];
+          for (int j = 1; j < p.ks; ++j) sum = __fadd_rn(sum, red[(j * kTile16 + r) * 8 + n]);
+          p.y[(int64_t)s_tok[n] * p.N + row] = f32_to_bf16_bits(sum);
+        }
+      }
+    }
+    if (!ROUTED) break;
+    __syncthreads();  // s_tok is read above and rewritten by the scan
+    mc = gather_tokens(p.ids, p.T, p.E, e, s_tok, s_state, p.xcap);
+    if (mc == 0) break;  // the same in every CTA of the cluster
+    // the first CTA has summed this chunk and every warp is done with the x slots
+    cta_sync();
+    if (!aborted) {
+      if (lane == 0)
+        for (int i = warp; i < nloc; i += W) {
+          fence_proxy_async();
+          mbar_expect_tx(bars0 + 8 * i, (uint32_t)(mc * kStageK * 2));
+          issue_x(xs0 + i * x_slot, bars0 + 8 * i, st0 + i, p.x, s_tok, mc, p.K, policy_evict_last());
+        }
+      last_issued = chunk + 1;
+    }
+  }
+  if (*s_abort && lane == 0) {
+    // let every copy this warp requested land before shared memory is released
+    for (int i = warp; i < nloc; i += W) mbar_wait(bars0 + 8 * i, last_issued & 1u);
   }
 }
 
@@ -982,10 +1084,11 @@ struct RoutedParams {
   int N, K, T, E;
   int nst, sl, ks;
   int warps, stages;
+  int xcap;  // activation rows per x slot: min(T, 8)
 };
 
-__host__ __device__ inline int routed_smem(int warps, int stages, int ks) {
-  return warps * ring_bytes<2>(stages, kMaxChunk) + warps * stages * 8 + ks * kTileRows * 8 * 4 + 16 * 4 + 1024;
+__host__ __device__ inline int routed_smem(int warps, int stages, int ks, int xcap) {
+  return warps * ring_bytes<2>(stages, xcap) + warps * stages * 8 + ks * kTileRows * 8 * 4 + 16 * 4 + 1024;
 }
 
 __global__ void __launch_bounds__(kRoutedWarps * 32) tc_routed_kernel(const __grid_constant__ Maps maps,
@@ -995,7 +1098,7 @@ __global__ void __launch_bounds__(kRoutedWarps * 32) tc_routed_kernel(const __gr
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int S = p.stages, W = p.warps;
-  const int x_slot = kMaxChunk * kXPitch;
+  const int x_slot = p.xcap * kXPitch;
   const int e = blockIdx.y;
   const int row_base = blockIdx.x * kTileRows;
   const int tensor_row = e * p.N + row_base;
@@ -1005,7 +1108,7 @@ __global__ void __launch_bounds__(kRoutedWarps * 32) tc_routed_kernel(const __gr
   R.x_slot = x_slot;
   R.codes0 = smem_u32(base) + (uint32_t)(warp * S * kCodeSlotBytes);
   R.xs0 = smem_u32(base) + (uint32_t)(W * S * kCodeSlotBytes + warp * S * x_slot);
-  const uint32_t bar_off = (uint32_t)(W * ring_bytes<2>(S, kMaxChunk));
+  const uint32_t bar_off = (uint32_t)(W * ring_bytes<2>(S, p.xcap));
   R.bars0 = smem_u32(base) + bar_off + (uint32_t)(warp * S * 8);
   float* red = reinterpret_cast<float*>(base + bar_off + W * S * 8);  // [ks][32 rows][8 columns]
   int* s_tok = reinterpret_cast<int*>(red + p.ks * kTileRows * 8);
@@ -1176,14 +1279,21 @@ cudaError_t make_maps(Maps* m, const uint32_t* Wq, const uint16_t* S, const uint
 template <int NSUB>
 int stream_smem(int stages, int mc) {
   using G = Geo<NSUB>;
-  return G::kWarps * ring_bytes<NSUB>(stages, mc) + G::kWarps * stages * 8 + 64 + 1024;
+  return G::kWarps * ring_bytes<NSUB>(stages, mc) + G::kWarps * stages * 8 + kStreamMisc + 1024;
 }
 
 // Per-CTA shared-memory budget of the persistent kernel: the measured best
 // for 32-row warps; two CTAs per SM for 16-row warps.
 constexpr int kHalfSm = 228 * 1024 / 2 - 1024;  // per-CTA budget for two CTAs per SM (1 KB reserved each)
+// CTAs per SM the persistent kernel is sized for, and the per-CTA budget.
 template <int NSUB>
-constexpr int stream_smem_target() { return NSUB == 2 ? W4A16_TC_SMEM_TARGET : kHalfSm; }
+constexpr int stream_ctas_per_sm() { return Geo<NSUB>::kWarps >= 8 && NSUB == 2 ? 1 : 2; }
+template <int NSUB>
+constexpr int stream_budget() { return stream_ctas_per_sm<NSUB>() == 1 ? kSmemLimit - 1024 : kHalfSm; }
+template <int NSUB>
+constexpr int stream_smem_target() {
+  return NSUB == 2 && Geo<NSUB>::kWarps == 4 ? W4A16_TC_SMEM_TARGET : stream_budget<NSUB>();
+}
 
 // Deepest ring (up to W4A16_TC_MAX_STAGES, at least 2 stages per warp) that
 // keeps a CTA's shared memory under the budget.
@@ -1216,13 +1326,14 @@ cudaError_t allow_smem(Kern fn, DeviceInfo& d) {
 // units to amortise it over.
 template <int NSUB>
 bool stage_activations(int M, int K, int units, int sms) {
-  return units >= 2 * Geo<NSUB>::kWarps * 2 * sms && stream_smem<NSUB>(2, 0) + xstage_bytes(M, K) <= kHalfSm;
+  return units >= 2 * Geo<NSUB>::kWarps * stream_ctas_per_sm<NSUB>() * sms &&
+         stream_smem<NSUB>(2, 0) + xstage_bytes(M, K) <= stream_budget<NSUB>();
 }
 
 template <int NSUB>
 int staged_stages(int M, int K) {
   for (int s = W4A16_TC_MAX_STAGES; s > 2; --s)
-    if (stream_smem<NSUB>(s, 0) + xstage_bytes(M, K) <= kHalfSm) return s;
+    if (stream_smem<NSUB>(s, 0) + xstage_bytes(M, K) <= stream_budget<NSUB>()) return s;
   return 2;
 }
 
@@ -1292,13 +1403,16 @@ cudaError_t launch_stream_t(const Maps& map, StreamParams p, int sms, DeviceInfo
                 : stream_launch_t<NSUB, false, false>(map, p, sms, smem, d, stream, on);
 }
 
-// Row subtiles per warp of the persistent kernel for a chunk of M rows: at
-// M = 1 32-row warps stream faster (measured); with more activation rows
-// 16-row warps, twice as many per SM, do.
+// Row subtiles per warp of the persistent kernel for a chunk of M rows.
+// 16-row warps fit twice as many per SM; on the shapes the persistent
+// kernel serves (LM heads, 16384^2) 32-row warps were measured faster at
+// every M, so 16-row warps are used from W4A16_TC_STREAM_NSUB1_MIN_M rows
+// on (never, by default).
 int stream_nsub(int M) { return M >= W4A16_TC_STREAM_NSUB1_MIN_M ? 1 : 2; }
 
 // Launch shape of the tile kernel for one chunk of M rows.
 struct TilePlan {
+  int xcap = 0;   // activation rows per x slot
   int kc = 0;     // CTAs per 16-row tile (cluster size); 0: the tile kernel does not apply
   int nloc = 0;   // stage slots per CTA
   int warps = 0;  // warps per CTA
@@ -1322,6 +1436,7 @@ TilePlan tile_plan(const Shape& s, int N, int M, bool force) {
     const int nloc = ksl * s.sl;
     const int smem = tile_smem(nloc, M, s.ks);
     if (smem > kSmemLimit) continue;
+    tp.xcap = M;
     tp.kc = kc;
     tp.nloc = nloc;
     tp.warps = ksl < kTileMaxWarps ? ksl : kTileMaxWarps;
@@ -1332,20 +1447,22 @@ TilePlan tile_plan(const Shape& s, int N, int M, bool force) {
   return tp;
 }
 
-cudaError_t launch_tile(const LaunchArgs& a, const Shape& s, const TilePlan& tp, DeviceInfo& d) {
+cudaError_t launch_tile(const LaunchArgs& a, const Shape& s, const TilePlan& tp, DeviceInfo& d, bool routed) {
   Maps maps;
-  if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, a.N, a.K, kTile16)) return e;
+  const int64_t rows = routed ? (int64_t)a.N * a.E : a.N;
+  if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, rows, a.K, kTile16)) return e;
   TileParams p;
-  p.x = a.x; p.y = a.y; p.flags = a.flags;
-  p.N = a.N; p.K = a.K; p.M = a.M; p.row0 = a.row0;
+  p.x = a.x; p.y = a.y; p.flags = a.flags; p.ids = a.ids;
+  p.N = a.N; p.K = a.K; p.M = a.M; p.row0 = a.row0; p.T = a.T; p.E = a.E;
   p.nst = s.nst; p.sl = s.sl; p.ks = s.ks;
   p.kc = tp.kc;
   p.nloc = tp.nloc;
-  p.prefetch = a.pdl >= 2;
-  const bool allcols = a.M > 1;
-  auto* fn = allcols ? tc_tile_kernel<true> : tc_tile_kernel<false>;
+  p.xcap = tp.xcap;
+  p.prefetch = !routed && a.pdl >= 2;
+  auto* fn = routed ? tc_tile_kernel<true, true> : a.M > 1 ? tc_tile_kernel<true, false> : tc_tile_kernel<false, false>;
   if (cudaError_t e = allow_smem(fn, d)) return e;
-  return launch_ex(fn, dim3(tp.ctas), dim3(tp.warps * 32), tp.smem, a.stream, a.pdl > 0, maps, p, tp.kc);
+  const dim3 grid(tp.ctas, routed ? a.E : 1);
+  return launch_ex(fn, grid, dim3(tp.warps * 32), tp.smem, a.stream, a.pdl > 0, maps, p, tp.kc);
 }
 
 std::mutex g_dev_mu;
@@ -1363,8 +1480,9 @@ DeviceInfo& device_info(int dev) {
 }
 
 // Workspace of one (device, stream), fixed layout:
-//   [kWsTiles] int arrival counters (zero between launches) | fp32 slice
-//   partials [units][8][rows] (rows = 16 or 32 per unit).
+//   [kWsTiles] int counters (zero between launches: tile arrivals, and the
+//   last two for the unit scheduler) | fp32 slice partials [units][8][rows]
+//   (rows = 16 or 32 per unit).
 // ksplit > 1 only happens when a chunk has fewer than kTargetUnits 32-row
 // tiles, and then (from the slicing rule of tc_shape) it has fewer than
 // 2 kTargetUnits 32-row units: twice as many 16-row ones, the same bytes.
@@ -1389,8 +1507,12 @@ StreamWork stream_work(const Shape& s, int N, int M) {
   return w;
 }
 
+// The last two counters of the workspace are the persistent kernel's unit
+// scheduler (grabbed units, finished warps); the tiles use the others.
+constexpr int kWsSched = kWsTiles - 2;
+
 bool workspace_fits(const Shape& s, const StreamWork& w) {
-  return s.ks == 1 || (w.tiles <= kWsTiles && (size_t)w.units * 8 * w.rows * 4 <= kWsPartBytes);
+  return s.ks == 1 || (w.tiles <= kWsSched && (size_t)w.units * 8 * w.rows * 4 <= kWsPartBytes);
 }
 
 cudaError_t launch_stream(const Maps& maps, StreamParams p, const StreamWork& w, DeviceInfo& d,
@@ -1493,24 +1615,34 @@ cudaError_t launch_tc(const LaunchArgs& a, const w4a16_plan& plan) {
   p.xpitch = 0;
   p.part = nullptr;
   p.cnt = nullptr;
+  p.sched = nullptr;
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DeviceInfo& d = device_info(dev);
   if (a.tc_path != 1) {
     const TilePlan tp = tile_plan(s, a.N, a.M, a.tc_path == 2);
-    if (tp.kc > 0) return launch_tile(a, s, tp, d);
+    if (tp.kc > 0) return launch_tile(a, s, tp, d, false);
     if (a.tc_path == 2) return cudaErrorInvalidConfiguration;
   }
   const StreamWork w = stream_work(s, a.N, a.M);
   Maps maps;
   if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, a.N, a.K, w.rows)) return e;
-  if (s.ks > 1) {
-    if (!workspace_fits(s, w)) return cudaErrorInvalidValue;
-    void* ws = nullptr;
-    if (cudaError_t e = workspace(dev, a.stream, &ws)) return e;
-    p.cnt = static_cast<int*>(ws);
-    p.part = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsCounterBytes);
-  }
+  if (!workspace_fits(s, w)) return cudaErrorInvalidValue;
+  void* ws = nullptr;
+  if (cudaError_t e = workspace(dev, a.stream, &ws)) return e;
+  p.cnt = static_cast<int*>(ws);
+  p.sched = p.cnt + kWsSched;
+  p.part = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsCounterBytes);
   return launch_stream(maps, p, w, d, a.stream, a.pdl);
+}
+
+// Tokens per chunk of the routed tile kernel: twice the mean per expert (at
+// least one, at most eight); an expert with more tokens takes more chunks
+// over the same resident weights.
+int routed_xcap(int T, int E) {
+  int x = 2 * cdiv(T, E);
+  if (x > T) x = T;
+  if (x > kMaxChunk) x = kMaxChunk;
+  return x < 1 ? 1 : x;
 }
 
 cudaError_t launch_tc_id(const LaunchArgs& a, const w4a16_plan& plan) {
@@ -1518,15 +1650,25 @@ cudaError_t launch_tc_id(const LaunchArgs& a, const w4a16_plan& plan) {
   const Shape s = tc_shape(a.N, a.K);
   int dev = 0;
   if (cudaError_t e = cudaGetDevice(&dev)) return e;
+  if (a.tc_path != 1) {  // the tile kernel in routed mode, where it fits
+    const TilePlan tp = tile_plan(s, a.N, routed_xcap(a.T, a.E), true);
+    if (tp.kc > 0) {
+      std::lock_guard<std::mutex> lk(g_dev_mu);
+      return launch_tile(a, s, tp, device_info(dev), true);
+    }
+  }
   RoutedParams p;
   p.x = a.x; p.S = a.S; p.B = a.B; p.y = a.y; p.ids = a.ids; p.flags = a.flags;
   p.N = a.N; p.K = a.K; p.T = a.T; p.E = a.E;
   p.nst = s.nst; p.sl = s.sl; p.ks = s.ks;
   p.warps = s.ks < kRoutedWarps ? s.ks : kRoutedWarps;
-  p.stages = 3;
-  while (p.stages > 2 && routed_smem(p.warps, p.stages, p.ks) > kSmemLimit) --p.stages;
-  while (p.warps > 1 && routed_smem(p.warps, p.stages, p.ks) > kSmemLimit) --p.warps;
-  const int smem = routed_smem(p.warps, p.stages, p.ks);
+  p.xcap = a.T < kMaxChunk ? a.T : kMaxChunk;  // a chunk never holds more tokens than there are
+  // a ring no deeper than the stages a warp has (all in flight at once), at most 3
+  const int per_warp = (s.ks + p.warps - 1) / p.warps * s.sl;
+  p.stages = per_warp < 3 ? per_warp : 3;
+  while (p.stages > 1 && routed_smem(p.warps, p.stages, p.ks, p.xcap) > kSmemLimit) --p.stages;
+  while (p.warps > 1 && routed_smem(p.warps, p.stages, p.ks, p.xcap) > kSmemLimit) --p.warps;
+  const int smem = routed_smem(p.warps, p.stages, p.ks, p.xcap);
   if (smem > kSmemLimit) return cudaErrorInvalidConfiguration;
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);
@@ -1583,6 +1725,7 @@ cudaError_t launch_tc_noalloc(const LaunchArgs& a) {
   p.xpitch = 0;
   p.part = nullptr;
   p.cnt = nullptr;
+  p.sched = nullptr;
   Maps maps;
   if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, a.N, a.K, w.rows)) return e;
   std::lock_guard<std::mutex> lk(g_dev_mu);
@@ -1592,12 +1735,14 @@ cudaError_t launch_tc_noalloc(const LaunchArgs& a) {
     if (cudaError_t e = cudaGetSymbolAddress((void**)&ptr, g_noalloc_scratch)) return e;
     g_noalloc_ptr[dev] = ptr;
   }
-  if (s.ks > 1) {
-    p.cnt = static_cast<int*>(g_noalloc_ptr[dev]);
-    p.part = reinterpret_cast<float*>(static_cast<char*>(g_noalloc_ptr[dev]) + kWsCounterBytes);
-    // the array keeps whatever the previous call left: the counters must start at zero
+  p.cnt = static_cast<int*>(g_noalloc_ptr[dev]);
+  p.sched = p.cnt + kWsSched;
+  p.part = reinterpret_cast<float*>(static_cast<char*>(g_noalloc_ptr[dev]) + kWsCounterBytes);
+  // The array keeps whatever the previous call left: the counters must start
+  // at zero (every launch also leaves them at zero when it completes).
+  if (s.ks > 1)
     if (cudaError_t e = cudaMemsetAsync(p.cnt, 0, (size_t)w.tiles * 4, a.stream)) return e;
-  }
+  if (cudaError_t e = cudaMemsetAsync(p.sched, 0, 2 * sizeof(int), a.stream)) return e;
   return launch_stream(maps, p, w, d, a.stream, a.pdl);
 }
 

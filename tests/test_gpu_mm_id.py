@@ -15,7 +15,7 @@ def _experts(seed, E, N, K):
     return hw, ops.W4Matrix.from_host(hw)
 
 
-@pytest.mark.parametrize("kernel", ["auto", "simt", "tc", "vanilla"])
+@pytest.mark.parametrize("kernel", ["auto", "simt", "tc", "vanilla", "tc_stream", "tc_tile"])
 def test_routed_experts_config(kernel):
     E, N, K = EXPERTS
     hw, w = _experts(0, E, N, K)
@@ -30,15 +30,45 @@ def test_routed_experts_config(kernel):
     assert ops.device_status() == 0
 
 
+@pytest.mark.parametrize("kernel", ["auto", "tc_stream"])
 @pytest.mark.parametrize("T,E", [(1, 1), (3, 5), (20, 3), (64, 8)])
-def test_routed_small_full(T, E):
+def test_routed_small_full(T, E, kernel):
     N, K = 70, 512
     hw, w = _experts(T * 10 + E, E, N, K)
     ids_np = synth.make_ids(T, T, E)
     xb = synth.make_x(E, T, K)
-    y = ops.mm_id(to_dev_bf16(xb), w, torch.from_numpy(ids_np).cuda())
+    y = ops.mm_id(to_dev_bf16(xb), w, torch.from_numpy(ids_np).cuda(), kernel=kernel)
     yr, ad = oracle.mm_id(xb, hw.Wq, hw.scales, hw.biases, ids_np, T, N, K, E)
-    assert_parity(y, yr, ad, f"mm_id T={T} E={E}")
+    assert_parity(y, yr, ad, f"mm_id T={T} E={E} {kernel}")
+
+
+@pytest.mark.parametrize("kernel", ["tc_tile", "tc_stream"])
+def test_bad_ids_tensor_core(kernel):
+    """Out-of-range ids on the tensor-core launch shapes (K % 512 == 0), with
+    several tiles per expert and an expert that takes two token chunks."""
+    E, N, K = 5, 100, 1024
+    hw, w = _experts(9, E, N, K)
+    ids_np = np.array([1, -1, 3, 7, 1, 1, 0, 99, 1, 4, -5], dtype=np.int32)
+    T = len(ids_np)
+    xb = synth.make_x(9, T, K)
+    y = torch.full((T, N), 7.0, dtype=torch.bfloat16, device="cuda")
+    ops.mm_id(to_dev_bf16(xb), w, torch.from_numpy(ids_np).cuda(), out=y, kernel=kernel)
+    assert ops.device_status() & ops.DEVICE_BAD_ID
+    yr, ad = oracle.mm_id(xb, hw.Wq, hw.scales, hw.biases, ids_np, T, N, K, E)
+    assert_parity(y, yr, ad, f"bad ids {kernel}")
+    yb = bf16_bits(y)
+    for t in (1, 3, 7, 10):
+        assert np.all(yb[t] == 0)
+
+
+def test_routed_launch_shapes_agree_bitwise():
+    E, N, K, T = 6, 300, 2048, 37
+    _, w = _experts(11, E, N, K)
+    ids = torch.from_numpy(synth.make_ids(11, T, E)).cuda()
+    x = to_dev_bf16(synth.make_x(11, T, K))
+    a = bf16_bits(ops.mm_id(x, w, ids, kernel="tc_tile"))
+    b = bf16_bits(ops.mm_id(x, w, ids, kernel="tc_stream"))
+    assert np.array_equal(a, b)
 
 
 def test_bad_ids_give_zero_rows_and_raise_the_flag():
