@@ -46,6 +46,11 @@ DECODE_LAYER = [("q", 2048, 2560), ("k", 512, 2560), ("v", 512, 2560), ("o", 256
                 ("gate", 10240, 2560), ("up", 10240, 2560), ("down", 2560, 10240)]
 WORKLOAD = ("W4A16 g64 decode-layer projection set at M=1, hidden 2560: q 2048x2560, k 512x2560, "
             "v 512x2560, o 2560x2048, gate 10240x2560, up 10240x2560, down 2560x10240")
+# The launches of one step.  A decoder layer's q/k/v projections are
+# independent given their input, as are gate/up; they go through one
+# w4a16_mm_group call each.  o and down depend on earlier results (attention,
+# the gated activation) and run as their own w4a16_mm calls.
+LAUNCHES = [("qkv", ("q", "k", "v")), ("o", ("o",)), ("gate_up", ("gate", "up")), ("down", ("down",))]
 # Single workloads for --case: name -> (N, K, E)
 CASES = {"q": (2048, 2560, 1), "kv": (512, 2560, 1), "o": (2560, 2048, 1), "gate": (10240, 2560, 1),
          "down": (2560, 10240, 1), "wide_up": (12288, 1536, 1), "wide_down": (1536, 12288, 1),
@@ -64,6 +69,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--kernel", default="auto", help="auto | simt | tc | vanilla")
     ap.add_argument("--no-extras", action="store_true", help="skip the per-config context measurements")
+    ap.add_argument("--ungrouped", action="store_true", help="time the layer as seven w4a16_mm calls")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work budget of the oracle baseline")
     ap.add_argument("--case", default=None,
@@ -249,13 +255,19 @@ def run_ours(args, world, rank, local):
         make_ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
         external_ok = False
 
-    def enqueue_layer(layer, evs=None):
-        for i, (name, N, K) in enumerate(DECODE_LAYER):
+    grouped = not args.ungrouped and args.kernel == "auto"
+    launches = LAUNCHES if grouped else [(name, (name,)) for name, _, _ in DECODE_LAYER]
+
+    def enqueue_layer(layer, evs=None, launches=launches):
+        for i, (_, names) in enumerate(launches):
             if evs is not None:
                 evs[i].record()
-            ops.mm(xs[name], layer[name], out=ys[name], kernel=kernel)
+            if len(names) == 1:
+                ops.mm(xs[names[0]], layer[names[0]], out=ys[names[0]], kernel=kernel)
+            else:
+                ops.mm_group([xs[n] for n in names], [layer[n] for n in names], [ys[n] for n in names])
         if evs is not None:
-            evs[len(DECODE_LAYER)].record()
+            evs[len(launches)].record()
 
     graphs, ev_graphs, graph_events = [], [], []
     with torch.cuda.stream(stream):
@@ -269,7 +281,7 @@ def run_ours(args, world, rank, local):
             graphs.append(g)
             if external_ok:  # a twin graph with event nodes between the launches
                 ge = torch.cuda.CUDAGraph()
-                evs = [make_ev() for _ in range(len(DECODE_LAYER) + 1)]
+                evs = [make_ev() for _ in range(len(launches) + 1)]
                 with torch.cuda.graph(ge, stream=stream):
                     enqueue_layer(layer, evs)
                 ev_graphs.append(ge)
@@ -302,9 +314,14 @@ def run_ours(args, world, rank, local):
     ms_per_step = ms_total / args.steps
     value = world * step_bytes * args.steps / (ms_total * 1e-3) / 1e9
 
-    # Per-launch durations of the timed kernel, from a second pass over the
-    # same rotating layers whose graphs carry event nodes between launches.
-    launch_ms, launch_bytes = [], []
+    dims = {name: (N, K) for name, N, K in DECODE_LAYER}
+
+    def launch_bytes(names):
+        return sum(roofline.mm_bytes(1, *dims[n]) for n in names)
+
+    # Per-launch durations, from a second pass over the same rotating layers
+    # whose graphs carry event nodes between launches.
+    launch_ms = []
     if external_ok:
         with torch.cuda.stream(stream):
             for rep in range(3):
@@ -312,36 +329,58 @@ def run_ours(args, world, rank, local):
                     ge.replay()
         torch.cuda.synchronize()
         for evs in graph_events:
-            for i, (_, N, K) in enumerate(DECODE_LAYER):
-                launch_ms.append(evs[i].elapsed_time(evs[i + 1]))
-                launch_bytes.append(roofline.mm_bytes(1, N, K))
+            launch_ms.append([evs[i].elapsed_time(evs[i + 1]) for i in range(len(launches))])
     else:  # eager launches queued behind a spin kernel, so events bracket only the kernels
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(DECODE_LAYER) + 1)]
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(launches) + 1)]
         with torch.cuda.stream(stream):
             for layer in layers:
                 torch.cuda._sleep(50_000_000)
                 enqueue_layer(layer, evs)
                 torch.cuda.synchronize()
-                for i, (_, N, K) in enumerate(DECODE_LAYER):
-                    launch_ms.append(evs[i].elapsed_time(evs[i + 1]))
-                    launch_bytes.append(roofline.mm_bytes(1, N, K))
+                launch_ms.append([evs[i].elapsed_time(evs[i + 1]) for i in range(len(launches))])
     peak, peak_kind = measured_peak()
     # The dominant kernel is every launch of the step (the tile kernel runs all
-    # seven projections), and programmatic dependent launch overlaps each
-    # launch with its neighbours, so its average launch duration is the timed
-    # region over the launches in it, and its achieved rate is the step's
-    # algorithmic bytes over the step time.
-    launches_per_step = len(DECODE_LAYER)
+    # of them), and programmatic dependent launch overlaps each launch with its
+    # neighbours, so its average launch duration is the timed region over the
+    # launches in it, and its achieved rate is the step's algorithmic bytes
+    # over the step time.
+    launches_per_step = len(launches)
     launch_us = 1e3 * ms_total / (args.steps * launches_per_step)
     achieved = step_bytes / (launches_per_step * launch_us * 1e-6) / 1e9
-    per_matrix = {}
-    for i, (name, N, K) in enumerate(DECODE_LAYER):
-        ms = [launch_ms[j] for j in range(i, len(launch_ms), len(DECODE_LAYER))]
-        us = 1e3 * sum(ms) / len(ms)
-        per_matrix[name] = {"N": N, "K": K, "us": round(us, 3),
-                            "GBps": round(roofline.mm_bytes(1, N, K) / (us * 1e-6) / 1e9, 1)}
+    per_launch = {}
+    for i, (lname, names) in enumerate(launches):
+        us = 1e3 * sum(r[i] for r in launch_ms) / len(launch_ms)
+        per_launch[lname] = {"matrices": [f"{n} {dims[n][0]}x{dims[n][1]}" for n in names], "us": round(us, 3),
+                             "GBps": round(launch_bytes(names) / (us * 1e-6) / 1e9, 1)}
 
-    e2e = measure_e2e(torch, ops, layers, args.steps, kernel, step_bytes, world, dist)
+    # The same layer as seven separate w4a16_mm calls (context for the grouping).
+    ungrouped = None
+    if grouped and not args.no_extras:
+        seven = [(name, (name,)) for name, _, _ in DECODE_LAYER]
+        g7 = []
+        with torch.cuda.stream(stream):
+            for layer in layers:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    enqueue_layer(layer, launches=seven)
+                g7.append(g)
+            for s_ in range(args.warmup):
+                g7[s_ % len(g7)].replay()
+        torch.cuda.synchronize()
+        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n7 = max(1, min(args.steps, 5000))
+        with torch.cuda.stream(stream):
+            a_.record()
+            for s_ in range(n7):
+                g7[s_ % len(g7)].replay()
+            b_.record()
+        torch.cuda.synchronize()
+        ms7 = a_.elapsed_time(b_) / n7
+        ungrouped = {"launches_per_step": 7, "ms_per_step": round(ms7, 6),
+                     "GBps": round(step_bytes / (ms7 * 1e-3) / 1e9, 2)}
+        del g7
+
+    e2e = measure_e2e(torch, ops, layers, args.steps, kernel, step_bytes, world, dist, launches)
     extras = None if args.no_extras else measure_extras(torch, ops, synth, roofline, l2, kernel, peak)
 
     cpu = None
@@ -358,7 +397,9 @@ def run_ours(args, world, rank, local):
                        "kernel": plan["kernel"], "plan": plan,
                        "l2_policy": f"inputs larger than L2: {copies} rotating layer copies "
                                     f"({copies * weight_bytes / 1e6:.0f} MB > 3x L2 {l2 / 1e6:.0f} MB)",
-                       "cuda_graphs": True, "parallelism": f"replicas x{world}"},
+                       "cuda_graphs": True, "parallelism": f"replicas x{world}",
+                       "launches": [f"{ln}: " + ("w4a16_mm_group" if len(nm) > 1 else "w4a16_mm") + f"({', '.join(nm)})"
+                                    for ln, nm in launches]},
             "roofline": {"bound": "hbm", "kernel": DOMINANT_KERNEL, "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "traffic": ncu_traffic(DOMINANT_KERNEL),
@@ -370,13 +411,14 @@ def run_ours(args, world, rank, local):
                          "launches_timed": args.steps * launches_per_step,
                          "timing": "CUDA events around the timed region on the launching stream; "
                                    "average launch = region / launches (launches overlap)"},
-            "per_matrix_serialised": {
+            "per_launch_serialised": {
                 "timing": ("event nodes between the launches of twin graphs, replayed after the timed region; "
                            "the event nodes stop the launches from overlapping, so these are upper bounds"
                            if external_ok else "events behind a spin kernel"),
-                **per_matrix},
+                **per_launch},
+            "ungrouped_layer": ungrouped,
             "e2e": e2e,
-            "gpu_launches": args.steps * len(DECODE_LAYER),
+            "gpu_launches": args.steps * launches_per_step,
             "clocks": clocks,
         }
         if cpu is not None:
@@ -388,10 +430,11 @@ def run_ours(args, world, rank, local):
         dist.destroy_process_group()
 
 
-def measure_e2e(torch, ops, layers, steps, kernel, step_bytes, world, dist):
+def measure_e2e(torch, ops, layers, steps, kernel, step_bytes, world, dist, launches):
     """Through the public API, every step: pinned host -> device copy of the
-    step's activations, the seven calls, device -> pinned host read of the
-    outputs (with the synchronisation that read implies)."""
+    step's activations, the layer's calls (the same launches as the timed
+    region), device -> pinned host read of the outputs (with the
+    synchronisation that read implies)."""
     k_in = [K for _, N, K in DECODE_LAYER]
     n_out = [N for _, N, K in DECODE_LAYER]
     h_in = torch.empty(sum(k_in), dtype=torch.bfloat16, pin_memory=True)
@@ -406,11 +449,16 @@ def measure_e2e(torch, ops, layers, steps, kernel, step_bytes, world, dist):
         a, b = a + K, b + N
     n = max(1, min(steps, 5000))
 
+    idx = {name: i for i, (name, N, K) in enumerate(DECODE_LAYER)}
+
     def step(s):
         d_in.copy_(h_in, non_blocking=True)
         layer = layers[s % len(layers)]
-        for i, (name, N, K) in enumerate(DECODE_LAYER):
-            ops.mm(ins[i], layer[name], out=outs[i], kernel=kernel)
+        for _, names in launches:
+            if len(names) == 1:
+                ops.mm(ins[idx[names[0]]], layer[names[0]], out=outs[idx[names[0]]], kernel=kernel)
+            else:
+                ops.mm_group([ins[idx[n]] for n in names], [layer[n] for n in names], [outs[idx[n]] for n in names])
         h_out.copy_(d_out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
@@ -424,7 +472,8 @@ def measure_e2e(torch, ops, layers, steps, kernel, step_bytes, world, dist):
     dt = max_over_ranks(dist, time.perf_counter() - t0)
     return {"value": round(world * step_bytes * n / dt / 1e9, 2), "unit": UNIT,
             "h2d_bytes_per_step": int(h_in.numel() * 2), "d2h_bytes_per_step": int(h_out.numel() * 2),
-            "steps": n, "ms_per_step": round(1e3 * dt / n, 4), "api": "skinny_gemm_gb300.ops.mm (eager)"}
+            "steps": n, "ms_per_step": round(1e3 * dt / n, 4),
+            "api": "skinny_gemm_gb300.ops.mm / mm_group (eager, the C ABI through ctypes)"}
 
 
 def time_graph_launches(torch, fn_list, reps):

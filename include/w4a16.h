@@ -142,6 +142,34 @@ int w4a16_mm_kernel(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* s
 int w4a16_mm_noalloc(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* scales,
                      const w4a16_bf16* biases, w4a16_bf16* y, int M, int N, int K, void* stream);
 
+/* Grouped projections: several independent w4a16_mm calls that share K and
+ * M, in one launch where that pays (a decoder layer's q/k/v projections read
+ * the same activations, as do gate/up; launching them together saves the
+ * per-launch latency that dominates decode-sized matmuls).  No counterpart
+ * on the pages; each item is exactly the operation of w4a16_mm above.
+ *
+ * `items` is a HOST array of `count` (1..W4A16_MAX_GROUP) descriptors; the
+ * pointers inside are device pointers with w4a16_mm's layout and alignment
+ * (x [M][K], Wq [N][K/8], scales/biases [N][K/64], y [M][N]).  Items are
+ * independent: no item's y may overlap any other item's operands or y.  Row
+ * m of every item's y equals, bit for bit, w4a16_mm on that item.  When the
+ * shapes do not allow one launch (K % 512 != 0, or an item too large for the
+ * tile launch shape) the items run as consecutive w4a16_mm calls.  Errors
+ * are those of w4a16_mm, checked for every item before anything is
+ * launched; count outside 1..W4A16_MAX_GROUP is W4A16_ERR_SHAPE. */
+#define W4A16_MAX_GROUP 8
+
+typedef struct {
+  const w4a16_bf16* x;      /* [M][K] activations of this item */
+  const uint32_t* Wq;       /* [N][K/8] packed codes */
+  const w4a16_bf16* scales; /* [N][K/64] */
+  const w4a16_bf16* biases; /* [N][K/64] */
+  w4a16_bf16* y;            /* [M][N] output */
+  int N;                    /* output columns of this item */
+} w4a16_mm_item;
+
+int w4a16_mm_group(const w4a16_mm_item* items, int count, int M, int K, void* stream);
+
 /* Routed experts, top-1 (the W4A16 analogue of llama.cpp's mul_mat_id named
  * in [HY4] "What was missing and what this adds"):
  *   y[t][n] = sum_k x[t][k] * w_{ids[t]}[n][k]

@@ -279,6 +279,39 @@ int w4a16_mm_noalloc(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* 
   return W4A16_OK;
 }
 
+int w4a16_mm_group(const w4a16_mm_item* items, int count, int M, int K, void* stream) {
+  if (env().fault == kFaultValidate) return fail(W4A16_ERR_SHAPE, "injected validation fault (W4A16_FAULT)");
+  if (count < 1 || count > W4A16_MAX_GROUP)
+    return fail(W4A16_ERR_SHAPE, "count = %d must be in 1..%d", count, W4A16_MAX_GROUP);
+  if (!items) return fail(W4A16_ERR_NULL, "null item array");
+  int Ns[W4A16_MAX_GROUP];
+  for (int i = 0; i < count; ++i) {
+    const w4a16_mm_item& it = items[i];
+    if (int rc = validate_mm(it.x, it.Wq, it.scales, it.biases, it.y, M, it.N, K)) return rc;
+    Ns[i] = it.N;
+  }
+  if (M == 0) return W4A16_OK;
+  if (env().force_kernel != W4A16_KERNEL_AUTO || !tc_group_supported(Ns, count, K)) {
+    for (int i = 0; i < count; ++i) {
+      const w4a16_mm_item& it = items[i];
+      if (int rc = run_mm(it.x, it.Wq, it.scales, it.biases, it.y, M, it.N, K, W4A16_KERNEL_AUTO, stream)) return rc;
+    }
+    return W4A16_OK;
+  }
+  if (env().fault == kFaultLaunch) return fail(W4A16_ERR_CUDA, "injected launch fault (W4A16_FAULT)");
+  int* flags = nullptr;
+  if (int rc = flag_pointer(&flags)) return rc;
+  GroupItem g[W4A16_MAX_GROUP];
+  for (int i = 0; i < count; ++i)
+    g[i] = GroupItem{items[i].x, items[i].Wq, items[i].scales, items[i].biases, items[i].y, items[i].N};
+  for (int row0 = 0; row0 < M; row0 += kMaxChunk) {
+    const int mc = (M - row0 < kMaxChunk) ? M - row0 : kMaxChunk;
+    cudaError_t e = launch_tc_group(g, count, mc, row0, K, env().pdl, flags, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "w4a16_mm_group launch");
+  }
+  return W4A16_OK;
+}
+
 int w4a16_get_plan(int N, int K, int kernel, w4a16_plan* out) {
   if (!out) return fail(W4A16_ERR_NULL, "null plan pointer");
   if (int rc = check_nk(N, K)) return rc;

@@ -43,6 +43,18 @@ bool tc_supported(int N, int K);
 bool tc_tile_fits(int N, int K, int M);
 cudaError_t launch_tc(const LaunchArgs& a, const w4a16_plan& p);
 cudaError_t launch_tc_id(const LaunchArgs& a, const w4a16_plan& p);
+// Grouped tensor-core launch (w4a16_mm_group): items sharing K and M.
+struct GroupItem {
+  const uint16_t* x;
+  const uint32_t* Wq;
+  const uint16_t* S;
+  const uint16_t* B;
+  uint16_t* y;
+  int N;
+};
+bool tc_group_supported(const int* N, int count, int K);
+cudaError_t launch_tc_group(const GroupItem* items, int count, int M, int row0, int K, int pdl, int* flags,
+                            cudaStream_t stream);
 // Tensor-core w4a16_mm with its split-K scratch in a fixed device array (no allocation).
 cudaError_t launch_tc_noalloc(const LaunchArgs& a);
 size_t tc_noalloc_scratch_bytes();

@@ -89,6 +89,9 @@ namespace {
 #ifndef W4A16_TC_STREAM_NSUB1_MIN_M
 #define W4A16_TC_STREAM_NSUB1_MIN_M 9  // smallest chunk the persistent kernel runs with 16-row warps
 #endif
+#ifndef W4A16_TC_TILE_SLICES_PER_WARP
+#define W4A16_TC_TILE_SLICES_PER_WARP 1  // K-slices one warp of the tile kernel computes (in turn)
+#endif
 #ifndef W4A16_TC_TILE_SLICES
 #define W4A16_TC_TILE_SLICES 5        // most K-slices one CTA of the tile kernel takes, where a cluster can split
 #endif
@@ -267,18 +270,18 @@ struct Maps {
   CUtensorMap biases;
 };
 
-// The weight part of a stage: codes (two boxes) and the 8 groups' scales and
-// biases of 16 * NSUB rows from tensor_row, into slot memory dst; arms `bar`
+// The weight part of a stage: codes (two boxes, to dst) and the 8 groups'
+// scales and biases (to pdst) of 16 * NSUB rows from tensor_row; arms `bar`
 // for those bytes plus `mc` activation chunks still to come.
 template <int NSUB>
-__device__ __forceinline__ void issue_weights(uint32_t dst, uint32_t bar, const Maps* maps, int st, int tensor_row,
-                                              int mc, uint64_t pol_stream, uint64_t pol_keep) {
+__device__ __forceinline__ void issue_weights(uint32_t dst, uint32_t pdst, uint32_t bar, const Maps* maps, int st,
+                                              int tensor_row, int mc, uint64_t pol_stream, uint64_t pol_keep) {
   using G = Geo<NSUB>;
   mbar_expect_tx(bar, 2 * G::kBox + 2 * G::kParam + (uint32_t)(mc * kStageK * 2));
   tma_load_2d(dst, &maps->codes, st * kStageWords, tensor_row, bar, pol_stream);
   tma_load_2d(dst + G::kBox, &maps->codes, st * kStageWords + kBoxWords, tensor_row, bar, pol_stream);
-  tma_load_2d(dst + 2 * G::kBox, &maps->scales, st * 8, tensor_row, bar, pol_keep);
-  tma_load_2d(dst + 2 * G::kBox + G::kParam, &maps->biases, st * 8, tensor_row, bar, pol_keep);
+  tma_load_2d(pdst, &maps->scales, st * 8, tensor_row, bar, pol_keep);
+  tma_load_2d(pdst + G::kParam, &maps->biases, st * 8, tensor_row, bar, pol_keep);
 }
 
 // The activation part of a stage: 512 bf16 of each row toks[0..mc) into rows
@@ -294,8 +297,9 @@ __device__ __forceinline__ void issue_x(uint32_t xdst, uint32_t bar, int st, con
 template <int NSUB>
 __device__ __forceinline__ uint32_t ring_issue_w(Ring& R, const Maps* maps, int st, int tensor_row, int mc) {
   const uint32_t slot = R.issued % (uint32_t)R.S;
-  issue_weights<NSUB>(R.codes0 + slot * Geo<NSUB>::kSlot, R.bars0 + 8 * slot, maps, st, tensor_row, mc,
-                      R.pol_stream, R.pol_keep);
+  const uint32_t dst = R.codes0 + slot * Geo<NSUB>::kSlot;
+  issue_weights<NSUB>(dst, dst + 2 * Geo<NSUB>::kBox, R.bars0 + 8 * slot, maps, st, tensor_row, mc, R.pol_stream,
+                      R.pol_keep);
   ++R.issued;
   return slot;
 }
@@ -366,19 +370,20 @@ __device__ __forceinline__ void ldsm_offsets(int lane, uint32_t (&off)[2][4]) {
 // chains interleaved.  With ALLCOLS false (one activation row) the odd
 // columns are not rescaled; the even columns' arithmetic is unchanged.
 template <int NSUB, bool ALLCOLS, bool XSTAGED>
-__device__ __forceinline__ void compute_stage(uint32_t cbase, uint32_t xbase, bool xvalid, uint32_t sxbase,
-                                              uint32_t sx_stride, bool xvalid_cols, float (&p)[NSUB][4],
-                                              const uint32_t (&loff)[NSUB][4], int g) {
+__device__ __forceinline__ void compute_stage(uint32_t cbase, uint32_t pbase, uint32_t xbase, bool xvalid,
+                                              uint32_t sxbase, uint32_t sx_stride, bool xvalid_cols,
+                                              float (&p)[NSUB][4], const uint32_t (&loff)[NSUB][4], int g) {
   constexpr int GB = W4A16_TC_GROUP_BATCH;
-  // Slot layout for 16 * NSUB rows: two code boxes, then scales, then biases.
-  constexpr uint32_t kBox = 16 * NSUB * 128, kScales = 2 * kBox, kBiases = kScales + 16 * NSUB * 16;
+  // Codes: two boxes of 16 * NSUB rows x 128 bytes at cbase; scales then
+  // biases (16 bytes per row) at pbase.
+  constexpr uint32_t kBox = 16 * NSUB * 128, kBiases = 16 * NSUB * 16;
   // scale / bias of the 8 groups for this lane's rows 16(i>>1) + g + 8(i&1)
   uint4 ps[2 * NSUB], pb[2 * NSUB];
 #pragma unroll
   for (int i = 0; i < 2 * NSUB; ++i) {
     const uint32_t r = 16 * (i >> 1) + g + 8 * (i & 1);
-    ps[i] = lds128(cbase + kScales + r * 16);
-    pb[i] = lds128(cbase + kBiases + r * 16);
+    ps[i] = lds128(pbase + r * 16);
+    pb[i] = lds128(pbase + kBiases + r * 16);
   }
 #pragma unroll
   for (int gp = 0; gp < 8; gp += GB) {
@@ -507,6 +512,7 @@ struct StreamParams {
   int stages;
   int xpitch;       // bytes per activation row of the pre-staged copy (0: per-stage copies)
   int prefetch;     // request the first weight stages before waiting for earlier kernels
+  int dyn;          // deal units after the first dynamically (else round-robin)
 };
 
 // Columns of the group-sum table: the even count >= mc (lane t reads columns 2t, 2t+1).
@@ -566,29 +572,33 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
   const int TW = gridDim.x * kW;
 
   // Work units of this warp.  The first is static (unit gw), so its weights
-  // can be requested before the wait for earlier kernels; every later one is
-  // grabbed from a counter in the workspace (unit TW + count) as soon as the
-  // previous one starts streaming, so warps on faster SMs take more units.
-  // Lane 0 streams the units in order and records each in s_units (a ring
-  // of 8 per warp, ahead of the computing lanes by at most S stages); -1
-  // marks the end.
+  // can be requested before the wait for earlier kernels.  With p.dyn every
+  // later one is grabbed from a counter in the workspace (unit TW + count) as
+  // soon as the previous one starts streaming, so warps that run faster take
+  // more units; otherwise the warp takes units gw + TW, gw + 2 TW, ...
+  // Lane 0 streams the units in order; dealt ones it records in s_units (a
+  // ring of 8 per warp, ahead of the computing lanes by at most S stages;
+  // -1 marks the end).
   int* s_units = s_tok + kMaxChunk + 8 * warp;
   int iu = -1, ist = 0, iend = 0, nxt = -1;  // lane 0: unit being issued, its stage cursor, the next unit
+  int irow = 0;                              // lane 0: first weight row of unit iu
   uint32_t iseq = 0;
-  auto grab = [&]() {
-    const int v = TW + atomicAdd(p.sched, 1);
+  auto grab = [&]() {  // the unit after iu
+    const int v = p.dyn ? TW + atomicAdd(p.sched, 1) : iu + TW;
     return v < p.units ? v : -1;
   };
   auto begin_unit = [&](int u) {
     iu = u;
-    s_units[iseq++ & 7u] = u;
+    if (p.dyn) s_units[iseq++ & 7u] = u;
     if (u >= 0) {
-      ist = (u % p.ks) * p.sl;
+      const int tile = p.ks == 1 ? u : u / p.ks;  // one division per unit at most
+      irow = tile * kRows;
+      ist = (u - tile * p.ks) * p.sl;
       iend = min(ist + p.sl, p.nst);
     }
   };
   auto issue_stage = [&](bool with_x) {
-    const uint32_t slot = ring_issue_w<NSUB>(R, &maps, ist, (iu / p.ks) * kRows, xring);
+    const uint32_t slot = ring_issue_w<NSUB>(R, &maps, ist, irow, xring);
     if (with_x) ring_issue_x(R, slot, ist, p.x, s_tok, xring, p.K);
     ++ist;
   };
@@ -616,7 +626,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
   if (lane == 0) {
     if (iu >= 0) {
       nxt = grab();
-      const int first = (iu % p.ks) * p.sl;
+      const int first = ist - (int)R.issued;  // the unit's first stage
       for (uint32_t i = 0; i < R.issued; ++i) ring_issue_x(R, i, first + (int)i, p.x, s_tok, xring, p.K);
     }
     for (int i = (int)R.issued; i < S; ++i) issue_next(true);
@@ -741,12 +751,18 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
     for (int i = 0; i < 2 * NSUB; ++i) pr[i] = tile * kRows + 16 * (i >> 1) + g + 8 * (i & 1);
   };
 
-  // consume cursor: the units in the order lane 0 recorded them
+  // consume cursor: round-robin units follow from gw; dealt ones are read
+  // in the order lane 0 recorded them
+  int u = gw;
   for (uint32_t cseq = 0; !timed_out; ++cseq) {
-    __syncwarp();
-    const int u = s_units[cseq & 7u];
-    if (u < 0) break;
-    const int tile = u / p.ks, slice = u - tile * p.ks;
+    if (p.dyn) {
+      __syncwarp();
+      u = s_units[cseq & 7u];
+    } else if (cseq > 0) {
+      u += TW;
+    }
+    if (u < 0 || u >= p.units) break;
+    const int tile = p.ks == 1 ? u : u / p.ks, slice = u - tile * p.ks;
     const int s0 = slice * p.sl, s1 = min(s0 + p.sl, p.nst);
     int prow[2 * NSUB];
     rows_of(tile, prow);
@@ -771,7 +787,8 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
       } else {
         xbase = ordered(R.xs0 + slot * x_slot + g * kXPitch + 16 * t);
       }
-      compute_stage<NSUB, ALLCOLS, XSTAGED>(cbase, xbase, g < mc, sxbase, sx_cols(mc) * 4, 2 * t < mc, acc, loff, g);
+      compute_stage<NSUB, ALLCOLS, XSTAGED>(cbase, cbase + 2 * G::kBox, xbase, g < mc, sxbase, sx_cols(mc) * 4,
+                                            2 * t < mc, acc, loff, g);
       ++R.consumed;
       __syncwarp();
       if (lane == 0) {
@@ -836,10 +853,11 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
       ++R.consumed;
     }
   }
-  // The last warp out resets the unit counters for the next launch (every
-  // warp has made its last grab before it counts itself out).
+  // With dynamic dealing the last warp out resets the unit counters for the
+  // next launch (every warp has made its last grab before it counts itself
+  // out); round-robin dealing leaves them untouched at zero.
   __syncwarp();
-  if (lane == 0) {
+  if (p.dyn && lane == 0) {
     __threadfence();
     if (atomicAdd(p.sched + 1, 1) == TW - 1) {
       __threadfence();
@@ -861,16 +879,27 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
 // atomics or global fences.
 
 constexpr int kTile16 = Geo<1>::kRows;
-constexpr int kSlot16 = Geo<1>::kSlot;   // codes 2 x 2 KB | scales 256 | biases 256 | pad (1 KB alignment)
 constexpr int kTileMaxWarps = 16;
 constexpr int kMaxCluster = 8;
 
+// Operands of the tile kernel per item: one item for w4a16_mm and
+// w4a16_mm_id, up to kMaxGroup for w4a16_mm_group (items share K, M and
+// hence the slicing).
+constexpr int kMaxGroup = W4A16_MAX_GROUP;
+template <int G>
+struct TileArgs {
+  Maps maps[G];
+  const uint16_t* x[G];
+  uint16_t* y[G];
+  int N[G];
+  int tile0[G + 1];  // first 16-row tile of item i in the grid; tile0[items] = all tiles
+};
+
 struct TileParams {
-  const uint16_t* x;
-  uint16_t* y;
   int* flags;
   const int32_t* ids;  // routed mode: expert id per token
-  int N, K, M, row0;   // plain mode: rows row0 .. row0 + M of x (M <= xcap)
+  int items;           // items in TileArgs
+  int K, M, row0;      // plain mode: rows row0 .. row0 + M of x (M <= xcap)
   int T, E;            // routed mode: tokens, experts
   int nst, sl, ks;
   int kc;        // CTAs (one cluster) per 16-row tile
@@ -879,12 +908,14 @@ struct TileParams {
   int prefetch;  // request the weights before waiting for earlier kernels
 };
 
-// Shared memory (the same layout in every CTA of a cluster): slots
-// [nloc][kSlot16] | activation chunks [nloc][xcap][kXPitch] | barriers
-// [nloc] | slice sums [ks][16][8] fp32 (used in the first CTA) | tokens [8],
-// abort flag, token-scan state [2].
+// Shared memory (the same layout in every CTA of a cluster): codes
+// [nloc][4096] | scales and biases [nloc][512] | activation chunks
+// [nloc][xcap][kXPitch] | barriers [nloc] | slice sums [ks][16][xcap] fp32
+// (used in the first CTA) | tokens [8], abort flag, token-scan state [2].
+constexpr int kCodes16 = 2 * Geo<1>::kBox;    // 4096
+constexpr int kParams16 = 2 * Geo<1>::kParam;  // 512
 __host__ __device__ inline int tile_smem(int nloc, int xcap, int ks) {
-  return nloc * (kSlot16 + xcap * kXPitch) + nloc * 8 + ks * kTile16 * 8 * 4 + 64 + 1024;
+  return nloc * (kCodes16 + kParams16 + xcap * kXPitch) + nloc * 8 + ks * kTile16 * xcap * 4 + 64 + 1024;
 }
 
 __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
@@ -917,26 +948,35 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
 //
 // The bound of 768 threads caps registers at 80, so that five CTAs of five
 // warps fit on an SM (by registers).
-template <bool ALLCOLS, bool ROUTED>
-__global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Maps maps, TileParams p) {
+template <bool ALLCOLS, bool ROUTED, int G>
+__global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ TileArgs<G> ta, TileParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, W = blockDim.x >> 5;
   const int g = lane >> 2, t = lane & 3;
   const int kc = p.kc;
   // with cluster dimensions (kc, 1, 1) the rank in the cluster is blockIdx.x % kc
-  const int tile = blockIdx.x / kc, crank = blockIdx.x - tile * kc;
+  const int tile_g = blockIdx.x / kc, crank = blockIdx.x - tile_g * kc;
+  int item = 0;
+  if (G > 1)
+    while (item + 1 < p.items && tile_g >= ta.tile0[item + 1]) ++item;
+  const int tile = tile_g - ta.tile0[item];
+  const Maps& maps = ta.maps[item];
+  const uint16_t* __restrict__ xin = ta.x[item];
+  uint16_t* __restrict__ yout = ta.y[item];
+  const int N = ta.N[item];
   const int j0 = crank * p.ks / kc, j1 = (crank + 1) * p.ks / kc;  // this CTA's slices
   const int st0 = j0 * p.sl, nloc = min(j1 * p.sl, p.nst) - st0;  // and stages
   const int e = ROUTED ? (int)blockIdx.y : 0;
   const int tile_row = tile * kTile16;
-  const int tensor_row = e * p.N + tile_row;  // row of the stacked [E][N] weights
-  const int x_slot = p.xcap * kXPitch;
+  const int tensor_row = e * N + tile_row;  // row of the stacked [E][N] weights
+  const int x_slot = p.xcap * kXPitch, xcap = p.xcap;
   const uint32_t codes0 = smem_u32(base);
-  const uint32_t xs0 = codes0 + (uint32_t)(p.nloc * kSlot16);
+  const uint32_t params0 = codes0 + (uint32_t)(p.nloc * kCodes16);
+  const uint32_t xs0 = params0 + (uint32_t)(p.nloc * kParams16);
   const uint32_t bars0 = xs0 + (uint32_t)(p.nloc * x_slot);
   float* red = reinterpret_cast<float*>(base + (bars0 - codes0) + p.nloc * 8);
-  int* s_tok = reinterpret_cast<int*>(red + p.ks * kTile16 * 8);
+  int* s_tok = reinterpret_cast<int*>(red + p.ks * kTile16 * xcap);
   int* s_abort = s_tok + kMaxChunk;
   int* s_state = s_abort + 1;  // token scan: [0] position, [1] count
 
@@ -951,8 +991,8 @@ __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Ma
 
   // lane 0 of warp w requests local stages w, w + W, ...
   auto weights = [&](int i, int xrows) {
-    issue_weights<1>(codes0 + i * kSlot16, bars0 + 8 * i, &maps, st0 + i, tensor_row, xrows, policy_evict_first(),
-                     policy_evict_last());
+    issue_weights<1>(codes0 + i * kCodes16, params0 + i * kParams16, bars0 + 8 * i, &maps, st0 + i, tensor_row, xrows,
+                     policy_evict_first(), policy_evict_last());
   };
   if (!ROUTED && lane == 0 && p.prefetch)
     for (int i = warp; i < nloc; i += W) weights(i, p.M);
@@ -972,7 +1012,7 @@ __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Ma
         if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(p.flags, W4A16_DEVICE_BAD_ID);
         for (int i = threadIdx.x; i < cnt * kTile16; i += blockDim.x) {
           const int row = tile_row + i % kTile16;
-          if (row < p.N) p.y[(int64_t)s_tok[i / kTile16] * p.N + row] = 0;
+          if (row < N) yout[(int64_t)s_tok[i / kTile16] * N + row] = 0;
         }
         __syncthreads();
       }
@@ -987,7 +1027,7 @@ __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Ma
   if (lane == 0)
     for (int i = warp; i < nloc; i += W) {
       if (ROUTED || !p.prefetch) weights(i, mc);
-      issue_x(xs0 + i * x_slot, bars0 + 8 * i, st0 + i, p.x, s_tok, mc, p.K, policy_evict_last());
+      issue_x(xs0 + i * x_slot, bars0 + 8 * i, st0 + i, xin, s_tok, mc, p.K, policy_evict_last());
     }
 
   // slice sums go to the first CTA of the cluster, once every CTA of it runs
@@ -1024,14 +1064,17 @@ __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Ma
           ok = false;
           break;
         }
-        const uint32_t cbase = ordered(codes0 + i * kSlot16);
+        const uint32_t cbase = ordered(codes0 + i * kCodes16);
+        const uint32_t pbase = ordered(params0 + i * kParams16);
         const uint32_t xbase = ordered(xs0 + i * x_slot + g * kXPitch + 16 * t);
-        compute_stage<1, ALLCOLS, false>(cbase, xbase, g < mc, 0u, 0u, false, acc, loff, g);
+        compute_stage<1, ALLCOLS, false>(cbase, pbase, xbase, g < mc, 0u, 0u, false, acc, loff, g);
       }
       if (!ok) break;
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        st_cluster_f32(red_dst + 4 * ((j * kTile16 + g + 8 * (i >> 1)) * 8 + 2 * t + (i & 1)), acc[0][i]);
+      for (int i = 0; i < 4; ++i) {
+        const int n = 2 * t + (i & 1);
+        if (n < xcap) st_cluster_f32(red_dst + 4 * ((j * kTile16 + g + 8 * (i >> 1)) * xcap + n), acc[0][i]);
+      }
     }
     if (!ok && lane == 0 && *s_abort == 0) {
       atomicOr(p.flags, W4A16_DEVICE_TIMEOUT);
@@ -1043,10 +1086,10 @@ __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Ma
       for (int i = threadIdx.x; i < kTile16 * mc; i += blockDim.x) {
         const int n = i / kTile16, r = i - n * kTile16;
         const int row = tile_row + r;
-        if (row < p.N) {
-          float sum = red[r * 8 + n];
-          for (int j = 1; j < p.ks; ++j) sum = __fadd_rn(sum, red[(j * kTile16 + r) * 8 + n]);
-          p.y[(int64_t)s_tok[n] * p.N + row] = f32_to_bf16_bits(sum);
+        if (row < N) {
+          float sum = red[r * xcap + n];
+          for (int j = 1; j < p.ks; ++j) sum = __fadd_rn(sum, red[(j * kTile16 + r) * xcap + n]);
+          yout[(int64_t)s_tok[n] * N + row] = f32_to_bf16_bits(sum);
         }
       }
     }
@@ -1061,7 +1104,7 @@ __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Ma
         for (int i = warp; i < nloc; i += W) {
           fence_proxy_async();
           mbar_expect_tx(bars0 + 8 * i, (uint32_t)(mc * kStageK * 2));
-          issue_x(xs0 + i * x_slot, bars0 + 8 * i, st0 + i, p.x, s_tok, mc, p.K, policy_evict_last());
+          issue_x(xs0 + i * x_slot, bars0 + 8 * i, st0 + i, xin, s_tok, mc, p.K, policy_evict_last());
         }
       last_issued = chunk + 1;
     }
@@ -1167,7 +1210,7 @@ __global__ void __launch_bounds__(kRoutedWarps * 32) tc_routed_kernel(const __gr
         }
         const uint32_t cbase = ordered(R.codes0 + slot * kCodeSlotBytes);
         const uint32_t xbase = ordered(R.xs0 + slot * x_slot + g * kXPitch + 16 * t);
-        compute_stage<2, true, false>(cbase, xbase, g < mc, 0u, 0u, false, acc, loff, g);
+        compute_stage<2, true, false>(cbase, cbase + 2 * Geo<2>::kBox, xbase, g < mc, 0u, 0u, false, acc, loff, g);
         ++R.consumed;
         __syncwarp();
         if (lane == 0) {
@@ -1341,9 +1384,9 @@ int staged_stages(int M, int K) {
 // kernel of the stream (the kernels wait for it with griddepcontrol.wait
 // before touching anything it may have written), and with clusters of
 // `cluster` CTAs along x when cluster > 1.
-template <typename Kern, typename Params>
-cudaError_t launch_ex(Kern fn, dim3 grid, dim3 block, int smem, cudaStream_t stream, bool pdl, const Maps& maps,
-                      const Params& p, int cluster = 1) {
+template <typename Kern, typename... Args>
+cudaError_t launch_ex(Kern fn, dim3 grid, dim3 block, int smem, cudaStream_t stream, bool pdl, int cluster,
+                      const Args&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -1365,7 +1408,7 @@ cudaError_t launch_ex(Kern fn, dim3 grid, dim3 block, int smem, cudaStream_t str
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, fn, maps, p);
+  return cudaLaunchKernelEx(&cfg, fn, args...);
 }
 
 template <int NSUB, bool A, bool X>
@@ -1380,7 +1423,7 @@ cudaError_t stream_launch_t(const Maps& map, const StreamParams& p, int sms, int
   int grid = sms * per_sm;
   const int need = (p.units + kW - 1) / kW;
   if (grid > need) grid = need;
-  return launch_ex(fn, dim3(grid), dim3(kW * 32), smem, stream, pdl, map, p);
+  return launch_ex(fn, dim3(grid), dim3(kW * 32), smem, stream, pdl, 1, map, p);
 }
 
 // Persistent grid for one chunk: every SM filled to its occupancy, never more
@@ -1393,6 +1436,9 @@ cudaError_t launch_stream_t(const Maps& map, StreamParams p, int sms, DeviceInfo
   p.xpitch = staged ? 2 * p.K + 64 : 0;
   p.stages = staged ? staged_stages<NSUB>(p.M, p.K) : stream_stages<NSUB>(p.M);
   p.prefetch = pdl >= 2;
+  // Dynamic dealing pays where K is split (16384^2: 46 -> 44 us); without a
+  // split (the LM heads) round-robin was measured faster.
+  p.dyn = p.ks > 1;
   int smem = stream_smem<NSUB>(p.stages, staged ? 0 : p.M);
   if (staged) smem += xstage_bytes(p.M, p.K);
   const bool on = pdl > 0;
@@ -1443,7 +1489,8 @@ TilePlan tile_plan(const Shape& s, int N, int M, bool force) {
     tp.xcap = M;
     tp.kc = kc;
     tp.nloc = nloc;
-    tp.warps = ksl < kTileMaxWarps ? ksl : kTileMaxWarps;
+    const int warps = cdiv(ksl, W4A16_TC_TILE_SLICES_PER_WARP);
+    tp.warps = warps < kTileMaxWarps ? warps : kTileMaxWarps;
     tp.smem = smem;
     tp.ctas = tiles16 * kc;
     return tp;
@@ -1451,22 +1498,42 @@ TilePlan tile_plan(const Shape& s, int N, int M, bool force) {
   return tp;
 }
 
-cudaError_t launch_tile(const LaunchArgs& a, const Shape& s, const TilePlan& tp, DeviceInfo& d, bool routed) {
-  Maps maps;
-  const int64_t rows = routed ? (int64_t)a.N * a.E : a.N;
-  if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, rows, a.K, kTile16)) return e;
+TileParams tile_params(const Shape& s, const TilePlan& tp, int K, int M, int row0, int* flags, int pdl) {
   TileParams p;
-  p.x = a.x; p.y = a.y; p.flags = a.flags; p.ids = a.ids;
-  p.N = a.N; p.K = a.K; p.M = a.M; p.row0 = a.row0; p.T = a.T; p.E = a.E;
+  p.flags = flags;
+  p.ids = nullptr;
+  p.items = 1;
+  p.K = K; p.M = M; p.row0 = row0; p.T = 0; p.E = 1;
   p.nst = s.nst; p.sl = s.sl; p.ks = s.ks;
   p.kc = tp.kc;
   p.nloc = tp.nloc;
   p.xcap = tp.xcap;
-  p.prefetch = !routed && a.pdl >= 2;
-  auto* fn = routed ? tc_tile_kernel<true, true> : a.M > 1 ? tc_tile_kernel<true, false> : tc_tile_kernel<false, false>;
+  p.prefetch = pdl >= 2;
+  return p;
+}
+
+cudaError_t launch_tile(const LaunchArgs& a, const Shape& s, const TilePlan& tp, DeviceInfo& d, bool routed) {
+  TileArgs<1> ta;
+  const int64_t rows = routed ? (int64_t)a.N * a.E : a.N;
+  if (cudaError_t e = make_maps(&ta.maps[0], a.Wq, a.S, a.B, rows, a.K, kTile16)) return e;
+  ta.x[0] = a.x;
+  ta.y[0] = a.y;
+  ta.N[0] = a.N;
+  ta.tile0[0] = 0;
+  ta.tile0[1] = cdiv(a.N, kTile16);
+  TileParams p = tile_params(s, tp, a.K, a.M, a.row0, a.flags, a.pdl);
+  if (routed) {
+    p.ids = a.ids;
+    p.T = a.T;
+    p.E = a.E;
+    p.prefetch = 0;  // the weights to read depend on the ids
+  }
+  void (*fn)(TileArgs<1>, TileParams) = routed  ? tc_tile_kernel<true, true, 1>
+                                        : a.M > 1 ? tc_tile_kernel<true, false, 1>
+                                                  : tc_tile_kernel<false, false, 1>;
   if (cudaError_t e = allow_smem(fn, d)) return e;
   const dim3 grid(tp.ctas, routed ? a.E : 1);
-  return launch_ex(fn, grid, dim3(tp.warps * 32), tp.smem, a.stream, a.pdl > 0, maps, p, tp.kc);
+  return launch_ex(fn, grid, dim3(tp.warps * 32), tp.smem, a.stream, a.pdl > 0, tp.kc, ta, p);
 }
 
 std::mutex g_dev_mu;
@@ -1681,9 +1748,56 @@ cudaError_t launch_tc_id(const LaunchArgs& a, const w4a16_plan& plan) {
   }
   Maps maps;
   if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, (int64_t)a.N * a.E, a.K)) return e;
-  return launch_ex(tc_routed_kernel, dim3(s.tiles, a.E), dim3(p.warps * 32), smem, a.stream, a.pdl > 0, maps, p);
+  return launch_ex(tc_routed_kernel, dim3(s.tiles, a.E), dim3(p.warps * 32), smem, a.stream, a.pdl > 0, 1, maps, p);
 }
 
+bool tc_group_supported(const int* N, int count, int K) {
+  if (count < 1 || count > kMaxGroup || K % kStageK) return false;
+  for (int i = 0; i < count; ++i) {
+    const Shape s = tc_shape(N[i], K);
+    if (s.nst * s.tiles > W4A16_TC_TILE_MAX_UNITS) return false;  // each item alone would take the tile kernel
+  }
+  return tile_plan(tc_shape(N[0], K), N[0], kMaxChunk, false).kc > 0;
+}
+
+// One tile-kernel launch over items that share K and M: their tiles follow
+// one another in the grid; every item keeps its own canonical slicing (a
+// function of K alone for these shapes), so its rows equal a w4a16_mm call
+// on it bit for bit.
+cudaError_t launch_tc_group(const GroupItem* items, int count, int M, int row0, int K, int pdl, int* flags,
+                            cudaStream_t stream) {
+  int dev = 0;
+  if (cudaError_t e = cudaGetDevice(&dev)) return e;
+  const Shape s = tc_shape(items[0].N, K);
+  const TilePlan tp = tile_plan(s, items[0].N, M, false);
+  if (tp.kc == 0) return cudaErrorInvalidConfiguration;
+  TileArgs<kMaxGroup> ta;
+  int tiles = 0;
+  for (int i = 0; i < count; ++i) {
+    if (cudaError_t e = make_maps(&ta.maps[i], items[i].Wq, items[i].S, items[i].B, items[i].N, K, kTile16)) return e;
+    ta.x[i] = items[i].x;
+    ta.y[i] = items[i].y;
+    ta.N[i] = items[i].N;
+    ta.tile0[i] = tiles;
+    tiles += cdiv(items[i].N, kTile16);
+  }
+  for (int i = count; i < kMaxGroup; ++i) {
+    ta.maps[i] = ta.maps[0];
+    ta.x[i] = nullptr;
+    ta.y[i] = nullptr;
+    ta.N[i] = 0;
+    ta.tile0[i] = tiles;
+  }
+  ta.tile0[kMaxGroup] = tiles;
+  TileParams p = tile_params(s, tp, K, M, row0, flags, pdl);
+  p.items = count;
+  void (*fn)(TileArgs<kMaxGroup>, TileParams) =
+      M > 1 ? tc_tile_kernel<true, false, kMaxGroup> : tc_tile_kernel<false, false, kMaxGroup>;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = device_info(dev);
+  if (cudaError_t e = allow_smem(fn, d)) return e;
+  return launch_ex(fn, dim3(tiles * tp.kc), dim3(tp.warps * 32), tp.smem, stream, pdl > 0, tp.kc, ta, p);
+}
 
 // ---- no-allocation variant ----------------------------------------------------------------
 //

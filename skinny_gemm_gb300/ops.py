@@ -4,8 +4,8 @@ Every computation runs in the library's CUDA kernels.  PyTorch supplies the
 device memory, the current CUDA stream and the output allocation; there is
 no CPU or PyTorch fallback, and a missing or unbuildable library raises.
 
-Names follow the C ABI in ``include/w4a16.h``: ``mm``, ``mm_id``,
-``unpack``, ``dequant``, ``get_plan``, ``device_status``.
+Names follow the C ABI in ``include/w4a16.h``: ``mm``, ``mm_group``,
+``mm_id``, ``unpack``, ``dequant``, ``get_plan``, ``device_status``.
 """
 from __future__ import annotations
 
@@ -24,9 +24,10 @@ KERNELS = {"auto": 0, "simt": 1, "tc": 2, "vanilla": 3, "tc_stream": 4, "tc_tile
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 DEVICE_BAD_ID = 1
 
-EXPORTS = ("w4a16_mm", "w4a16_mm_kernel", "w4a16_mm_id", "w4a16_mm_id_kernel", "w4a16_unpack",
-           "w4a16_dequant", "w4a16_get_plan", "w4a16_device_status", "w4a16_last_error",
+EXPORTS = ("w4a16_mm", "w4a16_mm_kernel", "w4a16_mm_group", "w4a16_mm_id", "w4a16_mm_id_kernel",
+           "w4a16_unpack", "w4a16_dequant", "w4a16_get_plan", "w4a16_device_status", "w4a16_last_error",
            "w4a16_debug_reload_env", "w4a16_version")
+MAX_GROUP = 8
 
 
 class W4A16Error(RuntimeError):
@@ -52,6 +53,12 @@ class Plan(ctypes.Structure):
         return d
 
 
+class Item(ctypes.Structure):
+    """w4a16_mm_item: one projection of a w4a16_mm_group call (device pointers)."""
+    _fields_ = [("x", ctypes.c_void_p), ("Wq", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("biases", ctypes.c_void_p), ("y", ctypes.c_void_p), ("N", ctypes.c_int)]
+
+
 _lock = threading.Lock()
 _lib: ctypes.CDLL | None = None
 
@@ -71,14 +78,15 @@ def lib() -> ctypes.CDLL:
             L.w4a16_mm.argtypes = [P, P, P, P, P, i, i, i, P]
             L.w4a16_mm_kernel.argtypes = [P, P, P, P, P, i, i, i, i, P]
             L.w4a16_mm_noalloc.argtypes = [P, P, P, P, P, i, i, i, P]
+            L.w4a16_mm_group.argtypes = [ctypes.POINTER(Item), i, i, i, P]
             L.w4a16_mm_id.argtypes = [P, P, P, P, P, P, i, i, i, i, P]
             L.w4a16_mm_id_kernel.argtypes = [P, P, P, P, P, P, i, i, i, i, i, P]
             L.w4a16_unpack.argtypes = [P, P, i, i, P]
             L.w4a16_dequant.argtypes = [P, P, P, P, i, i, P]
             L.w4a16_get_plan.argtypes = [i, i, i, ctypes.POINTER(Plan)]
             L.w4a16_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
-            for f in ("w4a16_mm", "w4a16_mm_kernel", "w4a16_mm_noalloc", "w4a16_mm_id", "w4a16_mm_id_kernel", "w4a16_unpack",
-                      "w4a16_dequant", "w4a16_get_plan", "w4a16_device_status"):
+            for f in ("w4a16_mm", "w4a16_mm_kernel", "w4a16_mm_noalloc", "w4a16_mm_group", "w4a16_mm_id",
+                      "w4a16_mm_id_kernel", "w4a16_unpack", "w4a16_dequant", "w4a16_get_plan", "w4a16_device_status"):
                 getattr(L, f).restype = ctypes.c_int
             L.w4a16_last_error.restype = ctypes.c_char_p
             L.w4a16_version.restype = ctypes.c_char_p
@@ -186,6 +194,33 @@ def mm(x: torch.Tensor, w: W4Matrix, out: torch.Tensor | None = None, kernel=Non
         rc = L.w4a16_mm_kernel(*args, k, _stream_ptr(stream))
     _raise(rc)
     return out
+
+
+def mm_group(xs, ws, outs=None, stream=None) -> list:
+    """[mm(x, w) for x, w in zip(xs, ws)] through one ``w4a16_mm_group`` call.
+
+    The projections must share K and the number of activation rows M; each
+    result equals ``mm(x, w)`` bit for bit."""
+    xs, ws = list(xs), list(ws)
+    if not 1 <= len(xs) == len(ws) <= MAX_GROUP:
+        raise ValueError(f"need 1..{MAX_GROUP} (x, w) pairs")
+    K = ws[0].K
+    M = xs[0].numel() // K if K else 0
+    if outs is None:
+        outs = [torch.empty(*x.shape[:-1], w.N, dtype=torch.bfloat16, device=x.device) for x, w in zip(xs, ws)]
+    items = (Item * len(xs))()
+    for i, (x, w, y) in enumerate(zip(xs, ws, outs)):
+        if w.E != 1:
+            raise ValueError("mm_group takes single matrices")
+        _dev_tensor(x, torch.bfloat16, "x")
+        _dev_tensor(y, torch.bfloat16, "out")
+        if w.K != K or x.shape[-1] != K or x.numel() != M * K:
+            raise ValueError("every item must have the same K and the same number of rows")
+        if y.numel() != M * w.N:
+            raise ValueError("out has the wrong number of elements")
+        items[i] = Item(x.data_ptr(), w.Wq.data_ptr(), w.scales.data_ptr(), w.biases.data_ptr(), y.data_ptr(), w.N)
+    _raise(lib().w4a16_mm_group(items, len(xs), M, K, _stream_ptr(stream)))
+    return outs
 
 
 def mm_id(x: torch.Tensor, w: W4Matrix, ids: torch.Tensor, out: torch.Tensor | None = None, kernel=None,

@@ -169,3 +169,25 @@ def test_python_layer_rejects_host_tensors():
 
 def test_version_string(L):
     assert "sm_103a" in L.w4a16_version().decode()
+
+
+def _items(n, N=256, over=None):
+    arr = (ops.Item * max(n, 1))()
+    for i in range(n):
+        f = dict(x=P, Wq=P, scales=P, biases=P, y=P, N=N)
+        f.update((over or {}).get(i, {}))
+        arr[i] = ops.Item(**f)
+    return arr
+
+
+def test_mm_group_errors(L):
+    assert L.w4a16_mm_group(_items(2), 0, 1, 512, None) == ops.ERR_SHAPE
+    assert L.w4a16_mm_group(_items(9), 9, 1, 512, None) == ops.ERR_SHAPE
+    assert L.w4a16_mm_group(None, 2, 1, 512, None) == ops.ERR_NULL
+    assert L.w4a16_mm_group(_items(3), 3, 1, 100, None) == ops.ERR_SHAPE  # K % 64
+    assert L.w4a16_mm_group(_items(3, over={2: {"N": 0}}), 3, 1, 512, None) == ops.ERR_SHAPE
+    assert L.w4a16_mm_group(_items(3, over={1: {"y": None}}), 3, 1, 512, None) == ops.ERR_NULL
+    assert L.w4a16_mm_group(_items(3, over={1: {"x": P + 8}}), 3, 1, 512, None) == ops.ERR_ALIGN
+    # M == 0 is a no-op once every item is valid, and items are still checked
+    assert L.w4a16_mm_group(_items(3), 3, 0, 512, None) == ops.OK
+    assert L.w4a16_mm_group(_items(3, over={0: {"N": -1}}), 3, 0, 512, None) == ops.ERR_SHAPE
