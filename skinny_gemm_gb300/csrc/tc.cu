@@ -369,14 +369,15 @@ __device__ __forceinline__ void ldsm_offsets(int lane, uint32_t (&off)[2][4]) {
 // 2t+1).  GB groups at a time: their loads are issued first and their MMA
 // chains interleaved.  With ALLCOLS false (one activation row) the odd
 // columns are not rescaled; the even columns' arithmetic is unchanged.
-template <int NSUB, bool ALLCOLS, bool XSTAGED>
+template <int NSUB, bool ALLCOLS, bool XSTAGED, int BOXROWS = 16 * NSUB>
 __device__ __forceinline__ void compute_stage(uint32_t cbase, uint32_t pbase, uint32_t xbase, bool xvalid,
                                               uint32_t sxbase, uint32_t sx_stride, bool xvalid_cols,
                                               float (&p)[NSUB][4], const uint32_t (&loff)[NSUB][4], int g) {
   constexpr int GB = W4A16_TC_GROUP_BATCH;
-  // Codes: two boxes of 16 * NSUB rows x 128 bytes at cbase; scales then
-  // biases (16 bytes per row) at pbase.
-  constexpr uint32_t kBox = 16 * NSUB * 128, kBiases = 16 * NSUB * 16;
+  // Codes: two boxes of BOXROWS rows x 128 bytes at cbase (the warp's rows
+  // picked by loff); scales then biases (16 bytes per row, BOXROWS rows
+  // each) at pbase, pbase pointing at the warp's first row.
+  constexpr uint32_t kBox = BOXROWS * 128, kBiases = BOXROWS * 16;
   // scale / bias of the 8 groups for this lane's rows 16(i>>1) + g + 8(i&1)
   uint4 ps[2 * NSUB], pb[2 * NSUB];
 #pragma unroll
@@ -909,13 +910,14 @@ struct TileParams {
 };
 
 // Shared memory (the same layout in every CTA of a cluster): codes
-// [nloc][4096] | scales and biases [nloc][512] | activation chunks
-// [nloc][xcap][kXPitch] | barriers [nloc] | slice sums [ks][16][xcap] fp32
+// [nloc][4096 R] | scales and biases [nloc][512 R] | activation chunks
+// [nloc][xcap][kXPitch] | barriers [nloc] | slice sums [ks][16 R][xcap] fp32
 // (used in the first CTA) | tokens [8], abort flag, token-scan state [2].
-constexpr int kCodes16 = 2 * Geo<1>::kBox;    // 4096
-constexpr int kParams16 = 2 * Geo<1>::kParam;  // 512
-__host__ __device__ inline int tile_smem(int nloc, int xcap, int ks) {
-  return nloc * (kCodes16 + kParams16 + xcap * kXPitch) + nloc * 8 + ks * kTile16 * xcap * 4 + 64 + 1024;
+// R = 1 or 2 m16 row subtiles per CTA (16 or 32 rows): with R = 2 two warps,
+// one per subtile, share every stage's activation chunk.
+__host__ __device__ inline int tile_smem(int nloc, int xcap, int ks, int R = 1) {
+  return nloc * (R * (2 * Geo<1>::kBox + 2 * Geo<1>::kParam) + xcap * kXPitch) + nloc * 8 +
+         ks * kTile16 * R * xcap * 4 + 64 + 1024;
 }
 
 __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
@@ -948,8 +950,9 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
 //
 // The bound of 768 threads caps registers at 80, so that five CTAs of five
 // warps fit on an SM (by registers).
-template <bool ALLCOLS, bool ROUTED, int G>
+template <bool ALLCOLS, bool ROUTED, int G, int R>
 __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ TileArgs<G> ta, TileParams p) {
+  constexpr int kRowsR = 16 * R, kCodesR = 2 * R * Geo<1>::kBox, kParamsR = 2 * R * Geo<1>::kParam;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, W = blockDim.x >> 5;
@@ -968,15 +971,15 @@ __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Ti
   const int j0 = crank * p.ks / kc, j1 = (crank + 1) * p.ks / kc;  // this CTA's slices
   const int st0 = j0 * p.sl, nloc = min(j1 * p.sl, p.nst) - st0;  // and stages
   const int e = ROUTED ? (int)blockIdx.y : 0;
-  const int tile_row = tile * kTile16;
+  const int tile_row = tile * kRowsR;
   const int tensor_row = e * N + tile_row;  // row of the stacked [E][N] weights
   const int x_slot = p.xcap * kXPitch, xcap = p.xcap;
   const uint32_t codes0 = smem_u32(base);
-  const uint32_t params0 = codes0 + (uint32_t)(p.nloc * kCodes16);
-  const uint32_t xs0 = params0 + (uint32_t)(p.nloc * kParams16);
+  const uint32_t params0 = codes0 + (uint32_t)(p.nloc * kCodesR);
+  const uint32_t xs0 = params0 + (uint32_t)(p.nloc * kParamsR);
   const uint32_t bars0 = xs0 + (uint32_t)(p.nloc * x_slot);
   float* red = reinterpret_cast<float*>(base + (bars0 - codes0) + p.nloc * 8);
-  int* s_tok = reinterpret_cast<int*>(red + p.ks * kTile16 * xcap);
+  int* s_tok = reinterpret_cast<int*>(red + p.ks * kRowsR * xcap);
   int* s_abort = s_tok + kMaxChunk;
   int* s_state = s_abort + 1;  // token scan: [0] position, [1] count
 
@@ -991,7 +994,7 @@ __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Ti
 
   // lane 0 of warp w requests local stages w, w + W, ...
   auto weights = [&](int i, int xrows) {
-    issue_weights<1>(codes0 + i * kCodes16, params0 + i * kParams16, bars0 + 8 * i, &maps, st0 + i, tensor_row, xrows,
+    issue_weights<R>(codes0 + i * kCodesR, params0 + i * kParamsR, bars0 + 8 * i, &maps, st0 + i, tensor_row, xrows,
                      policy_evict_first(), policy_evict_last());
   };
   if (!ROUTED && lane == 0 && p.prefetch)
@@ -1010,9 +1013,9 @@ __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Ti
         const int cnt = gather_tokens(p.ids, p.T, p.E, -1, s_tok, s_state);
         if (cnt == 0) break;
         if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(p.flags, W4A16_DEVICE_BAD_ID);
-        for (int i = threadIdx.x; i < cnt * kTile16; i += blockDim.x) {
-          const int row = tile_row + i % kTile16;
-          if (row < N) yout[(int64_t)s_tok[i / kTile16] * N + row] = 0;
+        for (int i = threadIdx.x; i < cnt * kRowsR; i += blockDim.x) {
+          const int row = tile_row + i % kRowsR;
+          if (row < N) yout[(int64_t)s_tok[i / kRowsR] * N + row] = 0;
         }
         __syncthreads();
       }
@@ -1037,9 +1040,13 @@ __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Ti
     red_dst = map_to_rank(red_dst, 0);
     cluster_wait();
   }
+  // warp w computes subtile w % R (W is a multiple of R) of slices j0 + w / R, + W / R, ...
+  const int sub = R == 1 ? 0 : warp % R;
   uint32_t loff2[2][4];
   ldsm_offsets(lane, loff2);
-  const uint32_t loff[1][4] = {{loff2[0][0], loff2[0][1], loff2[0][2], loff2[0][3]}};
+  uint32_t loff[1][4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) loff[0][q] = sub ? loff2[1][q] : loff2[0][q];
   auto cta_sync = [&]() {
     __syncwarp();
     if (kc > 1) {
@@ -1055,7 +1062,7 @@ __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Ti
     // every stage barrier completes one phase per chunk (weights + x, then x)
     const uint32_t parity = chunk & 1u;
     bool ok = *s_abort == 0;
-    for (int j = j0 + warp; j < j1 && ok; j += W) {
+    for (int j = j0 + warp / R; j < j1 && ok; j += W / R) {
       float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
       const int s1 = min((j + 1) * p.sl, p.nst);
       for (int st = j * p.sl; st < s1; ++st) {
@@ -1064,16 +1071,17 @@ __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Ti
           ok = false;
           break;
         }
-        const uint32_t cbase = ordered(codes0 + i * kCodes16);
-        const uint32_t pbase = ordered(params0 + i * kParams16);
+        const uint32_t cbase = ordered(codes0 + i * kCodesR);
+        const uint32_t pbase = ordered(params0 + i * kParamsR + sub * kTile16 * 16);
         const uint32_t xbase = ordered(xs0 + i * x_slot + g * kXPitch + 16 * t);
-        compute_stage<1, ALLCOLS, false>(cbase, pbase, xbase, g < mc, 0u, 0u, false, acc, loff, g);
+        compute_stage<1, ALLCOLS, false, kRowsR>(cbase, pbase, xbase, g < mc, 0u, 0u, false, acc, loff, g);
       }
       if (!ok) break;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int n = 2 * t + (i & 1);
-        if (n < xcap) st_cluster_f32(red_dst + 4 * ((j * kTile16 + g + 8 * (i >> 1)) * xcap + n), acc[0][i]);
+        if (n < xcap)
+          st_cluster_f32(red_dst + 4 * ((j * kRowsR + kTile16 * sub + g + 8 * (i >> 1)) * xcap + n), acc[0][i]);
       }
     }
     if (!ok && lane == 0 && *s_abort == 0) {
@@ -1083,12 +1091,12 @@ __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Ti
     cta_sync();
     const bool aborted = *s_abort != 0;  // sticky: later chunks skip the work but keep the barriers
     if (crank == 0 && !aborted) {
-      for (int i = threadIdx.x; i < kTile16 * mc; i += blockDim.x) {
-        const int n = i / kTile16, r = i - n * kTile16;
+      for (int i = threadIdx.x; i < kRowsR * mc; i += blockDim.x) {
+        const int n = i / kRowsR, r = i - n * kRowsR;
         const int row = tile_row + r;
         if (row < N) {
           float sum = red[r * xcap + n];
-          for (int j = 1; j < p.ks; ++j) sum = __fadd_rn(sum, red[(j * kTile16 + r) * xcap + n]);
+          for (int j = 1; j < p.ks; ++j) sum = __fadd_rn(sum, red[(j * kRowsR + r) * xcap + n]);
           yout[(int64_t)s_tok[n] * N + row] = f32_to_bf16_bits(sum);
         }
       }
@@ -1459,12 +1467,23 @@ int stream_nsub(int M) { return M >= W4A16_TC_STREAM_NSUB1_MIN_M ? 1 : 2; }
 // Launch shape of the tile kernel for one chunk of M rows.
 struct TilePlan {
   int xcap = 0;   // activation rows per x slot
-  int kc = 0;     // CTAs per 16-row tile (cluster size); 0: the tile kernel does not apply
+  int R = 1;      // 16-row subtiles per CTA
+  int kc = 0;     // CTAs per row tile (cluster size); 0: the tile kernel does not apply
   int nloc = 0;   // stage slots per CTA
   int warps = 0;  // warps per CTA
   int smem = 0;   // dynamic shared memory per CTA
-  int ctas = 0;   // grid size
+  int ctas = 0;   // grid size (per expert for the routed mode)
 };
+
+// CTAs of the tile kernel (80 registers a thread at most) that fit on an SM.
+int tile_ctas_per_sm(int warps, int smem) {
+  int n = (228 * 1024) / (smem + 1024);
+  const int by_regs = 65536 / (warps * 32 * 80);
+  const int by_warps = 64 / warps;
+  if (by_regs < n) n = by_regs;
+  if (by_warps < n) n = by_warps;
+  return n < 32 ? n : 32;
+}
 
 // The tile kernel serves shapes whose canonical slices are single stages (a
 // persistent grid would give each warp about one unit); measured faster
@@ -1472,10 +1491,10 @@ struct TilePlan {
 // larger shapes.  A tile's slices are dealt to clusters of kc CTAs with at
 // most W4A16_TC_TILE_SLICES each; kc grows (up to 8) until a CTA fits in
 // shared memory.  `force` drops the size condition.
-TilePlan tile_plan(const Shape& s, int N, int M, bool force) {
+TilePlan tile_plan_r(const Shape& s, int N, int M, bool force, int R) {
   TilePlan tp;
   if (!force && s.nst * s.tiles > W4A16_TC_TILE_MAX_UNITS) return tp;
-  const int tiles16 = cdiv(N, kTile16);
+  const int tiles = cdiv(N, kTile16 * R);
   // Cluster sizes 1, 2, 3, 5 and 8 only: on 2560x10240 and 1536x12288, 5
   // beat 4, 6 and 7 (and 3 beat 4) by 10-40% (measured).
   static const int kSizes[] = {1, 2, 3, 5, 8};
@@ -1484,18 +1503,35 @@ TilePlan tile_plan(const Shape& s, int N, int M, bool force) {
     const int ksl = cdiv(s.ks, kc);
     if (ksl > W4A16_TC_TILE_SLICES && kc < kMaxCluster) continue;  // too many slices per CTA
     const int nloc = ksl * s.sl;
-    const int smem = tile_smem(nloc, M, s.ks);
+    const int smem = tile_smem(nloc, M, s.ks, R);
     if (smem > kSmemLimit) continue;
+    const int warps = R * cdiv(ksl, W4A16_TC_TILE_SLICES_PER_WARP);
+    if (warps > kTileMaxWarps) continue;
     tp.xcap = M;
+    tp.R = R;
     tp.kc = kc;
     tp.nloc = nloc;
-    const int warps = cdiv(ksl, W4A16_TC_TILE_SLICES_PER_WARP);
-    tp.warps = warps < kTileMaxWarps ? warps : kTileMaxWarps;
+    tp.warps = warps;
     tp.smem = smem;
-    tp.ctas = tiles16 * kc;
+    tp.ctas = tiles * kc;
     return tp;
   }
   return tp;
+}
+
+// With several activation rows, 32-row CTAs (R = 2) halve the activation
+// chunks per weight in shared memory; they are taken when they need fewer
+// waves of CTAs than 16-row ones (on 2560x10240 at M = 5 the 16-row CTAs no
+// longer fit in one wave).
+TilePlan tile_plan(const Shape& s, int N, int M, bool force, int sms = 152) {
+  const TilePlan one = tile_plan_r(s, N, M, force, 1);
+  if (M < 2) return one;
+  const TilePlan two = tile_plan_r(s, N, M, force, 2);
+  if (two.kc == 0) return one;
+  if (one.kc == 0) return two;
+  const int w1 = cdiv(one.ctas, sms * tile_ctas_per_sm(one.warps, one.smem));
+  const int w2 = cdiv(two.ctas, sms * tile_ctas_per_sm(two.warps, two.smem));
+  return w2 < w1 ? two : one;
 }
 
 TileParams tile_params(const Shape& s, const TilePlan& tp, int K, int M, int row0, int* flags, int pdl) {
@@ -1512,15 +1548,25 @@ TileParams tile_params(const Shape& s, const TilePlan& tp, int K, int M, int row
   return p;
 }
 
+// The tile kernel instance for (columns, mode, items, row subtiles).
+template <int G>
+using TileFn = void (*)(TileArgs<G>, TileParams);
+template <int G>
+TileFn<G> tile_fn(bool allcols, bool routed, int R) {
+  if (routed) return tc_tile_kernel<true, true, G, 1>;
+  if (R == 2) return allcols ? tc_tile_kernel<true, false, G, 2> : tc_tile_kernel<false, false, G, 2>;
+  return allcols ? tc_tile_kernel<true, false, G, 1> : tc_tile_kernel<false, false, G, 1>;
+}
+
 cudaError_t launch_tile(const LaunchArgs& a, const Shape& s, const TilePlan& tp, DeviceInfo& d, bool routed) {
   TileArgs<1> ta;
   const int64_t rows = routed ? (int64_t)a.N * a.E : a.N;
-  if (cudaError_t e = make_maps(&ta.maps[0], a.Wq, a.S, a.B, rows, a.K, kTile16)) return e;
+  if (cudaError_t e = make_maps(&ta.maps[0], a.Wq, a.S, a.B, rows, a.K, kTile16 * tp.R)) return e;
   ta.x[0] = a.x;
   ta.y[0] = a.y;
   ta.N[0] = a.N;
   ta.tile0[0] = 0;
-  ta.tile0[1] = cdiv(a.N, kTile16);
+  ta.tile0[1] = cdiv(a.N, kTile16 * tp.R);
   TileParams p = tile_params(s, tp, a.K, a.M, a.row0, a.flags, a.pdl);
   if (routed) {
     p.ids = a.ids;
@@ -1528,9 +1574,7 @@ cudaError_t launch_tile(const LaunchArgs& a, const Shape& s, const TilePlan& tp,
     p.E = a.E;
     p.prefetch = 0;  // the weights to read depend on the ids
   }
-  void (*fn)(TileArgs<1>, TileParams) = routed  ? tc_tile_kernel<true, true, 1>
-                                        : a.M > 1 ? tc_tile_kernel<true, false, 1>
-                                                  : tc_tile_kernel<false, false, 1>;
+  TileFn<1> fn = tile_fn<1>(a.M > 1, routed, tp.R);
   if (cudaError_t e = allow_smem(fn, d)) return e;
   const dim3 grid(tp.ctas, routed ? a.E : 1);
   return launch_ex(fn, grid, dim3(tp.warps * 32), tp.smem, a.stream, a.pdl > 0, tp.kc, ta, p);
@@ -1690,7 +1734,7 @@ cudaError_t launch_tc(const LaunchArgs& a, const w4a16_plan& plan) {
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DeviceInfo& d = device_info(dev);
   if (a.tc_path != 1) {
-    const TilePlan tp = tile_plan(s, a.N, a.M, a.tc_path == 2);
+    const TilePlan tp = tile_plan(s, a.N, a.M, a.tc_path == 2, d.sms);
     if (tp.kc > 0) return launch_tile(a, s, tp, d, false);
     if (a.tc_path == 2) return cudaErrorInvalidConfiguration;
   }
@@ -1722,7 +1766,7 @@ cudaError_t launch_tc_id(const LaunchArgs& a, const w4a16_plan& plan) {
   int dev = 0;
   if (cudaError_t e = cudaGetDevice(&dev)) return e;
   if (a.tc_path != 1) {  // the tile kernel in routed mode, where it fits
-    const TilePlan tp = tile_plan(s, a.N, routed_xcap(a.T, a.E), true);
+    const TilePlan tp = tile_plan_r(s, a.N, routed_xcap(a.T, a.E), true, 1);
     if (tp.kc > 0) {
       std::lock_guard<std::mutex> lk(g_dev_mu);
       return launch_tile(a, s, tp, device_info(dev), true);
@@ -1769,17 +1813,20 @@ cudaError_t launch_tc_group(const GroupItem* items, int count, int M, int row0, 
   int dev = 0;
   if (cudaError_t e = cudaGetDevice(&dev)) return e;
   const Shape s = tc_shape(items[0].N, K);
-  const TilePlan tp = tile_plan(s, items[0].N, M, false);
+  int Ntot = 0;
+  for (int i = 0; i < count; ++i) Ntot += cdiv(items[i].N, 32) * 32;
+  const TilePlan tp = tile_plan(s, Ntot, M, false);  // the plan depends on N only through the CTA count
   if (tp.kc == 0) return cudaErrorInvalidConfiguration;
+  const int rows = kTile16 * tp.R;
   TileArgs<kMaxGroup> ta;
   int tiles = 0;
   for (int i = 0; i < count; ++i) {
-    if (cudaError_t e = make_maps(&ta.maps[i], items[i].Wq, items[i].S, items[i].B, items[i].N, K, kTile16)) return e;
+    if (cudaError_t e = make_maps(&ta.maps[i], items[i].Wq, items[i].S, items[i].B, items[i].N, K, rows)) return e;
     ta.x[i] = items[i].x;
     ta.y[i] = items[i].y;
     ta.N[i] = items[i].N;
     ta.tile0[i] = tiles;
-    tiles += cdiv(items[i].N, kTile16);
+    tiles += cdiv(items[i].N, rows);
   }
   for (int i = count; i < kMaxGroup; ++i) {
     ta.maps[i] = ta.maps[0];
@@ -1791,8 +1838,7 @@ cudaError_t launch_tc_group(const GroupItem* items, int count, int M, int row0, 
   ta.tile0[kMaxGroup] = tiles;
   TileParams p = tile_params(s, tp, K, M, row0, flags, pdl);
   p.items = count;
-  void (*fn)(TileArgs<kMaxGroup>, TileParams) =
-      M > 1 ? tc_tile_kernel<true, false, kMaxGroup> : tc_tile_kernel<false, false, kMaxGroup>;
+  TileFn<kMaxGroup> fn = tile_fn<kMaxGroup>(M > 1, false, tp.R);
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DeviceInfo& d = device_info(dev);
   if (cudaError_t e = allow_smem(fn, d)) return e;
