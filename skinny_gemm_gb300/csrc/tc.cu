@@ -637,12 +637,12 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
   if (XSTAGED) {
     // Activation rows in B-fragment order, then the sum of every 64-group of
     // every row with the same MMA chain the per-stage path uses.
-    // Four chunks per thread per round, loads first, so their latencies overlap.
+    // Eight chunks per thread per round, loads first, so their latencies overlap.
     const int chunks = p.K / 8, total = mc * chunks;
-    for (int c0 = threadIdx.x; c0 < total; c0 += 4 * blockDim.x) {
-      uint4 u[4];
+    for (int c0 = threadIdx.x; c0 < total; c0 += 8 * blockDim.x) {
+      uint4 u[8];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < 8; ++j) {
         const int c = c0 + j * blockDim.x;
         if (c < total) {
           const int n = c / chunks, wd = c - n * chunks;
@@ -650,7 +650,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
         }
       }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < 8; ++j) {
         const int c = c0 + j * blockDim.x;
         if (c < total) {
           const int n = c / chunks, wd = c - n * chunks;
@@ -661,18 +661,23 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
       }
     }
     __syncthreads();
-    // Group sums, four groups per warp at a time with their MMA chains interleaved.
-    const int ngroups = p.K / kGroup;
-    for (int g0 = warp; g0 < ngroups; g0 += 4 * kW) {
+    // Group sums: one MMA chain yields eight groups of one activation row, the
+    // group in the MMA column (lanes with g = column load it).  An output
+    // column depends only on its own B column, so every sum has the bits of
+    // the per-stage chain (activation row in the column).  Four chains per
+    // warp at a time, interleaved.
+    const int nblk = p.K / kGroup / 8, tasks = mc * nblk;
+    for (int k0 = warp; k0 < tasks; k0 += 4 * kW) {
       uint32_t b[4][2][2][2];
       float v[4][4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int gi = g0 + j * kW;
+        const int k = k0 + j * kW;
+        const int n = k / nblk, blk = k - n * nblk;
 #pragma unroll
         for (int cb = 0; cb < 2; ++cb) {
           uint4 u = make_uint4(0, 0, 0, 0);
-          if (g < mc && gi < ngroups) u = lds128(xst + g * p.xpitch + 128 * gi + 64 * cb + 16 * t);
+          if (k < tasks) u = lds128(xst + n * p.xpitch + 128 * (8 * blk + g) + 64 * cb + 16 * t);
           b[j][cb][0][0] = u.x;
           b[j][cb][0][1] = u.y;
           b[j][cb][1][0] = u.z;
@@ -688,10 +693,12 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
           mma_bf16(v[j], kOnes, kOnes, kOnes, kOnes, b[j][step >> 1][step & 1][0], b[j][step >> 1][step & 1][1]);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int gi = g0 + j * kW;
-        if (g == 0 && 2 * t < mc && gi < ngroups) {
-          asm volatile("st.shared.v2.f32 [%0], {%1,%2};" ::"r"(sxs + (gi * sx_cols(mc) + 2 * t) * 4), "f"(v[j][0]),
-                       "f"(v[j][1])
+        const int k = k0 + j * kW;
+        const int n = k / nblk, blk = k - n * nblk;
+        if (g == 0 && k < tasks) {  // row 0 of D: columns 2t, 2t+1 are groups 8 blk + 2t, + 1
+          const int gi = 8 * blk + 2 * t;
+          asm volatile("st.shared.f32 [%0], %1;" ::"r"(sxs + (gi * sx_cols(mc) + n) * 4), "f"(v[j][0]) : "memory");
+          asm volatile("st.shared.f32 [%0], %1;" ::"r"(sxs + ((gi + 1) * sx_cols(mc) + n) * 4), "f"(v[j][1])
                        : "memory");
         }
       }
