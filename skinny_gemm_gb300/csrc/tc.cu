@@ -209,6 +209,12 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 
 // 16-byte global load cached in L2 only (activations another kernel may just
 // have written).
+__device__ __forceinline__ int ld_relaxed_gpu(const int* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
   uint4 v;
   asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
@@ -506,15 +512,37 @@ struct StreamParams {
   uint16_t* y;
   float* part;      // [units][8][rows] slice partials (ksplit > 1)
   int* cnt;         // [tiles] arrival counters, zero between launches
-  int* sched;       // [2] unit-grab and finished-warp counters, zero between launches
+  int* sched;       // [1] unit-grab counter, zero between launches
   int* flags;
   int N, K, M, row0;
   int nst, sl, ks, tiles, units;  // tiles and units of 16 * NSUB rows
+  int kfull;        // slices of full length per tile: ks, or ks - 1 when the last is shorter
   int stages;
   int xpitch;       // bytes per activation row of the pre-staged copy (0: per-stage copies)
   int prefetch;     // request the first weight stages before waiting for earlier kernels
   int dyn;          // deal units after the first dynamically (else round-robin)
 };
+
+// Tile and slice of work unit u.  Units whose slice has the full length come
+// first, tile-major; the shorter last slice of every tile (when the slice
+// length does not divide the stage count) comes after all of them, so the
+// units dealt last are the shortest and the warps finish closer together.
+// The order of the units changes no result: every partial has its fixed
+// place and the sums run in slice order.
+__device__ __forceinline__ int unit_tile(const StreamParams& p, int u, int& slice) {
+  if (p.ks == 1) {
+    slice = 0;
+    return u;
+  }
+  const int nfull = p.tiles * p.kfull;
+  if (u >= nfull) {
+    slice = p.ks - 1;
+    return u - nfull;
+  }
+  const int tile = u / p.kfull;  // one division per unit
+  slice = u - tile * p.kfull;
+  return tile;
+}
 
 // Columns of the group-sum table: the even count >= mc (lane t reads columns 2t, 2t+1).
 __host__ __device__ inline int sx_cols(int mc) { return (mc + 1) & ~1; }
@@ -580,21 +608,31 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
   // Lane 0 streams the units in order; dealt ones it records in s_units (a
   // ring of 8 per warp, ahead of the computing lanes by at most S stages;
   // -1 marks the end).
+  //
+  // Every warp with a first unit grabs until one grab fails, so a launch
+  // makes exactly max(0, units - TW) + min(TW, units) grabs; the one that
+  // draws the last count resets the counter for the next launch.  A grab's
+  // count is only looked at when its unit begins, a unit later, so the
+  // atomic's round trip never stalls the warp.
   int* s_units = s_tok + kMaxChunk + 8 * warp;
-  int iu = -1, ist = 0, iend = 0, nxt = -1;  // lane 0: unit being issued, its stage cursor, the next unit
-  int irow = 0;                              // lane 0: first weight row of unit iu
+  int iu = -1, ist = 0, iend = 0;  // lane 0: unit being issued, its stage cursor
+  int nxt = -1;                    // lane 0: count of the grab for the unit after iu (unit TW + nxt)
+  int irow = 0;                    // lane 0: first weight row of unit iu
   uint32_t iseq = 0;
-  auto grab = [&]() {  // the unit after iu
-    const int v = p.dyn ? TW + atomicAdd(p.sched, 1) : iu + TW;
+  const int last_grab = max(0, p.units - TW) + min(TW, p.units) - 1;
+  auto grab = [&]() { return p.dyn ? atomicAdd(p.sched, 1) : iu; };
+  auto resolve = [&](int c) {  // the unit of grab count c, -1 past the end
+    if (p.dyn && c == last_grab) *p.sched = 0;
+    const int v = TW + c;
     return v < p.units ? v : -1;
   };
   auto begin_unit = [&](int u) {
     iu = u;
     if (p.dyn) s_units[iseq++ & 7u] = u;
     if (u >= 0) {
-      const int tile = p.ks == 1 ? u : u / p.ks;  // one division per unit at most
-      irow = tile * kRows;
-      ist = (u - tile * p.ks) * p.sl;
+      int slice;
+      irow = unit_tile(p, u, slice) * kRows;
+      ist = slice * p.sl;
       iend = min(ist + p.sl, p.nst);
     }
   };
@@ -606,7 +644,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
   auto issue_next = [&](bool with_x) {  // after the wait only (grabs touch the workspace)
     if (iu < 0) return;
     if (ist == iend) {
-      begin_unit(nxt);
+      begin_unit(resolve(nxt));
       if (iu < 0) return;
       nxt = grab();
     }
@@ -770,8 +808,14 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
       u += TW;
     }
     if (u < 0 || u >= p.units) break;
-    const int tile = p.ks == 1 ? u : u / p.ks, slice = u - tile * p.ks;
+    int slice;
+    const int tile = unit_tile(p, u, slice);
     const int s0 = slice * p.sl, s1 = min(s0 + p.sl, p.nst);
+    // The last slice of a tile reads the tile's arrival count before its
+    // stages (the value is used after them, so the load never stalls).
+    const bool last_slice = p.ks > 1 && slice == p.ks - 1;
+    int seen = 0;
+    if (last_slice && lane == 0) seen = ld_relaxed_gpu(p.cnt + tile);
     int prow[2 * NSUB];
     rows_of(tile, prow);
 
@@ -829,7 +873,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
           if (n < mc && row < p.N) p.y[(int64_t)s_tok[n] * p.N + row] = f32_to_bf16_bits(acc[s][i]);
         }
     } else {
-      float* q = p.part + (int64_t)u * 8 * kRows;
+      float* q = p.part + ((int64_t)tile * p.ks + slice) * 8 * kRows;
 #pragma unroll
       for (int s = 0; s < NSUB; ++s)
 #pragma unroll
@@ -838,7 +882,14 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
           const int n = 2 * t + (i & 1);
           if (n < mc) __stcg(q + n * kRows + r, acc[s][i]);
         }
-      pend_tile = tile;
+      // A last slice that found every other slice arrived adds the tile up at
+      // once: reduce_tile's fence by lane 0 (after it read the count) and warp
+      // barrier order the loads after the others' partial stores and this
+      // warp's own.  Nobody else touches the count in this launch.
+      if (last_slice && __shfl_sync(0xffffffffu, seen, 0) == p.ks - 1)
+        reduce_tile(tile);
+      else
+        pend_tile = tile;
     }
   }
   if (!timed_out) {
@@ -854,23 +905,16 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
   }
   if (timed_out) {
     if (lane == 0) atomicOr(p.flags, W4A16_DEVICE_TIMEOUT);
+    // finish this warp's grabs (up to the one that fails), so the count of
+    // grabs stays exact and the counter is reset
+    if (p.dyn && lane == 0 && iu >= 0)
+      for (int v = resolve(nxt); v >= 0; v = resolve(grab())) {
+      }
     // let copies already in flight land before shared memory is released
     const uint32_t issued = __shfl_sync(0xffffffffu, R.issued, 0);
     while (R.consumed < issued) {
       mbar_wait(R.bars0 + 8 * (R.consumed % (uint32_t)S), (R.consumed / (uint32_t)S) & 1u);
       ++R.consumed;
-    }
-  }
-  // With dynamic dealing the last warp out resets the unit counters for the
-  // next launch (every warp has made its last grab before it counts itself
-  // out); round-robin dealing leaves them untouched at zero.
-  __syncwarp();
-  if (p.dyn && lane == 0) {
-    __threadfence();
-    if (atomicAdd(p.sched + 1, 1) == TW - 1) {
-      __threadfence();
-      p.sched[0] = 0;
-      p.sched[1] = 0;
     }
   }
 }
@@ -1641,6 +1685,7 @@ cudaError_t launch_stream(const Maps& maps, StreamParams p, const StreamWork& w,
                           cudaStream_t stream, int pdl) {
   p.tiles = w.tiles;
   p.units = w.units;
+  p.kfull = p.nst % p.sl == 0 ? p.ks : p.ks - 1;
   return w.nsub == 1 ? launch_stream_t<1>(maps, p, d.sms, d, stream, pdl)
                      : launch_stream_t<2>(maps, p, d.sms, d, stream, pdl);
 }
