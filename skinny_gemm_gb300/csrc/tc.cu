@@ -520,7 +520,6 @@ struct StreamParams {
   int stages;
   int xpitch;       // bytes per activation row of the pre-staged copy (0: per-stage copies)
   int prefetch;     // request the first weight stages before waiting for earlier kernels
-  int dyn;          // deal units after the first dynamically (else round-robin)
 };
 
 // Tile and slice of work unit u.  Units whose slice has the full length come
@@ -529,8 +528,9 @@ struct StreamParams {
 // units dealt last are the shortest and the warps finish closer together.
 // The order of the units changes no result: every partial has its fixed
 // place and the sums run in slice order.
+template <bool SPLIT>
 __device__ __forceinline__ int unit_tile(const StreamParams& p, int u, int& slice) {
-  if (p.ks == 1) {
+  if (!SPLIT) {
     slice = 0;
     return u;
   }
@@ -560,7 +560,10 @@ __host__ __device__ inline int xstage_bytes(int mc, int K) {
 template <int NSUB>
 constexpr int stream_min_blocks() { return NSUB == 1 ? 2 : Geo<NSUB>::kWarps >= 8 ? 1 : W4A16_TC_MIN_BLOCKS; }
 
-template <int NSUB, bool ALLCOLS, bool XSTAGED>
+// SPLIT: K is split over several units per tile (ks > 1); the units after
+// the first are then dealt dynamically, else round-robin (measured faster
+// without a split, on the LM heads).
+template <int NSUB, bool ALLCOLS, bool XSTAGED, bool SPLIT>
 __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB>()) tc_stream_kernel(
     const __grid_constant__ Maps maps, StreamParams p) {
   using G = Geo<NSUB>;
@@ -601,10 +604,11 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
   const int TW = gridDim.x * kW;
 
   // Work units of this warp.  The first is static (unit gw), so its weights
-  // can be requested before the wait for earlier kernels.  With p.dyn every
-  // later one is grabbed from a counter in the workspace (unit TW + count) as
-  // soon as the previous one starts streaming, so warps that run faster take
-  // more units; otherwise the warp takes units gw + TW, gw + 2 TW, ...
+  // can be requested before the wait for earlier kernels.  With SPLIT every
+  // later one is grabbed from a counter in the workspace (unit TW + count)
+  // when at most one stage of the previous one is left to request, so warps
+  // that run faster take more units and no warp commits to a unit long
+  // before it can start it; otherwise the warp takes units gw + TW, ...
   // Lane 0 streams the units in order; dealt ones it records in s_units (a
   // ring of 8 per warp, ahead of the computing lanes by at most S stages;
   // -1 marks the end).
@@ -612,26 +616,26 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
   // Every warp with a first unit grabs until one grab fails, so a launch
   // makes exactly max(0, units - TW) + min(TW, units) grabs; the one that
   // draws the last count resets the counter for the next launch.  A grab's
-  // count is only looked at when its unit begins, a unit later, so the
-  // atomic's round trip never stalls the warp.
+  // count is only looked at when its unit begins, a stage or two later, so
+  // the atomic's round trip does not stall the warp.
   int* s_units = s_tok + kMaxChunk + 8 * warp;
   int iu = -1, ist = 0, iend = 0;  // lane 0: unit being issued, its stage cursor
-  int nxt = -1;                    // lane 0: count of the grab for the unit after iu (unit TW + nxt)
+  int nxt = -1;                    // lane 0: count of the grab for the unit after iu (unit TW + nxt), -1 before it
   int irow = 0;                    // lane 0: first weight row of unit iu
   uint32_t iseq = 0;
   const int last_grab = max(0, p.units - TW) + min(TW, p.units) - 1;
-  auto grab = [&]() { return p.dyn ? atomicAdd(p.sched, 1) : iu; };
+  auto grab = [&]() { return atomicAdd(p.sched, 1); };
   auto resolve = [&](int c) {  // the unit of grab count c, -1 past the end
-    if (p.dyn && c == last_grab) *p.sched = 0;
+    if (c == last_grab) *p.sched = 0;
     const int v = TW + c;
     return v < p.units ? v : -1;
   };
   auto begin_unit = [&](int u) {
     iu = u;
-    if (p.dyn) s_units[iseq++ & 7u] = u;
+    if (SPLIT) s_units[iseq++ & 7u] = u;
     if (u >= 0) {
       int slice;
-      irow = unit_tile(p, u, slice) * kRows;
+      irow = unit_tile<SPLIT>(p, u, slice) * kRows;
       ist = slice * p.sl;
       iend = min(ist + p.sl, p.nst);
     }
@@ -644,11 +648,16 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
   auto issue_next = [&](bool with_x) {  // after the wait only (grabs touch the workspace)
     if (iu < 0) return;
     if (ist == iend) {
-      begin_unit(resolve(nxt));
+      if (SPLIT) {
+        begin_unit(resolve(nxt));
+        nxt = -1;
+      } else {
+        begin_unit(iu + TW < p.units ? iu + TW : -1);
+      }
       if (iu < 0) return;
-      nxt = grab();
     }
     issue_stage(with_x);
+    if (SPLIT && nxt < 0 && iend - ist <= 1) nxt = grab();
   };
   // The weights never depend on earlier kernels: with p.prefetch the first
   // unit's first stages are requested before the wait for those kernels and
@@ -664,7 +673,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
   pdl_wait();
   if (lane == 0) {
     if (iu >= 0) {
-      nxt = grab();
+      if (SPLIT && iend - ist <= 1) nxt = grab();
       const int first = ist - (int)R.issued;  // the unit's first stage
       for (uint32_t i = 0; i < R.issued; ++i) ring_issue_x(R, i, first + (int)i, p.x, s_tok, xring, p.K);
     }
@@ -801,7 +810,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
   // in the order lane 0 recorded them
   int u = gw;
   for (uint32_t cseq = 0; !timed_out; ++cseq) {
-    if (p.dyn) {
+    if (SPLIT) {
       __syncwarp();
       u = s_units[cseq & 7u];
     } else if (cseq > 0) {
@@ -809,11 +818,11 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
     }
     if (u < 0 || u >= p.units) break;
     int slice;
-    const int tile = unit_tile(p, u, slice);
+    const int tile = unit_tile<SPLIT>(p, u, slice);
     const int s0 = slice * p.sl, s1 = min(s0 + p.sl, p.nst);
     // The last slice of a tile reads the tile's arrival count before its
     // stages (the value is used after them, so the load never stalls).
-    const bool last_slice = p.ks > 1 && slice == p.ks - 1;
+    const bool last_slice = SPLIT && slice == p.ks - 1;
     int seen = 0;
     if (last_slice && lane == 0) seen = ld_relaxed_gpu(p.cnt + tile);
     int prow[2 * NSUB];
@@ -863,7 +872,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
       count_arrival(pend_tile);
       pend_tile = -1;
     }
-    if (p.ks == 1) {
+    if (!SPLIT) {
 #pragma unroll
       for (int s = 0; s < NSUB; ++s)
 #pragma unroll
@@ -907,8 +916,8 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
     if (lane == 0) atomicOr(p.flags, W4A16_DEVICE_TIMEOUT);
     // finish this warp's grabs (up to the one that fails), so the count of
     // grabs stays exact and the counter is reset
-    if (p.dyn && lane == 0 && iu >= 0)
-      for (int v = resolve(nxt); v >= 0; v = resolve(grab())) {
+    if (SPLIT && lane == 0 && iu >= 0)
+      for (int v = nxt >= 0 ? resolve(nxt) : 0; v >= 0; v = resolve(grab())) {
       }
     // let copies already in flight land before shared memory is released
     const uint32_t issued = __shfl_sync(0xffffffffu, R.issued, 0);
@@ -1470,11 +1479,11 @@ cudaError_t launch_ex(Kern fn, dim3 grid, dim3 block, int smem, cudaStream_t str
   return cudaLaunchKernelEx(&cfg, fn, args...);
 }
 
-template <int NSUB, bool A, bool X>
+template <int NSUB, bool A, bool X, bool SPLIT>
 cudaError_t stream_launch_t(const Maps& map, const StreamParams& p, int sms, int smem, DeviceInfo& d,
                             cudaStream_t stream, bool pdl) {
   constexpr int kW = Geo<NSUB>::kWarps;
-  auto* fn = tc_stream_kernel<NSUB, A, X>;
+  auto* fn = tc_stream_kernel<NSUB, A, X, SPLIT>;
   if (cudaError_t e = allow_smem(fn, d)) return e;
   int per_sm = 0;
   if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kW * 32, smem)) return e;
@@ -1495,17 +1504,17 @@ cudaError_t launch_stream_t(const Maps& map, StreamParams p, int sms, DeviceInfo
   p.xpitch = staged ? 2 * p.K + 64 : 0;
   p.stages = staged ? staged_stages<NSUB>(p.M, p.K) : stream_stages<NSUB>(p.M);
   p.prefetch = pdl >= 2;
-  // Dynamic dealing pays where K is split (16384^2: 46 -> 44 us); without a
-  // split (the LM heads) round-robin was measured faster.
-  p.dyn = p.ks > 1;
   int smem = stream_smem<NSUB>(p.stages, staged ? 0 : p.M);
   if (staged) smem += xstage_bytes(p.M, p.K);
   const bool on = pdl > 0;
-  if (allcols)
-    return staged ? stream_launch_t<NSUB, true, true>(map, p, sms, smem, d, stream, on)
-                  : stream_launch_t<NSUB, true, false>(map, p, sms, smem, d, stream, on);
-  return staged ? stream_launch_t<NSUB, false, true>(map, p, sms, smem, d, stream, on)
-                : stream_launch_t<NSUB, false, false>(map, p, sms, smem, d, stream, on);
+  using Fn = cudaError_t (*)(const Maps&, const StreamParams&, int, int, DeviceInfo&, cudaStream_t, bool);
+  // [allcols][staged][split]
+  static const Fn fns[2][2][2] = {
+      {{stream_launch_t<NSUB, false, false, false>, stream_launch_t<NSUB, false, false, true>},
+       {stream_launch_t<NSUB, false, true, false>, stream_launch_t<NSUB, false, true, true>}},
+      {{stream_launch_t<NSUB, true, false, false>, stream_launch_t<NSUB, true, false, true>},
+       {stream_launch_t<NSUB, true, true, false>, stream_launch_t<NSUB, true, true, true>}}};
+  return fns[allcols][staged][p.ks > 1](map, p, sms, smem, d, stream, on);
 }
 
 // Row subtiles per warp of the persistent kernel for a chunk of M rows.
@@ -1686,8 +1695,10 @@ cudaError_t launch_stream(const Maps& maps, StreamParams p, const StreamWork& w,
   p.tiles = w.tiles;
   p.units = w.units;
   p.kfull = p.nst % p.sl == 0 ? p.ks : p.ks - 1;
-  return w.nsub == 1 ? launch_stream_t<1>(maps, p, d.sms, d, stream, pdl)
-                     : launch_stream_t<2>(maps, p, d.sms, d, stream, pdl);
+#if W4A16_TC_STREAM_NSUB1_MIN_M <= 8  // else no chunk (8 rows at most) takes 16-row warps
+  if (w.nsub == 1) return launch_stream_t<1>(maps, p, d.sms, d, stream, pdl);
+#endif
+  return launch_stream_t<2>(maps, p, d.sms, d, stream, pdl);
 }
 
 struct Workspace {
