@@ -207,17 +207,10 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// 16-byte global load cached in L2 only (activations another kernel may just
-// have written).
+// Relaxed load at GPU scope (a counter other CTAs update atomically).
 __device__ __forceinline__ int ld_relaxed_gpu(const int* p) {
   int v;
   asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
   return v;
 }
 
@@ -596,6 +589,8 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
   if (lane == 0)
     for (int i = 0; i < S; ++i) mbar_init(R.bars0 + 8 * i, 1);
   if (threadIdx.x < mc) s_tok[threadIdx.x] = p.row0 + threadIdx.x;
+  const uint32_t xbar = smem_u32(s_tok + kMaxChunk + 8 * 8);  // the pre-staged activations' copy
+  if (XSTAGED && threadIdx.x == 0) mbar_init(xbar, 1);
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   __syncthreads();
 
@@ -671,6 +666,11 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
       for (int i = 0; i < S && iu >= 0 && ist < iend; ++i) issue_stage(false);
   }
   pdl_wait();
+  if (XSTAGED && threadIdx.x == 0) {  // each activation row in one bulk copy (16-byte aligned: K % 512 == 0)
+    mbar_expect_tx(xbar, (uint32_t)(mc * 2 * p.K));
+    for (int n = 0; n < mc; ++n)
+      bulk_load(xst + n * p.xpitch, p.x + (int64_t)(p.row0 + n) * p.K, 2 * p.K, xbar, R.pol_keep);
+  }
   if (lane == 0) {
     if (iu >= 0) {
       if (SPLIT && iend - ist <= 1) nxt = grab();
@@ -681,31 +681,21 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
   }
   __syncwarp();
 
+  bool timed_out = false;
   if (XSTAGED) {
-    // Activation rows in B-fragment order, then the sum of every 64-group of
-    // every row with the same MMA chain the per-stage path uses.
-    // Eight chunks per thread per round, loads first, so their latencies overlap.
-    const int chunks = p.K / 8, total = mc * chunks;
-    for (int c0 = threadIdx.x; c0 < total; c0 += 8 * blockDim.x) {
-      uint4 u[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int c = c0 + j * blockDim.x;
-        if (c < total) {
-          const int n = c / chunks, wd = c - n * chunks;
-          u[j] = ld_cg_v4(p.x + (int64_t)(p.row0 + n) * p.K + 8 * wd);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int c = c0 + j * blockDim.x;
-        if (c < total) {
-          const int n = c / chunks, wd = c - n * chunks;
-          uint32_t b[2][2];
-          frag_from_chunk(u[j], b);
-          sts128(xst + n * p.xpitch + 16 * wd, make_uint4(b[0][0], b[0][1], b[1][0], b[1][1]));
-        }
-      }
+    // Activation rows in B-fragment order (one bulk copy, then each 16-byte
+    // chunk permuted in place), then the sum of every 64-group of every row
+    // with the same MMA chain the per-stage path uses.  The copy goes out
+    // through the tensor-memory-access path, which returns it well ahead of
+    // per-thread loads while the first weight stages are in flight.
+    timed_out = __syncthreads_or(!mbar_wait(xbar, 0)) != 0;
+    const int chunks = p.K / 8, total = timed_out ? 0 : mc * chunks;
+    for (int c = threadIdx.x; c < total; c += blockDim.x) {
+      const int n = c / chunks, wd = c - n * chunks;
+      const uint32_t a = xst + n * p.xpitch + 16 * wd;
+      uint32_t b[2][2];
+      frag_from_chunk(lds128(a), b);
+      sts128(a, make_uint4(b[0][0], b[0][1], b[1][0], b[1][1]));
     }
     __syncthreads();
     // Group sums: one MMA chain yields eight groups of one activation row, the
@@ -713,7 +703,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
     // column depends only on its own B column, so every sum has the bits of
     // the per-stage chain (activation row in the column).  Four chains per
     // warp at a time, interleaved.
-    const int nblk = p.K / kGroup / 8, tasks = mc * nblk;
+    const int nblk = p.K / kGroup / 8, tasks = timed_out ? 0 : mc * nblk;
     for (int k0 = warp; k0 < tasks; k0 += 4 * kW) {
       uint32_t b[4][2][2][2];
       float v[4][4];
@@ -760,7 +750,6 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
 #pragma unroll
     for (int i = 0; i < 4; ++i) loff[s][i] = loff2[s][i];
 
-  bool timed_out = false;
   int pend_tile = -1;               // partials stored, arrival not yet counted
   int cnt_tile = -1, cnt_old = 0;   // arrival counted (lane 0 holds the old count)
 
@@ -920,6 +909,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
       for (int v = nxt >= 0 ? resolve(nxt) : 0; v >= 0; v = resolve(grab())) {
       }
     // let copies already in flight land before shared memory is released
+    if (XSTAGED) mbar_wait(xbar, 0);
     const uint32_t issued = __shfl_sync(0xffffffffu, R.issued, 0);
     while (R.consumed < issued) {
       mbar_wait(R.bars0 + 8 * (R.consumed % (uint32_t)S), (R.consumed / (uint32_t)S) & 1u);
