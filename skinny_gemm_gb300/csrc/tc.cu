@@ -513,6 +513,8 @@ struct StreamParams {
   int stages;
   int xpitch;       // bytes per activation row of the pre-staged copy (0: per-stage copies)
   int prefetch;     // request the first weight stages before waiting for earlier kernels
+  const int32_t* ids;  // routed mode: expert id of each of T tokens, E experts of N rows each
+  int T, E;
 };
 
 // Tile and slice of work unit u.  Units whose slice has the full length come
@@ -553,20 +555,70 @@ __host__ __device__ inline int xstage_bytes(int mc, int K) {
 template <int NSUB>
 constexpr int stream_min_blocks() { return NSUB == 1 ? 2 : Geo<NSUB>::kWarps >= 8 ? 1 : W4A16_TC_MIN_BLOCKS; }
 
+// Routed mode: the chunk table every CTA builds from the expert ids after the
+// wait for earlier kernels.  The tokens of each expert, in token order, form
+// chunks of at most `cap` tokens; a chunk is one expert and its token rows.
+// Chunks are numbered in the order of their first tokens (the order changes
+// no result: every chunk writes its own rows with the canonical arithmetic).
+// Layout (ints): [0] chunks, [1] tokens with an id out of range, then per
+// chunk its expert, its token count and kMaxChunk tokens, then the
+// out-of-range tokens.
+constexpr int kRoutedStreamMaxT = 32;  // tokens the routed mode takes: one per lane
+__host__ __device__ inline int routed_table_bytes(int T) { return (2 + T * (2 + kMaxChunk) + T) * 4; }
+
+// Warp 0 only, T <= 32, token t in lane t.  Warp match and ballot only: no
+// loop over tokens or experts.
+__device__ __forceinline__ void build_chunks(const int32_t* __restrict__ ids, int T, int E, int cap, int* tab) {
+  const int lane = threadIdx.x & 31;
+  const int v = lane < T ? ids[lane] : -1;
+  const bool ok = lane < T && v >= 0 && v < E;
+  const int key = ok ? v : -1;
+  const unsigned lt = (1u << lane) - 1u;
+  const unsigned same = __match_any_sync(0xffffffffu, key);       // tokens of this expert
+  const int before = __popc(same & lt);                            // ... ahead of this one
+  const bool start = ok && before % cap == 0;                      // first token of a chunk
+  // the tokens of this token's chunk (expert, chunk within the expert); its
+  // lowest lane starts the chunk
+  const unsigned mine = __match_any_sync(0xffffffffu, ok ? key * 32 + before / cap : -1);
+  const unsigned starts = __ballot_sync(0xffffffffu, start);
+  const int c = __popc(starts & ((1u << (__ffs(mine) - 1)) - 1u));  // chunks that start earlier
+  if (ok) {
+    int* ch = tab + 2 + c * (2 + kMaxChunk);
+    ch[2 + before % cap] = lane;
+    if (start) {
+      ch[0] = key;
+      ch[1] = min(cap, __popc(same) - before);
+    }
+  }
+  const bool bad = lane < T && !ok;
+  const unsigned badm = __ballot_sync(0xffffffffu, bad);
+  if (bad) tab[2 + T * (2 + kMaxChunk) + __popc(badm & lt)] = lane;
+  if (lane == 0) {
+    tab[0] = __popc(starts);
+    tab[1] = __popc(badm);
+  }
+}
+
 // SPLIT: K is split over several units per tile (ks > 1); the units after
 // the first are then dealt dynamically, else round-robin (measured faster
 // without a split, on the LM heads).
-template <int NSUB, bool ALLCOLS, bool XSTAGED, bool SPLIT>
-__global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB>()) tc_stream_kernel(
+// ROUTED (w4a16_mm_id): a unit is one chunk of tokens routed to one expert
+// times one tile of that expert, over the whole K; the slice sums are folded
+// in slice order as they complete, so every row equals w4a16_mm on the
+// selected expert bit for bit.  Units are dealt round-robin over the chunks
+// the ids select, so only the weights of experts with tokens are read.
+template <int NSUB, bool ALLCOLS, bool XSTAGED, bool SPLIT, bool ROUTED = false>
+__global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_min_blocks<NSUB>()) tc_stream_kernel(
     const __grid_constant__ Maps maps, StreamParams p) {
   using G = Geo<NSUB>;
   constexpr int kW = G::kWarps, kRows = G::kRows;
+  static_assert(!ROUTED || (!XSTAGED && !SPLIT), "the routed mode copies activations per stage, whole-K units");
   extern __shared__ uint8_t smem_raw[];
   pdl_launch_dependents();
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int S = p.stages, mc = p.M;
+  const int S = p.stages, mc = p.M;   // routed mode: mc = chunk capacity
   const int xring = XSTAGED ? 0 : mc;  // activation rows copied per stage
   const int x_slot = xring * kXPitch;
 
@@ -582,13 +634,14 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
   int* s_tok = reinterpret_cast<int*>(base + bar_off + kW * S * 8);
   const uint32_t xst = smem_u32(base) + bar_off + (uint32_t)(kW * S * 8 + kStreamMisc);  // 16-byte aligned
   const uint32_t sxs = xst + (uint32_t)(mc * p.xpitch);
+  int* s_tab = reinterpret_cast<int*>(base + (xst - smem_u32(base)));  // routed mode: chunk table
   R.issued = R.consumed = 0;
   R.pol_stream = policy_evict_first();
   R.pol_keep = policy_evict_last();
 
   if (lane == 0)
     for (int i = 0; i < S; ++i) mbar_init(R.bars0 + 8 * i, 1);
-  if (threadIdx.x < mc) s_tok[threadIdx.x] = p.row0 + threadIdx.x;
+  if (!ROUTED && threadIdx.x < mc) s_tok[threadIdx.x] = p.row0 + threadIdx.x;
   const uint32_t xbar = smem_u32(s_tok + kMaxChunk + 8 * 8);  // the pre-staged activations' copy
   if (XSTAGED && threadIdx.x == 0) mbar_init(xbar, 1);
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -614,7 +667,10 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
   // count is only looked at when its unit begins, a stage or two later, so
   // the atomic's round trip does not stall the warp.
   int* s_units = s_tok + kMaxChunk + 8 * warp;
+  int units = p.units;             // routed mode: set from the chunk table
   int iu = -1, ist = 0, iend = 0;  // lane 0: unit being issued, its stage cursor
+  const int* itok = s_tok;         // lane 0: activation rows of unit iu
+  int imc = xring;                 // and their count
   int nxt = -1;                    // lane 0: count of the grab for the unit after iu (unit TW + nxt), -1 before it
   int irow = 0;                    // lane 0: first weight row of unit iu
   uint32_t iseq = 0;
@@ -629,15 +685,25 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
     iu = u;
     if (SPLIT) s_units[iseq++ & 7u] = u;
     if (u >= 0) {
-      int slice;
-      irow = unit_tile<SPLIT>(p, u, slice) * kRows;
-      ist = slice * p.sl;
-      iend = min(ist + p.sl, p.nst);
+      if (ROUTED) {
+        const int c = u / p.tiles;
+        const int* ch = s_tab + 2 + c * (2 + kMaxChunk);
+        irow = ch[0] * p.N + (u - c * p.tiles) * kRows;  // row of the stacked [E][N] weights
+        imc = ch[1];
+        itok = ch + 2;
+        ist = 0;
+        iend = p.nst;
+      } else {
+        int slice;
+        irow = unit_tile<SPLIT>(p, u, slice) * kRows;
+        ist = slice * p.sl;
+        iend = min(ist + p.sl, p.nst);
+      }
     }
   };
   auto issue_stage = [&](bool with_x) {
-    const uint32_t slot = ring_issue_w<NSUB>(R, &maps, ist, irow, xring);
-    if (with_x) ring_issue_x(R, slot, ist, p.x, s_tok, xring, p.K);
+    const uint32_t slot = ring_issue_w<NSUB>(R, &maps, ist, irow, imc);
+    if (with_x) ring_issue_x(R, slot, ist, p.x, itok, imc, p.K);
     ++ist;
   };
   auto issue_next = [&](bool with_x) {  // after the wait only (grabs touch the workspace)
@@ -647,7 +713,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
         begin_unit(resolve(nxt));
         nxt = -1;
       } else {
-        begin_unit(iu + TW < p.units ? iu + TW : -1);
+        begin_unit(iu + TW < units ? iu + TW : -1);
       }
       if (iu < 0) return;
     }
@@ -661,11 +727,27 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
   // flight while the activations are staged.
   if (lane == 0) {
     fence_proxy_async();
-    begin_unit(gw < p.units ? gw : -1);
-    if (p.prefetch)
-      for (int i = 0; i < S && iu >= 0 && ist < iend; ++i) issue_stage(false);
+    if (!ROUTED) {
+      begin_unit(gw < units ? gw : -1);
+      if (p.prefetch)
+        for (int i = 0; i < S && iu >= 0 && ist < iend; ++i) issue_stage(false);
+    }
   }
   pdl_wait();
+  if (ROUTED) {
+    // the chunks the ids select (the same table in every CTA); the first
+    // CTA also writes zero rows for tokens whose id is out of range
+    if (warp == 0) build_chunks(p.ids, p.T, p.E, mc, s_tab);
+    __syncthreads();
+    units = s_tab[0] * p.tiles;
+    if (blockIdx.x == 0 && s_tab[1] > 0) {
+      const int* bad = s_tab + 2 + p.T * (2 + kMaxChunk);
+      if (threadIdx.x == 0) atomicOr(p.flags, W4A16_DEVICE_BAD_ID);
+      for (int64_t i = threadIdx.x; i < (int64_t)s_tab[1] * p.N; i += blockDim.x)
+        p.y[(int64_t)bad[i / p.N] * p.N + i % p.N] = 0;
+    }
+    if (lane == 0) begin_unit(gw < units ? gw : -1);
+  }
   if (XSTAGED && threadIdx.x == 0) {  // each activation row in one bulk copy (16-byte aligned: K % 512 == 0)
     mbar_expect_tx(xbar, (uint32_t)(mc * 2 * p.K));
     for (int n = 0; n < mc; ++n)
@@ -805,10 +887,19 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
     } else if (cseq > 0) {
       u += TW;
     }
-    if (u < 0 || u >= p.units) break;
-    int slice;
-    const int tile = unit_tile<SPLIT>(p, u, slice);
-    const int s0 = slice * p.sl, s1 = min(s0 + p.sl, p.nst);
+    if (u < 0 || u >= units) break;
+    int slice = 0, tile, umc = mc;
+    const int* utok = s_tok;
+    if (ROUTED) {
+      const int c = u / p.tiles;
+      const int* ch = s_tab + 2 + c * (2 + kMaxChunk);
+      tile = u - c * p.tiles;
+      umc = ch[1];
+      utok = ch + 2;
+    } else {
+      tile = unit_tile<SPLIT>(p, u, slice);
+    }
+    const int s0 = ROUTED ? 0 : slice * p.sl, s1 = ROUTED ? p.nst : min(s0 + p.sl, p.nst);
     // The last slice of a tile reads the tile's arrival count before its
     // stages (the value is used after them, so the load never stalls).
     const bool last_slice = SPLIT && slice == p.ks - 1;
@@ -822,6 +913,8 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
     for (int s = 0; s < NSUB; ++s)
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[s][i] = 0.0f;
+    float sum[NSUB][4];       // routed mode: the slice sums folded so far, in slice order
+    int fold_at = s0 + p.sl;  // and the stage that ends the current slice
 
     for (int st = s0; st < s1; ++st) {
       uint32_t slot;
@@ -837,8 +930,19 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
       } else {
         xbase = ordered(R.xs0 + slot * x_slot + g * kXPitch + 16 * t);
       }
-      compute_stage<NSUB, ALLCOLS, XSTAGED>(cbase, cbase + 2 * G::kBox, xbase, g < mc, sxbase, sx_cols(mc) * 4,
-                                            2 * t < mc, acc, loff, g);
+      compute_stage<NSUB, ALLCOLS, XSTAGED>(cbase, cbase + 2 * G::kBox, xbase, g < umc, sxbase, sx_cols(mc) * 4,
+                                            2 * t < umc, acc, loff, g);
+      if (ROUTED && (st + 1 == fold_at || st + 1 == s1)) {
+        const bool first = fold_at == s0 + p.sl;
+#pragma unroll
+        for (int s = 0; s < NSUB; ++s)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            sum[s][i] = first ? acc[s][i] : __fadd_rn(sum[s][i], acc[s][i]);
+            acc[s][i] = 0.0f;
+          }
+        fold_at += p.sl;
+      }
       ++R.consumed;
       __syncwarp();
       if (lane == 0) {
@@ -861,7 +965,16 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, stream_min_blocks<NSUB
       count_arrival(pend_tile);
       pend_tile = -1;
     }
-    if (!SPLIT) {
+    if (ROUTED) {
+#pragma unroll
+      for (int s = 0; s < NSUB; ++s)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int row = prow[2 * s + (i >> 1)];
+          const int n = 2 * t + (i & 1);
+          if (n < umc && row < p.N) p.y[(int64_t)utok[n] * p.N + row] = f32_to_bf16_bits(sum[s][i]);
+        }
+    } else if (!SPLIT) {
 #pragma unroll
       for (int s = 0; s < NSUB; ++s)
 #pragma unroll
@@ -1813,11 +1926,43 @@ int routed_xcap(int T, int E) {
   return x < 1 ? 1 : x;
 }
 
+// The persistent kernel in routed mode (T <= kRoutedStreamMaxT): 32-row
+// whole-K units of the chunks the ids select, dealt round-robin over a full
+// grid.  Nothing is requested before the wait for earlier kernels (the ids
+// decide which weights are read).  The caller holds g_dev_mu.
+cudaError_t launch_stream_routed(const LaunchArgs& a, DeviceInfo& d) {
+  const Shape s = tc_shape(a.N, a.K);
+  StreamParams p{};
+  p.x = a.x; p.S = a.S; p.B = a.B; p.y = a.y; p.flags = a.flags;
+  p.N = a.N; p.K = a.K; p.M = routed_xcap(a.T, a.E); p.row0 = 0;
+  p.nst = s.nst; p.sl = s.sl; p.ks = s.ks;
+  p.tiles = cdiv(a.N, kTileRows);
+  p.stages = stream_stages<2>(p.M);
+  p.ids = a.ids; p.T = a.T; p.E = a.E;
+  Maps maps;
+  if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, (int64_t)a.N * a.E, a.K, kTileRows)) return e;
+  const int smem = stream_smem<2>(p.stages, p.M) + routed_table_bytes(a.T);
+  constexpr int kW = Geo<2>::kWarps;
+  auto* fn = p.M > 1 ? tc_stream_kernel<2, true, false, false, true> : tc_stream_kernel<2, false, false, false, true>;
+  if (cudaError_t e = allow_smem(fn, d)) return e;
+  int per_sm = 0;
+  if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kW * 32, smem)) return e;
+  if (per_sm < 1) per_sm = 1;
+  int grid = d.sms * per_sm;
+  const int need = cdiv(a.T * p.tiles, kW);  // at most T chunks
+  if (grid > need) grid = need;
+  return launch_ex(fn, dim3(grid), dim3(kW * 32), smem, a.stream, a.pdl > 0, 1, maps, p);
+}
+
 cudaError_t launch_tc_id(const LaunchArgs& a, const w4a16_plan& plan) {
   (void)plan;
   const Shape s = tc_shape(a.N, a.K);
   int dev = 0;
   if (cudaError_t e = cudaGetDevice(&dev)) return e;
+  if (a.tc_path != 2 && a.T <= kRoutedStreamMaxT) {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    return launch_stream_routed(a, device_info(dev));
+  }
   if (a.tc_path != 1) {  // the tile kernel in routed mode, where it fits
     const TilePlan tp = tile_plan_r(s, a.N, routed_xcap(a.T, a.E), true, 1);
     if (tp.kc > 0) {

@@ -103,3 +103,35 @@ def test_all_tokens_on_one_expert_spans_chunks():
     y = ops.mm_id(to_dev_bf16(xb), w, torch.from_numpy(ids_np).cuda())
     yr, ad = oracle.mm_id(xb, hw.Wq, hw.scales, hw.biases, ids_np, T, N, K, E)
     assert_parity(y, yr, ad, "one expert, 19 tokens")
+
+
+@pytest.mark.parametrize("kernel", ["auto", "tc_stream", "tc_tile"])
+def test_routed_rows_equal_mm_on_the_expert(kernel):
+    """Every routed row is the w4a16_mm result of its token on the selected
+    expert, bit for bit (the same canonical arithmetic on every launch shape)."""
+    E, N, K = EXPERTS
+    _, w = _experts(0, E, N, K)
+    T = 8
+    ids_np = synth.make_ids(0, T, E)
+    x = to_dev_bf16(synth.make_x(0, T, K))
+    y = bf16_bits(ops.mm_id(x, w, torch.from_numpy(ids_np).cuda(), kernel=kernel))
+    for t in range(T):
+        e = int(ids_np[t])
+        we = ops.W4Matrix(w.Wq[e], w.scales[e], w.biases[e], N, K)
+        assert np.array_equal(y[t], bf16_bits(ops.mm(x[t:t + 1], we, kernel="tc"))[0]), f"token {t}"
+
+
+def test_routed_many_tokens_take_the_other_launch_shapes():
+    """More tokens than the persistent routed mode takes (64): the tile and
+    per-expert kernels, still equal to each other bit for bit."""
+    E, N, K, T = 3, 200, 1024, 80
+    hw, w = _experts(12, E, N, K)
+    ids_np = synth.make_ids(12, T, E)
+    ids = torch.from_numpy(ids_np).cuda()
+    xb = synth.make_x(12, T, K)
+    x = to_dev_bf16(xb)
+    a = ops.mm_id(x, w, ids, kernel="tc_stream")
+    b = ops.mm_id(x, w, ids)
+    assert np.array_equal(bf16_bits(a), bf16_bits(b))
+    yr, ad = oracle.mm_id(xb, hw.Wq, hw.scales, hw.biases, ids_np, T, N, K, E)
+    assert_parity(a, yr, ad, "mm_id T=80")
