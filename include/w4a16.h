@@ -98,7 +98,9 @@ typedef enum {
                                identical bits */
   W4A16_KERNEL_VANILLA = 3, /* debug control: one thread per output, no sharing */
   W4A16_KERNEL_TC_STREAM = 4, /* tensor-core kernel, persistent grid: work units dealt to
-                                 warps round-robin, split-K through the workspace */
+                                 warps (round-robin, or from a counter when K is split),
+                                 split-K through the workspace.  w4a16_mm_id: T <= 32 its
+                                 routed mode, more tokens a grid of tile x expert CTAs */
   W4A16_KERNEL_TC_TILE = 5  /* tensor-core kernel, one CTA per 16-row tile holding the
                                tile's whole K range; needs that to fit in shared memory
                                (otherwise W4A16_ERR_KERNEL) */
@@ -174,9 +176,12 @@ int w4a16_mm_group(const w4a16_mm_item* items, int count, int M, int K, void* st
  * in [HY4] "What was missing and what this adds"):
  *   y[t][n] = sum_k x[t][k] * w_{ids[t]}[n][k]
  * Wq is u32 [E][N][K/8], scales/biases bf16 [E][N][K/64], ids int32 [T] on
- * the DEVICE, y bf16 [T][N].  Each expert's weights are streamed once for
- * all tokens routed to it (in chunks of up to eight tokens); experts no
- * token selects are not read.  An id outside 0..E-1 cannot be checked on the
+ * the DEVICE, y bf16 [T][N].  The tokens of an expert are taken in chunks
+ * of up to eight; experts no token selects are not read.  With T <= 32 every
+ * chunk streams its expert's weights once (the chunks run side by side, the
+ * units of all of them dealt over one persistent grid); with more tokens a
+ * CTA holds a tile of an expert's weights in shared memory while all its
+ * chunks stream through.  An id outside 0..E-1 cannot be checked on the
  * host without a synchronisation: its row of y is written as zeros and the
  * sticky device flag W4A16_DEVICE_BAD_ID is raised (see w4a16_device_status).
  * T == 0 is a successful no-op. */
