@@ -476,8 +476,12 @@ def measure_e2e(torch, ops, layers, steps, kernel, step_bytes, world, dist, laun
             "api": "skinny_gemm_gb300.ops.mm / mm_group (eager, the C ABI through ctypes)"}
 
 
-def time_graph_launches(torch, fn_list, reps):
-    """Median-free average: capture fn_list (one call each) in a graph, replay reps times."""
+def time_graph_launches(torch, fn_list, reps, min_calls=32):
+    """Average time per call: fn_list (one call each), repeated to at least
+    min_calls calls, captured in one graph and replayed reps times.  The
+    repetition keeps the replay boundary (where a launch cannot overlap the
+    previous one) rare, as it is in a decode loop."""
+    rounds = max(1, -(-min_calls // len(fn_list)))
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         for fn in fn_list:
@@ -485,8 +489,9 @@ def time_graph_launches(torch, fn_list, reps):
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
-        for fn in fn_list:
-            fn()
+        for _ in range(rounds):
+            for fn in fn_list:
+                fn()
     with torch.cuda.stream(stream):
         for _ in range(3):
             g.replay()
@@ -498,7 +503,7 @@ def time_graph_launches(torch, fn_list, reps):
             g.replay()
         b.record()
     torch.cuda.synchronize()
-    return a.elapsed_time(b) / (reps * len(fn_list))  # ms per call
+    return a.elapsed_time(b) / (reps * rounds * len(fn_list))  # ms per call
 
 
 def measure_extras(torch, ops, synth, roofline, l2, kernel, peak):

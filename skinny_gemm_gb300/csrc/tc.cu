@@ -86,6 +86,9 @@ namespace {
 #ifndef W4A16_TC_TILE_MAX_UNITS
 #define W4A16_TC_TILE_MAX_UNITS 4863  // largest stages x row tiles the tile kernel takes
 #endif
+#ifndef W4A16_TC_DYN_ALL
+#define W4A16_TC_DYN_ALL 1  // 0: deal units round-robin when K is not split
+#endif
 #ifndef W4A16_TC_STREAM_NSUB1_MIN_M
 #define W4A16_TC_STREAM_NSUB1_MIN_M 9  // smallest chunk the persistent kernel runs with 16-row warps
 #endif
@@ -599,9 +602,9 @@ __device__ __forceinline__ void build_chunks(const int32_t* __restrict__ ids, in
   }
 }
 
-// SPLIT: K is split over several units per tile (ks > 1); the units after
-// the first are then dealt dynamically, else round-robin (measured faster
-// without a split, on the LM heads).
+// SPLIT: K is split over several units per tile (ks > 1).  The units after
+// a warp's first are grabbed from a counter (LM head 262144x2560: 66.3 ->
+// 65.3 us against round-robin dealing; 262144x1536 and 16384^2 unchanged).
 // ROUTED (w4a16_mm_id): a unit is one chunk of tokens routed to one expert
 // times one tile of that expert, over the whole K; the slice sums are folded
 // in slice order as they complete, so every row equals w4a16_mm on the
@@ -613,6 +616,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   using G = Geo<NSUB>;
   constexpr int kW = G::kWarps, kRows = G::kRows;
   static_assert(!ROUTED || (!XSTAGED && !SPLIT), "the routed mode copies activations per stage, whole-K units");
+  constexpr bool DYN = (SPLIT || W4A16_TC_DYN_ALL) && !ROUTED;  // units after the first from the counter
   extern __shared__ uint8_t smem_raw[];
   pdl_launch_dependents();
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -652,7 +656,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   const int TW = gridDim.x * kW;
 
   // Work units of this warp.  The first is static (unit gw), so its weights
-  // can be requested before the wait for earlier kernels.  With SPLIT every
+  // can be requested before the wait for earlier kernels.  With DYN every
   // later one is grabbed from a counter in the workspace (unit TW + count)
   // when at most one stage of the previous one is left to request, so warps
   // that run faster take more units and no warp commits to a unit long
@@ -683,7 +687,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   };
   auto begin_unit = [&](int u) {
     iu = u;
-    if (SPLIT) s_units[iseq++ & 7u] = u;
+    if (DYN) s_units[iseq++ & 7u] = u;
     if (u >= 0) {
       if (ROUTED) {
         const int c = u / p.tiles;
@@ -709,7 +713,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   auto issue_next = [&](bool with_x) {  // after the wait only (grabs touch the workspace)
     if (iu < 0) return;
     if (ist == iend) {
-      if (SPLIT) {
+      if (DYN) {
         begin_unit(resolve(nxt));
         nxt = -1;
       } else {
@@ -718,7 +722,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
       if (iu < 0) return;
     }
     issue_stage(with_x);
-    if (SPLIT && nxt < 0 && iend - ist <= 1) nxt = grab();
+    if (DYN && nxt < 0 && iend - ist <= 1) nxt = grab();
   };
   // The weights never depend on earlier kernels: with p.prefetch the first
   // unit's first stages are requested before the wait for those kernels and
@@ -755,7 +759,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   }
   if (lane == 0) {
     if (iu >= 0) {
-      if (SPLIT && iend - ist <= 1) nxt = grab();
+      if (DYN && iend - ist <= 1) nxt = grab();
       const int first = ist - (int)R.issued;  // the unit's first stage
       for (uint32_t i = 0; i < R.issued; ++i) ring_issue_x(R, i, first + (int)i, p.x, s_tok, xring, p.K);
     }
@@ -881,7 +885,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   // in the order lane 0 recorded them
   int u = gw;
   for (uint32_t cseq = 0; !timed_out; ++cseq) {
-    if (SPLIT) {
+    if (DYN) {
       __syncwarp();
       u = s_units[cseq & 7u];
     } else if (cseq > 0) {
@@ -1018,7 +1022,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
     if (lane == 0) atomicOr(p.flags, W4A16_DEVICE_TIMEOUT);
     // finish this warp's grabs (up to the one that fails), so the count of
     // grabs stays exact and the counter is reset
-    if (SPLIT && lane == 0 && iu >= 0)
+    if (DYN && lane == 0 && iu >= 0)
       for (int v = nxt >= 0 ? resolve(nxt) : 0; v >= 0; v = resolve(grab())) {
       }
     // let copies already in flight land before shared memory is released
