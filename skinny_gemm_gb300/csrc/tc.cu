@@ -658,7 +658,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   // Work units of this warp.  The first is static (unit gw), so its weights
   // can be requested before the wait for earlier kernels.  With DYN every
   // later one is grabbed from a counter in the workspace (unit TW + count)
-  // when at most one stage of the previous one is left to request, so warps
+  // when at most `lead` stages of the previous one are left to request, so warps
   // that run faster take more units and no warp commits to a unit long
   // before it can start it; otherwise the warp takes units gw + TW, ...
   // Lane 0 streams the units in order; dealt ones it records in s_units (a
@@ -679,6 +679,10 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   int irow = 0;                    // lane 0: first weight row of unit iu
   uint32_t iseq = 0;
   const int last_grab = max(0, p.units - TW) + min(TW, p.units) - 1;
+  // Stages of the current unit still to request when the next is grabbed:
+  // one, or two for units of three stages or fewer (LM head 262144x1536:
+  // 41.8 -> 41.5 us; one is best from five stages on: 262144x2560, 16384^2).
+  const int lead = p.sl <= 3 ? 2 : 1;
   auto grab = [&]() { return atomicAdd(p.sched, 1); };
   auto resolve = [&](int c) {  // the unit of grab count c, -1 past the end
     if (c == last_grab) *p.sched = 0;
@@ -722,7 +726,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
       if (iu < 0) return;
     }
     issue_stage(with_x);
-    if (DYN && nxt < 0 && iend - ist <= 1) nxt = grab();
+    if (DYN && nxt < 0 && iend - ist <= lead) nxt = grab();
   };
   // The weights never depend on earlier kernels: with p.prefetch the first
   // unit's first stages are requested before the wait for those kernels and
@@ -759,7 +763,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   }
   if (lane == 0) {
     if (iu >= 0) {
-      if (DYN && iend - ist <= 1) nxt = grab();
+      if (DYN && iend - ist <= lead) nxt = grab();
       const int first = ist - (int)R.issued;  // the unit's first stage
       for (uint32_t i = 0; i < R.issued; ++i) ring_issue_x(R, i, first + (int)i, p.x, s_tok, xring, p.K);
     }
