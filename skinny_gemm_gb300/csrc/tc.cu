@@ -843,31 +843,46 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   int pend_tile = -1;               // partials stored, arrival not yet counted
   int cnt_tile = -1, cnt_old = 0;   // arrival counted (lane 0 holds the old count)
 
-  auto reduce_tile = [&](int tile) {
-    // Sum the ksplit partials of a finished tile in slice order.  Lane 0's
-    // fence (after it saw the last arrival) and the warp barrier order every
-    // lane's loads after the other units' partial stores.  Loads are issued
-    // eight slices at a time; the additions stay in slice order.
+  auto reduce_tiles = [&](int ta, int tb) {
+    // Sum the ksplit partials of finished tiles ta and tb (-1: none) in
+    // slice order.  Lane 0's fence (after it saw the last arrivals) and the
+    // warp barrier order every lane's loads after the other units' partial
+    // stores.  Loads are issued eight slices of both tiles at a time; the
+    // additions stay in slice order.
     if (lane == 0) __threadfence();
     __syncwarp();
     // lane = (column n0, row r): with 16 rows two columns at a time
     const int r = lane % kRows, n0 = lane / kRows;
-    const int row = tile * kRows + r;
+    const int tt[2] = {ta, tb};
     for (int n = n0; n < mc; n += 32 / kRows) {
-      const float* q = p.part + ((int64_t)tile * p.ks * 8 + n) * kRows + r;
-      float sum = 0.0f;
+      float sum[2] = {0.0f, 0.0f};
       for (int s0 = 0; s0 < p.ks; s0 += 8) {
-        float v[8];
+        float v[2][8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = (s0 + j < p.ks) ? __ldcg(q + (int64_t)(s0 + j) * 8 * kRows) : 0.0f;
+        for (int h = 0; h < 2; ++h) {
+          const float* q = p.part + ((int64_t)max(tt[h], 0) * p.ks * 8 + n) * kRows + r;
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (s0 + j < p.ks) sum = (s0 + j == 0) ? v[0] : __fadd_rn(sum, v[j]);
+          for (int j = 0; j < 8; ++j)
+            v[h][j] = (tt[h] >= 0 && s0 + j < p.ks) ? __ldcg(q + (int64_t)(s0 + j) * 8 * kRows) : 0.0f;
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (s0 + j < p.ks) sum[h] = (s0 + j == 0) ? v[h][0] : __fadd_rn(sum[h], v[h][j]);
       }
-      if (row < p.N) p.y[(int64_t)s_tok[n] * p.N + row] = f32_to_bf16_bits(sum);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int row = tt[h] * kRows + r;
+        if (tt[h] >= 0 && row < p.N) p.y[(int64_t)s_tok[n] * p.N + row] = f32_to_bf16_bits(sum[h]);
+      }
     }
-    if (lane == 0) p.cnt[tile] = 0;
+    if (lane == 0) {
+      if (ta >= 0) p.cnt[ta] = 0;
+      if (tb >= 0) p.cnt[tb] = 0;
+    }
   };
+  auto reduce_tile = [&](int tile) { reduce_tiles(tile, -1); };
 
   // Count the arrival of this warp's stored partials of `tile`: a warp
   // barrier, then one release fence by lane 0 before its atomic.
@@ -1012,15 +1027,15 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
     }
   }
   if (!timed_out) {
-    if (cnt_tile >= 0) {
-      const int old = __shfl_sync(0xffffffffu, cnt_old, 0);
-      if (old == p.ks - 1) reduce_tile(cnt_tile);
-    }
+    // The tile counted one unit ago and this warp's last one: both arrivals
+    // are known before either sum, so their loads go out together.
+    int prev = -1, last = -1;
+    if (cnt_tile >= 0 && __shfl_sync(0xffffffffu, cnt_old, 0) == p.ks - 1) prev = cnt_tile;
     if (pend_tile >= 0) {
       count_arrival(pend_tile);
-      const int old = __shfl_sync(0xffffffffu, cnt_old, 0);
-      if (old == p.ks - 1) reduce_tile(cnt_tile);
+      if (__shfl_sync(0xffffffffu, cnt_old, 0) == p.ks - 1) last = pend_tile;
     }
+    if (prev >= 0 || last >= 0) reduce_tiles(prev, last);
   }
   if (timed_out) {
     if (lane == 0) atomicOr(p.flags, W4A16_DEVICE_TIMEOUT);
