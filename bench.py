@@ -535,14 +535,28 @@ def measure_extras(torch, ops, synth, roofline, l2, kernel, peak):
         verify[f"{N}x{K}"]["t5_over_t1"] = round(t[5][0] / t[1][0], 3)
         del ws
     out["verify"] = verify
-    lm = {}
+    lm, lm_argmax = {}, {}
     for (N, K) in [(262144, 1536), (262144, 2560)]:
         ws = cold_set(N, K, 8)
         for M in (1, 3):
             ms, g = gbps(ws, M, N, K, 10)
             lm[f"{N}x{K}_M{M}"] = {"us": round(1e3 * ms, 2), "GBps": round(g, 1), "frac": round(g / peak, 4)}
+        # greedy head: w4a16_mm_argmax against w4a16_mm followed by torch.argmax over the logits
+        for M in (1, 3):
+            x = torch.randn(M, K, device="cuda").to(torch.bfloat16)
+            y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+            idx = torch.empty(M, dtype=torch.int32, device="cuda")
+            val = torch.empty(M, dtype=torch.bfloat16, device="cuda")
+            fused = [lambda w=w: ops.mm_argmax(x, w, idx=idx, val=val) for w in ws]
+            unfused = [lambda w=w: (ops.mm(x, w, out=y, kernel=kernel), torch.argmax(y, dim=-1)) for w in ws]
+            ms_f = time_graph_launches(torch, fused, 10)
+            ms_u = time_graph_launches(torch, unfused, 10)
+            g = (roofline.mm_bytes(M, N, K) - 2 * M * N + 6 * M) / (ms_f * 1e-3) / 1e9  # no logits, idx + val out
+            lm_argmax[f"{N}x{K}_M{M}"] = {"us": round(1e3 * ms_f, 2), "GBps": round(g, 1), "frac": round(g / peak, 4),
+                                          "mm_then_torch_argmax_us": round(1e3 * ms_u, 2)}
         del ws
     out["lm_head"] = lm
+    out["lm_head_argmax"] = lm_argmax
     dense = {}
     ws = cold_set(16384, 16384, 9)
     for M in (1, 2, 4, 8):

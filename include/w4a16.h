@@ -144,6 +144,22 @@ int w4a16_mm_kernel(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* s
 int w4a16_mm_noalloc(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* scales,
                      const w4a16_bf16* biases, w4a16_bf16* y, int M, int N, int K, void* stream);
 
+/* Fused argmax over the outputs (greedy decoding on a tied LM head; the
+ * drafter of [G4MK] "Implementation notes" runs its head with an in-kernel
+ * argmax):
+ *   idx[m] = argmax_n bf16(y[m][n]),  val[m] = bf16(y[m][idx[m]])
+ * where y is exactly what w4a16_mm computes (the same canonical arithmetic,
+ * so idx is the argmax of w4a16_mm's rows bit for bit); y is never written.
+ * Ties go to the smallest n; a NaN output ranks above every number and
+ * -0 just below +0.
+ * idx int32 [M] (4-byte aligned) and val bf16 [M] (may be NULL) are device
+ * pointers.  Runs the persistent tensor-core kernel: needs K % 512 == 0
+ * (otherwise W4A16_ERR_KERNEL).  Uses the per-(device, stream) workspace of
+ * w4a16_mm (allocated on first use, as there); other errors as w4a16_mm. */
+int w4a16_mm_argmax(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* scales,
+                    const w4a16_bf16* biases, int32_t* idx, w4a16_bf16* val, int M, int N, int K,
+                    void* stream);
+
 /* Grouped projections: several independent w4a16_mm calls that share K and
  * M, in one launch where that pays (a decoder layer's q/k/v projections read
  * the same activations, as do gate/up; launching them together saves the

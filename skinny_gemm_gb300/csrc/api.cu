@@ -279,6 +279,32 @@ int w4a16_mm_noalloc(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* 
   return W4A16_OK;
 }
 
+int w4a16_mm_argmax(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* scales, const w4a16_bf16* biases,
+                    int32_t* idx, w4a16_bf16* val, int M, int N, int K, void* stream) {
+  if (env().fault == kFaultValidate) return fail(W4A16_ERR_SHAPE, "injected validation fault (W4A16_FAULT)");
+  if (int rc = validate_mm(x, Wq, scales, biases, idx, M, N, K)) return rc;
+  if (M == 0) return W4A16_OK;
+  if (misaligned(idx, 4) || misaligned(val, 2)) return fail(W4A16_ERR_ALIGN, "idx must be 4-byte and val 2-byte aligned");
+  if (!tc_supported(N, K))
+    return fail(W4A16_ERR_KERNEL, "w4a16_mm_argmax runs the tensor-core kernel, which needs K %% 512 == 0 (K = %d)", K);
+  if (env().fault == kFaultLaunch) return fail(W4A16_ERR_CUDA, "injected launch fault (W4A16_FAULT)");
+  LaunchArgs a{};
+  a.x = x; a.Wq = Wq; a.S = scales; a.B = biases; a.y = nullptr;
+  a.N = N; a.K = K;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.pdl = env().pdl;
+  a.tc_path = 1;
+  if (int rc = flag_pointer(&a.flags)) return rc;
+  for (int row0 = 0; row0 < M; row0 += kMaxChunk) {
+    a.row0 = row0;
+    a.M = (M - row0 < kMaxChunk) ? M - row0 : kMaxChunk;
+    cudaError_t e = launch_tc_argmax(a, idx, val);
+    if (e == cudaErrorInvalidValue) return fail(W4A16_ERR_SHAPE, "N = %d, K = %d exceeds the persistent kernel's workspace", N, K);
+    if (e != cudaSuccess) return cuda_fail(e, "w4a16_mm_argmax launch");
+  }
+  return W4A16_OK;
+}
+
 int w4a16_mm_group(const w4a16_mm_item* items, int count, int M, int K, void* stream) {
   if (env().fault == kFaultValidate) return fail(W4A16_ERR_SHAPE, "injected validation fault (W4A16_FAULT)");
   if (count < 1 || count > W4A16_MAX_GROUP)

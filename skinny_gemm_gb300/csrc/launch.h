@@ -43,6 +43,8 @@ bool tc_supported(int N, int K);
 bool tc_tile_fits(int N, int K, int M);
 cudaError_t launch_tc(const LaunchArgs& a, const w4a16_plan& p);
 cudaError_t launch_tc_id(const LaunchArgs& a, const w4a16_plan& p);
+// w4a16_mm_argmax: the persistent kernel in argmax mode (rows a.row0 .. a.row0 + a.M).
+cudaError_t launch_tc_argmax(const LaunchArgs& a, int32_t* idx, uint16_t* val);
 // Grouped tensor-core launch (w4a16_mm_group): items sharing K and M.
 struct GroupItem {
   const uint16_t* x;

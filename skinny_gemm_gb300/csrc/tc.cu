@@ -499,7 +499,9 @@ __host__ __device__ inline int ring_bytes(int stages, int mcap) {
 // ---- persistent kernel (w4a16_mm) ------------------------------------------------------
 
 // Bytes after the barriers: token rows [8] and every warp's unit ring [8] (ints).
-constexpr int kStreamMisc = 4 * (kMaxChunk + 8 * 8) + 32;
+// tokens [8] | dealt units [8 warps][8] | activation barrier | argmax mode:
+// best keys [8 warps][8 columns] and the CTA's [8] (u64)
+constexpr int kStreamMisc = 4 * (kMaxChunk + 8 * 8) + 32 + 8 * (8 * 8 + 8);
 
 struct StreamParams {
   const uint16_t* x;
@@ -518,7 +520,30 @@ struct StreamParams {
   int prefetch;     // request the first weight stages before waiting for earlier kernels
   const int32_t* ids;  // routed mode: expert id of each of T tokens, E experts of N rows each
   int T, E;
+  unsigned long long* best;  // argmax mode: [8] running keys, zero between launches
+  int* done;                 // and the finished-CTA counter, zero between launches
+  int32_t* idx;              // argmax of activation row row0 + n over the N outputs
+  uint16_t* val;             // and its value (may be null)
 };
+
+// Argmax mode: an output value as a key whose unsigned order is the value's
+// order (bf16 bits mapped to an order-preserving 16-bit code, every NaN
+// above +inf), ties going to the smaller row n.
+__device__ __forceinline__ unsigned long long argmax_key(uint16_t b, int n) {
+  const bool nan = (b & 0x7F80u) == 0x7F80u && (b & 0x7Fu) != 0u;
+  const uint32_t ord = nan ? 0xFFFFu : (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
+  return ((unsigned long long)ord << 32) | (0xFFFFFFFFu - (uint32_t)n);
+}
+
+__device__ __forceinline__ unsigned long long max_u64(unsigned long long a, unsigned long long b) {
+  return a > b ? a : b;
+}
+
+// Maximum over the lanes given by the xor masks from `from` down to 1.
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long k, int from, int to) {
+  for (int m = from; m >= to; m >>= 1) k = max_u64(k, __shfl_xor_sync(0xffffffffu, k, m));
+  return k;
+}
 
 // Tile and slice of work unit u.  Units whose slice has the full length come
 // first, tile-major; the shorter last slice of every tile (when the slice
@@ -610,12 +635,17 @@ __device__ __forceinline__ void build_chunks(const int32_t* __restrict__ ids, in
 // in slice order as they complete, so every row equals w4a16_mm on the
 // selected expert bit for bit.  Units are dealt round-robin over the chunks
 // the ids select, so only the weights of experts with tokens are read.
-template <int NSUB, bool ALLCOLS, bool XSTAGED, bool SPLIT, bool ROUTED = false>
+// ARGMAX (w4a16_mm_argmax): the outputs are not stored; every warp keeps the
+// largest key of each activation row over its units, the CTAs merge theirs
+// with 64-bit atomic maxima, and the last CTA out writes the argmax of every
+// row (the outputs' bits are those w4a16_mm stores).
+template <int NSUB, bool ALLCOLS, bool XSTAGED, bool SPLIT, bool ROUTED = false, bool ARGMAX = false>
 __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_min_blocks<NSUB>()) tc_stream_kernel(
     const __grid_constant__ Maps maps, StreamParams p) {
   using G = Geo<NSUB>;
   constexpr int kW = G::kWarps, kRows = G::kRows;
   static_assert(!ROUTED || (!XSTAGED && !SPLIT), "the routed mode copies activations per stage, whole-K units");
+  static_assert(!ARGMAX || (!ROUTED && NSUB == 2), "argmax over plain 32-row units");
   constexpr bool DYN = (SPLIT || W4A16_TC_DYN_ALL) && !ROUTED;  // units after the first from the counter
   extern __shared__ uint8_t smem_raw[];
   pdl_launch_dependents();
@@ -648,6 +678,9 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   if (!ROUTED && threadIdx.x < mc) s_tok[threadIdx.x] = p.row0 + threadIdx.x;
   const uint32_t xbar = smem_u32(s_tok + kMaxChunk + 8 * 8);  // the pre-staged activations' copy
   if (XSTAGED && threadIdx.x == 0) mbar_init(xbar, 1);
+  unsigned long long* s_best = reinterpret_cast<unsigned long long*>(s_tok + kMaxChunk + 8 * 8 + 8);  // [warp][8]
+  unsigned long long* s_cta_best = s_best + 8 * 8;
+  if (ARGMAX && threadIdx.x < 8 * 8 + 8) s_best[threadIdx.x] = 0ull;
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   __syncthreads();
 
@@ -871,10 +904,21 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
           for (int j = 0; j < 8; ++j)
             if (s0 + j < p.ks) sum[h] = (s0 + j == 0) ? v[h][0] : __fadd_rn(sum[h], v[h][j]);
       }
+      if (ARGMAX) {
+        unsigned long long k = 0ull;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int row = tt[h] * kRows + r;
-        if (tt[h] >= 0 && row < p.N) p.y[(int64_t)s_tok[n] * p.N + row] = f32_to_bf16_bits(sum[h]);
+        for (int h = 0; h < 2; ++h) {
+          const int row = tt[h] * kRows + r;
+          if (tt[h] >= 0 && row < p.N) k = max_u64(k, argmax_key(f32_to_bf16_bits(sum[h]), row));
+        }
+        k = warp_max_u64(k, 16, 1);  // the 32 rows of the tile
+        if (lane == 0) s_best[warp * 8 + n] = max_u64(s_best[warp * 8 + n], k);
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int row = tt[h] * kRows + r;
+          if (tt[h] >= 0 && row < p.N) p.y[(int64_t)s_tok[n] * p.N + row] = f32_to_bf16_bits(sum[h]);
+        }
       }
     }
     if (lane == 0) {
@@ -997,6 +1041,22 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
           const int n = 2 * t + (i & 1);
           if (n < umc && row < p.N) p.y[(int64_t)utok[n] * p.N + row] = f32_to_bf16_bits(sum[s][i]);
         }
+    } else if (!SPLIT && ARGMAX) {
+      // columns 2t and 2t + 1: the lane's rows, then the eight lanes of t
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int n = 2 * t + c;
+        unsigned long long k = 0ull;
+#pragma unroll
+        for (int s = 0; s < NSUB; ++s)
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const int row = prow[2 * s + rr];
+            if (row < p.N) k = max_u64(k, argmax_key(f32_to_bf16_bits(acc[s][2 * rr + c]), row));
+          }
+        k = warp_max_u64(k, 16, 4);
+        if (g == 0 && n < mc) s_best[warp * 8 + n] = max_u64(s_best[warp * 8 + n], k);
+      }
     } else if (!SPLIT) {
 #pragma unroll
       for (int s = 0; s < NSUB; ++s)
@@ -1050,6 +1110,34 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
     while (R.consumed < issued) {
       mbar_wait(R.bars0 + 8 * (R.consumed % (uint32_t)S), (R.consumed / (uint32_t)S) & 1u);
       ++R.consumed;
+    }
+  }
+  if (ARGMAX) {
+    // this warp's keys into the CTA's, the CTA's into the launch's; the last
+    // CTA out (every CTA fences its atomics before counting itself) turns
+    // the keys into indices and values and leaves both counters at zero
+    __syncwarp();
+    if (lane < mc) atomicMax(s_cta_best + lane, s_best[warp * 8 + lane]);
+    __syncthreads();
+    if (threadIdx.x < mc) {
+      atomicMax(p.best + threadIdx.x, s_cta_best[threadIdx.x]);
+      __threadfence();
+    }
+    __syncthreads();
+    int* s_last = reinterpret_cast<int*>(s_cta_best);  // the CTA's keys are merged by now
+    if (threadIdx.x == 0) {
+      __threadfence();
+      *s_last = atomicAdd(p.done, 1) == (int)gridDim.x - 1;
+    }
+    __syncthreads();
+    if (*s_last && threadIdx.x < mc) {  // one thread per activation row
+      __threadfence();
+      const int n = threadIdx.x;
+      const unsigned long long k = atomicExch(p.best + n, 0ull);
+      const uint32_t ord = (uint32_t)(k >> 32);
+      p.idx[p.row0 + n] = (int32_t)(0xFFFFFFFFu - (uint32_t)k);
+      if (p.val) p.val[p.row0 + n] = (uint16_t)((ord & 0x8000u) ? (ord & 0x7FFFu) : (~ord & 0xFFFFu));
+      if (n == 0) *p.done = 0;
     }
   }
 }
@@ -1605,11 +1693,11 @@ cudaError_t launch_ex(Kern fn, dim3 grid, dim3 block, int smem, cudaStream_t str
   return cudaLaunchKernelEx(&cfg, fn, args...);
 }
 
-template <int NSUB, bool A, bool X, bool SPLIT>
+template <int NSUB, bool A, bool X, bool SPLIT, bool ARGMAX = false>
 cudaError_t stream_launch_t(const Maps& map, const StreamParams& p, int sms, int smem, DeviceInfo& d,
                             cudaStream_t stream, bool pdl) {
   constexpr int kW = Geo<NSUB>::kWarps;
-  auto* fn = tc_stream_kernel<NSUB, A, X, SPLIT>;
+  auto* fn = tc_stream_kernel<NSUB, A, X, SPLIT, false, ARGMAX>;
   if (cudaError_t e = allow_smem(fn, d)) return e;
   int per_sm = 0;
   if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kW * 32, smem)) return e;
@@ -1634,13 +1722,24 @@ cudaError_t launch_stream_t(const Maps& map, StreamParams p, int sms, DeviceInfo
   if (staged) smem += xstage_bytes(p.M, p.K);
   const bool on = pdl > 0;
   using Fn = cudaError_t (*)(const Maps&, const StreamParams&, int, int, DeviceInfo&, cudaStream_t, bool);
+  const bool split = p.ks > 1;
+  if (p.idx) {  // argmax mode (32-row warps only)
+    if (NSUB != 2) return cudaErrorInvalidConfiguration;
+    // [allcols][staged][split]
+    static const Fn fns[2][2][2] = {
+        {{stream_launch_t<2, false, false, false, true>, stream_launch_t<2, false, false, true, true>},
+         {stream_launch_t<2, false, true, false, true>, stream_launch_t<2, false, true, true, true>}},
+        {{stream_launch_t<2, true, false, false, true>, stream_launch_t<2, true, false, true, true>},
+         {stream_launch_t<2, true, true, false, true>, stream_launch_t<2, true, true, true, true>}}};
+    return fns[allcols][staged][split](map, p, sms, smem, d, stream, on);
+  }
   // [allcols][staged][split]
   static const Fn fns[2][2][2] = {
       {{stream_launch_t<NSUB, false, false, false>, stream_launch_t<NSUB, false, false, true>},
        {stream_launch_t<NSUB, false, true, false>, stream_launch_t<NSUB, false, true, true>}},
       {{stream_launch_t<NSUB, true, false, false>, stream_launch_t<NSUB, true, false, true>},
        {stream_launch_t<NSUB, true, true, false>, stream_launch_t<NSUB, true, true, true>}}};
-  return fns[allcols][staged][p.ks > 1](map, p, sms, smem, d, stream, on);
+  return fns[allcols][staged][split](map, p, sms, smem, d, stream, on);
 }
 
 // Row subtiles per warp of the persistent kernel for a chunk of M rows.
@@ -1808,12 +1907,14 @@ StreamWork stream_work(const Shape& s, int N, int M) {
   return w;
 }
 
-// The last two counters of the workspace are the persistent kernel's unit
-// scheduler (grabbed units, finished warps); the tiles use the others.
-constexpr int kWsSched = kWsTiles - 2;
+// The last 32 counters of the workspace belong to the persistent kernel's
+// schedulers: the unit-grab counter, the argmax mode's finished-CTA counter
+// and its eight 64-bit keys; the tiles' arrival counters are the others.
+constexpr int kWsSched = kWsTiles - 2;   // grab counter, then the finished-CTA counter
+constexpr int kWsBest = kWsTiles - 32;   // u64 [8] (byte offset a multiple of 8)
 
 bool workspace_fits(const Shape& s, const StreamWork& w) {
-  return s.ks == 1 || (w.tiles <= kWsSched && (size_t)w.units * 8 * w.rows * 4 <= kWsPartBytes);
+  return s.ks == 1 || (w.tiles <= kWsBest && (size_t)w.units * 8 * w.rows * 4 <= kWsPartBytes);
 }
 
 cudaError_t launch_stream(const Maps& maps, StreamParams p, const StreamWork& w, DeviceInfo& d,
@@ -1906,13 +2007,15 @@ void plan_tc(int N, int K, int tc_path, w4a16_plan* p) {
   p->smem_bytes = smem;
 }
 
-cudaError_t launch_tc(const LaunchArgs& a, const w4a16_plan& plan) {
-  (void)plan;
+// w4a16_mm (idx == nullptr) or, always on the persistent kernel, its argmax
+// mode (w4a16_mm_argmax).
+cudaError_t launch_tc_impl(const LaunchArgs& a, int32_t* idx, uint16_t* val) {
   const Shape s = tc_shape(a.N, a.K);
   int dev = 0;
   if (cudaError_t e = cudaGetDevice(&dev)) return e;
-  StreamParams p;
+  StreamParams p{};
   p.x = a.x; p.S = a.S; p.B = a.B; p.y = a.y; p.flags = a.flags;
+  p.idx = idx; p.val = val;
   p.N = a.N; p.K = a.K; p.M = a.M; p.row0 = a.row0;
   p.nst = s.nst; p.sl = s.sl; p.ks = s.ks; p.tiles = s.tiles; p.units = s.units;
   p.stages = 2;
@@ -1922,7 +2025,7 @@ cudaError_t launch_tc(const LaunchArgs& a, const w4a16_plan& plan) {
   p.sched = nullptr;
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DeviceInfo& d = device_info(dev);
-  if (a.tc_path != 1) {
+  if (a.tc_path != 1 && !idx) {
     const TilePlan tp = tile_plan(s, a.N, a.M, a.tc_path == 2, d.sms);
     if (tp.kc > 0) return launch_tile(a, s, tp, d, false);
     if (a.tc_path == 2) return cudaErrorInvalidConfiguration;
@@ -1935,8 +2038,19 @@ cudaError_t launch_tc(const LaunchArgs& a, const w4a16_plan& plan) {
   if (cudaError_t e = workspace(dev, a.stream, &ws)) return e;
   p.cnt = static_cast<int*>(ws);
   p.sched = p.cnt + kWsSched;
+  p.done = p.cnt + kWsSched + 1;
+  p.best = reinterpret_cast<unsigned long long*>(p.cnt + kWsBest);
   p.part = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsCounterBytes);
   return launch_stream(maps, p, w, d, a.stream, a.pdl);
+}
+
+cudaError_t launch_tc(const LaunchArgs& a, const w4a16_plan& plan) {
+  (void)plan;
+  return launch_tc_impl(a, nullptr, nullptr);
+}
+
+cudaError_t launch_tc_argmax(const LaunchArgs& a, int32_t* idx, uint16_t* val) {
+  return idx ? launch_tc_impl(a, idx, val) : cudaErrorInvalidValue;
 }
 
 // Tokens per chunk of the routed tile kernel: twice the mean per expert (at
@@ -2102,7 +2216,7 @@ cudaError_t launch_tc_noalloc(const LaunchArgs& a) {
   int dev = 0;
   if (cudaError_t e = cudaGetDevice(&dev)) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  StreamParams p;
+  StreamParams p{};
   p.x = a.x; p.S = a.S; p.B = a.B; p.y = a.y; p.flags = a.flags;
   p.N = a.N; p.K = a.K; p.M = a.M; p.row0 = a.row0;
   p.nst = s.nst; p.sl = s.sl; p.ks = s.ks; p.tiles = s.tiles; p.units = s.units;

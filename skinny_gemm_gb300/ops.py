@@ -24,7 +24,7 @@ KERNELS = {"auto": 0, "simt": 1, "tc": 2, "vanilla": 3, "tc_stream": 4, "tc_tile
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 DEVICE_BAD_ID = 1
 
-EXPORTS = ("w4a16_mm", "w4a16_mm_kernel", "w4a16_mm_group", "w4a16_mm_id", "w4a16_mm_id_kernel",
+EXPORTS = ("w4a16_mm", "w4a16_mm_kernel", "w4a16_mm_group", "w4a16_mm_argmax", "w4a16_mm_id", "w4a16_mm_id_kernel",
            "w4a16_unpack", "w4a16_dequant", "w4a16_get_plan", "w4a16_device_status", "w4a16_last_error",
            "w4a16_debug_reload_env", "w4a16_version")
 MAX_GROUP = 8
@@ -79,13 +79,14 @@ def lib() -> ctypes.CDLL:
             L.w4a16_mm_kernel.argtypes = [P, P, P, P, P, i, i, i, i, P]
             L.w4a16_mm_noalloc.argtypes = [P, P, P, P, P, i, i, i, P]
             L.w4a16_mm_group.argtypes = [ctypes.POINTER(Item), i, i, i, P]
+            L.w4a16_mm_argmax.argtypes = [P, P, P, P, P, P, i, i, i, P]
             L.w4a16_mm_id.argtypes = [P, P, P, P, P, P, i, i, i, i, P]
             L.w4a16_mm_id_kernel.argtypes = [P, P, P, P, P, P, i, i, i, i, i, P]
             L.w4a16_unpack.argtypes = [P, P, i, i, P]
             L.w4a16_dequant.argtypes = [P, P, P, P, i, i, P]
             L.w4a16_get_plan.argtypes = [i, i, i, ctypes.POINTER(Plan)]
             L.w4a16_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
-            for f in ("w4a16_mm", "w4a16_mm_kernel", "w4a16_mm_noalloc", "w4a16_mm_group", "w4a16_mm_id",
+            for f in ("w4a16_mm", "w4a16_mm_kernel", "w4a16_mm_noalloc", "w4a16_mm_group", "w4a16_mm_argmax", "w4a16_mm_id",
                       "w4a16_mm_id_kernel", "w4a16_unpack", "w4a16_dequant", "w4a16_get_plan", "w4a16_device_status"):
                 getattr(L, f).restype = ctypes.c_int
             L.w4a16_last_error.restype = ctypes.c_char_p
@@ -194,6 +195,37 @@ def mm(x: torch.Tensor, w: W4Matrix, out: torch.Tensor | None = None, kernel=Non
         rc = L.w4a16_mm_kernel(*args, k, _stream_ptr(stream))
     _raise(rc)
     return out
+
+
+def mm_argmax(x: torch.Tensor, w: W4Matrix, idx: torch.Tensor | None = None, val: torch.Tensor | None = None,
+              stream=None):
+    """(idx, val) through ``w4a16_mm_argmax``: for every row of x (leading dims
+    flatten into M) the index of the largest output of ``mm(x, w)`` and that
+    output (ties to the smallest index), without writing the outputs.
+
+    idx is int32 [..], val bf16 [..]; pass ``val=False`` to skip the values."""
+    if w.E != 1:
+        raise ValueError("mm_argmax takes a single matrix")
+    _dev_tensor(x, torch.bfloat16, "x")
+    if x.shape[-1] != w.K:
+        raise ValueError(f"x has K={x.shape[-1]}, weights have K={w.K}")
+    M = x.numel() // w.K
+    if idx is None:
+        idx = torch.empty(x.shape[:-1], dtype=torch.int32, device=x.device)
+    _dev_tensor(idx, torch.int32, "idx")
+    if idx.numel() != M:
+        raise ValueError("idx must have one element per row")
+    if val is None:
+        val = torch.empty(x.shape[:-1], dtype=torch.bfloat16, device=x.device)
+    if val is not False:
+        _dev_tensor(val, torch.bfloat16, "val")
+        if val.numel() != M:
+            raise ValueError("val must have one element per row")
+    vp = val.data_ptr() if val is not False else None
+    rc = lib().w4a16_mm_argmax(x.data_ptr(), w.Wq.data_ptr(), w.scales.data_ptr(), w.biases.data_ptr(), idx.data_ptr(),
+                               vp, M, w.N, w.K, _stream_ptr(stream))
+    _raise(rc)
+    return idx, (val if val is not False else None)
 
 
 def mm_group(xs, ws, outs=None, stream=None) -> list:

@@ -104,6 +104,19 @@ def test_mm_id_errors(L):
     assert L.w4a16_mm_id(P, P, P, P, None, P, 8, 64, 64, 8, None) == ops.ERR_NULL
 
 
+def test_mm_argmax_errors(L):
+    """Fail-closed checks of w4a16_mm_argmax, all before any device call."""
+    f = L.w4a16_mm_argmax
+    assert f(P, P, P, P, P, P, 0, 64, 512, None) == ops.OK          # M == 0: no-op
+    assert f(P, P, P, P, P, None, -1, 64, 512, None) == ops.ERR_SHAPE
+    assert f(P, P, P, P, P, P, 1, 64, 96, None) == ops.ERR_SHAPE    # K % 64
+    assert f(P, P, P, P, None, P, 1, 64, 512, None) == ops.ERR_NULL  # idx
+    assert f(P + 8, P, P, P, P, P, 1, 64, 512, None) == ops.ERR_ALIGN
+    assert f(P, P, P, P, P + 2, P, 1, 64, 512, None) == ops.ERR_ALIGN  # idx 4-byte
+    assert f(P, P, P, P, P, P + 1, 1, 64, 512, None) == ops.ERR_ALIGN  # val 2-byte
+    assert f(P, P, P, P, P, P, 1, 64, 448, None) == ops.ERR_KERNEL   # tensor-core family only
+
+
 def test_debug_entry_point_errors(L):
     assert L.w4a16_unpack(P, P, 4, 12, None) == ops.ERR_SHAPE
     assert L.w4a16_unpack(None, P, 4, 64, None) == ops.ERR_NULL

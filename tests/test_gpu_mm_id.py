@@ -135,3 +135,22 @@ def test_routed_many_tokens_take_the_other_launch_shapes():
     assert np.array_equal(bf16_bits(a), bf16_bits(b))
     yr, ad = oracle.mm_id(xb, hw.Wq, hw.scales, hw.biases, ids_np, T, N, K, E)
     assert_parity(a, yr, ad, "mm_id T=80")
+
+
+@pytest.mark.parametrize("T,E,same", [(32, 40, False), (32, 3, True), (31, 9, False), (2, 2, True)])
+def test_routed_persistent_mode_edges(T, E, same):
+    """The persistent routed mode at its token limit (32), with more experts
+    than tokens, one expert taking every token (four chunks of eight), a row
+    count that is not a multiple of the 32-row unit, and K = 1536 (three
+    slice sums folded per unit); bitwise equal to the tile launch shape."""
+    N, K = 200, 1536
+    hw, w = _experts(T + 100 * E, E, N, K)
+    ids_np = np.full(T, E - 1, dtype=np.int32) if same else synth.make_ids(T + E, T, E)
+    ids = torch.from_numpy(ids_np).cuda()
+    xb = synth.make_x(T * E, T, K)
+    x = to_dev_bf16(xb)
+    a = ops.mm_id(x, w, ids)
+    b = ops.mm_id(x, w, ids, kernel="tc_tile")
+    assert np.array_equal(bf16_bits(a), bf16_bits(b))
+    yr, ad = oracle.mm_id(xb, hw.Wq, hw.scales, hw.biases, ids_np, T, N, K, E)
+    assert_parity(a, yr, ad, f"routed T={T} E={E}")
