@@ -554,6 +554,16 @@ def measure_extras(torch, ops, synth, roofline, l2, kernel, peak):
             g = (roofline.mm_bytes(M, N, K) - 2 * M * N + 6 * M) / (ms_f * 1e-3) / 1e9  # no logits, idx + val out
             lm_argmax[f"{N}x{K}_M{M}"] = {"us": round(1e3 * ms_f, 2), "GBps": round(g, 1), "frac": round(g / peak, 4),
                                           "mm_then_torch_argmax_us": round(1e3 * ms_u, 2)}
+        if K == 2560:  # the tied table as embeddings: a decode step's rows and a prefill's
+            emb = {}
+            for T in (8, 4096):
+                ids = torch.from_numpy(synth.make_ids(1, T, N)).cuda()
+                e_out = torch.empty(T, K, dtype=torch.bfloat16, device="cuda")
+                ms_e = time_graph_launches(torch, [lambda w=w: ops.embed(ids, w, out=e_out) for w in ws], 10)
+                nb = T * K * (0.5 + 4 / 64) + T * K * 2 + 4 * T
+                emb[f"T{T}"] = {"us": round(1e3 * ms_e, 3), "GBps": round(nb / (ms_e * 1e-3) / 1e9, 1),
+                                "frac": round(nb / (ms_e * 1e-3) / 1e9 / peak, 4)}
+            out["embed_262144x2560"] = emb
         del ws
     out["lm_head"] = lm
     out["lm_head_argmax"] = lm_argmax

@@ -210,6 +210,18 @@ int w4a16_mm_id_kernel(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16
                        const w4a16_bf16* biases, const int32_t* ids, w4a16_bf16* y,
                        int T, int N, int K, int E, int kernel, void* stream);
 
+/* Quantized embedding rows (the row lookup of [W2D2] "Task 1: Implement
+ * Quantized Linear and Embedding": gather the selected packed rows, unpack,
+ * q * scale + bias; the table stays packed):
+ *   out[t][k] = bf16(fp32 fma(q[ids[t]][k], s, b))   for t < T, k < K
+ * with the single-rounding fp32 fma of w4a16_dequant and round-to-nearest-
+ * even to bf16.  Wq u32 [N][K/8], scales/biases bf16 [N][K/64] (the table:
+ * N rows of width K), ids int32 [T] and out bf16 [T][K] on the DEVICE (out
+ * 16-byte aligned).  An id outside 0..N-1 gives a zero row and raises
+ * W4A16_DEVICE_BAD_ID.  T in 0..65535; T == 0 is a successful no-op. */
+int w4a16_embed(const uint32_t* Wq, const w4a16_bf16* scales, const w4a16_bf16* biases, const int32_t* ids,
+                w4a16_bf16* out, int T, int N, int K, void* stream);
+
 /* Debug: q[N][K] (one byte per code) from Wq[N][K/8].  Bit-exact
  * ([W2D2 "Packed Storage Layout"]). */
 int w4a16_unpack(const uint32_t* Wq, uint8_t* q, int N, int K, void* stream);

@@ -154,6 +154,23 @@ class Oracle:
         _check(self.lib.oracle_dequant(_ptr(w_), _ptr(s), _ptr(b), N, K, _ptr(out)), "dequant")
         return out
 
+    def embed(self, Wq, scales, biases, ids, N: int, K: int) -> np.ndarray:
+        """bf16 bits [T][K] of the table rows ids ([W2D2] "Task 1: Implement
+        Quantized Linear and Embedding": row lookup, unpack, q * scale +
+        bias): the exact q*s + b of ``dequant``, rounded once to fp32 (what a
+        single-rounding fma gives) and then to bf16 with ``bf16_from_f32``.
+        An id outside 0..N-1 gives a row of zeros."""
+        ids = np.asarray(ids, dtype=np.int64).reshape(-1)
+        ok = (ids >= 0) & (ids < N)
+        rows = np.where(ok, ids, 0)
+        Wq = np.asarray(Wq).reshape(N, K // 8)
+        s = np.asarray(scales).reshape(N, K // GROUP)
+        b = np.asarray(biases).reshape(N, K // GROUP)
+        w = self.dequant(Wq[rows], s[rows], b[rows], len(ids), K)
+        out = self.bf16_from_f32(w.astype(np.float32)).reshape(len(ids), K)
+        out[~ok] = 0
+        return out
+
     def mm(self, x, Wq, scales, biases, M: int, N: int, K: int, cols=None, threads: int = 0):
         """(y, absdot), both fp64 [M][ncols]: y = x W^T on the sampled columns."""
         x_ = _c(x, np.uint16)
@@ -219,6 +236,10 @@ def unpack(Wq, N, K):
 
 def dequant(Wq, scales, biases, N, K):
     return default().dequant(Wq, scales, biases, N, K)
+
+
+def embed(Wq, scales, biases, ids, N, K):
+    return default().embed(Wq, scales, biases, ids, N, K)
 
 
 def mm(x, Wq, scales, biases, M, N, K, cols=None, threads: int = 0):

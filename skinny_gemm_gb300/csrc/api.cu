@@ -254,6 +254,22 @@ int w4a16_dequant(const uint32_t* Wq, const w4a16_bf16* scales, const w4a16_bf16
   return e == cudaSuccess ? W4A16_OK : cuda_fail(e, "w4a16_dequant launch");
 }
 
+int w4a16_embed(const uint32_t* Wq, const w4a16_bf16* scales, const w4a16_bf16* biases, const int32_t* ids,
+                w4a16_bf16* out, int T, int N, int K, void* stream) {
+  if (env().fault == kFaultValidate) return fail(W4A16_ERR_SHAPE, "injected validation fault (W4A16_FAULT)");
+  if (T < 0 || T > 65535) return fail(W4A16_ERR_SHAPE, "T = %d must be in 0..65535", T);
+  if (int rc = check_nk(N, K)) return rc;
+  if (T == 0) return W4A16_OK;
+  if (!Wq || !scales || !biases || !ids || !out) return fail(W4A16_ERR_NULL, "null tensor pointer");
+  if (misaligned(Wq, 4) || misaligned(scales, 2) || misaligned(biases, 2) || misaligned(ids, 4) || misaligned(out, 16))
+    return fail(W4A16_ERR_ALIGN, "Wq and ids 4-byte, scales/biases 2-byte and out 16-byte alignment required");
+  if (env().fault == kFaultLaunch) return fail(W4A16_ERR_CUDA, "injected launch fault (W4A16_FAULT)");
+  int* flags = nullptr;
+  if (int rc = flag_pointer(&flags)) return rc;
+  cudaError_t e = launch_embed(Wq, scales, biases, ids, out, T, N, K, flags, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? W4A16_OK : cuda_fail(e, "w4a16_embed launch");
+}
+
 int w4a16_mm_noalloc(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* scales, const w4a16_bf16* biases,
                      w4a16_bf16* y, int M, int N, int K, void* stream) {
   if (int rc = validate_mm(x, Wq, scales, biases, y, M, N, K)) return rc;

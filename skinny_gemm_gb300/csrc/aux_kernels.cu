@@ -12,6 +12,11 @@
 // ([W2D2 "Make Failures Small and Synchronous": compare an intermediate such
 // as a dequantized weight group).  dequant computes fp32 fma(q, s, b) with a
 // single rounding.
+//
+// embed: the quantized embedding row lookup of [W2D2] "Task 1: Implement
+// Quantized Linear and Embedding" (gather the selected packed rows, unpack,
+// q * scale + bias): the same single-rounding fp32 fma as dequant, then the
+// output's round-to-nearest-even to bf16.
 #include "common.cuh"
 #include "launch.h"
 
@@ -98,6 +103,32 @@ __global__ void dequant_kernel(const uint32_t* __restrict__ Wq, const uint16_t* 
   reinterpret_cast<float4*>(w)[2 * i + 1] = hi;
 }
 
+// One thread per packed word (eight codes) of token t's row; grid.y = token.
+// 16 bytes of bf16 out per thread.  An id outside 0..N-1 gives a zero row
+// and raises the device flag.
+__global__ void embed_kernel(const uint32_t* __restrict__ Wq, const uint16_t* __restrict__ S,
+                             const uint16_t* __restrict__ B, const int32_t* __restrict__ ids, uint16_t* __restrict__ out,
+                             int N, int K, int* flags) {
+  const int t = blockIdx.y;
+  const int words = K / 8;
+  const int wi = blockIdx.x * blockDim.x + threadIdx.x;
+  if (wi >= words) return;
+  const int n = ids[t];
+  uint4 v = make_uint4(0, 0, 0, 0);
+  if (n < 0 || n >= N) {
+    if (wi == 0) atomicOr(flags, W4A16_DEVICE_BAD_ID);
+  } else {
+    const int64_t gi = (int64_t)n * (K / kGroup) + (8 * wi) / kGroup;
+    const float s = bf16_bits_to_f32(S[gi]), b = bf16_bits_to_f32(B[gi]);
+    const uint32_t word = Wq[(int64_t)n * words + wi];
+    uint32_t h[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) h[i] = f32_to_bf16_bits(__fmaf_rn((float)((word >> (4 * i)) & 0xFu), s, b));
+    v = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+  }
+  reinterpret_cast<uint4*>(out + (int64_t)t * K)[wi] = v;
+}
+
 }  // namespace
 
 void plan_vanilla(int N, int K, w4a16_plan* p) {
@@ -129,6 +160,14 @@ cudaError_t launch_unpack(const uint32_t* Wq, uint8_t* q, int N, int K, cudaStre
   const int threads = 256;
   const int64_t blocks = (nwords + threads - 1) / threads;
   unpack_kernel<<<(unsigned)blocks, threads, 0, s>>>(Wq, q, nwords);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_embed(const uint32_t* Wq, const uint16_t* S, const uint16_t* B, const int32_t* ids,
+                         uint16_t* out, int T, int N, int K, int* flags, cudaStream_t s) {
+  const int threads = 128;
+  const dim3 grid((unsigned)((K / 8 + threads - 1) / threads), (unsigned)T);
+  embed_kernel<<<grid, threads, 0, s>>>(Wq, S, B, ids, out, N, K, flags);
   return cudaGetLastError();
 }
 

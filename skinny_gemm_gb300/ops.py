@@ -24,8 +24,8 @@ KERNELS = {"auto": 0, "simt": 1, "tc": 2, "vanilla": 3, "tc_stream": 4, "tc_tile
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 DEVICE_BAD_ID = 1
 
-EXPORTS = ("w4a16_mm", "w4a16_mm_kernel", "w4a16_mm_group", "w4a16_mm_argmax", "w4a16_mm_id", "w4a16_mm_id_kernel",
-           "w4a16_unpack", "w4a16_dequant", "w4a16_get_plan", "w4a16_device_status", "w4a16_last_error",
+EXPORTS = ("w4a16_mm", "w4a16_mm_kernel", "w4a16_mm_group", "w4a16_mm_argmax", "w4a16_embed", "w4a16_mm_id",
+           "w4a16_mm_id_kernel", "w4a16_unpack", "w4a16_dequant", "w4a16_get_plan", "w4a16_device_status", "w4a16_last_error",
            "w4a16_debug_reload_env", "w4a16_version")
 MAX_GROUP = 8
 
@@ -80,14 +80,16 @@ def lib() -> ctypes.CDLL:
             L.w4a16_mm_noalloc.argtypes = [P, P, P, P, P, i, i, i, P]
             L.w4a16_mm_group.argtypes = [ctypes.POINTER(Item), i, i, i, P]
             L.w4a16_mm_argmax.argtypes = [P, P, P, P, P, P, i, i, i, P]
+            L.w4a16_embed.argtypes = [P, P, P, P, P, i, i, i, P]
             L.w4a16_mm_id.argtypes = [P, P, P, P, P, P, i, i, i, i, P]
             L.w4a16_mm_id_kernel.argtypes = [P, P, P, P, P, P, i, i, i, i, i, P]
             L.w4a16_unpack.argtypes = [P, P, i, i, P]
             L.w4a16_dequant.argtypes = [P, P, P, P, i, i, P]
             L.w4a16_get_plan.argtypes = [i, i, i, ctypes.POINTER(Plan)]
             L.w4a16_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
-            for f in ("w4a16_mm", "w4a16_mm_kernel", "w4a16_mm_noalloc", "w4a16_mm_group", "w4a16_mm_argmax", "w4a16_mm_id",
-                      "w4a16_mm_id_kernel", "w4a16_unpack", "w4a16_dequant", "w4a16_get_plan", "w4a16_device_status"):
+            for f in ("w4a16_mm", "w4a16_mm_kernel", "w4a16_mm_noalloc", "w4a16_mm_group", "w4a16_mm_argmax",
+                      "w4a16_embed", "w4a16_mm_id", "w4a16_mm_id_kernel", "w4a16_unpack", "w4a16_dequant",
+                      "w4a16_get_plan", "w4a16_device_status"):
                 getattr(L, f).restype = ctypes.c_int
             L.w4a16_last_error.restype = ctypes.c_char_p
             L.w4a16_version.restype = ctypes.c_char_p
@@ -226,6 +228,24 @@ def mm_argmax(x: torch.Tensor, w: W4Matrix, idx: torch.Tensor | None = None, val
                                vp, M, w.N, w.K, _stream_ptr(stream))
     _raise(rc)
     return idx, (val if val is not False else None)
+
+
+def embed(ids: torch.Tensor, w: W4Matrix, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Rows ids of the packed table w (N rows of width K), dequantized to bf16
+    [..., K] through ``w4a16_embed``; ids int32 on the device."""
+    if w.E != 1:
+        raise ValueError("embed takes a single table")
+    _dev_tensor(ids, torch.int32, "ids")
+    T = ids.numel()
+    if out is None:
+        out = torch.empty(*ids.shape, w.K, dtype=torch.bfloat16, device=ids.device)
+    _dev_tensor(out, torch.bfloat16, "out")
+    if out.numel() != T * w.K:
+        raise ValueError("out has the wrong number of elements")
+    rc = lib().w4a16_embed(w.Wq.data_ptr(), w.scales.data_ptr(), w.biases.data_ptr(), ids.data_ptr(), out.data_ptr(),
+                           T, w.N, w.K, _stream_ptr(stream))
+    _raise(rc)
+    return out
 
 
 def mm_group(xs, ws, outs=None, stream=None) -> list:

@@ -398,7 +398,28 @@ def pin_mm_id(o):
             assert np.array_equal(ym[0], y[t])
 
 
+def pin_embed(o):
+    """Embedding rows: zero codes give bf16(b) and all-15 codes bf16(15 s + b),
+    both exactly representable, so element for element the stored bias (resp.
+    the exact value); each output row is its id's row; a bad id gives zeros."""
+    rng = _rng(27)
+    N, K = 5, 256
+    S = random_bf16(rng, (N, K // G), -0.02, 0.02)
+    B = random_bf16(rng, (N, K // G))
+    ids = np.array([4, 0, 7, 2, 2, -3], dtype=np.int32)
+    e0 = o.embed(np.zeros((N, K // 8), dtype=np.uint32), S, B, ids, N, K)
+    e15 = o.embed(np.full((N, K // 8), 0xFFFFFFFF, dtype=np.uint32), S, B, ids, N, K)
+    for t, n in enumerate(ids):
+        if 0 <= n < N:
+            assert np.array_equal(e0[t], np.repeat(B[n], G)), f"zero codes, token {t}"
+            want = 15.0 * torch_bf16_to_f64(S[n]) + torch_bf16_to_f64(B[n])
+            got = torch_bf16_to_f64(e15[t].reshape(K // G, G))
+            assert np.all(np.abs(got - want[:, None]) <= np.abs(want[:, None]) * 2.0 ** -8), f"all-15 codes, token {t}"
+        else:
+            assert np.all(e0[t] == 0) and np.all(e15[t] == 0), "out-of-range id must give a zero row"
+
+
 PINS = [pin_packing_golden, pin_unpack_exhaustive, pin_dequant_endpoints, pin_dequant_random,
         pin_ulp, pin_bf16_special, pin_mm_zero_codes, pin_mm_all15, pin_mm_identity, pin_mm_ramp,
         pin_mm_sampled_columns, pin_mm_id, pin_mm_bruteforce, pin_bf16_decode_all,
-        pin_bf16_from_f64_exact, pin_bf16_from_f32_sweep]
+        pin_bf16_from_f64_exact, pin_bf16_from_f32_sweep, pin_embed]

@@ -117,6 +117,17 @@ def test_mm_argmax_errors(L):
     assert f(P, P, P, P, P, P, 1, 64, 448, None) == ops.ERR_KERNEL   # tensor-core family only
 
 
+def test_embed_errors(L):
+    f = L.w4a16_embed
+    assert f(P, P, P, P, P, 0, 64, 64, None) == ops.OK                 # T == 0: no-op
+    assert f(P, P, P, P, P, -1, 64, 64, None) == ops.ERR_SHAPE
+    assert f(P, P, P, P, P, 65536, 64, 64, None) == ops.ERR_SHAPE
+    assert f(P, P, P, P, P, 2, 64, 96, None) == ops.ERR_SHAPE           # K % 64
+    assert f(P, P, P, None, P, 2, 64, 64, None) == ops.ERR_NULL         # ids
+    assert f(P, P, P, P, P + 8, 2, 64, 64, None) == ops.ERR_ALIGN       # out 16-byte
+    assert f(P, P, P, P + 2, P, 2, 64, 64, None) == ops.ERR_ALIGN       # ids 4-byte
+
+
 def test_debug_entry_point_errors(L):
     assert L.w4a16_unpack(P, P, 4, 12, None) == ops.ERR_SHAPE
     assert L.w4a16_unpack(None, P, 4, 64, None) == ops.ERR_NULL
