@@ -83,8 +83,12 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_unpack.restype = i32
     lib.oracle_dequant.argtypes = [P, P, P, i64, i64, P]
     lib.oracle_dequant.restype = i32
+    lib.oracle_dequant_g.argtypes = [P, P, P, i64, i64, i64, P]
+    lib.oracle_dequant_g.restype = i32
     lib.oracle_mm.argtypes = [P, P, P, P, i64, i64, i64, P, i64, P, P, i32]
     lib.oracle_mm.restype = i32
+    lib.oracle_mm_g.argtypes = [P, P, P, P, i64, i64, i64, i64, P, i64, P, P, i32]
+    lib.oracle_mm_g.restype = i32
     lib.oracle_mm_id.argtypes = [P, P, P, P, P, i64, i64, i64, i64, P, i64, P, P, i32]
     lib.oracle_mm_id.restype = i32
     return lib
@@ -146,12 +150,16 @@ class Oracle:
         _check(self.lib.oracle_unpack(_ptr(w), N, K, _ptr(q)), "unpack")
         return q
 
-    def dequant(self, Wq, scales, biases, N: int, K: int) -> np.ndarray:
-        """Weights w[N][K] = q*s + b in fp64."""
+    def dequant(self, Wq, scales, biases, N: int, K: int, group: int = GROUP) -> np.ndarray:
+        """Weights w[N][K] = q*s + b in fp64 (scale and bias per `group` codes)."""
         w_ = _c(Wq, np.uint32)
         s, b = _c(scales, np.uint16), _c(biases, np.uint16)
         out = np.empty((N, K), dtype=np.float64)
-        _check(self.lib.oracle_dequant(_ptr(w_), _ptr(s), _ptr(b), N, K, _ptr(out)), "dequant")
+        if group == GROUP:
+            rc = self.lib.oracle_dequant(_ptr(w_), _ptr(s), _ptr(b), N, K, _ptr(out))
+        else:
+            rc = self.lib.oracle_dequant_g(_ptr(w_), _ptr(s), _ptr(b), N, K, group, _ptr(out))
+        _check(rc, "dequant")
         return out
 
     def embed(self, Wq, scales, biases, ids, N: int, K: int) -> np.ndarray:
@@ -171,8 +179,9 @@ class Oracle:
         out[~ok] = 0
         return out
 
-    def mm(self, x, Wq, scales, biases, M: int, N: int, K: int, cols=None, threads: int = 0):
-        """(y, absdot), both fp64 [M][ncols]: y = x W^T on the sampled columns."""
+    def mm(self, x, Wq, scales, biases, M: int, N: int, K: int, cols=None, threads: int = 0, group: int = GROUP):
+        """(y, absdot), both fp64 [M][ncols]: y = x W^T on the sampled columns
+        (scale and bias per `group` codes: 64, or the book's 128)."""
         x_ = _c(x, np.uint16)
         w_ = _c(Wq, np.uint32)
         s, b = _c(scales, np.uint16), _c(biases, np.uint16)
@@ -180,8 +189,13 @@ class Oracle:
         nc = N if c is None else c.size
         y = np.empty((M, nc), dtype=np.float64)
         ad = np.empty((M, nc), dtype=np.float64)
-        _check(self.lib.oracle_mm(_ptr(x_), _ptr(w_), _ptr(s), _ptr(b), M, N, K, _ptr(c), nc, _ptr(y), _ptr(ad),
-                                  threads), "mm")
+        if group == GROUP:
+            rc = self.lib.oracle_mm(_ptr(x_), _ptr(w_), _ptr(s), _ptr(b), M, N, K, _ptr(c), nc, _ptr(y), _ptr(ad),
+                                    threads)
+        else:
+            rc = self.lib.oracle_mm_g(_ptr(x_), _ptr(w_), _ptr(s), _ptr(b), M, N, K, group, _ptr(c), nc, _ptr(y),
+                                      _ptr(ad), threads)
+        _check(rc, "mm")
         return y, ad
 
     def mm_id(self, x, Wq, scales, biases, ids, T: int, N: int, K: int, E: int, cols=None, threads: int = 0):
@@ -234,16 +248,16 @@ def unpack(Wq, N, K):
     return default().unpack(Wq, N, K)
 
 
-def dequant(Wq, scales, biases, N, K):
-    return default().dequant(Wq, scales, biases, N, K)
+def dequant(Wq, scales, biases, N, K, group: int = GROUP):
+    return default().dequant(Wq, scales, biases, N, K, group)
 
 
 def embed(Wq, scales, biases, ids, N, K):
     return default().embed(Wq, scales, biases, ids, N, K)
 
 
-def mm(x, Wq, scales, biases, M, N, K, cols=None, threads: int = 0):
-    return default().mm(x, Wq, scales, biases, M, N, K, cols, threads)
+def mm(x, Wq, scales, biases, M, N, K, cols=None, threads: int = 0, group: int = GROUP):
+    return default().mm(x, Wq, scales, biases, M, N, K, cols, threads, group)
 
 
 def mm_id(x, Wq, scales, biases, ids, T, N, K, E, cols=None, threads: int = 0):

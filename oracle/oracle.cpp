@@ -16,7 +16,10 @@
  *                                                   equation w^ = q s + b]
  *   y[m,n] = sum_k x[m,k] * w[n,k]                [W2D2 "Mathematical Formulation",
  *                                                   C[i,k] = sum_j A[i,j] B[k,j]]
- * with G = 64 [G4MK "Usage": the dequant path assumes group size 64].  The
+ * with G = 64 [G4MK "Usage": the dequant path assumes group size 64], or
+ * G = 128 through the _g entry points [W2D2 "Packed Storage Layout": the
+ * book's group size; its "Reconstruct a Stored Group" is the same equation
+ * with 128 codes per scale and bias].  The
  * loops follow [W2D2 "Computation Flow"]: for every output, walk groups g,
  * packs p inside the group and the eight nibbles of each pack, reconstruct
  * the weight and add a*w to one accumulator.  The pages accumulate in float;
@@ -105,11 +108,11 @@ inline int code_at(const uint32_t* Wq, int64_t K, int64_t n, int64_t k) {
   return (int)((word >> (4 * (k % 8))) & 0xFu);
 }
 
-// One output element, in the page's loop order.
+// One output element, in the page's loop order, groups of G codes.
 void dot_one(const uint16_t* xrow, const uint32_t* Wq, const uint16_t* S, const uint16_t* B,
-             int64_t K, int64_t n, double* y, double* absdot) {
-  const int64_t groups = K / kGroup;
-  const int64_t words_per_group = kGroup / 8;
+             int64_t K, int64_t n, int64_t G, double* y, double* absdot) {
+  const int64_t groups = K / G;
+  const int64_t words_per_group = G / 8;
   double sum = 0.0, abs_sum = 0.0;
   for (int64_t g = 0; g < groups; ++g) {
     const double scale = bf16_decode(S[n * groups + g]);
@@ -119,7 +122,7 @@ void dot_one(const uint16_t* xrow, const uint32_t* Wq, const uint16_t* S, const 
       for (int bit_offset = 0; bit_offset < 32; bit_offset += 4) {
         const int q = (int)((packed >> bit_offset) & 0xFu);
         const double w = (double)q * scale + bias;
-        const double a = bf16_decode(xrow[g * kGroup + p * 8 + bit_offset / 4]);
+        const double a = bf16_decode(xrow[g * G + p * 8 + bit_offset / 4]);
         sum += a * w;
         abs_sum += std::fabs(a * w);
       }
@@ -145,7 +148,8 @@ void parallel_over(int64_t n, int threads, F fn) {
   for (auto& th : pool) th.join();
 }
 
-bool shape_ok(int64_t K) { return K > 0 && K % kGroup == 0; }
+bool group_ok(int64_t G) { return G == 64 || G == 128; }
+bool shape_ok(int64_t K, int64_t G = kGroup) { return group_ok(G) && K > 0 && K % G == 0; }
 
 }  // namespace
 
@@ -199,35 +203,47 @@ int oracle_unpack(const uint32_t* Wq, int64_t N, int64_t K, uint8_t* q) {
   return 0;
 }
 
-// w[n][k] = q*s + b in fp64 for the whole matrix.
-int oracle_dequant(const uint32_t* Wq, const uint16_t* S, const uint16_t* B, int64_t N, int64_t K,
-                   double* w) {
+// w[n][k] = q*s + b in fp64 for the whole matrix, groups of G codes.
+int oracle_dequant_g(const uint32_t* Wq, const uint16_t* S, const uint16_t* B, int64_t N, int64_t K, int64_t G,
+                     double* w) {
   if (!Wq || !S || !B || !w) return -1;
-  if (N < 0 || !shape_ok(K)) return -2;
-  const int64_t groups = K / kGroup;
+  if (N < 0 || !shape_ok(K, G)) return -2;
+  const int64_t groups = K / G;
   for (int64_t n = 0; n < N; ++n)
     for (int64_t k = 0; k < K; ++k)
-      w[n * K + k] = (double)code_at(Wq, K, n, k) * bf16_decode(S[n * groups + k / kGroup]) +
-                     bf16_decode(B[n * groups + k / kGroup]);
+      w[n * K + k] = (double)code_at(Wq, K, n, k) * bf16_decode(S[n * groups + k / G]) +
+                     bf16_decode(B[n * groups + k / G]);
   return 0;
 }
 
+int oracle_dequant(const uint32_t* Wq, const uint16_t* S, const uint16_t* B, int64_t N, int64_t K,
+                   double* w) {
+  return oracle_dequant_g(Wq, S, B, N, K, kGroup, w);
+}
+
 // y[m][j] = sum_k x[m,k] w[cols[j], k] for j < ncols (all n when cols is NULL,
-// then ncols must equal N).  absdot (optional) gets sum_k |x w|.
-int oracle_mm(const uint16_t* x, const uint32_t* Wq, const uint16_t* S, const uint16_t* B, int64_t M,
-              int64_t N, int64_t K, const int64_t* cols, int64_t ncols, double* y, double* absdot,
-              int threads) {
+// then ncols must equal N), groups of G codes.  absdot (optional) gets
+// sum_k |x w|.
+int oracle_mm_g(const uint16_t* x, const uint32_t* Wq, const uint16_t* S, const uint16_t* B, int64_t M,
+                int64_t N, int64_t K, int64_t G, const int64_t* cols, int64_t ncols, double* y, double* absdot,
+                int threads) {
   if (!x || !Wq || !S || !B || !y) return -1;
-  if (M < 0 || N < 0 || ncols < 0 || !shape_ok(K)) return -2;
+  if (M < 0 || N < 0 || ncols < 0 || !shape_ok(K, G)) return -2;
   if (!cols && ncols != N) return -2;
   for (int64_t j = 0; cols && j < ncols; ++j)
     if (cols[j] < 0 || cols[j] >= N) return -2;
   parallel_over(ncols, threads, [&](int64_t j) {
     const int64_t n = cols ? cols[j] : j;
     for (int64_t m = 0; m < M; ++m)
-      dot_one(x + m * K, Wq, S, B, K, n, &y[m * ncols + j], absdot ? &absdot[m * ncols + j] : nullptr);
+      dot_one(x + m * K, Wq, S, B, K, n, G, &y[m * ncols + j], absdot ? &absdot[m * ncols + j] : nullptr);
   });
   return 0;
+}
+
+int oracle_mm(const uint16_t* x, const uint32_t* Wq, const uint16_t* S, const uint16_t* B, int64_t M,
+              int64_t N, int64_t K, const int64_t* cols, int64_t ncols, double* y, double* absdot,
+              int threads) {
+  return oracle_mm_g(x, Wq, S, B, M, N, K, kGroup, cols, ncols, y, absdot, threads);
 }
 
 // Routed experts: Wq[E][N][K/8], S/B[E][N][K/64], ids[T]; y[t][j] for the
@@ -250,7 +266,7 @@ int oracle_mm_id(const uint16_t* x, const uint32_t* Wq, const uint16_t* S, const
         if (absdot) absdot[t * ncols + j] = 0.0;
         continue;
       }
-      dot_one(x + t * K, Wq + e * words, S + e * params, B + e * params, K, n, &y[t * ncols + j],
+      dot_one(x + t * K, Wq + e * words, S + e * params, B + e * params, K, n, kGroup, &y[t * ncols + j],
               absdot ? &absdot[t * ncols + j] : nullptr);
     }
   });

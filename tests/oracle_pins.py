@@ -419,7 +419,28 @@ def pin_embed(o):
             assert np.all(e0[t] == 0) and np.all(e15[t] == 0), "out-of-range id must give a zero row"
 
 
+def pin_group128(o):
+    """Group size 128: equal, bit for bit, to group size 64 with every scale and
+    bias repeated over the two 64-halves of its group (the same weights, the
+    same loop order); zero codes give the closed form sum_g b_g sum_{k in g} x_k;
+    dequant's bias follows the 128-group."""
+    rng = _rng(28)
+    M, N, K = 2, 5, 512
+    x = random_bf16(rng, (M, K))
+    W = rng.integers(0, 2**32, size=(N, K // 8), dtype=np.uint64).astype(np.uint32)
+    S = random_bf16(rng, (N, K // 128), -0.02, 0.02)
+    B = random_bf16(rng, (N, K // 128))
+    y128, ad128 = o.mm(x, W, S, B, M, N, K, group=128)
+    y64, ad64 = o.mm(x, W, np.repeat(S, 2, axis=1), np.repeat(B, 2, axis=1), M, N, K)
+    assert np.array_equal(y128, y64) and np.array_equal(ad128, ad64), "group 128 != repeated group 64"
+    y0, ad0 = o.mm(x, np.zeros_like(W), S, B, M, N, K, group=128)
+    xs = torch_bf16_to_f64(x).reshape(M, K // 128, 128).sum(axis=2)
+    _check_close(y0, xs @ torch_bf16_to_f64(B).T, ad0, what="group 128, zero codes")
+    w0 = o.dequant(np.zeros_like(W), S, B, N, K, group=128)
+    assert np.array_equal(w0, np.repeat(torch_bf16_to_f64(B), 128, axis=1)), "group 128 dequant bias"
+
+
 PINS = [pin_packing_golden, pin_unpack_exhaustive, pin_dequant_endpoints, pin_dequant_random,
         pin_ulp, pin_bf16_special, pin_mm_zero_codes, pin_mm_all15, pin_mm_identity, pin_mm_ramp,
         pin_mm_sampled_columns, pin_mm_id, pin_mm_bruteforce, pin_bf16_decode_all,
-        pin_bf16_from_f64_exact, pin_bf16_from_f32_sweep, pin_embed]
+        pin_bf16_from_f64_exact, pin_bf16_from_f32_sweep, pin_embed, pin_group128]

@@ -22,14 +22,16 @@ MUTANTS = {
                                   "return (int)((word >> (28 - 4 * (k % 8))) & 0xFu);"),
     "wrong_scale_group": ("const double scale = bf16_decode(S[n * groups + g]);",
                           "const double scale = bf16_decode(S[n * groups + (g + 1) % groups]);"),
-    "activation_group_offset_dropped": ("xrow[g * kGroup + p * 8 + bit_offset / 4]", "xrow[p * 8 + bit_offset / 4]"),
+    "activation_group_offset_dropped": ("xrow[g * G + p * 8 + bit_offset / 4]", "xrow[p * 8 + bit_offset / 4]"),
     "rows_swapped": ("dot_one(x + m * K, Wq,", "dot_one(x + (M - 1 - m) * K, Wq,"),
     "absdot_signed": ("abs_sum += std::fabs(a * w);", "abs_sum += a * w;"),
     "ties_away_from_zero": ("else r = (std::fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;", "else r = fl + 1.0;"),
     "truncation": ("if (diff > 0.5) r = fl + 1.0;", "if (diff > 2.0) r = fl + 1.0;"),
     "decode_exponent_bias": ("efield - 127 - 7", "efield - 127 - 6"),
     "wrong_expert": ("dot_one(x + t * K, Wq + e * words", "dot_one(x + t * K, Wq + (E - 1 - e) * words"),
-    "dequant_scale_group": ("bf16_decode(S[n * groups + k / kGroup]) +", "bf16_decode(S[n * groups]) +"),
+    "dequant_scale_group": ("bf16_decode(S[n * groups + k / G]) +", "bf16_decode(S[n * groups]) +"),
+    "group_size_fixed_at_64": ("const int64_t words_per_group = G / 8;", "const int64_t words_per_group = 8;"),
+    "dequant_bias_group_halved": ("bf16_decode(B[n * groups + k / G]);", "bf16_decode(B[n * groups + k / G / 2]);"),
 }
 
 
