@@ -210,6 +210,17 @@ int w4a16_mm_id_kernel(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16
                        const w4a16_bf16* biases, const int32_t* ids, w4a16_bf16* y,
                        int T, int N, int K, int E, int kernel, void* stream);
 
+/* Tables quantized with a larger group (the tiny-llm book quantizes with 128
+ * codes per scale and bias, [W2D2] "Packed Storage Layout"): dst[n][j] =
+ * src[n][j / (group / 64)], the scales (or biases) of every group repeated
+ * over its 64-code parts, bf16 [N][K/group] -> bf16 [N][K/64] on the device.
+ * With the expanded scales and biases the group-64 entry points compute
+ * q * s + b with each weight's own s and b, i.e. the larger-group matmul
+ * (the parameters then cost 4/64 instead of 4/group bytes per weight).
+ * group: a multiple of 64 that divides K, at most 4096.  Call it once when
+ * the weights are loaded. */
+int w4a16_expand_groups(const w4a16_bf16* src, w4a16_bf16* dst, int N, int K, int group, void* stream);
+
 /* Quantized embedding rows (the row lookup of [W2D2] "Task 1: Implement
  * Quantized Linear and Embedding": gather the selected packed rows, unpack,
  * q * scale + bias; the table stays packed):

@@ -254,6 +254,16 @@ int w4a16_dequant(const uint32_t* Wq, const w4a16_bf16* scales, const w4a16_bf16
   return e == cudaSuccess ? W4A16_OK : cuda_fail(e, "w4a16_dequant launch");
 }
 
+int w4a16_expand_groups(const w4a16_bf16* src, w4a16_bf16* dst, int N, int K, int group, void* stream) {
+  if (int rc = check_nk(N, K)) return rc;
+  if (group < kGroup || group % kGroup || group > 4096 || K % group)
+    return fail(W4A16_ERR_SHAPE, "group = %d must be a multiple of 64 that divides K = %d", group, K);
+  if (!src || !dst) return fail(W4A16_ERR_NULL, "null tensor pointer");
+  if (misaligned(src, 2) || misaligned(dst, 2)) return fail(W4A16_ERR_ALIGN, "src and dst must be 2-byte aligned");
+  cudaError_t e = launch_expand_groups(src, dst, N, K, group, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? W4A16_OK : cuda_fail(e, "w4a16_expand_groups launch");
+}
+
 int w4a16_embed(const uint32_t* Wq, const w4a16_bf16* scales, const w4a16_bf16* biases, const int32_t* ids,
                 w4a16_bf16* out, int T, int N, int K, void* stream) {
   if (env().fault == kFaultValidate) return fail(W4A16_ERR_SHAPE, "injected validation fault (W4A16_FAULT)");

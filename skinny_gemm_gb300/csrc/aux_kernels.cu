@@ -17,6 +17,10 @@
 // Quantized Linear and Embedding" (gather the selected packed rows, unpack,
 // q * scale + bias): the same single-rounding fp32 fma as dequant, then the
 // output's round-to-nearest-even to bf16.
+//
+// expand_groups: scales or biases of a table quantized with a larger group
+// (the book's 128 codes per scale and bias) repeated over its 64-code halves,
+// so that the group-64 kernels compute q * s + b with the same s and b.
 #include "common.cuh"
 #include "launch.h"
 
@@ -129,6 +133,12 @@ __global__ void embed_kernel(const uint32_t* __restrict__ Wq, const uint16_t* __
   reinterpret_cast<uint4*>(out + (int64_t)t * K)[wi] = v;
 }
 
+__global__ void expand_groups_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst, int64_t n64,
+                                     int rep) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n64) dst[i] = src[i / rep];
+}
+
 }  // namespace
 
 void plan_vanilla(int N, int K, w4a16_plan* p) {
@@ -168,6 +178,14 @@ cudaError_t launch_embed(const uint32_t* Wq, const uint16_t* S, const uint16_t* 
   const int threads = 128;
   const dim3 grid((unsigned)((K / 8 + threads - 1) / threads), (unsigned)T);
   embed_kernel<<<grid, threads, 0, s>>>(Wq, S, B, ids, out, N, K, flags);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_expand_groups(const uint16_t* src, uint16_t* dst, int N, int K, int group, cudaStream_t s) {
+  const int64_t n64 = (int64_t)N * (K / kGroup);
+  const int threads = 256;
+  const int64_t blocks = (n64 + threads - 1) / threads;
+  expand_groups_kernel<<<(unsigned)blocks, threads, 0, s>>>(src, dst, n64, group / kGroup);
   return cudaGetLastError();
 }
 

@@ -69,6 +69,7 @@ cudaError_t launch_vanilla_id(const LaunchArgs& a, const w4a16_plan& p);
 cudaError_t launch_unpack(const uint32_t* Wq, uint8_t* q, int N, int K, cudaStream_t s);
 cudaError_t launch_dequant(const uint32_t* Wq, const uint16_t* S, const uint16_t* B, float* w, int N, int K,
                            cudaStream_t s);
+cudaError_t launch_expand_groups(const uint16_t* src, uint16_t* dst, int N, int K, int group, cudaStream_t s);
 cudaError_t launch_embed(const uint32_t* Wq, const uint16_t* S, const uint16_t* B, const int32_t* ids,
                          uint16_t* out, int T, int N, int K, int* flags, cudaStream_t s);
 

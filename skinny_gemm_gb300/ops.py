@@ -24,8 +24,8 @@ KERNELS = {"auto": 0, "simt": 1, "tc": 2, "vanilla": 3, "tc_stream": 4, "tc_tile
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 DEVICE_BAD_ID = 1
 
-EXPORTS = ("w4a16_mm", "w4a16_mm_kernel", "w4a16_mm_group", "w4a16_mm_argmax", "w4a16_embed", "w4a16_mm_id",
-           "w4a16_mm_id_kernel", "w4a16_unpack", "w4a16_dequant", "w4a16_get_plan", "w4a16_device_status", "w4a16_last_error",
+EXPORTS = ("w4a16_mm", "w4a16_mm_kernel", "w4a16_mm_group", "w4a16_mm_argmax", "w4a16_embed", "w4a16_expand_groups",
+           "w4a16_mm_id", "w4a16_mm_id_kernel", "w4a16_unpack", "w4a16_dequant", "w4a16_get_plan", "w4a16_device_status", "w4a16_last_error",
            "w4a16_debug_reload_env", "w4a16_version")
 MAX_GROUP = 8
 
@@ -81,6 +81,7 @@ def lib() -> ctypes.CDLL:
             L.w4a16_mm_group.argtypes = [ctypes.POINTER(Item), i, i, i, P]
             L.w4a16_mm_argmax.argtypes = [P, P, P, P, P, P, i, i, i, P]
             L.w4a16_embed.argtypes = [P, P, P, P, P, i, i, i, P]
+            L.w4a16_expand_groups.argtypes = [P, P, i, i, i, P]
             L.w4a16_mm_id.argtypes = [P, P, P, P, P, P, i, i, i, i, P]
             L.w4a16_mm_id_kernel.argtypes = [P, P, P, P, P, P, i, i, i, i, i, P]
             L.w4a16_unpack.argtypes = [P, P, i, i, P]
@@ -88,7 +89,7 @@ def lib() -> ctypes.CDLL:
             L.w4a16_get_plan.argtypes = [i, i, i, ctypes.POINTER(Plan)]
             L.w4a16_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
             for f in ("w4a16_mm", "w4a16_mm_kernel", "w4a16_mm_noalloc", "w4a16_mm_group", "w4a16_mm_argmax",
-                      "w4a16_embed", "w4a16_mm_id", "w4a16_mm_id_kernel", "w4a16_unpack", "w4a16_dequant",
+                      "w4a16_embed", "w4a16_expand_groups", "w4a16_mm_id", "w4a16_mm_id_kernel", "w4a16_unpack", "w4a16_dequant",
                       "w4a16_get_plan", "w4a16_device_status"):
                 getattr(L, f).restype = ctypes.c_int
             L.w4a16_last_error.restype = ctypes.c_char_p
@@ -169,6 +170,23 @@ class W4Matrix:
         s = torch.from_numpy(host.scales.view("int16")).view(torch.bfloat16).to(device)
         b = torch.from_numpy(host.biases.view("int16")).view(torch.bfloat16).to(device)
         return cls(wq, s, b, host.N, host.K, host.E)
+
+    @classmethod
+    def from_group(cls, Wq: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor, N: int, K: int,
+                   group: int, stream=None) -> "W4Matrix":
+        """A table quantized with `group` codes per scale and bias (a multiple
+        of 64, e.g. the book's 128): scales/biases bf16 [N][K/group] expanded
+        once on the device through ``w4a16_expand_groups``."""
+        _dev_tensor(scales, torch.bfloat16, "scales")
+        _dev_tensor(biases, torch.bfloat16, "biases")
+        if scales.numel() != N * (K // group) or biases.numel() != N * (K // group):
+            raise ValueError(f"scales and biases must hold N * K / group = {N * (K // group)} values")
+        out = []
+        for t in (scales, biases):
+            d = torch.empty(N, K // GROUP, dtype=torch.bfloat16, device=t.device)
+            _raise(lib().w4a16_expand_groups(t.data_ptr(), d.data_ptr(), N, K, group, _stream_ptr(stream)))
+            out.append(d)
+        return cls(Wq, out[0], out[1], N, K)
 
     @property
     def nbytes(self) -> int:

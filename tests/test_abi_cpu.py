@@ -128,6 +128,15 @@ def test_embed_errors(L):
     assert f(P, P, P, P + 2, P, 2, 64, 64, None) == ops.ERR_ALIGN       # ids 4-byte
 
 
+def test_expand_groups_errors(L):
+    f = L.w4a16_expand_groups
+    assert f(P, P, 4, 256, 96, None) == ops.ERR_SHAPE     # not a multiple of 64
+    assert f(P, P, 4, 384, 256, None) == ops.ERR_SHAPE    # does not divide K
+    assert f(P, P, 4, 96, 128, None) == ops.ERR_SHAPE     # K % 64
+    assert f(None, P, 4, 256, 128, None) == ops.ERR_NULL
+    assert f(P + 1, P, 4, 256, 128, None) == ops.ERR_ALIGN
+
+
 def test_debug_entry_point_errors(L):
     assert L.w4a16_unpack(P, P, 4, 12, None) == ops.ERR_SHAPE
     assert L.w4a16_unpack(None, P, 4, 64, None) == ops.ERR_NULL

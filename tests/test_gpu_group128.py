@@ -1,0 +1,66 @@
+"""Tables quantized with 128 codes per scale and bias (the tiny-llm book's
+group size): parameters expanded once with w4a16_expand_groups, then the
+group-64 kernels, against the oracle's group-128 definition."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_cases import assert_parity, bf16_bits, sample_cols, to_dev_bf16
+from skinny_gemm_gb300 import ops, synth
+
+pytestmark = pytest.mark.gpu
+
+
+def g128_weights(seed, N, K):
+    """Seeded codes; one scale and bias per 128 codes (every other group-64
+    draw of the generator, the same distributions)."""
+    hw = synth.make_weights(seed, N, K)
+    s = np.ascontiguousarray(hw.scales[:, ::2])
+    b = np.ascontiguousarray(hw.biases[:, ::2])
+    dev = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()  # noqa: E731
+    wq = torch.from_numpy(hw.Wq.view(np.int32)).cuda()
+    return hw.Wq, s, b, ops.W4Matrix.from_group(wq, dev(s), dev(b), N, K, 128)
+
+
+def test_expand_is_a_repeat():
+    N, K = 300, 1280
+    s = synth.make_weights(1, N, K).scales[:, :K // 128].copy()
+    src = torch.from_numpy(s.view(np.int16)).view(torch.bfloat16).cuda()
+    dst = torch.empty(N, K // 64, dtype=torch.bfloat16, device="cuda")
+    assert ops.lib().w4a16_expand_groups(src.data_ptr(), dst.data_ptr(), N, K, 128, None) == ops.OK
+    torch.cuda.synchronize()
+    assert np.array_equal(bf16_bits(dst), np.repeat(s, 2, axis=1))
+    dst4 = torch.empty(N, K // 64, dtype=torch.bfloat16, device="cuda")
+    s4 = np.ascontiguousarray(s[:, :K // 256])
+    src4 = torch.from_numpy(s4.view(np.int16)).view(torch.bfloat16).cuda()
+    assert ops.lib().w4a16_expand_groups(src4.data_ptr(), dst4.data_ptr(), N, K, 256, None) == ops.OK
+    torch.cuda.synchronize()
+    assert np.array_equal(bf16_bits(dst4), np.repeat(s4, 4, axis=1))
+
+
+@pytest.mark.parametrize("N,K,M", [(70, 1024, 1), (10240, 2560, 1), (2560, 10240, 5), (500, 384, 3), (333, 2048, 11)])
+@pytest.mark.parametrize("kernel", [None, "tc_stream"])
+def test_group128_parity(N, K, M, kernel):
+    if kernel == "tc_stream" and K % 512:
+        pytest.skip("the tensor-core family needs K % 512 == 0")
+    Wq, s, b, w = g128_weights(N + K, N, K)
+    xb = synth.make_x(M + N, M, K)
+    y = ops.mm(to_dev_bf16(xb), w, kernel=kernel)
+    cols = sample_cols(N, 1024)
+    yr, ad = oracle.mm(xb, Wq, s, b, M, N, K, cols=cols, threads=oracle.host_threads(), group=128)
+    assert_parity(y[:, torch.from_numpy(cols).cuda()], yr, ad, f"group 128 {N}x{K} M={M}")
+
+
+def test_group128_lm_head_rows_invariant():
+    N, K = 262144, 2560
+    Wq, s, b, w = g128_weights(3, N, K)
+    xb = synth.make_x(9, 3, K)
+    x = to_dev_bf16(xb)
+    y3 = bf16_bits(ops.mm(x, w))
+    for m in range(3):
+        assert np.array_equal(bf16_bits(ops.mm(x[m:m + 1], w))[0], y3[m])
+    cols = sample_cols(N, 512)
+    yr, ad = oracle.mm(xb, Wq, s, b, 3, N, K, cols=cols, threads=oracle.host_threads(), group=128)
+    y = torch.from_numpy(y3.view(np.int16)).view(torch.bfloat16).cuda()
+    assert_parity(y[:, torch.from_numpy(cols).cuda()], yr, ad, "group 128 LM head")
