@@ -157,11 +157,17 @@ int run_mm(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* S, const w
   a.pdl = env().pdl;
   a.tc_path = plan.kernel == W4A16_KERNEL_TC_STREAM ? 1 : plan.kernel == W4A16_KERNEL_TC_TILE ? 2 : 0;
   if (int rc = flag_pointer(&a.flags)) return rc;
-  for (int row0 = 0; row0 < M; row0 += kMaxChunk) {
+  const bool tc = plan.kernel == W4A16_KERNEL_TC || plan.kernel == W4A16_KERNEL_TC_STREAM ||
+                  plan.kernel == W4A16_KERNEL_TC_TILE;
+  if (a.tc_path == 2 && !tc_tile_fits(N, K, M < kMaxChunk ? M : kMaxChunk))
+    return fail(W4A16_ERR_KERNEL, "the tile kernel cannot hold K = %d for %d rows in shared memory", K,
+                M < kMaxChunk ? M : kMaxChunk);
+  // The tensor-core family takes all M rows at once (the tile kernel streams
+  // them over resident weights, the persistent kernel launches per chunk);
+  // the CUDA-core and control kernels take chunks of at most eight rows.
+  for (int row0 = 0; row0 < M; row0 += tc ? M : kMaxChunk) {
     a.row0 = row0;
-    a.M = (M - row0 < kMaxChunk) ? M - row0 : kMaxChunk;
-    if (a.tc_path == 2 && !tc_tile_fits(N, K, a.M))
-      return fail(W4A16_ERR_KERNEL, "the tile kernel cannot hold K = %d for %d rows in shared memory", K, a.M);
+    a.M = tc ? M : (M - row0 < kMaxChunk) ? M - row0 : kMaxChunk;
     cudaError_t e = cudaSuccess;
     switch (plan.kernel) {
       case W4A16_KERNEL_SIMT: e = launch_simt(a, plan); break;
@@ -356,11 +362,8 @@ int w4a16_mm_group(const w4a16_mm_item* items, int count, int M, int K, void* st
   GroupItem g[W4A16_MAX_GROUP];
   for (int i = 0; i < count; ++i)
     g[i] = GroupItem{items[i].x, items[i].Wq, items[i].scales, items[i].biases, items[i].y, items[i].N};
-  for (int row0 = 0; row0 < M; row0 += kMaxChunk) {
-    const int mc = (M - row0 < kMaxChunk) ? M - row0 : kMaxChunk;
-    cudaError_t e = launch_tc_group(g, count, mc, row0, K, env().pdl, flags, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "w4a16_mm_group launch");
-  }
+  cudaError_t e = launch_tc_group(g, count, M, 0, K, env().pdl, flags, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "w4a16_mm_group launch");
   return W4A16_OK;
 }
 

@@ -21,7 +21,8 @@ struct LaunchArgs {
   const uint16_t* S;
   const uint16_t* B;
   uint16_t* y;
-  int M;          // rows in this chunk (1..8); unused for mm_id
+  int M;          // rows (1..8 for the CUDA-core and control kernels; any for the tensor-core
+                  // family, which takes them eight at a time); unused for mm_id
   int row0;       // first activation row of the chunk
   int N, K;
   const int32_t* ids;  // mm_id only
@@ -55,6 +56,7 @@ struct GroupItem {
   int N;
 };
 bool tc_group_supported(const int* N, int count, int K);
+// M rows in one launch, eight at a time over resident weights.
 cudaError_t launch_tc_group(const GroupItem* items, int count, int M, int row0, int K, int pdl, int* flags,
                             cudaStream_t stream);
 // Tensor-core w4a16_mm with its split-K scratch in a fixed device array (no allocation).

@@ -1174,7 +1174,7 @@ struct TileParams {
   int* flags;
   const int32_t* ids;  // routed mode: expert id per token
   int items;           // items in TileArgs
-  int K, M, row0;      // plain mode: rows row0 .. row0 + M of x (M <= xcap)
+  int K, M, row0;      // plain mode: rows row0 .. row0 + M of x, xcap at a time
   int T, E;            // routed mode: tokens, experts
   int nst, sl, ks;
   int kc;        // CTAs (one cluster) per 16-row tile
@@ -1212,7 +1212,9 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
-// Plain mode (w4a16_mm): blockIdx.x = tile * kc + rank; one chunk of M rows.
+// Plain mode (w4a16_mm): blockIdx.x = tile * kc + rank; the M rows go through
+// in chunks of xcap (at most eight) while the weights stay in shared memory,
+// so a launch reads them once for any M.
 // Routed mode (w4a16_mm_id): blockIdx.y = expert e.  After the wait for
 // earlier kernels every CTA collects, in token order, the tokens routed to e
 // (at most xcap at a time) and exits when there are none, so an untouched
@@ -1258,7 +1260,7 @@ __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Ti
   int* s_state = s_abort + 1;  // token scan: [0] position, [1] count
 
   for (int i = threadIdx.x; i < nloc; i += blockDim.x) mbar_init(bars0 + 8 * i, 1);
-  if (!ROUTED && threadIdx.x < p.M) s_tok[threadIdx.x] = p.row0 + threadIdx.x;
+  if (!ROUTED && threadIdx.x < min(p.M, xcap)) s_tok[threadIdx.x] = p.row0 + threadIdx.x;
   if (threadIdx.x == 0) {
     *s_abort = 0;
     s_state[0] = 0;
@@ -1272,14 +1274,14 @@ __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Ti
                      policy_evict_first(), policy_evict_last());
   };
   if (!ROUTED && lane == 0 && p.prefetch)
-    for (int i = warp; i < nloc; i += W) weights(i, p.M);
+    for (int i = warp; i < nloc; i += W) weights(i, min(p.M, xcap));
   pdl_wait();
   // Only now let the next kernel launch: its CTAs then fetch their weights
   // while this one computes, and at most one kernel waits ahead (CTAs
   // launched further ahead would only hold SM resources and slow this one).
   pdl_launch_dependents();
 
-  int mc = p.M;
+  int mc = min(p.M, xcap);  // rows of the current chunk
   if (ROUTED) {
     if (e == 0 && crank == 0) {
       // tokens whose expert id is out of range: zero rows, raise the flag
@@ -1375,9 +1377,15 @@ __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Ti
         }
       }
     }
-    if (!ROUTED) break;
-    __syncthreads();  // s_tok is read above and rewritten by the scan
-    mc = gather_tokens(p.ids, p.T, p.E, e, s_tok, s_state, p.xcap);
+    __syncthreads();  // s_tok is read above and rewritten below
+    if (ROUTED) {
+      mc = gather_tokens(p.ids, p.T, p.E, e, s_tok, s_state, p.xcap);
+    } else {  // the next xcap rows, while the weights stay resident
+      const int c0 = (int)(chunk + 1) * xcap;
+      mc = c0 < p.M ? min(xcap, p.M - c0) : 0;
+      if (threadIdx.x < mc) s_tok[threadIdx.x] = p.row0 + c0 + threadIdx.x;
+      __syncthreads();
+    }
     if (mc == 0) break;  // the same in every CTA of the cluster
     // the first CTA has summed this chunk and every warp is done with the x slots
     cta_sync();
@@ -2026,14 +2034,11 @@ cudaError_t launch_tc_impl(const LaunchArgs& a, int32_t* idx, uint16_t* val) {
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DeviceInfo& d = device_info(dev);
   if (a.tc_path != 1 && !idx) {
-    const TilePlan tp = tile_plan(s, a.N, a.M, a.tc_path == 2, d.sms);
+    // one launch for all M rows: eight at a time over the resident weights
+    const TilePlan tp = tile_plan(s, a.N, min(a.M, kMaxChunk), a.tc_path == 2, d.sms);
     if (tp.kc > 0) return launch_tile(a, s, tp, d, false);
     if (a.tc_path == 2) return cudaErrorInvalidConfiguration;
   }
-  const StreamWork w = stream_work(s, a.N, a.M);
-  Maps maps;
-  if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, a.N, a.K, w.rows)) return e;
-  if (!workspace_fits(s, w)) return cudaErrorInvalidValue;
   void* ws = nullptr;
   if (cudaError_t e = workspace(dev, a.stream, &ws)) return e;
   p.cnt = static_cast<int*>(ws);
@@ -2041,7 +2046,17 @@ cudaError_t launch_tc_impl(const LaunchArgs& a, int32_t* idx, uint16_t* val) {
   p.done = p.cnt + kWsSched + 1;
   p.best = reinterpret_cast<unsigned long long*>(p.cnt + kWsBest);
   p.part = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsCounterBytes);
-  return launch_stream(maps, p, w, d, a.stream, a.pdl);
+  // the persistent kernel: one launch per chunk of at most eight rows
+  for (int r0 = 0; r0 < a.M; r0 += kMaxChunk) {
+    p.row0 = a.row0 + r0;
+    p.M = min(kMaxChunk, a.M - r0);
+    const StreamWork w = stream_work(s, a.N, p.M);
+    Maps maps;
+    if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, a.N, a.K, w.rows)) return e;
+    if (!workspace_fits(s, w)) return cudaErrorInvalidValue;
+    if (cudaError_t e = launch_stream(maps, p, w, d, a.stream, a.pdl)) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_tc(const LaunchArgs& a, const w4a16_plan& plan) {
@@ -2150,7 +2165,7 @@ cudaError_t launch_tc_group(const GroupItem* items, int count, int M, int row0, 
   const Shape s = tc_shape(items[0].N, K);
   int Ntot = 0;
   for (int i = 0; i < count; ++i) Ntot += cdiv(items[i].N, 32) * 32;
-  const TilePlan tp = tile_plan(s, Ntot, M, false);  // the plan depends on N only through the CTA count
+  const TilePlan tp = tile_plan(s, Ntot, min(M, kMaxChunk), false);  // depends on N only through the CTA count
   if (tp.kc == 0) return cudaErrorInvalidConfiguration;
   const int rows = kTile16 * tp.R;
   TileArgs<kMaxGroup> ta;

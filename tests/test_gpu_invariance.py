@@ -113,3 +113,25 @@ def test_mm_id_rows_equal_mm_on_selected_expert():
         we = ops.W4Matrix(w.Wq[e].contiguous(), w.scales[e].contiguous(), w.biases[e].contiguous(), N, K)
         ref = bf16_bits(ops.mm(x[t:t + 1], we))
         assert np.array_equal(y[t], ref[0]), f"token {t} (expert {e})"
+
+
+@pytest.mark.parametrize("N,K", [(10240, 2560), (2560, 10240), (300, 1024)])
+def test_many_rows_one_launch(N, K):
+    """More than eight rows in one tile-kernel launch (the rows stream through
+    in chunks of eight over resident weights): every row bitwise equal to its
+    M = 1 call and within tolerance of the oracle; the persistent launch shape
+    (a launch per chunk) gives the same bits."""
+    hw_seed = 4
+    w = dev_weights(hw_seed, N, K)
+    M = 37
+    xb = synth.make_x(33, M, K)
+    x = to_dev_bf16(xb)
+    y = bf16_bits(ops.mm(x, w))
+    assert np.array_equal(y, bf16_bits(ops.mm(x, w, kernel="tc_stream")))
+    for m in (0, 7, 8, 9, 31, 32, 36):
+        assert np.array_equal(y[m], bf16_bits(ops.mm(x[m:m + 1], w))[0]), f"row {m}"
+    from gpu_cases import host_weights, oracle_mm, sample_cols
+    cols = sample_cols(N, 256)
+    yr, ad = oracle_mm(xb, host_weights(hw_seed, N, K), cols=cols)
+    yt = torch.from_numpy(y.view(np.int16)).view(torch.bfloat16).cuda()
+    assert_parity(yt[:, torch.from_numpy(cols).cuda()], yr, ad, f"{N}x{K} M={M}")
