@@ -1377,6 +1377,8 @@ __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Ti
         }
       }
     }
+    // the last chunk (uniform in the cluster); one-row launches have only one
+    if (!ROUTED && (!ALLCOLS || (int)(chunk + 1) * xcap >= p.M)) break;
     __syncthreads();  // s_tok is read above and rewritten below
     if (ROUTED) {
       mc = gather_tokens(p.ids, p.T, p.E, e, s_tok, s_state, p.xcap);
