@@ -1,4 +1,4 @@
-// tc.cu -- tensor-core W4A16 skinny GEMM for sm_103a (M = 1..8 per launch).
+// tc.cu -- tensor-core W4A16 skinny GEMM for sm_103a (activation rows eight at a time).
 //
 // Citations (page titles; sections in quotes):
 //   [W2D2] tiny-llm book, "Week 2 Day 2: Keep W4 Packed"
@@ -26,11 +26,13 @@
 //
 // Data path of one warp:
 //  * Packed codes stream HBM -> shared memory by TMA (cp.async.bulk.tensor,
-//    128-byte swizzle), 32 rows x 256 codes (4 KB) per stage, into a ring of
-//    `stages` slots, each guarded by an mbarrier.  The stage's activation
-//    chunk (M rows x 256 bf16) arrives by cp.async.bulk into padded rows of
-//    the same slot.  Lane 0 issues both; the ring runs ahead across work
-//    units, so DRAM latency is paid once per warp, not once per tile.
+//    128-byte swizzle), 32 rows x 512 codes (two 128-byte boxes, 8 KB) and
+//    the 8 groups' scales and biases per stage, into a ring of `stages`
+//    slots, each guarded by an mbarrier.  The stage's activation chunk (up
+//    to 8 rows x 512 bf16) arrives by cp.async.bulk into padded rows of the
+//    same slot, or the activation rows are staged once per CTA.  Lane 0
+//    issues the copies; the ring runs ahead across work units, so DRAM
+//    latency is paid once per warp, not once per tile.
 //  * ldmatrix.x4 hands every lane, for rows g and g+8 of a 16-row subtile,
 //    the packed words the m16n8k16 A fragment needs (bank-conflict free
 //    thanks to the swizzle).
@@ -41,14 +43,22 @@
 //    codes i and i+4 of a packed word); the activations are permuted the
 //    same way with PRMT, so each dot product is unchanged.
 //
-// w4a16_mm runs a persistent grid: work units (32 rows x one K-slice) are
-// dealt round-robin to warps, which gives every SM the same share of bytes
-// whatever N is.  With ksplit > 1 a unit writes its fp32 partial to a
-// workspace and bumps a per-tile counter; the warp that completes a tile
-// adds the partials in slice order (the result does not depend on which
-// warp arrives last) and resets the counter.  w4a16_mm_id runs one CTA per
-// (row tile, expert); its warps compute whole slices and add them in slice
-// order in shared memory.
+// Launch shapes (the arithmetic above in every one):
+//  * tc_tile_kernel -- shapes whose slices are single stages: a CTA (or a
+//    cluster of CTAs splitting K) holds a 16- or 32-row tile's weights in
+//    shared memory and adds the slice sums in slice order through
+//    distributed shared memory; activation rows stream through eight at a
+//    time.  Also w4a16_mm_group (several matrices in one grid) and, for
+//    more than 32 tokens, w4a16_mm_id (one CTA per row tile and expert).
+//  * tc_stream_kernel -- larger shapes: a persistent grid whose warps take
+//    work units (32 rows x one K-slice) from a counter; with ksplit > 1 a
+//    unit writes its fp32 partial to a workspace and bumps a per-tile
+//    counter, and the warp that completes a tile adds the partials in slice
+//    order (the result does not depend on which warp arrives last).  Its
+//    routed mode serves w4a16_mm_id up to 32 tokens (whole-K units of the
+//    chunks the ids select) and its argmax mode w4a16_mm_argmax.
+//  * tc_routed_kernel -- w4a16_mm_id with the persistent shape selected and
+//    more than 32 tokens: one CTA per (row tile, expert).
 //
 // No spin-wait is unbounded: an mbarrier wait that exceeds its iteration
 // limit raises W4A16_DEVICE_TIMEOUT and the warp stops computing.
