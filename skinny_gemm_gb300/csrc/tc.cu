@@ -509,9 +509,11 @@ __host__ __device__ inline int ring_bytes(int stages, int mcap) {
 // ---- persistent kernel (w4a16_mm) ------------------------------------------------------
 
 // Bytes after the barriers: token rows [8] and every warp's unit ring [8] (ints).
-// tokens [8] | dealt units [8 warps][8] | activation barrier | argmax mode:
-// best keys [8 warps][8 columns] and the CTA's [8] (u64)
-constexpr int kStreamMisc = 4 * (kMaxChunk + 8 * 8) + 32 + 8 * (8 * 8 + 8);
+// tokens [8] | dealt units [8 warps][8] | activation barrier
+constexpr int kStreamMisc = 4 * (kMaxChunk + 8 * 8) + 32;
+// argmax mode, after the pre-staged activations: best keys [8 warps][8
+// columns] and the CTA's [8] (u64)
+constexpr int kArgmaxSmem = 8 * (8 * 8 + 8);
 
 struct StreamParams {
   const uint16_t* x;
@@ -688,7 +690,8 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   if (!ROUTED && threadIdx.x < mc) s_tok[threadIdx.x] = p.row0 + threadIdx.x;
   const uint32_t xbar = smem_u32(s_tok + kMaxChunk + 8 * 8);  // the pre-staged activations' copy
   if (XSTAGED && threadIdx.x == 0) mbar_init(xbar, 1);
-  unsigned long long* s_best = reinterpret_cast<unsigned long long*>(s_tok + kMaxChunk + 8 * 8 + 8);  // [warp][8]
+  unsigned long long* s_best =  // [warp][8]; the offset is a multiple of 8
+      reinterpret_cast<unsigned long long*>(base + (xst - smem_u32(base)) + (XSTAGED ? xstage_bytes(mc, p.K) : 0));
   unsigned long long* s_cta_best = s_best + 8 * 8;
   if (ARGMAX && threadIdx.x < 8 * 8 + 8) s_best[threadIdx.x] = 0ull;
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -1643,9 +1646,9 @@ constexpr int stream_smem_target() {
 // Deepest ring (up to W4A16_TC_MAX_STAGES, at least 2 stages per warp) that
 // keeps a CTA's shared memory under the budget.
 template <int NSUB>
-int stream_stages(int mc) {
+int stream_stages(int mc, int extra = 0) {
   for (int s = W4A16_TC_MAX_STAGES; s > 2; --s)
-    if (stream_smem<NSUB>(s, mc) <= stream_smem_target<NSUB>()) return s;
+    if (stream_smem<NSUB>(s, mc) + extra <= stream_smem_target<NSUB>()) return s;
   return 2;
 }
 
@@ -1670,15 +1673,15 @@ cudaError_t allow_smem(Kern fn, DeviceInfo& d) {
 // + group sums over all of K); it pays off when every warp has several work
 // units to amortise it over.
 template <int NSUB>
-bool stage_activations(int M, int K, int units, int sms) {
+bool stage_activations(int M, int K, int units, int sms, int extra = 0) {
   return units >= 2 * Geo<NSUB>::kWarps * stream_ctas_per_sm<NSUB>() * sms &&
-         stream_smem<NSUB>(2, 0) + xstage_bytes(M, K) <= stream_budget<NSUB>();
+         stream_smem<NSUB>(2, 0) + xstage_bytes(M, K) + extra <= stream_budget<NSUB>();
 }
 
 template <int NSUB>
-int staged_stages(int M, int K) {
+int staged_stages(int M, int K, int extra = 0) {
   for (int s = W4A16_TC_MAX_STAGES; s > 2; --s)
-    if (stream_smem<NSUB>(s, 0) + xstage_bytes(M, K) <= stream_budget<NSUB>()) return s;
+    if (stream_smem<NSUB>(s, 0) + xstage_bytes(M, K) + extra <= stream_budget<NSUB>()) return s;
   return 2;
 }
 
@@ -1734,11 +1737,12 @@ cudaError_t stream_launch_t(const Maps& map, const StreamParams& p, int sms, int
 template <int NSUB>
 cudaError_t launch_stream_t(const Maps& map, StreamParams p, int sms, DeviceInfo& d, cudaStream_t stream, int pdl) {
   const bool allcols = p.M > 1;
-  const bool staged = stage_activations<NSUB>(p.M, p.K, p.units, sms);
+  const int extra = p.idx ? kArgmaxSmem : 0;  // the argmax mode's keys
+  const bool staged = stage_activations<NSUB>(p.M, p.K, p.units, sms, extra);
   p.xpitch = staged ? 2 * p.K + 64 : 0;
-  p.stages = staged ? staged_stages<NSUB>(p.M, p.K) : stream_stages<NSUB>(p.M);
+  p.stages = staged ? staged_stages<NSUB>(p.M, p.K, extra) : stream_stages<NSUB>(p.M, extra);
   p.prefetch = pdl >= 2;
-  int smem = stream_smem<NSUB>(p.stages, staged ? 0 : p.M);
+  int smem = stream_smem<NSUB>(p.stages, staged ? 0 : p.M) + extra;
   if (staged) smem += xstage_bytes(p.M, p.K);
   const bool on = pdl > 0;
   using Fn = cudaError_t (*)(const Maps&, const StreamParams&, int, int, DeviceInfo&, cudaStream_t, bool);
