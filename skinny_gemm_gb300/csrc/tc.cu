@@ -2129,7 +2129,14 @@ cudaError_t launch_tc_id(const LaunchArgs& a, const w4a16_plan& plan) {
   if (cudaError_t e = cudaGetDevice(&dev)) return e;
   if (a.tc_path != 2 && a.T <= kRoutedStreamMaxT) {
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    return launch_stream_routed(a, device_info(dev));
+    DeviceInfo& d = device_info(dev);
+    // The persistent routed mode pays when the chunks can give every warp of
+    // its grid (two CTAs of four warps per SM) a unit: at most T chunks of
+    // ceil(N / 32) units each.  With fewer, the tile kernel splits K over
+    // more CTAs instead (measured: 8 x 6144x2048 at T = 8: 12.6 against 15.2
+    // us; 8 x 2048x2048 at T = 8: 11.2 against 7.5; 16 x 512x8192 at T = 4:
+    // 26.1 against 7.5).
+    if (a.tc_path == 1 || (int64_t)a.T * cdiv(a.N, kTileRows) >= 8 * d.sms) return launch_stream_routed(a, d);
   }
   if (a.tc_path != 1) {  // the tile kernel in routed mode, where it fits
     const TilePlan tp = tile_plan_r(s, a.N, routed_xcap(a.T, a.E), true, 1);
