@@ -33,9 +33,10 @@
  * verify GEMM is arithmetic-identical to the sequential GEMV, batch equals
  * sequential bitwise]).  The kernel and its reduction order are chosen from
  * (N, K) only, never from M, so row m of any call equals, bit for bit, the
- * M = 1 call on x[m].  Calls with M > 8 run as consecutive chunks of at most
- * eight rows through the same kernels.  w4a16_mm_id rows equal w4a16_mm on
- * the selected expert, bit for bit.
+ * M = 1 call on x[m].  Calls with M > 8 take the rows eight at a time
+ * through the same arithmetic (the tile kernel in one launch over resident
+ * weights, the other kernels one launch per chunk).  w4a16_mm_id rows equal
+ * w4a16_mm on the selected expert, bit for bit.
  *
  * Ownership and synchronisation.  All tensor pointers are DEVICE pointers
  * owned by the caller.  `stream` is a cudaStream_t (NULL = legacy default
@@ -49,8 +50,9 @@
  * (device, stream): 4.78 MiB, enough for every shape, allocated with
  * cudaMalloc (and its counters zeroed on the stream) by the first call that
  * needs it on that stream.  The tile kernel exchanges them in shared memory
- * and needs none.  It stays
- * allocated until the process exits.  Calls
+ * and needs none.  The argmax entry point and the dynamic dealing of work
+ * units use a few counters of the same workspace.  It stays allocated until
+ * the process exits.  Calls
  * on one stream are ordered and share it safely; calls on different streams
  * use different workspaces.  A call that would need to allocate while its
  * stream is being captured into a CUDA graph fails with W4A16_ERR_CUDA, so
