@@ -44,15 +44,15 @@
  * done and never synchronise, except w4a16_device_status and the one-time
  * workspace set-up below.
  *
- * Workspace.  When the tensor-core kernel's persistent grid splits K across
- * warps of different SMs (w4a16_get_plan: ksplit > 1 with that launch shape)
- * it exchanges fp32 slice sums through a workspace the library owns, one per
- * (device, stream): 4.78 MiB, enough for every shape, allocated with
- * cudaMalloc (and its counters zeroed on the stream) by the first call that
- * needs it on that stream.  The tile kernel exchanges them in shared memory
- * and needs none.  The argmax entry point and the dynamic dealing of work
- * units use a few counters of the same workspace.  It stays allocated until
- * the process exits.  Calls
+ * Workspace.  The tensor-core kernel's persistent grid deals its work units
+ * through a counter in a workspace the library owns, one per (device,
+ * stream), and when it splits K across warps of different SMs
+ * (w4a16_get_plan: ksplit > 1 with that launch shape) it exchanges fp32
+ * slice sums through the same workspace: 4.78 MiB, enough for every shape,
+ * allocated with cudaMalloc (and its counters zeroed on the stream) by the
+ * first call that needs it on that stream.  The tile kernel exchanges its
+ * slice sums in shared memory and needs none.  w4a16_mm_argmax keeps its
+ * keys there too.  It stays allocated until the process exits.  Calls
  * on one stream are ordered and share it safely; calls on different streams
  * use different workspaces.  A call that would need to allocate while its
  * stream is being captured into a CUDA graph fails with W4A16_ERR_CUDA, so
