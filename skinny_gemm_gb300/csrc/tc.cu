@@ -1239,7 +1239,9 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
 //
 // The bound of 768 threads caps registers at 80, so that five CTAs of five
 // warps fit on an SM (by registers).
-template <bool ALLCOLS, bool ROUTED, int G, int R>
+// MULTI: more activation rows than one chunk (M > xcap); a separate instance,
+// so that one-chunk launches carry none of the loop's code.
+template <bool ALLCOLS, bool ROUTED, int G, int R, bool MULTI = false>
 __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ TileArgs<G> ta, TileParams p) {
   constexpr int kRowsR = 16 * R, kCodesR = 2 * R * Geo<1>::kBox, kParamsR = 2 * R * Geo<1>::kParam;
   extern __shared__ uint8_t smem_raw[];
@@ -1390,8 +1392,8 @@ __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Ti
         }
       }
     }
-    // the last chunk (uniform in the cluster); one-row launches have only one
-    if (!ROUTED && (!ALLCOLS || (int)(chunk + 1) * xcap >= p.M)) break;
+    // the last chunk (uniform in the cluster)
+    if (!ROUTED && (!MULTI || (int)(chunk + 1) * xcap >= p.M)) break;
     __syncthreads();  // s_tok is read above and rewritten below
     if (ROUTED) {
       mc = gather_tokens(p.ids, p.T, p.E, e, s_tok, s_state, p.xcap);
@@ -1861,8 +1863,9 @@ TileParams tile_params(const Shape& s, const TilePlan& tp, int K, int M, int row
 template <int G>
 using TileFn = void (*)(TileArgs<G>, TileParams);
 template <int G>
-TileFn<G> tile_fn(bool allcols, bool routed, int R) {
+TileFn<G> tile_fn(bool allcols, bool routed, int R, bool multi = false) {
   if (routed) return tc_tile_kernel<true, true, G, 1>;
+  if (multi) return R == 2 ? tc_tile_kernel<true, false, G, 2, true> : tc_tile_kernel<true, false, G, 1, true>;
   if (R == 2) return allcols ? tc_tile_kernel<true, false, G, 2> : tc_tile_kernel<false, false, G, 2>;
   return allcols ? tc_tile_kernel<true, false, G, 1> : tc_tile_kernel<false, false, G, 1>;
 }
@@ -1883,7 +1886,7 @@ cudaError_t launch_tile(const LaunchArgs& a, const Shape& s, const TilePlan& tp,
     p.E = a.E;
     p.prefetch = 0;  // the weights to read depend on the ids
   }
-  TileFn<1> fn = tile_fn<1>(a.M > 1, routed, tp.R);
+  TileFn<1> fn = tile_fn<1>(a.M > 1, routed, tp.R, !routed && a.M > tp.xcap);
   if (cudaError_t e = allow_smem(fn, d)) return e;
   const dim3 grid(tp.ctas, routed ? a.E : 1);
   return launch_ex(fn, grid, dim3(tp.warps * 32), tp.smem, a.stream, a.pdl > 0, tp.kc, ta, p);
@@ -2211,7 +2214,7 @@ cudaError_t launch_tc_group(const GroupItem* items, int count, int M, int row0, 
   ta.tile0[kMaxGroup] = tiles;
   TileParams p = tile_params(s, tp, K, M, row0, flags, pdl);
   p.items = count;
-  TileFn<kMaxGroup> fn = tile_fn<kMaxGroup>(M > 1, false, tp.R);
+  TileFn<kMaxGroup> fn = tile_fn<kMaxGroup>(M > 1, false, tp.R, M > tp.xcap);
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DeviceInfo& d = device_info(dev);
   if (cudaError_t e = allow_smem(fn, d)) return e;
