@@ -1833,7 +1833,9 @@ TilePlan tile_plan_r(const Shape& s, int N, int M, bool force, int R) {
 // With several activation rows, 32-row CTAs (R = 2) halve the activation
 // chunks per weight in shared memory; they are taken when they need fewer
 // waves of CTAs than 16-row ones (on 2560x10240 at M = 5 the 16-row CTAs no
-// longer fit in one wave).
+// longer fit in one wave), or as few when both fit in one (12288x1536 at
+// M = 3 / 5: 6.08 -> 5.78 / 6.20 -> 5.98 us; on a tie at two waves 16-row
+// CTAs stay faster: 10240x2560 at M = 5, 7.4 against 8.0 us).
 TilePlan tile_plan(const Shape& s, int N, int M, bool force, int sms = 152) {
   const TilePlan one = tile_plan_r(s, N, M, force, 1);
   if (M < 2) return one;
@@ -1842,7 +1844,7 @@ TilePlan tile_plan(const Shape& s, int N, int M, bool force, int sms = 152) {
   if (one.kc == 0) return two;
   const int w1 = cdiv(one.ctas, sms * tile_ctas_per_sm(one.warps, one.smem));
   const int w2 = cdiv(two.ctas, sms * tile_ctas_per_sm(two.warps, two.smem));
-  return w2 < w1 ? two : one;
+  return (w2 < w1 || (w2 == w1 && w1 == 1)) ? two : one;
 }
 
 TileParams tile_params(const Shape& s, const TilePlan& tp, int K, int M, int row0, int* flags, int pdl) {
