@@ -19,7 +19,8 @@
  *   normal  z    = Box-Muller on h(.., 2i) and h(.., 2i+1) in fp64
  *   bf16(v)      = IEEE round-to-nearest-even of the fp32 value (float)v
  *
- * Tensor ids: x = 1, packed codes = 2, scales = 3, bias noise = 4, ids = 5.
+ * Tensor ids: x = 1, packed codes = 2, scales = 3, bias noise = 4, ids = 5,
+ * STQ1_0 code and sign bytes = 6, STQ1_0 scales = 7.
  *
  * Ownership: every pointer is a HOST pointer owned by the caller; the
  * library allocates nothing and keeps no state.  Calls are thread-safe.
@@ -39,7 +40,9 @@ enum {
   W4A16_SYNTH_TID_CODES = 2,
   W4A16_SYNTH_TID_SCALES = 3,
   W4A16_SYNTH_TID_BIAS_NOISE = 4,
-  W4A16_SYNTH_TID_IDS = 5
+  W4A16_SYNTH_TID_IDS = 5,
+  W4A16_SYNTH_TID_STQ1_BITS = 6,
+  W4A16_SYNTH_TID_STQ1_SCALE = 7
 };
 
 /* Raw counter hash h(seed, tid, i) for i in [offset, offset + n). */
@@ -65,6 +68,25 @@ int w4a16_synth_group_params(uint64_t seed, uint64_t offset, int64_t n,
 /* Expert ids: out[t] = floor(E * (h(seed, 5, t) >> 32) / 2^32), uniform on
  * 0..E-1.  Returns -2 if E <= 0. */
 int w4a16_synth_ids(uint64_t seed, int64_t T, int32_t E, int32_t* out);
+
+/* Float32 activations: out[i] = (float)(N(0,1) draw number offset+i of
+ * tensor id 1) -- the draws of w4a16_synth_x before their bf16 rounding. */
+int w4a16_synth_x_f32(uint64_t seed, uint64_t offset, int64_t n, float* out);
+
+/* STQ1_0 blocks of the "Hy4-preview Metal kernels for llama.cpp" page
+ * (section "Notes and gotchas"), 42 bytes each, for blocks
+ * [offset, offset + n) of a row-major [N][K/256] block matrix:
+ *   bytes 0..39  = little-endian bytes of h(seed, 6, 5*blk + w), w = 0..4
+ *                  (32 bytes of 4-bit group codes, then 8 bytes of group
+ *                  sign bits: every code uniform on 0..15, every sign bit
+ *                  uniform, all independent),
+ *   bytes 40..41 = fp16(0.002 + 0.018 * u), u from h(seed, 7, blk), little
+ *                  endian (finite, as the page's "Test-data hygiene" asks).
+ * out must hold 42 * n bytes. */
+int w4a16_synth_stq1(uint64_t seed, uint64_t offset, int64_t n, uint8_t* out);
+
+/* fp16 bits of v, IEEE round to nearest even (the encoder the blocks use). */
+int w4a16_synth_fp16(float v, uint16_t* out);
 
 /* Number of host threads the generator uses (all online cores, <= 64). */
 int w4a16_synth_threads(void);

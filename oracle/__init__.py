@@ -15,6 +15,9 @@ Citations (page titles; sections in quotes):
 
 Acceptance bound used by the parity tests (written out in ``tolerance``):
   |y - y_ref| <= ulp_bf16(y_ref) + 1e-3 * sum_k |x[m,k] * w[n,k]|
+and for the float32 STQ1_0 path of [HY4] ``stq1_tolerance``.
+
+  [HY4]  "Hy4-preview Metal kernels for llama.cpp"
 """
 from __future__ import annotations
 
@@ -91,6 +94,16 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_mm_g.restype = i32
     lib.oracle_mm_id.argtypes = [P, P, P, P, P, i64, i64, i64, i64, P, i64, P, P, i32]
     lib.oracle_mm_id.restype = i32
+    lib.oracle_fp16_to_double.argtypes = [ctypes.c_uint16]
+    lib.oracle_fp16_to_double.restype = ctypes.c_double
+    lib.oracle_stq1_lanes.argtypes = [i32, i32, P]
+    lib.oracle_stq1_lanes.restype = i32
+    lib.oracle_stq1_dequant.argtypes = [P, i64, i64, P]
+    lib.oracle_stq1_dequant.restype = i32
+    lib.oracle_stq1_mm.argtypes = [P, P, i64, i64, i64, P, i64, P, P, i32]
+    lib.oracle_stq1_mm.restype = i32
+    lib.oracle_stq1_mm_id.argtypes = [P, P, P, i64, i64, i64, i64, P, i64, P, P, i32]
+    lib.oracle_stq1_mm_id.restype = i32
     return lib
 
 
@@ -212,6 +225,72 @@ class Oracle:
                                      _ptr(y), _ptr(ad), threads), "mm_id")
         return y, ad
 
+    # -- STQ1_0, the ternary format of [HY4] (blocks: uint8 [N][K/256][42]) --
+    def fp16_to_f64(self, h: int) -> float:
+        return self.lib.oracle_fp16_to_double(int(h) & 0xFFFF)
+
+    def stq1_lanes(self, c: int, s: int) -> list[int]:
+        """The four lane values of group code c under group sign bit s."""
+        v = np.zeros(4, dtype=np.int32)
+        _check(self.lib.oracle_stq1_lanes(int(c), int(s), _ptr(v)), "stq1_lanes")
+        return [int(t) for t in v]
+
+    def stq1_dequant(self, blocks, N: int, K: int) -> np.ndarray:
+        """Weights w[N][K] = d * v in fp64."""
+        b = _c(blocks, np.uint8)
+        out = np.empty((N, K), dtype=np.float64)
+        _check(self.lib.oracle_stq1_dequant(_ptr(b), N, K, _ptr(out)), "stq1_dequant")
+        return out
+
+    def stq1_mm(self, x, blocks, M: int, N: int, K: int, cols=None, threads: int = 0):
+        """(y, absdot), fp64 [M][ncols]: y = x W^T for float32 x [M][K]."""
+        x_ = _c(x, np.float32)
+        b = _c(blocks, np.uint8)
+        c = None if cols is None else _c(cols, np.int64)
+        nc = N if c is None else c.size
+        y = np.empty((M, nc), dtype=np.float64)
+        ad = np.empty((M, nc), dtype=np.float64)
+        _check(self.lib.oracle_stq1_mm(_ptr(x_), _ptr(b), M, N, K, _ptr(c), nc, _ptr(y), _ptr(ad), threads),
+               "stq1_mm")
+        return y, ad
+
+    def stq1_mm_id(self, x, blocks, ids, T: int, N: int, K: int, E: int, cols=None, threads: int = 0):
+        """(y, absdot), fp64 [T][ncols]: y[t] = W[ids[t]] x[t]; bad ids give zero rows."""
+        x_ = _c(x, np.float32)
+        b = _c(blocks, np.uint8)
+        i_ = _c(ids, np.int32)
+        c = None if cols is None else _c(cols, np.int64)
+        nc = N if c is None else c.size
+        y = np.empty((T, nc), dtype=np.float64)
+        ad = np.empty((T, nc), dtype=np.float64)
+        _check(self.lib.oracle_stq1_mm_id(_ptr(x_), _ptr(b), _ptr(i_), T, N, K, E, _ptr(c), nc, _ptr(y), _ptr(ad),
+                                          threads), "stq1_mm_id")
+        return y, ad
+
+    def stq1_get_rows(self, blocks, ids, N: int, K: int) -> np.ndarray:
+        """float32 [T][K]: the weights d * v of the rows ids ([HY4] kernel table:
+        kernel_get_rows_stq1_0, the row gather), exact in float32; an id outside
+        0..N-1 gives a row of zeros."""
+        ids = np.asarray(ids, dtype=np.int64).reshape(-1)
+        ok = (ids >= 0) & (ids < N)
+        b = np.asarray(blocks, dtype=np.uint8).reshape(N, -1)
+        w = self.stq1_dequant(b[np.where(ok, ids, 0)], len(ids), K)
+        out = w.astype(np.float32)
+        out[~ok] = 0
+        return out
+
+
+def stq1_tolerance(absdot, K: int) -> np.ndarray:
+    """Acceptance bound for the float32 STQ1_0 outputs:
+        |y - y_ref| <= (2^-16 + (K/256 + 16) * 2^-23) * sum_k |x[m,k] * w[n,k]|
+    The activations enter the tensor cores as three bf16 parts that sum to x
+    exactly; the products with ternary weights are exact; what rounds is the
+    fp32 accumulation: 16 steps of 16 products per 256-weight block (each
+    step allowed a 2^-22 relative error), then one fused multiply-add with
+    the block scale per block, the K-slice sums and the sum of the three
+    parts (one 2^-24 rounding each, bounded here by 2^-23 apiece)."""
+    return (2.0 ** -16 + (K // 256 + 16) * 2.0 ** -23) * np.asarray(absdot, dtype=np.float64)
+
 
 _default = None
 
@@ -262,6 +341,22 @@ def mm(x, Wq, scales, biases, M, N, K, cols=None, threads: int = 0, group: int =
 
 def mm_id(x, Wq, scales, biases, ids, T, N, K, E, cols=None, threads: int = 0):
     return default().mm_id(x, Wq, scales, biases, ids, T, N, K, E, cols, threads)
+
+
+def stq1_dequant(blocks, N, K):
+    return default().stq1_dequant(blocks, N, K)
+
+
+def stq1_mm(x, blocks, M, N, K, cols=None, threads: int = 0):
+    return default().stq1_mm(x, blocks, M, N, K, cols, threads)
+
+
+def stq1_mm_id(x, blocks, ids, T, N, K, E, cols=None, threads: int = 0):
+    return default().stq1_mm_id(x, blocks, ids, T, N, K, E, cols, threads)
+
+
+def stq1_get_rows(blocks, ids, N, K):
+    return default().stq1_get_rows(blocks, ids, N, K)
 
 
 def host_threads() -> int:

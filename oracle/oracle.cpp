@@ -35,6 +35,10 @@
  * The pages name llama.cpp's mul_mat_id ([HY4] kernel table) without a
  * signature; top-1 routing is the plainest reading.
  *
+ * STQ1_0 (the ternary format of [HY4]): stq1_* below, with the block layout
+ * and the reading of the lane decode written beside the code.  Activations
+ * are float32 and outputs fp64, as in the page's _f32 kernels.
+ *
  * bf16: raw 16-bit patterns.  Decoding and round-to-nearest-even encoding are
  * written here from the bfloat16 definition (1 sign, 8 exponent bits with
  * bias 127, 7 fraction bits; subnormal spacing 2^-133), with plain fp64
@@ -150,6 +154,93 @@ void parallel_over(int64_t n, int threads, F fn) {
 
 bool group_ok(int64_t G) { return G == 64 || G == 128; }
 bool shape_ok(int64_t K, int64_t G = kGroup) { return group_ok(G) && K > 0 && K % G == 0; }
+
+// ---- STQ1_0: the ternary format of [HY4] ------------------------------------
+//
+// One block holds 256 weights in 42 bytes [HY4 "Notes and gotchas": "42-byte
+// block stride" and the block-layout note]: 32 bytes of 4-bit group codes,
+// 8 bytes of group sign bits, and an fp16 scale d, in that order (the order
+// the page lists them; read as the byte layout).  Weight w of a block belongs
+// to group g = (w/64)*16 + w%16 at lane p = (w%64)/16 [same note].  Code
+// nibble g is qs[g/2] >> 4*(g%2) (low nibble first, as the W4 codes of
+// [W2D2 "Packed Storage Layout"]); sign bit g is bit g%8 of sign[g/8]; d is
+// little endian.  The lane values of a group [HY4 "Results", the fourth
+// decode pass]: the code's high two bits name the zero lane, its low two
+// bits flip the signs of two of the other three lanes, and the sign bit
+// negates the whole group.  Which two lanes the flips reach is not written
+// out; the reading taken here is: the three non-zero lanes in ascending lane
+// order, bit 0 flips the first, bit 1 the second, the third stays +1.
+// A weight is d * v with v in {-1, 0, +1}.
+
+const int kStqWeights = 256;
+const int kStqBytes = 42;
+
+// IEEE binary16 from its definition: 1 sign, 5 exponent bits with bias 15,
+// 10 fraction bits; subnormals frac * 2^-24.
+double fp16_decode(uint16_t h) {
+  const int sign = (h >> 15) & 1;
+  const int efield = (h >> 10) & 0x1F;
+  const int frac = h & 0x3FF;
+  double mag;
+  if (efield == 0x1F) {
+    if (frac != 0) return std::nan("");
+    mag = INFINITY;
+  } else if (efield == 0) {
+    mag = std::ldexp((double)frac, -24);
+  } else {
+    mag = std::ldexp((double)(1024 + frac), efield - 15 - 10);
+  }
+  return sign ? -mag : mag;
+}
+
+// The four lane values of code c (0..15) under group sign s (0 or 1).
+void stq1_lanes(int c, int s, int v[4]) {
+  const int zero_lane = c >> 2;
+  int rank = 0;  // position among the non-zero lanes, ascending
+  for (int l = 0; l < 4; ++l) {
+    if (l == zero_lane) {
+      v[l] = 0;
+      continue;
+    }
+    const int flip = rank == 0 ? (c & 1) : rank == 1 ? ((c >> 1) & 1) : 0;
+    v[l] = flip ? -1 : 1;
+    ++rank;
+  }
+  if (s)
+    for (int l = 0; l < 4; ++l) v[l] = -v[l];
+}
+
+// Weight w (0..255) of one block.
+double stq1_weight(const uint8_t* block, int w) {
+  const int g = (w / 64) * 16 + w % 16;
+  const int p = (w % 64) / 16;
+  const int c = (block[g / 2] >> (4 * (g % 2))) & 0xF;
+  const int s = (block[32 + g / 8] >> (g % 8)) & 1;
+  int v[4];
+  stq1_lanes(c, s, v);
+  const uint16_t dbits = (uint16_t)(block[40] | (block[41] << 8));
+  return fp16_decode(dbits) * (double)v[p];
+}
+
+// One output of y = x W^T: row n of a [N][K/256][42] block matrix against a
+// float32 activation row, in fp64, weights in storage order.
+void stq1_dot_one(const float* xrow, const uint8_t* blocks, int64_t K, int64_t n, double* y, double* absdot) {
+  const int64_t nb = K / kStqWeights;
+  double sum = 0.0, abs_sum = 0.0;
+  for (int64_t b = 0; b < nb; ++b) {
+    const uint8_t* block = blocks + (n * nb + b) * kStqBytes;
+    for (int w = 0; w < kStqWeights; ++w) {
+      const double a = (double)xrow[b * kStqWeights + w];
+      const double wt = stq1_weight(block, w);
+      sum += a * wt;
+      abs_sum += std::fabs(a * wt);
+    }
+  }
+  *y = sum;
+  if (absdot) *absdot = abs_sum;
+}
+
+bool stq1_shape_ok(int64_t K) { return K > 0 && K % kStqWeights == 0; }
 
 }  // namespace
 
@@ -268,6 +359,70 @@ int oracle_mm_id(const uint16_t* x, const uint32_t* Wq, const uint16_t* S, const
       }
       dot_one(x + t * K, Wq + e * words, S + e * params, B + e * params, K, n, kGroup, &y[t * ncols + j],
               absdot ? &absdot[t * ncols + j] : nullptr);
+    }
+  });
+  return 0;
+}
+
+// ---- STQ1_0 [HY4] ---------------------------------------------------------------
+
+double oracle_fp16_to_double(uint16_t h) { return fp16_decode(h); }
+
+// v[4] of code c under sign s (the lane values of one group).
+int oracle_stq1_lanes(int c, int s, int* v) {
+  if (!v || c < 0 || c > 15 || (s != 0 && s != 1)) return -2;
+  stq1_lanes(c, s, v);
+  return 0;
+}
+
+// w[n][k] in fp64 for a [N][K/256][42] block matrix.
+int oracle_stq1_dequant(const uint8_t* blocks, int64_t N, int64_t K, double* w) {
+  if (!blocks || !w) return -1;
+  if (N < 0 || !stq1_shape_ok(K)) return -2;
+  const int64_t nb = K / kStqWeights;
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t k = 0; k < K; ++k)
+      w[n * K + k] = stq1_weight(blocks + (n * nb + k / kStqWeights) * kStqBytes, (int)(k % kStqWeights));
+  return 0;
+}
+
+// y[m][j] = sum_k x[m,k] w[cols[j], k] (all n when cols is NULL), x float32.
+int oracle_stq1_mm(const float* x, const uint8_t* blocks, int64_t M, int64_t N, int64_t K, const int64_t* cols,
+                   int64_t ncols, double* y, double* absdot, int threads) {
+  if (!x || !blocks || !y) return -1;
+  if (M < 0 || N < 0 || ncols < 0 || !stq1_shape_ok(K)) return -2;
+  if (!cols && ncols != N) return -2;
+  for (int64_t j = 0; cols && j < ncols; ++j)
+    if (cols[j] < 0 || cols[j] >= N) return -2;
+  parallel_over(ncols, threads, [&](int64_t j) {
+    const int64_t n = cols ? cols[j] : j;
+    for (int64_t m = 0; m < M; ++m)
+      stq1_dot_one(x + m * K, blocks, K, n, &y[m * ncols + j], absdot ? &absdot[m * ncols + j] : nullptr);
+  });
+  return 0;
+}
+
+// Routed experts over blocks[E][N][K/256][42]: y[t] = W[ids[t]] x[t]; an id
+// outside 0..E-1 gives a zero row.
+int oracle_stq1_mm_id(const float* x, const uint8_t* blocks, const int32_t* ids, int64_t T, int64_t N, int64_t K,
+                      int64_t E, const int64_t* cols, int64_t ncols, double* y, double* absdot, int threads) {
+  if (!x || !blocks || !ids || !y) return -1;
+  if (T < 0 || N < 0 || E <= 0 || ncols < 0 || !stq1_shape_ok(K)) return -2;
+  if (!cols && ncols != N) return -2;
+  for (int64_t j = 0; cols && j < ncols; ++j)
+    if (cols[j] < 0 || cols[j] >= N) return -2;
+  const int64_t per_expert = N * (K / kStqWeights) * kStqBytes;
+  parallel_over(ncols, threads, [&](int64_t j) {
+    const int64_t n = cols ? cols[j] : j;
+    for (int64_t t = 0; t < T; ++t) {
+      const int64_t e = ids[t];
+      if (e < 0 || e >= E) {
+        y[t * ncols + j] = 0.0;
+        if (absdot) absdot[t * ncols + j] = 0.0;
+        continue;
+      }
+      stq1_dot_one(x + t * K, blocks + e * per_expert, K, n, &y[t * ncols + j],
+                   absdot ? &absdot[t * ncols + j] : nullptr);
     }
   });
   return 0;

@@ -13,6 +13,11 @@
  * "Gemma 4 E4B & E2B -- single-launch Metal megakernels" model card, section
  * "Usage").  Scales are kept finite and positive-range, as the "Hy4-preview
  * Metal kernels for llama.cpp" notes ("Test-data hygiene") advise.
+ *
+ * The same page's STQ1_0 blocks (section "Notes and gotchas": 32 bytes of
+ * 4-bit group codes, 8 bytes of group sign bits, an fp16 scale; 42 bytes per
+ * 256 weights) are drawn as uniform random bytes and a finite fp16 scale,
+ * with float32 activations for its _f32 kernels.
  */
 #include "w4a16_synth.h"
 
@@ -46,6 +51,31 @@ static inline uint16_t f32_to_bf16(float f) {
   if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (uint16_t)((u >> 16) | 0x0040u);
   u += 0x7FFFu + ((u >> 16) & 1u);
   return (uint16_t)(u >> 16);
+}
+
+/* IEEE-754 binary32 -> binary16, round to nearest, ties to even, through
+ * exact double arithmetic: v = r * spacing with r rounded to an integer. */
+static uint16_t f32_to_fp16(float f) {
+  const uint16_t sign = signbit(f) ? 0x8000 : 0;
+  if (isnan(f)) return (uint16_t)(sign | 0x7E00);
+  double a = fabs((double)f);
+  if (isinf(a)) return (uint16_t)(sign | 0x7C00);
+  if (a == 0.0) return sign;
+  int ex;
+  frexp(a, &ex); /* a = m * 2^ex, m in [0.5, 1): binade exponent ex - 1 */
+  int e = ex - 1;
+  int spacing_exp = (e < -14) ? -24 : e - 10;
+  double q = ldexp(a, -spacing_exp), fl = floor(q), diff = q - fl, r;
+  if (diff > 0.5) r = fl + 1.0;
+  else if (diff < 0.5) r = fl;
+  else r = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+  double res = ldexp(r, spacing_exp);
+  if (res >= 65520.0) return (uint16_t)(sign | 0x7C00);
+  if (res < ldexp(1.0, -14)) return (uint16_t)(sign | (uint16_t)r); /* subnormal or 2^-14 itself */
+  frexp(res, &ex);
+  e = ex - 1;
+  double sig = ldexp(res, -(e - 10)); /* in [1024, 2048) */
+  return (uint16_t)(sign | (uint16_t)((e + 15) << 10) | (uint16_t)((int)sig - 1024));
 }
 
 static inline double uniform24(uint64_t h) { return (double)(h >> 40) * (1.0 / 16777216.0); }
@@ -191,5 +221,50 @@ int w4a16_synth_ids(uint64_t seed, int64_t T, int32_t E, int32_t* out) {
     uint64_t h = hash_at(key, (uint64_t)t) >> 32;
     out[t] = (int32_t)((h * (uint64_t)E) >> 32);
   }
+  return 0;
+}
+
+static void do_x_f32(void* p, int64_t lo, int64_t hi) {
+  ctx_t* c = (ctx_t*)p;
+  float* o = (float*)c->out;
+  for (int64_t i = lo; i < hi; ++i) o[i] = (float)normal_at(c->key, c->offset + (uint64_t)i);
+}
+
+int w4a16_synth_x_f32(uint64_t seed, uint64_t offset, int64_t n, float* out) {
+  if (n < 0) return -2;
+  if (n > 0 && !out) return -1;
+  ctx_t c = {stream_key(seed, W4A16_SYNTH_TID_X), offset, out, NULL, 0};
+  parallel_for(n, do_x_f32, &c);
+  return 0;
+}
+
+static void do_stq1(void* p, int64_t lo, int64_t hi) {
+  ctx_t* c = (ctx_t*)p;
+  uint8_t* o = (uint8_t*)c->out;
+  for (int64_t i = lo; i < hi; ++i) {
+    const uint64_t blk = c->offset + (uint64_t)i;
+    uint8_t* b = o + i * 42;
+    for (int w = 0; w < 5; ++w) { /* 40 bytes: qs[32] then sign[8] */
+      const uint64_t h = hash_at(c->key, blk * 5 + (uint64_t)w);
+      for (int j = 0; j < 8; ++j) b[w * 8 + j] = (uint8_t)(h >> (8 * j));
+    }
+    const uint16_t d = f32_to_fp16((float)(0.002 + 0.018 * uniform24(hash_at(c->key2, blk))));
+    b[40] = (uint8_t)(d & 0xFF);
+    b[41] = (uint8_t)(d >> 8);
+  }
+}
+
+int w4a16_synth_stq1(uint64_t seed, uint64_t offset, int64_t n, uint8_t* out) {
+  if (n < 0) return -2;
+  if (n > 0 && !out) return -1;
+  ctx_t c = {stream_key(seed, W4A16_SYNTH_TID_STQ1_BITS), offset, out, NULL,
+             stream_key(seed, W4A16_SYNTH_TID_STQ1_SCALE)};
+  parallel_for(n, do_stq1, &c);
+  return 0;
+}
+
+int w4a16_synth_fp16(float v, uint16_t* out) {
+  if (!out) return -1;
+  *out = f32_to_fp16(v);
   return 0;
 }

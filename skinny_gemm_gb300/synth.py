@@ -35,8 +35,12 @@ def _load() -> ctypes.CDLL:
             lib.w4a16_synth_codes.argtypes = [u64, u64, i64, P]
             lib.w4a16_synth_group_params.argtypes = [u64, u64, i64, P, P]
             lib.w4a16_synth_ids.argtypes = [u64, i64, ctypes.c_int32, P]
+            lib.w4a16_synth_x_f32.argtypes = [u64, u64, i64, P]
+            lib.w4a16_synth_stq1.argtypes = [u64, u64, i64, P]
+            lib.w4a16_synth_fp16.argtypes = [ctypes.c_float, P]
             for f in ("w4a16_synth_hash", "w4a16_synth_x", "w4a16_synth_codes",
-                      "w4a16_synth_group_params", "w4a16_synth_ids", "w4a16_synth_threads"):
+                      "w4a16_synth_group_params", "w4a16_synth_ids", "w4a16_synth_threads",
+                      "w4a16_synth_x_f32", "w4a16_synth_stq1", "w4a16_synth_fp16"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -109,6 +113,33 @@ def make_weights(seed: int, N: int, K: int, E: int = 1) -> HostW4:
         raise ValueError("K must be a multiple of 64")
     s, b = make_group_params(seed, N, K, E)
     return HostW4(make_codes(seed, N, K, E), s, b, N, K, E)
+
+
+def make_x_f32(seed: int, M: int, K: int, row0: int = 0) -> np.ndarray:
+    """Float32 activations x[M][K], rows row0..row0+M-1 of the seeded stream."""
+    out = np.empty((M, K), dtype=np.float32)
+    _ok(_load().w4a16_synth_x_f32(seed, row0 * K, M * K, _p(out)), "x f32")
+    return out
+
+
+STQ1_WEIGHTS = 256  # weights per STQ1_0 block
+STQ1_BYTES = 42     # bytes per STQ1_0 block
+
+
+def make_stq1(seed: int, N: int, K: int, E: int = 1) -> np.ndarray:
+    """STQ1_0 blocks uint8 [N][K/256][42] (or [E][N][K/256][42]) in the page's layout."""
+    if K % STQ1_WEIGHTS:
+        raise ValueError("K must be a multiple of 256")
+    shape = (N, K // STQ1_WEIGHTS, STQ1_BYTES) if E == 1 else (E, N, K // STQ1_WEIGHTS, STQ1_BYTES)
+    out = np.empty(shape, dtype=np.uint8)
+    _ok(_load().w4a16_synth_stq1(seed, 0, out.size // STQ1_BYTES, _p(out)), "stq1")
+    return out
+
+
+def fp16_bits(v: float) -> int:
+    out = np.zeros(1, dtype=np.uint16)
+    _ok(_load().w4a16_synth_fp16(ctypes.c_float(v), _p(out)), "fp16")
+    return int(out[0])
 
 
 def threads() -> int:

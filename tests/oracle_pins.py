@@ -440,7 +440,159 @@ def pin_group128(o):
     assert np.array_equal(w0, np.repeat(torch_bf16_to_f64(B), 128, axis=1)), "group 128 dequant bias"
 
 
+# ---- STQ1_0, the ternary format of [HY4] "Notes and gotchas" -------------------
+
+SQW, SQB = 256, 42  # weights and bytes per block
+
+
+def _stq1_block(codes, signs, dbits: int) -> np.ndarray:
+    """One 42-byte block from 64 group codes, 64 sign bits and fp16 bits, laid
+    out as the page lists: qs[32] (two codes a byte, group g in byte g/2, low
+    nibble for even g), sign[8] (bit g%8 of byte g/8), d little endian."""
+    b = np.zeros(SQB, dtype=np.uint8)
+    for g in range(64):
+        b[g // 2] |= (int(codes[g]) & 0xF) << (4 * (g % 2))
+        b[32 + g // 8] |= (int(signs[g]) & 1) << (g % 8)
+    b[40], b[41] = dbits & 0xFF, dbits >> 8
+    return b
+
+
+def _fp16(bits: int) -> float:
+    """fp16 bits -> float via numpy's float16 (a library decoder)."""
+    return float(np.array([bits], dtype=np.uint16).view(np.float16).astype(np.float64)[0])
+
+
+ONE16 = 0x3C00  # fp16 1.0
+
+
+def _stq1_group0(o, c: int, s: int) -> list[int]:
+    """Lane values of group 0 read back through dequant (the path mm takes):
+    every group holds code c and sign s, d = 1; group 0 owns weights 0, 16, 32, 48."""
+    w = o.stq1_dequant(_stq1_block([c] * 64, [s] * 64, ONE16), 1, SQW)[0]
+    return [int(w[16 * p]) for p in range(4)]
+
+
+def pin_stq1_codebook(o):
+    """The 32 group patterns against what the page fixes: one zero lane, named
+    by the code's high bits; three +-1 lanes; a 32-entry codebook whose sign = 1
+    half is the negation of the sign = 0 half, i.e. codebook bytes
+    q' = 0xAA - q with lane l stored as v + 1 in bits 2l..2l+1; two low code
+    bits that each flip one lane's sign; all 32 patterns distinct, which with
+    one zero and three unit lanes is every such pattern.  Last the reading of
+    which lanes the flips reach (ascending order of the non-zero lanes)."""
+    import itertools
+    pats = {}
+    for s in (0, 1):
+        for c in range(16):
+            v = _stq1_group0(o, c, s)
+            assert v == o.stq1_lanes(c, s), f"dequant and the lane table disagree at code {c}, sign {s}"
+            assert v.count(0) == 1 and v.index(0) == c >> 2, f"zero lane of code {c}"
+            assert all(abs(t) == 1 for i, t in enumerate(v) if i != c >> 2)
+            pats[(c, s)] = v
+    byte = {k: sum((v[l] + 1) << (2 * l) for l in range(4)) for k, v in pats.items()}
+    for c in range(16):
+        assert byte[(c, 1)] == 0xAA - byte[(c, 0)], f"codebook byte identity fails at code {c}"
+    every = {p for p in itertools.product((-1, 0, 1), repeat=4) if p.count(0) == 1}
+    assert {tuple(v) for v in pats.values()} == every and len(every) == 32
+    for z in range(4):
+        base = pats[(4 * z, 0)]
+        assert all(t in (0, 1) for t in base), "flip bits 00 flip nothing"
+        d1 = [i for i in range(4) if pats[(4 * z + 1, 0)][i] != base[i]]
+        d2 = [i for i in range(4) if pats[(4 * z + 2, 0)][i] != base[i]]
+        d3 = [i for i in range(4) if pats[(4 * z + 3, 0)][i] != base[i]]
+        assert len(d1) == 1 and len(d2) == 1 and d1 != d2 and sorted(d1 + d2) == d3, f"flip bits, zero lane {z}"
+        nz = [i for i in range(4) if i != z]
+        assert d1 == [nz[0]] and d2 == [nz[1]], "reading: bit 0 flips the first non-zero lane, bit 1 the second"
+
+
+def pin_stq1_layout(o):
+    """Where each weight, code, sign bit and scale sits: the page's map
+    g = (w/64)*16 + w%16, p = (w%64)/16 seen through zero lanes and a single
+    negated group, fp16 scales against numpy's decoder, and the block order
+    of a row-major [N][K/256] matrix."""
+    w = o.stq1_dequant(_stq1_block([0] * 64, [0] * 64, ONE16), 1, SQW)[0]
+    want = np.array([0.0 if (k % 64) // 16 == 0 else 1.0 for k in range(SQW)])
+    assert np.array_equal(w, want), "code 0 everywhere: lane 0 (w % 64 < 16) must be the zero lane"
+    codes = [12] * 64                 # zero lane 3 everywhere ...
+    codes[5] = 0                      # ... but group 5 (an odd group: high nibble of qs[2]) and
+    codes[20] = 4                     # group 20 (even: low nibble of qs[10]) zero at lanes 0 and 1
+    w = o.stq1_dequant(_stq1_block(codes, [0] * 64, ONE16), 1, SQW)[0]
+    zeros = {k for k in range(SQW) if w[k] == 0}
+    want_zeros = {(g // 16) * 64 + 48 + g % 16 for g in range(64) if g not in (5, 20)} | {5, 64 + 16 + 4}
+    assert zeros == want_zeros, f"zero lanes at {sorted(zeros ^ want_zeros)[:6]} differ from the page's map"
+    signs = [0] * 64
+    signs[10] = 1                     # bit 2 of sign[1]
+    w = o.stq1_dequant(_stq1_block([0] * 64, signs, ONE16), 1, SQW)[0]
+    neg = {k for k in range(SQW) if w[k] < 0}
+    assert neg == {16 + 10, 32 + 10, 48 + 10}, f"negated weights {sorted(neg)}: group 10 is weights 26, 42, 58"
+    for dbits in (0x3555, 0x0001, 0x03FF, 0x0400, 0xBC00, 0x7BFF, 0x1819, 0x251F):
+        w = o.stq1_dequant(_stq1_block([0] * 64, [0] * 64, dbits), 1, SQW)[0]
+        assert w[16] == _fp16(dbits) and w[0] == 0.0, f"fp16 scale 0x{dbits:04x}"
+    ds = [[0x3C00, 0x4000], [0x4200, 0x4400], [0x4500, 0x4600]]  # 1, 2, 3, 4, 5, 6
+    blocks = np.stack([np.stack([_stq1_block([0] * 64, [0] * 64, d) for d in row]) for row in ds])
+    W = o.stq1_dequant(blocks, 3, 2 * SQW)
+    for n in range(3):
+        for b in range(2):
+            assert W[n, b * SQW + 16] == _fp16(ds[n][b]), f"block ({n}, {b}) out of place"
+
+
+def pin_stq1_mm(o):
+    """y = x W^T against closed forms and against dequant: with code 0 and no
+    signs every block adds d * (sum of its lane 1..3 activations); all
+    signs set negates it; unit activations read back single columns of W; a
+    random case equals numpy's fp64 product of the dequantized matrix, and
+    absdot its |x| |W| product; sampled columns equal the full result."""
+    rng = _rng(31)
+    N, K, M = 3, 512, 2
+    dbits = [[int(b) for b in rng.integers(0x1400, 0x3000, size=K // SQW)] for _ in range(N)]
+    for sgn in (0, 1):
+        blocks = np.stack([np.stack([_stq1_block([0] * 64, [sgn] * 64, d) for d in row]) for row in dbits])
+        x = rng.standard_normal((M, K)).astype(np.float32)
+        y, ad = o.stq1_mm(x, blocks, M, N, K)
+        # weight w = 64 t + 16 p + j of a block is lane p: sum lanes 1..3
+        x64 = x.astype(np.float64).reshape(M, K // SQW, 4, 4, 16)[:, :, :, 1:, :].sum(axis=(2, 3, 4))
+        dv = np.array([[_fp16(d) for d in row] for row in dbits])
+        want = (1 - 2 * sgn) * x64 @ dv.T
+        _check_close(y, want, ad, what=f"stq1 closed form, signs {sgn}")
+    blocks = rng.integers(0, 256, size=(N, K // SQW, SQB), dtype=np.uint8)
+    blocks[:, :, 40:] = np.frombuffer(np.array(rng.uniform(0.002, 0.02, N * (K // SQW)), dtype=np.float16)
+                                      .tobytes(), dtype=np.uint8).reshape(N, K // SQW, 2)
+    W = o.stq1_dequant(blocks, N, K)
+    eye = np.eye(K, dtype=np.float32)[::37]
+    y, _ = o.stq1_mm(eye, blocks, eye.shape[0], N, K)
+    assert np.array_equal(y, W[:, ::37].T), "unit activations must read back columns of W"
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    y, ad = o.stq1_mm(x, blocks, M, N, K)
+    _check_close(y, x.astype(np.float64) @ W.T, ad, what="stq1 random vs dequant")
+    _check_close(ad, np.abs(x.astype(np.float64)) @ np.abs(W).T, ad, what="stq1 absdot")
+    ys, _ = o.stq1_mm(x, blocks, M, N, K, cols=np.array([2, 0]))
+    assert np.array_equal(ys, y[:, [2, 0]])
+
+
+def pin_stq1_mm_id(o):
+    """Routed STQ1_0: token t equals the plain product on expert ids[t]; a bad
+    id gives a zero row; get_rows returns the dequantized rows (zeros for a bad id)."""
+    rng = _rng(32)
+    E, N, K, T = 3, 4, 256, 6
+    blocks = rng.integers(0, 256, size=(E, N, K // SQW, SQB), dtype=np.uint8)
+    blocks[..., 41] &= 0x3F  # finite scales
+    x = rng.standard_normal((T, K)).astype(np.float32)
+    ids = np.array([2, 0, 5, 1, -1, 2], dtype=np.int32)
+    y, ad = o.stq1_mm_id(x, blocks, ids, T, N, K, E)
+    for t in range(T):
+        if 0 <= ids[t] < E:
+            ym, am = o.stq1_mm(x[t:t + 1], blocks[ids[t]], 1, N, K)
+            assert np.array_equal(ym[0], y[t]) and np.array_equal(am[0], ad[t]), f"token {t}"
+        else:
+            assert np.all(y[t] == 0) and np.all(ad[t] == 0), "out-of-range id must give a zero row"
+    rows = o.stq1_get_rows(blocks[1], np.array([3, 0, 9, 3]), N, K)
+    W = o.stq1_dequant(blocks[1], N, K)
+    assert np.array_equal(rows[0], W[3].astype(np.float32)) and np.array_equal(rows[1], W[0].astype(np.float32))
+    assert np.all(rows[2] == 0) and np.array_equal(rows[3], rows[0])
+
+
 PINS = [pin_packing_golden, pin_unpack_exhaustive, pin_dequant_endpoints, pin_dequant_random,
         pin_ulp, pin_bf16_special, pin_mm_zero_codes, pin_mm_all15, pin_mm_identity, pin_mm_ramp,
         pin_mm_sampled_columns, pin_mm_id, pin_mm_bruteforce, pin_bf16_decode_all,
-        pin_bf16_from_f64_exact, pin_bf16_from_f32_sweep, pin_embed, pin_group128]
+        pin_bf16_from_f64_exact, pin_bf16_from_f32_sweep, pin_embed, pin_group128,
+        pin_stq1_codebook, pin_stq1_layout, pin_stq1_mm, pin_stq1_mm_id]

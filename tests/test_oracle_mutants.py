@@ -32,6 +32,24 @@ MUTANTS = {
     "dequant_scale_group": ("bf16_decode(S[n * groups + k / G]) +", "bf16_decode(S[n * groups]) +"),
     "group_size_fixed_at_64": ("const int64_t words_per_group = G / 8;", "const int64_t words_per_group = 8;"),
     "dequant_bias_group_halved": ("bf16_decode(B[n * groups + k / G]);", "bf16_decode(B[n * groups + k / G / 2]);"),
+    # STQ1_0
+    "stq1_zero_lane_from_low_bits": ("const int zero_lane = c >> 2;", "const int zero_lane = c & 3;"),
+    "stq1_flip_bits_swapped": ("const int flip = rank == 0 ? (c & 1) : rank == 1 ? ((c >> 1) & 1) : 0;",
+                               "const int flip = rank == 0 ? ((c >> 1) & 1) : rank == 1 ? (c & 1) : 0;"),
+    "stq1_flip_reaches_last_lane": ("const int flip = rank == 0 ? (c & 1) : rank == 1 ? ((c >> 1) & 1) : 0;",
+                                    "const int flip = rank == 2 ? (c & 1) : rank == 1 ? ((c >> 1) & 1) : 0;"),
+    "stq1_group_sign_ignored": ("  if (s)\n    for (int l = 0; l < 4; ++l) v[l] = -v[l];", "  (void)s;"),
+    "stq1_element_offset_map": ("const int g = (w / 64) * 16 + w % 16;\n  const int p = (w % 64) / 16;",
+                                "const int g = w / 4;\n  const int p = w % 4;"),
+    "stq1_lane_group_transposed": ("const int g = (w / 64) * 16 + w % 16;\n  const int p = (w % 64) / 16;",
+                                   "const int g = (w / 64) * 16 + (w % 64) / 4;\n  const int p = w % 4;"),
+    "stq1_high_nibble_first": ("(block[g / 2] >> (4 * (g % 2)))", "(block[g / 2] >> (4 - 4 * (g % 2)))"),
+    "stq1_sign_bit_msb_first": ("(block[32 + g / 8] >> (g % 8))", "(block[32 + g / 8] >> (7 - g % 8))"),
+    "stq1_scale_big_endian": ("(uint16_t)(block[40] | (block[41] << 8))", "(uint16_t)(block[41] | (block[40] << 8))"),
+    "stq1_fp16_exponent_bias": ("efield - 15 - 10", "efield - 15 - 9"),
+    "stq1_blocks_reversed": ("blocks + (n * nb + b) * kStqBytes", "blocks + (n * nb + (nb - 1 - b)) * kStqBytes"),
+    "stq1_x_block_offset_dropped": ("xrow[b * kStqWeights + w]", "xrow[w]"),
+    "stq1_wrong_expert": ("blocks + e * per_expert", "blocks + (E - 1 - e) * per_expert"),
 }
 
 

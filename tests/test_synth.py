@@ -65,3 +65,20 @@ def test_experts_are_distinct_draws():
     w = synth.make_weights(0, 64, 128, E=3)
     assert w.Wq.shape == (3, 64, 16) and w.scales.shape == (3, 64, 2)
     assert not np.array_equal(w.Wq[0], w.Wq[1])
+
+
+def test_stq1_blocks_and_f32_activations():
+    b = synth.make_stq1(3, 64, 2048)
+    assert b.shape == (64, 8, 42) and np.array_equal(b, synth.make_stq1(3, 64, 2048))
+    assert np.array_equal(synth.make_stq1(3, 64, 2048, E=2)[0], b)
+    d = b[:, :, 40:].copy().view(np.float16).astype(np.float64)
+    assert np.all(np.isfinite(d)) and d.min() >= 0.00199 and d.max() <= 0.0201
+    codes = np.concatenate([b[:, :, :32] & 0xF, b[:, :, :32] >> 4]).ravel()
+    assert np.all(np.abs(np.bincount(codes, minlength=16) / codes.size - 1 / 16) < 0.01)
+    signs = np.unpackbits(b[:, :, 32:40])
+    assert abs(signs.mean() - 0.5) < 0.01
+    x = synth.make_x_f32(0, 3, 512)
+    bits = (x.view(np.uint32).astype(np.uint64) + 0x7FFF + ((x.view(np.uint32) >> 16) & 1)) >> 16
+    assert np.array_equal(bits.astype(np.uint16), synth.make_x(0, 3, 512)), "bf16 x is the rounded f32 x"
+    for v in (1.0, 0.002, 0.02, 1e-5, 65504.0, -3.25):
+        assert synth.fp16_bits(v) == int(np.array([v], np.float32).astype(np.float16).view(np.uint16)[0])
