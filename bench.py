@@ -55,7 +55,8 @@ LAUNCHES = [("qkv", ("q", "k", "v")), ("o", ("o",)), ("gate_up", ("gate", "up"))
 CASES = {"q": (2048, 2560, 1), "kv": (512, 2560, 1), "o": (2560, 2048, 1), "gate": (10240, 2560, 1),
          "down": (2560, 10240, 1), "wide_up": (12288, 1536, 1), "wide_down": (1536, 12288, 1),
          "lm_head_1536": (262144, 1536, 1), "lm_head_2560": (262144, 2560, 1), "dense_16384": (16384, 16384, 1),
-         "routed": (6144, 2048, 8)}
+         "routed": (6144, 2048, 8),
+         "stq1_16384": (16384, 16384, 1), "stq1_expert": (6144, 2048, 1), "stq1_routed": (6144, 2048, 8)}
 FALLBACK_HBM_GBS = 6800.0
 DOMINANT_KERNEL = "tc_tile_kernel"  # runs every projection of the decode-layer step
 NOMINAL_HBM_GBS = 8000.0
@@ -183,13 +184,16 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# The translation unit of the dominant kernel and the headers it includes.
+DOMINANT_SOURCES = ("common.cuh", "launch.h", "route.cuh", "tc.cu")
+
+
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "skinny_gemm_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in DOMINANT_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -590,6 +594,8 @@ def measure_extras(torch, ops, synth, roofline, l2, kernel, peak):
     nb, touched = roofline.mm_id_bytes(ids_np, T, N, K, E)
     out["routed"] = {"experts_touched": touched, "bytes": nb, "us": round(1e3 * ms, 2),
                      "GBps": round(nb / (ms * 1e-3) / 1e9, 1), "frac": round(nb / (ms * 1e-3) / 1e9 / peak, 4)}
+    del ws
+    out["stq1"] = measure_stq1(torch, ops, synth, roofline, l2, peak)
     return out
 
 
@@ -665,6 +671,9 @@ def run_case(args):
     N, K, E = CASES[args.case]
     M = args.M
     l2 = int(getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 126 * 2**20))
+    if args.case.startswith("stq1"):
+        run_stq1_case(args, torch, ops, roofline, synth, N, K, E, M, l2)
+        return
     hw = synth.make_weights(11, N, K, E)
     base = ops.W4Matrix.from_host(hw)
     copies = max(1, math.ceil(3 * l2 / base.nbytes))
@@ -693,6 +702,72 @@ def run_case(args):
     us = 1e3 * a.elapsed_time(b) / args.steps
     print(json.dumps({"case": args.case, "M": M, "N": N, "K": K, "E": E, "us_per_call": round(us, 3),
                       "GBps": round(nbytes / (us * 1e-6) / 1e9, 1), "plan": ops.get_plan(N, K, args.kernel)}))
+
+
+def stq1_cold_set(torch, ops, synth, N, K, E, l2, seed):
+    base = ops.STQ1Matrix.from_host(synth.make_stq1(seed, N, K, E), N, K, E)
+    copies = max(1, math.ceil(3 * l2 / base.packed.numel()))
+    return [base] + [ops.STQ1Matrix(base.packed.clone(), N, K, E) for _ in range(copies - 1)]
+
+
+def run_stq1_case(args, torch, ops, roofline, synth, N, K, E, M, l2):
+    """An STQ1_0 workload alone: eager launches round-robin over cold copies."""
+    ws = stq1_cold_set(torch, ops, synth, N, K, E, l2, 12)
+    copies = len(ws)
+    x = torch.randn(M, K, device="cuda")
+    y = torch.empty(M, N, device="cuda")
+    if E > 1:
+        ids_np = synth.make_ids(0, M, E)
+        ids = torch.from_numpy(ids_np).cuda()
+        call = lambda w: ops.stq1_mm_id(x, w, ids, out=y)  # noqa: E731
+        nbytes = roofline.stq1_mm_id_bytes(ids_np, M, N, K, E)[0]
+    else:
+        call = lambda w: ops.stq1_mm(x, w, out=y)  # noqa: E731
+        nbytes = roofline.stq1_mm_bytes(M, N, K)
+    for i in range(args.warmup):
+        call(ws[i % copies])
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(20_000_000)
+    a.record()
+    for i in range(args.steps):
+        call(ws[i % copies])
+    b.record()
+    torch.cuda.synchronize()
+    us = 1e3 * a.elapsed_time(b) / args.steps
+    print(json.dumps({"case": args.case, "M": M, "N": N, "K": K, "E": E, "us_per_call": round(us, 3),
+                      "GBps": round(nbytes / (us * 1e-6) / 1e9, 1), "plan": ops.stq1_get_plan(N, K)}))
+
+
+def measure_stq1(torch, ops, synth, roofline, l2, peak):
+    """STQ1_0 ternary workloads of the Hy4 page: the 16384^2 matvec of its
+    bandwidth table, the 6144x2048 expert at batch 1..8, eight routed experts."""
+    out = {}
+
+    def timed(ws, M, N, K, reps):
+        x = torch.randn(M, K, device="cuda")
+        y = torch.empty(M, N, device="cuda")
+        ms = time_graph_launches(torch, [lambda w=w: ops.stq1_mm(x, w, out=y) for w in ws], reps)
+        g = roofline.stq1_mm_bytes(M, N, K) / (ms * 1e-3) / 1e9
+        return {"us": round(1e3 * ms, 2), "GBps": round(g, 1), "frac": round(g / peak, 4)}
+
+    for (N, K, Ms) in [(16384, 16384, (1, 2)), (6144, 2048, (1, 2, 4, 5, 8))]:
+        ws = stq1_cold_set(torch, ops, synth, N, K, 1, l2, 10)
+        for M in Ms:
+            out[f"{N}x{K}_M{M}"] = timed(ws, M, N, K, 10)
+        del ws
+    E, N, K, T = 8, 6144, 2048, 8
+    ws = stq1_cold_set(torch, ops, synth, N, K, E, l2, 0)
+    ids_np = synth.make_ids(0, T, E)
+    ids = torch.from_numpy(ids_np).cuda()
+    x = torch.randn(T, K, device="cuda")
+    y = torch.empty(T, N, device="cuda")
+    ms = time_graph_launches(torch, [lambda w=w: ops.stq1_mm_id(x, w, ids, out=y) for w in ws], 20)
+    nb, touched = roofline.stq1_mm_id_bytes(ids_np, T, N, K, E)
+    out["routed_8x6144x2048_T8"] = {"experts_touched": touched, "us": round(1e3 * ms, 2),
+                                    "GBps": round(nb / (ms * 1e-3) / 1e9, 1),
+                                    "frac": round(nb / (ms * 1e-3) / 1e9 / peak, 4)}
+    return out
 
 
 def main():

@@ -14,6 +14,8 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "stq1.cuh"
+#include "stq1.h"
 
 namespace w4a16 {
 namespace {
@@ -389,6 +391,87 @@ int w4a16_device_status(void* stream, int* flags) {
     return fail(W4A16_ERR_DEVICE, "a kernel reported bad input (flags 0x%x)", v);
   }
   return W4A16_OK;
+}
+
+// ---- STQ1_0 (include/stq1.h) ----------------------------------------------------
+
+size_t stq1_packed_bytes(int N, int K) { return stq1_packed_size(N, K); }
+
+int stq1_get_plan(int N, int K, stq1_plan* out) {
+  if (!out) return fail(W4A16_ERR_NULL, "null plan pointer");
+  if (!stq1_shape_ok(N, K))
+    return fail(W4A16_ERR_SHAPE, "N = %d must be >= 1 and K = %d a multiple of 256 in 256..%d", N, K, STQ1_MAX_K);
+  Stq1Plan p;
+  stq1_make_plan(N, K, &p);
+  out->ksplit = p.ks;
+  out->blocks_per_slice = p.bps;
+  out->rows_per_pass = p.xcap;
+  return W4A16_OK;
+}
+
+int stq1_pack(const uint8_t* blocks, uint8_t* packed, int N, int K, void* stream) {
+  if (!stq1_shape_ok(N, K))
+    return fail(W4A16_ERR_SHAPE, "N = %d must be >= 1 and K = %d a multiple of 256 in 256..%d", N, K, STQ1_MAX_K);
+  if (!blocks || !packed) return fail(W4A16_ERR_NULL, "null tensor pointer");
+  if (misaligned(blocks, 2) || misaligned(packed, 16))
+    return fail(W4A16_ERR_ALIGN, "blocks must be 2-byte and packed 16-byte aligned");
+  cudaError_t e = launch_stq1_pack(blocks, packed, N, K, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? W4A16_OK : cuda_fail(e, "stq1_pack launch");
+}
+
+int stq1_mm(const float* x, const uint8_t* packed, float* y, int M, int N, int K, void* stream) {
+  if (env().fault == kFaultValidate) return fail(W4A16_ERR_SHAPE, "injected validation fault (W4A16_FAULT)");
+  if (M < 0 || M > kMaxDim) return fail(W4A16_ERR_SHAPE, "M = %d must be in 0..2^30", M);
+  if (!stq1_shape_ok(N, K) || N > kMaxDim)
+    return fail(W4A16_ERR_SHAPE, "N = %d must be in 1..2^30 and K = %d a multiple of 256 in 256..%d", N, K,
+                STQ1_MAX_K);
+  if (M == 0) return W4A16_OK;
+  if (!x || !packed || !y) return fail(W4A16_ERR_NULL, "null tensor pointer");
+  if (misaligned(x, 16) || misaligned(packed, 16) || misaligned(y, 4))
+    return fail(W4A16_ERR_ALIGN, "x and packed must be 16-byte and y 4-byte aligned");
+  if (env().fault == kFaultLaunch) return fail(W4A16_ERR_CUDA, "injected launch fault (W4A16_FAULT)");
+  Stq1Plan pl;
+  stq1_make_plan(N, K, &pl);
+  for (int row0 = 0; row0 < M; row0 += pl.xcap) {
+    const int rows = M - row0 < pl.xcap ? M - row0 : pl.xcap;
+    cudaError_t e = launch_stq1_mm(x, packed, y, rows, row0, N, K, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "stq1_mm launch");
+  }
+  return W4A16_OK;
+}
+
+int stq1_mm_id(const float* x, const uint8_t* packed, const int32_t* ids, float* y, int T, int N, int K, int E,
+               void* stream) {
+  if (env().fault == kFaultValidate) return fail(W4A16_ERR_SHAPE, "injected validation fault (W4A16_FAULT)");
+  if (T < 0 || T > kMaxDim) return fail(W4A16_ERR_EXPERTS, "T = %d must be in 0..2^30", T);
+  if (E <= 0 || E > 65535) return fail(W4A16_ERR_EXPERTS, "E = %d must be in 1..65535", E);
+  if (!stq1_shape_ok(N, K) || N > kMaxDim)
+    return fail(W4A16_ERR_SHAPE, "N = %d must be in 1..2^30 and K = %d a multiple of 256 in 256..%d", N, K,
+                STQ1_MAX_K);
+  if (T == 0) return W4A16_OK;
+  if (!x || !packed || !ids || !y) return fail(W4A16_ERR_NULL, "null tensor pointer");
+  if (misaligned(x, 16) || misaligned(packed, 16) || misaligned(y, 4) || misaligned(ids, 4))
+    return fail(W4A16_ERR_ALIGN, "x and packed must be 16-byte, y and ids 4-byte aligned");
+  if (env().fault == kFaultLaunch) return fail(W4A16_ERR_CUDA, "injected launch fault (W4A16_FAULT)");
+  int* flags = nullptr;
+  if (int rc = flag_pointer(&flags)) return rc;
+  cudaError_t e = launch_stq1_mm_id(x, packed, ids, y, T, N, K, E, flags, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? W4A16_OK : cuda_fail(e, "stq1_mm_id launch");
+}
+
+int stq1_get_rows(const uint8_t* packed, const int32_t* ids, float* out, int T, int N, int K, void* stream) {
+  if (T < 0 || T > kMaxDim) return fail(W4A16_ERR_SHAPE, "T = %d must be in 0..2^30", T);
+  if (!stq1_shape_ok(N, K) || N > kMaxDim)
+    return fail(W4A16_ERR_SHAPE, "N = %d must be in 1..2^30 and K = %d a multiple of 256 in 256..%d", N, K,
+                STQ1_MAX_K);
+  if (T == 0) return W4A16_OK;
+  if (!packed || !ids || !out) return fail(W4A16_ERR_NULL, "null tensor pointer");
+  if (misaligned(packed, 16) || misaligned(ids, 4) || misaligned(out, 4))
+    return fail(W4A16_ERR_ALIGN, "packed must be 16-byte, ids and out 4-byte aligned");
+  int* flags = nullptr;
+  if (int rc = flag_pointer(&flags)) return rc;
+  cudaError_t e = launch_stq1_get_rows(packed, ids, out, T, N, K, flags, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? W4A16_OK : cuda_fail(e, "stq1_get_rows launch");
 }
 
 const char* w4a16_last_error(void) { return g_last_error.c_str(); }

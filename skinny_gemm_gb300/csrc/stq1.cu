@@ -1,0 +1,574 @@
+// stq1.cu -- the STQ1_0 ternary matmul on the tensor cores (sm_103a).
+//
+// "Hy4-preview Metal kernels for llama.cpp" gives the format (section "Notes
+// and gotchas": 42-byte blocks of 256 weights, 4-bit group codes, group sign
+// bits, an fp16 scale, and the weight-to-group map), the kernels a model
+// needs (the kernel table: matvec, small batches, routed experts, row
+// gather) and the structure of a group (section "Results", the fourth decode
+// pass: one zero lane named by the code's high bits, two sign flips in its
+// low bits, the sign bit negating the group).  The Metal schedule itself is
+// not the design here:
+//
+//  * Weights keep the page's 42 bytes per 256, repacked once (stq1_pack) into
+//    672-byte records per 16-row tile and block, so each lane loads its codes,
+//    sign bits and scales with one 16-, one 4- and one 4-byte load.
+//  * The contraction runs on the tensor cores (mma.sync m16n8k16, bf16 in,
+//    fp32 accumulate).  Ternary lanes are exact in bf16; x enters as three
+//    bf16 parts h0 + h1 + h2 = x (exact: each part takes the next 8 bits of
+//    the 24-bit significand), as three columns of B, so the products are
+//    exact and only the fp32 accumulation rounds.  Within a block the MMA k
+//    order is chosen so that each lane's A fragment holds whole groups: k
+//    position 2t+i of chunk j is lane i of group 16t + j, position 2t+8+i is
+//    lane 2+i; lane t of a quad then owns groups 16t .. 16t+15, eight
+//    contiguous code bytes and sixteen contiguous sign bits of the page's
+//    own block.  B follows the same order (the activations are staged in it).
+//  * A group decodes through a 32-entry table in shared memory (code and
+//    sign bit -> the bf16 pairs of lanes 0,1 and 2,3), one 8-byte slot per
+//    warp lane so that lookups never conflict.  The page found a table
+//    lookup faster than arithmetic decoding on its GPU; here it also keeps
+//    the decode at a few instructions per group: the table offsets of 16
+//    groups come from four word-wide mask/multiply steps and one byte
+//    permute per group.
+//  * Each CTA stages the activation parts once; its 8 warps take K slices of
+//    one to eight 16-row tiles per round, add their fp32 partials in shared
+//    memory in slice order, and write y.  The slice count and every order
+//    depend on (N, K) only, so any row of a multi-row call equals the
+//    one-row call bit for bit.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdint>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "common.cuh"
+#include "stq1.cuh"
+#include "w4a16.h"
+
+namespace w4a16 {
+namespace {
+
+constexpr int kBlockW = 256;     // weights per block
+constexpr int kBlockBytes = 42;  // bytes per block in the page's layout
+constexpr int kRec = 672;        // bytes per (16-row tile, block) record
+constexpr int kSignOff = 512;
+constexpr int kScaleOff = 640;
+constexpr int kWarps = 8;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kDepth = 4;                 // records in flight per warp
+constexpr int kLutBytes = 32 * 32 * 8;    // [label][lane] uint2
+constexpr int kMaxRows = 8;               // activation rows per pass
+constexpr int kTokBytes = 64;             // int tok[8], count, next token
+constexpr int kSmemCap = 227 * 1024;
+constexpr int kTargetWarps = 2432;        // 152 SMs x 16 warps
+constexpr int kGroupStride = 4096;        // staged bytes per block and 8 columns
+
+__host__ __device__ constexpr int red_bytes(int mc) { return kWarps * 16 * 8 * mc * 4; }
+__host__ __device__ constexpr int fixed_smem(int mc) { return kLutBytes + red_bytes(mc) + kTokBytes; }
+
+struct Params {
+  const float* x;
+  const uint8_t* w;
+  float* y;
+  const int32_t* ids;
+  int* flags;
+  int M, row0;  // plain calls: rows row0 .. row0 + M - 1
+  int N, K, nb, tiles;
+  int ks, bps, rt, rounds;
+  int xcap;
+  long long wstride;  // bytes per expert
+  int T, E;
+};
+
+__device__ __forceinline__ uint32_t ld_nc_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+// bf16 bits of lane l of a group with code c and sign bit s.
+__device__ uint32_t lane_bf16(int c, int s, int l) {
+  const int zero = c >> 2;
+  if (l == zero) return 0u;
+  const int rank = l - (l > zero ? 1 : 0);  // place among the three other lanes
+  const int flip = rank == 0 ? (c & 1) : rank == 1 ? ((c >> 1) & 1) : 0;
+  return (flip ^ s) ? 0xBF80u : 0x3F80u;
+}
+
+__device__ void fill_lut(uint2* lut) {
+  for (int i = threadIdx.x; i < 32 * 32; i += blockDim.x) {
+    const int label = i >> 5, c = label & 15, s = label >> 4;
+    lut[i] = make_uint2(lane_bf16(c, s, 0) | (lane_bf16(c, s, 1) << 16),
+                        lane_bf16(c, s, 2) | (lane_bf16(c, s, 3) << 16));
+  }
+}
+
+// Activation rows tok[0 .. mrows) of x as bf16 parts in MMA fragment order:
+// column c = 3m + q (part q of row m) is column c % 8 of MMA group c / 8;
+// within a group the bytes of (block b, chunk j, column n, quad lane t) are
+// at ((b*16 + j) * ncols_in_group + n) * 32 + t * 8, holding lanes 0..3 of
+// group 16t + j as the two B registers.
+__device__ void stage_rows(uint8_t* bsm, const float* x, const int* tok, int mrows, int K, int nb) {
+  const int ncols = 3 * mrows;
+  for (int m = 0; m < mrows; ++m) {
+    const float* row = x + (long long)tok[m] * K;
+    for (int k = threadIdx.x; k < K; k += blockDim.x) {
+      const float v = row[k];
+      const __nv_bfloat16 h0 = __float2bfloat16_rn(v);
+      const float r1 = __fsub_rn(v, __bfloat162float(h0));
+      const __nv_bfloat16 h1 = __float2bfloat16_rn(r1);
+      const float r2 = __fsub_rn(r1, __bfloat162float(h1));
+      const __nv_bfloat16 h2 = __float2bfloat16_rn(r2);
+      const int b = k >> 8, w = k & 255, t = w >> 6, p = (w >> 4) & 3, j = w & 15;
+      const int within = t * 8 + (p >> 1) * 4 + (p & 1) * 2;
+#pragma unroll
+      for (int q = 0; q < 3; ++q) {
+        const int c = 3 * m + q, g = c >> 3, n = c & 7;
+        const int ncg = min(8, ncols - 8 * g);
+        const int off = g * nb * kGroupStride + ((b * 16 + j) * ncg + n) * 32 + within;
+        *reinterpret_cast<__nv_bfloat16*>(bsm + off) = q == 0 ? h0 : q == 1 ? h1 : h2;
+      }
+    }
+  }
+}
+
+struct Rec {
+  uint4 c;     // codes: rows r (x, y) and r + 8 (z, w), 16 groups each
+  uint32_t s;  // sign bits: row r (low half), row r + 8 (high half)
+  uint32_t d;  // fp16 scales: row r (low), row r + 8 (high)
+};
+
+// Table offsets (label * 256, label = code | sign << 4, one byte each) of the
+// 16 groups of one row: L[0] groups 0,2,4,6; L[1] 1,3,5,7; L[2] 8,..,14;
+// L[3] 9,..,15.  The multiply moves sign bits 0, 2, 4, 6 to bits 4, 12, 20,
+// 28 (its other partial products land elsewhere and are masked off).
+__device__ __forceinline__ void labels(uint32_t lo, uint32_t hi, uint32_t sg, uint32_t L[4]) {
+  constexpr uint32_t kSpread = 0x00410410u;
+  L[0] = (lo & 0x0F0F0F0Fu) | (((sg & 0x55u) * kSpread) & 0x10101010u);
+  L[1] = ((lo >> 4) & 0x0F0F0F0Fu) | ((((sg >> 1) & 0x55u) * kSpread) & 0x10101010u);
+  L[2] = (hi & 0x0F0F0F0Fu) | ((((sg >> 8) & 0x55u) * kSpread) & 0x10101010u);
+  L[3] = ((hi >> 4) & 0x0F0F0F0Fu) | ((((sg >> 9) & 0x55u) * kSpread) & 0x10101010u);
+}
+
+__device__ __forceinline__ void mma_bf16(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// One record: 16 chunks of 16 k, MC MMAs each (column groups past ncols are
+// skipped), then pa += d * block sum per row.
+template <int MC>
+__device__ __forceinline__ void process(const Rec& r, int b, const uint8_t* lut, uint32_t lane8,
+                                        const uint8_t* bsm, int nb, int ncols, int lane, float pa[MC][4]) {
+  uint32_t La[4], Lb[4];
+  labels(r.c.x, r.c.y, r.s & 0xFFFFu, La);
+  labels(r.c.z, r.c.w, r.s >> 16, Lb);
+  float acc[MC][4];
+#pragma unroll
+  for (int g = 0; g < MC; ++g) acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0.f;
+  const int n = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int wi = (j & 1) + 2 * (j >> 3);
+    const uint32_t sel = 0x5504u | ((uint32_t)((j >> 1) & 3) << 4);  // [0, 0, label, lane8]
+    const uint2 ea = *reinterpret_cast<const uint2*>(lut + __byte_perm(La[wi], lane8, sel));
+    const uint2 eb = *reinterpret_cast<const uint2*>(lut + __byte_perm(Lb[wi], lane8, sel));
+#pragma unroll
+    for (int g = 0; g < MC; ++g) {
+      if (8 * g < ncols) {
+        const int ncg = min(8, ncols - 8 * g);
+        uint2 bf = make_uint2(0u, 0u);
+        if (n < ncg)
+          bf = *reinterpret_cast<const uint2*>(bsm + g * nb * kGroupStride + ((b * 16 + j) * ncg + n) * 32 + t * 8);
+        mma_bf16(acc[g], ea.x, eb.x, ea.y, eb.y, bf.x, bf.y);
+      }
+    }
+  }
+  const float dr = __half2float(__ushort_as_half((unsigned short)(r.d & 0xFFFFu)));
+  const float dr8 = __half2float(__ushort_as_half((unsigned short)(r.d >> 16)));
+#pragma unroll
+  for (int g = 0; g < MC; ++g) {
+    pa[g][0] = __fmaf_rn(dr, acc[g][0], pa[g][0]);
+    pa[g][1] = __fmaf_rn(dr, acc[g][1], pa[g][1]);
+    pa[g][2] = __fmaf_rn(dr8, acc[g][2], pa[g][2]);
+    pa[g][3] = __fmaf_rn(dr8, acc[g][3], pa[g][3]);
+  }
+}
+
+// End of a round: the warps' partials through shared memory, summed over the
+// K slices in slice order, then the three parts (h0 + h1) + h2, into y.
+template <int MC>
+__device__ void finish_round(const Params& p, float* red, const int* tok, int mrows, int round, int warp, int lane,
+                             float pa[MC][4]) {
+  constexpr int stride = 8 * MC;
+  const int r = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int g = 0; g < MC; ++g) {
+    *reinterpret_cast<float2*>(red + (warp * 16 + r) * stride + 8 * g + 2 * t) = make_float2(pa[g][0], pa[g][1]);
+    *reinterpret_cast<float2*>(red + (warp * 16 + r + 8) * stride + 8 * g + 2 * t) = make_float2(pa[g][2], pa[g][3]);
+  }
+  __syncthreads();
+  const int outs = p.rt * mrows * 16;
+  for (int o = threadIdx.x; o < outs; o += kThreads) {
+    const int rr = o & 15, mo = o >> 4;
+    const int lt = mo / mrows, m = mo - lt * mrows;
+    const int tile = round * p.rt + lt;
+    const int n = tile * 16 + rr;
+    if (tile < p.tiles && n < p.N) {
+      float part[3];
+#pragma unroll
+      for (int q = 0; q < 3; ++q) {
+        const int col = 3 * m + q;
+        float s = red[(lt * p.ks * 16 + rr) * stride + col];
+        for (int sl = 1; sl < p.ks; ++sl) s = __fadd_rn(s, red[((lt * p.ks + sl) * 16 + rr) * stride + col]);
+        part[q] = s;
+      }
+      p.y[(long long)tok[m] * p.N + n] = __fadd_rn(__fadd_rn(part[0], part[1]), part[2]);
+    }
+  }
+  __syncthreads();
+}
+
+// The record of item `it` of this warp: round `it / bps` of this CTA, block
+// `slice * bps + it % bps` of the warp's tile; zeros past the matrix.
+__device__ __forceinline__ void fetch(const Params& p, const uint8_t* wbase, int it, int n_items, int lt, int slice,
+                                      int lane, Rec& r) {
+  r.c = make_uint4(0u, 0u, 0u, 0u);
+  r.s = 0u;
+  r.d = 0u;
+  if (it >= n_items) return;
+  const int rl = it / p.bps, i = it - rl * p.bps;
+  const int tile = (blockIdx.x + rl * gridDim.x) * p.rt + lt;
+  const int b = slice * p.bps + i;
+  if (tile >= p.tiles || b >= p.nb) return;
+  const uint8_t* rec = wbase + ((long long)tile * p.nb + b) * kRec;
+  r.c = ld_stream_v4(rec + 16 * lane);
+  r.s = ld_nc_u32(rec + kSignOff + 4 * lane);
+  r.d = ld_nc_u32(rec + kScaleOff + 4 * (lane >> 2));
+}
+
+template <int MC>
+__device__ void run_rows(const Params& p, const uint8_t* wbase, const uint8_t* lut, float* red, const int* tok,
+                         const uint8_t* bsm, int mrows, int n_items, int warp, int lane, int lt, int slice) {
+  const int ncols = 3 * mrows;
+  const uint32_t lane8 = (uint32_t)lane * 8u;
+  Rec ring[kDepth];
+#pragma unroll
+  for (int s = 0; s < kDepth; ++s) fetch(p, wbase, s, n_items, lt, slice, lane, ring[s]);
+  float pa[MC][4];
+#pragma unroll
+  for (int g = 0; g < MC; ++g) pa[g][0] = pa[g][1] = pa[g][2] = pa[g][3] = 0.f;
+  for (int base = 0; base < n_items; base += kDepth) {
+#pragma unroll
+    for (int s = 0; s < kDepth; ++s) {
+      const int it = base + s;
+      if (it < n_items) {  // the same for every warp of the CTA
+        const Rec cur = ring[s];
+        fetch(p, wbase, it + kDepth, n_items, lt, slice, lane, ring[s]);
+        const int rl = it / p.bps, i = it - rl * p.bps;
+        const int round = blockIdx.x + rl * gridDim.x;
+        const int tile = round * p.rt + lt;
+        const int b = slice * p.bps + i;
+        if (tile < p.tiles && b < p.nb) process<MC>(cur, b, lut, lane8, bsm, p.nb, ncols, lane, pa);
+        if (i == p.bps - 1) {
+          finish_round<MC>(p, red, tok, mrows, round, warp, lane, pa);
+#pragma unroll
+          for (int g = 0; g < MC; ++g) pa[g][0] = pa[g][1] = pa[g][2] = pa[g][3] = 0.f;
+        }
+      }
+    }
+  }
+}
+
+template <int MC, bool ROUTED>
+__global__ void __launch_bounds__(kThreads, 2) stq1_mm_kernel(const Params p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint2* lut = reinterpret_cast<uint2*>(smem);
+  float* red = reinterpret_cast<float*>(smem + kLutBytes);
+  int* tok = reinterpret_cast<int*>(smem + kLutBytes + red_bytes(MC));
+  uint8_t* bsm = smem + fixed_smem(MC);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lt = warp / p.ks, slice = warp - lt * p.ks;
+  const uint8_t* wbase = p.w;
+  int e = 0;
+  if (ROUTED) {
+    e = blockIdx.y;
+    wbase += (long long)e * p.wstride;
+    if (blockIdx.x == 0 && blockIdx.y == 0) {
+      // tokens routed outside 0..E-1: zero rows and the device flag
+      for (int t = 0; t < p.T; ++t) {
+        const int id = __ldg(p.ids + t);
+        if (id < 0 || id >= p.E) {
+          if (threadIdx.x == 0) atomicOr(p.flags, W4A16_DEVICE_BAD_ID);
+          for (int n = threadIdx.x; n < p.N; n += blockDim.x) p.y[(long long)t * p.N + n] = 0.f;
+        }
+      }
+    }
+  }
+  fill_lut(lut);
+  const int my_rounds = (int)blockIdx.x < p.rounds ? (p.rounds - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int n_items = my_rounds * p.bps;
+  int next = 0;  // routed: first token not yet gathered
+  for (;;) {
+    int mrows;
+    if (ROUTED) {
+      __syncthreads();  // the previous pass is done with tok and the staged rows
+      if (warp == 0) {
+        int cnt = 0, t0 = next;
+        while (cnt < p.xcap && t0 < p.T) {
+          const int t = t0 + lane;
+          const bool hit = t < p.T && __ldg(p.ids + t) == e;
+          const unsigned mask = __ballot_sync(0xFFFFFFFFu, hit);
+          const int hits = __popc(mask);
+          const int take = min(hits, p.xcap - cnt);
+          const int pos = __popc(mask & ((1u << lane) - 1u));
+          if (hit && pos < take) tok[cnt + pos] = t;
+          cnt += take;
+          if (take < hits) {  // stop at the first hit not taken
+            unsigned rest = mask;
+            for (int q = 0; q < take; ++q) rest &= rest - 1u;
+            t0 += __ffs(rest) - 1;
+            break;
+          }
+          t0 += 32;
+        }
+        if (lane == 0) {
+          tok[kMaxRows] = cnt;
+          tok[kMaxRows + 1] = min(t0, p.T);
+        }
+      }
+      __syncthreads();
+      mrows = tok[kMaxRows];
+      next = tok[kMaxRows + 1];
+      if (mrows == 0) break;
+    } else {
+      if ((int)threadIdx.x < p.M) tok[threadIdx.x] = p.row0 + (int)threadIdx.x;
+      mrows = p.M;
+      __syncthreads();
+    }
+    stage_rows(bsm, p.x, tok, mrows, p.K, p.nb);
+    __syncthreads();
+    run_rows<MC>(p, wbase, reinterpret_cast<const uint8_t*>(lut), red, tok, bsm, mrows, n_items, warp, lane, lt,
+                 slice);
+    if (!ROUTED) break;
+  }
+}
+
+// ---- repack and row gather -----------------------------------------------------------
+
+__global__ void stq1_pack_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int N, int nb,
+                                 int tiles) {
+  const long long total = (long long)tiles * 16 * nb;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int b = (int)(i % nb);
+    const long long row = i / nb;
+    const int r = (int)(row & 15), half = r >> 3, l0 = (r & 7) * 4;
+    uint8_t* rec = dst + ((row >> 4) * nb + b) * kRec;
+    uint16_t h[21];
+    if (row < N) {
+      const uint16_t* s16 = reinterpret_cast<const uint16_t*>(src + (row * nb + b) * kBlockBytes);
+#pragma unroll
+      for (int q = 0; q < 21; ++q) h[q] = s16[q];
+    } else {
+#pragma unroll
+      for (int q = 0; q < 21; ++q) h[q] = 0;
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      uint16_t* cd = reinterpret_cast<uint16_t*>(rec + 16 * (l0 + t) + 8 * half);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) cd[q] = h[4 * t + q];                                       // qs bytes 8t..8t+7
+      *reinterpret_cast<uint16_t*>(rec + kSignOff + 4 * (l0 + t) + 2 * half) = h[16 + t];    // sign bytes 2t, 2t+1
+    }
+    *reinterpret_cast<uint16_t*>(rec + kScaleOff + 4 * (r & 7) + 2 * half) = h[20];          // d
+  }
+}
+
+// out[t][k] = W[ids[t]][k]; one thread per (token, block, group).
+__global__ void stq1_rows_kernel(const uint8_t* __restrict__ w, const int32_t* __restrict__ ids,
+                                 float* __restrict__ out, int T, int N, int K, int nb, int* flags) {
+  const long long total = (long long)T * nb * 64;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int gq = (int)(i & 63), tq = gq >> 4, j = gq & 15;
+    const long long rest = i >> 6;
+    const int b = (int)(rest % nb);
+    const long long t = rest / nb;
+    float* o = out + t * K + b * kBlockW + tq * 64 + j;
+    const int n = __ldg(ids + t);
+    if (n < 0 || n >= N) {
+      if (b == 0 && gq == 0) atomicOr(flags, W4A16_DEVICE_BAD_ID);
+      o[0] = o[16] = o[32] = o[48] = 0.f;
+      continue;
+    }
+    const int r = n & 15, half = r >> 3, l = (r & 7) * 4 + tq;
+    const uint8_t* rec = w + ((long long)(n >> 4) * nb + b) * kRec;
+    const int code = (rec[16 * l + 8 * half + (j >> 1)] >> (4 * (j & 1))) & 15;
+    const int s = (rec[kSignOff + 4 * l + 2 * half + (j >> 3)] >> (j & 7)) & 1;
+    const float d = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(
+        rec + kScaleOff + 4 * (r & 7) + 2 * half)));
+#pragma unroll
+    for (int q = 0; q < 4; ++q) o[16 * q] = d * __uint_as_float(lane_bf16(code, s, q) << 16);
+  }
+}
+
+// ---- host side -------------------------------------------------------------------------
+
+int sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  if (!cached[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = v > 0 ? v : 152;
+  }
+  return cached[dev];
+}
+
+template <int MC, bool ROUTED>
+cudaError_t launch_kernel(const Params& p, dim3 grid_cap, int smem, cudaStream_t s) {
+  auto fn = stq1_mm_kernel<MC, ROUTED>;
+  static std::mutex mu;
+  static std::map<std::pair<int, int>, int> occ;  // (device, smem) -> CTAs per SM
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = occ.find({dev, smem});
+    if (it == occ.end()) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemCap);
+      if (e != cudaSuccess) return e;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem);
+      if (e != cudaSuccess) return e;
+      if (per_sm < 1) per_sm = 1;
+      occ[{dev, smem}] = per_sm;
+    } else {
+      per_sm = it->second;
+    }
+  }
+  const int slots = per_sm * sm_count();
+  dim3 grid = grid_cap;
+  if (ROUTED) {
+    // CTAs per expert: the resident slots over the experts T tokens are
+    // expected to touch when drawn uniformly, E (1 - (1 - 1/E)^T).
+    double touched = (double)p.E;
+    double miss = 1.0;
+    for (int t = 0; t < p.T && t < 4096; ++t) miss *= 1.0 - 1.0 / p.E;
+    touched *= 1.0 - miss;
+    if (touched < 1.0) touched = 1.0;
+    int gx = (int)(slots / touched);
+    grid.x = (unsigned)(gx < 1 ? 1 : gx < p.rounds ? gx : p.rounds);
+  } else {
+    grid.x = (unsigned)(slots < p.rounds ? slots : p.rounds);
+  }
+  fn<<<grid, kThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+Params base_params(int N, int K) {
+  Stq1Plan pl;
+  stq1_make_plan(N, K, &pl);
+  Params p{};
+  p.N = N;
+  p.K = K;
+  p.nb = pl.nb;
+  p.tiles = pl.tiles;
+  p.ks = pl.ks;
+  p.bps = pl.bps;
+  p.rt = pl.rt;
+  p.rounds = pl.rounds;
+  p.xcap = pl.xcap;
+  p.wstride = (long long)stq1_packed_size(N, K);
+  return p;
+}
+
+int groups_for(int rows) { return (3 * rows + 7) / 8; }
+
+}  // namespace
+
+bool stq1_shape_ok(int N, int K) { return N >= 1 && K >= kBlockW && K <= 32768 && K % kBlockW == 0; }
+
+size_t stq1_packed_size(int N, int K) {
+  if (!stq1_shape_ok(N, K)) return 0;
+  return (size_t)((N + 15) / 16) * (size_t)(K / kBlockW) * kRec;
+}
+
+void stq1_make_plan(int N, int K, Stq1Plan* pl) {
+  pl->nb = K / kBlockW;
+  pl->tiles = (N + 15) / 16;
+  int ks = 1;
+  while (ks < kWarps && 2 * ks <= pl->nb && (long long)pl->tiles * ks < kTargetWarps) ks *= 2;
+  pl->ks = ks;
+  pl->bps = (pl->nb + ks - 1) / ks;
+  pl->rt = kWarps / ks;
+  pl->rounds = (pl->tiles + pl->rt - 1) / pl->rt;
+  const long long room = (long long)kSmemCap - fixed_smem(3);
+  long long rows = room / (6LL * K);
+  pl->xcap = (int)(rows < kMaxRows ? rows : kMaxRows);
+}
+
+cudaError_t launch_stq1_pack(const uint8_t* src, uint8_t* dst, int N, int K, cudaStream_t s) {
+  const int nb = K / kBlockW, tiles = (N + 15) / 16;
+  const long long total = (long long)tiles * 16 * nb;
+  long long blocks = (total + 255) / 256;
+  if (blocks > 65535) blocks = 65535;
+  stq1_pack_kernel<<<(unsigned)blocks, 256, 0, s>>>(src, dst, N, nb, tiles);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_stq1_mm(const float* x, const uint8_t* w, float* y, int M, int row0, int N, int K,
+                           cudaStream_t s) {
+  Params p = base_params(N, K);
+  if (M < 1 || M > p.xcap) return cudaErrorInvalidValue;
+  p.x = x;
+  p.w = w;
+  p.y = y;
+  p.M = M;
+  p.row0 = row0;
+  const int mc = groups_for(M);
+  const int smem = fixed_smem(mc) + 6 * M * K;
+  const dim3 grid(1, 1, 1);
+  if (mc == 1) return launch_kernel<1, false>(p, grid, smem, s);
+  if (mc == 2) return launch_kernel<2, false>(p, grid, smem, s);
+  return launch_kernel<3, false>(p, grid, smem, s);
+}
+
+cudaError_t launch_stq1_mm_id(const float* x, const uint8_t* w, const int32_t* ids, float* y, int T, int N,
+                              int K, int E, int* flags, cudaStream_t s) {
+  Params p = base_params(N, K);
+  p.x = x;
+  p.w = w;
+  p.y = y;
+  p.ids = ids;
+  p.flags = flags;
+  p.T = T;
+  p.E = E;
+  const int rows = p.xcap < T ? p.xcap : T;
+  p.xcap = rows;
+  const int mc = groups_for(rows);
+  const int smem = fixed_smem(mc) + 6 * rows * K;
+  const dim3 grid(1, (unsigned)E, 1);
+  if (mc == 1) return launch_kernel<1, true>(p, grid, smem, s);
+  if (mc == 2) return launch_kernel<2, true>(p, grid, smem, s);
+  return launch_kernel<3, true>(p, grid, smem, s);
+}
+
+cudaError_t launch_stq1_get_rows(const uint8_t* w, const int32_t* ids, float* out, int T, int N, int K,
+                                 int* flags, cudaStream_t s) {
+  const int nb = K / kBlockW;
+  const long long total = (long long)T * nb * 64;
+  long long blocks = (total + 255) / 256;
+  if (blocks > 65535) blocks = 65535;
+  stq1_rows_kernel<<<(unsigned)blocks, 256, 0, s>>>(w, ids, out, T, N, K, nb, flags);
+  return cudaGetLastError();
+}
+
+}  // namespace w4a16

@@ -5,7 +5,10 @@ device memory, the current CUDA stream and the output allocation; there is
 no CPU or PyTorch fallback, and a missing or unbuildable library raises.
 
 Names follow the C ABI in ``include/w4a16.h``: ``mm``, ``mm_group``,
-``mm_id``, ``unpack``, ``dequant``, ``get_plan``, ``device_status``.
+``mm_id``, ``unpack``, ``dequant``, ``get_plan``, ``device_status``; and in
+``include/stq1.h`` for the STQ1_0 ternary format: ``stq1_mm``,
+``stq1_mm_id``, ``stq1_get_rows``, ``stq1_get_plan`` over an ``STQ1Matrix``
+(repacked on the device by ``stq1_pack``).
 """
 from __future__ import annotations
 
@@ -26,8 +29,10 @@ DEVICE_BAD_ID = 1
 
 EXPORTS = ("w4a16_mm", "w4a16_mm_kernel", "w4a16_mm_group", "w4a16_mm_argmax", "w4a16_embed", "w4a16_expand_groups",
            "w4a16_mm_id", "w4a16_mm_id_kernel", "w4a16_unpack", "w4a16_dequant", "w4a16_get_plan", "w4a16_device_status", "w4a16_last_error",
-           "w4a16_debug_reload_env", "w4a16_version")
+           "w4a16_debug_reload_env", "w4a16_version",
+           "stq1_packed_bytes", "stq1_pack", "stq1_mm", "stq1_mm_id", "stq1_get_rows", "stq1_get_plan")
 MAX_GROUP = 8
+STQ1_BLOCK_WEIGHTS, STQ1_BLOCK_BYTES = 256, 42
 
 
 class W4A16Error(RuntimeError):
@@ -51,6 +56,10 @@ class Plan(ctypes.Structure):
         d = {f: getattr(self, f) for f, _ in self._fields_}
         d["kernel"] = KERNEL_NAMES.get(self.kernel, self.kernel)
         return d
+
+
+class Stq1Plan(ctypes.Structure):
+    _fields_ = [("ksplit", ctypes.c_int), ("blocks_per_slice", ctypes.c_int), ("rows_per_pass", ctypes.c_int)]
 
 
 class Item(ctypes.Structure):
@@ -88,9 +97,17 @@ def lib() -> ctypes.CDLL:
             L.w4a16_dequant.argtypes = [P, P, P, P, i, i, P]
             L.w4a16_get_plan.argtypes = [i, i, i, ctypes.POINTER(Plan)]
             L.w4a16_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
+            L.stq1_packed_bytes.argtypes = [i, i]
+            L.stq1_packed_bytes.restype = ctypes.c_size_t
+            L.stq1_pack.argtypes = [P, P, i, i, P]
+            L.stq1_mm.argtypes = [P, P, P, i, i, i, P]
+            L.stq1_mm_id.argtypes = [P, P, P, P, i, i, i, i, P]
+            L.stq1_get_rows.argtypes = [P, P, P, i, i, i, P]
+            L.stq1_get_plan.argtypes = [i, i, ctypes.POINTER(Stq1Plan)]
             for f in ("w4a16_mm", "w4a16_mm_kernel", "w4a16_mm_noalloc", "w4a16_mm_group", "w4a16_mm_argmax",
                       "w4a16_embed", "w4a16_expand_groups", "w4a16_mm_id", "w4a16_mm_id_kernel", "w4a16_unpack", "w4a16_dequant",
-                      "w4a16_get_plan", "w4a16_device_status"):
+                      "w4a16_get_plan", "w4a16_device_status", "stq1_pack", "stq1_mm", "stq1_mm_id", "stq1_get_rows",
+                      "stq1_get_plan"):
                 getattr(L, f).restype = ctypes.c_int
             L.w4a16_last_error.restype = ctypes.c_char_p
             L.w4a16_version.restype = ctypes.c_char_p
@@ -342,6 +359,105 @@ def device_status(stream=None) -> int:
     if rc not in (OK, ERR_DEVICE):
         _raise(rc)
     return flags.value
+
+
+# ---- STQ1_0 ternary matrices (include/stq1.h) -------------------------------------------
+
+@dataclass
+class STQ1Matrix:
+    """An STQ1_0 matrix (or E stacked experts) repacked on the GPU for the
+    stq1 kernels: ``packed`` uint8 [E * stq1_packed_bytes(N, K)]."""
+
+    packed: torch.Tensor
+    N: int
+    K: int
+    E: int = 1
+
+    @classmethod
+    def from_blocks(cls, blocks: torch.Tensor, N: int, K: int, E: int = 1, stream=None) -> "STQ1Matrix":
+        """From the page's 42-byte blocks, uint8 [.., N, K/256, 42] on the GPU."""
+        _dev_tensor(blocks, torch.uint8, "blocks")
+        per = stq1_packed_bytes(N, K)
+        if per == 0:
+            raise ValueError(f"STQ1_0 needs N >= 1 and K a multiple of 256 in 256..32768 (N={N}, K={K})")
+        if blocks.numel() != E * N * (K // STQ1_BLOCK_WEIGHTS) * STQ1_BLOCK_BYTES:
+            raise ValueError("blocks must hold E * N * K/256 blocks of 42 bytes")
+        packed = torch.empty(E * per, dtype=torch.uint8, device=blocks.device)
+        src = blocks.reshape(E, -1)
+        for e in range(E):
+            _raise(lib().stq1_pack(src[e].data_ptr(), packed.data_ptr() + e * per, N, K, _stream_ptr(stream)))
+        return cls(packed, N, K, E)
+
+    @classmethod
+    def from_host(cls, blocks, N: int, K: int, E: int = 1, device="cuda") -> "STQ1Matrix":
+        """From a numpy uint8 array of blocks (``synth.make_stq1``)."""
+        return cls.from_blocks(torch.from_numpy(blocks.reshape(-1).copy()).to(device), N, K, E)
+
+    @property
+    def nbytes(self) -> int:
+        """Bytes of the weights in the page's format (42 per 256 weights)."""
+        return self.E * self.N * (self.K // STQ1_BLOCK_WEIGHTS) * STQ1_BLOCK_BYTES
+
+
+def stq1_packed_bytes(N: int, K: int) -> int:
+    return int(lib().stq1_packed_bytes(N, K))
+
+
+def stq1_mm(x: torch.Tensor, w: STQ1Matrix, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y[..., N] = x[..., K] W^T (float32) through ``stq1_mm``."""
+    if w.E != 1:
+        raise ValueError("stq1_mm takes a single matrix; use stq1_mm_id for stacked experts")
+    _dev_tensor(x, torch.float32, "x")
+    if x.shape[-1] != w.K:
+        raise ValueError(f"x has K={x.shape[-1]}, weights have K={w.K}")
+    M = x.numel() // w.K
+    if out is None:
+        out = torch.empty(*x.shape[:-1], w.N, dtype=torch.float32, device=x.device)
+    _dev_tensor(out, torch.float32, "out")
+    if out.numel() != M * w.N:
+        raise ValueError("out has the wrong number of elements")
+    _raise(lib().stq1_mm(x.data_ptr(), w.packed.data_ptr(), out.data_ptr(), M, w.N, w.K, _stream_ptr(stream)))
+    return out
+
+
+def stq1_mm_id(x: torch.Tensor, w: STQ1Matrix, ids: torch.Tensor, out: torch.Tensor | None = None,
+               stream=None) -> torch.Tensor:
+    """y[t] = W[ids[t]] x[t] (float32) through ``stq1_mm_id``; x [T, K], ids int32 [T]."""
+    _dev_tensor(x, torch.float32, "x")
+    _dev_tensor(ids, torch.int32, "ids")
+    if x.dim() != 2 or x.shape[1] != w.K:
+        raise ValueError("x must be [T, K]")
+    T = x.shape[0]
+    if ids.numel() != T:
+        raise ValueError("ids must hold one expert id per token")
+    if out is None:
+        out = torch.empty(T, w.N, dtype=torch.float32, device=x.device)
+    _dev_tensor(out, torch.float32, "out")
+    _raise(lib().stq1_mm_id(x.data_ptr(), w.packed.data_ptr(), ids.data_ptr(), out.data_ptr(), T, w.N, w.K, w.E,
+                            _stream_ptr(stream)))
+    return out
+
+
+def stq1_get_rows(ids: torch.Tensor, w: STQ1Matrix, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Rows ids of W as float32 [..., K] through ``stq1_get_rows``."""
+    if w.E != 1:
+        raise ValueError("stq1_get_rows takes a single matrix")
+    _dev_tensor(ids, torch.int32, "ids")
+    T = ids.numel()
+    if out is None:
+        out = torch.empty(*ids.shape, w.K, dtype=torch.float32, device=ids.device)
+    _dev_tensor(out, torch.float32, "out")
+    if out.numel() != T * w.K:
+        raise ValueError("out has the wrong number of elements")
+    _raise(lib().stq1_get_rows(w.packed.data_ptr(), ids.data_ptr(), out.data_ptr(), T, w.N, w.K,
+                               _stream_ptr(stream)))
+    return out
+
+
+def stq1_get_plan(N: int, K: int) -> dict:
+    p = Stq1Plan()
+    _raise(lib().stq1_get_plan(N, K, ctypes.byref(p)))
+    return {f: getattr(p, f) for f, _ in p._fields_}
 
 
 def version() -> str:

@@ -38,3 +38,21 @@ def mm_id_bytes(ids, T: int, N: int, K: int, E: int, group: int = GROUP) -> tupl
     """(bytes, distinct experts touched) of a routed call."""
     touched = len({int(e) for e in ids[:T] if 0 <= int(e) < E})
     return touched * weight_bytes(N, K, group) + 2 * T * K + 2 * T * N, touched
+
+
+# STQ1_0 ("Hy4-preview Metal kernels for llama.cpp", section "Notes and
+# gotchas"): 42 bytes per 256 weights; float32 activations in, float32 out.
+STQ1_BLOCK_WEIGHTS, STQ1_BLOCK_BYTES = 256, 42
+
+
+def stq1_weight_bytes(N: int, K: int) -> int:
+    return N * (K // STQ1_BLOCK_WEIGHTS) * STQ1_BLOCK_BYTES
+
+
+def stq1_mm_bytes(M: int, N: int, K: int) -> int:
+    return stq1_weight_bytes(N, K) + 4 * M * K + 4 * M * N
+
+
+def stq1_mm_id_bytes(ids, T: int, N: int, K: int, E: int) -> tuple[int, int]:
+    touched = len({int(e) for e in ids[:T] if 0 <= int(e) < E})
+    return touched * stq1_weight_bytes(N, K) + 4 * T * K + 4 * T * N, touched

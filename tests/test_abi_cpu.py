@@ -16,6 +16,7 @@ from skinny_gemm_gb300 import _build, ops, synth
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 DECL = re.compile(r"^\s*(?:int|void|const char\s*\*)\s+(w4a16_\w+)\s*\(", re.M)
+STQ1_DECL = re.compile(r"^\s*(?:int|size_t)\s+(stq1_\w+)\s*\(", re.M)
 
 P = 0x10000  # 16-byte-aligned fake address
 
@@ -31,15 +32,19 @@ def _exported(path: str) -> set[str]:
 
 def test_every_declared_symbol_is_exported():
     headers = sorted(os.path.basename(h) for h in glob.glob(os.path.join(ROOT, "include", "*.h")))
-    assert headers == ["w4a16.h", "w4a16_synth.h"]
+    assert headers == ["stq1.h", "w4a16.h", "w4a16_synth.h"]
     cuda_syms = _exported(_build.build_cuda())
     decl = _declared("w4a16.h")
     assert len(decl) >= 10
     missing = [s for s in decl if s not in cuda_syms]
     assert not missing, f"declared but not exported by libw4a16.so: {missing}"
+    decl = STQ1_DECL.findall(open(os.path.join(ROOT, "include", "stq1.h")).read())
+    assert len(decl) == 6
+    missing = [s for s in decl if s not in cuda_syms]
+    assert not missing, f"declared in stq1.h but not exported by libw4a16.so: {missing}"
     synth_syms = _exported(_build.build_synth())
     decl = _declared("w4a16_synth.h")
-    assert len(decl) == 6
+    assert len(decl) == 9
     assert not [s for s in decl if s not in synth_syms]
     # the binding names exactly the exported C calls
     assert set(ops.EXPORTS) <= cuda_syms
@@ -224,3 +229,42 @@ def test_mm_group_errors(L):
     # M == 0 is a no-op once every item is valid, and items are still checked
     assert L.w4a16_mm_group(_items(3), 3, 0, 512, None) == ops.OK
     assert L.w4a16_mm_group(_items(3, over={0: {"N": -1}}), 3, 0, 512, None) == ops.ERR_SHAPE
+
+
+def test_stq1_sizes_plans_and_errors(L, monkeypatch):
+    assert L.stq1_packed_bytes(16, 256) == 672
+    assert L.stq1_packed_bytes(17, 512) == 2 * 2 * 672
+    assert L.stq1_packed_bytes(6144, 2048) == 6144 * 8 * 42            # the page's bytes when N % 16 == 0
+    for N, K in [(0, 256), (4, 300), (4, 0), (4, 32768 + 256)]:
+        assert L.stq1_packed_bytes(N, K) == 0
+    plan = ops.Stq1Plan()
+    assert L.stq1_get_plan(6144, 2048, ctypes.byref(plan)) == ops.OK
+    assert (plan.ksplit, plan.blocks_per_slice, plan.rows_per_pass) == (8, 1, 8)
+    assert L.stq1_get_plan(16384, 16384, ctypes.byref(plan)) == ops.OK
+    assert (plan.ksplit, plan.blocks_per_slice, plan.rows_per_pass) == (4, 16, 2)
+    assert L.stq1_get_plan(16, 256, ctypes.byref(plan)) == ops.OK and plan.ksplit == 1
+    assert L.stq1_get_plan(4, 384, ctypes.byref(plan)) == ops.ERR_SHAPE
+    assert L.stq1_get_plan(4, 32768, ctypes.byref(plan)) == ops.OK and plan.rows_per_pass == 1
+    mm, mid, rows, pack = L.stq1_mm, L.stq1_mm_id, L.stq1_get_rows, L.stq1_pack
+    assert mm(P, P, P, 0, 64, 512, None) == ops.OK                      # M == 0: no-op
+    assert mm(P, P, P, -1, 64, 512, None) == ops.ERR_SHAPE
+    assert mm(P, P, P, 1, 64, 320, None) == ops.ERR_SHAPE and "multiple of 256" in _err(L)
+    assert mm(P, P, P, 1, 0, 512, None) == ops.ERR_SHAPE
+    assert mm(None, P, P, 1, 64, 512, None) == ops.ERR_NULL
+    assert mm(P + 4, P, P, 1, 64, 512, None) == ops.ERR_ALIGN
+    assert mm(P, P + 8, P, 1, 64, 512, None) == ops.ERR_ALIGN
+    assert mm(P, P, P + 2, 1, 64, 512, None) == ops.ERR_ALIGN
+    assert mid(P, P, P, P, 0, 64, 512, 8, None) == ops.OK
+    assert mid(P, P, P, P, 4, 64, 512, 0, None) == ops.ERR_EXPERTS
+    assert mid(P, P, P, P, -1, 64, 512, 8, None) == ops.ERR_EXPERTS
+    assert mid(P, P, None, P, 4, 64, 512, 8, None) == ops.ERR_NULL
+    assert mid(P, P, P + 2, P, 4, 64, 512, 8, None) == ops.ERR_ALIGN
+    assert rows(P, P, P, 0, 64, 512, None) == ops.OK
+    assert rows(P, None, P, 3, 64, 512, None) == ops.ERR_NULL
+    assert rows(P, P, P, 3, 64, 500, None) == ops.ERR_SHAPE
+    assert pack(P + 1, P, 64, 512, None) == ops.ERR_ALIGN                 # blocks 2-byte
+    assert pack(P, P + 8, 64, 512, None) == ops.ERR_ALIGN                 # packed 16-byte
+    assert pack(P, P, 64, 128, None) == ops.ERR_SHAPE
+    monkeypatch.setenv("W4A16_FAULT", "validate")
+    L.w4a16_debug_reload_env()
+    assert mm(P, P, P, 1, 64, 512, None) == ops.ERR_SHAPE and "injected" in _err(L)
