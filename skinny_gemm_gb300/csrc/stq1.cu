@@ -57,15 +57,15 @@ constexpr int kScaleOff = 640;
 constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kDepth = 4;                 // records in flight per warp
-constexpr int kLutBytes = 32 * 32 * 8;    // [label][lane] uint2
 constexpr int kMaxRows = 8;               // activation rows per pass
 constexpr int kTokBytes = 64;             // int tok[8], count, next token
-constexpr int kSmemCap = 227 * 1024;
+constexpr int kSmemCap = 227 * 1024 - 32 * 32 * 8;  // dynamic share; the decode table is static
+constexpr int kSlack = 256;                          // staged-area tail read by unused columns
 constexpr int kTargetWarps = 2432;        // 152 SMs x 16 warps
 constexpr int kGroupStride = 4096;        // staged bytes per block and 8 columns
 
 __host__ __device__ constexpr int red_bytes(int mc) { return kWarps * 16 * 8 * mc * 4; }
-__host__ __device__ constexpr int fixed_smem(int mc) { return kLutBytes + red_bytes(mc) + kTokBytes; }
+__host__ __device__ constexpr int fixed_smem(int mc) { return 2 * red_bytes(mc) + kTokBytes + kSlack; }
 
 struct Params {
   const float* x;
@@ -96,38 +96,89 @@ __device__ uint32_t lane_bf16(int c, int s, int l) {
   return (flip ^ s) ? 0xBF80u : 0x3F80u;
 }
 
-__device__ void fill_lut(uint2* lut) {
+// Decode table: the bf16 pairs (lanes 0,1 | lanes 2,3) of label = code | sign << 4,
+// one 8-byte copy per warp lane at byte label * 256 + lane * 8, so the 32
+// lookups of a warp fall in distinct banks whatever the labels.
+__shared__ uint2 s_lut[32 * 32];
+
+__device__ void fill_lut() {
   for (int i = threadIdx.x; i < 32 * 32; i += blockDim.x) {
     const int label = i >> 5, c = label & 15, s = label >> 4;
-    lut[i] = make_uint2(lane_bf16(c, s, 0) | (lane_bf16(c, s, 1) << 16),
-                        lane_bf16(c, s, 2) | (lane_bf16(c, s, 3) << 16));
+    s_lut[i] = make_uint2(lane_bf16(c, s, 0) | (lane_bf16(c, s, 1) << 16),
+                          lane_bf16(c, s, 2) | (lane_bf16(c, s, 3) << 16));
   }
 }
 
-// Activation rows tok[0 .. mrows) of x as bf16 parts in MMA fragment order:
-// column c = 3m + q (part q of row m) is column c % 8 of MMA group c / 8;
-// within a group the bytes of (block b, chunk j, column n, quad lane t) are
-// at ((b*16 + j) * ncols_in_group + n) * 32 + t * 8, holding lanes 0..3 of
-// group 16t + j as the two B registers.
-__device__ void stage_rows(uint8_t* bsm, const float* x, const int* tok, int mrows, int K, int nb) {
-  const int ncols = 3 * mrows;
-  for (int m = 0; m < mrows; ++m) {
-    const float* row = x + (long long)tok[m] * K;
-    for (int k = threadIdx.x; k < K; k += blockDim.x) {
-      const float v = row[k];
-      const __nv_bfloat16 h0 = __float2bfloat16_rn(v);
-      const float r1 = __fsub_rn(v, __bfloat162float(h0));
-      const __nv_bfloat16 h1 = __float2bfloat16_rn(r1);
-      const float r2 = __fsub_rn(r1, __bfloat162float(h1));
-      const __nv_bfloat16 h2 = __float2bfloat16_rn(r2);
-      const int b = k >> 8, w = k & 255, t = w >> 6, p = (w >> 4) & 3, j = w & 15;
-      const int within = t * 8 + (p >> 1) * 4 + (p & 1) * 2;
+__device__ __forceinline__ uint2 lut_entry(uint32_t byte_offset) {
+  return *reinterpret_cast<const uint2*>(reinterpret_cast<const char*>(s_lut) + byte_offset);
+}
+
+// Columns of a pass of up to R activation rows: 3R parts, in MMA groups of 8.
+template <int R>
+struct Cols {
+  static constexpr int NC = 3 * R;
+  static constexpr int MC = (NC + 7) / 8;
+  __host__ __device__ static constexpr int ncg(int g) { return NC - 8 * g < 8 ? NC - 8 * g : 8; }
+};
+
+// Activation rows tok[0 .. mrows) of x as bf16 parts in MMA fragment order.
+// Column c = 3m + q (part q of row m) is column n = c % 8 of MMA group
+// g = c / 8.  Group g occupies `gstride` bytes from g * gstride; in it the
+// 8-byte slot of (block b, chunk j, column n, quad lane t) is at
+// ((b*16 + j) * ncg(g) + n) * 32 + t * 8 and holds the parts of
+// x[256b + 64t + 16p + j], p = 0..3 (lanes 0..3 of group 16t + j): the two
+// B registers of that lane.  Each thread loads the four values of a slot
+// for four slots before converting any (sixteen loads in flight).
+template <int R>
+__device__ void stage_rows(uint8_t* bsm, const float* __restrict__ x, const int* tok, int mrows, int K, int nb,
+                           int gstride) {
+  using C = Cols<R>;
+  const int per_row = nb * 64;
+  const int total = mrows * per_row;
+  for (int base = threadIdx.x; base < total; base += 4 * kThreads) {
+    float v[4][4];
 #pragma unroll
-      for (int q = 0; q < 3; ++q) {
-        const int c = 3 * m + q, g = c >> 3, n = c & 7;
-        const int ncg = min(8, ncols - 8 * g);
-        const int off = g * nb * kGroupStride + ((b * 16 + j) * ncg + n) * 32 + within;
-        *reinterpret_cast<__nv_bfloat16*>(bsm + off) = q == 0 ? h0 : q == 1 ? h1 : h2;
+    for (int u = 0; u < 4; ++u) {
+      const int it = base + u * kThreads;
+      if (it < total) {
+        const int m = it / per_row, w = it - m * per_row;
+        const float* src = x + (long long)tok[m] * K + (w >> 6) * kBlockW + ((w >> 4) & 3) * 64 + (w & 15);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[u][q] = __ldg(src + 16 * q);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int it = base + u * kThreads;
+      if (it < total) {
+        const int m = it / per_row, w = it - m * per_row;
+        const int b = w >> 6, t = (w >> 4) & 3, j = w & 15;
+        uint32_t part[3][2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t bits[3][2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float f = v[u][2 * h + e];
+            const __nv_bfloat16 h0 = __float2bfloat16_rn(f);
+            const float r1 = __fsub_rn(f, __bfloat162float(h0));
+            const __nv_bfloat16 h1 = __float2bfloat16_rn(r1);
+            const float r2 = __fsub_rn(r1, __bfloat162float(h1));
+            const __nv_bfloat16 h2 = __float2bfloat16_rn(r2);
+            bits[0][e] = __bfloat16_as_ushort(h0);
+            bits[1][e] = __bfloat16_as_ushort(h1);
+            bits[2][e] = __bfloat16_as_ushort(h2);
+          }
+#pragma unroll
+          for (int q = 0; q < 3; ++q) part[q][h] = bits[q][0] | (bits[q][1] << 16);
+        }
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+          const int c = 3 * m + q, g = c >> 3, n = c & 7;
+          const int ncg = g < C::MC - 1 ? 8 : C::ncg(C::MC - 1);
+          *reinterpret_cast<uint2*>(bsm + g * gstride + ((b * 16 + j) * ncg + n) * 32 + t * 8) =
+              make_uint2(part[q][0], part[q][1]);
+        }
       }
     }
   }
@@ -159,31 +210,34 @@ __device__ __forceinline__ void mma_bf16(float c[4], uint32_t a0, uint32_t a1, u
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// One record: 16 chunks of 16 k, MC MMAs each (column groups past ncols are
-// skipped), then pa += d * block sum per row.
-template <int MC>
-__device__ __forceinline__ void process(const Rec& r, int b, const uint8_t* lut, uint32_t lane8,
-                                        const uint8_t* bsm, int nb, int ncols, int lane, float pa[MC][4]) {
+// One record (block b of a 16-row tile): 16 chunks of 16 k, one MMA per
+// active column group, then pa += d * block sum per row.  Lanes whose column
+// lies past a group's last one read the neighbouring slots (inside the
+// staged area and its slack); those columns of C are never used.
+template <int R>
+__device__ __forceinline__ void process(const Rec& r, const uint8_t* bsm, int b, int gstride, int active_groups,
+                                        uint32_t lane8, int n, int t, float pa[Cols<R>::MC][4]) {
+  using C = Cols<R>;
   uint32_t La[4], Lb[4];
   labels(r.c.x, r.c.y, r.s & 0xFFFFu, La);
   labels(r.c.z, r.c.w, r.s >> 16, Lb);
-  float acc[MC][4];
+  const uint2* bq[C::MC];
+  float acc[C::MC][4];
 #pragma unroll
-  for (int g = 0; g < MC; ++g) acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0.f;
-  const int n = lane >> 2, t = lane & 3;
+  for (int g = 0; g < C::MC; ++g) {
+    bq[g] = reinterpret_cast<const uint2*>(bsm + g * gstride + (b * 16 * C::ncg(g) + n) * 32 + t * 8);
+    acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0.f;
+  }
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const int wi = (j & 1) + 2 * (j >> 3);
     const uint32_t sel = 0x5504u | ((uint32_t)((j >> 1) & 3) << 4);  // [0, 0, label, lane8]
-    const uint2 ea = *reinterpret_cast<const uint2*>(lut + __byte_perm(La[wi], lane8, sel));
-    const uint2 eb = *reinterpret_cast<const uint2*>(lut + __byte_perm(Lb[wi], lane8, sel));
+    const uint2 ea = lut_entry(__byte_perm(La[wi], lane8, sel));
+    const uint2 eb = lut_entry(__byte_perm(Lb[wi], lane8, sel));
 #pragma unroll
-    for (int g = 0; g < MC; ++g) {
-      if (8 * g < ncols) {
-        const int ncg = min(8, ncols - 8 * g);
-        uint2 bf = make_uint2(0u, 0u);
-        if (n < ncg)
-          bf = *reinterpret_cast<const uint2*>(bsm + g * nb * kGroupStride + ((b * 16 + j) * ncg + n) * 32 + t * 8);
+    for (int g = 0; g < C::MC; ++g) {
+      if (g == 0 || g < active_groups) {
+        const uint2 bf = bq[g][j * C::ncg(g) * 4];
         mma_bf16(acc[g], ea.x, eb.x, ea.y, eb.y, bf.x, bf.y);
       }
     }
@@ -191,7 +245,7 @@ __device__ __forceinline__ void process(const Rec& r, int b, const uint8_t* lut,
   const float dr = __half2float(__ushort_as_half((unsigned short)(r.d & 0xFFFFu)));
   const float dr8 = __half2float(__ushort_as_half((unsigned short)(r.d >> 16)));
 #pragma unroll
-  for (int g = 0; g < MC; ++g) {
+  for (int g = 0; g < C::MC; ++g) {
     pa[g][0] = __fmaf_rn(dr, acc[g][0], pa[g][0]);
     pa[g][1] = __fmaf_rn(dr, acc[g][1], pa[g][1]);
     pa[g][2] = __fmaf_rn(dr8, acc[g][2], pa[g][2]);
@@ -199,100 +253,93 @@ __device__ __forceinline__ void process(const Rec& r, int b, const uint8_t* lut,
   }
 }
 
-// End of a round: the warps' partials through shared memory, summed over the
-// K slices in slice order, then the three parts (h0 + h1) + h2, into y.
-template <int MC>
-__device__ void finish_round(const Params& p, float* red, const int* tok, int mrows, int round, int warp, int lane,
-                             float pa[MC][4]) {
-  constexpr int stride = 8 * MC;
+// End of a round: the warps' partials through shared memory (buffer `buf`
+// of two, so one barrier per round), summed over the K slices in slice
+// order, then the three parts (h0 + h1) + h2, into y.
+template <int R>
+__device__ void finish_round(const Params& p, float* red, int buf, const int* tok, int mrows, int tile0, int warp,
+                             int lane, float pa[Cols<R>::MC][4]) {
+  using C = Cols<R>;
+  constexpr int stride = 8 * C::MC;
+  float* rb = red + buf * (kWarps * 16 * stride);
   const int r = lane >> 2, t = lane & 3;
 #pragma unroll
-  for (int g = 0; g < MC; ++g) {
-    *reinterpret_cast<float2*>(red + (warp * 16 + r) * stride + 8 * g + 2 * t) = make_float2(pa[g][0], pa[g][1]);
-    *reinterpret_cast<float2*>(red + (warp * 16 + r + 8) * stride + 8 * g + 2 * t) = make_float2(pa[g][2], pa[g][3]);
+  for (int g = 0; g < C::MC; ++g) {
+    *reinterpret_cast<float2*>(rb + (warp * 16 + r) * stride + 8 * g + 2 * t) = make_float2(pa[g][0], pa[g][1]);
+    *reinterpret_cast<float2*>(rb + (warp * 16 + r + 8) * stride + 8 * g + 2 * t) = make_float2(pa[g][2], pa[g][3]);
   }
   __syncthreads();
   const int outs = p.rt * mrows * 16;
   for (int o = threadIdx.x; o < outs; o += kThreads) {
     const int rr = o & 15, mo = o >> 4;
     const int lt = mo / mrows, m = mo - lt * mrows;
-    const int tile = round * p.rt + lt;
+    const int tile = tile0 + lt;
     const int n = tile * 16 + rr;
     if (tile < p.tiles && n < p.N) {
       float part[3];
 #pragma unroll
       for (int q = 0; q < 3; ++q) {
         const int col = 3 * m + q;
-        float s = red[(lt * p.ks * 16 + rr) * stride + col];
-        for (int sl = 1; sl < p.ks; ++sl) s = __fadd_rn(s, red[((lt * p.ks + sl) * 16 + rr) * stride + col]);
+        float s = rb[(lt * p.ks * 16 + rr) * stride + col];
+        for (int sl = 1; sl < p.ks; ++sl) s = __fadd_rn(s, rb[((lt * p.ks + sl) * 16 + rr) * stride + col]);
         part[q] = s;
       }
       p.y[(long long)tok[m] * p.N + n] = __fadd_rn(__fadd_rn(part[0], part[1]), part[2]);
     }
   }
-  __syncthreads();
 }
 
-// The record of item `it` of this warp: round `it / bps` of this CTA, block
-// `slice * bps + it % bps` of the warp's tile; zeros past the matrix.
-__device__ __forceinline__ void fetch(const Params& p, const uint8_t* wbase, int it, int n_items, int lt, int slice,
-                                      int lane, Rec& r) {
-  r.c = make_uint4(0u, 0u, 0u, 0u);
-  r.s = 0u;
-  r.d = 0u;
-  if (it >= n_items) return;
-  const int rl = it / p.bps, i = it - rl * p.bps;
-  const int tile = (blockIdx.x + rl * gridDim.x) * p.rt + lt;
-  const int b = slice * p.bps + i;
-  if (tile >= p.tiles || b >= p.nb) return;
-  const uint8_t* rec = wbase + ((long long)tile * p.nb + b) * kRec;
-  r.c = ld_stream_v4(rec + 16 * lane);
-  r.s = ld_nc_u32(rec + kSignOff + 4 * lane);
-  r.d = ld_nc_u32(rec + kScaleOff + 4 * (lane >> 2));
+// A warp's stream of records: round rl of this CTA (tile (blockIdx.x + rl *
+// gridDim.x) * rt + lt), blocks slice * bps .. slice * bps + bps - 1.
+struct Cursor {
+  const uint8_t* rec;
+  int tile, i;
+};
+
+__device__ __forceinline__ void cursor_start(Cursor& c, const Params& p, const uint8_t* wbase, int lt, int slice) {
+  c.tile = (int)blockIdx.x * p.rt + lt;
+  c.i = 0;
+  c.rec = wbase + ((long long)c.tile * p.nb + slice * p.bps) * kRec;
 }
 
-template <int MC>
-__device__ void run_rows(const Params& p, const uint8_t* wbase, const uint8_t* lut, float* red, const int* tok,
-                         const uint8_t* bsm, int mrows, int n_items, int warp, int lane, int lt, int slice) {
-  const int ncols = 3 * mrows;
-  const uint32_t lane8 = (uint32_t)lane * 8u;
-  Rec ring[kDepth];
-#pragma unroll
-  for (int s = 0; s < kDepth; ++s) fetch(p, wbase, s, n_items, lt, slice, lane, ring[s]);
-  float pa[MC][4];
-#pragma unroll
-  for (int g = 0; g < MC; ++g) pa[g][0] = pa[g][1] = pa[g][2] = pa[g][3] = 0.f;
-  for (int base = 0; base < n_items; base += kDepth) {
-#pragma unroll
-    for (int s = 0; s < kDepth; ++s) {
-      const int it = base + s;
-      if (it < n_items) {  // the same for every warp of the CTA
-        const Rec cur = ring[s];
-        fetch(p, wbase, it + kDepth, n_items, lt, slice, lane, ring[s]);
-        const int rl = it / p.bps, i = it - rl * p.bps;
-        const int round = blockIdx.x + rl * gridDim.x;
-        const int tile = round * p.rt + lt;
-        const int b = slice * p.bps + i;
-        if (tile < p.tiles && b < p.nb) process<MC>(cur, b, lut, lane8, bsm, p.nb, ncols, lane, pa);
-        if (i == p.bps - 1) {
-          finish_round<MC>(p, red, tok, mrows, round, warp, lane, pa);
-#pragma unroll
-          for (int g = 0; g < MC; ++g) pa[g][0] = pa[g][1] = pa[g][2] = pa[g][3] = 0.f;
-        }
-      }
-    }
+__device__ __forceinline__ bool cursor_valid(const Cursor& c, const Params& p, int slice) {
+  return c.tile < p.tiles && slice * p.bps + c.i < p.nb;
+}
+
+__device__ __forceinline__ void cursor_next(Cursor& c, const Params& p, const uint8_t* wbase, int slice) {
+  if (++c.i == p.bps) {
+    c.i = 0;
+    c.tile += (int)gridDim.x * p.rt;
+    c.rec = wbase + ((long long)c.tile * p.nb + slice * p.bps) * kRec;
+  } else {
+    c.rec += kRec;
   }
 }
 
-template <int MC, bool ROUTED>
+__device__ __forceinline__ void fetch(Cursor& c, const Params& p, const uint8_t* wbase, int slice, int lane,
+                                      Rec& r) {
+  if (cursor_valid(c, p, slice)) {
+    r.c = ld_stream_v4(c.rec + 16 * lane);
+    r.s = ld_nc_u32(c.rec + kSignOff + 4 * lane);
+    r.d = ld_nc_u32(c.rec + kScaleOff + 4 * (lane >> 2));
+  } else {
+    r.c = make_uint4(0u, 0u, 0u, 0u);
+    r.s = 0u;
+    r.d = 0u;
+  }
+  cursor_next(c, p, wbase, slice);
+}
+
+template <int R, bool ROUTED>
 __global__ void __launch_bounds__(kThreads, 2) stq1_mm_kernel(const Params p) {
+  using C = Cols<R>;
   extern __shared__ __align__(16) uint8_t smem[];
-  uint2* lut = reinterpret_cast<uint2*>(smem);
-  float* red = reinterpret_cast<float*>(smem + kLutBytes);
-  int* tok = reinterpret_cast<int*>(smem + kLutBytes + red_bytes(MC));
-  uint8_t* bsm = smem + fixed_smem(MC);
+  float* red = reinterpret_cast<float*>(smem);
+  int* tok = reinterpret_cast<int*>(smem + 2 * red_bytes(C::MC));
+  uint8_t* bsm = smem + 2 * red_bytes(C::MC) + kTokBytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int lt = warp / p.ks, slice = warp - lt * p.ks;
+  const int gstride = p.nb * kGroupStride;
   const uint8_t* wbase = p.w;
   int e = 0;
   if (ROUTED) {
@@ -309,9 +356,11 @@ __global__ void __launch_bounds__(kThreads, 2) stq1_mm_kernel(const Params p) {
       }
     }
   }
-  fill_lut(lut);
+  fill_lut();
   const int my_rounds = (int)blockIdx.x < p.rounds ? (p.rounds - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
   const int n_items = my_rounds * p.bps;
+  const uint32_t lane8 = (uint32_t)lane * 8u;
+  const int n = lane >> 2, t = lane & 3;
   int next = 0;  // routed: first token not yet gathered
   for (;;) {
     int mrows;
@@ -320,13 +369,13 @@ __global__ void __launch_bounds__(kThreads, 2) stq1_mm_kernel(const Params p) {
       if (warp == 0) {
         int cnt = 0, t0 = next;
         while (cnt < p.xcap && t0 < p.T) {
-          const int t = t0 + lane;
-          const bool hit = t < p.T && __ldg(p.ids + t) == e;
+          const int tt = t0 + lane;
+          const bool hit = tt < p.T && __ldg(p.ids + tt) == e;
           const unsigned mask = __ballot_sync(0xFFFFFFFFu, hit);
           const int hits = __popc(mask);
           const int take = min(hits, p.xcap - cnt);
           const int pos = __popc(mask & ((1u << lane) - 1u));
-          if (hit && pos < take) tok[cnt + pos] = t;
+          if (hit && pos < take) tok[cnt + pos] = tt;
           cnt += take;
           if (take < hits) {  // stop at the first hit not taken
             unsigned rest = mask;
@@ -350,10 +399,38 @@ __global__ void __launch_bounds__(kThreads, 2) stq1_mm_kernel(const Params p) {
       mrows = p.M;
       __syncthreads();
     }
-    stage_rows(bsm, p.x, tok, mrows, p.K, p.nb);
+    // weights first: the first records are in flight while the rows are staged
+    Cursor fc, cc;
+    cursor_start(fc, p, wbase, lt, slice);
+    cursor_start(cc, p, wbase, lt, slice);
+    Rec ring[kDepth];
+#pragma unroll
+    for (int s = 0; s < kDepth; ++s) fetch(fc, p, wbase, slice, lane, ring[s]);
+    stage_rows<R>(bsm, p.x, tok, mrows, p.K, p.nb, gstride);
     __syncthreads();
-    run_rows<MC>(p, wbase, reinterpret_cast<const uint8_t*>(lut), red, tok, bsm, mrows, n_items, warp, lane, lt,
-                 slice);
+    const int active = (3 * mrows + 7) / 8;
+    float pa[C::MC][4];
+#pragma unroll
+    for (int g = 0; g < C::MC; ++g) pa[g][0] = pa[g][1] = pa[g][2] = pa[g][3] = 0.f;
+    int buf = 0;
+    for (int base = 0; base < n_items; base += kDepth) {
+#pragma unroll
+      for (int s = 0; s < kDepth; ++s) {
+        if (base + s < n_items) {  // the same for every warp of the CTA
+          const Rec cur = ring[s];
+          fetch(fc, p, wbase, slice, lane, ring[s]);
+          if (cursor_valid(cc, p, slice))
+            process<R>(cur, bsm, slice * p.bps + cc.i, gstride, active, lane8, n, t, pa);
+          if (cc.i == p.bps - 1) {
+            finish_round<R>(p, red, buf, tok, mrows, cc.tile - lt, warp, lane, pa);
+            buf ^= 1;
+#pragma unroll
+            for (int g = 0; g < C::MC; ++g) pa[g][0] = pa[g][1] = pa[g][2] = pa[g][3] = 0.f;
+          }
+          cursor_next(cc, p, wbase, slice);
+        }
+      }
+    }
     if (!ROUTED) break;
   }
 }
@@ -431,9 +508,9 @@ int sm_count() {
   return cached[dev];
 }
 
-template <int MC, bool ROUTED>
+template <int R, bool ROUTED>
 cudaError_t launch_kernel(const Params& p, dim3 grid_cap, int smem, cudaStream_t s) {
-  auto fn = stq1_mm_kernel<MC, ROUTED>;
+  auto fn = stq1_mm_kernel<R, ROUTED>;
   static std::mutex mu;
   static std::map<std::pair<int, int>, int> occ;  // (device, smem) -> CTAs per SM
   int dev = 0;
@@ -490,7 +567,26 @@ Params base_params(int N, int K) {
   return p;
 }
 
-int groups_for(int rows) { return (3 * rows + 7) / 8; }
+int pow2_at_least(int v) {
+  int r = 1;
+  while (r < v) r *= 2;
+  return r;
+}
+
+int smem_for(int R, int K) { return fixed_smem((3 * R + 7) / 8) + 6 * R * K; }
+
+template <bool ROUTED>
+cudaError_t launch_rows(const Params& p, int R, cudaStream_t s) {
+  const int smem = smem_for(R, p.K);
+  const dim3 grid(1, ROUTED ? (unsigned)p.E : 1u, 1);
+  switch (R) {
+    case 1: return launch_kernel<1, ROUTED>(p, grid, smem, s);
+    case 2: return launch_kernel<2, ROUTED>(p, grid, smem, s);
+    case 4: return launch_kernel<4, ROUTED>(p, grid, smem, s);
+    case 8: return launch_kernel<8, ROUTED>(p, grid, smem, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 }  // namespace
 
@@ -510,9 +606,10 @@ void stq1_make_plan(int N, int K, Stq1Plan* pl) {
   pl->bps = (pl->nb + ks - 1) / ks;
   pl->rt = kWarps / ks;
   pl->rounds = (pl->tiles + pl->rt - 1) / pl->rt;
-  const long long room = (long long)kSmemCap - fixed_smem(3);
-  long long rows = room / (6LL * K);
-  pl->xcap = (int)(rows < kMaxRows ? rows : kMaxRows);
+  // rows per pass: the largest power of two up to 8 whose staged parts fit
+  int x = kMaxRows;
+  while (x > 1 && smem_for(x, K) > kSmemCap) x /= 2;
+  pl->xcap = x;
 }
 
 cudaError_t launch_stq1_pack(const uint8_t* src, uint8_t* dst, int N, int K, cudaStream_t s) {
@@ -533,12 +630,7 @@ cudaError_t launch_stq1_mm(const float* x, const uint8_t* w, float* y, int M, in
   p.y = y;
   p.M = M;
   p.row0 = row0;
-  const int mc = groups_for(M);
-  const int smem = fixed_smem(mc) + 6 * M * K;
-  const dim3 grid(1, 1, 1);
-  if (mc == 1) return launch_kernel<1, false>(p, grid, smem, s);
-  if (mc == 2) return launch_kernel<2, false>(p, grid, smem, s);
-  return launch_kernel<3, false>(p, grid, smem, s);
+  return launch_rows<false>(p, pow2_at_least(M), s);
 }
 
 cudaError_t launch_stq1_mm_id(const float* x, const uint8_t* w, const int32_t* ids, float* y, int T, int N,
@@ -551,14 +643,15 @@ cudaError_t launch_stq1_mm_id(const float* x, const uint8_t* w, const int32_t* i
   p.flags = flags;
   p.T = T;
   p.E = E;
-  const int rows = p.xcap < T ? p.xcap : T;
-  p.xcap = rows;
-  const int mc = groups_for(rows);
-  const int smem = fixed_smem(mc) + 6 * rows * K;
-  const dim3 grid(1, (unsigned)E, 1);
-  if (mc == 1) return launch_kernel<1, true>(p, grid, smem, s);
-  if (mc == 2) return launch_kernel<2, true>(p, grid, smem, s);
-  return launch_kernel<3, true>(p, grid, smem, s);
+  // Tokens per pass: twice the mean per expert (at least two), at most T and
+  // the staging limit; an expert with more tokens takes more passes.
+  long long want = 2LL * ((T + E - 1) / E);
+  if (want < 2) want = 2;
+  if (want > T) want = T;
+  int R = pow2_at_least((int)want);
+  if (R > p.xcap) R = p.xcap;
+  p.xcap = R;
+  return launch_rows<true>(p, R, s);
 }
 
 cudaError_t launch_stq1_get_rows(const uint8_t* w, const int32_t* ids, float* out, int T, int N, int K,
