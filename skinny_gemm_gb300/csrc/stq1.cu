@@ -60,7 +60,7 @@ constexpr int kDepth = 4;                 // records in flight per warp
 constexpr int kMaxRows = 8;               // activation rows per pass
 constexpr int kTokBytes = 64;             // int tok[8], count, next token
 constexpr int kSmemCap = 227 * 1024 - 32 * 32 * 8;  // dynamic share; the decode table is static
-constexpr int kSlack = 256;                          // staged-area tail read by unused columns
+constexpr int kSlack = 256;                          // spare bytes after the staged rows
 constexpr int kTargetWarps = 2432;        // 152 SMs x 16 warps
 constexpr int kGroupStride = 4096;        // staged bytes per block and 8 columns
 
@@ -212,8 +212,9 @@ __device__ __forceinline__ void mma_bf16(float c[4], uint32_t a0, uint32_t a1, u
 
 // One record (block b of a 16-row tile): 16 chunks of 16 k, one MMA per
 // active column group, then pa += d * block sum per row.  Lanes whose column
-// lies past a group's last one read the neighbouring slots (inside the
-// staged area and its slack); those columns of C are never used.
+// lies past a group's last one read that last column's slot again (a
+// broadcast: no extra shared-memory traffic); those columns of C are never
+// used.
 template <int R>
 __device__ __forceinline__ void process(const Rec& r, const uint8_t* bsm, int b, int gstride, int active_groups,
                                         uint32_t lane8, int n, int t, float pa[Cols<R>::MC][4]) {
@@ -225,7 +226,8 @@ __device__ __forceinline__ void process(const Rec& r, const uint8_t* bsm, int b,
   float acc[C::MC][4];
 #pragma unroll
   for (int g = 0; g < C::MC; ++g) {
-    bq[g] = reinterpret_cast<const uint2*>(bsm + g * gstride + (b * 16 * C::ncg(g) + n) * 32 + t * 8);
+    const int col = n < C::ncg(g) ? n : C::ncg(g) - 1;
+    bq[g] = reinterpret_cast<const uint2*>(bsm + g * gstride + (b * 16 * C::ncg(g) + col) * 32 + t * 8);
     acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0.f;
   }
 #pragma unroll
