@@ -58,7 +58,7 @@ constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kDepth = 4;                 // records in flight per warp
 constexpr int kMaxRows = 8;               // activation rows per pass
-constexpr int kTokBytes = 64;             // int tok[8], count, next token
+constexpr int kTokBytes = 192;            // int tok[8], count, next token; 32-word expert bitmap
 constexpr int kSmemCap = 227 * 1024 - 32 * 32 * 8;  // dynamic share; the decode table is static
 constexpr int kSlack = 256;                          // spare bytes after the staged rows
 constexpr int kTargetWarps = 2432;        // 152 SMs x 16 warps
@@ -79,6 +79,7 @@ struct Params {
   int xcap;
   long long wstride;  // bytes per expert
   int T, E;
+  int flat;  // routed: deal (expert, round) units over one grid (E <= 1024)
 };
 
 __device__ __forceinline__ uint32_t ld_nc_u32(const void* p) {
@@ -211,7 +212,8 @@ __device__ __forceinline__ void mma_bf16(float c[4], uint32_t a0, uint32_t a1, u
 }
 
 // One record (block b of a 16-row tile): 16 chunks of 16 k, one MMA per
-// active column group, then pa += d * block sum per row.  Lanes whose column
+// active column group (even and odd chunks in two accumulators), then
+// pa += d * (even + odd) per row.  Lanes whose column
 // lies past a group's last one read that last column's slot again (a
 // broadcast: no extra shared-memory traffic); those columns of C are never
 // used.
@@ -223,12 +225,13 @@ __device__ __forceinline__ void process(const Rec& r, const uint8_t* bsm, int b,
   labels(r.c.x, r.c.y, r.s & 0xFFFFu, La);
   labels(r.c.z, r.c.w, r.s >> 16, Lb);
   const uint2* bq[C::MC];
-  float acc[C::MC][4];
+  float acc[2][C::MC][4];  // even and odd chunks: two shorter MMA dependency chains
 #pragma unroll
   for (int g = 0; g < C::MC; ++g) {
     const int col = n < C::ncg(g) ? n : C::ncg(g) - 1;
     bq[g] = reinterpret_cast<const uint2*>(bsm + g * gstride + (b * 16 * C::ncg(g) + col) * 32 + t * 8);
-    acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0.f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) acc[h][g][0] = acc[h][g][1] = acc[h][g][2] = acc[h][g][3] = 0.f;
   }
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
@@ -240,7 +243,7 @@ __device__ __forceinline__ void process(const Rec& r, const uint8_t* bsm, int b,
     for (int g = 0; g < C::MC; ++g) {
       if (g == 0 || g < active_groups) {
         const uint2 bf = bq[g][j * C::ncg(g) * 4];
-        mma_bf16(acc[g], ea.x, eb.x, ea.y, eb.y, bf.x, bf.y);
+        mma_bf16(acc[j & 1][g], ea.x, eb.x, ea.y, eb.y, bf.x, bf.y);
       }
     }
   }
@@ -248,10 +251,10 @@ __device__ __forceinline__ void process(const Rec& r, const uint8_t* bsm, int b,
   const float dr8 = __half2float(__ushort_as_half((unsigned short)(r.d >> 16)));
 #pragma unroll
   for (int g = 0; g < C::MC; ++g) {
-    pa[g][0] = __fmaf_rn(dr, acc[g][0], pa[g][0]);
-    pa[g][1] = __fmaf_rn(dr, acc[g][1], pa[g][1]);
-    pa[g][2] = __fmaf_rn(dr8, acc[g][2], pa[g][2]);
-    pa[g][3] = __fmaf_rn(dr8, acc[g][3], pa[g][3]);
+    pa[g][0] = __fmaf_rn(dr, __fadd_rn(acc[0][g][0], acc[1][g][0]), pa[g][0]);
+    pa[g][1] = __fmaf_rn(dr, __fadd_rn(acc[0][g][1], acc[1][g][1]), pa[g][1]);
+    pa[g][2] = __fmaf_rn(dr8, __fadd_rn(acc[0][g][2], acc[1][g][2]), pa[g][2]);
+    pa[g][3] = __fmaf_rn(dr8, __fadd_rn(acc[0][g][3], acc[1][g][3]), pa[g][3]);
   }
 }
 
@@ -291,16 +294,23 @@ __device__ void finish_round(const Params& p, float* red, int buf, const int* to
   }
 }
 
-// A warp's stream of records: round rl of this CTA (tile (blockIdx.x + rl *
-// gridDim.x) * rt + lt), blocks slice * bps .. slice * bps + bps - 1.
-struct Cursor {
-  const uint8_t* rec;
-  int tile, i;
+// The rounds a CTA runs on one matrix: first, first + step, ... (count).
+struct Span {
+  int first, count, step;
 };
 
-__device__ __forceinline__ void cursor_start(Cursor& c, const Params& p, const uint8_t* wbase, int lt, int slice) {
-  c.tile = (int)blockIdx.x * p.rt + lt;
+// A warp's stream of records: round `first + k * step` of its span (tile
+// round * rt + lt), blocks slice * bps .. slice * bps + bps - 1 of each.
+struct Cursor {
+  const uint8_t* rec;
+  int tile, i, tile_step;
+};
+
+__device__ __forceinline__ void cursor_start(Cursor& c, const Params& p, const uint8_t* wbase, const Span& sp, int lt,
+                                             int slice) {
+  c.tile = sp.first * p.rt + lt;
   c.i = 0;
+  c.tile_step = sp.step * p.rt;
   c.rec = wbase + ((long long)c.tile * p.nb + slice * p.bps) * kRec;
 }
 
@@ -311,7 +321,7 @@ __device__ __forceinline__ bool cursor_valid(const Cursor& c, const Params& p, i
 __device__ __forceinline__ void cursor_next(Cursor& c, const Params& p, const uint8_t* wbase, int slice) {
   if (++c.i == p.bps) {
     c.i = 0;
-    c.tile += (int)gridDim.x * p.rt;
+    c.tile += c.tile_step;
     c.rec = wbase + ((long long)c.tile * p.nb + slice * p.bps) * kRec;
   } else {
     c.rec += kRec;
@@ -332,42 +342,22 @@ __device__ __forceinline__ void fetch(Cursor& c, const Params& p, const uint8_t*
   cursor_next(c, p, wbase, slice);
 }
 
+// The rounds of `sp` on one matrix (expert e when routed): passes of at most
+// R activation rows (routed: the expert's tokens in order), each staged once,
+// then every warp's records of the span.
 template <int R, bool ROUTED>
-__global__ void __launch_bounds__(kThreads, 2) stq1_mm_kernel(const Params p) {
+__device__ void run_span(const Params& p, const uint8_t* wbase, int e, const Span& sp, float* red, int* tok,
+                         uint8_t* bsm, int warp, int lane, int lt, int slice) {
   using C = Cols<R>;
-  extern __shared__ __align__(16) uint8_t smem[];
-  float* red = reinterpret_cast<float*>(smem);
-  int* tok = reinterpret_cast<int*>(smem + 2 * red_bytes(C::MC));
-  uint8_t* bsm = smem + 2 * red_bytes(C::MC) + kTokBytes;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int lt = warp / p.ks, slice = warp - lt * p.ks;
   const int gstride = p.nb * kGroupStride;
-  const uint8_t* wbase = p.w;
-  int e = 0;
-  if (ROUTED) {
-    e = blockIdx.y;
-    wbase += (long long)e * p.wstride;
-    if (blockIdx.x == 0 && blockIdx.y == 0) {
-      // tokens routed outside 0..E-1: zero rows and the device flag
-      for (int t = 0; t < p.T; ++t) {
-        const int id = __ldg(p.ids + t);
-        if (id < 0 || id >= p.E) {
-          if (threadIdx.x == 0) atomicOr(p.flags, W4A16_DEVICE_BAD_ID);
-          for (int n = threadIdx.x; n < p.N; n += blockDim.x) p.y[(long long)t * p.N + n] = 0.f;
-        }
-      }
-    }
-  }
-  fill_lut();
-  const int my_rounds = (int)blockIdx.x < p.rounds ? (p.rounds - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-  const int n_items = my_rounds * p.bps;
+  const int n_items = sp.count * p.bps;
   const uint32_t lane8 = (uint32_t)lane * 8u;
   const int n = lane >> 2, t = lane & 3;
   int next = 0;  // routed: first token not yet gathered
   for (;;) {
     int mrows;
+    __syncthreads();  // earlier passes and spans are done with tok and the staged rows
     if (ROUTED) {
-      __syncthreads();  // the previous pass is done with tok and the staged rows
       if (warp == 0) {
         int cnt = 0, t0 = next;
         while (cnt < p.xcap && t0 < p.T) {
@@ -403,8 +393,8 @@ __global__ void __launch_bounds__(kThreads, 2) stq1_mm_kernel(const Params p) {
     }
     // weights first: the first records are in flight while the rows are staged
     Cursor fc, cc;
-    cursor_start(fc, p, wbase, lt, slice);
-    cursor_start(cc, p, wbase, lt, slice);
+    cursor_start(fc, p, wbase, sp, lt, slice);
+    cursor_start(cc, p, wbase, sp, lt, slice);
     Rec ring[kDepth];
 #pragma unroll
     for (int s = 0; s < kDepth; ++s) fetch(fc, p, wbase, slice, lane, ring[s]);
@@ -434,6 +424,76 @@ __global__ void __launch_bounds__(kThreads, 2) stq1_mm_kernel(const Params p) {
       }
     }
     if (!ROUTED) break;
+  }
+}
+
+// Index of the k-th set bit of a 1024-bit map.
+__device__ __forceinline__ int nth_set_bit(const unsigned* bm, int k) {
+  for (int w = 0; w < 32; ++w) {
+    const int c = __popc(bm[w]);
+    if (k < c) {
+      unsigned v = bm[w];
+      for (int q = 0; q < k; ++q) v &= v - 1u;
+      return 32 * w + __ffs(v) - 1;
+    }
+    k -= c;
+  }
+  return -1;
+}
+
+template <int R, bool ROUTED>
+__global__ void __launch_bounds__(kThreads, 2) stq1_mm_kernel(const Params p) {
+  using C = Cols<R>;
+  extern __shared__ __align__(16) uint8_t smem[];
+  float* red = reinterpret_cast<float*>(smem);
+  int* tok = reinterpret_cast<int*>(smem + 2 * red_bytes(C::MC));
+  unsigned* bitmap = reinterpret_cast<unsigned*>(tok + 16);
+  uint8_t* bsm = smem + 2 * red_bytes(C::MC) + kTokBytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lt = warp / p.ks, slice = warp - lt * p.ks;
+  fill_lut();
+  if (!ROUTED) {
+    const int mine = (int)blockIdx.x < p.rounds ? (p.rounds - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    run_span<R, false>(p, p.w, 0, Span{(int)blockIdx.x, mine, (int)gridDim.x}, red, tok, bsm, warp, lane, lt, slice);
+    return;
+  }
+  if (blockIdx.x == 0 && blockIdx.y == 0) {
+    // tokens routed outside 0..E-1: zero rows and the device flag
+    for (int tt = 0; tt < p.T; ++tt) {
+      const int id = __ldg(p.ids + tt);
+      if (id < 0 || id >= p.E) {
+        if (threadIdx.x == 0) atomicOr(p.flags, W4A16_DEVICE_BAD_ID);
+        for (int n = threadIdx.x; n < p.N; n += blockDim.x) p.y[(long long)tt * p.N + n] = 0.f;
+      }
+    }
+  }
+  if (!p.flat) {  // one grid column per expert
+    const int mine = (int)blockIdx.x < p.rounds ? (p.rounds - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    run_span<R, true>(p, p.w + (long long)blockIdx.y * p.wstride, (int)blockIdx.y,
+                      Span{(int)blockIdx.x, mine, (int)gridDim.x}, red, tok, bsm, warp, lane, lt, slice);
+    return;
+  }
+  // One grid over the experts some token selects: units (expert, round) in
+  // order, a contiguous range per CTA (at most a few experts each).
+  if (threadIdx.x < 32) bitmap[threadIdx.x] = 0u;
+  __syncthreads();
+  for (int tt = threadIdx.x; tt < p.T; tt += blockDim.x) {
+    const int id = __ldg(p.ids + tt);
+    if (id >= 0 && id < p.E) atomicOr(&bitmap[id >> 5], 1u << (id & 31));
+  }
+  __syncthreads();
+  int touched = 0;
+  for (int w = 0; w < 32; ++w) touched += __popc(bitmap[w]);
+  const long long units = (long long)touched * p.rounds;
+  long long u = units * blockIdx.x / gridDim.x;
+  const long long u_end = units * (blockIdx.x + 1) / gridDim.x;
+  while (u < u_end) {
+    const int ei = (int)(u / p.rounds);
+    const int r = (int)(u - (long long)ei * p.rounds);
+    const int cnt = (int)min((long long)(p.rounds - r), u_end - u);
+    const int e = nth_set_bit(bitmap, ei);
+    run_span<R, true>(p, p.w + (long long)e * p.wstride, e, Span{r, cnt, 1}, red, tok, bsm, warp, lane, lt, slice);
+    u += cnt;
   }
 }
 
@@ -535,7 +595,11 @@ cudaError_t launch_kernel(const Params& p, dim3 grid_cap, int smem, cudaStream_t
   }
   const int slots = per_sm * sm_count();
   dim3 grid = grid_cap;
-  if (ROUTED) {
+  if (ROUTED && p.flat) {
+    const long long units = (long long)p.E * p.rounds;
+    grid.x = (unsigned)(slots < units ? slots : units);
+    grid.y = 1;
+  } else if (ROUTED) {
     // CTAs per expert: the resident slots over the experts T tokens are
     // expected to touch when drawn uniformly, E (1 - (1 - 1/E)^T).
     double touched = (double)p.E;
@@ -580,7 +644,7 @@ int smem_for(int R, int K) { return fixed_smem((3 * R + 7) / 8) + 6 * R * K; }
 template <bool ROUTED>
 cudaError_t launch_rows(const Params& p, int R, cudaStream_t s) {
   const int smem = smem_for(R, p.K);
-  const dim3 grid(1, ROUTED ? (unsigned)p.E : 1u, 1);
+  const dim3 grid(1, ROUTED && !p.flat ? (unsigned)p.E : 1u, 1);
   switch (R) {
     case 1: return launch_kernel<1, ROUTED>(p, grid, smem, s);
     case 2: return launch_kernel<2, ROUTED>(p, grid, smem, s);
@@ -645,6 +709,7 @@ cudaError_t launch_stq1_mm_id(const float* x, const uint8_t* w, const int32_t* i
   p.flags = flags;
   p.T = T;
   p.E = E;
+  p.flat = E <= 1024 ? 1 : 0;
   // Tokens per pass: twice the mean per expert (at least two), at most T and
   // the staging limit; an expert with more tokens takes more passes.
   long long want = 2LL * ((T + E - 1) / E);
