@@ -558,16 +558,19 @@ __global__ void stq1_rows_kernel(const uint8_t* __restrict__ w, const int32_t* _
 
 // ---- host side -------------------------------------------------------------------------
 
+// Multiprocessors of the current device (cached per device).
 int sm_count() {
-  static int cached[64] = {};
+  static std::mutex mu;
+  static std::map<int, int> cached;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
-  if (!cached[dev]) {
-    int v = 0;
-    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-    cached[dev] = v > 0 ? v : 152;
-  }
-  return cached[dev];
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = cached.find(dev);
+  if (it != cached.end()) return it->second;
+  int v = 0;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 152;
+  cached[dev] = v;
+  return v;
 }
 
 template <int R, bool ROUTED>

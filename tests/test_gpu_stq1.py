@@ -152,3 +152,30 @@ def test_graph_capture_and_streams():
         g.replay()
         torch.cuda.synchronize()
         assert torch.equal(out.view(torch.int32), want.view(torch.int32))
+
+
+def test_mm_id_many_experts_grid_per_expert():
+    """E > 1024 experts: one grid column per expert instead of the dealt
+    units (small matrices keep the weights at 1100 x 672 bytes)."""
+    E, N, K, T = 1100, 20, 256, 9
+    blocks = synth.make_stq1(13, N, K, E)
+    ids_np = np.array([1099, 0, 517, 1099, 3, 1024, 1023, 0, 77], dtype=np.int32)
+    x = synth.make_x_f32(13, T, K)
+    w = ops.STQ1Matrix.from_host(blocks, N, K, E)
+    y = ops.stq1_mm_id(dev_x(x), w, torch.from_numpy(ids_np).cuda())
+    yr, ad = oracle.stq1_mm_id(x, blocks, ids_np, T, N, K, E, threads=oracle.host_threads())
+    check(y, yr, ad, K, "routed, 1100 experts")
+    assert ops.device_status() == 0
+
+
+def test_largest_k_one_row_per_pass():
+    N, K, M = 40, 32768, 3
+    assert ops.stq1_get_plan(N, K)["rows_per_pass"] == 1
+    blocks = synth.make_stq1(14, N, K)
+    x = synth.make_x_f32(14, M, K)
+    w = ops.STQ1Matrix.from_host(blocks, N, K)
+    xd = dev_x(x)
+    y = ops.stq1_mm(xd, w)
+    yr, ad = oracle.stq1_mm(x, blocks, M, N, K, threads=oracle.host_threads())
+    check(y, yr, ad, K, "K = 32768")
+    assert torch.equal(y[1:2].view(torch.int32), ops.stq1_mm(xd[1:2].contiguous(), w).view(torch.int32))
