@@ -156,7 +156,7 @@ def test_graph_capture_and_streams():
 
 def test_mm_id_many_experts_grid_per_expert():
     """E > 1024 experts: one grid column per expert instead of the dealt
-    units (small matrices keep the weights at 1100 x 672 bytes)."""
+    units (two-tile matrices keep the weights at 1100 x 1344 bytes)."""
     E, N, K, T = 1100, 20, 256, 9
     blocks = synth.make_stq1(13, N, K, E)
     ids_np = np.array([1099, 0, 517, 1099, 3, 1024, 1023, 0, 77], dtype=np.int32)
