@@ -89,11 +89,15 @@ def dist_env():
     return world, rank, local
 
 
-def init_dist(world):
+def init_dist(world, backend=None):
+    """The process group of a torchrun launch (None for one process): NCCL on
+    GPUs, gloo where there is none (the CPU tests of the multi-rank path)."""
     if world <= 1:
         return None
+    import torch
     import torch.distributed as dist
-    backend = "nccl"
+    if backend is None:
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
     dist.init_process_group(backend=backend)
     return dist
 
@@ -107,9 +111,16 @@ def max_over_ranks(dist, v: float) -> float:
     if dist is None:
         return v
     import torch
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    device = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_gbps(world: int, step_bytes: int, steps: int, ms_max: float) -> float:
+    """Whole-job throughput: the bytes every rank streamed over the slowest
+    rank's time (each rank runs its own replica of the step)."""
+    return world * step_bytes * steps / (ms_max * 1e-3) / 1e9
 
 
 # ---- peaks, clocks, ncu traffic ----------------------------------------------------
@@ -316,7 +327,7 @@ def run_ours(args, world, rank, local):
         barrier(dist)
     ms_total = max_over_ranks(dist, t_start.elapsed_time(t_end))
     ms_per_step = ms_total / args.steps
-    value = world * step_bytes * args.steps / (ms_total * 1e-3) / 1e9
+    value = aggregate_gbps(world, step_bytes, args.steps, ms_total)
 
     dims = {name: (N, K) for name, N, K in DECODE_LAYER}
 
