@@ -44,6 +44,17 @@
  * done and never synchronise, except w4a16_device_status and the one-time
  * workspace set-up below.
  *
+ * Overlapped launches.  The tensor-core kernels are launched as programmatic
+ * dependents: a call may start while the previous kernel on its stream is
+ * still running, and (unless the environment sets W4A16_PDL=1 or 0) it
+ * requests its first weight tiles before it waits for that kernel.  It reads
+ * activations and ids, and writes outputs, only after the wait.  So the
+ * weights (Wq, scales, biases) must not be written by work still pending on
+ * the same stream: finish writing them (synchronise, or make the stream wait
+ * on an event recorded after the writes) before the first call that reads
+ * them.  W4A16_PDL=1 keeps the overlap without the early fetch; 0 turns both
+ * off.
+ *
  * Workspace.  The tensor-core kernel's persistent grid deals its work units
  * through a counter in a workspace the library owns, one per (device,
  * stream), and when it splits K across warps of different SMs
