@@ -23,13 +23,12 @@
 //    contiguous code bytes and sixteen contiguous sign bits of the page's
 //    own block.  B follows the same order (the activations are staged in it).
 //  * A group decodes through a 32-entry table in shared memory (code and
-//    sign bit -> the high bytes of the four lanes as bf16 2v, whose low
-//    bytes are zero), one 4-byte slot per warp lane so that lookups never
-//    conflict; two byte permutes make the two bf16 pairs, and the block
-//    scale takes the 1/2 back (exact).  The page found a table lookup faster
-//    than arithmetic decoding on its GPU; here it also keeps the decode at a
-//    few instructions per group: the table offsets of 16 groups come from
-//    four word-wide mask/multiply steps and one byte permute per group.
+//    sign bit -> the bf16 pairs of lanes 0,1 and 2,3), one 8-byte slot per
+//    warp lane so that lookups never conflict.  The page found a table
+//    lookup faster than arithmetic decoding on its GPU; here it also keeps
+//    the decode at a few instructions per group: the table offsets of 16
+//    groups come from four word-wide mask/multiply steps and one byte
+//    permute per group.
 //  * Each CTA stages the activation parts once; its 8 warps take K slices of
 //    one to eight 16-row tiles per round, add their fp32 partials in shared
 //    memory in slice order, and write y.  The slice count and every order
@@ -89,43 +88,31 @@ __device__ __forceinline__ uint32_t ld_nc_u32(const void* p) {
   return v;
 }
 
-// Value (-1, 0 or +1) of lane l of a group with code c and sign bit s.
-__device__ int lane_value(int c, int s, int l) {
+// bf16 bits of lane l of a group with code c and sign bit s.
+__device__ uint32_t lane_bf16(int c, int s, int l) {
   const int zero = c >> 2;
-  if (l == zero) return 0;
+  if (l == zero) return 0u;
   const int rank = l - (l > zero ? 1 : 0);  // place among the three other lanes
   const int flip = rank == 0 ? (c & 1) : rank == 1 ? ((c >> 1) & 1) : 0;
-  return (flip ^ s) ? -1 : 1;
+  return (flip ^ s) ? 0xBF80u : 0x3F80u;
 }
 
-// bf16 bits of 1, -1, 0 (the row gather) and the high byte of bf16 2, -2, 0
-// (the matmul, whose weights enter the tensor cores doubled so that a lane is
-// a single byte; the block scale carries the 1/2 back, exactly).
-__device__ __forceinline__ uint32_t bf16_unit(int v) { return v > 0 ? 0x3F80u : v < 0 ? 0xBF80u : 0u; }
-__device__ __forceinline__ uint32_t hi_byte_two(int v) { return v > 0 ? 0x40u : v < 0 ? 0xC0u : 0u; }
-
-// Decode table: for label = code | sign << 4, the high bytes of the four
-// lanes' bf16 values 2v (byte l = lane l), one 4-byte copy per warp lane at
-// byte label * 256 + lane * 4, so the 32 lookups of a warp fall in distinct
-// banks whatever the labels (half of each 256-byte row is unused).
-__shared__ uint32_t s_lut[32 * 64];
+// Decode table: the bf16 pairs (lanes 0,1 | lanes 2,3) of label = code | sign << 4,
+// one 8-byte copy per warp lane at byte label * 256 + lane * 8, so the 32
+// lookups of a warp fall in distinct banks whatever the labels.
+__shared__ uint2 s_lut[32 * 32];
 
 __device__ void fill_lut() {
-  for (int i = threadIdx.x; i < 32 * 64; i += blockDim.x) {
-    const int label = i >> 6, c = label & 15, s = label >> 4;
-    s_lut[i] = hi_byte_two(lane_value(c, s, 0)) | (hi_byte_two(lane_value(c, s, 1)) << 8) |
-               (hi_byte_two(lane_value(c, s, 2)) << 16) | (hi_byte_two(lane_value(c, s, 3)) << 24);
+  for (int i = threadIdx.x; i < 32 * 32; i += blockDim.x) {
+    const int label = i >> 5, c = label & 15, s = label >> 4;
+    s_lut[i] = make_uint2(lane_bf16(c, s, 0) | (lane_bf16(c, s, 1) << 16),
+                          lane_bf16(c, s, 2) | (lane_bf16(c, s, 3) << 16));
   }
 }
 
-__device__ __forceinline__ uint32_t lut_entry(uint32_t byte_offset) {
-  return *reinterpret_cast<const uint32_t*>(reinterpret_cast<const char*>(s_lut) + byte_offset);
+__device__ __forceinline__ uint2 lut_entry(uint32_t byte_offset) {
+  return *reinterpret_cast<const uint2*>(reinterpret_cast<const char*>(s_lut) + byte_offset);
 }
-
-// bf16 pairs (2 v_0, 2 v_1) and (2 v_2, 2 v_3) from a table entry: each
-// value's high byte in place, its low byte zero.
-__device__ __forceinline__ uint32_t lanes01(uint32_t e) { return __byte_perm(e, 0u, 0x1404u); }
-__device__ __forceinline__ uint32_t lanes23(uint32_t e) { return __byte_perm(e, 0u, 0x3424u); }
 
 // Columns of a pass of up to R activation rows: 3R parts, in MMA groups of 8.
 template <int R>
@@ -232,7 +219,7 @@ __device__ __forceinline__ void mma_bf16(float c[4], uint32_t a0, uint32_t a1, u
 // used.
 template <int R>
 __device__ __forceinline__ void process(const Rec& r, const uint8_t* bsm, int b, int gstride, int active_groups,
-                                        uint32_t lane4, int n, int t, float pa[Cols<R>::MC][4]) {
+                                        uint32_t lane8, int n, int t, float pa[Cols<R>::MC][4]) {
   using C = Cols<R>;
   uint32_t La[4], Lb[4];
   labels(r.c.x, r.c.y, r.s & 0xFFFFu, La);
@@ -249,21 +236,19 @@ __device__ __forceinline__ void process(const Rec& r, const uint8_t* bsm, int b,
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const int wi = (j & 1) + 2 * (j >> 3);
-    const uint32_t sel = 0x5504u | ((uint32_t)((j >> 1) & 3) << 4);  // [0, 0, label, lane * 4]
-    const uint32_t ea = lut_entry(__byte_perm(La[wi], lane4, sel));
-    const uint32_t eb = lut_entry(__byte_perm(Lb[wi], lane4, sel));
-    const uint32_t a0 = lanes01(ea), a1 = lanes01(eb), a2 = lanes23(ea), a3 = lanes23(eb);
+    const uint32_t sel = 0x5504u | ((uint32_t)((j >> 1) & 3) << 4);  // [0, 0, label, lane8]
+    const uint2 ea = lut_entry(__byte_perm(La[wi], lane8, sel));
+    const uint2 eb = lut_entry(__byte_perm(Lb[wi], lane8, sel));
 #pragma unroll
     for (int g = 0; g < C::MC; ++g) {
       if (g == 0 || g < active_groups) {
         const uint2 bf = bq[g][j * C::ncg(g) * 4];
-        mma_bf16(acc[j & 1][g], a0, a1, a2, a3, bf.x, bf.y);
+        mma_bf16(acc[j & 1][g], ea.x, eb.x, ea.y, eb.y, bf.x, bf.y);
       }
     }
   }
-  // d / 2: the weights entered doubled (exact: a power of two)
-  const float dr = __fmul_rn(0.5f, __half2float(__ushort_as_half((unsigned short)(r.d & 0xFFFFu))));
-  const float dr8 = __fmul_rn(0.5f, __half2float(__ushort_as_half((unsigned short)(r.d >> 16))));
+  const float dr = __half2float(__ushort_as_half((unsigned short)(r.d & 0xFFFFu)));
+  const float dr8 = __half2float(__ushort_as_half((unsigned short)(r.d >> 16)));
 #pragma unroll
   for (int g = 0; g < C::MC; ++g) {
     pa[g][0] = __fmaf_rn(dr, __fadd_rn(acc[0][g][0], acc[1][g][0]), pa[g][0]);
@@ -366,7 +351,7 @@ __device__ void run_span(const Params& p, const uint8_t* wbase, int e, const Spa
   using C = Cols<R>;
   const int gstride = p.nb * kGroupStride;
   const int n_items = sp.count * p.bps;
-  const uint32_t lane4 = (uint32_t)lane * 4u;
+  const uint32_t lane8 = (uint32_t)lane * 8u;
   const int n = lane >> 2, t = lane & 3;
   int next = 0;  // routed: first token not yet gathered
   for (;;) {
@@ -427,7 +412,7 @@ __device__ void run_span(const Params& p, const uint8_t* wbase, int e, const Spa
           const Rec cur = ring[s];
           fetch(fc, p, wbase, slice, lane, ring[s]);
           if (cursor_valid(cc, p, slice))
-            process<R>(cur, bsm, slice * p.bps + cc.i, gstride, active, lane4, n, t, pa);
+            process<R>(cur, bsm, slice * p.bps + cc.i, gstride, active, lane8, n, t, pa);
           if (cc.i == p.bps - 1) {
             finish_round<R>(p, red, buf, tok, mrows, cc.tile - lt, warp, lane, pa);
             buf ^= 1;
@@ -567,7 +552,7 @@ __global__ void stq1_rows_kernel(const uint8_t* __restrict__ w, const int32_t* _
     const float d = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(
         rec + kScaleOff + 4 * (r & 7) + 2 * half)));
 #pragma unroll
-    for (int q = 0; q < 4; ++q) o[16 * q] = d * __uint_as_float(bf16_unit(lane_value(code, s, q)) << 16);
+    for (int q = 0; q < 4; ++q) o[16 * q] = d * __uint_as_float(lane_bf16(code, s, q) << 16);
   }
 }
 
