@@ -268,3 +268,26 @@ def test_stq1_sizes_plans_and_errors(L, monkeypatch):
     monkeypatch.setenv("W4A16_FAULT", "validate")
     L.w4a16_debug_reload_env()
     assert mm(P, P, P, 1, 64, 512, None) == ops.ERR_SHAPE and "injected" in _err(L)
+
+
+def test_stq1_plans_depend_on_shape_only():
+    """The K split and the rows per pass are functions of (N, K): a power of two
+    of slices up to 8 and no more than the blocks, enough 16-row-tile slices to
+    give every SM work (or all the split there is), and the largest power of
+    two of rows up to 8 whose staged activation parts (6 bytes per row and k)
+    fit in one CTA's shared memory."""
+    L = ops.lib()
+    for N, K in [(16, 256), (6144, 2048), (16384, 16384), (2048, 2560), (300, 4096), (262144, 1536),
+                 (40, 32768), (7, 8192), (1000, 12288)]:
+        plans = []
+        for _ in range(2):
+            p = ops.Stq1Plan()
+            assert L.stq1_get_plan(N, K, ctypes.byref(p)) == ops.OK
+            plans.append((p.ksplit, p.blocks_per_slice, p.rows_per_pass))
+        ks, bps, rows = plans[0]
+        assert plans[0] == plans[1]
+        nb, tiles = K // 256, -(-N // 16)
+        assert ks in (1, 2, 4, 8) and ks <= nb and bps == -(-nb // ks)
+        assert tiles * ks >= 2432 or ks == min(8, 1 << (nb.bit_length() - 1)), (N, K, ks)
+        assert rows in (1, 2, 4, 8) and 6 * rows * K <= 227 * 1024
+        assert rows == 8 or 6 * (2 * rows) * K > 200 * 1024, (N, K, rows)
