@@ -193,7 +193,10 @@ class W4Matrix:
                    group: int, stream=None) -> "W4Matrix":
         """A table quantized with `group` codes per scale and bias (a multiple
         of 64, e.g. the book's 128): scales/biases bf16 [N][K/group] expanded
-        once on the device through ``w4a16_expand_groups``."""
+        once on the device through ``w4a16_expand_groups``.  The stream is
+        synchronised after the expansion: the tensor-core calls may fetch
+        weights before earlier kernels on their stream finish (the
+        overlapped-launch contract of include/w4a16.h)."""
         _dev_tensor(scales, torch.bfloat16, "scales")
         _dev_tensor(biases, torch.bfloat16, "biases")
         if scales.numel() != N * (K // group) or biases.numel() != N * (K // group):
@@ -203,6 +206,7 @@ class W4Matrix:
             d = torch.empty(N, K // GROUP, dtype=torch.bfloat16, device=t.device)
             _raise(lib().w4a16_expand_groups(t.data_ptr(), d.data_ptr(), N, K, group, _stream_ptr(stream)))
             out.append(d)
+        (stream if stream is not None else torch.cuda.current_stream()).synchronize()
         return cls(Wq, out[0], out[1], N, K)
 
     @property
