@@ -458,12 +458,12 @@ __global__ void __launch_bounds__(kThreads, 2) stq1_mm_kernel(const Params p) {
     return;
   }
   if (blockIdx.x == 0 && blockIdx.y == 0) {
-    // tokens routed outside 0..E-1: zero rows and the device flag
-    for (int tt = 0; tt < p.T; ++tt) {
+    // tokens routed outside 0..E-1 (one thread per token): zero rows and the device flag
+    for (int tt = threadIdx.x; tt < p.T; tt += blockDim.x) {
       const int id = __ldg(p.ids + tt);
       if (id < 0 || id >= p.E) {
-        if (threadIdx.x == 0) atomicOr(p.flags, W4A16_DEVICE_BAD_ID);
-        for (int n = threadIdx.x; n < p.N; n += blockDim.x) p.y[(long long)tt * p.N + n] = 0.f;
+        atomicOr(p.flags, W4A16_DEVICE_BAD_ID);
+        for (int n = 0; n < p.N; ++n) p.y[(long long)tt * p.N + n] = 0.f;
       }
     }
   }
