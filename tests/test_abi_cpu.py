@@ -291,3 +291,22 @@ def test_stq1_plans_depend_on_shape_only():
         assert tiles * ks >= 2432 or ks == min(8, 1 << (nb.bit_length() - 1)), (N, K, ks)
         assert rows in (1, 2, 4, 8) and 6 * rows * K <= 227 * 1024
         assert rows == 8 or 6 * (2 * rows) * K > 200 * 1024, (N, K, rows)
+
+
+def test_stq1_python_layer_checks_before_any_launch():
+    """Host tensors, wrong dtypes and wrong block counts are refused in Python;
+    shapes the library rejects raise its ValueError (no device needed)."""
+    import torch
+    blocks = torch.zeros(4 * 2 * 42, dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        ops.STQ1Matrix.from_blocks(blocks, 4, 512)                       # a host tensor
+    with pytest.raises(ValueError):
+        ops.STQ1Matrix.from_blocks(blocks, 4, 300)                       # K % 256
+    w = ops.STQ1Matrix(torch.zeros(ops.stq1_packed_bytes(4, 512), dtype=torch.uint8), 4, 512)
+    with pytest.raises(ValueError):
+        ops.stq1_mm(torch.zeros(1, 512, dtype=torch.bfloat16), w)        # not float32 / not on the GPU
+    with pytest.raises(ValueError):
+        ops.stq1_get_rows(torch.zeros(3, dtype=torch.int64), w)          # ids must be int32
+    with pytest.raises(ops.W4A16ValueError):
+        ops.stq1_get_plan(4, 384)
+    assert ops.stq1_get_plan(6144, 2048) == {"ksplit": 8, "blocks_per_slice": 1, "rows_per_pass": 8}
