@@ -179,3 +179,45 @@ def test_largest_k_one_row_per_pass():
     yr, ad = oracle.stq1_mm(x, blocks, M, N, K, threads=oracle.host_threads())
     check(y, yr, ad, K, "K = 32768")
     assert torch.equal(y[1:2].view(torch.int32), ops.stq1_mm(xd[1:2].contiguous(), w).view(torch.int32))
+
+
+CANARY32 = 0x7FA1C0DE  # a NaN pattern none of these kernels writes (finite inputs give finite outputs)
+PAD = 2048
+
+
+def _guarded(n: int):
+    buf = torch.full((PAD + n + PAD,), CANARY32, dtype=torch.int32, device="cuda")
+    return buf, buf[PAD:PAD + n].view(torch.float32)
+
+
+def _check_guards(buf: torch.Tensor, n: int):
+    torch.cuda.synchronize()
+    b = buf.cpu().numpy()
+    assert np.all(b[:PAD] == CANARY32) and np.all(b[PAD + n:] == CANARY32), "write outside the output"
+    assert not np.any(b[PAD:PAD + n] == CANARY32), "some outputs were not written"
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 37, 512), (3, 129, 2048), (11, 20, 1024), (2, 16, 16384)])
+def test_output_guard_bands(M, N, K):
+    """Outputs inside canary bands: ragged tiles, several passes, the largest split."""
+    w = ops.STQ1Matrix.from_host(synth.make_stq1(70 + N, N, K), N, K)
+    x = dev_x(synth.make_x_f32(70, M, K))
+    buf, flat = _guarded(M * N)
+    ops.stq1_mm(x, w, out=flat.view(M, N))
+    _check_guards(buf, M * N)
+
+
+def test_routed_and_row_gather_guard_bands():
+    E, N, K, T = 3, 45, 512, 10
+    w = ops.STQ1Matrix.from_host(synth.make_stq1(71, N, K, E), N, K, E)
+    ids = torch.from_numpy(synth.make_ids(71, T, E)).cuda()
+    x = dev_x(synth.make_x_f32(71, T, K))
+    buf, flat = _guarded(T * N)
+    ops.stq1_mm_id(x, w, ids, out=flat.view(T, N))
+    _check_guards(buf, T * N)
+    w0 = ops.STQ1Matrix(w.packed[:ops.stq1_packed_bytes(N, K)], N, K)
+    rows = torch.tensor([44, 0, 17, 16, 3], dtype=torch.int32, device="cuda")
+    buf, flat = _guarded(5 * K)
+    ops.stq1_get_rows(rows, w0, out=flat.view(5, K))
+    _check_guards(buf, 5 * K)
+    assert ops.device_status() == 0
