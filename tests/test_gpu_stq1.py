@@ -32,11 +32,13 @@ def check(y: torch.Tensor, yr: np.ndarray, ad: np.ndarray, K: int, what: str):
                                 f"at flat index {worst}")
 
 
-@pytest.mark.parametrize("N,K,M", [(16, 256, 1), (20, 512, 1), (70, 512, 3), (300, 2048, 5), (1000, 4096, 8),
-                                   (37, 1024, 11), (129, 768, 2), (6144, 2048, 1), (6144, 2048, 4)])
+@pytest.mark.parametrize("N,K,M", [(1, 256, 2), (7, 512, 1), (16, 256, 1), (20, 512, 1), (70, 512, 3),
+                                   (300, 2048, 5), (1000, 4096, 8), (37, 1024, 11), (129, 768, 2), (6144, 2048, 1),
+                                   (6144, 2048, 4)])
 def test_parity_full(N, K, M):
-    """Ragged row tiles (N % 16 != 0), K = 1..16 blocks, every K split of the
-    plan (1, 2, 4, 8 slices), one to eight rows, and several passes (M = 11)."""
+    """Ragged row tiles (N % 16 != 0, down to one row), K = 1..16 blocks, every
+    K split of the plan (1, 2, 4, 8 slices), one to eight rows, and several
+    passes (M = 11)."""
     blocks = synth.make_stq1(N + K, N, K)
     x = synth.make_x_f32(M, M, K)
     w = ops.STQ1Matrix.from_host(blocks, N, K)
