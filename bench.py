@@ -1,25 +1,27 @@
 #!/usr/bin/env python3
 """Benchmark of the W4A16 group-64 skinny GEMM on GB300.
 
-One step = the decode-layer projection set of a hidden-2560 model at M = 1
-(q 2048x2560, k 512x2560, v 512x2560, o 2560x2048, gate 10240x2560,
-up 10240x2560, down 2560x10240), i.e. seven w4a16_mm calls streaming 51.6 MB
-of packed weights.  The metric is achieved HBM GB/s over the algorithmic
-bytes (codes + scales + biases + activations + outputs, read or written once;
-tiny-llm "Week 2 Day 2: Keep W4 Packed", section "Revisit the Decode
-Roofline") and its fraction of the measured GB300 copy bandwidth.
+One step = one w4a16_mm call of the tied LM head 262144x2560 at M = 1: the
+largest single-GPU configuration of the workload set, streaming 377.5 MB of
+packed weights, scales and biases.  The metric is achieved HBM GB/s over the
+algorithmic bytes (codes + scales + biases + activations + outputs, read or
+written once; tiny-llm "Week 2 Day 2: Keep W4 Packed", section "Revisit the
+Decode Roofline") and its fraction of the measured GB300 copy bandwidth.
 
-Timing: the layer weights are replicated into enough copies that one pass
-over them is > 3x the L2 size, and step s uses copy s mod L, so every step
-streams its weights from HBM (no L2 flush needed).  Each copy's seven calls
-are captured once in a CUDA graph; the timed region replays K graphs between
-CUDA events on the launching stream, bracketed by a barrier and a
-synchronize.  Per-launch durations (roofline) come from a second pass over
-twin graphs that carry event nodes between the launches.  SM clocks are
-sampled with nvidia-smi during the timed region.
+Timing: the weights are replicated into enough copies that one pass over
+them is > 3x the L2 size, and step s uses copy s mod L, so every step streams
+its weights from HBM (no L2 flush needed).  The timed region is K eager
+back-to-back calls on one stream between CUDA events (queued behind a short
+spin so the host never starves the GPU), bracketed by a barrier and a
+synchronize; consecutive calls overlap by programmatic dependent launch, as
+they do in a decode loop.  The line also reports the single-call cold
+latency: the median of isolated calls, each after a write of twice the L2
+size and bracketed by its own events.  SM clocks are sampled with nvidia-smi
+around a load phase and the timed region.  The decode-layer projection set
+and the other configurations are context numbers under "extras".
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-Under torchrun (N > 1) every rank runs its own independent layers (weak
+Under torchrun (N > 1) every rank runs its own independent replica (weak
 scaling, no collective on the data path); rank 0 prints one JSON line.
 """
 from __future__ import annotations
@@ -42,23 +44,24 @@ sys.path.insert(0, ROOT)
 
 METRIC = "achieved HBM GB/s and % of GB300 peak for W4A16 GEMV/skinny-GEMM (M=1..k+1)"
 UNIT = "GB/s"
+HEAD_N, HEAD_K = 262144, 2560
+WORKLOAD = "W4A16 g64 tied LM head 262144x2560 at M=1 (w4a16_mm; 377.5 MB of packed weights, scales and biases)"
+CONFIG = {"workload": WORKLOAD, "M": 1, "N": HEAD_N, "K": HEAD_K, "group_size": 64}
 DECODE_LAYER = [("q", 2048, 2560), ("k", 512, 2560), ("v", 512, 2560), ("o", 2560, 2048),
                 ("gate", 10240, 2560), ("up", 10240, 2560), ("down", 2560, 10240)]
-WORKLOAD = ("W4A16 g64 decode-layer projection set at M=1, hidden 2560: q 2048x2560, k 512x2560, "
-            "v 512x2560, o 2560x2048, gate 10240x2560, up 10240x2560, down 2560x10240")
-# The launches of one step.  A decoder layer's q/k/v projections are
-# independent given their input, as are gate/up; they go through one
-# w4a16_mm_group call each.  o and down depend on earlier results (attention,
-# the gated activation) and run as their own w4a16_mm calls.
+# The launches of one decode-layer step (an extra).  A decoder layer's q/k/v
+# projections are independent given their input, as are gate/up; they go
+# through one w4a16_mm_group call each.  o and down depend on earlier results
+# (attention, the gated activation) and run as their own w4a16_mm calls.
 LAUNCHES = [("qkv", ("q", "k", "v")), ("o", ("o",)), ("gate_up", ("gate", "up")), ("down", ("down",))]
 # Single workloads for --case: name -> (N, K, E)
 CASES = {"q": (2048, 2560, 1), "kv": (512, 2560, 1), "o": (2560, 2048, 1), "gate": (10240, 2560, 1),
          "down": (2560, 10240, 1), "wide_up": (12288, 1536, 1), "wide_down": (1536, 12288, 1),
          "lm_head_1536": (262144, 1536, 1), "lm_head_2560": (262144, 2560, 1), "dense_16384": (16384, 16384, 1),
-         "routed": (6144, 2048, 8),
+         "routed": (6144, 2048, 8), "tail_k_gate": (9216, 2304, 1),
          "stq1_16384": (16384, 16384, 1), "stq1_expert": (6144, 2048, 1), "stq1_routed": (6144, 2048, 8)}
 FALLBACK_HBM_GBS = 6800.0
-DOMINANT_KERNEL = "tc_tile_kernel"  # runs every projection of the decode-layer step
+DOMINANT_KERNEL = "tc_stream_kernel"  # the persistent grid runs every step (the only kernel)
 NOMINAL_HBM_GBS = 8000.0
 
 
@@ -70,7 +73,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--kernel", default="auto", help="auto | simt | tc | vanilla")
     ap.add_argument("--no-extras", action="store_true", help="skip the per-config context measurements")
-    ap.add_argument("--ungrouped", action="store_true", help="time the layer as seven w4a16_mm calls")
+    ap.add_argument("--no-workspace", action="store_true",
+                    help="run the calls through w4a16_mm without a workspace (w4a16_mm_ws otherwise)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work budget of the oracle baseline")
     ap.add_argument("--case", default=None,
@@ -246,6 +250,70 @@ def build_layers(torch, ops, synth, copies: int, seed: int):
     return layers, xs, ys
 
 
+def measure_decode_layer(torch, ops, synth, roofline, l2, steps, warmup, peak):
+    """The decode-layer projection set at M = 1 as four launches (qkv group,
+    o, gate/up group, down) replayed as CUDA graphs over rotating layer
+    copies; plus the same layer as seven w4a16_mm calls."""
+    step_bytes = layer_bytes(1)
+    weight_bytes = sum(roofline.weight_bytes(N, K) for _, N, K in DECODE_LAYER)
+    copies = max(2, math.ceil(3 * l2 / weight_bytes))
+    layers, xs, ys = build_layers(torch, ops, synth, copies, seed=0)
+    stream = torch.cuda.Stream()
+    dims = {name: (N, K) for name, N, K in DECODE_LAYER}
+
+    def enqueue_layer(layer, launches):
+        for _, names in launches:
+            if len(names) == 1:
+                ops.mm(xs[names[0]], layer[names[0]], out=ys[names[0]])
+            else:
+                ops.mm_group([xs[n] for n in names], [layer[n] for n in names], [ys[n] for n in names])
+
+    out = {"matrices": [f"{n} {N}x{K}" for n, N, K in DECODE_LAYER], "bytes_per_step": step_bytes,
+           "weight_copies": copies}
+    for label, launches in (("grouped", LAUNCHES), ("ungrouped", [(n, (n,)) for n, _, _ in DECODE_LAYER])):
+        graphs = []
+        with torch.cuda.stream(stream):
+            for layer in layers:
+                enqueue_layer(layer, launches)
+            torch.cuda.synchronize()
+            for layer in layers:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    enqueue_layer(layer, launches)
+                graphs.append(g)
+            for s_ in range(warmup):
+                graphs[s_ % len(graphs)].replay()
+        torch.cuda.synchronize()
+        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n = max(1, min(steps, 5000))
+        with torch.cuda.stream(stream):
+            a_.record()
+            for s_ in range(n):
+                graphs[s_ % len(graphs)].replay()
+            b_.record()
+        torch.cuda.synchronize()
+        ms = a_.elapsed_time(b_) / n
+        gb = step_bytes / (ms * 1e-3) / 1e9
+        out[label] = {"launches_per_step": len(launches), "us_per_step": round(1e3 * ms, 3), "GBps": round(gb, 1),
+                      "frac": round(gb / peak, 4),
+                      "launches": [("w4a16_mm_group" if len(nm) > 1 else "w4a16_mm") + f"({', '.join(nm)})"
+                                   for _, nm in launches]}
+        del graphs
+    del layers
+    return out
+
+
+def head_copies(torch, ops, synth, roofline, l2, seed):
+    """Rotating device copies of the seeded LM head (> 3x L2 in total)."""
+    hw = synth.make_weights(seed, HEAD_N, HEAD_K)
+    base = ops.W4Matrix.from_host(hw)
+    copies = max(2, math.ceil(3 * l2 / roofline.weight_bytes(HEAD_N, HEAD_K)))
+    ws = [base] + [ops.W4Matrix(base.Wq.clone(), base.scales.clone(), base.biases.clone(), HEAD_N, HEAD_K)
+                   for _ in range(copies - 1)]
+    torch.cuda.synchronize()  # the weights are written before any call reads them (overlapped launches)
+    return hw, ws
+
+
 def run_ours(args, world, rank, local):
     import torch
     from skinny_gemm_gb300 import ops, roofline, synth
@@ -254,61 +322,22 @@ def run_ours(args, world, rank, local):
     dist = init_dist(world)
     props = torch.cuda.get_device_properties(local)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2**20))
-    kernel = args.kernel
-    plan = ops.get_plan(10240, 2560, kernel)
-    step_bytes = layer_bytes(1)
-    weight_bytes = sum(roofline.weight_bytes(N, K) for _, N, K in DECODE_LAYER)
-    copies = max(2, math.ceil(3 * l2 / weight_bytes))
-    layers, xs, ys = build_layers(torch, ops, synth, copies, seed=1000 * rank)
-
+    N, K = HEAD_N, HEAD_K
+    step_bytes = roofline.mm_bytes(1, N, K)
+    wsel = None if args.no_workspace else "auto"
+    hw, ws = head_copies(torch, ops, synth, roofline, l2, seed=1000 * rank + 1)
+    copies = len(ws)
+    x = torch.from_numpy(synth.make_x(1000 * rank + 2, 1, K).view(np.int16)).view(torch.bfloat16).cuda()
+    y = torch.empty(1, N, dtype=torch.bfloat16, device="cuda")
     stream = torch.cuda.Stream()
-    try:
-        make_ev = lambda: torch.cuda.Event(enable_timing=True, external=True)  # noqa: E731
-        make_ev()
-        external_ok = True
-    except TypeError:
-        make_ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-        external_ok = False
+    plan = ops.get_plan(N, K)
 
-    grouped = not args.ungrouped and args.kernel == "auto"
-    launches = LAUNCHES if grouped else [(name, (name,)) for name, _, _ in DECODE_LAYER]
-
-    def enqueue_layer(layer, evs=None, launches=launches):
-        for i, (_, names) in enumerate(launches):
-            if evs is not None:
-                evs[i].record()
-            if len(names) == 1:
-                ops.mm(xs[names[0]], layer[names[0]], out=ys[names[0]], kernel=kernel)
-            else:
-                ops.mm_group([xs[n] for n in names], [layer[n] for n in names], [ys[n] for n in names])
-        if evs is not None:
-            evs[len(launches)].record()
-
-    graphs, ev_graphs, graph_events = [], [], []
-    with torch.cuda.stream(stream):
-        for layer in layers:  # eager warm-up of every launch before capture
-            enqueue_layer(layer)
-        torch.cuda.synchronize()
-        for layer in layers:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                enqueue_layer(layer)
-            graphs.append(g)
-            if external_ok:  # a twin graph with event nodes between the launches
-                ge = torch.cuda.CUDAGraph()
-                evs = [make_ev() for _ in range(len(launches) + 1)]
-                with torch.cuda.graph(ge, stream=stream):
-                    enqueue_layer(layer, evs)
-                ev_graphs.append(ge)
-                graph_events.append(evs)
-    torch.cuda.synchronize()
-
-    def replay(s):
-        graphs[s % len(graphs)].replay()
+    def call(s_):
+        ops.mm(x, ws[s_ % copies], out=y, workspace=wsel)
 
     with torch.cuda.stream(stream):
-        for s in range(args.warmup):
-            replay(s)
+        for s_ in range(max(3, args.warmup)):
+            call(s_)
     torch.cuda.synchronize()
 
     device_id = getattr(props, "uuid", None)
@@ -316,91 +345,39 @@ def run_ours(args, world, rank, local):
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(str(device_id) if device_id else None)
     with sampler:
+        # untimed load phase of about half a second, so the clock samples are taken under load
+        with torch.cuda.stream(stream):
+            t0 = time.perf_counter()
+            i = 0
+            while time.perf_counter() - t0 < 0.5:
+                for _ in range(64):
+                    call(i)
+                    i += 1
+                torch.cuda.current_stream().synchronize()
         barrier(dist)
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
+            torch.cuda._sleep(20_000_000)  # the host queues the calls while the GPU spins
             t_start.record()
-            for s in range(args.steps):
-                replay(s)
+            for s_ in range(args.steps):
+                call(s_)
             t_end.record()
         torch.cuda.synchronize()
         barrier(dist)
     ms_total = max_over_ranks(dist, t_start.elapsed_time(t_end))
     ms_per_step = ms_total / args.steps
     value = aggregate_gbps(world, step_bytes, args.steps, ms_total)
-
-    dims = {name: (N, K) for name, N, K in DECODE_LAYER}
-
-    def launch_bytes(names):
-        return sum(roofline.mm_bytes(1, *dims[n]) for n in names)
-
-    # Per-launch durations, from a second pass over the same rotating layers
-    # whose graphs carry event nodes between launches.
-    launch_ms = []
-    if external_ok:
-        with torch.cuda.stream(stream):
-            for rep in range(3):
-                for ge in ev_graphs:
-                    ge.replay()
-        torch.cuda.synchronize()
-        for evs in graph_events:
-            launch_ms.append([evs[i].elapsed_time(evs[i + 1]) for i in range(len(launches))])
-    else:  # eager launches queued behind a spin kernel, so events bracket only the kernels
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(launches) + 1)]
-        with torch.cuda.stream(stream):
-            for layer in layers:
-                torch.cuda._sleep(50_000_000)
-                enqueue_layer(layer, evs)
-                torch.cuda.synchronize()
-                launch_ms.append([evs[i].elapsed_time(evs[i + 1]) for i in range(len(launches))])
     peak, peak_kind = measured_peak()
-    # The dominant kernel is every launch of the step (the tile kernel runs all
-    # of them), and programmatic dependent launch overlaps each launch with its
-    # neighbours, so its average launch duration is the timed region over the
-    # launches in it, and its achieved rate is the step's algorithmic bytes
-    # over the step time.
-    launches_per_step = len(launches)
-    launch_us = 1e3 * ms_total / (args.steps * launches_per_step)
-    achieved = step_bytes / (launches_per_step * launch_us * 1e-6) / 1e9
-    per_launch = {}
-    for i, (lname, names) in enumerate(launches):
-        us = 1e3 * sum(r[i] for r in launch_ms) / len(launch_ms)
-        per_launch[lname] = {"matrices": [f"{n} {dims[n][0]}x{dims[n][1]}" for n in names], "us": round(us, 3),
-                             "GBps": round(launch_bytes(names) / (us * 1e-6) / 1e9, 1)}
+    launch_us = 1e3 * ms_per_step  # one launch per step
+    achieved = step_bytes / (launch_us * 1e-6) / 1e9
 
-    # The same layer as seven separate w4a16_mm calls (context for the grouping).
-    ungrouped = None
-    if grouped and not args.no_extras:
-        seven = [(name, (name,)) for name, _, _ in DECODE_LAYER]
-        g7 = []
-        with torch.cuda.stream(stream):
-            for layer in layers:
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream):
-                    enqueue_layer(layer, launches=seven)
-                g7.append(g)
-            for s_ in range(args.warmup):
-                g7[s_ % len(g7)].replay()
-        torch.cuda.synchronize()
-        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        n7 = max(1, min(args.steps, 5000))
-        with torch.cuda.stream(stream):
-            a_.record()
-            for s_ in range(n7):
-                g7[s_ % len(g7)].replay()
-            b_.record()
-        torch.cuda.synchronize()
-        ms7 = a_.elapsed_time(b_) / n7
-        ungrouped = {"launches_per_step": 7, "ms_per_step": round(ms7, 6),
-                     "GBps": round(step_bytes / (ms7 * 1e-3) / 1e9, 2)}
-        del g7
-
-    e2e = measure_e2e(torch, ops, layers, args.steps, kernel, step_bytes, world, dist, launches)
-    extras = None if args.no_extras else measure_extras(torch, ops, synth, roofline, l2, kernel, peak)
+    cold = single_call_cold(torch, lambda i: call(i), stream, l2, reps=60)
+    e2e = measure_e2e(torch, ops, ws, args.steps, step_bytes, world, dist, wsel)
+    extras = None if args.no_extras else measure_extras(torch, ops, synth, roofline, l2, peak, args)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(args.cpu_seconds)
+        cpu = cpu_baseline(args.cpu_seconds, hw)
 
     if rank == 0:
         clocks = sampler.summary()
@@ -408,32 +385,26 @@ def run_ours(args, world, rank, local):
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "accumulate": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "M": 1, "group_size": 64, "bytes_per_step": step_bytes,
-                       "kernel": plan["kernel"], "plan": plan,
-                       "l2_policy": f"inputs larger than L2: {copies} rotating layer copies "
-                                    f"({copies * weight_bytes / 1e6:.0f} MB > 3x L2 {l2 / 1e6:.0f} MB)",
-                       "cuda_graphs": True, "parallelism": f"replicas x{world}",
-                       "launches": [f"{ln}: " + ("w4a16_mm_group" if len(nm) > 1 else "w4a16_mm") + f"({', '.join(nm)})"
-                                    for ln, nm in launches]},
+            "config": dict(CONFIG),
+            "setup": {"api": "w4a16_mm_ws (the binding's per-stream workspace)" if wsel else "w4a16_mm (no workspace)",
+                      "plan": plan, "parallelism": f"replicas x{world}",
+                      "l2_policy": f"inputs larger than L2: {copies} rotating weight copies "
+                                   f"({copies * roofline.weight_bytes(N, K) / 1e6:.0f} MB > 3x L2 {l2 / 1e6:.0f} MB)",
+                      "launch": "eager back-to-back calls on one stream, programmatic dependent launch"},
             "roofline": {"bound": "hbm", "kernel": DOMINANT_KERNEL, "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "traffic": ncu_traffic(DOMINANT_KERNEL),
-                         "algorithmic_bytes_per_launch": round(step_bytes / launches_per_step),
+                         "algorithmic_bytes_per_launch": step_bytes,
                          "launch_us": round(launch_us, 3),
                          "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                          if peak_kind == "measured" else "fallback 6.8 TB/s",
                          "frac_of_nominal_8TBps": round(achieved / NOMINAL_HBM_GBS, 4),
-                         "launches_timed": args.steps * launches_per_step,
+                         "launches_timed": args.steps,
                          "timing": "CUDA events around the timed region on the launching stream; "
-                                   "average launch = region / launches (launches overlap)"},
-            "per_launch_serialised": {
-                "timing": ("event nodes between the launches of twin graphs, replayed after the timed region; "
-                           "the event nodes stop the launches from overlapping, so these are upper bounds"
-                           if external_ok else "events behind a spin kernel"),
-                **per_launch},
-            "ungrouped_layer": ungrouped,
+                                   "average launch = region / launches (one launch per step)"},
+            "single_call_cold": cold,
             "e2e": e2e,
-            "gpu_launches": args.steps * launches_per_step,
+            "gpu_launches": args.steps,
             "clocks": clocks,
         }
         if cpu is not None:
@@ -445,50 +416,61 @@ def run_ours(args, world, rank, local):
         dist.destroy_process_group()
 
 
-def measure_e2e(torch, ops, layers, steps, kernel, step_bytes, world, dist, launches):
-    """Through the public API, every step: pinned host -> device copy of the
-    step's activations, the layer's calls (the same launches as the timed
-    region), device -> pinned host read of the outputs (with the
-    synchronisation that read implies)."""
-    k_in = [K for _, N, K in DECODE_LAYER]
-    n_out = [N for _, N, K in DECODE_LAYER]
-    h_in = torch.empty(sum(k_in), dtype=torch.bfloat16, pin_memory=True)
-    h_out = torch.empty(sum(n_out), dtype=torch.bfloat16, pin_memory=True)
-    h_in.copy_(torch.randn(sum(k_in)).to(torch.bfloat16))
-    d_in = torch.empty(sum(k_in), dtype=torch.bfloat16, device="cuda")
-    d_out = torch.empty(sum(n_out), dtype=torch.bfloat16, device="cuda")
-    ins, outs, a, b = [], [], 0, 0
-    for K, N in zip(k_in, n_out):
-        ins.append(d_in[a:a + K].view(1, K))
-        outs.append(d_out[b:b + N].view(1, N))
-        a, b = a + K, b + N
-    n = max(1, min(steps, 5000))
+def single_call_cold(torch, call, stream, l2, reps=60):
+    """Median latency of isolated calls: before each, a write of twice the L2
+    size (the previous call's lines are gone and no kernel of ours runs
+    before it), then events around the call alone."""
+    from skinny_gemm_gb300 import roofline
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device="cuda")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        for i, (a, b) in enumerate(evs):
+            flush.fill_(i & 0xFF)
+            a.record()
+            call(i)
+            b.record()
+    torch.cuda.synchronize()
+    us = sorted(1e3 * a.elapsed_time(b) for a, b in evs)
+    med = statistics.median(us)
+    nb = roofline.mm_bytes(1, HEAD_N, HEAD_K)
+    peak, _ = measured_peak()
+    del flush
+    return {"us_median": round(med, 3), "us_min": round(us[0], 3), "us_max": round(us[-1], 3), "calls": reps,
+            "GBps": round(nb / (med * 1e-6) / 1e9, 1), "frac": round(nb / (med * 1e-6) / 1e9 / peak, 4),
+            "method": f"fill of {2 * l2 / 1e6:.0f} MB (2x L2) before each call, events around the call alone"}
 
-    idx = {name: i for i, (name, N, K) in enumerate(DECODE_LAYER)}
 
-    def step(s):
+def measure_e2e(torch, ops, ws, steps, step_bytes, world, dist, wsel):
+    """Through the public API with HOST buffers, every step: pinned host ->
+    device copy of the activation row, one LM-head call, device -> pinned
+    host copy of the 262144 logits, and the synchronisation that read
+    implies."""
+    K, N = HEAD_K, HEAD_N
+    h_in = torch.empty(1, K, dtype=torch.bfloat16, pin_memory=True)
+    h_out = torch.empty(1, N, dtype=torch.bfloat16, pin_memory=True)
+    h_in.copy_(torch.randn(1, K).to(torch.bfloat16))
+    d_in = torch.empty(1, K, dtype=torch.bfloat16, device="cuda")
+    d_out = torch.empty(1, N, dtype=torch.bfloat16, device="cuda")
+    n = max(1, min(steps, 2000))
+
+    def step(s_):
         d_in.copy_(h_in, non_blocking=True)
-        layer = layers[s % len(layers)]
-        for _, names in launches:
-            if len(names) == 1:
-                ops.mm(ins[idx[names[0]]], layer[names[0]], out=outs[idx[names[0]]], kernel=kernel)
-            else:
-                ops.mm_group([ins[idx[n]] for n in names], [layer[n] for n in names], [outs[idx[n]] for n in names])
+        ops.mm(d_in, ws[s_ % len(ws)], out=d_out, workspace=wsel)
         h_out.copy_(d_out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
-    for s in range(min(50, n)):
-        step(s)
+    for s_ in range(min(20, n)):
+        step(s_)
     barrier(dist)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for s in range(n):
-        step(s)
+    for s_ in range(n):
+        step(s_)
     dt = max_over_ranks(dist, time.perf_counter() - t0)
     return {"value": round(world * step_bytes * n / dt / 1e9, 2), "unit": UNIT,
             "h2d_bytes_per_step": int(h_in.numel() * 2), "d2h_bytes_per_step": int(h_out.numel() * 2),
             "steps": n, "ms_per_step": round(1e3 * dt / n, 4),
-            "api": "skinny_gemm_gb300.ops.mm / mm_group (eager, the C ABI through ctypes)"}
+            "api": "skinny_gemm_gb300.ops.mm (eager, the C ABI through ctypes) with host copies"}
 
 
 def time_graph_launches(torch, fn_list, reps, min_calls=32):
@@ -521,8 +503,9 @@ def time_graph_launches(torch, fn_list, reps, min_calls=32):
     return a.elapsed_time(b) / (reps * rounds * len(fn_list))  # ms per call
 
 
-def measure_extras(torch, ops, synth, roofline, l2, kernel, peak):
-    """Context numbers on the other workloads (M = 1..8), cold weights."""
+def measure_extras(torch, ops, synth, roofline, l2, peak, args):
+    """Context numbers on the other workloads (M = 1..8), cold weights; each
+    timed as CUDA-graph replays of at least 32 calls over rotating copies."""
     out = {}
 
     def cold_set(N, K, seed):
@@ -532,30 +515,33 @@ def measure_extras(torch, ops, synth, roofline, l2, kernel, peak):
         base = ops.W4Matrix.from_host(hw)
         ws = [base] + [ops.W4Matrix(base.Wq.clone(), base.scales.clone(), base.biases.clone(), N, K)
                        for _ in range(copies - 1)]
+        torch.cuda.synchronize()
         return ws
 
-    def gbps(ws, M, N, K, reps):
+    def timed(ws, M, N, K, reps, **kw):
         x = torch.randn(M, K, device="cuda").to(torch.bfloat16)
         y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
-        fns = [lambda w=w: ops.mm(x, w, out=y, kernel=kernel) for w in ws]
-        ms = time_graph_launches(torch, fns, reps)
-        return ms, roofline.mm_bytes(M, N, K) / (ms * 1e-3) / 1e9
+        ms = time_graph_launches(torch, [lambda w=w: ops.mm(x, w, out=y, **kw) for w in ws], reps)
+        g = roofline.mm_bytes(M, N, K) / (ms * 1e-3) / 1e9
+        return {"us": round(1e3 * ms, 3), "GBps": round(g, 1), "frac": round(g / peak, 4)}
 
+    out["decode_layer"] = measure_decode_layer(torch, ops, synth, roofline, l2, min(args.steps, 2000),
+                                               max(3, min(args.warmup, 50)), peak)
     verify = {}
     for (N, K) in [(10240, 2560), (2560, 10240), (12288, 1536), (1536, 12288)]:
         ws = cold_set(N, K, 7)
-        t = {M: gbps(ws, M, N, K, 20) for M in (1, 3, 5, 7)}
-        verify[f"{N}x{K}"] = {f"M{M}_us": round(1e3 * t[M][0], 3) for M in t}
-        verify[f"{N}x{K}"].update({f"M{M}_GBps": round(t[M][1], 1) for M in t})
-        verify[f"{N}x{K}"]["t5_over_t1"] = round(t[5][0] / t[1][0], 3)
+        t = {M: timed(ws, M, N, K, 20) for M in (1, 3, 5, 7)}
+        verify[f"{N}x{K}"] = {f"M{M}_us": t[M]["us"] for M in t}
+        verify[f"{N}x{K}"].update({f"M{M}_GBps": t[M]["GBps"] for M in t})
+        verify[f"{N}x{K}"]["t5_over_t1"] = round(t[5]["us"] / t[1]["us"], 3)
         del ws
     out["verify"] = verify
     lm, lm_argmax = {}, {}
     for (N, K) in [(262144, 1536), (262144, 2560)]:
         ws = cold_set(N, K, 8)
         for M in (1, 3):
-            ms, g = gbps(ws, M, N, K, 10)
-            lm[f"{N}x{K}_M{M}"] = {"us": round(1e3 * ms, 2), "GBps": round(g, 1), "frac": round(g / peak, 4)}
+            lm[f"{N}x{K}_M{M}"] = timed(ws, M, N, K, 10)
+        lm[f"{N}x{K}_M1_no_workspace"] = timed(ws, 1, N, K, 10, workspace=None)
         # greedy head: w4a16_mm_argmax against w4a16_mm followed by torch.argmax over the logits
         for M in (1, 3):
             x = torch.randn(M, K, device="cuda").to(torch.bfloat16)
@@ -563,7 +549,7 @@ def measure_extras(torch, ops, synth, roofline, l2, kernel, peak):
             idx = torch.empty(M, dtype=torch.int32, device="cuda")
             val = torch.empty(M, dtype=torch.bfloat16, device="cuda")
             fused = [lambda w=w: ops.mm_argmax(x, w, idx=idx, val=val) for w in ws]
-            unfused = [lambda w=w: (ops.mm(x, w, out=y, kernel=kernel), torch.argmax(y, dim=-1)) for w in ws]
+            unfused = [lambda w=w: (ops.mm(x, w, out=y), torch.argmax(y, dim=-1)) for w in ws]
             ms_f = time_graph_launches(torch, fused, 10)
             ms_u = time_graph_launches(torch, unfused, 10)
             g = (roofline.mm_bytes(M, N, K) - 2 * M * N + 6 * M) / (ms_f * 1e-3) / 1e9  # no logits, idx + val out
@@ -585,8 +571,8 @@ def measure_extras(torch, ops, synth, roofline, l2, kernel, peak):
     dense = {}
     ws = cold_set(16384, 16384, 9)
     for M in (1, 2, 4, 8):
-        ms, g = gbps(ws, M, 16384, 16384, 10)
-        dense[f"M{M}"] = {"us": round(1e3 * ms, 2), "GBps": round(g, 1), "frac": round(g / peak, 4)}
+        dense[f"M{M}"] = timed(ws, M, 16384, 16384, 10)
+    dense["M1_no_workspace"] = timed(ws, 1, 16384, 16384, 10, workspace=None)
     del ws
     out["dense_16384"] = dense
     # routed experts: 8 x 6144x2048, 8 tokens, ids uniform on 0..7 (seed 0)
@@ -600,46 +586,74 @@ def measure_extras(torch, ops, synth, roofline, l2, kernel, peak):
     ids = torch.from_numpy(ids_np).cuda()
     x = torch.randn(T, K, device="cuda").to(torch.bfloat16)
     y = torch.empty(T, N, dtype=torch.bfloat16, device="cuda")
-    fns = [lambda w=w: ops.mm_id(x, w, ids, out=y, kernel=kernel) for w in ws]
-    ms = time_graph_launches(torch, fns, 20)
+    torch.cuda.synchronize()
+    ms = time_graph_launches(torch, [lambda w=w: ops.mm_id(x, w, ids, out=y) for w in ws], 20)
     nb, touched = roofline.mm_id_bytes(ids_np, T, N, K, E)
     out["routed"] = {"experts_touched": touched, "bytes": nb, "us": round(1e3 * ms, 2),
                      "GBps": round(nb / (ms * 1e-3) / 1e9, 1), "frac": round(nb / (ms * 1e-3) / 1e9 / peak, 4)}
     del ws
+    # K % 512 != 0: the CUDA-core family (a hidden-2304 gate 9216x2304 and a 256000x2304 LM head), M = 1 and 5
+    tail = {}
+    for (N, K) in [(9216, 2304), (256000, 2304)]:
+        ws = cold_set(N, K, 10)
+        t1, t5 = timed(ws, 1, N, K, 20), timed(ws, 5, N, K, 20)
+        tail[f"{N}x{K}"] = {"kernel": ops.get_plan(N, K)["kernel"], "M1": t1, "M5": t5,
+                            "t5_over_t1": round(t5["us"] / t1["us"], 3)}
+        del ws
+    out["tail_k_simt"] = tail
     out["stq1"] = measure_stq1(torch, ops, synth, roofline, l2, peak)
     return out
 
 
 # ---- the oracle as the CPU baseline / reference arm --------------------------------------
 
-def oracle_layer_pass(oracle, host, xs, cols_frac: float, threads: int):
-    """One oracle pass over a column sample of the decode layer; returns algorithmic bytes."""
+def oracle_head_pass(oracle, hw, xb, ncols: int, threads: int) -> int:
+    """The oracle on the first `ncols` output columns of the LM head at M = 1;
+    returns their algorithmic bytes."""
     from skinny_gemm_gb300 import roofline
-    total = 0
-    for name, N, K in DECODE_LAYER:
-        hw = host[name]
-        nc = max(1, int(round(N * cols_frac)))
-        cols = np.arange(nc, dtype=np.int64)
-        oracle.mm(xs[name], hw.Wq, hw.scales, hw.biases, 1, N, K, cols=cols, threads=threads)
-        total += roofline.mm_bytes(1, nc, K)
-    return total
+    cols = np.arange(ncols, dtype=np.int64)
+    oracle.mm(xb, hw.Wq, hw.scales, hw.biases, 1, hw.N, hw.K, cols=cols, threads=threads)
+    return roofline.mm_bytes(1, ncols, hw.K)
 
 
-def cpu_baseline(seconds: float):
+def oracle_one_core(oracle, synth, roofline, seconds: float) -> dict:
+    """The oracle on one core on the two smallest configurations: the tiny
+    256x512 matvec and the decode-layer projection set, both at M = 1."""
+    out = {}
+    sets = {"tiny_256x512": [(256, 512)], "decode_layer_set": [(N, K) for _, N, K in DECODE_LAYER]}
+    for name, shapes in sets.items():
+        mats = [(synth.make_weights(3 + i, N, K), synth.make_x(4 + i, 1, K)) for i, (N, K) in enumerate(shapes)]
+        t0, passes, nbytes = time.perf_counter(), 0, 0
+        while True:
+            for hw, xb in mats:
+                oracle.mm(xb, hw.Wq, hw.scales, hw.biases, 1, hw.N, hw.K, threads=1)
+                nbytes += roofline.mm_bytes(1, hw.N, hw.K)
+            passes += 1
+            if time.perf_counter() - t0 >= seconds:
+                break
+        dt = time.perf_counter() - t0
+        out[name] = {"GBps": round(nbytes / dt / 1e9, 5), "s_per_pass": round(dt / passes, 4), "passes": passes}
+    out["cores"] = 1
+    return out
+
+
+def cpu_baseline(seconds: float, hw):
     import oracle
-    from skinny_gemm_gb300 import synth
-    host = {name: synth.make_weights(i, N, K) for i, (name, N, K) in enumerate(DECODE_LAYER)}
-    xs = {name: synth.make_x(100 + i, 1, K) for i, (name, N, K) in enumerate(DECODE_LAYER)}
+    from skinny_gemm_gb300 import roofline, synth
+    xb = synth.make_x(2, 1, hw.K)
     threads = oracle.host_threads()
     t0 = time.perf_counter()
-    nbytes = oracle_layer_pass(oracle, host, xs, 1.0, threads)
-    passes = 1
-    while time.perf_counter() - t0 < seconds:
-        nbytes += oracle_layer_pass(oracle, host, xs, 1.0, threads)
+    nbytes, passes = 0, 0
+    while True:
+        nbytes += oracle_head_pass(oracle, hw, xb, hw.N, threads)
         passes += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
     dt = time.perf_counter() - t0
+    one = oracle_one_core(oracle, synth, roofline, 1.0)
     return {"value": round(nbytes / dt / 1e9, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{passes} full fp64 oracle passes over the decode-layer set at M=1 ({dt:.1f} s)"}
+            "sample": f"{passes} full fp64 oracle passes over the 262144x2560 LM head at M=1 ({dt:.1f} s)",
+            "one_core": one}
 
 
 def run_reference(args, world, rank, local):
@@ -647,28 +661,29 @@ def run_reference(args, world, rank, local):
         return
     import oracle
     from skinny_gemm_gb300 import synth
-    host = {name: synth.make_weights(i, N, K) for i, (name, N, K) in enumerate(DECODE_LAYER)}
-    xs = {name: synth.make_x(100 + i, 1, K) for i, (name, N, K) in enumerate(DECODE_LAYER)}
+    hw = synth.make_weights(1, HEAD_N, HEAD_K)
+    xb = synth.make_x(2, 1, HEAD_K)
     threads = oracle.host_threads()
     # size each step so warm-up + timed steps take about two minutes of CPU time
     t0 = time.perf_counter()
-    oracle_layer_pass(oracle, host, xs, 0.01, threads)
-    per_frac = (time.perf_counter() - t0) / 0.01
+    probe = 2048
+    oracle_head_pass(oracle, hw, xb, probe, threads)
+    per_col = (time.perf_counter() - t0) / probe
     budget = 120.0 / max(1, args.steps + args.warmup)
-    frac = min(1.0, max(1e-4, budget / max(per_frac, 1e-9)))
+    ncols = int(min(HEAD_N, max(64, budget / max(per_col, 1e-12))))
     for _ in range(args.warmup):
-        oracle_layer_pass(oracle, host, xs, frac, threads)
+        oracle_head_pass(oracle, hw, xb, ncols, threads)
     t0 = time.perf_counter()
     nbytes = 0
     for _ in range(args.steps):
-        nbytes += oracle_layer_pass(oracle, host, xs, frac, threads)
+        nbytes += oracle_head_pass(oracle, hw, xb, ncols, threads)
     dt = time.perf_counter() - t0
     value = nbytes / dt / 1e9
-    sample = f"first {frac:.4%} of the output columns of each decode-layer matrix per step, fp64 oracle"
+    sample = f"first {ncols} of the 262144 output columns of the LM head per step, fp64 oracle"
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": WORKLOAD, "M": 1, "group_size": 64},
+            "data": "synthetic", "config": dict(CONFIG),
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -698,7 +713,8 @@ def run_case(args):
         call = lambda w: ops.mm_id(x, w, ids, out=y, kernel=args.kernel)  # noqa: E731
         nbytes = roofline.mm_id_bytes(ids_np, M, N, K, E)[0]
     else:
-        call = lambda w: ops.mm(x, w, out=y, kernel=args.kernel)  # noqa: E731
+        wsel = None if args.no_workspace else "auto"
+        call = lambda w: ops.mm(x, w, out=y, kernel=args.kernel, workspace=wsel)  # noqa: E731
         nbytes = roofline.mm_bytes(M, N, K)
     for i in range(args.warmup):
         call(ws[i % copies])

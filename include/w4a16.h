@@ -39,10 +39,12 @@
  * w4a16_mm on the selected expert, bit for bit.
  *
  * Ownership and synchronisation.  All tensor pointers are DEVICE pointers
- * owned by the caller.  `stream` is a cudaStream_t (NULL = legacy default
- * stream).  Compute calls only enqueue work: they return before the GPU is
- * done and never synchronise, except w4a16_device_status and the one-time
- * workspace set-up below.
+ * owned by the caller, and the library allocates no device memory: no
+ * compute call calls cudaMalloc or keeps per-stream state, so every call
+ * (its first one included) may be captured into a CUDA graph.  `stream` is
+ * a cudaStream_t (NULL = legacy default stream).  Compute calls only
+ * enqueue work: they return before the GPU is done and never synchronise,
+ * except w4a16_device_status.
  *
  * Overlapped launches.  The tensor-core kernels are launched as programmatic
  * dependents: a call may start while the previous kernel on its stream is
@@ -55,19 +57,21 @@
  * them.  W4A16_PDL=1 keeps the overlap without the early fetch; 0 turns both
  * off.
  *
- * Workspace.  The tensor-core kernel's persistent grid deals its work units
- * through a counter in a workspace the library owns, one per (device,
- * stream), and when it splits K across warps of different SMs
- * (w4a16_get_plan: ksplit > 1 with that launch shape) it exchanges fp32
- * slice sums through the same workspace: 4.78 MiB, enough for every shape,
- * allocated with cudaMalloc (and its counters zeroed on the stream) by the
- * first call that needs it on that stream.  The tile kernel exchanges its
- * slice sums in shared memory and needs none.  w4a16_mm_argmax keeps its
- * keys there too.  It stays allocated until the process exits.  Calls
- * on one stream are ordered and share it safely; calls on different streams
- * use different workspaces.  A call that would need to allocate while its
- * stream is being captured into a CUDA graph fails with W4A16_ERR_CUDA, so
- * make one call on a stream before capturing it.
+ * Workspace (optional for w4a16_mm_ws, required by w4a16_mm_argmax).  A
+ * caller-owned block of device memory of w4a16_workspace_bytes(N, K) bytes
+ * (4.78 MiB, the same for every shape; 256-byte aligned) in which the
+ * persistent tensor-core grid keeps a unit counter shared by all its CTAs,
+ * the fp32 slice sums of a K split across SMs and the argmax keys.  The
+ * caller zeroes it once before its first use (cudaMemsetAsync); every call
+ * that completes leaves it zeroed again, and after w4a16_device_status
+ * reports W4A16_DEVICE_TIMEOUT it must be zeroed again.  Calls that share a
+ * workspace must not overlap on the GPU (one stream, or ordered by events).
+ * Without a workspace (w4a16_mm) the same arithmetic runs in shapes that
+ * need none: work units are dealt inside each CTA, and a K split across SMs
+ * becomes a cluster of CTAs adding the slice sums in distributed shared
+ * memory or, where a cluster cannot hold a tile's K range, whole-K units
+ * that fold the slice sums in registers.  The results are the same bits
+ * either way.
  *
  * Alignment.  x and Wq must be 16-byte aligned (their rows then are too,
  * because K % 64 == 0); scales and biases 8-byte aligned; y 2-byte; ids
@@ -82,6 +86,7 @@
 #ifndef W4A16_H
 #define W4A16_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -111,9 +116,10 @@ typedef enum {
                                identical bits */
   W4A16_KERNEL_VANILLA = 3, /* debug control: one thread per output, no sharing */
   W4A16_KERNEL_TC_STREAM = 4, /* tensor-core kernel, persistent grid: work units dealt to
-                                 warps (round-robin, or from a counter when K is split),
-                                 split-K through the workspace.  w4a16_mm_id: T <= 32 its
-                                 routed mode, more tokens a grid of tile x expert CTAs */
+                                 warps from a counter (in the CTA without a workspace);
+                                 without a workspace a split K runs as whole-K units.
+                                 w4a16_mm_id: T <= 32 its routed mode, more tokens a grid
+                                 of tile x expert CTAs */
   W4A16_KERNEL_TC_TILE = 5  /* tensor-core kernel, one CTA per 16-row tile holding the
                                tile's whole K range; needs that to fit in shared memory
                                (otherwise W4A16_ERR_KERNEL) */
@@ -121,9 +127,25 @@ typedef enum {
 
 /* y[M][N] = x[M][K] W^T.  M == 0 is a successful no-op.  The kernel family
  * is the dispatcher's choice for (N, K) unless the environment variable
- * W4A16_FORCE_KERNEL names one (simt, tc, vanilla). */
+ * W4A16_FORCE_KERNEL names one (simt, tc, vanilla).  Uses no workspace. */
 int w4a16_mm(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* scales,
              const w4a16_bf16* biases, w4a16_bf16* y, int M, int N, int K, void* stream);
+
+/* w4a16_mm with the caller's workspace (see "Workspace" above; NULL runs
+ * w4a16_mm).  With one, the persistent grid deals its units from one
+ * counter over all SMs and splits K across SMs where the canonical slicing
+ * has several slices (w4a16_get_plan: workspace_bytes > 0 and ksplit > 1):
+ * the fastest launch shape for large matrices.  Results equal w4a16_mm bit
+ * for bit.  A workspace smaller than w4a16_workspace_bytes(N, K) is
+ * W4A16_ERR_SHAPE, one not 256-byte aligned W4A16_ERR_ALIGN. */
+int w4a16_mm_ws(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* scales,
+                const w4a16_bf16* biases, w4a16_bf16* y, int M, int N, int K, void* workspace,
+                size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace the tensor-core family can use for (N, K): 0 when it
+ * does not apply (K % 512 != 0 or an invalid shape), otherwise a fixed
+ * 5,013,504 bytes (32 KiB of counters + 4864 KiB of fp32 partials). */
+size_t w4a16_workspace_bytes(int N, int K);
 
 /* w4a16_mm with an explicit kernel family (for A/B comparisons and tests). */
 int w4a16_mm_kernel(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* scales,
@@ -135,9 +157,10 @@ int w4a16_mm_kernel(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* s
  * Who needs it: code running inside an engine that reserved all device
  * memory at start-up and hands out nothing more, processes under a hard
  * device-memory cap where a late cudaMalloc could fail mid-service, and
- * deployments that forbid allocation after initialisation.  w4a16_mm may
- * cudaMalloc its split-K workspace on the first call on a stream; this
- * entry point never calls cudaMalloc, cudaFree or any allocating routine.
+ * deployments that forbid allocation after initialisation.  Like w4a16_mm
+ * it never calls cudaMalloc, cudaFree or any allocating routine; unlike
+ * w4a16_mm it always runs the persistent grid with a K split across SMs,
+ * its workspace being a fixed array inside the library.
  *
  * It runs the same tensor-core kernel with the same arithmetic, so its
  * results equal w4a16_mm's bit for bit.  Its split-K scratch is one fixed
@@ -149,7 +172,11 @@ int w4a16_mm_kernel(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* s
  *
  * The first call on a device looks up the array's device address and sets
  * the kernel's shared-memory limit; make that first call before any CUDA
- * graph capture.  All calls share the one array and it keeps the last
+ * graph capture.  Under CUDA's default lazy module loading the array itself
+ * is committed on the device when the library's kernels are first loaded,
+ * which for a process that calls nothing else is that first call: a caller
+ * under a hard memory cap makes it at start-up (or sets
+ * CUDA_MODULE_LOADING=EAGER), so that nothing is committed mid-service.  All calls share the one array and it keeps the last
  * call's contents: each call clears the counters it uses (a memset on
  * `stream`) before its kernel.  Calls whose executions overlap on the GPU
  * (different streams, or graphs replayed concurrently) race on the array;
@@ -167,11 +194,12 @@ int w4a16_mm_noalloc(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* 
  * -0 just below +0.
  * idx int32 [M] (4-byte aligned) and val bf16 [M] (may be NULL) are device
  * pointers.  Runs the persistent tensor-core kernel: needs K % 512 == 0
- * (otherwise W4A16_ERR_KERNEL).  Uses the per-(device, stream) workspace of
- * w4a16_mm (allocated on first use, as there); other errors as w4a16_mm. */
+ * (otherwise W4A16_ERR_KERNEL).  The CTAs merge their keys in the caller's
+ * workspace (see "Workspace" above; NULL is W4A16_ERR_NULL, too small
+ * W4A16_ERR_SHAPE); other errors as w4a16_mm. */
 int w4a16_mm_argmax(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* scales,
                     const w4a16_bf16* biases, int32_t* idx, w4a16_bf16* val, int M, int N, int K,
-                    void* stream);
+                    void* workspace, size_t workspace_bytes, void* stream);
 
 /* Grouped projections: several independent w4a16_mm calls that share K and
  * M, in one launch where that pays (a decoder layer's q/k/v projections read
@@ -261,7 +289,7 @@ int w4a16_dequant(const uint32_t* Wq, const w4a16_bf16* scales, const w4a16_bf16
  * reduced on its own and the slice sums are added in slice order.  Both
  * depend on (N, K) only, never on M.  The other fields describe the launch
  * of one chunk of at most eight activation rows on this device (152 SMs are
- * assumed when no GPU is present). */
+ * assumed when no GPU is present), for w4a16_mm_ws given a workspace. */
 typedef struct {
   int kernel;        /* w4a16_kernel actually used */
   int ksplit;        /* K-slices per output row */
@@ -271,6 +299,7 @@ typedef struct {
   int threads;       /* threads per CTA */
   int grid_x;        /* CTAs per chunk */
   int smem_bytes;    /* dynamic shared memory per CTA (M = 1) */
+  int workspace_bytes; /* workspace this launch shape uses when one is given (w4a16_mm_ws), else 0 */
 } w4a16_plan;
 
 int w4a16_get_plan(int N, int K, int kernel, w4a16_plan* out);

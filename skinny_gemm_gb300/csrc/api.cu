@@ -144,10 +144,22 @@ int validate_mm(const void* x, const void* Wq, const void* S, const void* B, con
   return W4A16_OK;
 }
 
+// A caller's workspace: NULL (none), or at least tc_workspace_bytes() bytes,
+// 256-byte aligned.
+int check_workspace(const void* ws, size_t bytes) {
+  if (!ws) return W4A16_OK;
+  if (misaligned(ws, 256)) return fail(W4A16_ERR_ALIGN, "the workspace must be 256-byte aligned");
+  if (bytes < tc_workspace_bytes())
+    return fail(W4A16_ERR_SHAPE, "a workspace of %zu bytes is too small (w4a16_workspace_bytes: %zu)", bytes,
+                tc_workspace_bytes());
+  return W4A16_OK;
+}
+
 int run_mm(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* S, const w4a16_bf16* B, w4a16_bf16* y,
-           int M, int N, int K, int kernel, void* stream) {
+           int M, int N, int K, int kernel, void* stream, void* ws = nullptr, size_t ws_bytes = 0) {
   if (env().fault == kFaultValidate) return fail(W4A16_ERR_SHAPE, "injected validation fault (W4A16_FAULT)");
   if (int rc = validate_mm(x, Wq, S, B, y, M, N, K)) return rc;
+  if (int rc = check_workspace(ws, ws_bytes)) return rc;
   w4a16_plan plan;
   if (int rc = resolve_kernel(kernel, N, K, &plan)) return rc;
   if (M == 0) return W4A16_OK;
@@ -158,6 +170,8 @@ int run_mm(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* S, const w
   a.stream = static_cast<cudaStream_t>(stream);
   a.pdl = env().pdl;
   a.tc_path = plan.kernel == W4A16_KERNEL_TC_STREAM ? 1 : plan.kernel == W4A16_KERNEL_TC_TILE ? 2 : 0;
+  a.ws = ws;
+  a.ws_bytes = ws_bytes;
   if (int rc = flag_pointer(&a.flags)) return rc;
   const bool tc = plan.kernel == W4A16_KERNEL_TC || plan.kernel == W4A16_KERNEL_TC_STREAM ||
                   plan.kernel == W4A16_KERNEL_TC_TILE;
@@ -194,6 +208,16 @@ extern "C" {
 int w4a16_mm(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* scales, const w4a16_bf16* biases,
              w4a16_bf16* y, int M, int N, int K, void* stream) {
   return run_mm(x, Wq, scales, biases, y, M, N, K, W4A16_KERNEL_AUTO, stream);
+}
+
+int w4a16_mm_ws(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* scales, const w4a16_bf16* biases,
+                w4a16_bf16* y, int M, int N, int K, void* workspace, size_t workspace_bytes, void* stream) {
+  return run_mm(x, Wq, scales, biases, y, M, N, K, W4A16_KERNEL_AUTO, stream, workspace, workspace_bytes);
+}
+
+size_t w4a16_workspace_bytes(int N, int K) {
+  if (N <= 0 || K <= 0 || K % kGroup || !tc_supported(N, K)) return 0;
+  return tc_workspace_bytes();
 }
 
 int w4a16_mm_kernel(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* scales, const w4a16_bf16* biases,
@@ -314,10 +338,13 @@ int w4a16_mm_noalloc(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* 
 }
 
 int w4a16_mm_argmax(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* scales, const w4a16_bf16* biases,
-                    int32_t* idx, w4a16_bf16* val, int M, int N, int K, void* stream) {
+                    int32_t* idx, w4a16_bf16* val, int M, int N, int K, void* workspace, size_t workspace_bytes,
+                    void* stream) {
   if (env().fault == kFaultValidate) return fail(W4A16_ERR_SHAPE, "injected validation fault (W4A16_FAULT)");
   if (int rc = validate_mm(x, Wq, scales, biases, idx, M, N, K)) return rc;
   if (M == 0) return W4A16_OK;
+  if (!workspace) return fail(W4A16_ERR_NULL, "w4a16_mm_argmax needs a workspace (w4a16_workspace_bytes)");
+  if (int rc = check_workspace(workspace, workspace_bytes)) return rc;
   if (misaligned(idx, 4) || misaligned(val, 2)) return fail(W4A16_ERR_ALIGN, "idx must be 4-byte and val 2-byte aligned");
   if (!tc_supported(N, K))
     return fail(W4A16_ERR_KERNEL, "w4a16_mm_argmax runs the tensor-core kernel, which needs K %% 512 == 0 (K = %d)", K);
@@ -328,6 +355,8 @@ int w4a16_mm_argmax(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* s
   a.stream = static_cast<cudaStream_t>(stream);
   a.pdl = env().pdl;
   a.tc_path = 1;
+  a.ws = workspace;
+  a.ws_bytes = workspace_bytes;
   if (int rc = flag_pointer(&a.flags)) return rc;
   for (int row0 = 0; row0 < M; row0 += kMaxChunk) {
     a.row0 = row0;

@@ -151,6 +151,7 @@ void plan_vanilla(int N, int K, w4a16_plan* p) {
   p->grid_x = (N + 127) / 128;
   p->units = p->grid_x;
   p->smem_bytes = 0;
+  p->workspace_bytes = 0;
 }
 
 cudaError_t launch_vanilla(const LaunchArgs& a, const w4a16_plan& p) {

@@ -31,6 +31,8 @@ struct LaunchArgs {
   int pdl;             // 0: plain launch; 1: programmatic dependent launch; 2: and weights fetched before the wait
   int tc_path;         // tensor-core launch shape: 0 the dispatcher's choice, 1 persistent, 2 tile
   cudaStream_t stream;
+  void* ws = nullptr;  // the caller's workspace (w4a16_mm_ws, w4a16_mm_argmax), or none
+  size_t ws_bytes = 0;
 };
 
 // Per-family planning (depends on N and K only) and launching.
@@ -59,6 +61,8 @@ bool tc_group_supported(const int* N, int count, int K);
 // M rows in one launch, eight at a time over resident weights.
 cudaError_t launch_tc_group(const GroupItem* items, int count, int M, int row0, int K, int pdl, int* flags,
                             cudaStream_t stream);
+// Bytes of the persistent kernel's workspace (counters, split-K partials, argmax keys).
+size_t tc_workspace_bytes();
 // Tensor-core w4a16_mm with its split-K scratch in a fixed device array (no allocation).
 cudaError_t launch_tc_noalloc(const LaunchArgs& a);
 size_t tc_noalloc_scratch_bytes();

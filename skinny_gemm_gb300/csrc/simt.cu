@@ -232,6 +232,7 @@ void plan_simt(int N, int K, w4a16_plan* p) {
   p->grid_x = (int)((N + rows_per_cta - 1) / rows_per_cta);
   p->units = p->grid_x;
   p->smem_bytes = 0;
+  p->workspace_bytes = 0;
 }
 
 cudaError_t launch_simt(const LaunchArgs& a, const w4a16_plan& p) {

@@ -651,14 +651,22 @@ __device__ __forceinline__ void build_chunks(const int32_t* __restrict__ ids, in
 // largest key of each activation row over its units, the CTAs merge theirs
 // with 64-bit atomic maxima, and the last CTA out writes the argmax of every
 // row (the outputs' bits are those w4a16_mm stores).
-template <int NSUB, bool ALLCOLS, bool XSTAGED, bool SPLIT, bool ROUTED = false, bool ARGMAX = false>
+template <int NSUB, bool ALLCOLS, bool XSTAGED, bool SPLIT, bool ROUTED = false, bool ARGMAX = false,
+          bool WHOLEK = false>
 __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_min_blocks<NSUB>()) tc_stream_kernel(
     const __grid_constant__ Maps maps, StreamParams p) {
   using G = Geo<NSUB>;
   constexpr int kW = G::kWarps, kRows = G::kRows;
   static_assert(!ROUTED || (!XSTAGED && !SPLIT), "the routed mode copies activations per stage, whole-K units");
   static_assert(!ARGMAX || (!ROUTED && NSUB == 2), "argmax over plain 32-row units");
+  static_assert(!WHOLEK || (!ROUTED && !SPLIT && !ARGMAX), "whole-K units are a plain-mode schedule");
   constexpr bool DYN = (SPLIT || W4A16_TC_DYN_ALL) && !ROUTED;  // units after the first from the counter
+  constexpr bool FOLD = ROUTED || WHOLEK;  // whole-K units: slice sums folded in registers, in slice order
+  // Without a workspace (p.sched == nullptr) the units are dealt inside each
+  // CTA: CTA c owns the contiguous units [c U / grid, (c + 1) U / grid) and
+  // its warps take them from a shared-memory counter.  With one, from a
+  // counter shared by the whole grid.
+  const bool local = p.sched == nullptr;
   extern __shared__ uint8_t smem_raw[];
   pdl_launch_dependents();
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -694,12 +702,19 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
       reinterpret_cast<unsigned long long*>(base + (xst - smem_u32(base)) + (XSTAGED ? xstage_bytes(mc, p.K) : 0));
   unsigned long long* s_cta_best = s_best + 8 * 8;
   if (ARGMAX && threadIdx.x < 8 * 8 + 8) s_best[threadIdx.x] = 0ull;
+  int* s_grab = s_tok + kMaxChunk + 8 * 8 + 2;  // the CTA's own unit counter (no workspace)
+  if (threadIdx.x == 0) *s_grab = 0;
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   __syncthreads();
 
   // warp-major numbering: the first pass over the units spreads them evenly over CTAs
   const int gw = warp * gridDim.x + blockIdx.x;
   const int TW = gridDim.x * kW;
+  // dealing inside the CTA (no workspace): its range, first unit and stride
+  const bool own = !ROUTED && local;
+  const int cta_lo = own ? (int)((int64_t)blockIdx.x * p.units / gridDim.x) : 0;
+  const int cta_hi = own ? (int)((int64_t)(blockIdx.x + 1) * p.units / gridDim.x) : p.units;
+  const int first_u = own ? cta_lo + warp : gw;
 
   // Work units of this warp.  The first is static (unit gw), so its weights
   // can be requested before the wait for earlier kernels.  With DYN every
@@ -715,7 +730,9 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   // makes exactly max(0, units - TW) + min(TW, units) grabs; the one that
   // draws the last count resets the counter for the next launch.  A grab's
   // count is only looked at when its unit begins, a stage or two later, so
-  // the atomic's round trip does not stall the warp.
+  // the atomic's round trip does not stall the warp.  Dealt inside the CTA
+  // the same happens with the CTA's range and a shared-memory counter,
+  // which needs no reset.
   int* s_units = s_tok + kMaxChunk + 8 * warp;
   int units = p.units;             // routed mode: set from the chunk table
   int iu = -1, ist = 0, iend = 0;  // lane 0: unit being issued, its stage cursor
@@ -729,8 +746,12 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   // one, or two for units of three stages or fewer (LM head 262144x1536:
   // 41.8 -> 41.5 us; one is best from five stages on: 262144x2560, 16384^2).
   const int lead = p.sl <= 3 ? 2 : 1;
-  auto grab = [&]() { return atomicAdd(p.sched, 1); };
+  auto grab = [&]() { return own ? atomicAdd(s_grab, 1) : atomicAdd(p.sched, 1); };
   auto resolve = [&](int c) {  // the unit of grab count c, -1 past the end
+    if (own) {
+      const int v = cta_lo + kW + c;
+      return v < cta_hi ? v : -1;
+    }
     if (c == last_grab) *p.sched = 0;
     const int v = TW + c;
     return v < p.units ? v : -1;
@@ -745,6 +766,10 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
         irow = ch[0] * p.N + (u - c * p.tiles) * kRows;  // row of the stacked [E][N] weights
         imc = ch[1];
         itok = ch + 2;
+        ist = 0;
+        iend = p.nst;
+      } else if (WHOLEK) {
+        irow = u * kRows;
         ist = 0;
         iend = p.nst;
       } else {
@@ -766,6 +791,8 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
       if (DYN) {
         begin_unit(resolve(nxt));
         nxt = -1;
+      } else if (own) {
+        begin_unit(iu + kW < cta_hi ? iu + kW : -1);
       } else {
         begin_unit(iu + TW < units ? iu + TW : -1);
       }
@@ -782,7 +809,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   if (lane == 0) {
     fence_proxy_async();
     if (!ROUTED) {
-      begin_unit(gw < units ? gw : -1);
+      begin_unit(first_u < cta_hi ? first_u : -1);
       if (p.prefetch)
         for (int i = 0; i < S && iu >= 0 && ist < iend; ++i) issue_stage(false);
     }
@@ -959,15 +986,15 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
 
   // consume cursor: round-robin units follow from gw; dealt ones are read
   // in the order lane 0 recorded them
-  int u = gw;
+  int u = first_u;
   for (uint32_t cseq = 0; !timed_out; ++cseq) {
     if (DYN) {
       __syncwarp();
       u = s_units[cseq & 7u];
     } else if (cseq > 0) {
-      u += TW;
+      u += own ? kW : TW;
     }
-    if (u < 0 || u >= units) break;
+    if (u < 0 || u >= (own ? cta_hi : units)) break;
     int slice = 0, tile, umc = mc;
     const int* utok = s_tok;
     if (ROUTED) {
@@ -979,7 +1006,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
     } else {
       tile = unit_tile<SPLIT>(p, u, slice);
     }
-    const int s0 = ROUTED ? 0 : slice * p.sl, s1 = ROUTED ? p.nst : min(s0 + p.sl, p.nst);
+    const int s0 = FOLD ? 0 : slice * p.sl, s1 = FOLD ? p.nst : min(s0 + p.sl, p.nst);
     // The last slice of a tile reads the tile's arrival count before its
     // stages (the value is used after them, so the load never stalls).
     const bool last_slice = SPLIT && slice == p.ks - 1;
@@ -993,7 +1020,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
     for (int s = 0; s < NSUB; ++s)
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[s][i] = 0.0f;
-    float sum[NSUB][4];       // routed mode: the slice sums folded so far, in slice order
+    float sum[NSUB][4];       // whole-K units: the slice sums folded so far, in slice order
     int fold_at = s0 + p.sl;  // and the stage that ends the current slice
 
     for (int st = s0; st < s1; ++st) {
@@ -1012,7 +1039,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
       }
       compute_stage<NSUB, ALLCOLS, XSTAGED>(cbase, cbase + 2 * G::kBox, xbase, g < umc, sxbase, sx_cols(mc) * 4,
                                             2 * t < umc, acc, loff, g);
-      if (ROUTED && (st + 1 == fold_at || st + 1 == s1)) {
+      if (FOLD && (st + 1 == fold_at || st + 1 == s1)) {
         const bool first = fold_at == s0 + p.sl;
 #pragma unroll
         for (int s = 0; s < NSUB; ++s)
@@ -1045,7 +1072,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
       count_arrival(pend_tile);
       pend_tile = -1;
     }
-    if (ROUTED) {
+    if (FOLD) {  // routed rows go to their tokens; plain rows to row0 + n
 #pragma unroll
       for (int s = 0; s < NSUB; ++s)
 #pragma unroll
@@ -1114,7 +1141,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
     if (lane == 0) atomicOr(p.flags, W4A16_DEVICE_TIMEOUT);
     // finish this warp's grabs (up to the one that fails), so the count of
     // grabs stays exact and the counter is reset
-    if (DYN && lane == 0 && iu >= 0)
+    if (DYN && !own && lane == 0 && iu >= 0)
       for (int v = nxt >= 0 ? resolve(nxt) : 0; v >= 0; v = resolve(grab())) {
       }
     // let copies already in flight land before shared memory is released
@@ -1718,11 +1745,11 @@ cudaError_t launch_ex(Kern fn, dim3 grid, dim3 block, int smem, cudaStream_t str
   return cudaLaunchKernelEx(&cfg, fn, args...);
 }
 
-template <int NSUB, bool A, bool X, bool SPLIT, bool ARGMAX = false>
+template <int NSUB, bool A, bool X, bool SPLIT, bool ARGMAX = false, bool WHOLEK = false>
 cudaError_t stream_launch_t(const Maps& map, const StreamParams& p, int sms, int smem, DeviceInfo& d,
                             cudaStream_t stream, bool pdl) {
   constexpr int kW = Geo<NSUB>::kWarps;
-  auto* fn = tc_stream_kernel<NSUB, A, X, SPLIT, false, ARGMAX>;
+  auto* fn = tc_stream_kernel<NSUB, A, X, SPLIT, false, ARGMAX, WHOLEK>;
   if (cudaError_t e = allow_smem(fn, d)) return e;
   int per_sm = 0;
   if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kW * 32, smem)) return e;
@@ -1748,7 +1775,14 @@ cudaError_t launch_stream_t(const Maps& map, StreamParams p, int sms, DeviceInfo
   if (staged) smem += xstage_bytes(p.M, p.K);
   const bool on = pdl > 0;
   using Fn = cudaError_t (*)(const Maps&, const StreamParams&, int, int, DeviceInfo&, cudaStream_t, bool);
-  const bool split = p.ks > 1;
+  const bool split = p.ks > 1 && p.part != nullptr;
+  if (p.ks > 1 && !split) {  // no workspace: whole-K units, the slice sums folded in registers
+    static const Fn fold[2][2] = {{stream_launch_t<NSUB, false, false, false, false, true>,
+                                   stream_launch_t<NSUB, false, true, false, false, true>},
+                                  {stream_launch_t<NSUB, true, false, false, false, true>,
+                                   stream_launch_t<NSUB, true, true, false, false, true>}};
+    return fold[allcols][staged](map, p, sms, smem, d, stream, on);
+  }
   if (p.idx) {  // argmax mode (32-row warps only)
     if (NSUB != 2) return cudaErrorInvalidConfiguration;
     // [allcols][staged][split]
@@ -1949,7 +1983,7 @@ bool workspace_fits(const Shape& s, const StreamWork& w) {
 cudaError_t launch_stream(const Maps& maps, StreamParams p, const StreamWork& w, DeviceInfo& d,
                           cudaStream_t stream, int pdl) {
   p.tiles = w.tiles;
-  p.units = w.units;
+  p.units = p.ks > 1 && !p.part ? w.tiles : w.units;  // whole-K units without a workspace
   p.kfull = p.nst % p.sl == 0 ? p.ks : p.ks - 1;
 #if W4A16_TC_STREAM_NSUB1_MIN_M <= 8  // else no chunk (8 rows at most) takes 16-row warps
   if (w.nsub == 1) return launch_stream_t<1>(maps, p, d.sms, d, stream, pdl);
@@ -1957,32 +1991,19 @@ cudaError_t launch_stream(const Maps& maps, StreamParams p, const StreamWork& w,
   return launch_stream_t<2>(maps, p, d.sms, d, stream, pdl);
 }
 
-struct Workspace {
-  void* ptr = nullptr;
-};
-std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
-
-cudaError_t workspace(int dev, cudaStream_t stream, void** out) {
-  Workspace& w = g_ws[{dev, stream}];
-  if (w.ptr) {
-    *out = w.ptr;
-    return cudaSuccess;
-  }
-  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(stream, &cs) == cudaSuccess && cs != cudaStreamCaptureStatusNone)
-    return cudaErrorStreamCaptureUnsupported;  // allocate only outside capture
-  void* p = nullptr;
-  if (cudaError_t e = cudaMalloc(&p, kWsBytes)) return e;
-  if (cudaError_t e = cudaMemsetAsync(p, 0, kWsCounterBytes, stream)) {
-    cudaFree(p);
-    return e;
-  }
-  w.ptr = p;
-  *out = p;
-  return cudaSuccess;
+// Point the persistent kernel's counters, partials and argmax keys into a
+// caller's workspace of kWsBytes.
+void use_workspace(StreamParams& p, void* ws) {
+  p.cnt = static_cast<int*>(ws);
+  p.sched = p.cnt + kWsSched;
+  p.done = p.cnt + kWsSched + 1;
+  p.best = reinterpret_cast<unsigned long long*>(p.cnt + kWsBest);
+  p.part = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsCounterBytes);
 }
 
 }  // namespace
+
+size_t tc_workspace_bytes() { return kWsBytes; }
 
 bool tc_supported(int N, int K) {
   (void)N;
@@ -2007,6 +2028,7 @@ void plan_tc(int N, int K, int tc_path, w4a16_plan* p) {
   p->units = s.units;
   p->kernel = tc_path == 1 ? W4A16_KERNEL_TC_STREAM : tc_path == 2 ? W4A16_KERNEL_TC_TILE : W4A16_KERNEL_TC;
   const TilePlan tp = tc_path == 1 ? TilePlan() : tile_plan(s, N, 1, tc_path == 2);
+  p->workspace_bytes = 0;
   if (tp.kc > 0) {  // clusters of kc CTAs per 16-row tile
     p->rows_per_tile = kTile16;
     p->threads = tp.warps * 32;
@@ -2014,6 +2036,7 @@ void plan_tc(int N, int K, int tc_path, w4a16_plan* p) {
     p->smem_bytes = tp.smem;
     return;
   }
+  p->workspace_bytes = (int)kWsBytes;
   const StreamWork w = stream_work(s, N, 1);
   int smem, warps;
   if (w.nsub == 1) {
@@ -2054,19 +2077,26 @@ cudaError_t launch_tc_impl(const LaunchArgs& a, int32_t* idx, uint16_t* val) {
   p.sched = nullptr;
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DeviceInfo& d = device_info(dev);
+  const bool have_ws = a.ws != nullptr && a.ws_bytes >= kWsBytes;
+  if (idx && !have_ws) return cudaErrorInvalidValue;  // the argmax mode merges its keys in the workspace
   if (a.tc_path != 1 && !idx) {
     // one launch for all M rows: eight at a time over the resident weights
     const TilePlan tp = tile_plan(s, a.N, min(a.M, kMaxChunk), a.tc_path == 2, d.sms);
     if (tp.kc > 0) return launch_tile(a, s, tp, d, false);
     if (a.tc_path == 2) return cudaErrorInvalidConfiguration;
+    // K split over SMs needs the workspace; without one, the tile kernel's
+    // clusters add the slice sums in distributed shared memory where a
+    // cluster can hold a tile's K range
+    if (s.ks > 1 && !have_ws) {
+      const TilePlan tf = tile_plan(s, a.N, min(a.M, kMaxChunk), true, d.sms);
+      if (tf.kc > 0) return launch_tile(a, s, tf, d, false);
+    }
   }
-  void* ws = nullptr;
-  if (cudaError_t e = workspace(dev, a.stream, &ws)) return e;
-  p.cnt = static_cast<int*>(ws);
-  p.sched = p.cnt + kWsSched;
-  p.done = p.cnt + kWsSched + 1;
-  p.best = reinterpret_cast<unsigned long long*>(p.cnt + kWsBest);
-  p.part = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsCounterBytes);
+  // Persistent kernel.  With a workspace: units dealt over the whole grid
+  // from its counter, K split over SMs through its partials.  Without:
+  // units dealt inside each CTA, and a split K taken by whole-K units that
+  // fold the slice sums in registers (the same canonical sums).
+  if (have_ws) use_workspace(p, a.ws);
   // the persistent kernel: one launch per chunk of at most eight rows
   for (int r0 = 0; r0 < a.M; r0 += kMaxChunk) {
     p.row0 = a.row0 + r0;
@@ -2074,7 +2104,7 @@ cudaError_t launch_tc_impl(const LaunchArgs& a, int32_t* idx, uint16_t* val) {
     const StreamWork w = stream_work(s, a.N, p.M);
     Maps maps;
     if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, a.N, a.K, w.rows)) return e;
-    if (!workspace_fits(s, w)) return cudaErrorInvalidValue;
+    if (p.part && !workspace_fits(s, w)) return cudaErrorInvalidValue;
     if (cudaError_t e = launch_stream(maps, p, w, d, a.stream, a.pdl)) return e;
   }
   return cudaSuccess;

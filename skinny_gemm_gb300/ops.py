@@ -27,7 +27,7 @@ KERNELS = {"auto": 0, "simt": 1, "tc": 2, "vanilla": 3, "tc_stream": 4, "tc_tile
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 DEVICE_BAD_ID = 1
 
-EXPORTS = ("w4a16_mm", "w4a16_mm_kernel", "w4a16_mm_group", "w4a16_mm_argmax", "w4a16_embed", "w4a16_expand_groups",
+EXPORTS = ("w4a16_mm", "w4a16_mm_ws", "w4a16_workspace_bytes", "w4a16_mm_kernel", "w4a16_mm_noalloc", "w4a16_mm_group", "w4a16_mm_argmax", "w4a16_embed", "w4a16_expand_groups",
            "w4a16_mm_id", "w4a16_mm_id_kernel", "w4a16_unpack", "w4a16_dequant", "w4a16_get_plan", "w4a16_device_status", "w4a16_last_error",
            "w4a16_debug_reload_env", "w4a16_version",
            "stq1_packed_bytes", "stq1_pack", "stq1_mm", "stq1_mm_id", "stq1_get_rows", "stq1_get_plan")
@@ -50,7 +50,7 @@ class W4A16ValueError(W4A16Error, ValueError):
 class Plan(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int), ("ksplit", ctypes.c_int), ("slice_k", ctypes.c_int),
                 ("rows_per_tile", ctypes.c_int), ("units", ctypes.c_int), ("threads", ctypes.c_int),
-                ("grid_x", ctypes.c_int), ("smem_bytes", ctypes.c_int)]
+                ("grid_x", ctypes.c_int), ("smem_bytes", ctypes.c_int), ("workspace_bytes", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         d = {f: getattr(self, f) for f, _ in self._fields_}
@@ -83,12 +83,15 @@ def lib() -> ctypes.CDLL:
         if _lib is None:
             path = _build.build_cuda()
             L = ctypes.CDLL(path)
-            P, i = ctypes.c_void_p, ctypes.c_int
+            P, i, z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
             L.w4a16_mm.argtypes = [P, P, P, P, P, i, i, i, P]
+            L.w4a16_mm_ws.argtypes = [P, P, P, P, P, i, i, i, P, z, P]
+            L.w4a16_workspace_bytes.argtypes = [i, i]
+            L.w4a16_workspace_bytes.restype = z
             L.w4a16_mm_kernel.argtypes = [P, P, P, P, P, i, i, i, i, P]
             L.w4a16_mm_noalloc.argtypes = [P, P, P, P, P, i, i, i, P]
             L.w4a16_mm_group.argtypes = [ctypes.POINTER(Item), i, i, i, P]
-            L.w4a16_mm_argmax.argtypes = [P, P, P, P, P, P, i, i, i, P]
+            L.w4a16_mm_argmax.argtypes = [P, P, P, P, P, P, i, i, i, P, z, P]
             L.w4a16_embed.argtypes = [P, P, P, P, P, i, i, i, P]
             L.w4a16_expand_groups.argtypes = [P, P, i, i, i, P]
             L.w4a16_mm_id.argtypes = [P, P, P, P, P, P, i, i, i, i, P]
@@ -104,7 +107,7 @@ def lib() -> ctypes.CDLL:
             L.stq1_mm_id.argtypes = [P, P, P, P, i, i, i, i, P]
             L.stq1_get_rows.argtypes = [P, P, P, i, i, i, P]
             L.stq1_get_plan.argtypes = [i, i, ctypes.POINTER(Stq1Plan)]
-            for f in ("w4a16_mm", "w4a16_mm_kernel", "w4a16_mm_noalloc", "w4a16_mm_group", "w4a16_mm_argmax",
+            for f in ("w4a16_mm", "w4a16_mm_ws", "w4a16_mm_kernel", "w4a16_mm_noalloc", "w4a16_mm_group", "w4a16_mm_argmax",
                       "w4a16_embed", "w4a16_expand_groups", "w4a16_mm_id", "w4a16_mm_id_kernel", "w4a16_unpack", "w4a16_dequant",
                       "w4a16_get_plan", "w4a16_device_status", "stq1_pack", "stq1_mm", "stq1_mm_id", "stq1_get_rows",
                       "stq1_get_plan"):
@@ -140,6 +143,50 @@ def _dev_tensor(t: torch.Tensor, dtype: torch.dtype, name: str) -> torch.Tensor:
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     return t
+
+
+# ---- workspaces (include/w4a16.h "Workspace") --------------------------------------------
+#
+# The library allocates nothing; this binding is its caller and owns the
+# workspaces: one zeroed block per (device, stream), made with torch on the
+# first call on that stream outside graph capture (a call captured before
+# one exists runs without a workspace, which gives the same bits).
+
+_ws_lock = threading.Lock()
+_ws_cache: dict = {}
+
+
+def workspace_bytes(N: int, K: int) -> int:
+    return int(lib().w4a16_workspace_bytes(N, K))
+
+
+def _capturing() -> bool:
+    try:
+        return bool(torch.cuda.is_current_stream_capturing())
+    except Exception:
+        return False
+
+
+def workspace(stream=None, create: bool = True):
+    """The zeroed workspace of the current device and `stream` (uint8 tensor),
+    or None when there is none yet and one cannot be made now."""
+    s = stream if stream is not None else torch.cuda.current_stream()
+    key = (s.device.index if s.device.index is not None else torch.cuda.current_device(), int(s.cuda_stream))
+    with _ws_lock:
+        ws = _ws_cache.get(key)
+        if ws is None and create and not _capturing():
+            n = int(lib().w4a16_workspace_bytes(512, 512))
+            ws = torch.zeros(n, dtype=torch.uint8, device=f"cuda:{key[0]}")
+            torch.cuda.current_stream(ws.device).synchronize()
+            _ws_cache[key] = ws
+        return ws
+
+
+def _ws_args(ws):
+    if ws is None:
+        return None, 0
+    _dev_tensor(ws, torch.uint8, "workspace")
+    return ws.data_ptr(), ws.numel()
 
 
 def _kernel_id(kernel) -> int:
@@ -214,8 +261,12 @@ class W4Matrix:
         return sum(t.numel() * t.element_size() for t in (self.Wq, self.scales, self.biases))
 
 
-def mm(x: torch.Tensor, w: W4Matrix, out: torch.Tensor | None = None, kernel=None, stream=None) -> torch.Tensor:
-    """y[..., N] = x[..., K] W^T through ``w4a16_mm`` (leading dims flatten into M)."""
+def mm(x: torch.Tensor, w: W4Matrix, out: torch.Tensor | None = None, kernel=None, stream=None,
+       workspace="auto") -> torch.Tensor:
+    """y[..., N] = x[..., K] W^T (leading dims flatten into M) through
+    ``w4a16_mm_ws`` with this stream's workspace (``workspace="auto"``), a
+    given uint8 workspace tensor, or ``w4a16_mm`` (``workspace=None``); an
+    explicit ``kernel`` goes through ``w4a16_mm_kernel`` without one."""
     if w.E != 1:
         raise ValueError("mm takes a single matrix; use mm_id for stacked experts")
     _dev_tensor(x, torch.bfloat16, "x")
@@ -230,21 +281,27 @@ def mm(x: torch.Tensor, w: W4Matrix, out: torch.Tensor | None = None, kernel=Non
     L = lib()
     k = _kernel_id(kernel)
     args = (x.data_ptr(), w.Wq.data_ptr(), w.scales.data_ptr(), w.biases.data_ptr(), out.data_ptr(), M, w.N, w.K)
-    if k == 0:
-        rc = L.w4a16_mm(*args, _stream_ptr(stream))
-    else:
+    if k != 0:
         rc = L.w4a16_mm_kernel(*args, k, _stream_ptr(stream))
+    else:
+        ws = globals()["workspace"](stream) if isinstance(workspace, str) else workspace
+        if ws is None:
+            rc = L.w4a16_mm(*args, _stream_ptr(stream))
+        else:
+            rc = L.w4a16_mm_ws(*args, *_ws_args(ws), _stream_ptr(stream))
     _raise(rc)
     return out
 
 
 def mm_argmax(x: torch.Tensor, w: W4Matrix, idx: torch.Tensor | None = None, val: torch.Tensor | None = None,
-              stream=None):
+              stream=None, workspace="auto"):
     """(idx, val) through ``w4a16_mm_argmax``: for every row of x (leading dims
     flatten into M) the index of the largest output of ``mm(x, w)`` and that
     output (ties to the smallest index), without writing the outputs.
 
-    idx is int32 [..], val bf16 [..]; pass ``val=False`` to skip the values."""
+    idx is int32 [..], val bf16 [..]; pass ``val=False`` to skip the values.
+    The call needs a workspace: this stream's (``"auto"``; make one call on
+    the stream before capturing it into a CUDA graph) or a given one."""
     if w.E != 1:
         raise ValueError("mm_argmax takes a single matrix")
     _dev_tensor(x, torch.bfloat16, "x")
@@ -263,8 +320,12 @@ def mm_argmax(x: torch.Tensor, w: W4Matrix, idx: torch.Tensor | None = None, val
         if val.numel() != M:
             raise ValueError("val must have one element per row")
     vp = val.data_ptr() if val is not False else None
+    ws = globals()["workspace"](stream) if isinstance(workspace, str) else workspace
+    if ws is None and M > 0:
+        raise ValueError("mm_argmax needs a workspace: call it once on this stream before graph capture, "
+                         "or pass workspace=")
     rc = lib().w4a16_mm_argmax(x.data_ptr(), w.Wq.data_ptr(), w.scales.data_ptr(), w.biases.data_ptr(), idx.data_ptr(),
-                               vp, M, w.N, w.K, _stream_ptr(stream))
+                               vp, M, w.N, w.K, *_ws_args(ws), _stream_ptr(stream))
     _raise(rc)
     return idx, (val if val is not False else None)
 

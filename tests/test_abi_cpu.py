@@ -15,7 +15,7 @@ import pytest
 from skinny_gemm_gb300 import _build, ops, synth
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-DECL = re.compile(r"^\s*(?:int|void|const char\s*\*)\s+(w4a16_\w+)\s*\(", re.M)
+DECL = re.compile(r"^\s*(?:int|void|size_t|const char\s*\*)\s+(w4a16_\w+)\s*\(", re.M)
 STQ1_DECL = re.compile(r"^\s*(?:int|size_t)\s+(stq1_\w+)\s*\(", re.M)
 
 P = 0x10000  # 16-byte-aligned fake address
@@ -112,14 +112,40 @@ def test_mm_id_errors(L):
 def test_mm_argmax_errors(L):
     """Fail-closed checks of w4a16_mm_argmax, all before any device call."""
     f = L.w4a16_mm_argmax
-    assert f(P, P, P, P, P, P, 0, 64, 512, None) == ops.OK          # M == 0: no-op
-    assert f(P, P, P, P, P, None, -1, 64, 512, None) == ops.ERR_SHAPE
-    assert f(P, P, P, P, P, P, 1, 64, 96, None) == ops.ERR_SHAPE    # K % 64
-    assert f(P, P, P, P, None, P, 1, 64, 512, None) == ops.ERR_NULL  # idx
-    assert f(P + 8, P, P, P, P, P, 1, 64, 512, None) == ops.ERR_ALIGN
-    assert f(P, P, P, P, P + 2, P, 1, 64, 512, None) == ops.ERR_ALIGN  # idx 4-byte
-    assert f(P, P, P, P, P, P + 1, 1, 64, 512, None) == ops.ERR_ALIGN  # val 2-byte
-    assert f(P, P, P, P, P, P, 1, 64, 448, None) == ops.ERR_KERNEL   # tensor-core family only
+    WS, NB = 0x100000, L.w4a16_workspace_bytes(64, 512)
+    assert f(P, P, P, P, P, P, 0, 64, 512, None, 0, None) == ops.OK          # M == 0: no-op
+    assert f(P, P, P, P, P, None, -1, 64, 512, WS, NB, None) == ops.ERR_SHAPE
+    assert f(P, P, P, P, P, P, 1, 64, 96, WS, NB, None) == ops.ERR_SHAPE    # K % 64
+    assert f(P, P, P, P, None, P, 1, 64, 512, WS, NB, None) == ops.ERR_NULL  # idx
+    assert f(P + 8, P, P, P, P, P, 1, 64, 512, WS, NB, None) == ops.ERR_ALIGN
+    assert f(P, P, P, P, P + 2, P, 1, 64, 512, WS, NB, None) == ops.ERR_ALIGN  # idx 4-byte
+    assert f(P, P, P, P, P, P + 1, 1, 64, 512, WS, NB, None) == ops.ERR_ALIGN  # val 2-byte
+    assert f(P, P, P, P, P, P, 1, 64, 512, None, 0, None) == ops.ERR_NULL    # no workspace
+    assert f(P, P, P, P, P, P, 1, 64, 512, WS, NB - 1, None) == ops.ERR_SHAPE  # too small
+    assert f(P, P, P, P, P, P, 1, 64, 512, WS + 16, NB, None) == ops.ERR_ALIGN  # 256-byte alignment
+    assert f(P, P, P, P, P, P, 1, 64, 448, WS, NB, None) == ops.ERR_KERNEL   # tensor-core family only
+
+
+def test_workspace_bytes_and_mm_ws_errors(L):
+    """The workspace query and w4a16_mm_ws's fail-closed checks."""
+    nb = L.w4a16_workspace_bytes(262144, 2560)
+    assert nb == 5013504  # 32 KiB counters + 4864 KiB fp32 partials, every shape
+    assert L.w4a16_workspace_bytes(16384, 16384) == nb
+    assert L.w4a16_workspace_bytes(256, 448) == 0     # K % 512: the CUDA-core family, no workspace
+    assert L.w4a16_workspace_bytes(0, 512) == 0
+    assert L.w4a16_workspace_bytes(64, 96) == 0
+    f = L.w4a16_mm_ws
+    WS = 0x100000
+    assert f(P, P, P, P, P, 0, 64, 512, WS, nb, None) == ops.OK            # M == 0: no-op
+    assert f(P, P, P, P, P, 1, 64, 512, WS, nb - 256, None) == ops.ERR_SHAPE
+    assert f(P, P, P, P, P, 1, 64, 512, WS + 128, nb, None) == ops.ERR_ALIGN
+    assert f(P, P, P, P, P, 1, 64, 96, WS, nb, None) == ops.ERR_SHAPE      # K % 64
+    assert f(P, P, P, P, None, 1, 64, 512, WS, nb, None) == ops.ERR_NULL
+    # the plan reports the workspace the launch shape takes when one is given
+    lm = ops.get_plan(262144, 2560)
+    assert lm["kernel"] == "tc" and lm["workspace_bytes"] == nb
+    assert ops.get_plan(2048, 2560)["workspace_bytes"] == 0   # the tile kernel needs none
+    assert ops.get_plan(256, 448)["workspace_bytes"] == 0
 
 
 def test_embed_errors(L):

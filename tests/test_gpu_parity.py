@@ -50,8 +50,9 @@ def test_tc_ragged_shapes(N, K, M):
 @pytest.mark.parametrize("N,K", [(1, 512), (7, 1024), (31, 1536), (33, 2560), (95, 1536), (1000, 3072), (4099, 4096)])
 @pytest.mark.parametrize("M", [1, 5, 8])
 def test_tc_persistent_grid_ragged_shapes(N, K, M):
-    """The persistent launch shape (split-K through the workspace), forced on
-    shapes the dispatcher would give to the tile kernel."""
+    """The persistent launch shape without a workspace (units dealt inside each
+    CTA; a split K as whole-K units folding the slice sums), forced on shapes
+    the dispatcher would give to the tile kernel."""
     xb, hw, y = _run(M, N, K, "tc_stream", seed=N + K + 1, xseed=M + 40)
     yr, ad = oracle_mm(xb, hw)
     assert_parity(y, yr, ad, f"tc_stream M={M} N={N} K={K}")
@@ -149,11 +150,12 @@ def test_large_activation_magnitudes():
 
 
 def test_workspace_reuse_across_shapes():
-    """Split-K shapes of different sizes share one stream's workspace; each
-    call must find its counters at zero whatever ran before."""
-    for (M, N, K) in [(2, 1024, 2560), (1, 10240, 2560), (3, 2560, 10240), (1, 1024, 2560), (1, 10240, 2560),
-                      (4, 96, 1024), (1, 10240, 2560)]:
-        xb, hw, y = _run(M, N, K, "tc", seed=N % 7, xseed=M)
+    """Shapes of different sizes, split-K ones among them, share one stream's
+    workspace (the binding's default); each call must find its counters at
+    zero whatever ran before."""
+    for (M, N, K) in [(2, 1024, 2560), (1, 12288, 8192), (3, 2560, 10240), (1, 98304, 1536), (5, 12288, 8192),
+                      (4, 96, 1024), (1, 12288, 8192)]:
+        xb, hw, y = _run(M, N, K, "auto", seed=N % 7, xseed=M)
         cols = sample_cols(N, 1024, seed=N)
         yr, ad = oracle_mm(xb, hw, cols)
         assert_parity(y[:, torch.from_numpy(cols).cuda()], yr, ad, f"reuse M={M} N={N} K={K}")

@@ -34,6 +34,8 @@ def _noalloc(x, w, y):
 
 def test_noalloc_matches_mm_on_two_calls_in_a_row():
     for (M, N, K, seed) in [(3, 10240, 2560, 71), (1, 2560, 10240, 72)]:
+        # both shapes split K (so the scratch's counters and partials are used)
+        assert ops.get_plan(N, K)["ksplit"] > 1
         hw = synth.make_weights(seed, N, K)
         w = ops.W4Matrix.from_host(hw)
         xb = synth.make_x(seed, M, K)
@@ -50,6 +52,43 @@ def test_noalloc_matches_mm_on_two_calls_in_a_row():
         got = y.double().cpu().numpy()
         assert np.all(np.abs(got - ref) <= oracle.tolerance(ref, absdot)), f"M={M} N={N} K={K}"
         assert torch.equal(y.view(torch.int16), y_mm.view(torch.int16)), "same kernel, same bits"
+
+
+def test_noalloc_on_new_streams_takes_no_memory():
+    """After one warm-up call (the library's module is loaded and the array's
+    address looked up), calls on a brand-new stream leave the device's free
+    memory unchanged, and a call captured on another new stream replays with
+    w4a16_mm's bits."""
+    M, N, K = 2, 2560, 10240
+    hw = synth.make_weights(74, N, K)
+    w = ops.W4Matrix.from_host(hw)
+    x = _dev(synth.make_x(74, M, K))
+    ref = ops.mm(x, w)
+    y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    assert _noalloc(x, w, y) == ops.OK
+    torch.cuda.synchronize()
+    # eager calls on a new stream: the device's free memory does not move
+    free0, _ = torch.cuda.mem_get_info()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            assert _noalloc(x, w, y) == ops.OK
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+    # captured on another new stream (an allocation would break the capture)
+    s2 = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    y.fill_(float("nan"))
+    torch.cuda.synchronize()
+    rcs = []
+    with torch.cuda.graph(g, stream=s2):
+        rcs.append(_noalloc(x, w, y))
+    assert rcs == [ops.OK], ops.lib().w4a16_last_error().decode()
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
 
 
 def test_noalloc_rejects_unsupported_k():
