@@ -601,6 +601,23 @@ def measure_extras(torch, ops, synth, roofline, l2, peak, args):
                             "t5_over_t1": round(t5["us"] / t1["us"], 3)}
         del ws
     out["tail_k_simt"] = tail
+    # many activation rows: the tcgen05 prefill kernel (the default above 32
+    # rows) against the skinny tile kernel taking them eight at a time
+    pre = {}
+    for (N, K) in [(10240, 2560), (12288, 1536)]:
+        ws = cold_set(N, K, 11)
+        t = {M: timed(ws, M, N, K, 10) for M in (1, 8, 16, 32, 64, 128, 256)}
+        row = {f"M{M}_us": t[M]["us"] for M in t}
+        row.update({f"t{M}_over_t1": round(t[M]["us"] / t[1]["us"], 3) for M in (16, 32, 64, 128, 256)})
+        flops = {M: 2.0 * M * N * K / (t[M]["us"] * 1e-6) / 1e12 for M in (64, 128, 256)}
+        row.update({f"M{M}_TFLOPs": round(v, 1) for M, v in flops.items()})
+        for M in (16, 32):  # below the switch: the prefill kernel selected explicitly
+            row[f"M{M}_prefill_kernel_us"] = timed(ws, M, N, K, 10, kernel="tc_prefill")["us"]
+        for M in (64, 128):  # above it: the skinny tile kernel, eight rows at a time
+            row[f"M{M}_tile_kernel_us"] = timed(ws, M, N, K, 10, kernel="tc_tile")["us"]
+        pre[f"{N}x{K}"] = row
+        del ws
+    out["prefill"] = pre
     out["stq1"] = measure_stq1(torch, ops, synth, roofline, l2, peak)
     return out
 

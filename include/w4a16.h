@@ -120,9 +120,13 @@ typedef enum {
                                  without a workspace a split K runs as whole-K units.
                                  w4a16_mm_id: T <= 32 its routed mode, more tokens a grid
                                  of tile x expert CTAs */
-  W4A16_KERNEL_TC_TILE = 5  /* tensor-core kernel, one CTA per 16-row tile holding the
+  W4A16_KERNEL_TC_TILE = 5, /* tensor-core kernel, one CTA per 16-row tile holding the
                                tile's whole K range; needs that to fit in shared memory
                                (otherwise W4A16_ERR_KERNEL) */
+  W4A16_KERNEL_TC_PREFILL = 6 /* tensor-core kernel for many rows: each 64-code group of a
+                                 128-row tile expanded once to bf16 in shared memory, then
+                                 tcgen05.mma over up to 128 activation rows into tensor
+                                 memory; the default for M > 32 where the family applies */
 } w4a16_kernel;
 
 /* y[M][N] = x[M][K] W^T.  M == 0 is a successful no-op.  The kernel family

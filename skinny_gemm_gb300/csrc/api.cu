@@ -121,12 +121,14 @@ int resolve_kernel(int requested, int N, int K, w4a16_plan* plan) {
     case W4A16_KERNEL_VANILLA: plan_vanilla(N, K, plan); return W4A16_OK;
     case W4A16_KERNEL_TC:
     case W4A16_KERNEL_TC_STREAM:
-    case W4A16_KERNEL_TC_TILE: {
+    case W4A16_KERNEL_TC_TILE:
+    case W4A16_KERNEL_TC_PREFILL: {
       if (!tc_supported(N, K)) return fail(W4A16_ERR_KERNEL, "the tensor-core kernel needs K %% 512 == 0 (K = %d)", K);
       const int path = k == W4A16_KERNEL_TC_STREAM ? 1 : k == W4A16_KERNEL_TC_TILE ? 2 : 0;
       if (path == 2 && !tc_tile_fits(N, K, 1))
         return fail(W4A16_ERR_KERNEL, "the tile kernel cannot hold K = %d in shared memory", K);
       plan_tc(N, K, path, plan);
+      if (k == W4A16_KERNEL_TC_PREFILL) plan->kernel = W4A16_KERNEL_TC_PREFILL;
       return W4A16_OK;
     }
     default: return fail(W4A16_ERR_KERNEL, "unknown kernel selector %d", requested);
@@ -169,12 +171,13 @@ int run_mm(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* S, const w
   a.N = N; a.K = K;
   a.stream = static_cast<cudaStream_t>(stream);
   a.pdl = env().pdl;
-  a.tc_path = plan.kernel == W4A16_KERNEL_TC_STREAM ? 1 : plan.kernel == W4A16_KERNEL_TC_TILE ? 2 : 0;
+  a.tc_path = plan.kernel == W4A16_KERNEL_TC_STREAM ? 1 : plan.kernel == W4A16_KERNEL_TC_TILE ? 2
+             : plan.kernel == W4A16_KERNEL_TC_PREFILL ? 3 : 0;
   a.ws = ws;
   a.ws_bytes = ws_bytes;
   if (int rc = flag_pointer(&a.flags)) return rc;
   const bool tc = plan.kernel == W4A16_KERNEL_TC || plan.kernel == W4A16_KERNEL_TC_STREAM ||
-                  plan.kernel == W4A16_KERNEL_TC_TILE;
+                  plan.kernel == W4A16_KERNEL_TC_TILE || plan.kernel == W4A16_KERNEL_TC_PREFILL;
   if (a.tc_path == 2 && !tc_tile_fits(N, K, M < kMaxChunk ? M : kMaxChunk))
     return fail(W4A16_ERR_KERNEL, "the tile kernel cannot hold K = %d for %d rows in shared memory", K,
                 M < kMaxChunk ? M : kMaxChunk);
@@ -189,7 +192,8 @@ int run_mm(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* S, const w
       case W4A16_KERNEL_SIMT: e = launch_simt(a, plan); break;
       case W4A16_KERNEL_TC:
       case W4A16_KERNEL_TC_STREAM:
-      case W4A16_KERNEL_TC_TILE: e = launch_tc(a, plan); break;
+      case W4A16_KERNEL_TC_TILE:
+      case W4A16_KERNEL_TC_PREFILL: e = launch_tc(a, plan); break;
       case W4A16_KERNEL_VANILLA: e = launch_vanilla(a, plan); break;
       default: return fail(W4A16_ERR_KERNEL, "kernel %d cannot run", plan.kernel);
     }

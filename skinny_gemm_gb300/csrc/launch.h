@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "w4a16.h"
@@ -61,6 +62,16 @@ bool tc_group_supported(const int* N, int count, int K);
 // M rows in one launch, eight at a time over resident weights.
 cudaError_t launch_tc_group(const GroupItem* items, int count, int M, int row0, int K, int pdl, int* flags,
                             cudaStream_t stream);
+// A 2-D TMA tensor map of a row-major tensor (`inner` elements per row,
+// `outer` rows, rows `row_bytes` apart) with boxes of box_inner x box_outer.
+cudaError_t encode_map_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, int64_t inner,
+                          int64_t outer, int64_t row_bytes, int box_inner, int box_outer, CUtensorMapSwizzle swizzle);
+// Activation rows from which w4a16_mm runs the tcgen05 prefill kernel (below,
+// the skinny tile kernel taking eight rows at a time is faster).
+constexpr int kPrefillMinM = 33;
+// The tcgen05 prefill kernel (prefill.cu): rows a.row0 .. a.row0 + a.M, the
+// canonical slices of slice_k codes.
+cudaError_t launch_prefill(const LaunchArgs& a, int slice_k);
 // Bytes of the persistent kernel's workspace (counters, split-K partials, argmax keys).
 size_t tc_workspace_bytes();
 // Tensor-core w4a16_mm with its split-K scratch in a fixed device array (no allocation).

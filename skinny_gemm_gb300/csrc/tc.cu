@@ -2005,6 +2005,18 @@ void use_workspace(StreamParams& p, void* ws) {
 
 size_t tc_workspace_bytes() { return kWsBytes; }
 
+cudaError_t encode_map_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, int64_t inner,
+                          int64_t outer, int64_t row_bytes, int box_inner, int box_outer, CUtensorMapSwizzle swizzle) {
+  if (cudaError_t e = get_encoder()) return e;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, type, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 bool tc_supported(int N, int K) {
   (void)N;
   return K % kStageK == 0;
@@ -2079,6 +2091,8 @@ cudaError_t launch_tc_impl(const LaunchArgs& a, int32_t* idx, uint16_t* val) {
   DeviceInfo& d = device_info(dev);
   const bool have_ws = a.ws != nullptr && a.ws_bytes >= kWsBytes;
   if (idx && !have_ws) return cudaErrorInvalidValue;  // the argmax mode merges its keys in the workspace
+  // Many rows: the tcgen05 kernel expands each weight once for all of them
+  if (!idx && (a.tc_path == 3 || (a.tc_path == 0 && a.M >= kPrefillMinM))) return launch_prefill(a, s.sl * kStageK);
   if (a.tc_path != 1 && !idx) {
     // one launch for all M rows: eight at a time over the resident weights
     const TilePlan tp = tile_plan(s, a.N, min(a.M, kMaxChunk), a.tc_path == 2, d.sms);

@@ -23,7 +23,7 @@ from . import _build
 GROUP = 64
 
 OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_EXPERTS, ERR_CUDA, ERR_KERNEL, ERR_DEVICE = 0, -1, -2, -3, -4, -5, -6, -7
-KERNELS = {"auto": 0, "simt": 1, "tc": 2, "vanilla": 3, "tc_stream": 4, "tc_tile": 5}
+KERNELS = {"auto": 0, "simt": 1, "tc": 2, "vanilla": 3, "tc_stream": 4, "tc_tile": 5, "tc_prefill": 6}
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 DEVICE_BAD_ID = 1
 
