@@ -601,6 +601,28 @@ def measure_extras(torch, ops, synth, roofline, l2, peak, args):
                             "t5_over_t1": round(t5["us"] / t1["us"], 3)}
         del ws
     out["tail_k_simt"] = tail
+    # group-128 tables on the 262144x2560 head: read natively (0.53125 B per
+    # weight) against their expansion to group 64 (0.5625 B per weight)
+    N, K = 262144, 2560
+    hw = synth.make_weights(12, N, K)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()  # noqa: E731
+    s128, b128 = dev(hw.scales[:, ::2]), dev(hw.biases[:, ::2])
+    nat = ops.W4Matrix(torch.from_numpy(hw.Wq.view(np.int32)).cuda(), s128, b128, N, K, group=128)
+    copies = max(2, math.ceil(3 * l2 / (N * K * 0.53125)))
+    nats = [nat] + [ops.W4Matrix(nat.Wq.clone(), s128.clone(), b128.clone(), N, K, group=128)
+                    for _ in range(copies - 1)]
+    exps = [ops.W4Matrix.from_group(w.Wq, w.scales, w.biases, N, K, 128) for w in nats]
+    torch.cuda.synchronize()
+    g128 = {}
+    for M in (1, 3):
+        nb_nat = N * K // 2 + 4 * N * (K // 128) + 2 * M * K + 2 * M * N
+        tn, te = timed(nats, M, N, K, 10), timed(exps, M, N, K, 10)
+        g = nb_nat / (tn["us"] * 1e-6) / 1e9
+        g128[f"{N}x{K}_M{M}"] = {"native_us": tn["us"], "native_GBps": round(g, 1), "native_frac": round(g / peak, 4),
+                                 "native_bytes": nb_nat, "expanded_to_g64_us": te["us"],
+                                 "expanded_bytes": roofline.mm_bytes(M, N, K)}
+    del nats, exps
+    out["group128"] = g128
     # many activation rows: the tcgen05 prefill kernel (the default above 32
     # rows) against the skinny tile kernel taking them eight at a time
     pre = {}

@@ -255,6 +255,24 @@ int w4a16_mm_id_kernel(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16
                        const w4a16_bf16* biases, const int32_t* ids, w4a16_bf16* y,
                        int T, int N, int K, int E, int kernel, void* stream);
 
+/* The operation with the group size as an argument (the tiny-llm book
+ * quantizes with 128 codes per scale and bias, [W2D2] "Packed Storage
+ * Layout"): scales and biases are bf16 [N][K/group],
+ *   y[m,n] = bf16( sum_k x[m,k] * (q[n,k]*scales[n][k/group] + biases[n][k/group]) ).
+ * group 64 is w4a16_mm_ws.  group 128 reads the tables as they are, 0.53125
+ * bytes per weight instead of the 0.5625 of an expansion to group 64
+ * ([W2D2] "Revisit the Decode Roofline"), on the persistent tensor-core grid
+ * in whole-K work units: K % 512 == 0 and K <= 8192 (other K:
+ * W4A16_ERR_SHAPE; expand with w4a16_expand_groups instead), scales and
+ * biases 16-byte aligned (W4A16_ERR_ALIGN).  Every 64-group is rescaled with
+ * its 128-group's pair, so y equals, bit for bit, the group-64 entry points on
+ * the expanded tables, and row m of any call equals the M = 1 call on x[m].
+ * The workspace (may be NULL) only deals the work units; otherwise as
+ * w4a16_mm_ws. */
+int w4a16_mm_g(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* scales,
+               const w4a16_bf16* biases, w4a16_bf16* y, int M, int N, int K, int group, void* workspace,
+               size_t workspace_bytes, void* stream);
+
 /* Tables quantized with a larger group (the tiny-llm book quantizes with 128
  * codes per scale and bias, [W2D2] "Packed Storage Layout"): dst[n][j] =
  * src[n][j / (group / 64)], the scales (or biases) of every group repeated

@@ -219,6 +219,35 @@ int w4a16_mm_ws(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* scale
   return run_mm(x, Wq, scales, biases, y, M, N, K, W4A16_KERNEL_AUTO, stream, workspace, workspace_bytes);
 }
 
+int w4a16_mm_g(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* scales, const w4a16_bf16* biases,
+               w4a16_bf16* y, int M, int N, int K, int group, void* workspace, size_t workspace_bytes, void* stream) {
+  if (group == kGroup)
+    return run_mm(x, Wq, scales, biases, y, M, N, K, W4A16_KERNEL_AUTO, stream, workspace, workspace_bytes);
+  if (env().fault == kFaultValidate) return fail(W4A16_ERR_SHAPE, "injected validation fault (W4A16_FAULT)");
+  if (group != 128) return fail(W4A16_ERR_SHAPE, "group = %d must be 64 or 128", group);
+  if (int rc = validate_mm(x, Wq, scales, biases, y, M, N, K)) return rc;
+  if (K % 512 || K > 8192)
+    return fail(W4A16_ERR_SHAPE,
+                "group 128 runs natively for K %% 512 == 0 up to 8192 (K = %d); expand the tables to group 64 "
+                "with w4a16_expand_groups for other K", K);
+  if (misaligned(scales, 16) || misaligned(biases, 16))
+    return fail(W4A16_ERR_ALIGN, "group-128 scales and biases must be 16-byte aligned");
+  if (int rc = check_workspace(workspace, workspace_bytes)) return rc;
+  if (M == 0) return W4A16_OK;
+  if (env().fault == kFaultLaunch) return fail(W4A16_ERR_CUDA, "injected launch fault (W4A16_FAULT)");
+  LaunchArgs a{};
+  a.x = x; a.Wq = Wq; a.S = scales; a.B = biases; a.y = y;
+  a.N = N; a.K = K; a.M = M; a.row0 = 0;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.pdl = env().pdl;
+  a.tc_path = 1;
+  a.ws = workspace;
+  a.ws_bytes = workspace_bytes;
+  if (int rc = flag_pointer(&a.flags)) return rc;
+  cudaError_t e = launch_tc_g128(a);
+  return e == cudaSuccess ? W4A16_OK : cuda_fail(e, "w4a16_mm_g launch");
+}
+
 size_t w4a16_workspace_bytes(int N, int K) {
   if (N <= 0 || K <= 0 || K % kGroup || !tc_supported(N, K)) return 0;
   return tc_workspace_bytes();

@@ -72,6 +72,8 @@ constexpr int kPrefillMinM = 33;
 // The tcgen05 prefill kernel (prefill.cu): rows a.row0 .. a.row0 + a.M, the
 // canonical slices of slice_k codes.
 cudaError_t launch_prefill(const LaunchArgs& a, int slice_k);
+// w4a16_mm_g with group 128: the persistent kernel reading [N][K/128] tables.
+cudaError_t launch_tc_g128(const LaunchArgs& a);
 // Bytes of the persistent kernel's workspace (counters, split-K partials, argmax keys).
 size_t tc_workspace_bytes();
 // Tensor-core w4a16_mm with its split-K scratch in a fixed device array (no allocation).

@@ -285,15 +285,20 @@ struct Maps {
 // The weight part of a stage: codes (two boxes, to dst) and the 8 groups'
 // scales and biases (to pdst) of 16 * NSUB rows from tensor_row; arms `bar`
 // for those bytes plus `mc` activation chunks still to come.
-template <int NSUB>
+// With PARAMS false only the codes are requested (group-128 tables bring
+// their parameters per work unit instead, see Ring::pbytes).
+template <int NSUB, bool PARAMS = true>
 __device__ __forceinline__ void issue_weights(uint32_t dst, uint32_t pdst, uint32_t bar, const Maps* maps, int st,
-                                              int tensor_row, int mc, uint64_t pol_stream, uint64_t pol_keep) {
+                                              int tensor_row, int mc, uint64_t pol_stream, uint64_t pol_keep,
+                                              uint32_t extra_bytes = 0) {
   using G = Geo<NSUB>;
-  mbar_expect_tx(bar, 2 * G::kBox + 2 * G::kParam + (uint32_t)(mc * kStageK * 2));
+  mbar_expect_tx(bar, 2 * G::kBox + (PARAMS ? 2 * G::kParam : 0) + (uint32_t)(mc * kStageK * 2) + extra_bytes);
   tma_load_2d(dst, &maps->codes, st * kStageWords, tensor_row, bar, pol_stream);
   tma_load_2d(dst + G::kBox, &maps->codes, st * kStageWords + kBoxWords, tensor_row, bar, pol_stream);
-  tma_load_2d(pdst, &maps->scales, st * 8, tensor_row, bar, pol_keep);
-  tma_load_2d(pdst + G::kParam, &maps->biases, st * 8, tensor_row, bar, pol_keep);
+  if (PARAMS) {
+    tma_load_2d(pdst, &maps->scales, st * 8, tensor_row, bar, pol_keep);
+    tma_load_2d(pdst + G::kParam, &maps->biases, st * 8, tensor_row, bar, pol_keep);
+  }
 }
 
 // The activation part of a stage: 512 bf16 of each row toks[0..mc) into rows
@@ -381,10 +386,22 @@ __device__ __forceinline__ void ldsm_offsets(int lane, uint32_t (&off)[2][4]) {
 // 2t+1).  GB groups at a time: their loads are issued first and their MMA
 // chains interleaved.  With ALLCOLS false (one activation row) the odd
 // columns are not rescaled; the even columns' arithmetic is unchanged.
-template <int NSUB, bool ALLCOLS, bool XSTAGED, int BOXROWS = 16 * NSUB>
+__device__ __forceinline__ uint2 lds64u(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+// G128: the table has one scale and bias per 128 codes (the stage's 8
+// 64-groups use 4 of each); they are read at pbase + r * prow (scales) and
+// pbase + pbias + r * prow (biases), 8 bytes per row.  Each 64-group is then
+// rescaled with its 128-group's pair: the arithmetic of the group-64 kernel
+// on a table whose pairs repeat over the two halves of every 128-group.
+template <int NSUB, bool ALLCOLS, bool XSTAGED, int BOXROWS = 16 * NSUB, bool G128 = false>
 __device__ __forceinline__ void compute_stage(uint32_t cbase, uint32_t pbase, uint32_t xbase, bool xvalid,
                                               uint32_t sxbase, uint32_t sx_stride, bool xvalid_cols,
-                                              float (&p)[NSUB][4], const uint32_t (&loff)[NSUB][4], int g) {
+                                              float (&p)[NSUB][4], const uint32_t (&loff)[NSUB][4], int g,
+                                              uint32_t prow = 0, uint32_t pbias = 0) {
   constexpr int GB = W4A16_TC_GROUP_BATCH;
   // Codes: two boxes of BOXROWS rows x 128 bytes at cbase (the warp's rows
   // picked by loff); scales then biases (16 bytes per row, BOXROWS rows
@@ -395,8 +412,14 @@ __device__ __forceinline__ void compute_stage(uint32_t cbase, uint32_t pbase, ui
 #pragma unroll
   for (int i = 0; i < 2 * NSUB; ++i) {
     const uint32_t r = 16 * (i >> 1) + g + 8 * (i & 1);
-    ps[i] = lds128(pbase + r * 16);
-    pb[i] = lds128(pbase + kBiases + r * 16);
+    if (G128) {
+      const uint2 s2 = lds64u(pbase + r * prow), b2 = lds64u(pbase + pbias + r * prow);
+      ps[i] = make_uint4(s2.x, s2.y, 0u, 0u);
+      pb[i] = make_uint4(b2.x, b2.y, 0u, 0u);
+    } else {
+      ps[i] = lds128(pbase + r * 16);
+      pb[i] = lds128(pbase + kBiases + r * 16);
+    }
   }
 #pragma unroll
   for (int gp = 0; gp < 8; gp += GB) {
@@ -468,10 +491,11 @@ __device__ __forceinline__ void compute_stage(uint32_t cbase, uint32_t pbase, ui
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
           const int i = 2 * s + rr;
-          const uint32_t sw = component(ps[i], gi >> 1);
-          const uint32_t bw = component(pb[i], gi >> 1);
-          const float sc = (gi & 1) ? half_hi(sw) : half_lo(sw);
-          const float bi = (gi & 1) ? half_hi(bw) : half_lo(bw);
+          const int pi = G128 ? gi >> 1 : gi;  // this group's parameter pair in the row's stage slice
+          const uint32_t sw = component(ps[i], pi >> 1);
+          const uint32_t bw = component(pb[i], pi >> 1);
+          const float sc = (pi & 1) ? half_hi(sw) : half_lo(sw);
+          const float bi = (pi & 1) ? half_hi(bw) : half_lo(bw);
           const float cc = __fmaf_rn(-128.0f, sc, bi);
           p[s][2 * rr + 0] = __fmaf_rn(sc, acc[j][s][2 * rr + 0], p[s][2 * rr + 0]);
           p[s][2 * rr + 0] = __fmaf_rn(cc, sx[j][0], p[s][2 * rr + 0]);
@@ -530,6 +554,8 @@ struct StreamParams {
   int stages;
   int xpitch;       // bytes per activation row of the pre-staged copy (0: per-stage copies)
   int prefetch;     // request the first weight stages before waiting for earlier kernels
+  int g128;         // scales and biases are [N][K/128] (one pair per 128 codes)
+  int par_off;      // and then the byte offset of the per-unit parameter slots in shared memory
   const int32_t* ids;  // routed mode: expert id of each of T tokens, E experts of N rows each
   int T, E;
   unsigned long long* best;  // argmax mode: [8] running keys, zero between launches
@@ -652,7 +678,7 @@ __device__ __forceinline__ void build_chunks(const int32_t* __restrict__ ids, in
 // with 64-bit atomic maxima, and the last CTA out writes the argmax of every
 // row (the outputs' bits are those w4a16_mm stores).
 template <int NSUB, bool ALLCOLS, bool XSTAGED, bool SPLIT, bool ROUTED = false, bool ARGMAX = false,
-          bool WHOLEK = false>
+          bool WHOLEK = false, bool G128 = false>
 __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_min_blocks<NSUB>()) tc_stream_kernel(
     const __grid_constant__ Maps maps, StreamParams p) {
   using G = Geo<NSUB>;
@@ -660,8 +686,9 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   static_assert(!ROUTED || (!XSTAGED && !SPLIT), "the routed mode copies activations per stage, whole-K units");
   static_assert(!ARGMAX || (!ROUTED && NSUB == 2), "argmax over plain 32-row units");
   static_assert(!WHOLEK || (!ROUTED && !SPLIT && !ARGMAX), "whole-K units are a plain-mode schedule");
+  static_assert(!G128 || (!ROUTED && !SPLIT && !ARGMAX), "group-128 tables: plain whole-K units");
   constexpr bool DYN = (SPLIT || W4A16_TC_DYN_ALL) && !ROUTED;  // units after the first from the counter
-  constexpr bool FOLD = ROUTED || WHOLEK;  // whole-K units: slice sums folded in registers, in slice order
+  constexpr bool FOLD = ROUTED || WHOLEK || G128;  // whole-K units: slice sums folded in registers, in slice order
   // Without a workspace (p.sched == nullptr) the units are dealt inside each
   // CTA: CTA c owns the contiguous units [c U / grid, (c + 1) U / grid) and
   // its warps take them from a shared-memory counter.  With one, from a
@@ -692,6 +719,12 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   R.issued = R.consumed = 0;
   R.pol_stream = policy_evict_first();
   R.pol_keep = policy_evict_last();
+  // G128: a unit's scales and biases (its rows over the whole K, K / 64 bytes
+  // a row) arrive with its first stage, into one of S slots per warp (a unit
+  // has at least one stage, so at most S units are in flight)
+  const uint32_t prb = (uint32_t)(p.K / 64);
+  const uint32_t pslot = 2u * kRows * prb;
+  const uint32_t par0 = smem_u32(base) + (uint32_t)p.par_off + (uint32_t)(warp * S) * pslot;
 
   if (lane == 0)
     for (int i = 0; i < S; ++i) mbar_init(R.bars0 + 8 * i, 1);
@@ -740,7 +773,8 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   int imc = xring;                 // and their count
   int nxt = -1;                    // lane 0: count of the grab for the unit after iu (unit TW + nxt), -1 before it
   int irow = 0;                    // lane 0: first weight row of unit iu
-  uint32_t iseq = 0;
+  int ifirst = 0;                  // lane 0: first stage of unit iu
+  uint32_t iseq = 0, ipar = 0;     // lane 0: units dealt / begun
   const int last_grab = max(0, p.units - TW) + min(TW, p.units) - 1;
   // Stages of the current unit still to request when the next is grabbed:
   // one, or two for units of three stages or fewer (LM head 262144x1536:
@@ -759,6 +793,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   auto begin_unit = [&](int u) {
     iu = u;
     if (DYN) s_units[iseq++ & 7u] = u;
+    if (G128 && u >= 0) ++ipar;
     if (u >= 0) {
       if (ROUTED) {
         const int c = u / p.tiles;
@@ -768,7 +803,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
         itok = ch + 2;
         ist = 0;
         iend = p.nst;
-      } else if (WHOLEK) {
+      } else if (WHOLEK || G128) {
         irow = u * kRows;
         ist = 0;
         iend = p.nst;
@@ -778,10 +813,40 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
         ist = slice * p.sl;
         iend = min(ist + p.sl, p.nst);
       }
+      ifirst = ist;
     }
   };
   auto issue_stage = [&](bool with_x) {
-    const uint32_t slot = ring_issue_w<NSUB>(R, &maps, ist, irow, imc);
+    uint32_t slot;
+    if (G128) {
+      slot = R.issued % (uint32_t)R.S;
+      const uint32_t dst = R.codes0 + slot * G::kSlot, bar = R.bars0 + 8 * slot;
+      if (ist == ifirst) {
+        // the unit's rows of the group-128 scales and biases: one bulk copy
+        // each of the 16-byte multiple, plain loads for the few bytes past it
+        const int rows = min(kRows, p.N - irow);
+        const uint32_t nbytes = (uint32_t)rows * prb, bulk = nbytes & ~15u;
+        const uint32_t ps = par0 + ((ipar - 1) % (uint32_t)S) * pslot;
+        issue_weights<NSUB, false>(dst, 0, bar, &maps, ist, irow, imc, R.pol_stream, R.pol_keep, 2 * bulk);
+        const char* gs = reinterpret_cast<const char*>(p.S) + (int64_t)irow * prb;
+        const char* gb = reinterpret_cast<const char*>(p.B) + (int64_t)irow * prb;
+        if (bulk) {
+          bulk_load(ps, gs, bulk, bar, R.pol_keep);
+          bulk_load(ps + kRows * prb, gb, bulk, bar, R.pol_keep);
+        }
+        for (uint32_t o = bulk; o < nbytes; o += 2) {
+          const uint16_t vs = ld_nc_u16(reinterpret_cast<const uint16_t*>(gs + o));
+          const uint16_t vb = ld_nc_u16(reinterpret_cast<const uint16_t*>(gb + o));
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(ps + o), "h"(vs) : "memory");
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(ps + kRows * prb + o), "h"(vb) : "memory");
+        }
+      } else {
+        issue_weights<NSUB, false>(dst, 0, bar, &maps, ist, irow, imc, R.pol_stream, R.pol_keep);
+      }
+      ++R.issued;
+    } else {
+      slot = ring_issue_w<NSUB>(R, &maps, ist, irow, imc);
+    }
     if (with_x) ring_issue_x(R, slot, ist, p.x, itok, imc, p.K);
     ++ist;
   };
@@ -1037,8 +1102,13 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
       } else {
         xbase = ordered(R.xs0 + slot * x_slot + g * kXPitch + 16 * t);
       }
-      compute_stage<NSUB, ALLCOLS, XSTAGED>(cbase, cbase + 2 * G::kBox, xbase, g < umc, sxbase, sx_cols(mc) * 4,
-                                            2 * t < umc, acc, loff, g);
+      if (G128)
+        compute_stage<NSUB, ALLCOLS, XSTAGED, 16 * NSUB, true>(
+            cbase, par0 + (cseq % (uint32_t)S) * pslot + (uint32_t)st * 8u, xbase, g < umc, sxbase, sx_cols(mc) * 4,
+            2 * t < umc, acc, loff, g, prb, kRows * prb);
+      else
+        compute_stage<NSUB, ALLCOLS, XSTAGED>(cbase, cbase + 2 * G::kBox, xbase, g < umc, sxbase, sx_cols(mc) * 4,
+                                              2 * t < umc, acc, loff, g);
       if (FOLD && (st + 1 == fold_at || st + 1 == s1)) {
         const bool first = fold_at == s0 + p.sl;
 #pragma unroll
@@ -1745,11 +1815,11 @@ cudaError_t launch_ex(Kern fn, dim3 grid, dim3 block, int smem, cudaStream_t str
   return cudaLaunchKernelEx(&cfg, fn, args...);
 }
 
-template <int NSUB, bool A, bool X, bool SPLIT, bool ARGMAX = false, bool WHOLEK = false>
+template <int NSUB, bool A, bool X, bool SPLIT, bool ARGMAX = false, bool WHOLEK = false, bool G128 = false>
 cudaError_t stream_launch_t(const Maps& map, const StreamParams& p, int sms, int smem, DeviceInfo& d,
                             cudaStream_t stream, bool pdl) {
   constexpr int kW = Geo<NSUB>::kWarps;
-  auto* fn = tc_stream_kernel<NSUB, A, X, SPLIT, false, ARGMAX, WHOLEK>;
+  auto* fn = tc_stream_kernel<NSUB, A, X, SPLIT, false, ARGMAX, WHOLEK, G128>;
   if (cudaError_t e = allow_smem(fn, d)) return e;
   int per_sm = 0;
   if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kW * 32, smem)) return e;
@@ -1775,6 +1845,21 @@ cudaError_t launch_stream_t(const Maps& map, StreamParams p, int sms, DeviceInfo
   if (staged) smem += xstage_bytes(p.M, p.K);
   const bool on = pdl > 0;
   using Fn = cudaError_t (*)(const Maps&, const StreamParams&, int, int, DeviceInfo&, cudaStream_t, bool);
+  if (p.g128) {  // group-128 tables: whole-K units with their parameter rows in shared memory
+    // the ring as deep as fits next to S parameter slots of K bytes per warp
+    for (;; --p.stages) {
+      smem = stream_smem<NSUB>(p.stages, staged ? 0 : p.M) + extra + (staged ? xstage_bytes(p.M, p.K) : 0);
+      p.par_off = (smem - 1024 + 15) & ~15;
+      smem = p.par_off + Geo<NSUB>::kWarps * p.stages * p.K + 1024;
+      if (smem <= kSmemLimit) break;
+      if (p.stages <= 2) return cudaErrorInvalidValue;
+    }
+    static const Fn g128[2][2] = {{stream_launch_t<NSUB, false, false, false, false, false, true>,
+                                   stream_launch_t<NSUB, false, true, false, false, false, true>},
+                                  {stream_launch_t<NSUB, true, false, false, false, false, true>,
+                                   stream_launch_t<NSUB, true, true, false, false, false, true>}};
+    return g128[allcols][staged](map, p, sms, smem, d, stream, on);
+  }
   const bool split = p.ks > 1 && p.part != nullptr;
   if (p.ks > 1 && !split) {  // no workspace: whole-K units, the slice sums folded in registers
     static const Fn fold[2][2] = {{stream_launch_t<NSUB, false, false, false, false, true>,
@@ -1983,7 +2068,7 @@ bool workspace_fits(const Shape& s, const StreamWork& w) {
 cudaError_t launch_stream(const Maps& maps, StreamParams p, const StreamWork& w, DeviceInfo& d,
                           cudaStream_t stream, int pdl) {
   p.tiles = w.tiles;
-  p.units = p.ks > 1 && !p.part ? w.tiles : w.units;  // whole-K units without a workspace
+  p.units = p.ks > 1 && (!p.part || p.g128) ? w.tiles : w.units;  // whole-K units
   p.kfull = p.nst % p.sl == 0 ? p.ks : p.ks - 1;
 #if W4A16_TC_STREAM_NSUB1_MIN_M <= 8  // else no chunk (8 rows at most) takes 16-row warps
   if (w.nsub == 1) return launch_stream_t<1>(maps, p, d.sms, d, stream, pdl);
@@ -2265,6 +2350,45 @@ cudaError_t launch_tc_group(const GroupItem* items, int count, int M, int row0, 
   DeviceInfo& d = device_info(dev);
   if (cudaError_t e = allow_smem(fn, d)) return e;
   return launch_ex(fn, dim3(tiles * tp.kc), dim3(tp.warps * 32), tp.smem, stream, pdl > 0, tp.kc, ta, p);
+}
+
+// ---- group-128 tables ---------------------------------------------------------------------
+//
+// Scales and biases with one pair per 128 codes ([N][K/128], the tiny-llm
+// book's layout), read natively: the persistent grid in whole-K units, each
+// unit's parameter rows brought into shared memory by one bulk copy per
+// table with the unit's first stage (the rows are K / 64 bytes apart, too
+// irregular for a tensor map).  Every 64-group is rescaled with its
+// 128-group's pair, so the results equal the group-64 kernels on the
+// expanded tables bit for bit.  Rows eight at a time, one launch per chunk.
+cudaError_t launch_tc_g128(const LaunchArgs& a) {
+  const Shape s = tc_shape(a.N, a.K);
+  int dev = 0;
+  if (cudaError_t e = cudaGetDevice(&dev)) return e;
+  StreamParams p{};
+  p.x = a.x; p.S = a.S; p.B = a.B; p.y = a.y; p.flags = a.flags;
+  p.N = a.N; p.K = a.K;
+  p.nst = s.nst; p.sl = s.sl; p.ks = s.ks;
+  p.stages = 2;
+  p.g128 = 1;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = device_info(dev);
+  if (a.ws != nullptr && a.ws_bytes >= kWsBytes) {  // the grid-wide unit counter; no K split
+    use_workspace(p, a.ws);
+    p.part = nullptr;
+  }
+  for (int r0 = 0; r0 < a.M; r0 += kMaxChunk) {
+    p.row0 = a.row0 + r0;
+    p.M = min(kMaxChunk, a.M - r0);
+    const StreamWork w = stream_work(s, a.N, p.M);
+    if (w.nsub != 2) return cudaErrorInvalidConfiguration;
+    Maps maps;
+    if (cudaError_t e = make_code_map(&maps.codes, a.Wq, a.N, a.K, w.rows)) return e;
+    maps.scales = maps.codes;  // unused: the parameters come by bulk copy
+    maps.biases = maps.codes;
+    if (cudaError_t e = launch_stream(maps, p, w, d, a.stream, a.pdl)) return e;
+  }
+  return cudaSuccess;
 }
 
 // ---- no-allocation variant ----------------------------------------------------------------

@@ -27,7 +27,7 @@ KERNELS = {"auto": 0, "simt": 1, "tc": 2, "vanilla": 3, "tc_stream": 4, "tc_tile
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 DEVICE_BAD_ID = 1
 
-EXPORTS = ("w4a16_mm", "w4a16_mm_ws", "w4a16_workspace_bytes", "w4a16_mm_kernel", "w4a16_mm_noalloc", "w4a16_mm_group", "w4a16_mm_argmax", "w4a16_embed", "w4a16_expand_groups",
+EXPORTS = ("w4a16_mm", "w4a16_mm_ws", "w4a16_mm_g", "w4a16_workspace_bytes", "w4a16_mm_kernel", "w4a16_mm_noalloc", "w4a16_mm_group", "w4a16_mm_argmax", "w4a16_embed", "w4a16_expand_groups",
            "w4a16_mm_id", "w4a16_mm_id_kernel", "w4a16_unpack", "w4a16_dequant", "w4a16_get_plan", "w4a16_device_status", "w4a16_last_error",
            "w4a16_debug_reload_env", "w4a16_version",
            "stq1_packed_bytes", "stq1_pack", "stq1_mm", "stq1_mm_id", "stq1_get_rows", "stq1_get_plan")
@@ -86,6 +86,7 @@ def lib() -> ctypes.CDLL:
             P, i, z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
             L.w4a16_mm.argtypes = [P, P, P, P, P, i, i, i, P]
             L.w4a16_mm_ws.argtypes = [P, P, P, P, P, i, i, i, P, z, P]
+            L.w4a16_mm_g.argtypes = [P, P, P, P, P, i, i, i, i, P, z, P]
             L.w4a16_workspace_bytes.argtypes = [i, i]
             L.w4a16_workspace_bytes.restype = z
             L.w4a16_mm_kernel.argtypes = [P, P, P, P, P, i, i, i, i, P]
@@ -107,7 +108,7 @@ def lib() -> ctypes.CDLL:
             L.stq1_mm_id.argtypes = [P, P, P, P, i, i, i, i, P]
             L.stq1_get_rows.argtypes = [P, P, P, i, i, i, P]
             L.stq1_get_plan.argtypes = [i, i, ctypes.POINTER(Stq1Plan)]
-            for f in ("w4a16_mm", "w4a16_mm_ws", "w4a16_mm_kernel", "w4a16_mm_noalloc", "w4a16_mm_group", "w4a16_mm_argmax",
+            for f in ("w4a16_mm", "w4a16_mm_ws", "w4a16_mm_g", "w4a16_mm_kernel", "w4a16_mm_noalloc", "w4a16_mm_group", "w4a16_mm_argmax",
                       "w4a16_embed", "w4a16_expand_groups", "w4a16_mm_id", "w4a16_mm_id_kernel", "w4a16_unpack", "w4a16_dequant",
                       "w4a16_get_plan", "w4a16_device_status", "stq1_pack", "stq1_mm", "stq1_mm_id", "stq1_get_rows",
                       "stq1_get_plan"):
@@ -189,6 +190,11 @@ def _ws_args(ws):
     return ws.data_ptr(), ws.numel()
 
 
+def _g64(w, what: str) -> None:
+    if w.group != GROUP:
+        raise ValueError(f"{what} takes group-64 tables; expand group {w.group} with W4Matrix.from_group")
+
+
 def _kernel_id(kernel) -> int:
     if kernel is None:
         return 0
@@ -204,8 +210,9 @@ class W4Matrix:
     """Packed W4A16 weights on the GPU.
 
     Wq: int32 [.., N, K/8] (bit pattern of the uint32 words, eight codes each,
-    low nibble first); scales, biases: bfloat16 [.., N, K/64].  With E > 1
-    the leading dimension stacks E experts.
+    low nibble first); scales, biases: bfloat16 [.., N, K/group] (group 64,
+    or 128 for a single matrix read natively by ``mm``).  With E > 1 the
+    leading dimension stacks E experts.
     """
 
     Wq: torch.Tensor
@@ -214,15 +221,19 @@ class W4Matrix:
     N: int
     K: int
     E: int = 1
+    group: int = GROUP
 
     def __post_init__(self):
         lead = () if self.E == 1 else (self.E,)
+        if self.group not in (GROUP, 128) or (self.group != GROUP and self.E != 1):
+            raise ValueError(f"group {self.group}: 64, or 128 for a single matrix")
         if tuple(self.Wq.shape) != lead + (self.N, self.K // 8):
             raise ValueError(f"Wq shape {tuple(self.Wq.shape)} does not match N={self.N}, K={self.K}, E={self.E}")
         for name in ("scales", "biases"):
             t = getattr(self, name)
-            if tuple(t.shape) != lead + (self.N, self.K // GROUP):
-                raise ValueError(f"{name} shape {tuple(t.shape)} does not match N={self.N}, K={self.K}")
+            if tuple(t.shape) != lead + (self.N, self.K // self.group):
+                raise ValueError(f"{name} shape {tuple(t.shape)} does not match N={self.N}, K={self.K}, "
+                                 f"group={self.group}")
         _dev_tensor(self.Wq, torch.int32, "Wq")
         _dev_tensor(self.scales, torch.bfloat16, "scales")
         _dev_tensor(self.biases, torch.bfloat16, "biases")
@@ -272,6 +283,8 @@ def mm(x: torch.Tensor, w: W4Matrix, out: torch.Tensor | None = None, kernel=Non
     _dev_tensor(x, torch.bfloat16, "x")
     if x.shape[-1] != w.K:
         raise ValueError(f"x has K={x.shape[-1]}, weights have K={w.K}")
+    if w.group != GROUP and kernel not in (None, "auto", 0):
+        raise ValueError("group-128 tables run on their own kernel; no kernel selection")
     M = x.numel() // w.K
     if out is None:
         out = torch.empty(*x.shape[:-1], w.N, dtype=torch.bfloat16, device=x.device)
@@ -281,7 +294,10 @@ def mm(x: torch.Tensor, w: W4Matrix, out: torch.Tensor | None = None, kernel=Non
     L = lib()
     k = _kernel_id(kernel)
     args = (x.data_ptr(), w.Wq.data_ptr(), w.scales.data_ptr(), w.biases.data_ptr(), out.data_ptr(), M, w.N, w.K)
-    if k != 0:
+    if w.group != GROUP:
+        ws = globals()["workspace"](stream) if isinstance(workspace, str) else workspace
+        rc = L.w4a16_mm_g(*args, w.group, *_ws_args(ws), _stream_ptr(stream))
+    elif k != 0:
         rc = L.w4a16_mm_kernel(*args, k, _stream_ptr(stream))
     else:
         ws = globals()["workspace"](stream) if isinstance(workspace, str) else workspace
@@ -302,6 +318,7 @@ def mm_argmax(x: torch.Tensor, w: W4Matrix, idx: torch.Tensor | None = None, val
     idx is int32 [..], val bf16 [..]; pass ``val=False`` to skip the values.
     The call needs a workspace: this stream's (``"auto"``; make one call on
     the stream before capturing it into a CUDA graph) or a given one."""
+    _g64(w, "mm_argmax")
     if w.E != 1:
         raise ValueError("mm_argmax takes a single matrix")
     _dev_tensor(x, torch.bfloat16, "x")
@@ -333,6 +350,7 @@ def mm_argmax(x: torch.Tensor, w: W4Matrix, idx: torch.Tensor | None = None, val
 def embed(ids: torch.Tensor, w: W4Matrix, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Rows ids of the packed table w (N rows of width K), dequantized to bf16
     [..., K] through ``w4a16_embed``; ids int32 on the device."""
+    _g64(w, "embed")
     if w.E != 1:
         raise ValueError("embed takes a single table")
     _dev_tensor(ids, torch.int32, "ids")
@@ -364,6 +382,7 @@ def mm_group(xs, ws, outs=None, stream=None) -> list:
     for i, (x, w, y) in enumerate(zip(xs, ws, outs)):
         if w.E != 1:
             raise ValueError("mm_group takes single matrices")
+        _g64(w, "mm_group")
         _dev_tensor(x, torch.bfloat16, "x")
         _dev_tensor(y, torch.bfloat16, "out")
         if w.K != K or x.shape[-1] != K or x.numel() != M * K:
@@ -378,6 +397,7 @@ def mm_group(xs, ws, outs=None, stream=None) -> list:
 def mm_id(x: torch.Tensor, w: W4Matrix, ids: torch.Tensor, out: torch.Tensor | None = None, kernel=None,
           stream=None) -> torch.Tensor:
     """y[t] = W[ids[t]] x[t] through ``w4a16_mm_id``; x [T, K], ids int32 [T] on the GPU."""
+    _g64(w, "mm_id")
     _dev_tensor(x, torch.bfloat16, "x")
     _dev_tensor(ids, torch.int32, "ids")
     if x.dim() != 2 or x.shape[1] != w.K:
@@ -405,6 +425,7 @@ def unpack(w: W4Matrix, stream=None) -> torch.Tensor:
 
 def dequant(w: W4Matrix, stream=None) -> torch.Tensor:
     """fp32 weights fma(q, s, b) [N][K] through ``w4a16_dequant``."""
+    _g64(w, "dequant")
     out = torch.empty(w.N, w.K, dtype=torch.float32, device=w.Wq.device)
     _raise(lib().w4a16_dequant(w.Wq.data_ptr(), w.scales.data_ptr(), w.biases.data_ptr(), out.data_ptr(),
                                w.N, w.K, _stream_ptr(stream)))

@@ -336,3 +336,16 @@ def test_stq1_python_layer_checks_before_any_launch():
     with pytest.raises(ops.W4A16ValueError):
         ops.stq1_get_plan(4, 384)
     assert ops.stq1_get_plan(6144, 2048) == {"ksplit": 8, "blocks_per_slice": 1, "rows_per_pass": 8}
+
+
+def test_mm_g_errors(L):
+    """w4a16_mm_g: group 64 is w4a16_mm_ws; group 128 needs K % 512 == 0 up
+    to 8192 and 16-byte aligned tables; everything fails before a launch."""
+    f = L.w4a16_mm_g
+    assert f(P, P, P, P, P, 0, 64, 512, 128, None, 0, None) == ops.OK            # M == 0
+    assert f(P, P, P, P, P, 1, 64, 512, 96, None, 0, None) == ops.ERR_SHAPE      # group
+    assert f(P, P, P, P, P, 1, 64, 768, 128, None, 0, None) == ops.ERR_SHAPE     # K % 512
+    assert f(P, P, P, P, P, 1, 64, 8704, 128, None, 0, None) == ops.ERR_SHAPE    # K > 8192
+    assert f(P, P, P + 8, P, P, 1, 64, 512, 128, None, 0, None) == ops.ERR_ALIGN  # scales 16-byte
+    assert f(P, P, P, P, None, 1, 64, 512, 128, None, 0, None) == ops.ERR_NULL
+    assert f(P, P, P, P, P, 1, 64, 512, 128, 0x100000, 100, None) == ops.ERR_SHAPE  # workspace too small

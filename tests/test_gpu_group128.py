@@ -64,3 +64,68 @@ def test_group128_lm_head_rows_invariant():
     yr, ad = oracle.mm(xb, Wq, s, b, 3, N, K, cols=cols, threads=oracle.host_threads(), group=128)
     y = torch.from_numpy(y3.view(np.int16)).view(torch.bfloat16).cuda()
     assert_parity(y[:, torch.from_numpy(cols).cuda()], yr, ad, "group 128 LM head")
+
+
+# ---- native group-128 reads (w4a16_mm_g): the tables as they are ------------------------
+
+def g128_native(seed, N, K):
+    """The same tables as g128_weights, as a native group-128 W4Matrix and as
+    the group-64 expansion of them."""
+    Wq, s, b, wexp = g128_weights(seed, N, K)
+    dev = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()  # noqa: E731
+    wnat = ops.W4Matrix(wexp.Wq, dev(s), dev(b), N, K, group=128)
+    return Wq, s, b, wnat, wexp
+
+
+@pytest.mark.parametrize("N,K", [(1, 512), (31, 1024), (999, 1536), (1000, 2560), (4099, 4096), (96, 8192)])
+@pytest.mark.parametrize("M", [1, 3, 8, 11])
+def test_native_group128_parity_and_equal_to_expansion(N, K, M):
+    """Against the oracle's group-128 definition element by element, and bit
+    for bit against the group-64 kernels on the expanded tables.  Odd N with
+    K / 64 bytes per parameter row leaves a parameter tail that is not a
+    16-byte multiple (N = 999, 31, 1)."""
+    Wq, s, b, wnat, wexp = g128_native(N + K + 5, N, K)
+    xb = synth.make_x(M + 3, M, K)
+    x = to_dev_bf16(xb)
+    y = ops.mm(x, wnat)
+    y_exp = ops.mm(x, wexp)
+    y_nows = ops.mm(x, wnat, workspace=None)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y_exp.view(torch.int16)), "native group 128 vs expanded tables"
+    assert torch.equal(y.view(torch.int16), y_nows.view(torch.int16)), "with and without a workspace"
+    yr, ad = oracle.mm(xb, Wq, s, b, M, N, K, threads=oracle.host_threads(), group=128)
+    assert_parity(y, yr, ad, f"native group 128 {N}x{K} M={M}")
+    assert ops.device_status() == 0
+
+
+@pytest.mark.parametrize("N,K", [(262144, 2560), (262144, 1536), (12288, 8192)])
+def test_native_group128_large_rows_invariant(N, K):
+    """The LM heads and 12288x8192 (eight canonical K-slices, folded in order
+    inside whole-K units): rows of an M = 3 call equal the M = 1 calls and
+    the expanded tables' results; sampled columns against the oracle."""
+    Wq, s, b, wnat, wexp = g128_native(7, N, K)
+    xb = synth.make_x(10, 3, K)
+    x = to_dev_bf16(xb)
+    y3 = ops.mm(x, wnat)
+    for m in range(3):
+        assert torch.equal(ops.mm(x[m:m + 1], wnat).view(torch.int16), y3[m:m + 1].view(torch.int16))
+    assert torch.equal(y3.view(torch.int16), ops.mm(x, wexp).view(torch.int16))
+    cols = sample_cols(N, 384, seed=N + K)
+    yr, ad = oracle.mm(xb, Wq, s, b, 3, N, K, cols=cols, threads=oracle.host_threads(), group=128)
+    assert_parity(y3[:, torch.from_numpy(cols).cuda()], yr, ad, f"native group 128 {N}x{K}")
+
+
+def test_native_group128_rejects():
+    L = ops.lib()
+    N, K = 64, 768  # K % 512 != 0: expand instead
+    Wq, s, b, wnat, wexp = g128_native(1, 64, 1024)
+    x = torch.zeros(1, 1024, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(1, 64, dtype=torch.bfloat16, device="cuda")
+    args = (x.data_ptr(), wnat.Wq.data_ptr(), wnat.scales.data_ptr(), wnat.biases.data_ptr(), y.data_ptr())
+    assert L.w4a16_mm_g(*args, 1, N, K, 128, None, 0, None) == ops.ERR_SHAPE
+    assert L.w4a16_mm_g(*args, 1, 64, 1024, 96, None, 0, None) == ops.ERR_SHAPE
+    assert L.w4a16_mm_g(*args, 1, 64, 1024 * 9, 128, None, 0, None) == ops.ERR_SHAPE
+    with pytest.raises(ValueError):
+        ops.mm(x, wnat, kernel="simt")
+    with pytest.raises(ValueError):
+        ops.mm_id(x, wnat, torch.zeros(1, dtype=torch.int32, device="cuda"))
