@@ -339,8 +339,12 @@ int w4a16_device_status(void* stream, int* flags);
 const char* w4a16_last_error(void);
 
 /* Debug: re-read the environment switches W4A16_FAULT (validate | launch:
- * every compute call then fails with that error before launching anything)
- * and W4A16_FORCE_KERNEL (simt | tc | vanilla).  They are read once, at the
+ * every compute call then fails with that error before launching anything;
+ * wait: in every persistent-grid launch of w4a16_mm one stage of one warp
+ * expects 16 bytes more than its copies deliver, so that warp's bounded wait
+ * gives up, raises W4A16_DEVICE_TIMEOUT and leaves its rows unwritten; every
+ * copy still lands, so nothing is in flight when the kernel exits) and
+ * W4A16_FORCE_KERNEL (simt | tc | vanilla).  They are read once, at the
  * first call, otherwise. */
 void w4a16_debug_reload_env(void);
 

@@ -40,7 +40,7 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 // ---- debug switches read once from the environment -----------------------------
 
-enum Fault { kFaultNone = 0, kFaultValidate = 1, kFaultLaunch = 2 };
+enum Fault { kFaultNone = 0, kFaultValidate = 1, kFaultLaunch = 2, kFaultWait = 3 };
 
 struct EnvConfig {
   int fault = kFaultNone;
@@ -57,6 +57,7 @@ void load_env_locked() {
   if (const char* f = std::getenv("W4A16_FAULT")) {
     if (!std::strcmp(f, "validate")) c.fault = kFaultValidate;
     else if (!std::strcmp(f, "launch")) c.fault = kFaultLaunch;
+    else if (!std::strcmp(f, "wait")) c.fault = kFaultWait;
   }
   if (const char* v = std::getenv("W4A16_PDL")) {
     if (v[0] >= '0' && v[0] <= '2' && v[1] == 0) c.pdl = v[0] - '0';
@@ -175,6 +176,7 @@ int run_mm(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* S, const w
              : plan.kernel == W4A16_KERNEL_TC_PREFILL ? 3 : 0;
   a.ws = ws;
   a.ws_bytes = ws_bytes;
+  a.fault_wait = env().fault == kFaultWait;
   if (int rc = flag_pointer(&a.flags)) return rc;
   const bool tc = plan.kernel == W4A16_KERNEL_TC || plan.kernel == W4A16_KERNEL_TC_STREAM ||
                   plan.kernel == W4A16_KERNEL_TC_TILE || plan.kernel == W4A16_KERNEL_TC_PREFILL;

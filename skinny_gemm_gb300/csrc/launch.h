@@ -34,6 +34,7 @@ struct LaunchArgs {
   cudaStream_t stream;
   void* ws = nullptr;  // the caller's workspace (w4a16_mm_ws, w4a16_mm_argmax), or none
   size_t ws_bytes = 0;
+  int fault_wait = 0;  // debug (W4A16_FAULT=wait): the persistent kernel's first stage never completes
 };
 
 // Per-family planning (depends on N and K only) and launching.

@@ -163,9 +163,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait: true when the phase completed, false after kWaitLimit tries.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
+// Bounded wait: true when the phase completed, false after `limit` tries.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit = kWaitLimit) {
+  for (uint32_t i = 0; i < limit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
@@ -271,6 +271,7 @@ struct Ring {
   int S, x_slot;
   uint32_t issued, consumed;
   uint64_t pol_stream, pol_keep;
+  uint32_t limit = kWaitLimit;  // tries of a stage wait before the warp gives up
 };
 
 // Lane 0 only: start the loads of stage `st` (codes of 32 rows from
@@ -310,13 +311,16 @@ __device__ __forceinline__ void issue_x(uint32_t xdst, uint32_t bar, int st, con
     bulk_load(xdst + n * kXPitch, xs + (int64_t)toks[n] * K, kStageK * 2, bar, pol_keep);
 }
 
-// Lane 0 only: the weights of stage `st` into the next free slot; returns the slot.
+// Lane 0 only: the weights of stage `st` into the next free slot; returns the
+// slot.  `extra` bytes are expected on top of what the copies deliver (the
+// debug fault that lets a stage wait run out; 0 otherwise).
 template <int NSUB>
-__device__ __forceinline__ uint32_t ring_issue_w(Ring& R, const Maps* maps, int st, int tensor_row, int mc) {
+__device__ __forceinline__ uint32_t ring_issue_w(Ring& R, const Maps* maps, int st, int tensor_row, int mc,
+                                                 uint32_t extra = 0) {
   const uint32_t slot = R.issued % (uint32_t)R.S;
   const uint32_t dst = R.codes0 + slot * Geo<NSUB>::kSlot;
   issue_weights<NSUB>(dst, dst + 2 * Geo<NSUB>::kBox, R.bars0 + 8 * slot, maps, st, tensor_row, mc, R.pol_stream,
-                      R.pol_keep);
+                      R.pol_keep, extra);
   ++R.issued;
   return slot;
 }
@@ -338,7 +342,7 @@ __device__ __forceinline__ void ring_issue(Ring& R, const Maps* maps, int st, in
 __device__ __forceinline__ bool ring_wait(Ring& R, uint32_t& slot) {
   slot = R.consumed % (uint32_t)R.S;
   const uint32_t parity = (R.consumed / (uint32_t)R.S) & 1u;
-  const bool ok = mbar_wait(R.bars0 + 8 * slot, parity);
+  const bool ok = mbar_wait(R.bars0 + 8 * slot, parity, R.limit);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -555,6 +559,8 @@ struct StreamParams {
   int xpitch;       // bytes per activation row of the pre-staged copy (0: per-stage copies)
   int prefetch;     // request the first weight stages before waiting for earlier kernels
   int g128;         // scales and biases are [N][K/128] (one pair per 128 codes)
+  int fault_tx;     // debug: bytes the first stage of CTA 0's warp 0 expects beyond its copies
+  uint32_t wait_limit;  // tries of a stage wait (0: the default)
   int par_off;      // and then the byte offset of the per-unit parameter slots in shared memory
   const int32_t* ids;  // routed mode: expert id of each of T tokens, E experts of N rows each
   int T, E;
@@ -719,6 +725,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   R.issued = R.consumed = 0;
   R.pol_stream = policy_evict_first();
   R.pol_keep = policy_evict_last();
+  if (p.wait_limit) R.limit = p.wait_limit;
   // G128: a unit's scales and biases (its rows over the whole K, K / 64 bytes
   // a row) arrive with its first stage, into one of S slots per warp (a unit
   // has at least one stage, so at most S units are in flight)
@@ -845,7 +852,8 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
       }
       ++R.issued;
     } else {
-      slot = ring_issue_w<NSUB>(R, &maps, ist, irow, imc);
+      const bool fault = p.fault_tx && blockIdx.x == 0 && warp == 0 && R.issued == 0;
+      slot = ring_issue_w<NSUB>(R, &maps, ist, irow, imc, fault ? (uint32_t)p.fault_tx : 0u);
     }
     if (with_x) ring_issue_x(R, slot, ist, p.x, itok, imc, p.K);
     ++ist;
@@ -2196,6 +2204,10 @@ cudaError_t launch_tc_impl(const LaunchArgs& a, int32_t* idx, uint16_t* val) {
   // units dealt inside each CTA, and a split K taken by whole-K units that
   // fold the slice sums in registers (the same canonical sums).
   if (have_ws) use_workspace(p, a.ws);
+  if (a.fault_wait) {  // debug: one stage's wait runs out after 4096 tries
+    p.fault_tx = 16;
+    p.wait_limit = 1u << 12;
+  }
   // the persistent kernel: one launch per chunk of at most eight rows
   for (int r0 = 0; r0 < a.M; r0 += kMaxChunk) {
     p.row0 = a.row0 + r0;
