@@ -589,8 +589,12 @@ def measure_extras(torch, ops, synth, roofline, l2, peak, args):
     torch.cuda.synchronize()
     ms = time_graph_launches(torch, [lambda w=w: ops.mm_id(x, w, ids, out=y) for w in ws], 20)
     nb, touched = roofline.mm_id_bytes(ids_np, T, N, K, E)
+    # bytes read on speculation before the ids are known: the first 512-code
+    # stage of every expert, of which the untouched experts' are never used
+    spec = E * N * (512 // 2 + 512 // 64 * 4)
     out["routed"] = {"experts_touched": touched, "bytes": nb, "us": round(1e3 * ms, 2),
-                     "GBps": round(nb / (ms * 1e-3) / 1e9, 1), "frac": round(nb / (ms * 1e-3) / 1e9 / peak, 4)}
+                     "GBps": round(nb / (ms * 1e-3) / 1e9, 1), "frac": round(nb / (ms * 1e-3) / 1e9 / peak, 4),
+                     "l2_prefetch_bytes": spec, "l2_prefetch_wasted_bytes": (E - touched) * N * (512 // 2 + 512 // 64 * 4)}
     del ws
     # K % 512 != 0: the CUDA-core family (a hidden-2304 gate 9216x2304 and a 256000x2304 LM head), M = 1 and 5
     tail = {}

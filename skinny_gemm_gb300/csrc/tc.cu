@@ -94,7 +94,10 @@ namespace {
 #define W4A16_TC_GROUP_BATCH 2     // 64-groups whose loads and MMA chains are interleaved
 #endif
 #ifndef W4A16_TC_TILE_MAX_UNITS
-#define W4A16_TC_TILE_MAX_UNITS 4863  // largest stages x row tiles the tile kernel takes
+// largest stages x 32-row tiles the tile kernel takes (measured: at 6144 units
+// the tile kernel is 5-20% faster than the persistent grid, e.g. 24576x4096
+// at M = 4 19.2 against 24.5 us; from 7168 units on it is slower)
+#define W4A16_TC_TILE_MAX_UNITS 6655
 #endif
 #ifndef W4A16_TC_DYN_ALL
 #define W4A16_TC_DYN_ALL 1  // 0: deal units round-robin when K is not split
@@ -199,6 +202,12 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%2, %3}], [%4], %5;"
       ::"r"(dst), "l"(map), "r"(cx), "r"(cy), "r"(bar), "l"(policy)
       : "memory");
+}
+
+// A box of the tensor into L2 only (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int cx, int cy) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(cx), "r"(cy)
+               : "memory");
 }
 
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
@@ -561,6 +570,7 @@ struct StreamParams {
   int g128;         // scales and biases are [N][K/128] (one pair per 128 codes)
   int fault_tx;     // debug: bytes the first stage of CTA 0's warp 0 expects beyond its copies
   uint32_t wait_limit;  // tries of a stage wait (0: the default)
+  int l2_stages;        // routed mode: leading stages of every expert pulled into L2 before the ids are known
   int par_off;      // and then the byte offset of the per-unit parameter slots in shared memory
   const int32_t* ids;  // routed mode: expert id of each of T tokens, E experts of N rows each
   int T, E;
@@ -885,6 +895,20 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
       begin_unit(first_u < cta_hi ? first_u : -1);
       if (p.prefetch)
         for (int i = 0; i < S && iu >= 0 && ist < iend; ++i) issue_stage(false);
+    } else if (p.l2_stages > 0) {
+      // Routed: which experts are read is known only after the wait for the
+      // kernel that wrote the ids.  Until then the grid pulls the first
+      // l2_stages stages of every expert's tiles into L2 (a bounded budget;
+      // the bytes of experts no token selects are read for nothing).
+      const int per_e = p.tiles * p.l2_stages, total = p.E * per_e;
+      for (int k = gw; k < total; k += TW) {
+        const int e = k / per_e, r = k - e * per_e, tile = r / p.l2_stages, st = r - tile * p.l2_stages;
+        const int row = e * p.N + tile * kRows;
+        tma_prefetch_l2(&maps.codes, st * kStageWords, row);
+        tma_prefetch_l2(&maps.codes, st * kStageWords + kBoxWords, row);
+        tma_prefetch_l2(&maps.scales, st * 8, row);
+        tma_prefetch_l2(&maps.biases, st * 8, row);
+      }
     }
   }
   pdl_wait();
@@ -2253,6 +2277,9 @@ cudaError_t launch_stream_routed(const LaunchArgs& a, DeviceInfo& d) {
   p.tiles = cdiv(a.N, kTileRows);
   p.stages = stream_stages<2>(p.M);
   p.ids = a.ids; p.T = a.T; p.E = a.E;
+  // Before the ids arrive, pull the first stage of every expert into L2 when
+  // that costs at most 16 MB (the budget of bytes read on speculation).
+  p.l2_stages = a.pdl >= 2 && (int64_t)a.E * a.N * (kStageK / 2 + kStageK / kGroup * 4) <= (16 << 20) ? 1 : 0;
   Maps maps;
   if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, (int64_t)a.N * a.E, a.K, kTileRows)) return e;
   const int smem = stream_smem<2>(p.stages, p.M) + routed_table_bytes(a.T);
