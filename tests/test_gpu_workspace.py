@@ -26,7 +26,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 # (N, K): persistent-grid shapes with K split across SMs (ksplit > 1), one
 # without a split, and the LM head.
-SPLIT_SHAPES = [DENSE, (12288, 8192)]
+SPLIT_SHAPES = [DENSE, (16384, 8192)]
 NOSPLIT_SHAPE = (98304, 1536)
 
 
