@@ -24,7 +24,9 @@
  *   y[m][n] = sum_k x[m][k] * W[n][k]            float32 x and y
  *
  * Precision.  The activations enter the tensor cores as three bf16 parts
- * whose sum is x exactly; the products with ternary weights are exact; the
+ * (each the previous residual truncated to 8 significant bits) whose sum is
+ * x exactly for every finite |x| >= 2^-110 (and zero; smaller |x| lose at
+ * most 2^-133); the products with ternary weights are exact; the
  * accumulation is float32: one 256-weight block in the tensor core, then
  * y += d * block_sum with a fused multiply-add per block, the K slices and
  * the three parts added in a fixed order.  Bound (the parity tests use it):

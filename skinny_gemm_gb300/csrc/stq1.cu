@@ -14,9 +14,11 @@
 //    sign bits and scales with one 16-, one 4- and one 4-byte load.
 //  * The contraction runs on the tensor cores (mma.sync m16n8k16, bf16 in,
 //    fp32 accumulate).  Ternary lanes are exact in bf16; x enters as three
-//    bf16 parts h0 + h1 + h2 = x (exact: each part takes the next 8 bits of
-//    the 24-bit significand), as three columns of B, so the products are
-//    exact and only the fp32 accumulation rounds.  Within a block the MMA k
+//    bf16 parts h0 + h1 + h2 = x, each the previous residual truncated to
+//    its top 8 significant bits (exact for every finite |x| >= 2^-110: the
+//    lowest significand bit then sits at 2^-133 or above, the smallest bf16
+//    step; below that the parts lose at most 2^-133), as three columns of
+//    B, so the products are exact and only the fp32 accumulation rounds.  Within a block the MMA k
 //    order is chosen so that each lane's A fragment holds whole groups: k
 //    position 2t+i of chunk j is lane i of group 16t + j, position 2t+8+i is
 //    lane 2+i; lane t of a quad then owns groups 16t .. 16t+15, eight
@@ -160,15 +162,17 @@ __device__ void stage_rows(uint8_t* bsm, const float* __restrict__ x, const int*
           uint32_t bits[3][2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
+            // each part is the previous residual truncated to its top 16
+            // bits (a bf16 with the residual's sign and exponent), so no part
+            // rounds up and overflows, and every subtraction is exact
             const float f = v[u][2 * h + e];
-            const __nv_bfloat16 h0 = __float2bfloat16_rn(f);
-            const float r1 = __fsub_rn(f, __bfloat162float(h0));
-            const __nv_bfloat16 h1 = __float2bfloat16_rn(r1);
-            const float r2 = __fsub_rn(r1, __bfloat162float(h1));
-            const __nv_bfloat16 h2 = __float2bfloat16_rn(r2);
-            bits[0][e] = __bfloat16_as_ushort(h0);
-            bits[1][e] = __bfloat16_as_ushort(h1);
-            bits[2][e] = __bfloat16_as_ushort(h2);
+            const uint32_t b0 = __float_as_uint(f) & 0xFFFF0000u;
+            const float r1 = __fsub_rn(f, __uint_as_float(b0));
+            const uint32_t b1 = __float_as_uint(r1) & 0xFFFF0000u;
+            const float r2 = __fsub_rn(r1, __uint_as_float(b1));
+            bits[0][e] = b0 >> 16;
+            bits[1][e] = b1 >> 16;
+            bits[2][e] = __float_as_uint(r2) >> 16;
           }
 #pragma unroll
           for (int q = 0; q < 3; ++q) part[q][h] = bits[q][0] | (bits[q][1] << 16);
@@ -458,13 +462,25 @@ __global__ void __launch_bounds__(kThreads, 2) stq1_mm_kernel(const Params p) {
     return;
   }
   if (blockIdx.x == 0 && blockIdx.y == 0) {
-    // tokens routed outside 0..E-1 (one thread per token): zero rows and the device flag
-    for (int tt = threadIdx.x; tt < p.T; tt += blockDim.x) {
-      const int id = __ldg(p.ids + tt);
-      if (id < 0 || id >= p.E) {
-        atomicOr(p.flags, W4A16_DEVICE_BAD_ID);
-        for (int n = 0; n < p.N; ++n) p.y[(long long)tt * p.N + n] = 0.f;
+    // tokens routed outside 0..E-1: zero rows and the device flag.  The ids
+    // are checked a CTA's width at a time (one thread per token), the bad
+    // ones listed in shared memory, and their rows zeroed by every thread.
+    int* s_bad = reinterpret_cast<int*>(bsm);  // the activation area, not in use yet
+    int& s_nbad = s_bad[kThreads];
+    for (int t0 = 0; t0 < p.T; t0 += blockDim.x) {
+      if (threadIdx.x == 0) s_nbad = 0;
+      __syncthreads();
+      const int tt = t0 + (int)threadIdx.x;
+      if (tt < p.T) {
+        const int id = __ldg(p.ids + tt);
+        if (id < 0 || id >= p.E) s_bad[atomicAdd(&s_nbad, 1)] = tt;
       }
+      __syncthreads();
+      const int nbad = s_nbad;
+      if (nbad > 0 && threadIdx.x == 0) atomicOr(p.flags, W4A16_DEVICE_BAD_ID);
+      for (long long i = threadIdx.x; i < (long long)nbad * p.N; i += blockDim.x)
+        p.y[(long long)s_bad[i / p.N] * p.N + i % p.N] = 0.f;
+      __syncthreads();
     }
   }
   if (!p.flat) {  // one grid column per expert

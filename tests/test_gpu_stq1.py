@@ -223,3 +223,24 @@ def test_routed_and_row_gather_guard_bands():
     ops.stq1_get_rows(rows, w0, out=flat.view(5, K))
     _check_guards(buf, 5 * K)
     assert ops.device_status() == 0
+
+
+def test_extreme_activation_magnitudes():
+    """Activations near the float32 range's ends: |x| up to 3e38 (the three
+    truncated parts never overflow) and around 2^-120 (parts below the bf16
+    step may drop bits worth at most 2^-133 each, far inside the bound)."""
+    N, K = 48, 512
+    blocks = synth.make_stq1(31, N, K)
+    w = ops.STQ1Matrix.from_host(blocks, N, K)
+    rng = np.random.default_rng(5)
+    x = np.zeros((3, K), dtype=np.float32)
+    x[0, 7] = 3.0e38    # one value near the top of the range (a block sum of two such could overflow)
+    x[0, 300] = -2.5e38  # another block
+    x[1] = (rng.standard_normal(K) * 2.0 ** -120).astype(np.float32)
+    x[2] = rng.standard_normal(K).astype(np.float32) * np.float32(1e30)
+    y = ops.stq1_mm(dev_x(x), w)
+    yr, ad = oracle.stq1_mm(x, blocks, 3, N, K)
+    got = y.double().cpu().numpy()
+    assert np.all(np.isfinite(got[0])) and np.all(np.isfinite(got[2]))
+    tol = oracle.stq1_tolerance(ad, K) + 2.0 ** -133 * K
+    assert np.all(np.abs(got - yr) <= tol), float(np.max(np.abs(got - yr) - tol))
