@@ -82,7 +82,7 @@ namespace {
 #define W4A16_TC_STREAM_WARPS 4    // warps per CTA of the persistent kernel (32-row warps)
 #endif
 #ifndef W4A16_TC_MIN_BLOCKS
-#define W4A16_TC_MIN_BLOCKS 3      // persistent CTAs per SM the register budget must allow
+#define W4A16_TC_MIN_BLOCKS 2      // persistent CTAs per SM the register budget must allow
 #endif
 #ifndef W4A16_TC_MAX_STAGES
 #define W4A16_TC_MAX_STAGES 4      // deepest per-warp ring
@@ -110,6 +110,12 @@ namespace {
 #endif
 #ifndef W4A16_TC_TILE_SLICES
 #define W4A16_TC_TILE_SLICES 5        // most K-slices one CTA of the tile kernel takes, where a cluster can split
+#endif
+#ifndef W4A16_TC_PIPE
+#define W4A16_TC_PIPE 1  // persistent kernel: software-pipelined stage computation
+#endif
+#ifndef W4A16_TC_PIPE_BATCH
+#define W4A16_TC_PIPE_BATCH 1  // 64-groups per batch of the pipelined stage
 #endif
 
 constexpr int kTileRows = 32;           // two m16 subtiles per warp
@@ -230,6 +236,11 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Relaxed load at GPU scope (a counter other CTAs update atomically).
+// Release / acquire fence at GPU scope: with a relaxed atomic after (before)
+// it, the partial sums stored before it are visible to the warp that sees
+// the count.  Lighter than the sequentially consistent fence.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 __device__ __forceinline__ int ld_relaxed_gpu(const int* p) {
   int v;
   asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -519,6 +530,150 @@ __device__ __forceinline__ void compute_stage(uint32_t cbase, uint32_t pbase, ui
         }
     }
   }
+}
+
+// The same stage, software-pipelined for a warp that has the registers: the
+// shared-memory loads of group batch b + 1 go out before the MMAs of batch
+// b, and the rescale of batch b waits until the MMAs of batch b + 1 are
+// issued (its accumulators are complete by then).  Every p receives the
+// same operations in the same order as compute_stage, so the bits agree.
+template <int NSUB, bool ALLCOLS, bool XSTAGED, int BOXROWS = 16 * NSUB, bool G128 = false>
+__device__ __forceinline__ void compute_stage_pipe(uint32_t cbase, uint32_t pbase, uint32_t xbase, bool xvalid,
+                                                   uint32_t sxbase, uint32_t sx_stride, bool xvalid_cols,
+                                                   float (&p)[NSUB][4], const uint32_t (&loff)[NSUB][4], int g,
+                                                   uint32_t prow = 0, uint32_t pbias = 0) {
+  constexpr int GB = W4A16_TC_PIPE_BATCH, NB = 8 / GB;
+  constexpr uint32_t kBox = BOXROWS * 128, kBiases = BOXROWS * 16;
+  uint4 ps[2 * NSUB], pb[2 * NSUB];
+#pragma unroll
+  for (int i = 0; i < 2 * NSUB; ++i) {
+    const uint32_t r = 16 * (i >> 1) + g + 8 * (i & 1);
+    if (G128) {
+      const uint2 s2 = lds64u(pbase + r * prow), b2 = lds64u(pbase + pbias + r * prow);
+      ps[i] = make_uint4(s2.x, s2.y, 0u, 0u);
+      pb[i] = make_uint4(b2.x, b2.y, 0u, 0u);
+    } else {
+      ps[i] = lds128(pbase + r * 16);
+      pb[i] = lds128(pbase + kBiases + r * 16);
+    }
+  }
+  // Batch b uses buffer b % 2 of the loads and accumulators and b % 3 of the
+  // group sums: those of batch b - 1 are still to be read by its rescale
+  // when batch b + 1 is loaded.
+  uint32_t w[2][GB][NSUB][4];   // [buffer][group][subtile] code words
+  uint4 u[2][GB][2];            // [buffer][group][chunk] activations
+  float sx[3][GB][4];           // [buffer][group] group sums
+  float acc[2][GB][NSUB][4];    // [buffer][group][subtile]
+  auto load = [&](int b, int buf) {
+    const int sb = b % 3;
+#pragma unroll
+    for (int j = 0; j < GB; ++j) {
+      const int gi = b * GB + j;
+#pragma unroll
+      for (int s = 0; s < NSUB; ++s)
+        ldsm_x4(cbase + (gi >> 2) * kBox + loff[s][gi & 3], w[buf][j][s][0], w[buf][j][s][1], w[buf][j][s][2],
+                w[buf][j][s][3]);
+#pragma unroll
+      for (int cb = 0; cb < 2; ++cb) {
+        u[buf][j][cb] = make_uint4(0, 0, 0, 0);
+        if (xvalid) u[buf][j][cb] = lds128(xbase + 128 * gi + 64 * cb);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sx[sb][j][i] = 0.f;
+      if (XSTAGED && xvalid_cols) {
+        const float2 v = lds64f(sxbase + sx_stride * gi);
+        sx[sb][j][0] = v.x;
+        sx[sb][j][1] = v.y;
+      }
+    }
+  };
+  auto mmas = [&](int b, int buf) {
+    const int sb = b % 3;
+    uint32_t bx[GB][2][2][2];
+#pragma unroll
+    for (int j = 0; j < GB; ++j) {
+#pragma unroll
+      for (int cb = 0; cb < 2; ++cb) {
+        if (XSTAGED) {
+          bx[j][cb][0][0] = u[buf][j][cb].x;
+          bx[j][cb][0][1] = u[buf][j][cb].y;
+          bx[j][cb][1][0] = u[buf][j][cb].z;
+          bx[j][cb][1][1] = u[buf][j][cb].w;
+        } else {
+          frag_from_chunk(u[buf][j][cb], bx[j][cb]);
+        }
+      }
+#pragma unroll
+      for (int s = 0; s < NSUB; ++s)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[buf][j][s][i] = 0.f;
+    }
+#pragma unroll
+    for (int step = 0; step < 4; ++step) {
+      const int cb = step >> 1, h = step & 1;
+#pragma unroll
+      for (int j = 0; j < GB; ++j) {
+        if (!XSTAGED) mma_bf16(sx[sb][j], kOnes, kOnes, kOnes, kOnes, bx[j][cb][h][0], bx[j][cb][h][1]);
+#pragma unroll
+        for (int s = 0; s < NSUB; ++s) {
+          const uint32_t wg = w[buf][j][s][2 * cb], wg8 = w[buf][j][s][2 * cb + 1];
+          const uint32_t a0 = codes_as_bf16x2(wg >> (8 * h));
+          const uint32_t a1 = codes_as_bf16x2(wg8 >> (8 * h));
+          const uint32_t a2 = codes_as_bf16x2(wg >> (8 * h + 4));
+          const uint32_t a3 = codes_as_bf16x2(wg8 >> (8 * h + 4));
+          mma_bf16(acc[buf][j][s], a0, a1, a2, a3, bx[j][cb][h][0], bx[j][cb][h][1]);
+        }
+      }
+    }
+  };
+  auto rescale = [&](int b, int buf) {
+    const int sb = b % 3;
+#pragma unroll
+    for (int j = 0; j < GB; ++j) {
+      const int gi = b * GB + j;
+#pragma unroll
+      for (int s = 0; s < NSUB; ++s)
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          const int i = 2 * s + rr;
+          const int pi = G128 ? gi >> 1 : gi;
+          const uint32_t sw = component(ps[i], pi >> 1);
+          const uint32_t bw = component(pb[i], pi >> 1);
+          const float sc = (pi & 1) ? half_hi(sw) : half_lo(sw);
+          const float bi = (pi & 1) ? half_hi(bw) : half_lo(bw);
+          const float cc = __fmaf_rn(-128.0f, sc, bi);
+          p[s][2 * rr + 0] = __fmaf_rn(sc, acc[buf][j][s][2 * rr + 0], p[s][2 * rr + 0]);
+          p[s][2 * rr + 0] = __fmaf_rn(cc, sx[sb][j][0], p[s][2 * rr + 0]);
+          if (ALLCOLS) {
+            p[s][2 * rr + 1] = __fmaf_rn(sc, acc[buf][j][s][2 * rr + 1], p[s][2 * rr + 1]);
+            p[s][2 * rr + 1] = __fmaf_rn(cc, sx[sb][j][1], p[s][2 * rr + 1]);
+          }
+        }
+    }
+  };
+  load(0, 0);
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    if (b + 1 < NB) load(b + 1, (b + 1) & 1);
+    mmas(b, b & 1);
+    if (b > 0) rescale(b - 1, (b - 1) & 1);
+  }
+  rescale(NB - 1, (NB - 1) & 1);
+}
+
+// The persistent kernel's stage: pipelined unless W4A16_TC_PIPE is 0.
+template <int NSUB, bool ALLCOLS, bool XSTAGED, int BOXROWS = 16 * NSUB, bool G128 = false>
+__device__ __forceinline__ void compute_stage_sel(uint32_t cbase, uint32_t pbase, uint32_t xbase, bool xvalid,
+                                                  uint32_t sxbase, uint32_t sx_stride, bool xvalid_cols,
+                                                  float (&p)[NSUB][4], const uint32_t (&loff)[NSUB][4], int g,
+                                                  uint32_t prow = 0, uint32_t pbias = 0) {
+#if W4A16_TC_PIPE
+  compute_stage_pipe<NSUB, ALLCOLS, XSTAGED, BOXROWS, G128>(cbase, pbase, xbase, xvalid, sxbase, sx_stride,
+                                                            xvalid_cols, p, loff, g, prow, pbias);
+#else
+  compute_stage<NSUB, ALLCOLS, XSTAGED, BOXROWS, G128>(cbase, pbase, xbase, xvalid, sxbase, sx_stride, xvalid_cols,
+                                                       p, loff, g, prow, pbias);
+#endif
 }
 
 struct Shape {
@@ -943,42 +1098,43 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
 
   bool timed_out = false;
   if (XSTAGED) {
-    // Activation rows in B-fragment order (one bulk copy, then each 16-byte
-    // chunk permuted in place), then the sum of every 64-group of every row
-    // with the same MMA chain the per-stage path uses.  The copy goes out
-    // through the tensor-memory-access path, which returns it well ahead of
-    // per-thread loads while the first weight stages are in flight.
+    // Activation rows in B-fragment order and the sum of every 64-group of
+    // every row, from one bulk copy per row.  The copy goes out through the
+    // tensor-memory-access path, which returns it well ahead of per-thread
+    // loads while the first weight stages are in flight.
     timed_out = __syncthreads_or(!mbar_wait(xbar, 0)) != 0;
-    const int chunks = p.K / 8, total = timed_out ? 0 : mc * chunks;
-    for (int c = threadIdx.x; c < total; c += blockDim.x) {
-      const int n = c / chunks, wd = c - n * chunks;
-      const uint32_t a = xst + n * p.xpitch + 16 * wd;
-      uint32_t b[2][2];
-      frag_from_chunk(lds128(a), b);
-      sts128(a, make_uint4(b[0][0], b[0][1], b[1][0], b[1][1]));
-    }
-    __syncthreads();
-    // Group sums: one MMA chain yields eight groups of one activation row, the
-    // group in the MMA column (lanes with g = column load it).  An output
-    // column depends only on its own B column, so every sum has the bits of
-    // the per-stage chain (activation row in the column).  Four chains per
-    // warp at a time, interleaved.
+    // One pass over the staged rows: every 16-byte chunk is read, put in
+    // B-fragment order in registers and written back in place, and the same
+    // registers feed the group sums.  One MMA chain yields eight groups of
+    // one activation row, the group in the MMA column (lane (g, t) holds
+    // chunks t and 4 + t of group g, which together cover every chunk once).
+    // An output column depends only on its own B column, so every sum has
+    // the bits of the per-stage chain (activation row in the column).  Four
+    // chains per warp at a time, interleaved.
     const int nblk = p.K / kGroup / 8, tasks = timed_out ? 0 : mc * nblk;
     for (int k0 = warp; k0 < tasks; k0 += 4 * kW) {
       uint32_t b[4][2][2][2];
       float v[4][4];
+      uint4 raw[4][2];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int k = k0 + j * kW;
+        const int n = k / nblk, blk = k - n * nblk;
+#pragma unroll
+        for (int cb = 0; cb < 2; ++cb)
+          raw[j][cb] = k < tasks ? lds128(xst + n * p.xpitch + 128 * (8 * blk + g) + 64 * cb + 16 * t)
+                                 : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int k = k0 + j * kW;
         const int n = k / nblk, blk = k - n * nblk;
 #pragma unroll
         for (int cb = 0; cb < 2; ++cb) {
-          uint4 u = make_uint4(0, 0, 0, 0);
-          if (k < tasks) u = lds128(xst + n * p.xpitch + 128 * (8 * blk + g) + 64 * cb + 16 * t);
-          b[j][cb][0][0] = u.x;
-          b[j][cb][0][1] = u.y;
-          b[j][cb][1][0] = u.z;
-          b[j][cb][1][1] = u.w;
+          frag_from_chunk(raw[j][cb], b[j][cb]);
+          if (k < tasks)
+            sts128(xst + n * p.xpitch + 128 * (8 * blk + g) + 64 * cb + 16 * t,
+                   make_uint4(b[j][cb][0][0], b[j][cb][0][1], b[j][cb][1][0], b[j][cb][1][1]));
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) v[j][i] = 0.f;
@@ -1019,7 +1175,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
     // warp barrier order every lane's loads after the other units' partial
     // stores.  Loads are issued eight slices of both tiles at a time; the
     // additions stay in slice order.
-    if (lane == 0) __threadfence();
+    if (lane == 0) fence_acq_rel_gpu();
     __syncwarp();
     // lane = (column n0, row r): with 16 rows two columns at a time
     const int r = lane % kRows, n0 = lane / kRows;
@@ -1070,7 +1226,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   auto count_arrival = [&](int tile) {
     __syncwarp();
     if (lane == 0) {
-      __threadfence();
+      fence_acq_rel_gpu();
       cnt_old = atomicAdd(p.cnt + tile, 1);
     }
     cnt_tile = tile;
@@ -1135,12 +1291,12 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
         xbase = ordered(R.xs0 + slot * x_slot + g * kXPitch + 16 * t);
       }
       if (G128)
-        compute_stage<NSUB, ALLCOLS, XSTAGED, 16 * NSUB, true>(
+        compute_stage_sel<NSUB, ALLCOLS, XSTAGED, 16 * NSUB, true>(
             cbase, par0 + (cseq % (uint32_t)S) * pslot + (uint32_t)st * 8u, xbase, g < umc, sxbase, sx_cols(mc) * 4,
             2 * t < umc, acc, loff, g, prb, kRows * prb);
       else
-        compute_stage<NSUB, ALLCOLS, XSTAGED>(cbase, cbase + 2 * G::kBox, xbase, g < umc, sxbase, sx_cols(mc) * 4,
-                                              2 * t < umc, acc, loff, g);
+        compute_stage_sel<NSUB, ALLCOLS, XSTAGED>(cbase, cbase + 2 * G::kBox, xbase, g < umc, sxbase,
+                                                  sx_cols(mc) * 4, 2 * t < umc, acc, loff, g);
       if (FOLD && (st + 1 == fold_at || st + 1 == s1)) {
         const bool first = fold_at == s0 + p.sl;
 #pragma unroll

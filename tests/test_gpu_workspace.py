@@ -62,17 +62,19 @@ def test_split_shapes_use_the_split():
 
 
 def test_no_device_memory_taken_by_calls():
-    """After one warm-up call (module loading), w4a16_mm calls on a new
-    stream change nothing in the device's free memory."""
+    """After one warm-up call (module loading), w4a16_mm calls on a stream
+    the library has not seen change nothing in the device's free memory.
+    The stream is made before the first reading: torch's first stream
+    creation sets up its stream pool, which takes device memory of its own."""
     shapes = SPLIT_SHAPES + [NOSPLIT_SHAPE]
     ws = [dev_weights(31, N, K) for N, K in shapes]
     xs = [to_dev_bf16(synth.make_x(40, 2, K)) for _, K in shapes]
     ys = [torch.empty(2, N, dtype=torch.bfloat16, device="cuda") for N, _ in shapes]
     for x, w, y in zip(xs, ws, ys):
         ops.mm(x, w, out=y, workspace=None)
+    s = torch.cuda.Stream()
     torch.cuda.synchronize()
     free0, _ = torch.cuda.mem_get_info()
-    s = torch.cuda.Stream()
     with torch.cuda.stream(s):
         for _ in range(3):
             for x, w, y in zip(xs, ws, ys):

@@ -66,10 +66,12 @@ def test_noalloc_on_new_streams_takes_no_memory():
     ref = ops.mm(x, w)
     y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
     assert _noalloc(x, w, y) == ops.OK
-    torch.cuda.synchronize()
     # eager calls on a new stream: the device's free memory does not move
-    free0, _ = torch.cuda.mem_get_info()
+    # (the stream is made first: torch's first stream creation sets up its
+    # stream pool, which takes device memory of its own)
     s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
     with torch.cuda.stream(s):
         for _ in range(3):
             assert _noalloc(x, w, y) == ops.OK
