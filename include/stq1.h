@@ -23,15 +23,14 @@
  * get_rows for the row gather):
  *   y[m][n] = sum_k x[m][k] * W[n][k]            float32 x and y
  *
- * Precision.  The activations enter the tensor cores as three bf16 parts
- * (each the previous residual truncated to 8 significant bits) whose sum is
- * x exactly for every finite |x| >= 2^-110 (and zero; smaller |x| lose at
- * most 2^-133); the products with ternary weights are exact; the
- * accumulation is float32: one 256-weight block in the tensor core, then
- * y += d * block_sum with a fused multiply-add per block, the K slices and
- * the three parts added in a fixed order.  Bound (the parity tests use it):
+ * Precision.  Per group the four activations enter as a signed sum
+ * (x_r + e_q x_q) + e_p x_p over the three nonzero lanes p < q < r, rounded
+ * to float32 after each addition; the 64 group sums of a block are added in
+ * four chains (groups g = i mod 4, in order) and then (s0 + s1) + (s2 + s3);
+ * y += d * block_sum with a fused multiply-add per block; the K slices are
+ * added in slice order.  Bound (the parity tests use it):
  *   |y - y_ref| <= (2^-16 + (K/256 + 16) * 2^-23) * sum_k |x[m][k] W[n][k]|
- * Non-finite activations give NaN outputs.
+ * Non-finite activations give non-finite outputs.
  *
  * Batch invariance.  The K split and every reduction order depend on (N, K)
  * only; row m of any call equals, bit for bit, the one-row call on x[m], and
@@ -39,12 +38,12 @@
  *
  * Device layout.  The compute calls read a repacked copy (stq1_pack): for
  * every 16-row tile and block a 672-byte record (16 rows x 42 bytes, the
- * same bytes) arranged so that each lane of a warp loads its own codes,
- * sign bits and scales with three aligned loads:
- *   bytes   0..511  codes: lane L = 4*(r%8) + t holds 8 bytes of row r and
- *                   8 bytes of row r+8 (qs bytes 8t..8t+7 of each row)
- *   bytes 512..639  signs: lane L holds sign bytes 2t, 2t+1 of rows r, r+8
- *   bytes 640..671  d of rows r and r+8 at 640 + 4*(r%8)
+ * same bytes) in which each row's codes, sign bits and scale are
+ * contiguous, for a kernel that gives every lane one row:
+ *   bytes   0..255  qs bytes 0..15 of row r at 16*r
+ *   bytes 256..511  qs bytes 16..31 of row r at 256 + 16*r
+ *   bytes 512..639  sign bytes 0..7 of row r at 512 + 8*r
+ *   bytes 640..671  d of row r at 640 + 2*r
  * Records are ordered [ceil(N/16)][K/256]; rows past N are zero.
  *
  * Ownership and synchronisation.  All tensor pointers are DEVICE pointers
@@ -85,7 +84,7 @@ int stq1_pack(const uint8_t* blocks, uint8_t* packed, int N, int K, void* stream
 
 /* y[M][N] = x[M][K] W^T with W given as its repacked copy.  x 16-byte
  * aligned, y 4-byte aligned; M >= 0 (M = 0 is a no-op); rows go through in
- * passes of at most rows_per_pass (stq1_get_plan), each a single launch. */
+ * passes of at most rows_per_pass (stq1_get_plan, 8), each a single launch. */
 int stq1_mm(const float* x, const uint8_t* packed, float* y, int M, int N, int K, void* stream);
 
 /* Routed experts: packed holds E repacked N x K matrices back to back
@@ -97,9 +96,10 @@ int stq1_mm_id(const float* x, const uint8_t* packed, const int32_t* ids, float*
 /* Row gather: out[t][k] = W[ids[t]][k] as float32 (exact: d * v). */
 int stq1_get_rows(const uint8_t* packed, const int32_t* ids, float* out, int T, int N, int K, void* stream);
 
-/* The launch plan of (N, K): K split into ksplit slices per 16-row tile,
- * at most rows_per_pass activation rows per launch (shared memory holds
- * 6 * rows * K bytes of staged activations). */
+/* The launch plan of (N, K): 256 weight rows per CTA, K split into ksplit
+ * slices (the CTAs of one cluster, at most 8) of blocks_per_slice blocks
+ * (the last may be shorter), at most rows_per_pass activation rows per
+ * launch. */
 typedef struct {
   int ksplit;
   int blocks_per_slice;

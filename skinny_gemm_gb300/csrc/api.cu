@@ -494,11 +494,14 @@ int stq1_mm(const float* x, const uint8_t* packed, float* y, int M, int N, int K
   if (misaligned(x, 16) || misaligned(packed, 16) || misaligned(y, 4))
     return fail(W4A16_ERR_ALIGN, "x and packed must be 16-byte and y 4-byte aligned");
   if (env().fault == kFaultLaunch) return fail(W4A16_ERR_CUDA, "injected launch fault (W4A16_FAULT)");
+  int* flags = nullptr;
+  if (int rc = flag_pointer(&flags)) return rc;
   Stq1Plan pl;
   stq1_make_plan(N, K, &pl);
   for (int row0 = 0; row0 < M; row0 += pl.xcap) {
     const int rows = M - row0 < pl.xcap ? M - row0 : pl.xcap;
-    cudaError_t e = launch_stq1_mm(x, packed, y, rows, row0, N, K, static_cast<cudaStream_t>(stream));
+    cudaError_t e =
+        launch_stq1_mm(x, packed, y, rows, row0, N, K, flags, env().pdl, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "stq1_mm launch");
   }
   return W4A16_OK;
@@ -519,7 +522,8 @@ int stq1_mm_id(const float* x, const uint8_t* packed, const int32_t* ids, float*
   if (env().fault == kFaultLaunch) return fail(W4A16_ERR_CUDA, "injected launch fault (W4A16_FAULT)");
   int* flags = nullptr;
   if (int rc = flag_pointer(&flags)) return rc;
-  cudaError_t e = launch_stq1_mm_id(x, packed, ids, y, T, N, K, E, flags, static_cast<cudaStream_t>(stream));
+  cudaError_t e =
+      launch_stq1_mm_id(x, packed, ids, y, T, N, K, E, flags, env().pdl, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? W4A16_OK : cuda_fail(e, "stq1_mm_id launch");
 }
 

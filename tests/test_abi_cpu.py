@@ -267,10 +267,11 @@ def test_stq1_sizes_plans_and_errors(L, monkeypatch):
     assert L.stq1_get_plan(6144, 2048, ctypes.byref(plan)) == ops.OK
     assert (plan.ksplit, plan.blocks_per_slice, plan.rows_per_pass) == (8, 1, 8)
     assert L.stq1_get_plan(16384, 16384, ctypes.byref(plan)) == ops.OK
-    assert (plan.ksplit, plan.blocks_per_slice, plan.rows_per_pass) == (4, 16, 2)
+    assert (plan.ksplit, plan.blocks_per_slice, plan.rows_per_pass) == (4, 16, 8)
     assert L.stq1_get_plan(16, 256, ctypes.byref(plan)) == ops.OK and plan.ksplit == 1
     assert L.stq1_get_plan(4, 384, ctypes.byref(plan)) == ops.ERR_SHAPE
-    assert L.stq1_get_plan(4, 32768, ctypes.byref(plan)) == ops.OK and plan.rows_per_pass == 1
+    assert L.stq1_get_plan(4, 32768, ctypes.byref(plan)) == ops.OK and plan.rows_per_pass == 8
+    assert (plan.ksplit, plan.blocks_per_slice) == (8, 16)
     mm, mid, rows, pack = L.stq1_mm, L.stq1_mm_id, L.stq1_get_rows, L.stq1_pack
     assert mm(P, P, P, 0, 64, 512, None) == ops.OK                      # M == 0: no-op
     assert mm(P, P, P, -1, 64, 512, None) == ops.ERR_SHAPE
@@ -297,11 +298,10 @@ def test_stq1_sizes_plans_and_errors(L, monkeypatch):
 
 
 def test_stq1_plans_depend_on_shape_only():
-    """The K split and the rows per pass are functions of (N, K): a power of two
-    of slices up to 8 and no more than the blocks, enough 16-row-tile slices to
-    give every SM work (or all the split there is), and the largest power of
-    two of rows up to 8 whose staged activation parts (6 bytes per row and k)
-    fit in one CTA's shared memory."""
+    """The K split and the rows per pass are functions of (N, K): 256 weight
+    rows per CTA, K over a cluster of at most 8 CTAs and at most one slice
+    per block, as many slices as keep the grid within 256 CTAs (one wave at
+    two per SM), each slice non-empty; eight activation rows per pass."""
     L = ops.lib()
     for N, K in [(16, 256), (6144, 2048), (16384, 16384), (2048, 2560), (300, 4096), (262144, 1536),
                  (40, 32768), (7, 8192), (1000, 12288)]:
@@ -312,11 +312,11 @@ def test_stq1_plans_depend_on_shape_only():
             plans.append((p.ksplit, p.blocks_per_slice, p.rows_per_pass))
         ks, bps, rows = plans[0]
         assert plans[0] == plans[1]
-        nb, tiles = K // 256, -(-N // 16)
-        assert ks in (1, 2, 4, 8) and ks <= nb and bps == -(-nb // ks)
-        assert tiles * ks >= 2432 or ks == min(8, 1 << (nb.bit_length() - 1)), (N, K, ks)
-        assert rows in (1, 2, 4, 8) and 6 * rows * K <= 227 * 1024
-        assert rows == 8 or 6 * (2 * rows) * K > 200 * 1024, (N, K, rows)
+        nb, groups = K // 256, -(-N // 256)
+        assert 1 <= ks <= min(8, nb) and (ks - 1) * bps < nb <= ks * bps, (N, K, ks, bps)
+        want = max(1, min(8, nb, 256 // groups))
+        assert bps == -(-nb // want), (N, K, ks, bps)
+        assert rows == 8
 
 
 def test_stq1_python_layer_checks_before_any_launch():

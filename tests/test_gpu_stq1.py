@@ -36,9 +36,9 @@ def check(y: torch.Tensor, yr: np.ndarray, ad: np.ndarray, K: int, what: str):
                                    (300, 2048, 5), (1000, 4096, 8), (37, 1024, 11), (129, 768, 2), (6144, 2048, 1),
                                    (6144, 2048, 4)])
 def test_parity_full(N, K, M):
-    """Ragged row tiles (N % 16 != 0, down to one row), K = 1..16 blocks, every
-    K split of the plan (1, 2, 4, 8 slices), one to eight rows, and several
-    passes (M = 11)."""
+    """Ragged row tiles (N % 16 != 0, down to one row), K = 1..16 blocks, K
+    split over clusters of 1 to 8 CTAs, one to eight rows, and two passes
+    (M = 11)."""
     blocks = synth.make_stq1(N + K, N, K)
     x = synth.make_x_f32(M, M, K)
     w = ops.STQ1Matrix.from_host(blocks, N, K)
@@ -49,8 +49,8 @@ def test_parity_full(N, K, M):
 
 @pytest.mark.parametrize("M", [1, 2, 3])
 def test_parity_16384_sampled(M):
-    """The page's 16384x16384 matvec (and two and three rows: passes of two),
-    sampled output columns in every 16-row tile position."""
+    """The page's 16384x16384 matvec (and two and three rows), sampled output
+    columns in every 16-row tile position (four K slices of 16 blocks)."""
     N = K = 16384
     blocks = synth.make_stq1(16, N, K)
     x = synth.make_x_f32(160 + M, M, K)
@@ -170,9 +170,10 @@ def test_mm_id_many_experts_grid_per_expert():
     assert ops.device_status() == 0
 
 
-def test_largest_k_one_row_per_pass():
+def test_largest_k():
+    """K = 32768: eight slices of 16 blocks, three rows in one pass."""
     N, K, M = 40, 32768, 3
-    assert ops.stq1_get_plan(N, K)["rows_per_pass"] == 1
+    assert ops.stq1_get_plan(N, K) == {"ksplit": 8, "blocks_per_slice": 16, "rows_per_pass": 8}
     blocks = synth.make_stq1(14, N, K)
     x = synth.make_x_f32(14, M, K)
     w = ops.STQ1Matrix.from_host(blocks, N, K)
@@ -226,9 +227,9 @@ def test_routed_and_row_gather_guard_bands():
 
 
 def test_extreme_activation_magnitudes():
-    """Activations near the float32 range's ends: |x| up to 3e38 (the three
-    truncated parts never overflow) and around 2^-120 (parts below the bf16
-    step may drop bits worth at most 2^-133 each, far inside the bound)."""
+    """Activations near the float32 range's ends: |x| up to 3e38 (one such
+    value per group, so no table entry overflows) and around 2^-120 (float32
+    additions keep subnormal values)."""
     N, K = 48, 512
     blocks = synth.make_stq1(31, N, K)
     w = ops.STQ1Matrix.from_host(blocks, N, K)
