@@ -68,18 +68,29 @@ constexpr int kMaxRows = 8;            // activation rows per pass
 constexpr int kMaxCluster = 8;
 constexpr int kWaveCtas = 256;         // CTAs that surely run at once (two per SM, clusters packed)
 
-// Table of one pass of MR activation rows: [MR][32 labels][kGc(MR) + 1]
-// floats, kGc groups of (8 / MR) blocks; the row stride is odd so that the
-// 32 labels of one group fall in 32 distinct banks.
+// Table of one pass of MR activation rows over (8 / MR) blocks: per row and
+// block kTabBlock bytes (33 x 256, so every block starts 256-byte aligned);
+// in a block the 32 pairs of groups (2q, 2q + 1) are kPairBytes apart, the
+// even group's 32 entries (one per label) at 0, the odd group's at 128.  A
+// lookup address is then the block's base with its low byte replaced by the
+// label's byte offset (one byte permute) plus an immediate; the pair stride
+// (65 words) puts the 32 labels of a group in 32 distinct banks.  The table
+// area starts at the first 256-byte boundary of the dynamic shared memory.
+constexpr int kPairBytes = 260;
+constexpr int kTabBlock = 33 * 256;
 __host__ __device__ constexpr int tab_blocks(int mr) { return 8 / mr; }
-__host__ __device__ constexpr int tab_stride(int mr) { return 64 * tab_blocks(mr) + 1; }
-__host__ __device__ constexpr int tab_bytes(int mr) { return mr * 32 * tab_stride(mr) * 4; }
+__host__ __device__ constexpr int tab_row_bytes(int mr) { return tab_blocks(mr) * kTabBlock; }
+__host__ __device__ constexpr int tab_bytes(int mr) { return mr * tab_row_bytes(mr) + 256; }
 __host__ __device__ constexpr int ring_off(int mr) { return (tab_bytes(mr) + 127) & ~127; }
 __host__ __device__ constexpr int bar_off(int mr) { return ring_off(mr) + kWarps * kDepth * kSlot; }
 __host__ __device__ constexpr int tok_off(int mr) { return bar_off(mr) + kWarps * kDepth * 8; }
 __host__ __device__ constexpr int smem_bytes(int mr) { return tok_off(mr) + 4 * (kMaxRows + 2); }
-static_assert(kMaxCluster * kMaxRows * kRowsCta * 4 <= tab_bytes(1), "slice sums fit the table area");
-static_assert(kThreads * 4 + 4 <= tab_bytes(1), "the bad-id list fits the table area");
+static_assert(kMaxCluster * kMaxRows * kRowsCta * 4 + 256 <= tab_bytes(1), "slice sums fit the table area");
+static_assert(kThreads * 4 + 4 + 256 <= tab_bytes(1), "the bad-id list fits the table area");
+static_assert(32 * kPairBytes <= kTabBlock && 31 * kPairBytes + 256 <= kTabBlock, "pairs fit a block");
+
+// Offset of the 256-byte aligned table area from the dynamic shared memory.
+__device__ __forceinline__ uint32_t tab_align(uint32_t sbase) { return (256u - (sbase & 255u)) & 255u; }
 
 struct Params {
   const float* x;
@@ -120,22 +131,21 @@ __device__ __forceinline__ uint32_t word4(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-// Table labels (code | sign << 4, one per byte) of the 8 groups of one code
-// word: `even` holds groups 0, 2, 4, 6 in bytes 0..3, `odd` groups 1, 3, 5, 7;
-// s8 has the sign of group k at bit k.  The multiply moves sign bits 0, 2, 4,
-// 6 to bits 4, 12, 20, 28 (its other partial products land elsewhere and are
-// masked off).
+// Byte offsets in a pair of groups (4 * label, label = code | sign << 4,
+// plus 128 for the odd group) of the 8 groups of one code word: `even` holds
+// groups 0, 2, 4, 6 in bytes 0..3, `odd` groups 1, 3, 5, 7; s8 has the sign
+// of group k at bit k.  The multiply moves sign bits 0, 2, 4, 6 to bits 6,
+// 14, 22, 30 (its other partial products land elsewhere and are masked off).
 __device__ __forceinline__ void labels8(uint32_t w, uint32_t s8, uint32_t& even, uint32_t& odd) {
-  constexpr uint32_t kSpread = 0x00410410u;
-  even = (w & 0x0F0F0F0Fu) | (((s8 & 0x55u) * kSpread) & 0x10101010u);
-  odd = ((w >> 4) & 0x0F0F0F0Fu) | ((((s8 >> 1) & 0x55u) * kSpread) & 0x10101010u);
+  constexpr uint32_t kSpread = 0x01041040u;
+  even = ((w << 2) & 0x3C3C3C3Cu) | (((s8 & 0x55u) * kSpread) & 0x40404040u);
+  odd = ((w >> 2) & 0x3C3C3C3Cu) | ((((s8 >> 1) & 0x55u) * kSpread) & 0x40404040u) | 0x80808080u;
 }
 
 // The table of one chunk of blocks (cb .. ce - 1) for activation rows
 // tok[0 .. mrows): MR * tab_blocks(MR) * 64 = 512 (row, group) items, at most
 // two per thread.  Their activations are loaded (xload) while the previous
-// chunk's lookups run, then turned into entries: entry (label, group) of row
-// m at ((m * 32 + label) * tab_stride + group) floats.
+// chunk's lookups run, then turned into entries (layout: tab_row_bytes).
 constexpr int kItems = 512 / kThreads;
 
 template <int MR>
@@ -156,15 +166,15 @@ __device__ __forceinline__ void xload(const Params& p, const int* tok, int mrows
 }
 
 template <int MR>
-__device__ __forceinline__ void build_table(float* tab, int mrows, int cb, int ce, const float (&xl)[kItems][4]) {
-  constexpr int S = tab_stride(MR);
+__device__ __forceinline__ void build_table(uint8_t* tab, int mrows, int cb, int ce, const float (&xl)[kItems][4]) {
   const int groups = (ce - cb) * 64, items = mrows * groups;
 #pragma unroll
   for (int u = 0; u < kItems; ++u) {
     const int it = (int)threadIdx.x + u * kThreads;
     if (it >= items) continue;
     const int m = it / groups, gi = it - m * groups;
-    float* t = tab + (m * 32) * S + gi;
+    float* t = reinterpret_cast<float*>(tab + m * tab_row_bytes(MR) + (gi >> 6) * kTabBlock +
+                                        ((gi & 63) >> 1) * kPairBytes + (gi & 1) * 128);
 #pragma unroll
     for (int z = 0; z < 4; ++z) {  // the zero lane; p < q < r the others
       const float xp = xl[u][z == 0 ? 1 : 0], xq = xl[u][z <= 1 ? 2 : 1], xr = xl[u][z <= 2 ? 3 : 2];
@@ -172,8 +182,8 @@ __device__ __forceinline__ void build_table(float* tab, int mrows, int cb, int c
       const float e[4] = {__fadd_rn(uu, xp), __fsub_rn(uu, xp), __fadd_rn(v, xp), __fsub_rn(v, xp)};
 #pragma unroll
       for (int f = 0; f < 4; ++f) {  // code 4z + f: bit 0 negates lane p, bit 1 lane q
-        t[(4 * z + f) * S] = e[f];
-        t[(16 + 4 * z + f) * S] = -e[f];
+        t[4 * z + f] = e[f];
+        t[16 + 4 * z + f] = -e[f];
       }
     }
   }
@@ -181,12 +191,10 @@ __device__ __forceinline__ void build_table(float* tab, int mrows, int cb, int c
 
 // One block of this lane's row: the 64 groups' entries of every activation
 // row summed as (s_0 + s_1) + (s_2 + s_3), s_i over the groups i (mod 4).
-// `base` addresses the block's first group in activation row 0's table.
+// `base` (256-byte aligned) addresses the block in activation row 0's table.
 template <int MR>
 __device__ __forceinline__ void block_sums(const uint4& c0, const uint4& c1, const uint2& sg, uint32_t base,
                                            float (&bsum)[MR]) {
-  constexpr uint32_t kLabelBytes = 4u * tab_stride(MR);
-  constexpr uint32_t kRowBytes = 32u * kLabelBytes;
   float ch[MR][4];
 #pragma unroll
   for (int wi = 0; wi < 8; ++wi) {
@@ -196,12 +204,11 @@ __device__ __forceinline__ void block_sums(const uint4& c0, const uint4& c1, con
     labels8(w, s8, lab[0], lab[1]);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const int g = 8 * wi + k;  // byte k >> 1 of lab[k & 1]
-      const uint32_t label = __byte_perm(lab[k & 1], 0u, 0x4440u | (uint32_t)(k >> 1));
-      const uint32_t a = label * kLabelBytes + base + 4u * (uint32_t)g;
+      const int g = 8 * wi + k;  // byte k >> 1 of lab[k & 1]; pair g >> 1
+      const uint32_t a = __byte_perm(lab[k & 1], base, 0x7650u | (uint32_t)(k >> 1));
 #pragma unroll
       for (int m = 0; m < MR; ++m) {
-        const float v = lds_f32(a + m * kRowBytes);
+        const float v = lds_f32(a + (uint32_t)((g >> 1) * kPairBytes + m * tab_row_bytes(MR)));
         ch[m][g & 3] = g < 4 ? v : __fadd_rn(ch[m][g & 3], v);
       }
     }
@@ -218,7 +225,9 @@ __device__ bool run_pass(const Params& p, const uint8_t* wmat, uint8_t* smem, co
                          int rg, uint32_t& issued, uint32_t& consumed, uint64_t pol, bool requested) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = smem_u32(smem);
-  float* tab = reinterpret_cast<float*>(smem);
+  const uint32_t talign = tab_align(sbase);
+  uint8_t* tab = smem + talign;  // 256-byte aligned
+  float* part = reinterpret_cast<float*>(tab);
   const uint32_t ring = sbase + ring_off(MR) + warp * kDepth * kSlot;
   const uint32_t bars = sbase + bar_off(MR) + warp * kDepth * 8;
   const int row_w = rg * kRowsCta + 32 * warp;  // the warp's first weight row
@@ -280,7 +289,7 @@ __device__ bool run_pass(const Params& p, const uint8_t* wmat, uint8_t* smem, co
         request(next_b++);
       }
       float bsum[MR];
-      block_sums<MR>(c0, c1, sg, sbase + 4u * (uint32_t)((b - cb) * 64), bsum);
+      block_sums<MR>(c0, c1, sg, sbase + talign + (uint32_t)((b - cb) * kTabBlock), bsum);
       const float d = __half2float(__ushort_as_half(dh));
 #pragma unroll
       for (int m = 0; m < MR; ++m) acc[m] = __fmaf_rn(d, bsum[m], acc[m]);
@@ -310,15 +319,16 @@ __device__ bool run_pass(const Params& p, const uint8_t* wmat, uint8_t* smem, co
 #pragma unroll
     for (int m = 0; m < MR; ++m)
       if (m < mrows)
-        st_cluster_f32(cluster_map(sbase + 4u * (uint32_t)((rank * kMaxRows + m) * kRowsCta + row_c), 0u), acc[m]);
+        st_cluster_f32(cluster_map(sbase + talign + 4u * (uint32_t)((rank * kMaxRows + m) * kRowsCta + row_c), 0u),
+                     acc[m]);
   cluster_arrive();
   cluster_wait();
   if (rank == 0) {
     for (int o = threadIdx.x; o < mrows * kRowsCta; o += kThreads) {
       const int m = o / kRowsCta, r = o - m * kRowsCta, nn = rg * kRowsCta + r;
       if (nn >= p.N) continue;
-      float s = tab[m * kRowsCta + r];
-      for (int k = 1; k < p.ks; ++k) s = __fadd_rn(s, tab[(k * kMaxRows + m) * kRowsCta + r]);
+      float s = part[m * kRowsCta + r];
+      for (int k = 1; k < p.ks; ++k) s = __fadd_rn(s, part[(k * kMaxRows + m) * kRowsCta + r]);
       p.y[(long long)tok[m] * p.N + nn] = s;
     }
   }
