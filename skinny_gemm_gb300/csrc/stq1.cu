@@ -66,6 +66,7 @@ constexpr int kDepth = 4;              // blocks in flight per warp
 constexpr int kSlot = 2 * kRec;        // one block of a warp's two 16-row tiles
 constexpr int kMaxRows = 8;            // activation rows per pass
 constexpr int kMaxCluster = 8;
+constexpr int kMaxSpc = 4;  // K slices one CTA may take
 constexpr int kWaveCtas = 256;         // CTAs that surely run at once (two per SM, clusters packed)
 
 // Table of one pass of MR activation rows over (8 / MR) blocks: per row and
@@ -104,6 +105,7 @@ struct Params {
   long long wstride;   // bytes per expert
   int T, E;            // routed
   int prefetch;        // request the first records before waiting for earlier kernels
+  int spc, csz;        // K slices per CTA (1 .. kMaxSpc) and CTAs per cluster (ceil(ks / spc))
 };
 
 // bf16 bits of lane l of a group with code c and sign bit s (the row gather).
@@ -220,7 +222,8 @@ __device__ __forceinline__ void block_sums(const uint4& c0, const uint4& c1, con
 // The (up to MR) activation rows of one pass over this CTA's 256 weight rows
 // and K slice; the slice sums go to the first CTA of the cluster, which adds
 // them in slice order and writes y.  Returns false when a record wait ran out.
-template <int MR>
+// MULTI: the CTA may take several K slices (p.spc > 1; routed calls).
+template <int MR, bool MULTI>
 __device__ bool run_pass(const Params& p, const uint8_t* wmat, uint8_t* smem, const int* tok, int mrows, int rank,
                          int rg, uint32_t& issued, uint32_t& consumed, uint64_t pol, bool requested) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -235,7 +238,9 @@ __device__ bool run_pass(const Params& p, const uint8_t* wmat, uint8_t* smem, co
   const int ntiles = row_w < p.N ? min(2, p.tiles - tile0) : 0;
   const int half = lane >> 4, r16 = lane & 15;
   const bool lane_rec = half < ntiles;  // the lane's record exists (rows past N in it are zero)
-  const int b0 = rank * p.bps, b1 = min(p.nb, b0 + p.bps);
+  // this CTA's K slices s0 .. s1 - 1 and their blocks
+  const int s0 = rank * p.spc, s1 = min(p.ks, s0 + p.spc);
+  const int b0 = s0 * p.bps, b1 = min(p.nb, s1 * p.bps);
   bool ok = true;
 
   // lane 0 requests block b into the next slot; every lane counts it
@@ -256,11 +261,34 @@ __device__ bool run_pass(const Params& p, const uint8_t* wmat, uint8_t* smem, co
     for (int b = b0; b < next_b; ++b) request(b);
   }
 
-  float acc[MR];
+  // acc: the current slice's sum.  The first CTA of a cluster folds its
+  // finished slices' sums in slice order (fold); the others keep each one
+  // (sl) for the first CTA to fold in after its own.
+  constexpr int SPC = MULTI ? kMaxSpc : 1;
+  float acc[MR], fold[MR], sl[SPC][MR];
 #pragma unroll
-  for (int m = 0; m < MR; ++m) acc[m] = 0.f;
+  for (int m = 0; m < MR; ++m) {
+    acc[m] = fold[m] = 0.f;
+#pragma unroll
+    for (int j = 0; j < SPC; ++j) sl[j][m] = 0.f;
+  }
+  auto slice_done = [&](int j) {  // local slice j (0 .. spc - 1) has ended
+    if (rank == 0) {
+#pragma unroll
+      for (int m = 0; m < MR; ++m) fold[m] = j == 0 ? acc[m] : __fadd_rn(fold[m], acc[m]);
+    } else {
+#pragma unroll
+      for (int jj = 0; jj < SPC; ++jj)
+#pragma unroll
+        for (int m = 0; m < MR; ++m)
+          if (jj == j) sl[jj][m] = acc[m];
+    }
+#pragma unroll
+    for (int m = 0; m < MR; ++m) acc[m] = 0.f;
+  };
   float xl[kItems][4];
   xload<MR>(p, tok, mrows, b0, min(b1, b0 + tab_blocks(MR)), xl);
+  int slice_end = b0 + p.bps;  // MULTI: the first block of the next slice
   for (int cb = b0; cb < b1; cb += tab_blocks(MR)) {
     const int ce = min(b1, cb + tab_blocks(MR));
     __syncthreads();  // the previous chunk's lookups are done
@@ -291,10 +319,15 @@ __device__ bool run_pass(const Params& p, const uint8_t* wmat, uint8_t* smem, co
       float bsum[MR];
       block_sums<MR>(c0, c1, sg, sbase + talign + (uint32_t)((b - cb) * kTabBlock), bsum);
       const float d = __half2float(__ushort_as_half(dh));
+      if (MULTI && b == slice_end) {
+        slice_done((b - b0) / p.bps - 1);
+        slice_end += p.bps;
+      }
 #pragma unroll
       for (int m = 0; m < MR; ++m) acc[m] = __fmaf_rn(d, bsum[m], acc[m]);
     }
   }
+  slice_done(s1 - 1 - s0);
   if (!ok) {
     // let the copies in flight land before the slots are released
     while (consumed < issued) {
@@ -303,24 +336,35 @@ __device__ bool run_pass(const Params& p, const uint8_t* wmat, uint8_t* smem, co
     }
   }
 
-  // slice sums: [slice][activation row][row of the CTA] in the first CTA's table area
+  // slice sums: [slice][activation row][row of the CTA] in the first CTA's
+  // table area; slot 0 holds the first CTA's fold of its slices
   const int row_c = 32 * warp + lane, n = rg * kRowsCta + row_c;
-  if (p.ks == 1) {
+  if (p.csz == 1) {
     if (n < p.N)
 #pragma unroll
       for (int m = 0; m < MR; ++m)
-        if (m < mrows) p.y[(long long)tok[m] * p.N + n] = acc[m];
+        if (m < mrows) p.y[(long long)tok[m] * p.N + n] = fold[m];
     return ok;
   }
+  auto to_first = [&](int slice, int m, float v) {
+    st_cluster_f32(cluster_map(sbase + talign + 4u * (uint32_t)((slice * kMaxRows + m) * kRowsCta + row_c), 0u), v);
+  };
   __syncthreads();  // every warp's table reads are done
   cluster_arrive();
   cluster_wait();  // ... in every CTA of the cluster
-  if (n < p.N)
+  if (n < p.N) {
 #pragma unroll
-    for (int m = 0; m < MR; ++m)
-      if (m < mrows)
-        st_cluster_f32(cluster_map(sbase + talign + 4u * (uint32_t)((rank * kMaxRows + m) * kRowsCta + row_c), 0u),
-                     acc[m]);
+    for (int m = 0; m < MR; ++m) {
+      if (m >= mrows) continue;
+      if (rank == 0) {
+        to_first(0, m, fold[m]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < SPC; ++j)
+          if (j < s1 - s0) to_first(s0 + j, m, sl[j][m]);
+      }
+    }
+  }
   cluster_arrive();
   cluster_wait();
   if (rank == 0) {
@@ -328,7 +372,7 @@ __device__ bool run_pass(const Params& p, const uint8_t* wmat, uint8_t* smem, co
       const int m = o / kRowsCta, r = o - m * kRowsCta, nn = rg * kRowsCta + r;
       if (nn >= p.N) continue;
       float s = part[m * kRowsCta + r];
-      for (int k = 1; k < p.ks; ++k) s = __fadd_rn(s, part[(k * kMaxRows + m) * kRowsCta + r]);
+      for (int k = p.spc; k < p.ks; ++k) s = __fadd_rn(s, part[(k * kMaxRows + m) * kRowsCta + r]);
       p.y[(long long)tok[m] * p.N + nn] = s;
     }
   }
@@ -341,8 +385,8 @@ __global__ void __launch_bounds__(kThreads, 2) stq1_tab_kernel(const Params p) {
   pdl_launch_dependents();
   int* tok = reinterpret_cast<int*>(smem + tok_off(MR));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rank = p.ks > 1 ? (int)cluster_rank() : 0;
-  const int rg = (int)blockIdx.x / p.ks;
+  const int rank = p.csz > 1 ? (int)cluster_rank() : 0;
+  const int rg = (int)blockIdx.x / p.csz;
   const int e = ROUTED ? (int)blockIdx.y : 0;
   const uint8_t* wmat = p.w + (long long)e * p.wstride;
   const uint64_t pol = policy_evict_first();
@@ -358,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 2) stq1_tab_kernel(const Params p) {
   if (early) {
     const int row_w = rg * kRowsCta + 32 * warp, tile0 = row_w >> 4;
     const int ntiles = row_w < p.N ? min(2, p.tiles - tile0) : 0;
-    const int b0 = rank * p.bps, b1 = min(p.nb, b0 + p.bps);
+    const int b0 = rank * p.spc * p.bps, b1 = min(p.nb, (rank + 1) * p.spc * p.bps);
     for (int b = b0; b < b1 && b < b0 + kDepth && ntiles > 0; ++b) {
       if (lane == 0) {
         const uint32_t slot = issued % kDepth;
@@ -433,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 2) stq1_tab_kernel(const Params p) {
       mrows = p.M;
       __syncthreads();
     }
-    ok = run_pass<MR>(p, wmat, smem, tok, mrows, rank, rg, issued, consumed, pol, early) && ok;
+    ok = run_pass<MR, ROUTED>(p, wmat, smem, tok, mrows, rank, rg, issued, consumed, pol, early) && ok;
     if (!ROUTED) break;
   }
   if (!ok && lane == 0 && p.flags) atomicOr(p.flags, W4A16_DEVICE_TIMEOUT);
@@ -520,16 +564,16 @@ cudaError_t launch_tab(const Params& p, int pdl, cudaStream_t s) {
     }
   }
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3((unsigned)(p.ks * p.rgroups), ROUTED ? (unsigned)p.E : 1u, 1u);
+  cfg.gridDim = dim3((unsigned)(p.csz * p.rgroups), ROUTED ? (unsigned)p.E : 1u, 1u);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)smem_bytes(MR);
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   cfg.attrs = attr;
   unsigned n = 0;
-  if (p.ks > 1) {
+  if (p.csz > 1) {
     attr[n].id = cudaLaunchAttributeClusterDimension;
-    attr[n].val.clusterDim.x = (unsigned)p.ks;
+    attr[n].val.clusterDim.x = (unsigned)p.csz;
     attr[n].val.clusterDim.y = 1;
     attr[n].val.clusterDim.z = 1;
     ++n;
@@ -565,6 +609,8 @@ Params base_params(int N, int K) {
   p.rgroups = pl.rgroups;
   p.ks = pl.ks;
   p.bps = pl.bps;
+  p.spc = 1;  // one K slice per CTA: a cluster of ks CTAs per row group
+  p.csz = pl.ks;
   p.wstride = (long long)stq1_packed_size(N, K);
   return p;
 }
@@ -631,6 +677,11 @@ cudaError_t launch_stq1_mm_id(const float* x, const uint8_t* w, const int32_t* i
   p.flags = flags;
   p.T = T;
   p.E = E;
+  // Routed calls touch many experts: each CTA takes up to kMaxSpc K slices
+  // of its rows (the same slice sums, folded in the same order), so the grid
+  // has fewer, longer CTAs per expert.
+  p.spc = std::min(p.ks, kMaxSpc);
+  p.csz = (p.ks + p.spc - 1) / p.spc;
   // Tokens per pass: twice the mean per expert (at least two), at most T and
   // eight; an expert with more tokens takes more passes.
   long long want = 2LL * ((T + E - 1) / E);
