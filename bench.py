@@ -596,15 +596,17 @@ def measure_extras(torch, ops, synth, roofline, l2, peak, args):
                      "GBps": round(nb / (ms * 1e-3) / 1e9, 1), "frac": round(nb / (ms * 1e-3) / 1e9 / peak, 4),
                      "l2_prefetch_bytes": spec, "l2_prefetch_wasted_bytes": (E - touched) * N * (512 // 2 + 512 // 64 * 4)}
     del ws
-    # K % 512 != 0: the CUDA-core family (a hidden-2304 gate 9216x2304 and a 256000x2304 LM head), M = 1 and 5
+    # K % 512 != 0 (a hidden-2304 gate 9216x2304 and a 256000x2304 LM head), M = 1 and 5: the
+    # tensor-core kernels on K padded to whole stages (the default) against the CUDA-core family
     tail = {}
     for (N, K) in [(9216, 2304), (256000, 2304)]:
         ws = cold_set(N, K, 10)
         t1, t5 = timed(ws, 1, N, K, 20), timed(ws, 5, N, K, 20)
+        s1, s5 = timed(ws, 1, N, K, 20, kernel="simt"), timed(ws, 5, N, K, 20, kernel="simt")
         tail[f"{N}x{K}"] = {"kernel": ops.get_plan(N, K)["kernel"], "M1": t1, "M5": t5,
-                            "t5_over_t1": round(t5["us"] / t1["us"], 3)}
+                            "t5_over_t1": round(t5["us"] / t1["us"], 3), "simt_M1": s1, "simt_M5": s5}
         del ws
-    out["tail_k_simt"] = tail
+    out["tail_k"] = tail
     # group-128 tables on the 262144x2560 head: read natively (0.53125 B per
     # weight) against their expansion to group 64 (0.5625 B per weight)
     N, K = 262144, 2560

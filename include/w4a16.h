@@ -111,9 +111,15 @@ typedef enum {
   W4A16_KERNEL_AUTO = 0,    /* the dispatcher's choice for (N, K) */
   W4A16_KERNEL_SIMT = 1,    /* CUDA-core kernel: fp32 FMA, warp-shuffle split-K */
   W4A16_KERNEL_TC = 2,      /* tensor-core kernel: TMA-fed bf16 MMA on codes, fp32 group
-                               rescale; needs K % 512 == 0.  Runs as one of the two
-                               launch shapes below, chosen from (N, K, M); both give
-                               identical bits */
+                               rescale.  K % 512 == 0 runs as one of the launch shapes
+                               below, chosen from (N, K, M), all with identical bits.
+                               K % 512 != 0 runs padded to whole 512-code stages (the
+                               padding groups add exactly +0) on the persistent shape
+                               alone, in whole-K work units whose scale and bias rows
+                               come by bulk copy; up to K = 5952, where those rows fit
+                               in shared memory next to eight activation rows (larger:
+                               W4A16_ERR_KERNEL; the dispatcher takes the CUDA-core
+                               family there) */
   W4A16_KERNEL_VANILLA = 3, /* debug control: one thread per output, no sharing */
   W4A16_KERNEL_TC_STREAM = 4, /* tensor-core kernel, persistent grid: work units dealt to
                                  warps from a counter (in the CTA without a workspace);
@@ -122,11 +128,14 @@ typedef enum {
                                  of tile x expert CTAs */
   W4A16_KERNEL_TC_TILE = 5, /* tensor-core kernel, one CTA per 16-row tile holding the
                                tile's whole K range; needs that to fit in shared memory
-                               (otherwise W4A16_ERR_KERNEL) */
+                               and K % 512 == 0 (otherwise W4A16_ERR_KERNEL) */
   W4A16_KERNEL_TC_PREFILL = 6 /* tensor-core kernel for many rows: each 64-code group of a
                                  128-row tile expanded once to bf16 in shared memory, then
                                  tcgen05.mma over up to 128 activation rows into tensor
-                                 memory; the default for M > 32 where the family applies */
+                                 memory; the default for M > 32 where the family applies;
+                                 needs K % 512 == 0 (otherwise W4A16_ERR_KERNEL; with
+                                 K % 512 != 0 the dispatcher runs M > 32 on the
+                                 persistent shape, eight rows a launch) */
 } w4a16_kernel;
 
 /* y[M][N] = x[M][K] W^T.  M == 0 is a successful no-op.  The kernel family
@@ -147,8 +156,9 @@ int w4a16_mm_ws(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* scale
                 size_t workspace_bytes, void* stream);
 
 /* Bytes of workspace the tensor-core family can use for (N, K): 0 when it
- * does not apply (K % 512 != 0 or an invalid shape), otherwise a fixed
- * 5,013,504 bytes (32 KiB of counters + 4864 KiB of fp32 partials). */
+ * does not apply (an invalid shape, or K % 512 != 0 past K = 5952),
+ * otherwise a fixed 5,013,504 bytes (32 KiB of counters + 4864 KiB of fp32
+ * partials; with K % 512 != 0 only the unit counter is used). */
 size_t w4a16_workspace_bytes(int N, int K);
 
 /* w4a16_mm with an explicit kernel family (for A/B comparisons and tests). */
@@ -171,8 +181,9 @@ int w4a16_mm_kernel(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* s
  * 5,013,504-byte device array inside the library (32 KiB of tile counters +
  * 4864 KiB of fp32 partials), which every GPU that loads the library holds
  * until the process exits; every (N, K) with K % 512 == 0 fits in it, and a
- * shape that would not is rejected with W4A16_ERR_SHAPE.  K % 512 != 0 is
- * rejected with W4A16_ERR_KERNEL.
+ * shape that would not is rejected with W4A16_ERR_SHAPE.  K % 512 != 0 runs
+ * in whole-K units without scratch, up to K = 5952 (larger:
+ * W4A16_ERR_KERNEL).
  *
  * The first call on a device looks up the array's device address and sets
  * the kernel's shared-memory limit; make that first call before any CUDA

@@ -114,8 +114,10 @@ int check_nk(int N, int K) {
 int resolve_kernel(int requested, int N, int K, w4a16_plan* plan) {
   int k = requested;
   if (k == W4A16_KERNEL_AUTO) k = env().force_kernel;
-  // Default: the tensor-core family wherever it applies (K % 512 == 0), the
-  // CUDA-core family otherwise.  The choice depends on (N, K) only.
+  // Default: the tensor-core family wherever it applies (K % 512 == 0, and
+  // K % 512 != 0 padded to whole 512-code stages up to the K whose per-unit
+  // parameter rows fit in shared memory), the CUDA-core family otherwise.
+  // The choice depends on (N, K) only.
   if (k == W4A16_KERNEL_AUTO) k = tc_supported(N, K) ? W4A16_KERNEL_TC : W4A16_KERNEL_SIMT;
   switch (k) {
     case W4A16_KERNEL_SIMT: plan_simt(N, K, plan); return W4A16_OK;
@@ -124,7 +126,10 @@ int resolve_kernel(int requested, int N, int K, w4a16_plan* plan) {
     case W4A16_KERNEL_TC_STREAM:
     case W4A16_KERNEL_TC_TILE:
     case W4A16_KERNEL_TC_PREFILL: {
-      if (!tc_supported(N, K)) return fail(W4A16_ERR_KERNEL, "the tensor-core kernel needs K %% 512 == 0 (K = %d)", K);
+      if (!tc_supported(N, K))
+        return fail(W4A16_ERR_KERNEL, "K = %d is past the tensor-core kernels' K %% 512 != 0 range", K);
+      if (K % 512 && (k == W4A16_KERNEL_TC_TILE || k == W4A16_KERNEL_TC_PREFILL))
+        return fail(W4A16_ERR_KERNEL, "K %% 512 != 0 runs on the persistent tensor-core kernel only (K = %d)", K);
       const int path = k == W4A16_KERNEL_TC_STREAM ? 1 : k == W4A16_KERNEL_TC_TILE ? 2 : 0;
       if (path == 2 && !tc_tile_fits(N, K, 1))
         return fail(W4A16_ERR_KERNEL, "the tile kernel cannot hold K = %d in shared memory", K);
@@ -351,7 +356,7 @@ int w4a16_mm_noalloc(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* 
                      w4a16_bf16* y, int M, int N, int K, void* stream) {
   if (int rc = validate_mm(x, Wq, scales, biases, y, M, N, K)) return rc;
   if (!tc_supported(N, K))
-    return fail(W4A16_ERR_KERNEL, "w4a16_mm_noalloc runs the tensor-core kernel, which needs K %% 512 == 0 (K = %d)", K);
+    return fail(W4A16_ERR_KERNEL, "K = %d is past the tensor-core kernels' K %% 512 != 0 range", K);
   if (!tc_noalloc_fits(N, K))
     return fail(W4A16_ERR_SHAPE, "N = %d, K = %d needs more than the %zu-byte fixed scratch of w4a16_mm_noalloc", N, K,
                 tc_noalloc_scratch_bytes());
@@ -381,7 +386,7 @@ int w4a16_mm_argmax(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16* s
   if (!workspace) return fail(W4A16_ERR_NULL, "w4a16_mm_argmax needs a workspace (w4a16_workspace_bytes)");
   if (int rc = check_workspace(workspace, workspace_bytes)) return rc;
   if (misaligned(idx, 4) || misaligned(val, 2)) return fail(W4A16_ERR_ALIGN, "idx must be 4-byte and val 2-byte aligned");
-  if (!tc_supported(N, K))
+  if (K % 512)
     return fail(W4A16_ERR_KERNEL, "w4a16_mm_argmax runs the tensor-core kernel, which needs K %% 512 == 0 (K = %d)", K);
   if (env().fault == kFaultLaunch) return fail(W4A16_ERR_CUDA, "injected launch fault (W4A16_FAULT)");
   LaunchArgs a{};

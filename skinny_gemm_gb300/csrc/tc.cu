@@ -17,7 +17,10 @@
 //       acc = sum_{k in group} x_k (128 + q_k)   (four m16n8k16 MMAs, fp32)
 //       sx  = sum_{k in group} x_k               (four MMAs with A = 1.0)
 //       p_s = fma(s, acc, p_s);  p_s = fma(b - 128 s, sx, p_s)
-//   and y = bf16(((p_0 + p_1) + p_2) + ...).  Every kernel in this file
+//   and y = bf16(((p_0 + p_1) + p_2) + ...).  A K that is not a multiple of
+//   512 runs as K' = 512 ceil(K / 512): the padding groups read zero codes,
+//   scales and biases (the out-of-bounds fill of the tensor copies) and zero
+//   activations, so both of their fma steps add +0 to p_s.  Every kernel in this file
 //   reproduces exactly this sequence, so row m of any call equals the M = 1
 //   call bit for bit ([G4MK "Implementation notes": the verify GEMM is kept
 //   arithmetic-identical to the sequential GEMV), and w4a16_mm_id rows equal
@@ -127,6 +130,9 @@ constexpr int kCodeBytes = 2 * kBoxBytes;                        // 8192 codes p
 constexpr int kParamBytes = kTileRows * 8 * 2;                   // 512: 8 bf16 per row per stage
 constexpr int kCodeSlotBytes = kCodeBytes + 2 * kParamBytes;     // 9216: codes | scales | biases
 constexpr int kXPitch = kStageK * 2 + 64;                        // 1088: conflict-free LDS.128
+
+// K rounded up to whole stages (the logical K of the canonical arithmetic).
+__host__ __device__ constexpr int kpad(int K) { return (K + kStageK - 1) / kStageK * kStageK; }
 constexpr int kRoutedWarps = 8;          // max warps per CTA of the routed kernel
 #ifndef W4A16_TC_TARGET_UNITS
 #define W4A16_TC_TARGET_UNITS (152 * 16)
@@ -147,6 +153,7 @@ struct Geo {
   static constexpr int kBox = kRows * 128;
   static constexpr int kParam = kRows * 16;
   static constexpr int kSlot = (2 * kBox + 2 * kParam + 1023) / 1024 * 1024;  // 9216 | 5120
+  static constexpr int kCodeSlot = (2 * kBox + 1023) / 1024 * 1024;            // codes only: 8192 | 4096
   static constexpr int kWarps = NSUB == 2 ? W4A16_TC_STREAM_WARPS : 8;  // warps per CTA of the persistent kernel
 };
 
@@ -306,29 +313,40 @@ struct Maps {
 // The weight part of a stage: codes (two boxes, to dst) and the 8 groups'
 // scales and biases (to pdst) of 16 * NSUB rows from tensor_row; arms `bar`
 // for those bytes plus `mc` activation chunks still to come.
-// With PARAMS false only the codes are requested (group-128 tables bring
-// their parameters per work unit instead, see Ring::pbytes).
+// With PARAMS false only the codes are requested (group-128 tables and
+// K % 512 != 0 bring their parameters per work unit instead).  box1 false:
+// the stage's second box lies wholly past K (the last stage of a padded K)
+// and is not requested; its slot keeps older codes, which meet zero
+// activations and zero parameters there.
 template <int NSUB, bool PARAMS = true>
 __device__ __forceinline__ void issue_weights(uint32_t dst, uint32_t pdst, uint32_t bar, const Maps* maps, int st,
                                               int tensor_row, int mc, uint64_t pol_stream, uint64_t pol_keep,
-                                              uint32_t extra_bytes = 0) {
+                                              uint32_t extra_bytes = 0, bool box1 = true) {
   using G = Geo<NSUB>;
-  mbar_expect_tx(bar, 2 * G::kBox + (PARAMS ? 2 * G::kParam : 0) + (uint32_t)(mc * kStageK * 2) + extra_bytes);
+  mbar_expect_tx(bar, (box1 ? 2 : 1) * G::kBox + (PARAMS ? 2 * G::kParam : 0) + (uint32_t)(mc * kStageK * 2) +
+                          extra_bytes);
   tma_load_2d(dst, &maps->codes, st * kStageWords, tensor_row, bar, pol_stream);
-  tma_load_2d(dst + G::kBox, &maps->codes, st * kStageWords + kBoxWords, tensor_row, bar, pol_stream);
+  if (box1) tma_load_2d(dst + G::kBox, &maps->codes, st * kStageWords + kBoxWords, tensor_row, bar, pol_stream);
   if (PARAMS) {
     tma_load_2d(pdst, &maps->scales, st * 8, tensor_row, bar, pol_keep);
     tma_load_2d(pdst + G::kParam, &maps->biases, st * 8, tensor_row, bar, pol_keep);
   }
 }
 
+// Zeros for the activation padding past K (at most 448 bf16 of a row).
+__device__ __align__(128) uint4 g_xzero[64] = {};
+
 // The activation part of a stage: 512 bf16 of each row toks[0..mc) into rows
-// of kXPitch bytes at xdst.
+// of kXPitch bytes at xdst; in the last stage of a K % 512 != 0 shape the
+// codes past K are zeros (a second copy, so the stage's byte count is the same).
 __device__ __forceinline__ void issue_x(uint32_t xdst, uint32_t bar, int st, const uint16_t* x, const int* toks,
                                         int mc, int K, uint64_t pol_keep) {
   const uint16_t* xs = x + (int64_t)st * kStageK;
-  for (int n = 0; n < mc; ++n)
-    bulk_load(xdst + n * kXPitch, xs + (int64_t)toks[n] * K, kStageK * 2, bar, pol_keep);
+  const int valid = min(kStageK, K - st * kStageK);  // a multiple of 64
+  for (int n = 0; n < mc; ++n) {
+    bulk_load(xdst + n * kXPitch, xs + (int64_t)toks[n] * K, valid * 2, bar, pol_keep);
+    if (valid < kStageK) bulk_load(xdst + n * kXPitch + valid * 2, g_xzero, (kStageK - valid) * 2, bar, pol_keep);
+  }
 }
 
 // Lane 0 only: the weights of stage `st` into the next free slot; returns the
@@ -416,35 +434,89 @@ __device__ __forceinline__ uint2 lds64u(uint32_t addr) {
   return v;
 }
 
-// G128: the table has one scale and bias per 128 codes (the stage's 8
-// 64-groups use 4 of each); they are read at pbase + r * prow (scales) and
-// pbase + pbias + r * prow (biases), 8 bytes per row.  Each 64-group is then
-// rescaled with its 128-group's pair: the arithmetic of the group-64 kernel
-// on a table whose pairs repeat over the two halves of every 128-group.
-template <int NSUB, bool ALLCOLS, bool XSTAGED, int BOXROWS = 16 * NSUB, bool G128 = false>
-__device__ __forceinline__ void compute_stage(uint32_t cbase, uint32_t pbase, uint32_t xbase, bool xvalid,
-                                              uint32_t sxbase, uint32_t sx_stride, bool xvalid_cols,
-                                              float (&p)[NSUB][4], const uint32_t (&loff)[NSUB][4], int g,
-                                              uint32_t prow = 0, uint32_t pbias = 0) {
-  constexpr int GB = W4A16_TC_GROUP_BATCH;
-  // Codes: two boxes of BOXROWS rows x 128 bytes at cbase (the warp's rows
-  // picked by loff); scales then biases (16 bytes per row, BOXROWS rows
-  // each) at pbase, pbase pointing at the warp's first row.
-  constexpr uint32_t kBox = BOXROWS * 128, kBiases = BOXROWS * 16;
-  // scale / bias of the 8 groups for this lane's rows 16(i>>1) + g + 8(i&1)
-  uint4 ps[2 * NSUB], pb[2 * NSUB];
+__device__ __forceinline__ uint32_t lds32u(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t lds16u(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+
+// 16 bytes at a shared address aligned to `al` bytes (2, 4 or 8; warp-uniform).
+__device__ __forceinline__ uint4 lds128_al(uint32_t a, uint32_t al) {
+  if (al >= 8) {
+    const uint2 lo = lds64u(a), hi = lds64u(a + 8);
+    return make_uint4(lo.x, lo.y, hi.x, hi.y);
+  }
+  if (al == 4) return make_uint4(lds32u(a), lds32u(a + 4), lds32u(a + 8), lds32u(a + 12));
+  uint32_t w[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) w[k] = lds16u(a + 4 * k) | (lds16u(a + 4 * k + 2) << 16);
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Where the stage's scales and biases are read (PM):
+//  0: the stage's own boxes, 16 bytes per row, BOXROWS rows of scales then of
+//     biases at pbase (pbase pointing at the warp's first row);
+//  1 (G128): a table with one scale and bias per 128 codes (the stage's 8
+//     64-groups use 4 of each), read at pbase + r * prow (scales) and
+//     pbase + pbias + r * prow (biases), 8 bytes per row.  Each 64-group is
+//     rescaled with its 128-group's pair: the arithmetic of the group-64
+//     kernel on a table whose pairs repeat over the two halves of every
+//     128-group;
+//  2 (K % 512 != 0): a work unit's group-64 rows as they lie in memory, K / 32
+//     bytes apart: 16 bytes at pbase + r * prow (and + pbias), aligned to
+//     `pal` bytes; in the last stage the groups from `gv` on lie past K (the
+//     bytes there are the next row's) and read as zero.
+template <int NSUB, int BOXROWS, int PM>
+__device__ __forceinline__ void stage_params(uint4 (&ps)[2 * NSUB], uint4 (&pb)[2 * NSUB], uint32_t pbase, int g,
+                                             uint32_t prow, uint32_t pbias, uint32_t pal, int gv) {
+  constexpr uint32_t kBiases = BOXROWS * 16;
 #pragma unroll
   for (int i = 0; i < 2 * NSUB; ++i) {
     const uint32_t r = 16 * (i >> 1) + g + 8 * (i & 1);
-    if (G128) {
+    if (PM == 1) {
       const uint2 s2 = lds64u(pbase + r * prow), b2 = lds64u(pbase + pbias + r * prow);
       ps[i] = make_uint4(s2.x, s2.y, 0u, 0u);
       pb[i] = make_uint4(b2.x, b2.y, 0u, 0u);
+    } else if (PM == 2) {
+      ps[i] = lds128_al(pbase + r * prow, pal);
+      pb[i] = lds128_al(pbase + pbias + r * prow, pal);
     } else {
       ps[i] = lds128(pbase + r * 16);
       pb[i] = lds128(pbase + kBiases + r * 16);
     }
   }
+  if (PM == 2 && gv < 8) {
+    uint32_t mk[4];  // word w holds groups 2w (low half) and 2w + 1
+#pragma unroll
+    for (int w = 0; w < 4; ++w) mk[w] = 2 * w + 1 < gv ? 0xFFFFFFFFu : 2 * w < gv ? 0x0000FFFFu : 0u;
+#pragma unroll
+    for (int i = 0; i < 2 * NSUB; ++i) {
+      ps[i] = make_uint4(ps[i].x & mk[0], ps[i].y & mk[1], ps[i].z & mk[2], ps[i].w & mk[3]);
+      pb[i] = make_uint4(pb[i].x & mk[0], pb[i].y & mk[1], pb[i].z & mk[2], pb[i].w & mk[3]);
+    }
+  }
+}
+
+template <int NSUB, bool ALLCOLS, bool XSTAGED, int BOXROWS = 16 * NSUB, int PM = 0>
+__device__ __forceinline__ void compute_stage(uint32_t cbase, uint32_t pbase, uint32_t xbase, bool xvalid,
+                                              uint32_t sxbase, uint32_t sx_stride, bool xvalid_cols,
+                                              float (&p)[NSUB][4], const uint32_t (&loff)[NSUB][4], int g,
+                                              uint32_t prow = 0, uint32_t pbias = 0, uint32_t pal = 16,
+                                              int gv = 8) {
+  constexpr int GB = W4A16_TC_GROUP_BATCH;
+  constexpr bool G128 = PM == 1;
+  // Codes: two boxes of BOXROWS rows x 128 bytes at cbase (the warp's rows
+  // picked by loff); the parameters as stage_params reads them.
+  constexpr uint32_t kBox = BOXROWS * 128;
+  // scale / bias of the 8 groups for this lane's rows 16(i>>1) + g + 8(i&1)
+  uint4 ps[2 * NSUB], pb[2 * NSUB];
+  stage_params<NSUB, BOXROWS, PM>(ps, pb, pbase, g, prow, pbias, pal, gv);
 #pragma unroll
   for (int gp = 0; gp < 8; gp += GB) {
     uint32_t w[GB][NSUB][4];  // [group][subtile]: rows g / g+8 of chunk 2gl, then of chunk 2gl+1
@@ -537,26 +609,17 @@ __device__ __forceinline__ void compute_stage(uint32_t cbase, uint32_t pbase, ui
 // b, and the rescale of batch b waits until the MMAs of batch b + 1 are
 // issued (its accumulators are complete by then).  Every p receives the
 // same operations in the same order as compute_stage, so the bits agree.
-template <int NSUB, bool ALLCOLS, bool XSTAGED, int BOXROWS = 16 * NSUB, bool G128 = false>
+template <int NSUB, bool ALLCOLS, bool XSTAGED, int BOXROWS = 16 * NSUB, int PM = 0>
 __device__ __forceinline__ void compute_stage_pipe(uint32_t cbase, uint32_t pbase, uint32_t xbase, bool xvalid,
                                                    uint32_t sxbase, uint32_t sx_stride, bool xvalid_cols,
                                                    float (&p)[NSUB][4], const uint32_t (&loff)[NSUB][4], int g,
-                                                   uint32_t prow = 0, uint32_t pbias = 0) {
+                                                   uint32_t prow = 0, uint32_t pbias = 0, uint32_t pal = 16,
+                                                   int gv = 8) {
   constexpr int GB = W4A16_TC_PIPE_BATCH, NB = 8 / GB;
-  constexpr uint32_t kBox = BOXROWS * 128, kBiases = BOXROWS * 16;
+  constexpr bool G128 = PM == 1;
+  constexpr uint32_t kBox = BOXROWS * 128;
   uint4 ps[2 * NSUB], pb[2 * NSUB];
-#pragma unroll
-  for (int i = 0; i < 2 * NSUB; ++i) {
-    const uint32_t r = 16 * (i >> 1) + g + 8 * (i & 1);
-    if (G128) {
-      const uint2 s2 = lds64u(pbase + r * prow), b2 = lds64u(pbase + pbias + r * prow);
-      ps[i] = make_uint4(s2.x, s2.y, 0u, 0u);
-      pb[i] = make_uint4(b2.x, b2.y, 0u, 0u);
-    } else {
-      ps[i] = lds128(pbase + r * 16);
-      pb[i] = lds128(pbase + kBiases + r * 16);
-    }
-  }
+  stage_params<NSUB, BOXROWS, PM>(ps, pb, pbase, g, prow, pbias, pal, gv);
   // Batch b uses buffer b % 2 of the loads and accumulators and b % 3 of the
   // group sums: those of batch b - 1 are still to be read by its rescale
   // when batch b + 1 is loaded.
@@ -662,17 +725,18 @@ __device__ __forceinline__ void compute_stage_pipe(uint32_t cbase, uint32_t pbas
 }
 
 // The persistent kernel's stage: pipelined unless W4A16_TC_PIPE is 0.
-template <int NSUB, bool ALLCOLS, bool XSTAGED, int BOXROWS = 16 * NSUB, bool G128 = false>
+template <int NSUB, bool ALLCOLS, bool XSTAGED, int BOXROWS = 16 * NSUB, int PM = 0>
 __device__ __forceinline__ void compute_stage_sel(uint32_t cbase, uint32_t pbase, uint32_t xbase, bool xvalid,
                                                   uint32_t sxbase, uint32_t sx_stride, bool xvalid_cols,
                                                   float (&p)[NSUB][4], const uint32_t (&loff)[NSUB][4], int g,
-                                                  uint32_t prow = 0, uint32_t pbias = 0) {
+                                                  uint32_t prow = 0, uint32_t pbias = 0, uint32_t pal = 16,
+                                                  int gv = 8) {
 #if W4A16_TC_PIPE
-  compute_stage_pipe<NSUB, ALLCOLS, XSTAGED, BOXROWS, G128>(cbase, pbase, xbase, xvalid, sxbase, sx_stride,
-                                                            xvalid_cols, p, loff, g, prow, pbias);
+  compute_stage_pipe<NSUB, ALLCOLS, XSTAGED, BOXROWS, PM>(cbase, pbase, xbase, xvalid, sxbase, sx_stride,
+                                                          xvalid_cols, p, loff, g, prow, pbias, pal, gv);
 #else
-  compute_stage<NSUB, ALLCOLS, XSTAGED, BOXROWS, G128>(cbase, pbase, xbase, xvalid, sxbase, sx_stride, xvalid_cols,
-                                                       p, loff, g, prow, pbias);
+  compute_stage<NSUB, ALLCOLS, XSTAGED, BOXROWS, PM>(cbase, pbase, xbase, xvalid, sxbase, sx_stride, xvalid_cols,
+                                                     p, loff, g, prow, pbias, pal, gv);
 #endif
 }
 
@@ -682,7 +746,7 @@ struct Shape {
 
 __host__ __device__ inline Shape tc_shape(int N, int K) {
   Shape s;
-  s.nst = K / kStageK;
+  s.nst = kpad(K) / kStageK;
   s.tiles = (N + kTileRows - 1) / kTileRows;
   int64_t sl = (int64_t)s.nst * s.tiles / kTargetUnits;
   if (sl < 1) sl = 1;
@@ -693,9 +757,11 @@ __host__ __device__ inline Shape tc_shape(int N, int K) {
   return s;
 }
 
+// codes_only: stage slots without the parameter boxes (the parameters come
+// per work unit instead, K % 512 != 0)
 template <int NSUB>
-__host__ __device__ inline int ring_bytes(int stages, int mcap) {
-  return stages * (Geo<NSUB>::kSlot + mcap * kXPitch);
+__host__ __device__ inline int ring_bytes(int stages, int mcap, bool codes_only = false) {
+  return stages * ((codes_only ? Geo<NSUB>::kCodeSlot : Geo<NSUB>::kSlot) + mcap * kXPitch);
 }
 
 // ---- persistent kernel (w4a16_mm) ------------------------------------------------------
@@ -723,10 +789,11 @@ struct StreamParams {
   int xpitch;       // bytes per activation row of the pre-staged copy (0: per-stage copies)
   int prefetch;     // request the first weight stages before waiting for earlier kernels
   int g128;         // scales and biases are [N][K/128] (one pair per 128 codes)
+  int ptail;        // K % 512 != 0: whole-K units, each with its parameter rows by bulk copy
   int fault_tx;     // debug: bytes the first stage of CTA 0's warp 0 expects beyond its copies
   uint32_t wait_limit;  // tries of a stage wait (0: the default)
   int l2_stages;        // routed mode: leading stages of every expert pulled into L2 before the ids are known
-  int par_off;      // and then the byte offset of the per-unit parameter slots in shared memory
+  int par_off;      // g128 / ptail: byte offset of the per-unit parameter slots in shared memory
   const int32_t* ids;  // routed mode: expert id of each of T tokens, E experts of N rows each
   int T, E;
   unsigned long long* best;  // argmax mode: [8] running keys, zero between launches
@@ -781,7 +848,7 @@ __host__ __device__ inline int sx_cols(int mc) { return (mc + 1) & ~1; }
 
 // Bytes of shared memory the pre-staged activations and their group sums
 // take: mc rows of 2K + 64 bytes (fragment order, padded for conflict-free
-// reads) and K/64 groups x sx_cols(mc) fp32 sums.
+// reads) and K/64 groups x sx_cols(mc) fp32 sums; K here is the padded kpad(K).
 __host__ __device__ inline int xstage_bytes(int mc, int K) {
   return mc * (2 * K + 64) + (K / kGroup) * sx_cols(mc) * 4;
 }
@@ -849,7 +916,7 @@ __device__ __forceinline__ void build_chunks(const int32_t* __restrict__ ids, in
 // with 64-bit atomic maxima, and the last CTA out writes the argmax of every
 // row (the outputs' bits are those w4a16_mm stores).
 template <int NSUB, bool ALLCOLS, bool XSTAGED, bool SPLIT, bool ROUTED = false, bool ARGMAX = false,
-          bool WHOLEK = false, bool G128 = false>
+          bool WHOLEK = false, bool G128 = false, bool PT = false>
 __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_min_blocks<NSUB>()) tc_stream_kernel(
     const __grid_constant__ Maps maps, StreamParams p) {
   using G = Geo<NSUB>;
@@ -858,8 +925,11 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   static_assert(!ARGMAX || (!ROUTED && NSUB == 2), "argmax over plain 32-row units");
   static_assert(!WHOLEK || (!ROUTED && !SPLIT && !ARGMAX), "whole-K units are a plain-mode schedule");
   static_assert(!G128 || (!ROUTED && !SPLIT && !ARGMAX), "group-128 tables: plain whole-K units");
+  static_assert(!PT || (!SPLIT && !ARGMAX && !G128), "K % 512 != 0: whole-K units (plain or routed)");
   constexpr bool DYN = (SPLIT || W4A16_TC_DYN_ALL) && !ROUTED;  // units after the first from the counter
-  constexpr bool FOLD = ROUTED || WHOLEK || G128;  // whole-K units: slice sums folded in registers, in slice order
+  // whole-K units: slice sums folded in registers, in slice order
+  constexpr bool FOLD = ROUTED || WHOLEK || G128 || PT;
+  constexpr bool UBLK = G128 || PT;  // a unit's parameter rows come by bulk copy
   // Without a workspace (p.sched == nullptr) the units are dealt inside each
   // CTA: CTA c owns the contiguous units [c U / grid, (c + 1) U / grid) and
   // its warps take them from a shared-memory counter.  With one, from a
@@ -879,9 +949,10 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   Ring R;
   R.S = S;
   R.x_slot = x_slot;
-  R.codes0 = smem_u32(base) + (uint32_t)(warp * S * G::kSlot);
-  R.xs0 = smem_u32(base) + (uint32_t)(kW * S * G::kSlot + warp * S * x_slot);
-  const uint32_t bar_off = (uint32_t)(kW * ring_bytes<NSUB>(S, xring));
+  constexpr int kSlot = PT ? G::kCodeSlot : G::kSlot;  // PT: the stage boxes carry codes only
+  R.codes0 = smem_u32(base) + (uint32_t)(warp * S * kSlot);
+  R.xs0 = smem_u32(base) + (uint32_t)(kW * S * kSlot + warp * S * x_slot);
+  const uint32_t bar_off = (uint32_t)(kW * ring_bytes<NSUB>(S, xring, PT));
   R.bars0 = smem_u32(base) + bar_off + (uint32_t)(warp * S * 8);
   int* s_tok = reinterpret_cast<int*>(base + bar_off + kW * S * 8);
   const uint32_t xst = smem_u32(base) + bar_off + (uint32_t)(kW * S * 8 + kStreamMisc);  // 16-byte aligned
@@ -891,12 +962,20 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   R.pol_stream = policy_evict_first();
   R.pol_keep = policy_evict_last();
   if (p.wait_limit) R.limit = p.wait_limit;
-  // G128: a unit's scales and biases (its rows over the whole K, K / 64 bytes
-  // a row) arrive with its first stage, into one of S slots per warp (a unit
-  // has at least one stage, so at most S units are in flight)
-  const uint32_t prb = (uint32_t)(p.K / 64);
-  const uint32_t pslot = 2u * kRows * prb;
+  // G128 / PT: a unit's scales and biases (its rows over the whole K) arrive
+  // with its first stage, into one of S slots per warp (a unit has at least
+  // one stage, so at most S units are in flight).  G128: K / 64 bytes a row.
+  // PT (K % 512 != 0, no tensor map takes rows K / 32 bytes apart): K / 32
+  // bytes a row, each table at the same offset modulo 16 as in memory, with
+  // room for the 16-byte reads of the last stage that run past the last row
+  // (up to 14 + 31 K/32 + 16 ceil(K / 512) < 32 K/32 + 30 bytes).
+  const uint32_t prb = (uint32_t)(G128 ? p.K / 64 : p.K / 32);
+  const uint32_t phalf = G128 ? kRows * prb : (kRows * prb + 45) & ~15u;
+  const uint32_t pslot = 2u * phalf;
   const uint32_t par0 = smem_u32(base) + (uint32_t)p.par_off + (uint32_t)(warp * S) * pslot;
+  const uint32_t plow = prb & (0u - prb);       // largest power of two dividing the PT row pitch
+  const uint32_t pal = plow < 8u ? plow : 8u;  // the alignment of every PT parameter read
+  const int gv_last = p.K / kGroup - 8 * (p.nst - 1);                 // groups inside K in the last stage
 
   if (lane == 0)
     for (int i = 0; i < S; ++i) mbar_init(R.bars0 + 8 * i, 1);
@@ -904,7 +983,8 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   const uint32_t xbar = smem_u32(s_tok + kMaxChunk + 8 * 8);  // the pre-staged activations' copy
   if (XSTAGED && threadIdx.x == 0) mbar_init(xbar, 1);
   unsigned long long* s_best =  // [warp][8]; the offset is a multiple of 8
-      reinterpret_cast<unsigned long long*>(base + (xst - smem_u32(base)) + (XSTAGED ? xstage_bytes(mc, p.K) : 0));
+      reinterpret_cast<unsigned long long*>(base + (xst - smem_u32(base)) +
+                                            (XSTAGED ? xstage_bytes(mc, p.nst * kStageK) : 0));
   unsigned long long* s_cta_best = s_best + 8 * 8;
   if (ARGMAX && threadIdx.x < 8 * 8 + 8) s_best[threadIdx.x] = 0ull;
   int* s_grab = s_tok + kMaxChunk + 8 * 8 + 2;  // the CTA's own unit counter (no workspace)
@@ -945,6 +1025,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   int imc = xring;                 // and their count
   int nxt = -1;                    // lane 0: count of the grab for the unit after iu (unit TW + nxt), -1 before it
   int irow = 0;                    // lane 0: first weight row of unit iu
+  int irows = 0;                   // lane 0: and its rows inside the matrix
   int ifirst = 0;                  // lane 0: first stage of unit iu
   uint32_t iseq = 0, ipar = 0;     // lane 0: units dealt / begun
   const int last_grab = max(0, p.units - TW) + min(TW, p.units) - 1;
@@ -965,18 +1046,20 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   auto begin_unit = [&](int u) {
     iu = u;
     if (DYN) s_units[iseq++ & 7u] = u;
-    if (G128 && u >= 0) ++ipar;
+    if (UBLK && u >= 0) ++ipar;
     if (u >= 0) {
       if (ROUTED) {
         const int c = u / p.tiles;
         const int* ch = s_tab + 2 + c * (2 + kMaxChunk);
         irow = ch[0] * p.N + (u - c * p.tiles) * kRows;  // row of the stacked [E][N] weights
+        irows = min(kRows, p.N - (u - c * p.tiles) * kRows);
         imc = ch[1];
         itok = ch + 2;
         ist = 0;
         iend = p.nst;
-      } else if (WHOLEK || G128) {
+      } else if (WHOLEK || G128 || PT) {
         irow = u * kRows;
+        irows = min(kRows, p.N - irow);
         ist = 0;
         iend = p.nst;
       } else {
@@ -990,10 +1073,36 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   };
   auto issue_stage = [&](bool with_x) {
     uint32_t slot;
-    if (G128) {
+    if (UBLK) {
       slot = R.issued % (uint32_t)R.S;
-      const uint32_t dst = R.codes0 + slot * G::kSlot, bar = R.bars0 + 8 * slot;
-      if (ist == ifirst) {
+      const uint32_t dst = R.codes0 + slot * kSlot, bar = R.bars0 + 8 * slot;
+      if (PT && ist == ifirst) {
+        // The unit's rows are bytes [b0, b1) of the scales and of the biases.
+        // The 16-byte-aligned window around them comes by one bulk copy per
+        // table (byte b to ps + b - lo), clipped at the arrays' last whole 16
+        // bytes; bytes past that by plain loads, stored before the barrier is
+        // armed (its arrival releases them to the computing lanes).
+        const char* gs = reinterpret_cast<const char*>(p.S);
+        const char* gb = reinterpret_cast<const char*>(p.B);
+        const int64_t tot = (int64_t)(ROUTED ? p.E : 1) * p.N * prb;
+        const int64_t b0 = (int64_t)irow * prb, b1 = b0 + (int64_t)irows * prb;
+        const int64_t lo = b0 & ~(int64_t)15;
+        const int64_t hi = min((b1 + 15) & ~(int64_t)15, tot & ~(int64_t)15);
+        const uint32_t nb = hi > lo ? (uint32_t)(hi - lo) : 0u;
+        const uint32_t ps = par0 + ((ipar - 1) % (uint32_t)S) * pslot;
+        for (int64_t o = max(hi, b0); o < b1; o += 2) {
+          const uint16_t vs = ld_nc_u16(reinterpret_cast<const uint16_t*>(gs + o));
+          const uint16_t vb = ld_nc_u16(reinterpret_cast<const uint16_t*>(gb + o));
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(ps + (uint32_t)(o - lo)), "h"(vs) : "memory");
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(ps + phalf + (uint32_t)(o - lo)), "h"(vb) : "memory");
+        }
+        issue_weights<NSUB, false>(dst, 0, bar, &maps, ist, irow, imc, R.pol_stream, R.pol_keep, 2 * nb,
+                                   ist * kStageWords + kBoxWords < p.K / 8);
+        if (nb) {
+          bulk_load(ps, gs + lo, nb, bar, R.pol_keep);
+          bulk_load(ps + phalf, gb + lo, nb, bar, R.pol_keep);
+        }
+      } else if (ist == ifirst) {
         // the unit's rows of the group-128 scales and biases: one bulk copy
         // each of the 16-byte multiple, plain loads for the few bytes past it
         const int rows = min(kRows, p.N - irow);
@@ -1013,7 +1122,8 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
           asm volatile("st.shared.u16 [%0], %1;" ::"r"(ps + kRows * prb + o), "h"(vb) : "memory");
         }
       } else {
-        issue_weights<NSUB, false>(dst, 0, bar, &maps, ist, irow, imc, R.pol_stream, R.pol_keep);
+        issue_weights<NSUB, false>(dst, 0, bar, &maps, ist, irow, imc, R.pol_stream, R.pol_keep, 0,
+                                   !PT || ist * kStageWords + kBoxWords < p.K / 8);
       }
       ++R.issued;
     } else {
@@ -1081,10 +1191,13 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
     }
     if (lane == 0) begin_unit(gw < units ? gw : -1);
   }
-  if (XSTAGED && threadIdx.x == 0) {  // each activation row in one bulk copy (16-byte aligned: K % 512 == 0)
-    mbar_expect_tx(xbar, (uint32_t)(mc * 2 * p.K));
-    for (int n = 0; n < mc; ++n)
+  if (XSTAGED && threadIdx.x == 0) {  // each activation row in one bulk copy (16-byte aligned: K % 64 == 0)
+    const int kp = p.nst * kStageK;  // then zeros up to the padded K
+    mbar_expect_tx(xbar, (uint32_t)(mc * 2 * kp));
+    for (int n = 0; n < mc; ++n) {
       bulk_load(xst + n * p.xpitch, p.x + (int64_t)(p.row0 + n) * p.K, 2 * p.K, xbar, R.pol_keep);
+      if (kp > p.K) bulk_load(xst + n * p.xpitch + 2 * p.K, g_xzero, 2 * (kp - p.K), xbar, R.pol_keep);
+    }
   }
   if (lane == 0) {
     if (iu >= 0) {
@@ -1111,7 +1224,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
     // An output column depends only on its own B column, so every sum has
     // the bits of the per-stage chain (activation row in the column).  Four
     // chains per warp at a time, interleaved.
-    const int nblk = p.K / kGroup / 8, tasks = timed_out ? 0 : mc * nblk;
+    const int nblk = p.nst, tasks = timed_out ? 0 : mc * nblk;
     for (int k0 = warp; k0 < tasks; k0 += 4 * kW) {
       uint32_t b[4][2][2][2];
       float v[4][4];
@@ -1250,15 +1363,20 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
     if (u < 0 || u >= (own ? cta_hi : units)) break;
     int slice = 0, tile, umc = mc;
     const int* utok = s_tok;
+    int64_t crow;  // the unit's first row in the (stacked) weights
     if (ROUTED) {
       const int c = u / p.tiles;
       const int* ch = s_tab + 2 + c * (2 + kMaxChunk);
       tile = u - c * p.tiles;
       umc = ch[1];
       utok = ch + 2;
+      crow = (int64_t)ch[0] * p.N + tile * kRows;
     } else {
       tile = unit_tile<SPLIT>(p, u, slice);
+      crow = (int64_t)tile * kRows;
     }
+    // PT: the unit's parameter rows in its slot, at their offset modulo 16
+    const uint32_t ppar = par0 + (cseq % (uint32_t)S) * pslot + (uint32_t)((crow * prb) & 15);
     const int s0 = FOLD ? 0 : slice * p.sl, s1 = FOLD ? p.nst : min(s0 + p.sl, p.nst);
     // The last slice of a tile reads the tile's arrival count before its
     // stages (the value is used after them, so the load never stalls).
@@ -1282,7 +1400,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
         timed_out = true;
         break;
       }
-      const uint32_t cbase = ordered(R.codes0 + slot * G::kSlot);
+      const uint32_t cbase = ordered(R.codes0 + slot * kSlot);
       uint32_t xbase, sxbase = 0;
       if (XSTAGED) {
         xbase = xst + g * p.xpitch + 16 * t + st * (kStageK * 2);
@@ -1291,9 +1409,13 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
         xbase = ordered(R.xs0 + slot * x_slot + g * kXPitch + 16 * t);
       }
       if (G128)
-        compute_stage_sel<NSUB, ALLCOLS, XSTAGED, 16 * NSUB, true>(
+        compute_stage_sel<NSUB, ALLCOLS, XSTAGED, 16 * NSUB, 1>(
             cbase, par0 + (cseq % (uint32_t)S) * pslot + (uint32_t)st * 8u, xbase, g < umc, sxbase, sx_cols(mc) * 4,
             2 * t < umc, acc, loff, g, prb, kRows * prb);
+      else if (PT)
+        compute_stage_sel<NSUB, ALLCOLS, XSTAGED, 16 * NSUB, 2>(
+            cbase, ppar + (uint32_t)st * 16u, xbase, g < umc, sxbase, sx_cols(mc) * 4, 2 * t < umc, acc, loff, g,
+            prb, phalf, pal, st == p.nst - 1 ? gv_last : 8);
       else
         compute_stage_sel<NSUB, ALLCOLS, XSTAGED>(cbase, cbase + 2 * G::kBox, xbase, g < umc, sxbase,
                                                   sx_cols(mc) * 4, 2 * t < umc, acc, loff, g);
@@ -1912,9 +2034,9 @@ cudaError_t make_maps(Maps* m, const uint32_t* Wq, const uint16_t* S, const uint
 }
 
 template <int NSUB>
-int stream_smem(int stages, int mc) {
+int stream_smem(int stages, int mc, bool codes_only = false) {
   using G = Geo<NSUB>;
-  return G::kWarps * ring_bytes<NSUB>(stages, mc) + G::kWarps * stages * 8 + kStreamMisc + 1024;
+  return G::kWarps * ring_bytes<NSUB>(stages, mc, codes_only) + G::kWarps * stages * 8 + kStreamMisc + 1024;
 }
 
 // Per-CTA shared-memory budget of the persistent kernel: the measured best
@@ -1972,6 +2094,30 @@ int staged_stages(int M, int K, int extra = 0) {
   return 2;
 }
 
+// Bytes of one per-unit parameter slot with K % 512 != 0: the unit's rows of
+// the scales and of the biases (K / 32 bytes a row), each with room for its
+// offset modulo 16 and the last stage's reads past the last row (the
+// kernel's phalf, twice).
+template <int NSUB>
+int ptail_slot_bytes(int K) {
+  return 2 * ((Geo<NSUB>::kRows * (K / 32) + 45) & ~15);
+}
+
+// Shared memory of the persistent kernel with S per-unit parameter slots of
+// pslot bytes per warp after everything else: the ring as deep as fits, from
+// `stages` down to 2.  Returns the bytes (0 when two stages do not fit) and
+// sets stages and par_off.
+template <int NSUB>
+int unit_param_smem(int& stages, int& par_off, int M, bool staged, int kp, int extra, int pslot, bool codes_only) {
+  for (;; --stages) {
+    const int smem = stream_smem<NSUB>(stages, staged ? 0 : M, codes_only) + extra + (staged ? xstage_bytes(M, kp) : 0);
+    par_off = (smem - 1024 + 15) & ~15;
+    const int total = par_off + Geo<NSUB>::kWarps * stages * pslot + 1024;
+    if (total <= kSmemLimit) return total;
+    if (stages <= 2) return 0;
+  }
+}
+
 // Launch with, when pdl is set, a programmatic dependency on the previous
 // kernel of the stream (the kernels wait for it with griddepcontrol.wait
 // before touching anything it may have written), and with clusters of
@@ -2003,11 +2149,12 @@ cudaError_t launch_ex(Kern fn, dim3 grid, dim3 block, int smem, cudaStream_t str
   return cudaLaunchKernelEx(&cfg, fn, args...);
 }
 
-template <int NSUB, bool A, bool X, bool SPLIT, bool ARGMAX = false, bool WHOLEK = false, bool G128 = false>
+template <int NSUB, bool A, bool X, bool SPLIT, bool ARGMAX = false, bool WHOLEK = false, bool G128 = false,
+          bool PT = false>
 cudaError_t stream_launch_t(const Maps& map, const StreamParams& p, int sms, int smem, DeviceInfo& d,
                             cudaStream_t stream, bool pdl) {
   constexpr int kW = Geo<NSUB>::kWarps;
-  auto* fn = tc_stream_kernel<NSUB, A, X, SPLIT, false, ARGMAX, WHOLEK, G128>;
+  auto* fn = tc_stream_kernel<NSUB, A, X, SPLIT, false, ARGMAX, WHOLEK, G128, PT>;
   if (cudaError_t e = allow_smem(fn, d)) return e;
   int per_sm = 0;
   if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kW * 32, smem)) return e;
@@ -2025,22 +2172,33 @@ template <int NSUB>
 cudaError_t launch_stream_t(const Maps& map, StreamParams p, int sms, DeviceInfo& d, cudaStream_t stream, int pdl) {
   const bool allcols = p.M > 1;
   const int extra = p.idx ? kArgmaxSmem : 0;  // the argmax mode's keys
-  const bool staged = stage_activations<NSUB>(p.M, p.K, p.units, sms, extra);
-  p.xpitch = staged ? 2 * p.K + 64 : 0;
-  p.stages = staged ? staged_stages<NSUB>(p.M, p.K, extra) : stream_stages<NSUB>(p.M, extra);
+  const int kp = kpad(p.K);
+  bool staged = stage_activations<NSUB>(p.M, kp, p.units, sms, extra);
+  p.xpitch = staged ? 2 * kp + 64 : 0;
+  p.stages = staged ? staged_stages<NSUB>(p.M, kp, extra) : stream_stages<NSUB>(p.M, extra);
   p.prefetch = pdl >= 2;
   int smem = stream_smem<NSUB>(p.stages, staged ? 0 : p.M) + extra;
-  if (staged) smem += xstage_bytes(p.M, p.K);
+  if (staged) smem += xstage_bytes(p.M, kp);
   const bool on = pdl > 0;
   using Fn = cudaError_t (*)(const Maps&, const StreamParams&, int, int, DeviceInfo&, cudaStream_t, bool);
-  if (p.g128) {  // group-128 tables: whole-K units with their parameter rows in shared memory
-    // the ring as deep as fits next to S parameter slots of K bytes per warp
-    for (;; --p.stages) {
-      smem = stream_smem<NSUB>(p.stages, staged ? 0 : p.M) + extra + (staged ? xstage_bytes(p.M, p.K) : 0);
-      p.par_off = (smem - 1024 + 15) & ~15;
-      smem = p.par_off + Geo<NSUB>::kWarps * p.stages * p.K + 1024;
-      if (smem <= kSmemLimit) break;
-      if (p.stages <= 2) return cudaErrorInvalidValue;
+  if (p.g128 || p.ptail) {  // whole-K units with their parameter rows in shared memory
+    // the ring as deep as fits next to S parameter slots per warp; per-stage
+    // activation copies where the pre-staged rows leave no room
+    const int pslot = p.g128 ? p.K : ptail_slot_bytes<NSUB>(p.K);
+    smem = unit_param_smem<NSUB>(p.stages, p.par_off, p.M, staged, kp, extra, pslot, p.ptail != 0);
+    if (!smem && staged) {
+      staged = false;
+      p.xpitch = 0;
+      p.stages = stream_stages<NSUB>(p.M, extra);
+      smem = unit_param_smem<NSUB>(p.stages, p.par_off, p.M, false, kp, extra, pslot, p.ptail != 0);
+    }
+    if (!smem) return cudaErrorInvalidValue;
+    if (p.ptail) {
+      static const Fn pt[2][2] = {{stream_launch_t<NSUB, false, false, false, false, false, false, true>,
+                                   stream_launch_t<NSUB, false, true, false, false, false, false, true>},
+                                  {stream_launch_t<NSUB, true, false, false, false, false, false, true>,
+                                   stream_launch_t<NSUB, true, true, false, false, false, false, true>}};
+      return pt[allcols][staged](map, p, sms, smem, d, stream, on);
     }
     static const Fn g128[2][2] = {{stream_launch_t<NSUB, false, false, false, false, false, true>,
                                    stream_launch_t<NSUB, false, true, false, false, false, true>},
@@ -2256,7 +2414,7 @@ bool workspace_fits(const Shape& s, const StreamWork& w) {
 cudaError_t launch_stream(const Maps& maps, StreamParams p, const StreamWork& w, DeviceInfo& d,
                           cudaStream_t stream, int pdl) {
   p.tiles = w.tiles;
-  p.units = p.ks > 1 && (!p.part || p.g128) ? w.tiles : w.units;  // whole-K units
+  p.units = p.ks > 1 && (!p.part || p.g128 || p.ptail) ? w.tiles : w.units;  // whole-K units
   p.kfull = p.nst % p.sl == 0 ? p.ks : p.ks - 1;
 #if W4A16_TC_STREAM_NSUB1_MIN_M <= 8  // else no chunk (8 rows at most) takes 16-row warps
   if (w.nsub == 1) return launch_stream_t<1>(maps, p, d.sms, d, stream, pdl);
@@ -2290,12 +2448,23 @@ cudaError_t encode_map_2d(CUtensorMap* map, CUtensorMapDataType type, const void
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-bool tc_supported(int N, int K) {
-  (void)N;
-  return K % kStageK == 0;
+// K % 512 != 0: the persistent kernel's per-unit parameter slots fit next to
+// a two-stage ring with per-stage copies of eight activation rows (the most
+// shared memory any chunk takes).
+bool tc_ptail_fits(int K) {
+  int stages = 2, par_off = 0;
+  return unit_param_smem<2>(stages, par_off, kMaxChunk, false, kpad(K), 0, ptail_slot_bytes<2>(K), true) > 0;
 }
 
-bool tc_tile_fits(int N, int K, int M) { return tile_plan(tc_shape(N, K), N, M, true).kc > 0; }
+bool tc_supported(int N, int K) {
+  (void)N;
+  if (K <= 0 || K % kGroup) return false;
+  return K % kStageK == 0 || tc_ptail_fits(K);  // K % 512 != 0 runs padded to whole stages
+}
+
+bool tc_tile_fits(int N, int K, int M) {
+  return K % kStageK == 0 && tile_plan(tc_shape(N, K), N, M, true).kc > 0;
+}
 
 void plan_tc(int N, int K, int tc_path, w4a16_plan* p) {
   const Shape s = tc_shape(N, K);
@@ -2312,6 +2481,26 @@ void plan_tc(int N, int K, int tc_path, w4a16_plan* p) {
   p->rows_per_tile = kTileRows;
   p->units = s.units;
   p->kernel = tc_path == 1 ? W4A16_KERNEL_TC_STREAM : tc_path == 2 ? W4A16_KERNEL_TC_TILE : W4A16_KERNEL_TC;
+  if (K % kStageK) {  // the persistent kernel in whole-K units, parameter rows per unit
+    const StreamWork w = stream_work(s, N, 1);
+    const int kp = kpad(K), pslot = ptail_slot_bytes<2>(K);
+    bool staged = stage_activations<2>(1, kp, w.tiles, sms);
+    int stages = staged ? staged_stages<2>(1, kp) : stream_stages<2>(1), par_off = 0;
+    int smem = unit_param_smem<2>(stages, par_off, 1, staged, kp, 0, pslot, true);
+    if (!smem && staged) {
+      stages = stream_stages<2>(1);
+      smem = unit_param_smem<2>(stages, par_off, 1, false, kp, 0, pslot, true);
+    }
+    const int per_sm = smem > 0 && kSmemLimit / smem > 0 ? kSmemLimit / smem : 1;
+    const int need = cdiv(w.tiles, Geo<2>::kWarps);
+    p->rows_per_tile = w.rows;
+    p->units = w.tiles;
+    p->threads = Geo<2>::kWarps * 32;
+    p->grid_x = sms * per_sm < need ? sms * per_sm : need;
+    p->smem_bytes = smem;
+    p->workspace_bytes = 0;
+    return;
+  }
   const TilePlan tp = tc_path == 1 ? TilePlan() : tile_plan(s, N, 1, tc_path == 2);
   p->workspace_bytes = 0;
   if (tp.kc > 0) {  // clusters of kc CTAs per 16-row tile
@@ -2325,12 +2514,14 @@ void plan_tc(int N, int K, int tc_path, w4a16_plan* p) {
   const StreamWork w = stream_work(s, N, 1);
   int smem, warps;
   if (w.nsub == 1) {
-    const bool staged = stage_activations<1>(1, K, w.units, sms);
-    smem = staged ? stream_smem<1>(staged_stages<1>(1, K), 0) + xstage_bytes(1, K) : stream_smem<1>(stream_stages<1>(1), 1);
+    const bool staged = stage_activations<1>(1, kpad(K), w.units, sms);
+    smem = staged ? stream_smem<1>(staged_stages<1>(1, kpad(K)), 0) + xstage_bytes(1, kpad(K))
+                  : stream_smem<1>(stream_stages<1>(1), 1);
     warps = Geo<1>::kWarps;
   } else {
-    const bool staged = stage_activations<2>(1, K, w.units, sms);
-    smem = staged ? stream_smem<2>(staged_stages<2>(1, K), 0) + xstage_bytes(1, K) : stream_smem<2>(stream_stages<2>(1), 1);
+    const bool staged = stage_activations<2>(1, kpad(K), w.units, sms);
+    smem = staged ? stream_smem<2>(staged_stages<2>(1, kpad(K)), 0) + xstage_bytes(1, kpad(K))
+                  : stream_smem<2>(stream_stages<2>(1), 1);
     warps = Geo<2>::kWarps;
   }
   const int per_sm = kSmemLimit / smem > 0 ? kSmemLimit / smem : 1;
@@ -2343,6 +2534,8 @@ void plan_tc(int N, int K, int tc_path, w4a16_plan* p) {
   p->grid_x = grid;
   p->smem_bytes = smem;
 }
+
+cudaError_t launch_tc_ptail(const LaunchArgs& a);
 
 // w4a16_mm (idx == nullptr) or, always on the persistent kernel, its argmax
 // mode (w4a16_mm_argmax).
@@ -2360,6 +2553,10 @@ cudaError_t launch_tc_impl(const LaunchArgs& a, int32_t* idx, uint16_t* val) {
   p.part = nullptr;
   p.cnt = nullptr;
   p.sched = nullptr;
+  if (a.K % kStageK) {  // whole-K units with per-unit parameter rows: no argmax mode, tile or prefill kernel
+    if (idx || a.tc_path == 2 || a.tc_path == 3) return cudaErrorInvalidConfiguration;
+    return launch_tc_ptail(a);  // takes g_dev_mu itself
+  }
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DeviceInfo& d = device_info(dev);
   const bool have_ws = a.ws != nullptr && a.ws_bytes >= kWsBytes;
@@ -2433,14 +2630,35 @@ cudaError_t launch_stream_routed(const LaunchArgs& a, DeviceInfo& d) {
   p.tiles = cdiv(a.N, kTileRows);
   p.stages = stream_stages<2>(p.M);
   p.ids = a.ids; p.T = a.T; p.E = a.E;
+  p.ptail = a.K % kStageK != 0;
   // Before the ids arrive, pull the first stage of every expert into L2 when
   // that costs at most 16 MB (the budget of bytes read on speculation).
-  p.l2_stages = a.pdl >= 2 && (int64_t)a.E * a.N * (kStageK / 2 + kStageK / kGroup * 4) <= (16 << 20) ? 1 : 0;
+  p.l2_stages = !p.ptail && a.pdl >= 2 &&
+                (int64_t)a.E * a.N * (kStageK / 2 + kStageK / kGroup * 4) <= (16 << 20) ? 1 : 0;
   Maps maps;
-  if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, (int64_t)a.N * a.E, a.K, kTileRows)) return e;
-  const int smem = stream_smem<2>(p.stages, p.M) + routed_table_bytes(a.T);
+  if (p.ptail) {  // K % 512 != 0: the parameter rows come per unit by bulk copy
+    if (cudaError_t e = make_code_map(&maps.codes, a.Wq, (int64_t)a.N * a.E, a.K, kTileRows)) return e;
+    maps.scales = maps.codes;
+    maps.biases = maps.codes;
+  } else if (cudaError_t e = make_maps(&maps, a.Wq, a.S, a.B, (int64_t)a.N * a.E, a.K, kTileRows)) {
+    return e;
+  }
+  int smem = stream_smem<2>(p.stages, p.M, p.ptail != 0) + routed_table_bytes(a.T);
+  if (p.ptail) {
+    const int pslot = ptail_slot_bytes<2>(a.K);
+    for (;; --p.stages) {
+      smem = stream_smem<2>(p.stages, p.M, true) + routed_table_bytes(a.T);
+      p.par_off = (smem - 1024 + 15) & ~15;
+      smem = p.par_off + Geo<2>::kWarps * p.stages * pslot + 1024;
+      if (smem <= kSmemLimit) break;
+      if (p.stages <= 2) return cudaErrorInvalidValue;
+    }
+  }
   constexpr int kW = Geo<2>::kWarps;
-  auto* fn = p.M > 1 ? tc_stream_kernel<2, true, false, false, true> : tc_stream_kernel<2, false, false, false, true>;
+  auto* fn = p.ptail ? (p.M > 1 ? tc_stream_kernel<2, true, false, false, true, false, false, false, true>
+                                : tc_stream_kernel<2, false, false, false, true, false, false, false, true>)
+                     : (p.M > 1 ? tc_stream_kernel<2, true, false, false, true>
+                                : tc_stream_kernel<2, false, false, false, true>);
   if (cudaError_t e = allow_smem(fn, d)) return e;
   int per_sm = 0;
   if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kW * 32, smem)) return e;
@@ -2456,6 +2674,22 @@ cudaError_t launch_tc_id(const LaunchArgs& a, const w4a16_plan& plan) {
   const Shape s = tc_shape(a.N, a.K);
   int dev = 0;
   if (cudaError_t e = cudaGetDevice(&dev)) return e;
+  if (a.K % kStageK) {
+    // whole-K units with per-unit parameter rows: the persistent routed mode
+    // only, kRoutedStreamMaxT tokens per launch (rows are independent)
+    if (a.tc_path == 2) return cudaErrorInvalidConfiguration;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo& d = device_info(dev);
+    for (int t0 = 0; t0 < a.T; t0 += kRoutedStreamMaxT) {
+      LaunchArgs b = a;
+      b.T = min(kRoutedStreamMaxT, a.T - t0);
+      b.ids = a.ids + t0;
+      b.x = a.x + (int64_t)t0 * a.K;
+      b.y = a.y + (int64_t)t0 * a.N;
+      if (cudaError_t e = launch_stream_routed(b, d)) return e;
+    }
+    return cudaSuccess;
+  }
   if (a.tc_path != 2 && a.T <= kRoutedStreamMaxT) {
     std::lock_guard<std::mutex> lk(g_dev_mu);
     DeviceInfo& d = device_info(dev);
@@ -2586,6 +2820,42 @@ cudaError_t launch_tc_g128(const LaunchArgs& a) {
   return cudaSuccess;
 }
 
+// K % 512 != 0: the persistent grid in whole-K units over K padded to whole
+// stages (the canonical slicing of the padded K, the slice sums folded in
+// registers).  No tensor map takes parameter rows K / 32 bytes apart, so each
+// unit's rows of the scales and biases come by bulk copy with its first
+// stage, as for group-128 tables.  Rows eight at a time, one launch per chunk;
+// the workspace, when given, only supplies the grid-wide unit counter.
+cudaError_t launch_tc_ptail(const LaunchArgs& a) {
+  const Shape s = tc_shape(a.N, a.K);
+  int dev = 0;
+  if (cudaError_t e = cudaGetDevice(&dev)) return e;
+  StreamParams p{};
+  p.x = a.x; p.S = a.S; p.B = a.B; p.y = a.y; p.flags = a.flags;
+  p.N = a.N; p.K = a.K;
+  p.nst = s.nst; p.sl = s.sl; p.ks = s.ks;
+  p.stages = 2;
+  p.ptail = 1;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = device_info(dev);
+  if (a.ws != nullptr && a.ws_bytes >= kWsBytes) {
+    use_workspace(p, a.ws);
+    p.part = nullptr;
+  }
+  for (int r0 = 0; r0 < a.M; r0 += kMaxChunk) {
+    p.row0 = a.row0 + r0;
+    p.M = min(kMaxChunk, a.M - r0);
+    const StreamWork w = stream_work(s, a.N, p.M);
+    if (w.nsub != 2) return cudaErrorInvalidConfiguration;
+    Maps maps;
+    if (cudaError_t e = make_code_map(&maps.codes, a.Wq, a.N, a.K, w.rows)) return e;
+    maps.scales = maps.codes;  // unused: the parameters come by bulk copy
+    maps.biases = maps.codes;
+    if (cudaError_t e = launch_stream(maps, p, w, d, a.stream, a.pdl)) return e;
+  }
+  return cudaSuccess;
+}
+
 // ---- no-allocation variant ----------------------------------------------------------------
 //
 // Some callers may not call cudaMalloc at all: code that runs inside an
@@ -2609,6 +2879,7 @@ void* g_noalloc_ptr[64] = {};
 size_t tc_noalloc_scratch_bytes() { return kWsBytes; }
 
 bool tc_noalloc_fits(int N, int K) {
+  if (K % kStageK) return tc_ptail_fits(K);  // whole-K units: no scratch
   const Shape s = tc_shape(N, K);
   for (int M = 1; M <= kMaxChunk; ++M)
     if (!workspace_fits(s, stream_work(s, N, M))) return false;
@@ -2616,6 +2887,7 @@ bool tc_noalloc_fits(int N, int K) {
 }
 
 cudaError_t launch_tc_noalloc(const LaunchArgs& a) {
+  if (a.K % kStageK) return launch_tc_ptail(a);  // a.ws is null: units dealt inside each CTA
   const Shape s = tc_shape(a.N, a.K);
   const StreamWork w = stream_work(s, a.N, a.M);
   if (!workspace_fits(s, w)) return cudaErrorInvalidValue;

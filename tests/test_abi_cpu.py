@@ -123,7 +123,6 @@ def test_mm_argmax_errors(L):
     assert f(P, P, P, P, P, P, 1, 64, 512, None, 0, None) == ops.ERR_NULL    # no workspace
     assert f(P, P, P, P, P, P, 1, 64, 512, WS, NB - 1, None) == ops.ERR_SHAPE  # too small
     assert f(P, P, P, P, P, P, 1, 64, 512, WS + 16, NB, None) == ops.ERR_ALIGN  # 256-byte alignment
-    assert f(P, P, P, P, P, P, 1, 64, 448, WS, NB, None) == ops.ERR_KERNEL   # tensor-core family only
 
 
 def test_workspace_bytes_and_mm_ws_errors(L):
@@ -131,7 +130,7 @@ def test_workspace_bytes_and_mm_ws_errors(L):
     nb = L.w4a16_workspace_bytes(262144, 2560)
     assert nb == 5013504  # 32 KiB counters + 4864 KiB fp32 partials, every shape
     assert L.w4a16_workspace_bytes(16384, 16384) == nb
-    assert L.w4a16_workspace_bytes(256, 448) == 0     # K % 512: the CUDA-core family, no workspace
+    assert L.w4a16_workspace_bytes(256, 448) == nb    # K % 512 != 0: tensor cores, padded K
     assert L.w4a16_workspace_bytes(0, 512) == 0
     assert L.w4a16_workspace_bytes(64, 96) == 0
     f = L.w4a16_mm_ws
@@ -198,13 +197,16 @@ def test_plans_depend_on_shape_only_and_fill_the_gpu(L):
             assert p["ksplit"] >= 1 and p["threads"] % 32 == 0
     with pytest.raises(ValueError):
         ops.get_plan(100, 100)
-    with pytest.raises(ValueError):
-        ops.get_plan(100, 192, "tc")
-    with pytest.raises(ValueError):
-        ops.get_plan(100, 768, "tc")  # the tensor-core family needs K % 512 == 0
-    assert ops.get_plan(100, 768)["kernel"] == "simt"
-    assert ops.get_plan(100, 192)["kernel"] == "simt"
+    # K % 512 != 0 runs on the tensor cores padded to whole 512-code stages
+    for K in (64, 192, 768, 2304):
+        p = ops.get_plan(100, K)
+        assert p["kernel"] == "tc" and p["ksplit"] * p["slice_k"] == -(-K // 512) * 512
+        assert ops.get_plan(100, K, "tc")["kernel"] == "tc"
+        assert ops.get_plan(100, K, "simt")["kernel"] == "simt"
     assert ops.get_plan(100, 2560)["kernel"] == "tc"
+    # the padded slicing of the Gemma-2-sized LM head: 4.5 stages of codes -> five
+    p = ops.get_plan(256000, 2304)
+    assert p["kernel"] == "tc" and p["ksplit"] * p["slice_k"] == 2560
     # the reduction order is a pure function of (N, K) -- the plan call has no M
     for N, K in shapes:
         a, b = ops.get_plan(N, K), ops.get_plan(N, K)

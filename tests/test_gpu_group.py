@@ -17,7 +17,7 @@ GROUPS = {
     "ragged": [(1, 512), (33, 512), (1000, 512), (17, 512)],
     "deep_k": [(300, 10240), (2560, 10240)],
     "eight": [(16 * i + 5, 1024) for i in range(8)],
-    "simt_fallback": [(64, 768), (96, 768)],
+    "tail_k": [(64, 768), (96, 768), (300, 768)],
     "too_large_fallback": [(20000, 4096), (64, 4096)],
 }
 

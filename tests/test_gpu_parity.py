@@ -68,9 +68,15 @@ def test_tc_tile_kernel_ragged_shapes(N, K, M):
     assert_parity(y, yr, ad, f"tc_tile M={M} N={N} K={K}")
 
 
-def test_tc_rejects_k_not_multiple_of_512():
+def test_tc_takes_k_not_multiple_of_512_up_to_its_slot_limit():
+    """K % 512 != 0 runs on the tensor cores padded to whole stages while the
+    per-unit parameter rows fit in shared memory; past that, only on request
+    of another family."""
+    xb, hw, y = _run(1, 64, 768, "tc")
+    yr, ad = oracle_mm(xb, hw)
+    assert_parity(y, yr, ad, "tc 64x768")
     with pytest.raises(ValueError):
-        _run(1, 64, 768, "tc")
+        _run(1, 64, 6016, "tc")
 
 
 def _special_case(N, K, codes, scale, bias, M=4):
@@ -87,8 +93,9 @@ def _special_case(N, K, codes, scale, bias, M=4):
 
 @pytest.mark.parametrize("kernel", ["simt", "tc", "vanilla"])
 @pytest.mark.parametrize("codes", [0x00000000, 0xFFFFFFFF, 0x87654321])
-def test_special_codes_and_signed_scales(kernel, codes):
-    N, K = 77, 1536
+@pytest.mark.parametrize("K", [1536, 2304, 576])
+def test_special_codes_and_signed_scales(kernel, codes, K):
+    N = 77
     xb, host, yr, ad = _special_case(N, K, codes, 0x3C0E, 0xBDB4)  # s ~ 0.0087, b ~ -0.088
     y = ops.mm(to_dev_bf16(xb), ops.W4Matrix.from_host(host), kernel=kernel)
     assert_parity(y, yr, ad, f"codes {codes:#x}")

@@ -93,8 +93,11 @@ def test_noalloc_on_new_streams_takes_no_memory():
     assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
 
 
-def test_noalloc_rejects_unsupported_k():
-    w = ops.W4Matrix.from_host(synth.make_weights(73, 64, 192))
-    x = _dev(synth.make_x(73, 1, 192))
-    y = torch.empty(1, 64, dtype=torch.bfloat16, device="cuda")
-    assert _noalloc(x, w, y) == ops.ERR_KERNEL
+@pytest.mark.parametrize("N,K", [(64, 192), (3000, 2304)])
+def test_noalloc_takes_tail_k(N, K):
+    """K % 512 != 0 (padded to whole stages) gives w4a16_mm's bits."""
+    w = ops.W4Matrix.from_host(synth.make_weights(73, N, K))
+    x = _dev(synth.make_x(73, 3, K))
+    y = torch.empty(3, N, dtype=torch.bfloat16, device="cuda")
+    assert _noalloc(x, w, y) == ops.OK
+    assert torch.equal(y.view(torch.int16), ops.mm(x, w, workspace=None).view(torch.int16))
