@@ -925,10 +925,10 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
   static_assert(!ARGMAX || (!ROUTED && NSUB == 2), "argmax over plain 32-row units");
   static_assert(!WHOLEK || (!ROUTED && !SPLIT && !ARGMAX), "whole-K units are a plain-mode schedule");
   static_assert(!G128 || (!ROUTED && !SPLIT && !ARGMAX), "group-128 tables: plain whole-K units");
-  static_assert(!PT || (!SPLIT && !ARGMAX && !G128), "K % 512 != 0: whole-K units (plain or routed)");
+  static_assert(!PT || (!ARGMAX && !G128), "K % 512 != 0: plain (whole-K or split) or routed units");
   constexpr bool DYN = (SPLIT || W4A16_TC_DYN_ALL) && !ROUTED;  // units after the first from the counter
   // whole-K units: slice sums folded in registers, in slice order
-  constexpr bool FOLD = ROUTED || WHOLEK || G128 || PT;
+  constexpr bool FOLD = ROUTED || WHOLEK || G128 || (PT && !SPLIT);
   constexpr bool UBLK = G128 || PT;  // a unit's parameter rows come by bulk copy
   // Without a workspace (p.sched == nullptr) the units are dealt inside each
   // CTA: CTA c owns the contiguous units [c U / grid, (c + 1) U / grid) and
@@ -1057,7 +1057,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
         itok = ch + 2;
         ist = 0;
         iend = p.nst;
-      } else if (WHOLEK || G128 || PT) {
+      } else if (WHOLEK || G128 || (PT && !SPLIT)) {
         irow = u * kRows;
         irows = min(kRows, p.N - irow);
         ist = 0;
@@ -1065,6 +1065,7 @@ __global__ void __launch_bounds__(Geo<NSUB>::kWarps * 32, ROUTED ? 2 : stream_mi
       } else {
         int slice;
         irow = unit_tile<SPLIT>(p, u, slice) * kRows;
+        irows = min(kRows, p.N - irow);  // PT: a split unit brings its rows over the whole K
         ist = slice * p.sl;
         iend = min(ist + p.sl, p.nst);
       }
@@ -2193,12 +2194,17 @@ cudaError_t launch_stream_t(const Maps& map, StreamParams p, int sms, DeviceInfo
       smem = unit_param_smem<NSUB>(p.stages, p.par_off, p.M, false, kp, extra, pslot, p.ptail != 0);
     }
     if (!smem) return cudaErrorInvalidValue;
-    if (p.ptail) {
-      static const Fn pt[2][2] = {{stream_launch_t<NSUB, false, false, false, false, false, false, true>,
-                                   stream_launch_t<NSUB, false, true, false, false, false, false, true>},
-                                  {stream_launch_t<NSUB, true, false, false, false, false, false, true>,
-                                   stream_launch_t<NSUB, true, true, false, false, false, false, true>}};
-      return pt[allcols][staged](map, p, sms, smem, d, stream, on);
+    if (p.ptail) {  // [allcols][staged][split]: K split over SMs where a workspace is given
+      static const Fn pt[2][2][2] = {
+          {{stream_launch_t<NSUB, false, false, false, false, false, false, true>,
+            stream_launch_t<NSUB, false, false, true, false, false, false, true>},
+           {stream_launch_t<NSUB, false, true, false, false, false, false, true>,
+            stream_launch_t<NSUB, false, true, true, false, false, false, true>}},
+          {{stream_launch_t<NSUB, true, false, false, false, false, false, true>,
+            stream_launch_t<NSUB, true, false, true, false, false, false, true>},
+           {stream_launch_t<NSUB, true, true, false, false, false, false, true>,
+            stream_launch_t<NSUB, true, true, true, false, false, false, true>}}};
+      return pt[allcols][staged][p.ks > 1 && p.part != nullptr](map, p, sms, smem, d, stream, on);
     }
     static const Fn g128[2][2] = {{stream_launch_t<NSUB, false, false, false, false, false, true>,
                                    stream_launch_t<NSUB, false, true, false, false, false, true>},
@@ -2414,7 +2420,7 @@ bool workspace_fits(const Shape& s, const StreamWork& w) {
 cudaError_t launch_stream(const Maps& maps, StreamParams p, const StreamWork& w, DeviceInfo& d,
                           cudaStream_t stream, int pdl) {
   p.tiles = w.tiles;
-  p.units = p.ks > 1 && (!p.part || p.g128 || p.ptail) ? w.tiles : w.units;  // whole-K units
+  p.units = p.ks > 1 && (!p.part || p.g128) ? w.tiles : w.units;  // whole-K units
   p.kfull = p.nst % p.sl == 0 ? p.ks : p.ks - 1;
 #if W4A16_TC_STREAM_NSUB1_MIN_M <= 8  // else no chunk (8 rows at most) takes 16-row warps
   if (w.nsub == 1) return launch_stream_t<1>(maps, p, d.sms, d, stream, pdl);
@@ -2492,13 +2498,13 @@ void plan_tc(int N, int K, int tc_path, w4a16_plan* p) {
       smem = unit_param_smem<2>(stages, par_off, 1, false, kp, 0, pslot, true);
     }
     const int per_sm = smem > 0 && kSmemLimit / smem > 0 ? kSmemLimit / smem : 1;
-    const int need = cdiv(w.tiles, Geo<2>::kWarps);
+    const int need = cdiv(w.units, Geo<2>::kWarps);
     p->rows_per_tile = w.rows;
-    p->units = w.tiles;
+    p->units = w.units;  // split over SMs with a workspace (whole-K units without)
     p->threads = Geo<2>::kWarps * 32;
     p->grid_x = sms * per_sm < need ? sms * per_sm : need;
     p->smem_bytes = smem;
-    p->workspace_bytes = 0;
+    p->workspace_bytes = s.ks > 1 ? (int)kWsBytes : 0;
     return;
   }
   const TilePlan tp = tc_path == 1 ? TilePlan() : tile_plan(s, N, 1, tc_path == 2);
@@ -2820,12 +2826,16 @@ cudaError_t launch_tc_g128(const LaunchArgs& a) {
   return cudaSuccess;
 }
 
-// K % 512 != 0: the persistent grid in whole-K units over K padded to whole
-// stages (the canonical slicing of the padded K, the slice sums folded in
-// registers).  No tensor map takes parameter rows K / 32 bytes apart, so each
-// unit's rows of the scales and biases come by bulk copy with its first
-// stage, as for group-128 tables.  Rows eight at a time, one launch per chunk;
-// the workspace, when given, only supplies the grid-wide unit counter.
+// K % 512 != 0: the persistent grid over K padded to whole stages (the
+// canonical slicing of the padded K).  No tensor map takes parameter rows
+// K / 32 bytes apart, so each unit's rows of the scales and biases (over the
+// whole K) come by bulk copy with its first stage, as for group-128 tables.
+// With a workspace and one activation row the K split goes over SMs through
+// it as for K % 512 == 0 (9216x2304: 12.4 -> 10.9 us); otherwise the units
+// are whole-K, the slice sums folded in registers (with more rows the split
+// launch's staged activations and parameter slots leave room for one CTA per
+// SM: 9216x2304 at M = 5 19.3 us split against 12.3 whole-K).  Rows eight at
+// a time, one launch per chunk.
 cudaError_t launch_tc_ptail(const LaunchArgs& a) {
   const Shape s = tc_shape(a.N, a.K);
   int dev = 0;
@@ -2838,15 +2848,14 @@ cudaError_t launch_tc_ptail(const LaunchArgs& a) {
   p.ptail = 1;
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DeviceInfo& d = device_info(dev);
-  if (a.ws != nullptr && a.ws_bytes >= kWsBytes) {
-    use_workspace(p, a.ws);
-    p.part = nullptr;
-  }
+  if (a.ws != nullptr && a.ws_bytes >= kWsBytes) use_workspace(p, a.ws);
+  float* const part = p.part;
   for (int r0 = 0; r0 < a.M; r0 += kMaxChunk) {
     p.row0 = a.row0 + r0;
     p.M = min(kMaxChunk, a.M - r0);
     const StreamWork w = stream_work(s, a.N, p.M);
     if (w.nsub != 2) return cudaErrorInvalidConfiguration;
+    p.part = p.M == 1 && workspace_fits(s, w) ? part : nullptr;
     Maps maps;
     if (cudaError_t e = make_code_map(&maps.codes, a.Wq, a.N, a.K, w.rows)) return e;
     maps.scales = maps.codes;  // unused: the parameters come by bulk copy
