@@ -177,15 +177,21 @@ __device__ __forceinline__ void build_table(uint8_t* tab, int mrows, int cb, int
     const int m = it / groups, gi = it - m * groups;
     float* t = reinterpret_cast<float*>(tab + m * tab_row_bytes(MR) + (gi >> 6) * kTabBlock +
                                         ((gi & 63) >> 1) * kPairBytes + (gi & 1) * 128);
+    // The two groups of a pair lie 128 bytes (32 banks) apart, so an odd
+    // group's thread writes its sign-set half first: the two stores of a
+    // pair then go to banks 16 apart instead of to the same bank.
+    const int sw = (gi & 1) * 16;
+    const uint32_t sgn = (uint32_t)sw << 27;  // the sign bit for the odd groups' first stores
 #pragma unroll
     for (int z = 0; z < 4; ++z) {  // the zero lane; p < q < r the others
       const float xp = xl[u][z == 0 ? 1 : 0], xq = xl[u][z <= 1 ? 2 : 1], xr = xl[u][z <= 2 ? 3 : 2];
       const float uu = __fadd_rn(xr, xq), v = __fsub_rn(xr, xq);
       const float e[4] = {__fadd_rn(uu, xp), __fsub_rn(uu, xp), __fadd_rn(v, xp), __fsub_rn(v, xp)};
 #pragma unroll
-      for (int f = 0; f < 4; ++f) {  // code 4z + f: bit 0 negates lane p, bit 1 lane q
-        t[4 * z + f] = e[f];
-        t[16 + 4 * z + f] = -e[f];
+      for (int f = 0; f < 4; ++f) {  // code 4z + f: bit 0 negates lane p, bit 1 lane q; + 16: all negated
+        const uint32_t a = __float_as_uint(e[f]) ^ sgn;
+        t[4 * z + f + sw] = __uint_as_float(a);
+        t[4 * z + f + 16 - sw] = __uint_as_float(a ^ 0x80000000u);
       }
     }
   }
