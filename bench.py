@@ -58,7 +58,7 @@ LAUNCHES = [("qkv", ("q", "k", "v")), ("o", ("o",)), ("gate_up", ("gate", "up"))
 CASES = {"q": (2048, 2560, 1), "kv": (512, 2560, 1), "o": (2560, 2048, 1), "gate": (10240, 2560, 1),
          "down": (2560, 10240, 1), "wide_up": (12288, 1536, 1), "wide_down": (1536, 12288, 1),
          "lm_head_1536": (262144, 1536, 1), "lm_head_2560": (262144, 2560, 1), "dense_16384": (16384, 16384, 1),
-         "routed": (6144, 2048, 8), "tail_k_gate": (9216, 2304, 1), "tail_k_head": (256000, 2304, 1),
+         "routed": (6144, 2048, 8), "tail_k_gate": (9216, 2304, 1), "tail_k_q": (2048, 2304, 1), "tail_k_head": (256000, 2304, 1),
          "stq1_16384": (16384, 16384, 1), "stq1_expert": (6144, 2048, 1), "stq1_routed": (6144, 2048, 8)}
 FALLBACK_HBM_GBS = 6800.0
 DOMINANT_KERNEL = "tc_stream_kernel"  # the persistent grid runs every step (the only kernel)

@@ -128,8 +128,8 @@ int resolve_kernel(int requested, int N, int K, w4a16_plan* plan) {
     case W4A16_KERNEL_TC_PREFILL: {
       if (!tc_supported(N, K))
         return fail(W4A16_ERR_KERNEL, "K = %d is past the tensor-core kernels' K %% 512 != 0 range", K);
-      if (K % 512 && (k == W4A16_KERNEL_TC_TILE || k == W4A16_KERNEL_TC_PREFILL))
-        return fail(W4A16_ERR_KERNEL, "K %% 512 != 0 runs on the persistent tensor-core kernel only (K = %d)", K);
+      if (K % 512 && k == W4A16_KERNEL_TC_PREFILL)
+        return fail(W4A16_ERR_KERNEL, "the prefill kernel needs K %% 512 == 0 (K = %d)", K);
       const int path = k == W4A16_KERNEL_TC_STREAM ? 1 : k == W4A16_KERNEL_TC_TILE ? 2 : 0;
       if (path == 2 && !tc_tile_fits(N, K, 1))
         return fail(W4A16_ERR_KERNEL, "the tile kernel cannot hold K = %d in shared memory", K);

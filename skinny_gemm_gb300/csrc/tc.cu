@@ -1585,6 +1585,8 @@ constexpr int kMaxGroup = W4A16_MAX_GROUP;
 template <int G>
 struct TileArgs {
   Maps maps[G];
+  const uint16_t* S[G];  // the parameter tables (read by bulk copy with K % 512 != 0)
+  const uint16_t* B[G];
   const uint16_t* x[G];
   uint16_t* y[G];
   int N[G];
@@ -1610,9 +1612,17 @@ struct TileParams {
 // (used in the first CTA) | tokens [8], abort flag, token-scan state [2].
 // R = 1 or 2 m16 row subtiles per CTA (16 or 32 rows): with R = 2 two warps,
 // one per subtile, share every stage's activation chunk.
-__host__ __device__ inline int tile_smem(int nloc, int xcap, int ks, int R = 1) {
-  return nloc * (R * (2 * Geo<1>::kBox + 2 * Geo<1>::kParam) + xcap * kXPitch) + nloc * 8 +
-         ks * kTile16 * R * xcap * 4 + 64 + 1024;
+// ptK (K % 512 != 0, else 0): the stages carry codes only, and the CTA's
+// parameter rows (16 R rows over the whole K, scales then biases, each in
+// tile_pt_half bytes) follow the rest at the next 16-byte boundary.
+__host__ __device__ inline int tile_pt_half(int K, int R) { return (16 * R * (K / 32) + 45) & ~15; }
+__host__ __device__ inline int tile_smem_body(int nloc, int xcap, int ks, int R, bool pt) {
+  return nloc * (R * (2 * Geo<1>::kBox + (pt ? 0 : 2 * Geo<1>::kParam)) + xcap * kXPitch) + nloc * 8 +
+         ks * kTile16 * R * xcap * 4 + 64;
+}
+__host__ __device__ inline int tile_smem(int nloc, int xcap, int ks, int R = 1, int ptK = 0) {
+  const int body = tile_smem_body(nloc, xcap, ks, R, ptK != 0);
+  return (ptK ? ((body + 15) & ~15) + 2 * tile_pt_half(ptK, R) : body) + 1024;
 }
 
 __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
@@ -1649,9 +1659,13 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
 // warps fit on an SM (by registers).
 // MULTI: more activation rows than one chunk (M > xcap); a separate instance,
 // so that one-chunk launches carry none of the loop's code.
-template <bool ALLCOLS, bool ROUTED, int G, int R, bool MULTI = false>
+// PT: K % 512 != 0 (K padded to whole stages): the stages carry codes only
+// and the CTA's parameter rows come by bulk copy with its first stage, as in
+// the persistent kernel's PT mode.
+template <bool ALLCOLS, bool ROUTED, int G, int R, bool MULTI = false, bool PT = false>
 __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ TileArgs<G> ta, TileParams p) {
-  constexpr int kRowsR = 16 * R, kCodesR = 2 * R * Geo<1>::kBox, kParamsR = 2 * R * Geo<1>::kParam;
+  static_assert(!PT || G == 1, "K % 512 != 0: single matrices");
+  constexpr int kRowsR = 16 * R, kCodesR = 2 * R * Geo<1>::kBox, kParamsR = PT ? 0 : 2 * R * Geo<1>::kParam;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, W = blockDim.x >> 5;
@@ -1681,6 +1695,15 @@ __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Ti
   int* s_tok = reinterpret_cast<int*>(red + p.ks * kRowsR * xcap);
   int* s_abort = s_tok + kMaxChunk;
   int* s_state = s_abort + 1;  // token scan: [0] position, [1] count
+  // PT: the CTA's rows are bytes [pb0, pb0 + prows K/32) of the scales and of
+  // the biases, kept at their offset modulo 16 (tile_smem)
+  const uint32_t prb = (uint32_t)(p.K / 32);
+  const uint32_t phalf = (uint32_t)tile_pt_half(p.K, R);
+  const uint32_t pblk = codes0 + (uint32_t)((tile_smem_body(p.nloc, xcap, p.ks, R, true) + 15) & ~15);
+  const int64_t pb0 = (int64_t)tensor_row * prb;
+  const uint32_t plow = prb & (0u - prb);
+  const uint32_t pal = plow < 8u ? plow : 8u;
+  const int gv_last = p.K / kGroup - 8 * (p.nst - 1);
 
   for (int i = threadIdx.x; i < nloc; i += blockDim.x) mbar_init(bars0 + 8 * i, 1);
   if (!ROUTED && threadIdx.x < min(p.M, xcap)) s_tok[threadIdx.x] = p.row0 + threadIdx.x;
@@ -1693,8 +1716,39 @@ __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Ti
 
   // lane 0 of warp w requests local stages w, w + W, ...
   auto weights = [&](int i, int xrows) {
-    issue_weights<R>(codes0 + i * kCodesR, params0 + i * kParamsR, bars0 + 8 * i, &maps, st0 + i, tensor_row, xrows,
-                     policy_evict_first(), policy_evict_last());
+    if (PT) {
+      // With local stage 0: the 16-byte-aligned window around the CTA's
+      // parameter rows by one bulk copy per table, clipped at the tables'
+      // last whole 16 bytes, and bytes past that by plain loads stored
+      // before the stage's barrier is armed.
+      uint32_t nb = 0;
+      int64_t lo = 0;
+      const char* gs = reinterpret_cast<const char*>(ta.S[0]);
+      const char* gb = reinterpret_cast<const char*>(ta.B[0]);
+      if (i == 0) {
+        const int64_t tot = (int64_t)(ROUTED ? p.E : 1) * N * prb;
+        const int64_t b1 = pb0 + (int64_t)min(kRowsR, N - tile_row) * prb;
+        lo = pb0 & ~(int64_t)15;
+        const int64_t hi = min((b1 + 15) & ~(int64_t)15, tot & ~(int64_t)15);
+        nb = hi > lo ? (uint32_t)(hi - lo) : 0u;
+        for (int64_t o = max(hi, pb0); o < b1; o += 2) {
+          const uint16_t vs = ld_nc_u16(reinterpret_cast<const uint16_t*>(gs + o));
+          const uint16_t vb = ld_nc_u16(reinterpret_cast<const uint16_t*>(gb + o));
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(pblk + (uint32_t)(o - lo)), "h"(vs) : "memory");
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(pblk + phalf + (uint32_t)(o - lo)), "h"(vb) : "memory");
+        }
+      }
+      issue_weights<R, false>(codes0 + i * kCodesR, 0, bars0 + 8 * i, &maps, st0 + i, tensor_row, xrows,
+                              policy_evict_first(), policy_evict_last(), 2 * nb,
+                              (st0 + i) * kStageWords + kBoxWords < p.K / 8);
+      if (nb) {
+        bulk_load(pblk, gs + lo, nb, bars0, policy_evict_last());
+        bulk_load(pblk + phalf, gb + lo, nb, bars0, policy_evict_last());
+      }
+    } else {
+      issue_weights<R>(codes0 + i * kCodesR, params0 + i * kParamsR, bars0 + 8 * i, &maps, st0 + i, tensor_row,
+                       xrows, policy_evict_first(), policy_evict_last());
+    }
   };
   if (!ROUTED && lane == 0 && p.prefetch)
     for (int i = warp; i < nloc; i += W) weights(i, min(p.M, xcap));
@@ -1761,6 +1815,10 @@ __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Ti
     // every stage barrier completes one phase per chunk (weights + x, then x)
     const uint32_t parity = chunk & 1u;
     bool ok = *s_abort == 0;
+    // PT: the parameter rows arrive with local stage 0, but the warps compute
+    // their stages in parallel: every warp also waits for stage 0's first
+    // phase (the copies, and lane 0's plain stores released by its arrival)
+    if (PT && chunk == 0 && ok && !__all_sync(0xffffffffu, mbar_wait(bars0, 0))) ok = false;
     for (int j = j0 + warp / R; j < j1 && ok; j += W / R) {
       float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
       const int s1 = min((j + 1) * p.sl, p.nst);
@@ -1771,9 +1829,12 @@ __global__ void __launch_bounds__(768) tc_tile_kernel(const __grid_constant__ Ti
           break;
         }
         const uint32_t cbase = ordered(codes0 + i * kCodesR);
-        const uint32_t pbase = ordered(params0 + i * kParamsR + sub * kTile16 * 16);
+        const uint32_t pbase =
+            PT ? ordered(pblk + (uint32_t)(pb0 & 15) + (uint32_t)st * 16u + (uint32_t)(sub * kTile16) * prb)
+               : ordered(params0 + i * kParamsR + sub * kTile16 * 16);
         const uint32_t xbase = ordered(xs0 + i * x_slot + g * kXPitch + 16 * t);
-        compute_stage<1, ALLCOLS, false, kRowsR>(cbase, pbase, xbase, g < mc, 0u, 0u, false, acc, loff, g);
+        compute_stage<1, ALLCOLS, false, kRowsR, PT ? 2 : 0>(cbase, pbase, xbase, g < mc, 0u, 0u, false, acc, loff,
+                                                             g, prb, phalf, pal, st == p.nst - 1 ? gv_last : 8);
       }
       if (!ok) break;
 #pragma unroll
@@ -2273,7 +2334,7 @@ int tile_ctas_per_sm(int warps, int smem) {
 // larger shapes.  A tile's slices are dealt to clusters of kc CTAs with at
 // most W4A16_TC_TILE_SLICES each; kc grows (up to 8) until a CTA fits in
 // shared memory.  `force` drops the size condition.
-TilePlan tile_plan_r(const Shape& s, int N, int M, bool force, int R) {
+TilePlan tile_plan_r(const Shape& s, int N, int M, bool force, int R, int ptK = 0) {
   TilePlan tp;
   if (!force && s.nst * s.tiles > W4A16_TC_TILE_MAX_UNITS) return tp;
   const int tiles = cdiv(N, kTile16 * R);
@@ -2285,7 +2346,7 @@ TilePlan tile_plan_r(const Shape& s, int N, int M, bool force, int R) {
     const int ksl = cdiv(s.ks, kc);
     if (ksl > W4A16_TC_TILE_SLICES && kc < kMaxCluster) continue;  // too many slices per CTA
     const int nloc = ksl * s.sl;
-    const int smem = tile_smem(nloc, M, s.ks, R);
+    const int smem = tile_smem(nloc, M, s.ks, R, ptK);
     if (smem > kSmemLimit) continue;
     const int warps = R * cdiv(ksl, W4A16_TC_TILE_SLICES_PER_WARP);
     if (warps > kTileMaxWarps) continue;
@@ -2307,10 +2368,11 @@ TilePlan tile_plan_r(const Shape& s, int N, int M, bool force, int R) {
 // longer fit in one wave), or as few when both fit in one (12288x1536 at
 // M = 3 / 5: 6.08 -> 5.78 / 6.20 -> 5.98 us; on a tie at two waves 16-row
 // CTAs stay faster: 10240x2560 at M = 5, 7.4 against 8.0 us).
-TilePlan tile_plan(const Shape& s, int N, int M, bool force, int sms = 152) {
-  const TilePlan one = tile_plan_r(s, N, M, force, 1);
+// ptK: K when K % 512 != 0 (the padded-K mode's parameter rows), else 0.
+TilePlan tile_plan(const Shape& s, int N, int M, bool force, int sms = 152, int ptK = 0) {
+  const TilePlan one = tile_plan_r(s, N, M, force, 1, ptK);
   if (M < 2) return one;
-  const TilePlan two = tile_plan_r(s, N, M, force, 2);
+  const TilePlan two = tile_plan_r(s, N, M, force, 2, ptK);
   if (two.kc == 0) return one;
   if (one.kc == 0) return two;
   const int w1 = cdiv(one.ctas, sms * tile_ctas_per_sm(one.warps, one.smem));
@@ -2335,18 +2397,30 @@ TileParams tile_params(const Shape& s, const TilePlan& tp, int K, int M, int row
 // The tile kernel instance for (columns, mode, items, row subtiles).
 template <int G>
 using TileFn = void (*)(TileArgs<G>, TileParams);
-template <int G>
+template <int G, bool PT = false>
 TileFn<G> tile_fn(bool allcols, bool routed, int R, bool multi = false) {
-  if (routed) return tc_tile_kernel<true, true, G, 1>;
-  if (multi) return R == 2 ? tc_tile_kernel<true, false, G, 2, true> : tc_tile_kernel<true, false, G, 1, true>;
-  if (R == 2) return allcols ? tc_tile_kernel<true, false, G, 2> : tc_tile_kernel<false, false, G, 2>;
-  return allcols ? tc_tile_kernel<true, false, G, 1> : tc_tile_kernel<false, false, G, 1>;
+  if (routed) return tc_tile_kernel<true, true, G, 1, false, PT>;
+  if (multi)
+    return R == 2 ? tc_tile_kernel<true, false, G, 2, true, PT> : tc_tile_kernel<true, false, G, 1, true, PT>;
+  if (R == 2) return allcols ? tc_tile_kernel<true, false, G, 2, false, PT> : tc_tile_kernel<false, false, G, 2, false, PT>;
+  return allcols ? tc_tile_kernel<true, false, G, 1, false, PT> : tc_tile_kernel<false, false, G, 1, false, PT>;
 }
 
+// K % 512 != 0 (a plan made with ptK = K): the padded-K instances, whose
+// parameter rows come by bulk copy (no tensor map for them).
 cudaError_t launch_tile(const LaunchArgs& a, const Shape& s, const TilePlan& tp, DeviceInfo& d, bool routed) {
   TileArgs<1> ta;
+  const bool pt = a.K % kStageK != 0;
   const int64_t rows = routed ? (int64_t)a.N * a.E : a.N;
-  if (cudaError_t e = make_maps(&ta.maps[0], a.Wq, a.S, a.B, rows, a.K, kTile16 * tp.R)) return e;
+  if (pt) {
+    if (cudaError_t e = make_code_map(&ta.maps[0].codes, a.Wq, rows, a.K, kTile16 * tp.R)) return e;
+    ta.maps[0].scales = ta.maps[0].codes;  // unused
+    ta.maps[0].biases = ta.maps[0].codes;
+  } else if (cudaError_t e = make_maps(&ta.maps[0], a.Wq, a.S, a.B, rows, a.K, kTile16 * tp.R)) {
+    return e;
+  }
+  ta.S[0] = a.S;
+  ta.B[0] = a.B;
   ta.x[0] = a.x;
   ta.y[0] = a.y;
   ta.N[0] = a.N;
@@ -2359,7 +2433,8 @@ cudaError_t launch_tile(const LaunchArgs& a, const Shape& s, const TilePlan& tp,
     p.E = a.E;
     p.prefetch = 0;  // the weights to read depend on the ids
   }
-  TileFn<1> fn = tile_fn<1>(a.M > 1, routed, tp.R, !routed && a.M > tp.xcap);
+  TileFn<1> fn = pt ? tile_fn<1, true>(a.M > 1, routed, tp.R, !routed && a.M > tp.xcap)
+                    : tile_fn<1>(a.M > 1, routed, tp.R, !routed && a.M > tp.xcap);
   if (cudaError_t e = allow_smem(fn, d)) return e;
   const dim3 grid(tp.ctas, routed ? a.E : 1);
   return launch_ex(fn, grid, dim3(tp.warps * 32), tp.smem, a.stream, a.pdl > 0, tp.kc, ta, p);
@@ -2469,7 +2544,7 @@ bool tc_supported(int N, int K) {
 }
 
 bool tc_tile_fits(int N, int K, int M) {
-  return K % kStageK == 0 && tile_plan(tc_shape(N, K), N, M, true).kc > 0;
+  return tile_plan(tc_shape(N, K), N, M, true, 152, K % kStageK ? K : 0).kc > 0;
 }
 
 void plan_tc(int N, int K, int tc_path, w4a16_plan* p) {
@@ -2487,7 +2562,19 @@ void plan_tc(int N, int K, int tc_path, w4a16_plan* p) {
   p->rows_per_tile = kTileRows;
   p->units = s.units;
   p->kernel = tc_path == 1 ? W4A16_KERNEL_TC_STREAM : tc_path == 2 ? W4A16_KERNEL_TC_TILE : W4A16_KERNEL_TC;
-  if (K % kStageK) {  // the persistent kernel in whole-K units, parameter rows per unit
+  const int ptK = K % kStageK ? K : 0;
+  if (ptK && tc_path != 1) {  // the tile kernel where it applies (one row, with a workspace)
+    const TilePlan tp = tile_plan(s, N, 1, tc_path == 2, sms, ptK);
+    if (tp.kc > 0) {
+      p->rows_per_tile = kTile16;
+      p->threads = tp.warps * 32;
+      p->grid_x = tp.ctas;
+      p->smem_bytes = tp.smem;
+      p->workspace_bytes = 0;
+      return;
+    }
+  }
+  if (ptK) {  // the persistent kernel, parameter rows per unit
     const StreamWork w = stream_work(s, N, 1);
     const int kp = kpad(K), pslot = ptail_slot_bytes<2>(K);
     bool staged = stage_activations<2>(1, kp, w.tiles, sms);
@@ -2559,8 +2646,20 @@ cudaError_t launch_tc_impl(const LaunchArgs& a, int32_t* idx, uint16_t* val) {
   p.part = nullptr;
   p.cnt = nullptr;
   p.sched = nullptr;
-  if (a.K % kStageK) {  // whole-K units with per-unit parameter rows: no argmax mode, tile or prefill kernel
-    if (idx || a.tc_path == 2 || a.tc_path == 3) return cudaErrorInvalidConfiguration;
+  if (a.K % kStageK) {  // parameter rows by bulk copy: no argmax mode or prefill kernel
+    if (idx || a.tc_path == 3) return cudaErrorInvalidConfiguration;
+    if (a.tc_path != 1) {
+      // the tile kernel where it applies (as below; without a workspace the
+      // persistent grid's units would be whole-K, so clusters hold split shapes)
+      std::lock_guard<std::mutex> lk(g_dev_mu);
+      DeviceInfo& d = device_info(dev);
+      const bool have_ws = a.ws != nullptr && a.ws_bytes >= kWsBytes;
+      const int mc = min(a.M, kMaxChunk);
+      TilePlan tp = tile_plan(s, a.N, mc, a.tc_path == 2, d.sms, a.K);
+      if (tp.kc == 0 && a.tc_path != 2 && (s.ks > 1 && !have_ws)) tp = tile_plan(s, a.N, mc, true, d.sms, a.K);
+      if (tp.kc > 0) return launch_tile(a, s, tp, d, false);
+      if (a.tc_path == 2) return cudaErrorInvalidConfiguration;
+    }
     return launch_tc_ptail(a);  // takes g_dev_mu itself
   }
   std::lock_guard<std::mutex> lk(g_dev_mu);
@@ -2764,6 +2863,8 @@ cudaError_t launch_tc_group(const GroupItem* items, int count, int M, int row0, 
   int tiles = 0;
   for (int i = 0; i < count; ++i) {
     if (cudaError_t e = make_maps(&ta.maps[i], items[i].Wq, items[i].S, items[i].B, items[i].N, K, rows)) return e;
+    ta.S[i] = items[i].S;
+    ta.B[i] = items[i].B;
     ta.x[i] = items[i].x;
     ta.y[i] = items[i].y;
     ta.N[i] = items[i].N;
@@ -2772,6 +2873,8 @@ cudaError_t launch_tc_group(const GroupItem* items, int count, int M, int row0, 
   }
   for (int i = count; i < kMaxGroup; ++i) {
     ta.maps[i] = ta.maps[0];
+    ta.S[i] = nullptr;
+    ta.B[i] = nullptr;
     ta.x[i] = nullptr;
     ta.y[i] = nullptr;
     ta.N[i] = 0;

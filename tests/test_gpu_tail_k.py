@@ -41,19 +41,30 @@ def test_tail_k_parity(N, K, M):
     assert ops.device_status() == 0
 
 
-@pytest.mark.parametrize("N,K", TAIL)
+@pytest.mark.parametrize("N,K", TAIL + [(300, 5952), (2048, 2304)])
 def test_tail_k_launch_shapes(N, K):
-    """The dispatcher and the persistent kernel selected by name give the same
-    bits with and without a workspace; the tile and prefill kernels refuse."""
+    """The dispatcher, the persistent kernel (whole-K units without a
+    workspace, split with one at M = 1) and the tile kernel give the same bits;
+    the prefill kernel refuses."""
     w = dev_weights(N + K + 3, N, K)
     x = to_dev_bf16(synth.make_x(77, 8, K))
     for M in (1, 3, 8):
         a = bf16_bits(ops.mm(x[:M], w, kernel="tc_stream"))
         assert np.array_equal(a, bf16_bits(ops.mm(x[:M], w))), f"{N}x{K} M={M}: dispatcher differs"
         assert np.array_equal(a, bf16_bits(ops.mm(x[:M], w, workspace=None))), f"{N}x{K} M={M}: no workspace"
-    for kernel in ("tc_tile", "tc_prefill"):
-        with pytest.raises(ValueError):
-            ops.mm(x[:1], w, kernel=kernel)
+        ws = ops.workspace()
+        y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        args = (x[:M].data_ptr(), w.Wq.data_ptr(), w.scales.data_ptr(), w.biases.data_ptr(), y.data_ptr(), M, N, K)
+        assert ops.lib().w4a16_mm_ws(*args, *ops._ws_args(ws), None) == ops.OK
+        assert np.array_equal(a, bf16_bits(y)), f"{N}x{K} M={M}: with a workspace"
+        try:
+            b = bf16_bits(ops.mm(x[:M], w, kernel="tc_tile"))
+        except ops.W4A16ValueError:
+            assert M > 1, "the tile kernel holds these shapes at M = 1"
+            continue
+        assert np.array_equal(a, b), f"{N}x{K} M={M}: tile and persistent launches differ"
+    with pytest.raises(ValueError):
+        ops.mm(x[:1], w, kernel="tc_prefill")
 
 
 @pytest.mark.parametrize("N,K", [(9216, 2304), (3000, 5952)])
@@ -116,7 +127,7 @@ def test_tail_k_reads_no_activation_past_k(N, K, kernel):
     try:
         y = ops.mm(x, w, kernel=kernel)
     except ops.W4A16ValueError:
-        assert kernel in ("tc_tile", "tc_prefill")
+        assert kernel == "tc_prefill" or (kernel == "tc_tile" and N * K > 10**8)
         return
     for m in (0, 2):
         assert torch.isfinite(y[m].float()).all(), f"row {m} not finite"
