@@ -114,10 +114,10 @@ typedef enum {
                                rescale.  K % 512 == 0 runs as one of the launch shapes
                                below, chosen from (N, K, M), all with identical bits.
                                K % 512 != 0 runs padded to whole 512-code stages (the
-                               padding groups add exactly +0) on the persistent shape
-                               alone, in whole-K work units whose scale and bias rows
-                               come by bulk copy; up to K = 5952, where those rows fit
-                               in shared memory next to eight activation rows (larger:
+                               padding groups add exactly +0) on the persistent and tile
+                               shapes, whose work units bring their scale and bias rows
+                               by bulk copy; up to K = 5952, where those rows fit in
+                               shared memory next to eight activation rows (larger:
                                W4A16_ERR_KERNEL; the dispatcher takes the CUDA-core
                                family there) */
   W4A16_KERNEL_VANILLA = 3, /* debug control: one thread per output, no sharing */
@@ -128,7 +128,7 @@ typedef enum {
                                  of tile x expert CTAs */
   W4A16_KERNEL_TC_TILE = 5, /* tensor-core kernel, one CTA per 16-row tile holding the
                                tile's whole K range; needs that to fit in shared memory
-                               and K % 512 == 0 (otherwise W4A16_ERR_KERNEL) */
+                               (otherwise W4A16_ERR_KERNEL) */
   W4A16_KERNEL_TC_PREFILL = 6 /* tensor-core kernel for many rows: each 64-code group of a
                                  128-row tile expanded once to bf16 in shared memory, then
                                  tcgen05.mma over up to 128 activation rows into tensor
