@@ -123,6 +123,7 @@ def test_mm_argmax_errors(L):
     assert f(P, P, P, P, P, P, 1, 64, 512, None, 0, None) == ops.ERR_NULL    # no workspace
     assert f(P, P, P, P, P, P, 1, 64, 512, WS, NB - 1, None) == ops.ERR_SHAPE  # too small
     assert f(P, P, P, P, P, P, 1, 64, 512, WS + 16, NB, None) == ops.ERR_ALIGN  # 256-byte alignment
+    assert f(P, P, P, P, P, P, 1, 64, 448, WS, NB, None) == ops.ERR_KERNEL   # K % 512 == 0 only
 
 
 def test_workspace_bytes_and_mm_ws_errors(L):
@@ -213,6 +214,32 @@ def test_plans_depend_on_shape_only_and_fill_the_gpu(L):
         assert (a["ksplit"], a["slice_k"]) == (b["ksplit"], b["slice_k"])
         if a["kernel"] == "tc":
             assert (a["ksplit"] - 1) * a["slice_k"] < K <= a["ksplit"] * a["slice_k"]
+
+
+def test_padded_k_plans(L):
+    """K % 512 != 0 runs padded on the tensor cores up to the K whose per-unit
+    parameter rows fit in shared memory (5952), on the persistent or the tile
+    launch shape; never on the prefill kernel; larger K on the CUDA-core
+    family by default."""
+    nb = L.w4a16_workspace_bytes(262144, 2560)
+    for K in (576, 1152, 2304, 4160, 5952):
+        for N in (1, 300, 9216, 256000):
+            p = ops.get_plan(N, K)
+            assert p["kernel"] == "tc", (N, K, p)
+            assert p["ksplit"] * p["slice_k"] >= -(-K // 512) * 512 > (p["ksplit"] - 1) * p["slice_k"]
+            assert ops.get_plan(N, K, "tc_stream")["kernel"] == "tc_stream"
+            with pytest.raises(ValueError):
+                ops.get_plan(N, K, "tc_prefill")
+        assert ops.get_plan(300, K, "tc_tile")["kernel"] == "tc_tile"
+        assert L.w4a16_workspace_bytes(300, K) == nb
+    for K in (6016, 6912, 11008):
+        assert ops.get_plan(300, K)["kernel"] == "simt"
+        assert L.w4a16_workspace_bytes(300, K) == 0
+        with pytest.raises(ValueError):
+            ops.get_plan(300, K, "tc")
+    # the small and mid shapes take the tile kernel (16-row tiles), the large heads the persistent grid
+    assert ops.get_plan(9216, 2304)["rows_per_tile"] == 16
+    assert ops.get_plan(256000, 2304)["rows_per_tile"] == 32
 
 
 def test_split_plans_fit_the_fixed_workspace(L):
