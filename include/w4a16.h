@@ -128,7 +128,8 @@ typedef enum {
                                  of tile x expert CTAs */
   W4A16_KERNEL_TC_TILE = 5, /* tensor-core kernel, one CTA per 16-row tile holding the
                                tile's whole K range; needs that to fit in shared memory
-                               (otherwise W4A16_ERR_KERNEL) */
+                               (otherwise W4A16_ERR_KERNEL); w4a16_mm_id with K % 512 != 0
+                               runs the persistent routed mode only (W4A16_ERR_KERNEL) */
   W4A16_KERNEL_TC_PREFILL = 6 /* tensor-core kernel for many rows: each 64-code group of a
                                  128-row tile expanded once to bf16 in shared memory, then
                                  tcgen05.mma over up to 128 activation rows into tensor

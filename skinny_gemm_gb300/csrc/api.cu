@@ -279,6 +279,8 @@ int w4a16_mm_id_kernel(const w4a16_bf16* x, const uint32_t* Wq, const w4a16_bf16
   if (int rc = check_nk(N, K)) return rc;
   w4a16_plan plan;
   if (int rc = resolve_kernel(kernel, N, K, &plan)) return rc;
+  if (K % 512 && plan.kernel == W4A16_KERNEL_TC_TILE)
+    return fail(W4A16_ERR_KERNEL, "w4a16_mm_id with K %% 512 != 0 runs the persistent routed mode (K = %d)", K);
   if (T == 0) return W4A16_OK;
   if (!x || !Wq || !scales || !biases || !ids || !y) return fail(W4A16_ERR_NULL, "null tensor pointer");
   if (misaligned(x, 16) || misaligned(Wq, 16)) return fail(W4A16_ERR_ALIGN, "x and Wq must be 16-byte aligned");

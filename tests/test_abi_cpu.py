@@ -107,6 +107,9 @@ def test_mm_id_errors(L):
     assert L.w4a16_mm_id(P, P, P, P, P, P, 8, 64, 96, 8, None) == ops.ERR_SHAPE
     assert L.w4a16_mm_id(P, P, P, P, P + 2, P, 8, 64, 64, 8, None) == ops.ERR_ALIGN
     assert L.w4a16_mm_id(P, P, P, P, None, P, 8, 64, 64, 8, None) == ops.ERR_NULL
+    # K % 512 != 0: the routed tile kernel is refused before anything runs
+    assert L.w4a16_mm_id_kernel(P, P, P, P, P, P, 8, 64, 576, 8, ops.KERNELS["tc_tile"], None) == ops.ERR_KERNEL
+    assert L.w4a16_mm_id_kernel(P, P, P, P, P, P, 0, 64, 576, 8, ops.KERNELS["tc_tile"], None) == ops.ERR_KERNEL
 
 
 def test_mm_argmax_errors(L):
