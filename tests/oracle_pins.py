@@ -294,6 +294,31 @@ def pin_mm_all15(o):
         _check_close(y, want, ad, what=f"all-15 codes {M}x{N}x{K}")
 
 
+def pin_mm_zero_padding(o):
+    """K % 512 != 0 runs on the tensor cores as K' = 512 ceil(K / 512) with zero
+    activations, scales and biases in the padding groups (any codes there): the
+    definition then gains only exact zero terms, so the padded problem's
+    outputs and absolute dot products equal the unpadded ones."""
+    rng = _rng(26)
+    for (M, N, K) in [(1, 3, 64), (3, 5, 576), (2, 4, 2304)]:
+        Kp = -(-K // 512) * 512
+        x = random_bf16(rng, (M, K))
+        W = rng.integers(0, 2**32, size=(N, K // 8), dtype=np.uint64).astype(np.uint32)
+        S = random_bf16(rng, (N, K // G), -0.1, 0.1)
+        B = random_bf16(rng, (N, K // G))
+        xp = np.zeros((M, Kp), dtype=np.uint16)
+        xp[:, :K] = x
+        Wp = rng.integers(0, 2**32, size=(N, Kp // 8), dtype=np.uint64).astype(np.uint32)
+        Wp[:, :K // 8] = W
+        Sp = np.zeros((N, Kp // G), dtype=np.uint16)
+        Bp = np.zeros((N, Kp // G), dtype=np.uint16)
+        Sp[:, :K // G] = S
+        Bp[:, :K // G] = B
+        y, ad = o.mm(x, W, S, B, M, N, K)
+        yp, adp = o.mm(xp, Wp, Sp, Bp, M, N, Kp)
+        assert np.all(y == yp) and np.all(ad == adp), f"padding {M}x{N}x{K} changed the result"
+
+
 def pin_mm_identity(o):
     """s = 1, b = 0, code 1 on the diagonal: y = x exactly."""
     rng = _rng(23)
@@ -592,7 +617,8 @@ def pin_stq1_mm_id(o):
 
 
 PINS = [pin_packing_golden, pin_unpack_exhaustive, pin_dequant_endpoints, pin_dequant_random,
-        pin_ulp, pin_bf16_special, pin_mm_zero_codes, pin_mm_all15, pin_mm_identity, pin_mm_ramp,
+        pin_ulp, pin_bf16_special, pin_mm_zero_codes, pin_mm_all15, pin_mm_zero_padding, pin_mm_identity,
+        pin_mm_ramp,
         pin_mm_sampled_columns, pin_mm_id, pin_mm_bruteforce, pin_bf16_decode_all,
         pin_bf16_from_f64_exact, pin_bf16_from_f32_sweep, pin_embed, pin_group128,
         pin_stq1_codebook, pin_stq1_layout, pin_stq1_mm, pin_stq1_mm_id]
